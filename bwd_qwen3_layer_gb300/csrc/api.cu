@@ -1,0 +1,523 @@
+// C ABI of libkl (declared in include/kl.h): argument checks, status
+// plumbing, buffer carving and the layer / lm-head orchestration. Every step
+// runs in the kernels of gemm.cu, elementwise.cu, attention.cu and ce.cu on
+// the caller's stream; nothing here synchronises except kl_device_status.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "internal.h"
+#include "kl_common.cuh"
+
+namespace kl {
+
+static thread_local char g_last_error[512] = "";
+
+kl_status set_error(kl_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+kl_status cuda_check(cudaError_t e, const char* what) {
+  if (e == cudaErrorMemoryAllocation)
+    return set_error(KL_ERR_NO_MEMORY, "%s: %s", what, cudaGetErrorString(e));
+  return set_error(KL_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// One 32-bit error word per device, in static device memory (no allocation).
+__device__ uint32_t g_device_error_word;
+
+uint32_t* device_error_word() {
+  static uint32_t* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error_word) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<uint32_t*>(p);
+  }
+  return addr[dev];
+}
+
+int num_sms() {
+  static int n[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!n[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    n[dev] = v > 0 ? v : 148;
+  }
+  return n[dev];
+}
+
+namespace {
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kl_status run_gemms(int dtype, GemmSpec* specs, int n, cudaStream_t st) {
+  if (dtype == KL_BF16) return gemm_bf16(specs, n, st);
+  for (int i = 0; i < n; ++i) KL_TRY(gemm_f32(specs[i], st));
+  return KL_OK;
+}
+
+// C[M,N] = A[M,K] B[N,K]^T with both operands K-major (a forward projection).
+GemmSpec proj(int M, int N, int K, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+              int64_t ldc, int c_dtype, const void* R = nullptr, int r_dtype = KL_BF16) {
+  GemmSpec s;
+  s.M = M; s.N = N; s.nseg = 1;
+  s.A[0] = A; s.lda[0] = lda; s.B[0] = B; s.ldb[0] = ldb; s.K[0] = K;
+  s.a_mn = 0; s.b_mn = 0;
+  s.C = C; s.ldc = ldc; s.c_dtype = c_dtype;
+  s.R = R; s.ldr = ldc; s.r_dtype = r_dtype;
+  return s;
+}
+
+// dW[M=out, N=in] = dY[T,out]^T X[T,in]: both operands MN-major, K = T.
+GemmSpec wgrad(int out, int in, int T, const void* dY, const void* X, void* dW, int dw_dtype) {
+  GemmSpec s;
+  s.M = out; s.N = in; s.nseg = 1;
+  s.A[0] = dY; s.lda[0] = out; s.B[0] = X; s.ldb[0] = in; s.K[0] = T;
+  s.a_mn = 1; s.b_mn = 1;
+  s.C = dW; s.ldc = in; s.c_dtype = dw_dtype;
+  return s;
+}
+
+// dX[T, in] = dY[T, out] W[out, in]: A K-major, B MN-major, K = out.
+GemmSpec dgrad(int T, int in, int out, const void* dY, const void* W, void* dX, int dx_dtype) {
+  GemmSpec s;
+  s.M = T; s.N = in; s.nseg = 1;
+  s.A[0] = dY; s.lda[0] = out; s.B[0] = W; s.ldb[0] = in; s.K[0] = out;
+  s.a_mn = 0; s.b_mn = 1;
+  s.C = dX; s.ldc = in; s.c_dtype = dx_dtype;
+  return s;
+}
+
+struct Dims {
+  int B, S, T, H, Hq, Hkv, d, I, Dq, Dkv;
+  int dt;
+  size_t es;
+};
+
+kl_status check_cfg(const kl_layer_cfg* c, Dims* o) {
+  if (!c) return set_error(KL_ERR_INVALID_ARG, "null cfg");
+  if (c->B < 1 || c->S < 1 || c->H < 1 || c->Hq < 1 || c->Hkv < 1 || c->d < 2 || c->I < 1 ||
+      (c->d & 1) || c->Hq % c->Hkv || c->eps < 0.f || !(c->rope_base > 0.f))
+    return set_error(KL_ERR_INVALID_ARG, "bad layer cfg (B %d S %d H %d Hq %d Hkv %d d %d I %d)",
+                     c->B, c->S, c->H, c->Hq, c->Hkv, c->d, c->I);
+  if (c->dtype != KL_BF16 && c->dtype != KL_F32)
+    return set_error(KL_ERR_INVALID_ARG, "bad dtype %d", c->dtype);
+  const int64_t T = static_cast<int64_t>(c->B) * c->S;
+  if (T > (1 << 24)) return set_error(KL_ERR_UNSUPPORTED, "too many tokens");
+  if (c->dtype == KL_BF16) {
+    if (c->d != 128) return set_error(KL_ERR_UNSUPPORTED, "bf16 layer needs head dim 128");
+    if (c->H % 8 || c->I % 8)
+      return set_error(KL_ERR_UNSUPPORTED, "bf16 layer needs H and I multiples of 8");
+  } else if (c->d > 256) {
+    return set_error(KL_ERR_UNSUPPORTED, "fp32 layer needs head dim <= 256");
+  }
+  if (c->H * 4 > 48 * 1024) return set_error(KL_ERR_UNSUPPORTED, "hidden width above 12288");
+  o->B = c->B; o->S = c->S; o->T = static_cast<int>(T); o->H = c->H; o->Hq = c->Hq;
+  o->Hkv = c->Hkv; o->d = c->d; o->I = c->I; o->Dq = c->Hq * c->d; o->Dkv = c->Hkv * c->d;
+  o->dt = c->dtype;
+  o->es = dtype_size(c->dtype);
+  return KL_OK;
+}
+
+// Carves consecutive 256-byte aligned pieces out of one buffer.
+struct Carver {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carver(void* b) : base(static_cast<uint8_t*>(b)) {}
+  void* take(size_t bytes) {
+    void* p = base ? base + off : nullptr;
+    off += align_up(bytes, 256);
+    return p;
+  }
+};
+
+void carve_saved(const Dims& D, Carver& c, kl_layer_saved* s) {
+  const size_t T = D.T, es = D.es;
+  s->h1 = c.take(T * D.H * es);
+  s->rstd1 = static_cast<float*>(c.take(T * 4));
+  s->q = c.take(T * D.Dq * es);
+  s->k = c.take(T * D.Dkv * es);
+  s->v = c.take(T * D.Dkv * es);
+  s->o = c.take(T * D.Dq * es);
+  s->lse = static_cast<float*>(c.take(static_cast<size_t>(D.B) * D.Hq * D.S * 4));
+  s->x2 = c.take(T * D.H * es);
+  s->h2 = c.take(T * D.H * es);
+  s->rstd2 = static_cast<float*>(c.take(T * 4));
+  s->g = c.take(T * D.I * es);
+  s->u = c.take(T * D.I * es);
+  s->m = c.take(T * D.I * es);
+}
+
+struct BwdWs {
+  void *dm, *dg, *du, *dx2, *dO, *dq, *dk, *dv;
+  float *dh2, *dh1;
+  void* att;
+  size_t att_bytes;
+  void* norm;
+  size_t norm_bytes;
+};
+
+void carve_bwd(const Dims& D, Carver& c, BwdWs* w) {
+  const size_t T = D.T, es = D.es;
+  w->dm = c.take(T * D.I * es);
+  w->dg = c.take(T * D.I * es);
+  w->du = c.take(T * D.I * es);
+  w->dh2 = static_cast<float*>(c.take(T * D.H * 4));
+  w->dx2 = c.take(T * D.H * es);
+  w->dO = c.take(T * D.Dq * es);
+  w->dq = c.take(T * D.Dq * es);
+  w->dk = c.take(T * D.Dkv * es);
+  w->dv = c.take(T * D.Dkv * es);
+  w->dh1 = static_cast<float*>(c.take(T * D.H * 4));
+  w->att_bytes = attention_bwd_ws(D.B, D.S, D.Hq, D.Hkv, D.d);
+  w->att = c.take(w->att_bytes);
+  w->norm_bytes = rmsnorm_bwd_ws(D.T, D.H);
+  w->norm = c.take(w->norm_bytes);
+}
+
+kl_status check_ptrs(std::initializer_list<const void*> ptrs, const char* what) {
+  for (const void* p : ptrs) {
+    if (!p) return set_error(KL_ERR_INVALID_ARG, "%s: null pointer", what);
+    if (!al16(p)) return set_error(KL_ERR_INVALID_ARG, "%s: pointer not 16-byte aligned", what);
+  }
+  return KL_OK;
+}
+
+}  // namespace
+}  // namespace kl
+
+using namespace kl;
+
+extern "C" {
+
+const char* kl_version(void) { return "kl 0.1 (sm_103a)"; }
+
+const char* kl_status_str(kl_status s) {
+  switch (s) {
+    case KL_OK: return "ok";
+    case KL_ERR_INVALID_ARG: return "invalid argument";
+    case KL_ERR_UNSUPPORTED: return "unsupported";
+    case KL_ERR_CUDA: return "cuda error";
+    case KL_ERR_TIMEOUT: return "timeout";
+    case KL_ERR_NO_MEMORY: return "no memory";
+    case KL_ERR_DEVICE: return "device-side error";
+  }
+  return "unknown status";
+}
+
+const char* kl_last_error(void) { return g_last_error; }
+
+kl_status kl_device_status(void* stream, uint32_t* bits) {
+  KL_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  uint32_t v = 0;
+  KL_CUDA(cudaMemcpyFromSymbol(&v, g_device_error_word, sizeof(v)));
+  const uint32_t zero = 0;
+  KL_CUDA(cudaMemcpyToSymbol(g_device_error_word, &zero, sizeof(zero)));
+  if (bits) *bits = v;
+  if (v & KL_DEVERR_TIMEOUT) return set_error(KL_ERR_TIMEOUT, "a kernel wait timed out (bits 0x%x)", v);
+  if (v) return set_error(KL_ERR_DEVICE, "a kernel rejected its input (bits 0x%x)", v);
+  return KL_OK;
+}
+
+size_t kl_layer_saved_bytes(const kl_layer_cfg* cfg) {
+  Dims D;
+  if (check_cfg(cfg, &D) != KL_OK) return 0;
+  Carver c(nullptr);
+  kl_layer_saved s;
+  carve_saved(D, c, &s);
+  return c.off;
+}
+
+kl_status kl_layer_saved_carve(const kl_layer_cfg* cfg, void* base, size_t bytes,
+                               kl_layer_saved* out) {
+  Dims D;
+  KL_TRY(check_cfg(cfg, &D));
+  if (!base || !out) return set_error(KL_ERR_INVALID_ARG, "saved_carve: null pointer");
+  if (reinterpret_cast<uintptr_t>(base) & 255u)
+    return set_error(KL_ERR_INVALID_ARG, "saved_carve: base not 256-byte aligned");
+  Carver c(base);
+  kl_layer_saved s;
+  memset(&s, 0, sizeof(s));
+  carve_saved(D, c, &s);
+  if (c.off > bytes) return set_error(KL_ERR_NO_MEMORY, "saved_carve: need %zu bytes", c.off);
+  *out = s;
+  return KL_OK;
+}
+
+size_t kl_layer_fwd_workspace_bytes(const kl_layer_cfg* cfg) {
+  Dims D;
+  if (check_cfg(cfg, &D) != KL_OK) return 0;
+  return 256;
+}
+
+size_t kl_layer_bwd_workspace_bytes(const kl_layer_cfg* cfg) {
+  Dims D;
+  if (check_cfg(cfg, &D) != KL_OK) return 0;
+  Carver c(nullptr);
+  BwdWs w;
+  carve_bwd(D, c, &w);
+  return c.off;
+}
+
+kl_status kl_layer_forward(const kl_layer_cfg* cfg, const kl_layer_weights* w, const void* X,
+                           void* Y, kl_layer_saved* s, void* ws, size_t ws_bytes, void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  Dims D;
+  KL_TRY(check_cfg(cfg, &D));
+  if (!w || !s) return set_error(KL_ERR_INVALID_ARG, "layer_forward: null weights or saved");
+  KL_TRY(check_ptrs({w->gamma1, w->wq, w->wk, w->wv, w->wo, w->gamma2, w->wg, w->wu, w->wd}, "layer_forward weights"));
+  KL_TRY(check_ptrs({X, Y, s->h1, s->rstd1, s->q, s->k, s->v, s->o, s->lse, s->x2, s->h2, s->rstd2,
+                     s->g, s->u, s->m}, "layer_forward buffers"));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int T = D.T, H = D.H, I = D.I, dt = D.dt;
+  s->x = X;
+  KL_TRY(rmsnorm_fwd(T, H, dt, X, w->gamma1, cfg->eps, s->h1, s->rstd1, st));
+  {
+    GemmSpec g[3] = {proj(T, D.Dq, H, s->h1, H, w->wq, H, s->q, D.Dq, dt),
+                     proj(T, D.Dkv, H, s->h1, H, w->wk, H, s->k, D.Dkv, dt),
+                     proj(T, D.Dkv, H, s->h1, H, w->wv, H, s->v, D.Dkv, dt)};
+    KL_TRY(run_gemms(dt, g, 3, st));
+  }
+  KL_TRY(rope(D.B, D.S, D.Hq, D.d, cfg->rope_base, dt, s->q, 1, st));
+  KL_TRY(rope(D.B, D.S, D.Hkv, D.d, cfg->rope_base, dt, s->k, 1, st));
+  KL_TRY(attention_fwd(D.B, D.S, D.Hq, D.Hkv, D.d, dt, s->q, s->k, s->v, s->o, s->lse, st));
+  {
+    GemmSpec g = proj(T, H, D.Dq, s->o, D.Dq, w->wo, D.Dq, s->x2, H, dt, X, dt);
+    KL_TRY(run_gemms(dt, &g, 1, st));
+  }
+  KL_TRY(rmsnorm_fwd(T, H, dt, s->x2, w->gamma2, cfg->eps, s->h2, s->rstd2, st));
+  {
+    GemmSpec g[2] = {proj(T, I, H, s->h2, H, w->wg, H, s->g, I, dt),
+                     proj(T, I, H, s->h2, H, w->wu, H, s->u, I, dt)};
+    KL_TRY(run_gemms(dt, g, 2, st));
+  }
+  KL_TRY(swiglu_fwd(static_cast<int64_t>(T) * I, dt, s->g, s->u, s->m, st));
+  {
+    GemmSpec g = proj(T, H, I, s->m, I, w->wd, I, Y, H, dt, s->x2, dt);
+    KL_TRY(run_gemms(dt, &g, 1, st));
+  }
+  return KL_OK;
+}
+
+kl_status kl_layer_backward(const kl_layer_cfg* cfg, const kl_layer_weights* w,
+                            const kl_layer_saved* s, const void* dY, void* dX,
+                            const kl_layer_grads* gr, void* ws, size_t ws_bytes, void* stream) {
+  Dims D;
+  KL_TRY(check_cfg(cfg, &D));
+  if (!w || !s || !gr) return set_error(KL_ERR_INVALID_ARG, "layer_backward: null struct");
+  KL_TRY(check_ptrs({w->gamma1, w->wq, w->wk, w->wv, w->wo, w->gamma2, w->wg, w->wu, w->wd}, "layer_backward weights"));
+  KL_TRY(check_ptrs({s->x, s->h1, s->rstd1, s->q, s->k, s->v, s->o, s->lse, s->x2, s->h2,
+                     s->rstd2, s->g, s->u, s->m}, "layer_backward saved"));
+  KL_TRY(check_ptrs({dY, dX, gr->gamma1, gr->wq, gr->wk, gr->wv, gr->wo, gr->gamma2, gr->wg,
+                     gr->wu, gr->wd}, "layer_backward outputs"));
+  if (gr->dtype != KL_F32 && gr->dtype != KL_BF16)
+    return set_error(KL_ERR_INVALID_ARG, "layer_backward: bad gradient dtype");
+  if (D.dt == KL_F32 && gr->dtype != KL_F32)
+    return set_error(KL_ERR_UNSUPPORTED, "layer_backward: fp32 layer needs fp32 gradients");
+  const size_t need = kl_layer_bwd_workspace_bytes(cfg);
+  if (!ws || ws_bytes < need) return set_error(KL_ERR_NO_MEMORY, "layer_backward: workspace needs %zu bytes", need);
+  if (reinterpret_cast<uintptr_t>(ws) & 255u)
+    return set_error(KL_ERR_INVALID_ARG, "layer_backward: workspace not 256-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Carver c(ws);
+  BwdWs b;
+  carve_bwd(D, c, &b);
+  const int T = D.T, H = D.H, I = D.I, dt = D.dt, gdt = gr->dtype;
+
+  // MLP: dm = dY Wd, dWd = dY^T m
+  {
+    GemmSpec g[2] = {dgrad(T, I, H, dY, w->wd, b.dm, dt), wgrad(H, I, T, dY, s->m, gr->wd, gdt)};
+    KL_TRY(run_gemms(dt, g, 2, st));
+  }
+  KL_TRY(swiglu_bwd(static_cast<int64_t>(T) * I, dt, b.dm, s->g, s->u, b.dg, b.du, st));
+  {
+    GemmSpec dh = dgrad(T, H, I, b.dg, w->wg, b.dh2, KL_F32);
+    dh.nseg = 2;
+    dh.A[1] = b.du; dh.lda[1] = I; dh.B[1] = w->wu; dh.ldb[1] = H; dh.K[1] = I;
+    GemmSpec g[3] = {dh, wgrad(I, H, T, b.dg, s->h2, gr->wg, gdt),
+                     wgrad(I, H, T, b.du, s->h2, gr->wu, gdt)};
+    KL_TRY(run_gemms(dt, g, 3, st));
+  }
+  KL_TRY(rmsnorm_bwd(T, H, dt, b.dh2, KL_F32, s->x2, w->gamma2, s->rstd2, dY, b.dx2,
+                     static_cast<float*>(gr->gamma2), b.norm, b.norm_bytes, st));
+  // attention block: dO = dx2 Wo, dWo = dx2^T o
+  {
+    GemmSpec g[2] = {dgrad(T, D.Dq, H, b.dx2, w->wo, b.dO, dt),
+                     wgrad(H, D.Dq, T, b.dx2, s->o, gr->wo, gdt)};
+    KL_TRY(run_gemms(dt, g, 2, st));
+  }
+  float *dq_acc = nullptr, *dk_acc = nullptr, *dv_acc = nullptr;
+  KL_TRY(attention_bwd_accum(D.B, D.S, D.Hq, D.Hkv, D.d, dt, s->q, s->k, s->v, s->o, s->lse, b.dO,
+                             b.att, b.att_bytes, &dq_acc, &dk_acc, &dv_acc, st));
+  KL_TRY(rope_bwd_from_f32(D.B, D.S, D.Hq, D.d, cfg->rope_base, dt, dq_acc, b.dq, st));
+  KL_TRY(rope_bwd_from_f32(D.B, D.S, D.Hkv, D.d, cfg->rope_base, dt, dk_acc, b.dk, st));
+  KL_TRY(convert_f32(static_cast<int64_t>(T) * D.Dkv, dt, dv_acc, b.dv, st));
+  {
+    GemmSpec dh = dgrad(T, H, D.Dq, b.dq, w->wq, b.dh1, KL_F32);
+    dh.nseg = 3;
+    dh.A[1] = b.dk; dh.lda[1] = D.Dkv; dh.B[1] = w->wk; dh.ldb[1] = H; dh.K[1] = D.Dkv;
+    dh.A[2] = b.dv; dh.lda[2] = D.Dkv; dh.B[2] = w->wv; dh.ldb[2] = H; dh.K[2] = D.Dkv;
+    GemmSpec g[4] = {dh, wgrad(D.Dq, H, T, b.dq, s->h1, gr->wq, gdt),
+                     wgrad(D.Dkv, H, T, b.dk, s->h1, gr->wk, gdt),
+                     wgrad(D.Dkv, H, T, b.dv, s->h1, gr->wv, gdt)};
+    KL_TRY(run_gemms(dt, g, 4, st));
+  }
+  KL_TRY(rmsnorm_bwd(T, H, dt, b.dh1, KL_F32, s->x, w->gamma1, s->rstd1, b.dx2, dX,
+                     static_cast<float*>(gr->gamma1), b.norm, b.norm_bytes, st));
+  return KL_OK;
+}
+
+// ---------------------------------------------------------------------------
+// lm-head
+// ---------------------------------------------------------------------------
+static kl_status check_lm(const kl_lmhead_cfg* c) {
+  if (!c || c->N < 1 || c->H < 1 || c->V < 1)
+    return set_error(KL_ERR_INVALID_ARG, "bad lm-head cfg");
+  if ((c->dtype != KL_BF16 && c->dtype != KL_F32) || (c->dw_dtype != KL_BF16 && c->dw_dtype != KL_F32))
+    return set_error(KL_ERR_INVALID_ARG, "bad lm-head dtype");
+  if (c->dtype == KL_F32 && c->dw_dtype != KL_F32)
+    return set_error(KL_ERR_UNSUPPORTED, "fp32 lm-head needs fp32 dW");
+  if (c->dtype == KL_BF16 && (c->H % 8 || c->V % 8))
+    return set_error(KL_ERR_UNSUPPORTED, "bf16 lm-head needs H and V multiples of 8");
+  return KL_OK;
+}
+
+size_t kl_lmhead_workspace_bytes(const kl_lmhead_cfg* c) {
+  if (check_lm(c) != KL_OK) return 0;
+  const size_t NV = static_cast<size_t>(c->N) * c->V;
+  return align_up(NV * 4, 256) + align_up(NV * dtype_size(c->dtype), 256) + ce_ws(c->N);
+}
+
+kl_status kl_lmhead_ce_argmax(const kl_lmhead_cfg* c, const void* X, const void* W,
+                              const int32_t* targets, float* loss, int32_t* argmax, void* dlogits,
+                              void* dX, void* dW, void* ws, size_t ws_bytes, void* stream) {
+  KL_TRY(check_lm(c));
+  KL_TRY(check_ptrs({X, W, dX, dW}, "lmhead"));
+  if (!targets || !loss || !argmax) return set_error(KL_ERR_INVALID_ARG, "lmhead: null pointer");
+  if (dlogits && !al16(dlogits)) return set_error(KL_ERR_INVALID_ARG, "lmhead: dlogits not aligned");
+  const size_t need = kl_lmhead_workspace_bytes(c);
+  if (!ws || ws_bytes < need) return set_error(KL_ERR_NO_MEMORY, "lmhead: workspace needs %zu bytes", need);
+  if (reinterpret_cast<uintptr_t>(ws) & 255u)
+    return set_error(KL_ERR_INVALID_ARG, "lmhead: workspace not 256-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int N = c->N, H = c->H, V = c->V, dt = c->dtype;
+  const size_t NV = static_cast<size_t>(N) * V;
+  Carver cv(ws);
+  float* z = static_cast<float*>(cv.take(NV * 4));
+  void* dz_ws = cv.take(NV * dtype_size(dt));
+  void* ce = cv.take(ce_ws(N));
+  void* dz = dlogits ? dlogits : dz_ws;
+  {
+    GemmSpec g = proj(N, V, H, X, H, W, H, z, V, KL_F32);
+    KL_TRY(run_gemms(dt, &g, 1, st));
+  }
+  KL_TRY(ce_argmax(N, V, z, targets, loss, argmax, dz, dt, ce, ce_ws(N), st));
+  {
+    GemmSpec g[2] = {dgrad(N, H, V, dz, W, dX, dt), wgrad(V, H, N, dz, X, dW, c->dw_dtype)};
+    KL_TRY(run_gemms(dt, g, 2, st));
+  }
+  return KL_OK;
+}
+
+size_t kl_ce_workspace_bytes(int32_t N) { return N > 0 ? ce_ws(N) : 0; }
+
+kl_status kl_ce_argmax(int32_t N, int32_t V, const float* z, const int32_t* targets, float* loss,
+                       int32_t* argmax, void* dlogits, int32_t dz_dtype, void* ws, size_t ws_bytes,
+                       void* stream) {
+  if (dz_dtype != KL_F32 && dz_dtype != KL_BF16) return set_error(KL_ERR_INVALID_ARG, "ce: bad dtype");
+  return ce_argmax(N, V, z, targets, loss, argmax, dlogits, dz_dtype, ws, ws_bytes,
+                   static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------
+// individual kernels
+// ---------------------------------------------------------------------------
+kl_status kl_gemm(int32_t M, int32_t N, int32_t K, int32_t dtype, const void* A, int64_t lda,
+                  int32_t a_mn_major, const void* B, int64_t ldb, int32_t b_mn_major, void* C,
+                  int64_t ldc, int32_t c_dtype, const void* R, int64_t ldr, int32_t r_dtype,
+                  void* stream) {
+  if (M < 1 || N < 1 || K < 1 || !A || !B || !C) return set_error(KL_ERR_INVALID_ARG, "gemm: bad arguments");
+  if ((dtype != KL_F32 && dtype != KL_BF16) || (c_dtype != KL_F32 && c_dtype != KL_BF16) ||
+      (R && r_dtype != KL_F32 && r_dtype != KL_BF16))
+    return set_error(KL_ERR_INVALID_ARG, "gemm: bad dtype");
+  const int64_t a_rows_min = a_mn_major ? M : K, b_rows_min = b_mn_major ? N : K;
+  if (lda < a_rows_min || ldb < b_rows_min || ldc < N || (R && ldr < N))
+    return set_error(KL_ERR_INVALID_ARG, "gemm: leading dimension too small");
+  GemmSpec s;
+  s.M = M; s.N = N; s.nseg = 1;
+  s.A[0] = A; s.lda[0] = lda; s.B[0] = B; s.ldb[0] = ldb; s.K[0] = K;
+  s.a_mn = a_mn_major ? 1 : 0; s.b_mn = b_mn_major ? 1 : 0;
+  s.C = C; s.ldc = ldc; s.c_dtype = c_dtype;
+  s.R = R; s.ldr = ldr; s.r_dtype = r_dtype;
+  return run_gemms(dtype, &s, 1, static_cast<cudaStream_t>(stream));
+}
+
+kl_status kl_rmsnorm_fwd(int32_t rows, int32_t width, int32_t dtype, const void* x,
+                         const void* gamma, float eps, void* h, float* rstd, void* stream) {
+  return rmsnorm_fwd(rows, width, dtype, x, gamma, eps, h, rstd, static_cast<cudaStream_t>(stream));
+}
+
+size_t kl_rmsnorm_bwd_ws_bytes(int32_t rows, int32_t width) {
+  return rows > 0 && width > 0 ? rmsnorm_bwd_ws(rows, width) : 0;
+}
+
+kl_status kl_rmsnorm_bwd(int32_t rows, int32_t width, int32_t dtype, const void* dh,
+                         int32_t dh_dtype, const void* x, const void* gamma, const float* rstd,
+                         const void* resid, void* dx, float* dgamma, void* ws, size_t ws_bytes,
+                         void* stream) {
+  return rmsnorm_bwd(rows, width, dtype, dh, dh_dtype, x, gamma, rstd, resid, dx, dgamma, ws,
+                     ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
+kl_status kl_rope(int32_t B, int32_t S, int32_t heads, int32_t d, float base, int32_t dtype,
+                  void* x, int32_t direction, void* stream) {
+  return rope(B, S, heads, d, base, dtype, x, direction, static_cast<cudaStream_t>(stream));
+}
+
+kl_status kl_swiglu_fwd(int64_t n, int32_t dtype, const void* g, const void* u, void* m,
+                        void* stream) {
+  return swiglu_fwd(n, dtype, g, u, m, static_cast<cudaStream_t>(stream));
+}
+
+kl_status kl_swiglu_bwd(int64_t n, int32_t dtype, const void* dm, const void* g, const void* u,
+                        void* dg, void* du, void* stream) {
+  return swiglu_bwd(n, dtype, dm, g, u, dg, du, static_cast<cudaStream_t>(stream));
+}
+
+kl_status kl_attention_fwd(int32_t B, int32_t S, int32_t Hq, int32_t Hkv, int32_t d,
+                           int32_t dtype, const void* q, const void* k, const void* v, void* o,
+                           float* lse, void* stream) {
+  return attention_fwd(B, S, Hq, Hkv, d, dtype, q, k, v, o, lse, static_cast<cudaStream_t>(stream));
+}
+
+size_t kl_attention_bwd_ws_bytes(int32_t B, int32_t S, int32_t Hq, int32_t Hkv, int32_t d) {
+  if (B < 1 || S < 1 || Hq < 1 || Hkv < 1 || d < 1) return 0;
+  return attention_bwd_ws(B, S, Hq, Hkv, d);
+}
+
+kl_status kl_attention_bwd(int32_t B, int32_t S, int32_t Hq, int32_t Hkv, int32_t d,
+                           int32_t dtype, const void* q, const void* k, const void* v,
+                           const void* o, const float* lse, const void* dout, void* dq, void* dk,
+                           void* dv, void* ws, size_t ws_bytes, void* stream) {
+  if (!dq || !dk || !dv) return set_error(KL_ERR_INVALID_ARG, "attention_bwd: null output");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float *dq_acc = nullptr, *dk_acc = nullptr, *dv_acc = nullptr;
+  KL_TRY(attention_bwd_accum(B, S, Hq, Hkv, d, dtype, q, k, v, o, lse, dout, ws, ws_bytes, &dq_acc,
+                             &dk_acc, &dv_acc, st));
+  const int64_t T = static_cast<int64_t>(B) * S;
+  KL_TRY(convert_f32(T * Hq * d, dtype, dq_acc, dq, st));
+  KL_TRY(convert_f32(T * Hkv * d, dtype, dk_acc, dk, st));
+  KL_TRY(convert_f32(T * Hkv * d, dtype, dv_acc, dv, st));
+  return KL_OK;
+}
+
+}  // extern "C"

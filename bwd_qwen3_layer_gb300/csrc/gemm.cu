@@ -1,0 +1,521 @@
+// Matrix products of the layer ("From-scratch GPU LLM training", capability
+// list: the matrix-multiply gradient kernel): every projection forward
+// (y = x W^T), its input gradient (dx = dy W) and its weight gradient
+// (dW = dy^T x), and the lm-head products.
+//
+// bf16 path: one persistent, warp-specialised tcgen05 kernel.
+//   warp 0      TMA producer: 128x64 A tile and 256x64 B tile per stage,
+//               128-byte swizzle, 4-stage mbarrier ring.
+//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators)
+//               and one elected lane issues tcgen05.mma (M=128, N=256, K=16).
+//   warps 2..5  epilogue: tcgen05.ld the accumulator lane quarter they own,
+//               add the optional residual, convert, store; then release the
+//               accumulator so the MMA warp can start the tile after next.
+// Operands may be K-major or MN-major (the transpose bits of the instruction
+// descriptor), so dX and dW need no transposed copies. Up to four problems
+// share one launch (for example the q/k/v projections, or a dX and a dW
+// product), and one problem may accumulate up to three (A, B) segments (the
+// input gradient of the fused q/k/v projection).
+//
+// fp32 path: a plain shared-memory tiled FFMA kernel (no TF32).
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "kl_common.cuh"
+
+namespace kl {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr uint32_t A_BYTES = BM * BK * 2;
+constexpr uint32_t B_BYTES = BN * BK * 2;
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t TMEM_COLS = 2 * BN;
+constexpr int NUM_THREADS = 192;
+constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+
+struct GemmProb {
+  int M, N;
+  int nseg;
+  int kb[GEMM_MAX_SEG];
+  int a_mn, b_mn;
+  int m_tiles, n_tiles;
+  int tile_begin;
+  int tmap_base;
+  void* C;
+  int64_t ldc;
+  int c_f32;
+  int vec_ok;
+  const void* R;
+  int64_t ldr;
+  int r_f32;
+};
+
+struct GemmParams {
+  CUtensorMap tmA[GEMM_MAX_PROB * GEMM_MAX_SEG];
+  CUtensorMap tmB[GEMM_MAX_PROB * GEMM_MAX_SEG];
+  GemmProb prob[GEMM_MAX_PROB];
+  int nprob;
+  int total_tiles;
+  uint32_t* err;
+};
+
+__device__ __forceinline__ int find_prob(const GemmParams& p, int tile) {
+  int pi = 0;
+  while (pi + 1 < p.nprob && tile >= p.prob[pi + 1].tile_begin) ++pi;
+  return pi;
+}
+
+__device__ __forceinline__ void store_chunk(const GemmProb& pr, int row, int col0,
+                                            const uint32_t (&v)[32]) {
+  float f[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+  const int ncols = min(32, pr.N - col0);
+  const bool vec = pr.vec_ok && ncols == 32;
+  if (pr.R) {
+    if (pr.r_f32) {
+      const float* r = static_cast<const float*>(pr.R) + row * pr.ldr + col0;
+      if (vec) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          float4 a = *reinterpret_cast<const float4*>(r + j);
+          f[j] += a.x; f[j + 1] += a.y; f[j + 2] += a.z; f[j + 3] += a.w;
+        }
+      } else {
+        for (int j = 0; j < ncols; ++j) f[j] += r[j];
+      }
+    } else {
+      const __nv_bfloat16* r = static_cast<const __nv_bfloat16*>(pr.R) + row * pr.ldr + col0;
+      if (vec) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 8) {
+          uint4 a = *reinterpret_cast<const uint4*>(r + j);
+          float2 x0 = unpack_bf16x2(a.x), x1 = unpack_bf16x2(a.y), x2 = unpack_bf16x2(a.z),
+                 x3 = unpack_bf16x2(a.w);
+          f[j] += x0.x; f[j + 1] += x0.y; f[j + 2] += x1.x; f[j + 3] += x1.y;
+          f[j + 4] += x2.x; f[j + 5] += x2.y; f[j + 6] += x3.x; f[j + 7] += x3.y;
+        }
+      } else {
+        for (int j = 0; j < ncols; ++j) f[j] += __bfloat162float(r[j]);
+      }
+    }
+  }
+  if (pr.c_f32) {
+    float* c = static_cast<float*>(pr.C) + row * pr.ldc + col0;
+    if (vec) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4*>(c + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
+    } else {
+      for (int j = 0; j < ncols; ++j) c[j] = f[j];
+    }
+  } else {
+    __nv_bfloat16* c = static_cast<__nv_bfloat16*>(pr.C) + row * pr.ldc + col0;
+    if (vec) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 8) {
+        uint4 o;
+        o.x = pack_bf16x2(f[j], f[j + 1]);
+        o.y = pack_bf16x2(f[j + 2], f[j + 3]);
+        o.z = pack_bf16x2(f[j + 4], f[j + 5]);
+        o.w = pack_bf16x2(f[j + 6], f[j + 7]);
+        *reinterpret_cast<uint4*>(c + j) = o;
+      }
+    } else {
+      for (int j = 0; j < ncols; ++j) c[j] = __float2bfloat16_rn(f[j]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_bf16_tc_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer ----------------
+    for (int i = 0; i < p.nprob; ++i)
+      for (int s = 0; s < p.prob[i].nseg; ++s) {
+        tma_prefetch_desc(&p.tmA[p.prob[i].tmap_base + s]);
+        tma_prefetch_desc(&p.tmB[p.prob[i].tmap_base + s]);
+      }
+    int stage = 0;
+    uint32_t phase = 0;
+    long issued = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
+      const int pi = find_prob(p, tile);
+      const GemmProb& pr = p.prob[pi];
+      const int local = tile - pr.tile_begin;
+      const int m0 = (local % pr.m_tiles) * BM;
+      const int n0 = (local / pr.m_tiles) * BN;
+      for (int s = 0; ok && s < pr.nseg; ++s) {
+        const CUtensorMap* ta = &p.tmA[pr.tmap_base + s];
+        const CUtensorMap* tb = &p.tmB[pr.tmap_base + s];
+        for (int kb = 0; kb < pr.kb[s]; ++kb) {
+          if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u, p.err)) {
+            ok = false;
+            *abort_flag = 1;
+            break;
+          }
+          const uint32_t fb = full_bar(stage);
+          mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const uint32_t sa = sbase + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          const int k0 = kb * BK;
+          if (!pr.a_mn) {
+            tma_load_2d(sa, ta, k0, m0, fb);
+          } else {
+            tma_load_2d(sa, ta, m0, k0, fb);
+            tma_load_2d(sa + 8192, ta, m0 + 64, k0, fb);
+          }
+          if (!pr.b_mn) {
+            tma_load_2d(sb, tb, k0, n0, fb);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + 8192 * j, tb, n0 + 64 * j, k0, fb);
+          }
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+    // Wait (bounded) for the copies still in flight before the CTA can exit.
+    const long outstanding = issued < STAGES ? issued : STAGES;
+    for (long i = 0; i < outstanding; ++i) {
+      if (stage == 0) {
+        stage = STAGES - 1;
+        phase ^= 1u;
+      } else {
+        --stage;
+      }
+      mbar_wait(full_bar(stage), phase, p.err);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    int it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++it) {
+      const GemmProb& pr = p.prob[find_prob(p, tile)];
+      const int acc = it & 1;
+      const uint32_t use = static_cast<uint32_t>(it >> 1);
+      if (*abort_flag || !mbar_wait(tempty_bar(acc), (use & 1u) ^ 1u, p.err)) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+      const uint32_t idesc = idesc_bf16_f32(BM, BN, pr.a_mn, pr.b_mn);
+      uint32_t accumulate = 0;
+      for (int s = 0; ok && s < pr.nseg; ++s) {
+        for (int kb = 0; kb < pr.kb[s]; ++kb) {
+          if (*abort_flag || !mbar_wait(full_bar(stage), phase, p.err)) {
+            ok = false;
+            *abort_flag = 1;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = sbase + stage * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = pr.a_mn ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
+                                        : smem_desc_sw128(sa + k * 32, 16, 1024);
+            const uint64_t bd = pr.b_mn ? smem_desc_sw128(sb + k * 2048, 8192, 1024)
+                                        : smem_desc_sw128(sb + k * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, idesc, accumulate);
+            accumulate = 1;
+          }
+          umma_commit(empty_bar(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (ok) umma_commit(tfull_bar(acc));
+    }
+    // Every MMA issued must finish before TMEM is released.
+    umma_commit(drain_bar);
+    mbar_wait(drain_bar, 0, p.err);
+  } else if (warp >= 2) {
+    // ---------------- epilogue ----------------
+    const int quarter = warp & 3;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++it) {
+      const GemmProb& pr = p.prob[find_prob(p, tile)];
+      const int local = tile - pr.tile_begin;
+      const int m0 = (local % pr.m_tiles) * BM;
+      const int n0 = (local / pr.m_tiles) * BN;
+      const int acc = it & 1;
+      const uint32_t use = static_cast<uint32_t>(it >> 1);
+      if (*abort_flag || !mbar_wait(tfull_bar(acc), use & 1u, p.err)) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int row = m0 + quarter * 32 + lane;
+      for (int c = 0; c < BN / 32; ++c) {
+        const int col0 = n0 + c * 32;
+        if (col0 >= pr.N) break;
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(
+            tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN + c * 32),
+            v);
+        tmem_ld_wait();
+        if (row < pr.M) store_chunk(pr, row, col0, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host: tensor maps
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D bf16 map: inner extent `inner` (contiguous), `outer` rows with row
+// stride ld elements, box 64 x box_outer, 128-byte swizzle, zero fill.
+kl_status make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, int64_t ld,
+                   uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return set_error(KL_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {64, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return set_error(KL_ERR_INVALID_ARG, "tensor map encode failed (%d): inner %llu outer %llu ld %lld",
+                     static_cast<int>(r), (unsigned long long)inner, (unsigned long long)outer,
+                     (long long)ld);
+  return KL_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------------------
+// fp32 CUDA-core GEMM
+// ---------------------------------------------------------------------------
+constexpr int FT = 64;   // tile edge
+constexpr int FK = 16;   // k step
+
+__global__ void __launch_bounds__(256) gemm_f32_kernel(int M, int N, int nseg, GemmSpec spec) {
+  __shared__ float As[FK][FT + 1];
+  __shared__ float Bs[FK][FT + 1];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int m0 = blockIdx.y * FT, n0 = blockIdx.x * FT;
+  float acc[4][4] = {};
+  for (int s = 0; s < nseg; ++s) {
+    const float* A = static_cast<const float*>(spec.A[s]);
+    const float* B = static_cast<const float*>(spec.B[s]);
+    const int K = spec.K[s];
+    const int64_t lda = spec.lda[s], ldb = spec.ldb[s];
+    for (int k0 = 0; k0 < K; k0 += FK) {
+      for (int i = threadIdx.x; i < FK * FT; i += 256) {
+        int kk, mm;
+        if (spec.a_mn) { kk = i / FT; mm = i % FT; } else { mm = i / FK; kk = i % FK; }
+        const int gm = m0 + mm, gk = k0 + kk;
+        float a = 0.f;
+        if (gm < M && gk < K) a = spec.a_mn ? A[gk * lda + gm] : A[gm * lda + gk];
+        As[kk][mm] = a;
+        int nn;
+        if (spec.b_mn) { kk = i / FT; nn = i % FT; } else { nn = i / FK; kk = i % FK; }
+        const int gn = n0 + nn;
+        const int gk2 = k0 + kk;
+        float b = 0.f;
+        if (gn < N && gk2 < K) b = spec.b_mn ? B[gk2 * ldb + gn] : B[gn * ldb + gk2];
+        Bs[kk][nn] = b;
+      }
+      __syncthreads();
+#pragma unroll
+      for (int kk = 0; kk < FK; ++kk) {
+        float a[4], b[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      }
+      __syncthreads();
+    }
+  }
+  for (int i = 0; i < 4; ++i) {
+    const int gm = m0 + ty * 4 + i;
+    if (gm >= M) continue;
+    for (int j = 0; j < 4; ++j) {
+      const int gn = n0 + tx * 4 + j;
+      if (gn >= N) continue;
+      float v = acc[i][j];
+      if (spec.R) v += static_cast<const float*>(spec.R)[gm * spec.ldr + gn];
+      static_cast<float*>(spec.C)[gm * spec.ldc + gn] = v;
+    }
+  }
+}
+
+}  // namespace
+
+kl_status gemm_bf16(const GemmSpec* specs, int nspec, cudaStream_t st) {
+  if (nspec < 1 || nspec > GEMM_MAX_PROB) return set_error(KL_ERR_INVALID_ARG, "gemm: %d problems", nspec);
+  GemmParams p;  // built on the host, passed by value into the launch
+  memset(&p, 0, sizeof(p));
+  int tiles = 0, tm = 0;
+  for (int i = 0; i < nspec; ++i) {
+    const GemmSpec& s = specs[i];
+    if (s.M < 1 || s.N < 1 || s.nseg < 1 || s.nseg > GEMM_MAX_SEG || !s.C)
+      return set_error(KL_ERR_INVALID_ARG, "gemm: bad problem %d (M %d N %d nseg %d)", i, s.M, s.N, s.nseg);
+    if (s.c_dtype != KL_BF16 && s.c_dtype != KL_F32)
+      return set_error(KL_ERR_INVALID_ARG, "gemm: bad output dtype");
+    GemmProb& pr = p.prob[i];
+    pr.M = s.M;
+    pr.N = s.N;
+    pr.nseg = s.nseg;
+    pr.a_mn = s.a_mn;
+    pr.b_mn = s.b_mn;
+    pr.tmap_base = tm;
+    for (int g = 0; g < s.nseg; ++g) {
+      if (!s.A[g] || !s.B[g] || s.K[g] < 1)
+        return set_error(KL_ERR_INVALID_ARG, "gemm: problem %d segment %d: null operand or K < 1", i, g);
+      if (!aligned16(s.A[g]) || !aligned16(s.B[g]) || (s.lda[g] % 8) || (s.ldb[g] % 8))
+        return set_error(KL_ERR_INVALID_ARG,
+                         "gemm: bf16 operands need 16-byte aligned bases and row strides that are multiples of 8");
+      if (!s.a_mn) KL_TRY(make_map(&p.tmA[tm + g], s.A[g], s.K[g], s.M, s.lda[g], BM));
+      else KL_TRY(make_map(&p.tmA[tm + g], s.A[g], s.M, s.K[g], s.lda[g], 64));
+      if (!s.b_mn) KL_TRY(make_map(&p.tmB[tm + g], s.B[g], s.K[g], s.N, s.ldb[g], BN));
+      else KL_TRY(make_map(&p.tmB[tm + g], s.B[g], s.N, s.K[g], s.ldb[g], 64));
+      pr.kb[g] = (s.K[g] + BK - 1) / BK;
+    }
+    tm += s.nseg;
+    pr.m_tiles = (s.M + BM - 1) / BM;
+    pr.n_tiles = (s.N + BN - 1) / BN;
+    pr.tile_begin = tiles;
+    tiles += pr.m_tiles * pr.n_tiles;
+    pr.C = s.C;
+    pr.ldc = s.ldc;
+    pr.c_f32 = s.c_dtype == KL_F32;
+    pr.R = s.R;
+    pr.ldr = s.ldr;
+    pr.r_f32 = s.r_dtype == KL_F32;
+    const size_t ce = dtype_size(s.c_dtype), re = dtype_size(s.r_dtype);
+    pr.vec_ok = aligned16(s.C) && (s.ldc * ce) % 16 == 0 &&
+                (!s.R || (aligned16(s.R) && (s.ldr * re) % 16 == 0));
+  }
+  p.nprob = nspec;
+  p.total_tiles = tiles;
+  p.err = device_error_word();
+  static uint64_t attr_done = 0;  // one bit per device ordinal
+  int dev = 0;
+  KL_CUDA(cudaGetDevice(&dev));
+  if (dev < 64 && !(attr_done >> dev & 1u)) {
+    KL_CUDA(cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(SMEM_BYTES)));
+    attr_done |= uint64_t(1) << dev;
+  }
+  double flops = 0.0, bytes = 0.0;
+  for (int i = 0; i < nspec; ++i) {
+    const GemmSpec& s = specs[i];
+    double ksum = 0.0;
+    for (int g = 0; g < s.nseg; ++g) ksum += s.K[g];
+    flops += 2.0 * s.M * s.N * ksum;
+    bytes += 2.0 * (s.M + s.N) * ksum + static_cast<double>(s.M) * s.N * dtype_size(s.c_dtype) +
+             (s.R ? static_cast<double>(s.M) * s.N * dtype_size(s.r_dtype) : 0.0);
+  }
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  ProfScope ps("gemm_bf16_tc", st, flops, bytes);
+  gemm_bf16_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(p);
+  KL_CUDA(cudaGetLastError());
+  return KL_OK;
+}
+
+kl_status gemm_f32(const GemmSpec& s, cudaStream_t st) {
+  if (s.M < 1 || s.N < 1 || s.nseg < 1 || s.nseg > GEMM_MAX_SEG || !s.C)
+    return set_error(KL_ERR_INVALID_ARG, "gemm f32: bad problem");
+  if (s.c_dtype != KL_F32 || (s.R && s.r_dtype != KL_F32))
+    return set_error(KL_ERR_UNSUPPORTED, "gemm f32: output and addend must be fp32");
+  for (int g = 0; g < s.nseg; ++g)
+    if (!s.A[g] || !s.B[g] || s.K[g] < 1) return set_error(KL_ERR_INVALID_ARG, "gemm f32: bad segment");
+  dim3 grid((s.N + FT - 1) / FT, (s.M + FT - 1) / FT);
+  double ksum = 0.0;
+  for (int g = 0; g < s.nseg; ++g) ksum += s.K[g];
+  ProfScope ps("gemm_f32", st, 2.0 * s.M * s.N * ksum, 4.0 * ((s.M + s.N) * ksum + 1.0 * s.M * s.N));
+  gemm_f32_kernel<<<grid, 256, 0, st>>>(s.M, s.N, s.nseg, s);
+  KL_CUDA(cudaGetLastError());
+  return KL_OK;
+}
+
+}  // namespace kl

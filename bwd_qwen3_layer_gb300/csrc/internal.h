@@ -1,0 +1,101 @@
+// Host-side declarations shared by the translation units of libkl.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kl.h"
+
+namespace kl {
+
+// ---------------------------------------------------------------------------
+// GEMM: C[M,N] = sum over segments s of op(A_s) op(B_s)^T (+ R)
+// ---------------------------------------------------------------------------
+constexpr int GEMM_MAX_SEG = 3;
+constexpr int GEMM_MAX_PROB = 4;
+
+struct GemmSpec {
+  int M = 0, N = 0;
+  int nseg = 1;
+  const void* A[GEMM_MAX_SEG] = {};
+  int64_t lda[GEMM_MAX_SEG] = {};
+  const void* B[GEMM_MAX_SEG] = {};
+  int64_t ldb[GEMM_MAX_SEG] = {};
+  int K[GEMM_MAX_SEG] = {};
+  int a_mn = 0;  // 0: A is [M,K] (K contiguous); 1: A stored [K,M]
+  int b_mn = 0;  // 0: B is [N,K]; 1: B stored [K,N]
+  void* C = nullptr;
+  int64_t ldc = 0;
+  int c_dtype = KL_BF16;
+  const void* R = nullptr;  // optional addend, [M,N] with row stride ldr
+  int64_t ldr = 0;
+  int r_dtype = KL_BF16;
+};
+
+// bf16 operands on the tcgen05 tensor cores; up to GEMM_MAX_PROB independent
+// problems share one persistent launch.
+kl_status gemm_bf16(const GemmSpec* specs, int nspec, cudaStream_t st);
+// fp32 operands on CUDA cores (one problem).
+kl_status gemm_f32(const GemmSpec& spec, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// elementwise / normalisation kernels (elementwise.cu)
+// ---------------------------------------------------------------------------
+kl_status rmsnorm_fwd(int rows, int width, int dtype, const void* x, const void* gamma, float eps,
+                      void* h, float* rstd, cudaStream_t st);
+size_t rmsnorm_bwd_ws(int rows, int width);
+kl_status rmsnorm_bwd(int rows, int width, int dtype, const void* dh, int dh_dtype, const void* x,
+                      const void* gamma, const float* rstd, const void* resid, void* dx,
+                      float* dgamma, void* ws, size_t ws_bytes, cudaStream_t st);
+kl_status rope(int B, int S, int heads, int d, float base, int dtype, void* x, int direction,
+               cudaStream_t st);
+// Rotary backward of an fp32 accumulator src [B*S, heads, d] into dst (dtype).
+kl_status rope_bwd_from_f32(int B, int S, int heads, int d, float base, int dtype,
+                            const float* src, void* dst, cudaStream_t st);
+kl_status convert_f32(int64_t n, int dtype, const float* src, void* dst, cudaStream_t st);
+kl_status swiglu_fwd(int64_t n, int dtype, const void* g, const void* u, void* m, cudaStream_t st);
+kl_status swiglu_bwd(int64_t n, int dtype, const void* dm, const void* g, const void* u, void* dg,
+                     void* du, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// attention (attention.cu)
+// ---------------------------------------------------------------------------
+kl_status attention_fwd(int B, int S, int Hq, int Hkv, int d, int dtype, const void* q,
+                        const void* k, const void* v, void* o, float* lse, cudaStream_t st);
+size_t attention_bwd_ws(int B, int S, int Hq, int Hkv, int d);
+// dq_out/dk_out/dv_out: fp32 accumulators [T,H*d] written by the kernel
+// (inside ws); the caller converts (with rotary backward) afterwards.
+kl_status attention_bwd_accum(int B, int S, int Hq, int Hkv, int d, int dtype, const void* q,
+                              const void* k, const void* v, const void* o, const float* lse,
+                              const void* dout, void* ws, size_t ws_bytes, float** dq_acc,
+                              float** dk_acc, float** dv_acc, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// cross entropy (ce.cu)
+// ---------------------------------------------------------------------------
+size_t ce_ws(int N);
+kl_status ce_argmax(int N, int V, const float* z, const int32_t* targets, float* loss,
+                    int32_t* argmax, void* dz, int dz_dtype, void* ws, size_t ws_bytes,
+                    cudaStream_t st);
+
+// Counts a kernel launch and, while profiling is on, brackets it with CUDA
+// events on `st` (construct immediately before the launch; the destructor
+// records the stop event right after it). `flops` and `bytes` are the
+// launch's algorithmic work.
+class ProfScope {
+ public:
+  ProfScope(const char* name, cudaStream_t st, double flops, double bytes);
+  ~ProfScope();
+  ProfScope(const ProfScope&) = delete;
+  ProfScope& operator=(const ProfScope&) = delete;
+
+ private:
+  cudaStream_t st_;
+  int ev_;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline size_t dtype_size(int dt) { return dt == KL_F32 ? 4 : 2; }
+
+}  // namespace kl

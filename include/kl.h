@@ -1,0 +1,311 @@
+/*
+ * kl.h - C ABI of libkl: forward and backward of one Qwen3-style decoder layer
+ * and the lm-head softmax cross-entropy with argmax, on one NVIDIA GB300
+ * (sm_103a).
+ *
+ * What is computed follows the public pages on the subject:
+ *   - "From-scratch GPU LLM training" (keilab.pages.dev/ai/gpu-llm and the
+ *     markdown twin, section "What is built"): six gradient kernels (matrix
+ *     multiply, RMSNorm, SiLU/SwiGLU, RoPE, softmax cross-entropy,
+ *     scaled-dot-product attention); a GPU layer backward chaining them to 10
+ *     tensors; a forward that saves activations for the backward; an lm-head
+ *     softmax cross-entropy fused with argmax in a single launch; a
+ *     layer-streaming driver that holds one layer's weights at a time.
+ *   - "KYNETRA FOUNDRY" (hyperbridge-deck.pages.dev): pre-norm decoder wiring
+ *     (RMSNorm -> causal self-attention -> SwiGLU FFN, each in a residual),
+ *     grouped-query attention, rotary position embedding, tiled attention
+ *     with an online softmax (an exact reordering of plain attention).
+ *
+ * Conventions for every entry point
+ *   - Tensors are dense, row-major, token-major: T = B*S rows, token
+ *     t = b*S + s sits at position s. Activations [T, width]; q [T, Hq*d];
+ *     k, v [T, Hkv*d]; lse [B, Hq, S] fp32. Projection weights are stored
+ *     [out, in] and applied as y = x W^T.
+ *   - Rotary planes pair element i with element i + d/2; plane i turns by
+ *     s * rope_base^(-2i/d). Query head h reads key/value head
+ *     floor(h * Hkv / Hq). Attention scale 1/sqrt(d); causal mask keeps
+ *     keys j <= i.
+ *   - RMSNorm: h = gamma * x / sqrt(mean(x^2) + eps), statistics in fp32.
+ *   - SwiGLU: m = silu(gate) * up.
+ *   - dtype KL_BF16: weights and activations are bf16, every matrix product
+ *     runs on the tensor cores with fp32 accumulation, normalisation and
+ *     softmax statistics in fp32. dtype KL_F32: everything fp32, matrix
+ *     products on CUDA cores (no TF32).
+ *   - Pointers marked "device" must be device memory (or managed memory) of
+ *     the current device, 16-byte aligned. The caller owns every buffer:
+ *     outputs, saved activations and workspace. Sizes come from the *_bytes
+ *     queries. Only kl_stream_* allocates, and frees in kl_stream_destroy.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Work is enqueued asynchronously; no entry point synchronises
+ *     the stream except where stated.
+ *   - Errors: every call returns a kl_status and never aborts the process.
+ *     On a non-KL_OK return kl_last_error() describes it (thread-local). A
+ *     bad argument found on the host enqueues no work. Faults found inside a
+ *     kernel (a target id out of range, a bounded wait that ran out) are
+ *     recorded in a device error word and reported by kl_device_status().
+ */
+#ifndef KL_H_
+#define KL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KL_API __attribute__((visibility("default")))
+#else
+#define KL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kl_status {
+  KL_OK = 0,
+  KL_ERR_INVALID_ARG = 1,  /* null pointer, misaligned buffer, bad size */
+  KL_ERR_UNSUPPORTED = 2,  /* shape or dtype this build does not handle */
+  KL_ERR_CUDA = 3,         /* a CUDA runtime call failed */
+  KL_ERR_TIMEOUT = 4,      /* a bounded wait inside a kernel ran out */
+  KL_ERR_NO_MEMORY = 5,    /* workspace too small, or allocation failed */
+  KL_ERR_DEVICE = 6        /* a kernel rejected its input (see kl_last_error) */
+} kl_status;
+
+typedef enum kl_dtype { KL_F32 = 0, KL_BF16 = 1 } kl_dtype;
+
+/* Device error word bits, reported by kl_device_status(). */
+#define KL_DEVERR_TIMEOUT 0x1u      /* a pipeline wait gave up */
+#define KL_DEVERR_TARGET 0x2u       /* a CE target id was outside [0, V) */
+
+KL_API const char* kl_version(void);
+KL_API const char* kl_status_str(kl_status s);
+/* Message of the last failing call on this host thread ("" if none). */
+KL_API const char* kl_last_error(void);
+/* Synchronises `stream`, then reads and clears the current device's error
+ * word. Returns KL_OK if it was zero, KL_ERR_TIMEOUT or KL_ERR_DEVICE if a
+ * kernel recorded a fault; *bits (may be NULL) receives the raw word. */
+KL_API kl_status kl_device_status(void* stream, uint32_t* bits);
+
+/* Launch profiler. Every kernel launch of the library is counted. While
+ * profiling is on, each launch is also bracketed by CUDA events on its
+ * stream and tagged with its algorithmic work (FLOPs for contractions,
+ * minimal HBM bytes for the memory-bound kernels). kl_profile_enable(1)
+ * clears earlier records; kl_profile_read synchronises on the last event and
+ * aggregates per kernel name into out[0..max) (returns the entry count, or
+ * -1 on a CUDA error). Not thread-safe across concurrent streams' timing. */
+typedef struct kl_prof_entry {
+  char name[48];
+  int32_t launches;
+  double ms;           /* summed event time                                */
+  double flops;        /* summed algorithmic FLOPs                         */
+  double bytes;        /* summed algorithmic HBM bytes                     */
+} kl_prof_entry;
+KL_API kl_status kl_profile_enable(int32_t on);
+KL_API int32_t kl_profile_read(kl_prof_entry* out, int32_t max_entries);
+KL_API uint64_t kl_launch_count(void);
+
+/* ------------------------------------------------------------------------ */
+/* Decoder layer ("From-scratch GPU LLM training", "What is built": forward  */
+/* with saved activations; layer backward orchestrating the six kernels)    */
+/* ------------------------------------------------------------------------ */
+
+typedef struct kl_layer_cfg {
+  int32_t B, S;        /* batch, sequence length; T = B*S tokens           */
+  int32_t H;           /* hidden width                                      */
+  int32_t Hq, Hkv, d;  /* query heads, key/value heads, head dim           */
+  int32_t I;           /* SwiGLU intermediate width                        */
+  float eps;           /* RMSNorm epsilon                                   */
+  float rope_base;     /* rotary base                                       */
+  int32_t dtype;       /* kl_dtype of weights, activations and arithmetic  */
+} kl_layer_cfg;
+
+/* Device pointers, dtype = cfg.dtype. gamma*: [H]. wq [Hq*d, H],
+ * wk/wv [Hkv*d, H], wo [H, Hq*d], wg/wu [I, H], wd [H, I]. */
+typedef struct kl_layer_weights {
+  const void *gamma1, *wq, *wk, *wv, *wo, *gamma2, *wg, *wu, *wd;
+} kl_layer_weights;
+
+/* Activations the forward saves for the backward (device, caller-owned).
+ * Element type is cfg.dtype unless noted. The forward also records its
+ * input X in `x`; X must stay alive and unchanged until the backward. */
+typedef struct kl_layer_saved {
+  const void* x;       /* [T,H] the forward's input (pointer recorded)     */
+  void* h1;            /* [T,H] RMSNorm-1 output                           */
+  float* rstd1;        /* [T]   1/sqrt(mean(x^2)+eps) of X                 */
+  void* q;             /* [T,Hq*d]  query after RoPE                       */
+  void* k;             /* [T,Hkv*d] key after RoPE                         */
+  void* v;             /* [T,Hkv*d] value                                  */
+  void* o;             /* [T,Hq*d]  attention output                       */
+  float* lse;          /* [B,Hq,S]  softmax logsumexp (natural log)        */
+  void* x2;            /* [T,H] residual stream after attention            */
+  void* h2;            /* [T,H] RMSNorm-2 output                           */
+  float* rstd2;        /* [T]                                              */
+  void* g;             /* [T,I] gate projection                            */
+  void* u;             /* [T,I] up projection                              */
+  void* m;             /* [T,I] silu(g) * u                                */
+} kl_layer_saved;
+
+/* Gradients written by the backward (device, caller-owned). Projection
+ * gradients have element type `dtype` (KL_F32 or KL_BF16; KL_F32 only when
+ * cfg.dtype is KL_F32 or for the streaming driver's clip); gain gradients
+ * dgamma1/dgamma2 are always fp32 [H]. Each is overwritten, not added to. */
+typedef struct kl_layer_grads {
+  void *gamma1, *wq, *wk, *wv, *wo, *gamma2, *wg, *wu, *wd;
+  int32_t dtype;
+} kl_layer_grads;
+
+/* Bytes of one buffer holding every saved activation, and a carve of such a
+ * buffer into a kl_layer_saved (base must be 256-byte aligned, device). */
+KL_API size_t kl_layer_saved_bytes(const kl_layer_cfg* cfg);
+KL_API kl_status kl_layer_saved_carve(const kl_layer_cfg* cfg, void* base, size_t bytes,
+                               kl_layer_saved* out);
+/* Workspace bytes of the forward and the backward (device, caller-owned,
+ * 256-byte aligned; contents undefined between calls). */
+KL_API size_t kl_layer_fwd_workspace_bytes(const kl_layer_cfg* cfg);
+KL_API size_t kl_layer_bwd_workspace_bytes(const kl_layer_cfg* cfg);
+
+/* Y = x2 + W_d(silu(W_g h2) * W_u h2), h2 = RMSNorm(x2; gamma2),
+ * x2 = X + W_o Attn(RoPE(W_q h1), RoPE(W_k h1), W_v h1), h1 = RMSNorm(X; gamma1).
+ * X, Y: [T,H] device, cfg.dtype. Fills *saved (its buffers caller-owned).
+ * KL_BF16 needs d = 128, H, Hq*d, Hkv*d and I multiples of 64, Hq % Hkv = 0. */
+KL_API kl_status kl_layer_forward(const kl_layer_cfg* cfg, const kl_layer_weights* w,
+                           const void* X, void* Y, kl_layer_saved* saved,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/* Backward of kl_layer_forward for upstream gradient dY [T,H]: writes dX
+ * [T,H] (cfg.dtype) and all nine parameter gradients into *grads. */
+KL_API kl_status kl_layer_backward(const kl_layer_cfg* cfg, const kl_layer_weights* w,
+                            const kl_layer_saved* saved, const void* dY, void* dX,
+                            const kl_layer_grads* grads, void* ws, size_t ws_bytes,
+                            void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* lm-head softmax cross-entropy + argmax ("From-scratch GPU LLM training",  */
+/* capability list: softmax cross-entropy and argmax fused in one launch)    */
+/* ------------------------------------------------------------------------ */
+
+typedef struct kl_lmhead_cfg {
+  int32_t N;        /* tokens                                               */
+  int32_t H;        /* hidden width                                         */
+  int32_t V;        /* vocabulary                                           */
+  int32_t dtype;    /* kl_dtype of X, W, dX, dlogits                        */
+  int32_t dw_dtype; /* kl_dtype of dW (KL_F32 allowed with KL_BF16 inputs)  */
+} kl_lmhead_cfg;
+
+KL_API size_t kl_lmhead_workspace_bytes(const kl_lmhead_cfg* cfg);
+
+/* z = X W^T (fp32 logits, kept in workspace); per row lse, loss_n =
+ * lse - z[target]; *loss = mean_n loss_n (device fp32 scalar); argmax[n] =
+ * lowest index of the row maximum of the fp32 logits; dlogits = (softmax -
+ * onehot)/N; dX = dlogits W; dW = dlogits^T X.
+ * X [N,H], W [V,H], targets int32 [N] in [0,V), argmax int32 [N],
+ * dlogits [N,V] (may be NULL: kept in workspace), dX [N,H], dW [V,H].
+ * All device. */
+KL_API kl_status kl_lmhead_ce_argmax(const kl_lmhead_cfg* cfg, const void* X, const void* W,
+                              const int32_t* targets, float* loss, int32_t* argmax,
+                              void* dlogits, void* dX, void* dW, void* ws,
+                              size_t ws_bytes, void* stream);
+
+/* The single-launch cross-entropy step alone, on given fp32 logits z [N,V]:
+ * loss (device fp32 scalar, mean over rows), argmax int32 [N], dlogits [N,V]
+ * of type dz_dtype, scaled by 1/N. Workspace: kl_ce_workspace_bytes(N). */
+KL_API size_t kl_ce_workspace_bytes(int32_t N);
+KL_API kl_status kl_ce_argmax(int32_t N, int32_t V, const float* z, const int32_t* targets,
+                       float* loss, int32_t* argmax, void* dlogits, int32_t dz_dtype,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* The individual gradient kernels (the pages' six), for callers composing   */
+/* their own layers and for kernel-level tests. Same layouts as above.       */
+/* ------------------------------------------------------------------------ */
+
+/* C[M,N] = op(A) op(B)^T (+ R), fp32 accumulation.
+ * a_mn_major = 0: A is [M,K] with row stride lda (K contiguous);
+ *            = 1: A is stored [K,M] with row stride lda (M contiguous).
+ * b_mn_major = 0: B is [N,K] row stride ldb; = 1: B is stored [K,N].
+ * A, B have type `dtype`; C has c_dtype; R (may be NULL) has c_dtype... or
+ * r_dtype, [M,N] row stride ldr. KL_BF16 runs on the tensor cores and needs
+ * lda, ldb, K multiples of 8; KL_F32 on CUDA cores. */
+KL_API kl_status kl_gemm(int32_t M, int32_t N, int32_t K, int32_t dtype,
+                  const void* A, int64_t lda, int32_t a_mn_major,
+                  const void* B, int64_t ldb, int32_t b_mn_major,
+                  void* C, int64_t ldc, int32_t c_dtype,
+                  const void* R, int64_t ldr, int32_t r_dtype, void* stream);
+
+/* h = gamma * x * rstd, rstd = 1/sqrt(mean(x^2)+eps); x,h [rows,width]. */
+KL_API kl_status kl_rmsnorm_fwd(int32_t rows, int32_t width, int32_t dtype, const void* x,
+                         const void* gamma, float eps, void* h, float* rstd, void* stream);
+/* dx = resid + rstd*(dn - n*mean(dn*n)), dn = dh*gamma, n = x*rstd;
+ * dgamma = sum_rows dh*n (fp32 [width]). dh has dh_dtype (fp32 or dtype);
+ * resid (may be NULL) and dx have dtype. Workspace: kl_rmsnorm_bwd_ws_bytes. */
+KL_API size_t kl_rmsnorm_bwd_ws_bytes(int32_t rows, int32_t width);
+KL_API kl_status kl_rmsnorm_bwd(int32_t rows, int32_t width, int32_t dtype, const void* dh,
+                         int32_t dh_dtype, const void* x, const void* gamma, const float* rstd,
+                         const void* resid, void* dx, float* dgamma, void* ws, size_t ws_bytes,
+                         void* stream);
+/* In-place rotary embedding of x [B*S, heads, d]; direction +1 forward,
+ * -1 backward (rotation by the negative angle). */
+KL_API kl_status kl_rope(int32_t B, int32_t S, int32_t heads, int32_t d, float base, int32_t dtype,
+                  void* x, int32_t direction, void* stream);
+/* m = silu(g)*u; and its backward dg = dm*u*silu'(g), du = dm*silu(g). */
+KL_API kl_status kl_swiglu_fwd(int64_t n, int32_t dtype, const void* g, const void* u, void* m,
+                        void* stream);
+KL_API kl_status kl_swiglu_bwd(int64_t n, int32_t dtype, const void* dm, const void* g, const void* u,
+                        void* dg, void* du, void* stream);
+/* Causal GQA attention: q [T,Hq*d], k/v [T,Hkv*d] -> o [T,Hq*d], lse fp32 [B,Hq,S]. */
+KL_API kl_status kl_attention_fwd(int32_t B, int32_t S, int32_t Hq, int32_t Hkv, int32_t d,
+                           int32_t dtype, const void* q, const void* k, const void* v, void* o,
+                           float* lse, void* stream);
+/* Backward: dq [T,Hq*d], dk/dv [T,Hkv*d] (dtype), recomputing the softmax
+ * from lse. Workspace: kl_attention_bwd_ws_bytes. */
+KL_API size_t kl_attention_bwd_ws_bytes(int32_t B, int32_t S, int32_t Hq, int32_t Hkv, int32_t d);
+KL_API kl_status kl_attention_bwd(int32_t B, int32_t S, int32_t Hq, int32_t Hkv, int32_t d,
+                           int32_t dtype, const void* q, const void* k, const void* v,
+                           const void* o, const float* lse, const void* dout, void* dq,
+                           void* dk, void* dv, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Layer streaming ("From-scratch GPU LLM training", capability list: the   */
+/* full-depth model runs holding one layer's weights at a time, lossless    */
+/* against the bulk forward; end-to-end smoke trains under gradient clip)   */
+/* ------------------------------------------------------------------------ */
+
+typedef struct kl_stream kl_stream;
+
+typedef struct kl_stream_cfg {
+  kl_layer_cfg layer;  /* dims of every layer; dtype must be KL_BF16 or F32 */
+  int32_t n_layers;
+  int32_t V;           /* lm-head vocabulary                               */
+} kl_stream_cfg;
+
+typedef struct kl_stream_result {
+  float loss;          /* mean CE loss                                     */
+  float total_norm;    /* global L2 norm of all weight gradients, unclipped */
+  float clip_coef;     /* min(1, max_norm / (total_norm + 1e-6))            */
+} kl_stream_result;
+
+/* host_layers[n_layers]: HOST pointers (pinned or pageable) to each layer's
+ * weights in cfg.layer.dtype; host_lm_head [V,H] host. The driver keeps the
+ * pointers (no copy of the weights); they must stay valid until destroy.
+ * Allocates two device weight slots, the lm-head weight, saved activations
+ * for every layer and workspace on the current device. */
+KL_API kl_status kl_stream_create(const kl_stream_cfg* cfg, const kl_layer_weights* host_layers,
+                           const void* host_lm_head, kl_stream** out);
+/* One training step: streams layer weights in (copy stream, double-buffered),
+ * forward through every layer saving activations, lm-head CE on `targets`,
+ * backward in reverse re-streaming the weights, global-norm clip of every
+ * weight gradient at clip_max_norm. X [T,H] and targets [T] are device.
+ * grads[n_layers] and dW_lm [V,H]: destination of the clipped gradients, fp32,
+ * device or host pinned memory (copies use cudaMemcpyDefault). *result is
+ * written after the call returns; the call synchronises `stream`. */
+KL_API kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets,
+                        float clip_max_norm, const kl_layer_grads* grads, void* dW_lm,
+                        kl_stream_result* result, void* stream);
+/* Peak device bytes the driver allocated (weights slots + activations + ws). */
+KL_API size_t kl_stream_device_bytes(const kl_stream* s);
+KL_API void kl_stream_destroy(kl_stream* s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KL_H_ */

@@ -1,0 +1,88 @@
+"""tcgen05 bf16 GEMM and fp32 CUDA-core GEMM against the oracle's matrix
+product, for every operand major-ness, with tiles left ragged on M, N and K."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from bwd_qwen3_layer_gb300 import synth
+from _parity import assert_rel, dev, host
+
+pytestmark = pytest.mark.gpu
+
+SHAPES = [(200, 296, 136), (256, 512, 1024), (136, 264, 72), (8, 8, 8), (1024, 1280, 320)]
+
+
+def _operands(M, N, K, seed, bf16=True):
+    A = synth.normal(seed, "gemm.A", (M, K))
+    B = synth.normal(seed, "gemm.B", (N, K))
+    R = synth.normal(seed, "gemm.R", (M, N))
+    if bf16:
+        A, B, R = synth.round_bf16(A), synth.round_bf16(B), synth.round_bf16(R)
+    return A, B, R
+
+
+def _store(X, mn, dtype):
+    """X is the logical [rows, K] operand; MN-major stores its transpose."""
+    t = dev(X.T if mn else X, dtype)
+    return t, t.shape[1]
+
+
+@pytest.mark.parametrize("a_mn", [0, 1])
+@pytest.mark.parametrize("b_mn", [0, 1])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_gemm_bf16_fp32_out(kl, a_mn, b_mn, M, N, K):
+    A, B, _ = _operands(M, N, K, 1)
+    a, lda = _store(A, a_mn, torch.bfloat16)
+    b, ldb = _store(B, b_mn, torch.bfloat16)
+    C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    kl.kl_gemm(M, N, K, kl.KL_BF16, a.data_ptr(), lda, a_mn, b.data_ptr(), ldb, b_mn, C.data_ptr(), N,
+               kl.KL_F32)
+    torch.cuda.synchronize()
+    assert_rel(host(C), O.linear(A, B), 1e-5, f"C {M}x{N}x{K} a_mn={a_mn} b_mn={b_mn}")
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1)])
+def test_gemm_bf16_out_with_residual(kl, a_mn, b_mn):
+    M, N, K = 392, 520, 264
+    A, B, R = _operands(M, N, K, 2)
+    a, lda = _store(A, a_mn, torch.bfloat16)
+    b, ldb = _store(B, b_mn, torch.bfloat16)
+    r = dev(R, torch.bfloat16)
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    kl.kl_gemm(M, N, K, kl.KL_BF16, a.data_ptr(), lda, a_mn, b.data_ptr(), ldb, b_mn, C.data_ptr(), N,
+               kl.KL_BF16, r.data_ptr(), N, kl.KL_BF16)
+    torch.cuda.synchronize()
+    assert_rel(host(C), O.linear(A, B) + R, 4e-3, "C+R bf16")
+
+
+def test_gemm_bf16_zero_is_exact(kl):
+    """A zero operand gives an exact zero product and the residual passes bit-exactly."""
+    M, N, K = 256, 256, 128
+    _, B, R = _operands(M, N, K, 3)
+    a = torch.zeros(M, K, dtype=torch.bfloat16, device="cuda")
+    b = dev(B, torch.bfloat16)
+    r = dev(R, torch.bfloat16)
+    C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    kl.kl_gemm(M, N, K, kl.KL_BF16, a.data_ptr(), K, 0, b.data_ptr(), K, 0, C.data_ptr(), N, kl.KL_BF16,
+               r.data_ptr(), N, kl.KL_BF16)
+    torch.cuda.synchronize()
+    assert torch.equal(C, r)
+
+
+@pytest.mark.parametrize("a_mn", [0, 1])
+@pytest.mark.parametrize("b_mn", [0, 1])
+def test_gemm_f32(kl, a_mn, b_mn):
+    M, N, K = 70, 93, 45
+    A, B, R = _operands(M, N, K, 4, bf16=False)
+    a, lda = _store(A, a_mn, torch.float32)
+    b, ldb = _store(B, b_mn, torch.float32)
+    r = dev(R, torch.float32)
+    C = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    kl.kl_gemm(M, N, K, kl.KL_F32, a.data_ptr(), lda, a_mn, b.data_ptr(), ldb, b_mn, C.data_ptr(), N,
+               kl.KL_F32, r.data_ptr(), N, kl.KL_F32)
+    torch.cuda.synchronize()
+    A32 = A.astype(np.float32).astype(np.float64)
+    B32 = B.astype(np.float32).astype(np.float64)
+    R32 = R.astype(np.float32).astype(np.float64)
+    assert_rel(host(C), O.linear(A32, B32) + R32, 1e-6, "f32")
