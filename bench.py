@@ -32,7 +32,7 @@ METRIC = "layer fwd+bwd tokens/s (Qwen3-32B dims, bf16, 1 GB300); % of tensor-co
 CONFIG = {"workload": "qwen3_32b_layer_fwd_bwd", "batch": 1, "seq_len": 2048, "hidden": 5120,
           "heads_q": 64, "heads_kv": 8, "head_dim": 128, "intermediate": 25600, "rope_base": 1e6,
           "causal": True, "l2": "inputs larger than L2 (975 MB of weights per step)"}
-CPU_SAMPLE_S = 128   # tokens per oracle step (full layer dims)
+CPU_SAMPLE_S = 1024  # tokens per oracle step (full layer dims)
 
 
 def _env_int(name, default):
