@@ -81,6 +81,7 @@ _SIGNATURES = {
     "kl_lmhead_ce_argmax": (ctypes.c_int, [_P(LmheadCfg), _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "kl_ce_workspace_bytes": (_sz, [_i32]),
     "kl_ce_argmax": (ctypes.c_int, [_i32, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _sz, _vp]),
+    "kl_ce_argmax_noalloc": (ctypes.c_int, [_i32, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _vp]),
     "kl_gemm": (ctypes.c_int, [_i32, _i32, _i32, _i32, _vp, _i64, _i32, _vp, _i64, _i32, _vp, _i64, _i32,
                                _vp, _i64, _i32, _vp]),
     "kl_rmsnorm_fwd": (ctypes.c_int, [_i32, _i32, _i32, _vp, _vp, _f32, _vp, _vp, _vp]),
@@ -207,6 +208,14 @@ def kl_ce_workspace_bytes(N: int) -> int:
 
 def kl_ce_argmax(N, V, z, targets, loss, argmax, dlogits, dz_dtype, ws, ws_bytes, stream=None) -> None:
     check(load().kl_ce_argmax(N, V, z, targets, loss, argmax, dlogits, dz_dtype, ws, ws_bytes, _stream(stream)))
+
+
+KL_CE_NOALLOC_MAX_ROWS = 65535
+
+
+def kl_ce_argmax_noalloc(N, V, z, targets, loss, argmax, dlogits, dz_dtype, stream=None) -> None:
+    """kl_ce_argmax without a workspace argument (static scratch inside libkl)."""
+    check(load().kl_ce_argmax_noalloc(N, V, z, targets, loss, argmax, dlogits, dz_dtype, _stream(stream)))
 
 
 def kl_gemm(M, N, K, dtype, A, lda, a_mn, B, ldb, b_mn, C, ldc, c_dtype, R=0, ldr=0, r_dtype=KL_BF16,

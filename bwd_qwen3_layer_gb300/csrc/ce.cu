@@ -14,6 +14,8 @@
 #include <limits.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "internal.h"
 #include "kl_common.cuh"
 
@@ -231,3 +233,60 @@ kl_status ce_argmax(int N, int V, const float* z, const int32_t* targets, float*
 }
 
 }  // namespace kl
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point.
+//
+// Some callers cannot hand the library a workspace: a host application whose
+// device memory is owned by its own pool and forbids raw cudaMalloc, a plugin
+// with no allocator hook, or a latency-bound loop where cudaMalloc's implicit
+// device synchronisation is not acceptable. For them the cross-entropy step
+// can run on scratch that is compiled into the library instead: a static
+// device array sized for KL_CE_NOALLOC_MAX_ROWS rows (about 256 KB), present
+// on every device that loads libkl until the process exits.
+//
+// The array's device address is looked up once per device, on the first call
+// made with that device current (cudaGetSymbolAddress); make that first call
+// before any stream capture. All calls share the one array and each leaves
+// its contents behind: the completion counter is cleared before every launch,
+// and calls whose kernels may run at the same time on the GPU (different
+// streams without ordering between them) race on it and must not be issued.
+// ---------------------------------------------------------------------------
+// Per-row losses (rows 0 .. KL_CE_NOALLOC_MAX_ROWS-1), then the completion
+// counter at the next 256-byte boundary: the layout ce_argmax() expects.
+static __device__ __align__(256) float g_ce_noalloc_scratch[KL_CE_NOALLOC_MAX_ROWS + 1 + 64];
+
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {};   // device address of the array, per device ordinal
+}  // namespace
+
+extern "C" kl_status kl_ce_argmax_noalloc(int32_t N, int32_t V, const float* z,
+                                          const int32_t* targets, float* loss, int32_t* argmax,
+                                          void* dlogits, int32_t dz_dtype, void* stream) {
+  using namespace kl;
+  if (N < 1 || N > KL_CE_NOALLOC_MAX_ROWS)
+    return set_error(KL_ERR_UNSUPPORTED,
+                     "kl_ce_argmax_noalloc: N = %d rows is outside [1, %d], the size of the static scratch",
+                     N, KL_CE_NOALLOC_MAX_ROWS);
+  if (dz_dtype != KL_F32 && dz_dtype != KL_BF16)
+    return set_error(KL_ERR_INVALID_ARG, "kl_ce_argmax_noalloc: bad dlogits dtype");
+  int dev = 0;
+  KL_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return set_error(KL_ERR_UNSUPPORTED, "kl_ce_argmax_noalloc: device %d", dev);
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+      void* p = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&p, g_ce_noalloc_scratch);
+      if (e != cudaSuccess) return cuda_check(e, "cudaGetSymbolAddress(static CE scratch)");
+      g_noalloc_ptr[dev] = p;
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  const size_t bytes = sizeof(g_ce_noalloc_scratch);
+  return ce_argmax(N, V, z, targets, loss, argmax, dlogits, dz_dtype, scratch, bytes,
+                   static_cast<cudaStream_t>(stream));
+}
+

@@ -213,6 +213,25 @@ KL_API kl_status kl_ce_argmax(int32_t N, int32_t V, const float* z, const int32_
                        float* loss, int32_t* argmax, void* dlogits, int32_t dz_dtype,
                        void* ws, size_t ws_bytes, void* stream);
 
+/* Allocation-free form of kl_ce_argmax. The pages have no counterpart: this
+ * is a library addition for callers that cannot give the library device
+ * memory -- an application whose device memory belongs to its own pool and
+ * forbids raw cudaMalloc, a plugin without an allocator hook, or a loop that
+ * cannot afford cudaMalloc's implicit device synchronisation. Same inputs,
+ * outputs and results as kl_ce_argmax, but the per-row losses and the
+ * completion counter live in a static device array compiled into libkl
+ * (KL_CE_NOALLOC_MAX_ROWS + 65 floats, about 256 KB), which every device that
+ * loads the library keeps until process exit. Calls no cudaMalloc/cudaFree.
+ * The first call on each device (with that device current) looks up the
+ * array's address; make that first call before any stream capture. Every call
+ * shares the array and the counter is cleared before each launch, so calls
+ * whose kernels may overlap on the GPU (unordered streams) race: do not issue
+ * them. N above KL_CE_NOALLOC_MAX_ROWS returns KL_ERR_UNSUPPORTED. */
+#define KL_CE_NOALLOC_MAX_ROWS 65535
+KL_API kl_status kl_ce_argmax_noalloc(int32_t N, int32_t V, const float* z, const int32_t* targets,
+                                      float* loss, int32_t* argmax, void* dlogits, int32_t dz_dtype,
+                                      void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* The individual gradient kernels (the pages' six), for callers composing   */
 /* their own layers and for kernel-level tests. Same layouts as above.       */
