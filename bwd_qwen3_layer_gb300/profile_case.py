@@ -1,0 +1,101 @@
+"""Runs one kernel of the layer at its Qwen3-32B workload shape through the C
+ABI, a few times, with a small device footprint: the target for Nsight
+Compute captures of a single kernel.
+
+  python -m bwd_qwen3_layer_gb300.profile_case CASE [--iters N]
+
+Cases (T = 2048 tokens, hidden 5120, 64/8 heads of 128, intermediate 25600):
+  gemm_gateup   [g|u] = h2 [Wg;Wu]^T  as one 2048 x 51200 x 5120 product (K-major)
+  gemm_qkv      q,k,v projections, 2048 x 10240 x 5120
+  gemm_dgrad    dm = dY Wd, 2048 x 25600 x 5120 (B MN-major)
+  gemm_wgrad    dWd = dY^T m, 5120 x 25600 x 2048 (both MN-major)
+  attn_fwd      causal GQA attention forward, S = 2048
+  attn_bwd      its backward
+  ce            CE + argmax + dlogits on 4096 x 151936 fp32 logits
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+import torch
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+import bwd_qwen3_layer_gb300 as K  # noqa: E402
+
+T, H, I, HQ, HKV, D = 2048, 5120, 25600, 64, 8, 128
+
+
+def _rand(shape, std=1.0, dtype=torch.bfloat16):
+    return (torch.randn(shape, device="cuda") * std).to(dtype)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case")
+    ap.add_argument("--iters", type=int, default=3)
+    a = ap.parse_args()
+    torch.manual_seed(0)
+    K.load()
+    bf = K.KL_BF16
+    if a.case.startswith("gemm"):
+        if a.case == "gemm_gateup":
+            M, N, Kd, amn, bmn = T, 2 * I, H, 0, 0
+        elif a.case == "gemm_qkv":
+            M, N, Kd, amn, bmn = T, HQ * D + 2 * HKV * D, H, 0, 0
+        elif a.case == "gemm_dgrad":
+            M, N, Kd, amn, bmn = T, I, H, 0, 1
+        elif a.case == "gemm_wgrad":
+            M, N, Kd, amn, bmn = H, I, T, 1, 1
+        else:
+            raise SystemExit(f"unknown case {a.case}")
+        A = _rand((Kd, M) if amn else (M, Kd))
+        B = _rand((Kd, N) if bmn else (N, Kd), 0.02)
+        C = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        lda, ldb = (M if amn else Kd), (N if bmn else Kd)
+
+        def run():
+            K.kl_gemm(M, N, Kd, bf, A.data_ptr(), lda, amn, B.data_ptr(), ldb, bmn, C.data_ptr(), N, bf)
+    elif a.case in ("attn_fwd", "attn_bwd"):
+        q, k, v = _rand((T, HQ * D)), _rand((T, HKV * D)), _rand((T, HKV * D))
+        o = torch.empty_like(q)
+        lse = torch.empty(HQ, T, dtype=torch.float32, device="cuda")
+        K.kl_attention_fwd(1, T, HQ, HKV, D, bf, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                           lse.data_ptr())
+        do = _rand((T, HQ * D))
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(K.kl_attention_bwd_ws_bytes(1, T, HQ, HKV, D), dtype=torch.uint8, device="cuda")
+
+        def run():
+            if a.case == "attn_fwd":
+                K.kl_attention_fwd(1, T, HQ, HKV, D, bf, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr())
+            else:
+                K.kl_attention_bwd(1, T, HQ, HKV, D, bf, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                   ws.data_ptr(), ws.numel())
+    elif a.case == "ce":
+        N, V = 4096, 151936
+        z = torch.randn(N, V, device="cuda") * 4
+        tgt = torch.randint(0, V, (N,), device="cuda", dtype=torch.int32)
+        loss = torch.zeros(1, device="cuda")
+        arg = torch.empty(N, dtype=torch.int32, device="cuda")
+        dz = torch.empty(N, V, dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(K.kl_ce_workspace_bytes(N), dtype=torch.uint8, device="cuda")
+
+        def run():
+            K.kl_ce_argmax(N, V, z.data_ptr(), tgt.data_ptr(), loss.data_ptr(), arg.data_ptr(), dz.data_ptr(), bf,
+                           ws.data_ptr(), ws.numel())
+    else:
+        raise SystemExit(f"unknown case {a.case}")
+    for _ in range(a.iters):
+        run()
+    torch.cuda.synchronize()
+    K.kl_device_status()
+    print(f"{a.case}: {a.iters} launches ok")
+
+
+if __name__ == "__main__":
+    main()
