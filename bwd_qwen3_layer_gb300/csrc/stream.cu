@@ -1,31 +1,493 @@
-// Layer-streaming driver (placeholder until the streamed stack is wired).
+// Layer-streaming driver ("From-scratch GPU LLM training", capability list:
+// the full-depth model runs holding one layer's weights at a time, lossless
+// against the bulk forward; the end-to-end smoke trains under gradient
+// clipping).
+//
+// Weights of the decoder layers stay in host memory. Two device weight slots
+// hold the layer being computed and the next one, uploaded on a separate copy
+// stream while the current layer runs (events order the slot reuse). One
+// training step: forward through every layer saving its activations, lm-head
+// cross-entropy on the last hidden state, backward in reverse (the last two
+// layers are still resident; earlier ones are uploaded again), then the global
+// L2 norm of every weight gradient (deterministic two-stage reduction in
+// fp64) and the clip coefficient min(1, max_norm / (norm + 1e-6)), applied to
+// every gradient where it was delivered (device memory, or pinned host memory
+// through its device-visible address). Gradients bound for host memory are
+// computed into one of two device staging slots and copied out on the copy
+// stream while the next layer's backward runs.
+//
+// If the caller's layer weights are already device memory the driver runs in
+// "bulk" mode: no slots, no uploads, the same kernels in the same order. Its
+// results are what the streamed mode is compared with.
+#include <string.h>
+
+#include <vector>
+
 #include "internal.h"
 #include "kl_common.cuh"
+
+namespace kl {
+namespace {
+
+constexpr int SUMSQ_BLOCKS = 256;
+constexpr int SUMSQ_THREADS = 256;
+constexpr double CLIP_EPS = 1e-6;
+
+struct GradRef {
+  float* p;
+  int64_t n;
+};
+
+// partial[b] = sum of squares of p over the elements block b owns (fixed
+// assignment, fixed reduction order: deterministic).
+__global__ void __launch_bounds__(SUMSQ_THREADS) sumsq_kernel(const float* __restrict__ p, int64_t n,
+                                                              double* __restrict__ partial) {
+  __shared__ double red[SUMSQ_THREADS / 32];
+  double acc = 0.0;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(SUMSQ_THREADS) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(SUMSQ_BLOCKS) * SUMSQ_THREADS) {
+    const double v = p[i];
+    acc += v * v;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int w = 0; w < SUMSQ_THREADS / 32; ++w) t += red[w];
+    partial[blockIdx.x] = t;
+  }
+}
+
+// result = {loss, norm, coef}; partials [count][SUMSQ_BLOCKS] summed in order.
+__global__ void clip_finalize_kernel(const double* __restrict__ partial, int count,
+                                     const float* __restrict__ loss, float max_norm,
+                                     float* __restrict__ result) {
+  __shared__ double red[SUMSQ_THREADS / 32];
+  double acc = 0.0;
+  for (int i = threadIdx.x; i < count * SUMSQ_BLOCKS; i += blockDim.x) acc += partial[i];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int w = 0; w < SUMSQ_THREADS / 32; ++w) t += red[w];
+    const double norm = sqrt(t);
+    double coef = static_cast<double>(max_norm) / (norm + CLIP_EPS);
+    if (coef > 1.0) coef = 1.0;
+    result[0] = *loss;
+    result[1] = static_cast<float>(norm);
+    result[2] = static_cast<float>(coef);
+  }
+}
+
+// Every listed gradient *= coef (skipped entirely when coef == 1).
+__global__ void clip_scale_kernel(const GradRef* __restrict__ refs, int count,
+                                  const float* __restrict__ result) {
+  const float coef = result[2];
+  if (coef == 1.0f) return;
+  for (int r = blockIdx.y; r < count; r += gridDim.y) {
+    float* p = refs[r].p;
+    const int64_t n = refs[r].n;
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+      p[i] *= coef;
+  }
+}
+
+size_t weight_elems(const kl_layer_cfg& c, int which) {
+  const size_t H = c.H, Dq = static_cast<size_t>(c.Hq) * c.d, Dkv = static_cast<size_t>(c.Hkv) * c.d,
+               I = c.I;
+  switch (which) {
+    case 0: return H;          // gamma1
+    case 1: return Dq * H;     // wq
+    case 2: return Dkv * H;    // wk
+    case 3: return Dkv * H;    // wv
+    case 4: return H * Dq;     // wo
+    case 5: return H;          // gamma2
+    case 6: return I * H;      // wg
+    case 7: return I * H;      // wu
+    default: return H * I;     // wd
+  }
+}
+
+const void** wfield(kl_layer_weights& w, int i) {
+  const void** f[9] = {&w.gamma1, &w.wq, &w.wk, &w.wv, &w.wo, &w.gamma2, &w.wg, &w.wu, &w.wd};
+  return f[i];
+}
+void** gfield(kl_layer_grads& g, int i) {
+  void** f[9] = {&g.gamma1, &g.wq, &g.wk, &g.wv, &g.wo, &g.gamma2, &g.wg, &g.wu, &g.wd};
+  return f[i];
+}
+
+bool is_device_ptr(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+// Device-visible address of a destination buffer (device, managed, or
+// page-locked host memory); nullptr if the GPU cannot reach it.
+void* device_visible(void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return p;
+  if (a.type == cudaMemoryTypeHost) return a.devicePointer;
+  return nullptr;
+}
+
+}  // namespace
+}  // namespace kl
 
 using namespace kl;
 
 struct kl_stream {
-  int unused;
+  kl_stream_cfg cfg;
+  int device = 0;
+  bool bulk = false;
+  std::vector<kl_layer_weights> layers;  // as given (host, or device in bulk mode)
+  const void* lm_host = nullptr;
+  std::vector<void*> allocs;
+  size_t device_bytes = 0;
+  // streamed mode
+  kl_layer_weights slot[2] = {};
+  int slot_layer[2] = {-1, -1};
+  cudaStream_t copy = nullptr;
+  cudaEvent_t ev_loaded[2] = {}, ev_used[2] = {}, ev_lm = nullptr;
+  cudaEvent_t ev_gdone[2] = {}, ev_gfree[2] = {};
+  const void* lm_w = nullptr;
+  // activations and workspace
+  std::vector<kl_layer_saved> saved;
+  std::vector<void*> hidden;   // output of layer l
+  void* dx[2] = {};
+  void* bwd_ws = nullptr;
+  size_t bwd_ws_bytes = 0;
+  void* lm_ws = nullptr;
+  size_t lm_ws_bytes = 0;
+  float* loss = nullptr;
+  int32_t* argmax = nullptr;
+  // gradient staging (host destinations) and the clip
+  kl_layer_grads gstage[2] = {};
+  float* dwlm_stage = nullptr;
+  double* partials = nullptr;
+  float* result = nullptr;
+  GradRef* refs = nullptr;
+  int max_refs = 0;
+
+  void* alloc(size_t bytes, kl_status* st) {
+    void* p = nullptr;
+    if (*st != KL_OK) return nullptr;
+    const cudaError_t e = cudaMalloc(&p, align_up(bytes, 256));
+    if (e != cudaSuccess) {
+      *st = cuda_check(e, "kl_stream: cudaMalloc");
+      return nullptr;
+    }
+    allocs.push_back(p);
+    device_bytes += align_up(bytes, 256);
+    return p;
+  }
+  void release() {
+    for (void* p : allocs) cudaFree(p);
+    allocs.clear();
+    for (int i = 0; i < 2; ++i) {
+      if (ev_loaded[i]) cudaEventDestroy(ev_loaded[i]);
+      if (ev_used[i]) cudaEventDestroy(ev_used[i]);
+      if (ev_gdone[i]) cudaEventDestroy(ev_gdone[i]);
+      if (ev_gfree[i]) cudaEventDestroy(ev_gfree[i]);
+    }
+    if (ev_lm) cudaEventDestroy(ev_lm);
+    if (copy) cudaStreamDestroy(copy);
+  }
 };
+
+namespace {
+
+kl_status upload_layer(kl_stream* s, int layer, int slot) {
+  const kl_layer_cfg& c = s->cfg.layer;
+  const size_t es = dtype_size(c.dtype);
+  KL_CUDA(cudaStreamWaitEvent(s->copy, s->ev_used[slot], 0));
+  for (int i = 0; i < 9; ++i)
+    KL_CUDA(cudaMemcpyAsync(const_cast<void*>(*wfield(s->slot[slot], i)), *wfield(s->layers[layer], i),
+                            weight_elems(c, i) * es, cudaMemcpyHostToDevice, s->copy));
+  KL_CUDA(cudaEventRecord(s->ev_loaded[slot], s->copy));
+  s->slot_layer[slot] = layer;
+  return KL_OK;
+}
+
+// Makes `layer` resident (uploading into the slot not holding `keep` if
+// needed) and returns its slot.
+kl_status acquire(kl_stream* s, int layer, int keep_slot, int* slot_out) {
+  for (int i = 0; i < 2; ++i)
+    if (s->slot_layer[i] == layer) {
+      *slot_out = i;
+      return KL_OK;
+    }
+  const int v = keep_slot == 0 ? 1 : 0;
+  KL_TRY(upload_layer(s, layer, v));
+  *slot_out = v;
+  return KL_OK;
+}
+
+kl_status sumsq(kl_stream* s, const float* p, int64_t n, int index, cudaStream_t st) {
+  ProfScope ps("grad_sumsq", st, 0.0, 4.0 * n);
+  sumsq_kernel<<<SUMSQ_BLOCKS, SUMSQ_THREADS, 0, st>>>(p, n, s->partials + static_cast<int64_t>(index) * SUMSQ_BLOCKS);
+  KL_CUDA(cudaGetLastError());
+  return KL_OK;
+}
+
+}  // namespace
 
 extern "C" {
 
 kl_status kl_stream_create(const kl_stream_cfg* cfg, const kl_layer_weights* host_layers,
                            const void* host_lm_head, kl_stream** out) {
-  (void)cfg; (void)host_layers; (void)host_lm_head;
-  if (out) *out = nullptr;
-  return set_error(KL_ERR_UNSUPPORTED, "layer streaming not built yet");
+  if (!cfg || !host_layers || !host_lm_head || !out)
+    return set_error(KL_ERR_INVALID_ARG, "kl_stream_create: null argument");
+  *out = nullptr;
+  if (cfg->n_layers < 1 || cfg->V < 1) return set_error(KL_ERR_INVALID_ARG, "kl_stream_create: bad n_layers or V");
+  const kl_layer_cfg& c = cfg->layer;
+  const size_t saved_bytes = kl_layer_saved_bytes(&c);
+  if (saved_bytes == 0) return KL_ERR_INVALID_ARG;  // message set by the size query's checks
+  kl_lmhead_cfg lc = {c.B * c.S, c.H, cfg->V, c.dtype, KL_F32};
+  const size_t lm_ws = kl_lmhead_workspace_bytes(&lc);
+  if (lm_ws == 0) return KL_ERR_UNSUPPORTED;
+  for (int l = 0; l < cfg->n_layers; ++l)
+    for (int i = 0; i < 9; ++i)
+      if (!*wfield(const_cast<kl_layer_weights&>(host_layers[l]), i))
+        return set_error(KL_ERR_INVALID_ARG, "kl_stream_create: layer %d weight %d is null", l, i);
+
+  kl_stream* s = new kl_stream();
+  s->cfg = *cfg;
+  KL_CUDA(cudaGetDevice(&s->device));
+  s->layers.assign(host_layers, host_layers + cfg->n_layers);
+  s->lm_host = host_lm_head;
+  s->bulk = is_device_ptr(host_layers[0].wq);
+  kl_status st = KL_OK;
+  const int L = cfg->n_layers;
+  const size_t T = static_cast<size_t>(c.B) * c.S, es = dtype_size(c.dtype);
+  if (!s->bulk) {
+    for (int k = 0; k < 2; ++k)
+      for (int i = 0; i < 9; ++i) *wfield(s->slot[k], i) = s->alloc(weight_elems(c, i) * es, &st);
+    void* lm = s->alloc(static_cast<size_t>(cfg->V) * c.H * es, &st);
+    s->lm_w = lm;
+    if (st == KL_OK) {
+      cudaError_t e = cudaStreamCreateWithFlags(&s->copy, cudaStreamNonBlocking);
+      for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
+        e = cudaEventCreateWithFlags(&s->ev_loaded[k], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->ev_used[k], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->ev_gdone[k], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->ev_gfree[k], cudaEventDisableTiming);
+      }
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->ev_lm, cudaEventDisableTiming);
+      if (e != cudaSuccess) st = cuda_check(e, "kl_stream_create: stream/event");
+    }
+  } else {
+    if (!is_device_ptr(host_lm_head)) st = set_error(KL_ERR_INVALID_ARG, "kl_stream_create: device layers need a device lm-head weight");
+    s->lm_w = host_lm_head;
+    if (st == KL_OK) {
+      cudaError_t e = cudaStreamCreateWithFlags(&s->copy, cudaStreamNonBlocking);
+      for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
+        e = cudaEventCreateWithFlags(&s->ev_gdone[k], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->ev_gfree[k], cudaEventDisableTiming);
+      }
+      if (e != cudaSuccess) st = cuda_check(e, "kl_stream_create: stream/event");
+    }
+  }
+  s->saved.resize(L);
+  s->hidden.resize(L);
+  for (int l = 0; l < L && st == KL_OK; ++l) {
+    void* mem = s->alloc(saved_bytes, &st);
+    if (st == KL_OK) st = kl_layer_saved_carve(&c, mem, saved_bytes, &s->saved[l]);
+    s->hidden[l] = s->alloc(T * c.H * es, &st);
+  }
+  s->dx[0] = s->alloc(T * c.H * es, &st);
+  s->dx[1] = s->alloc(T * c.H * es, &st);
+  s->bwd_ws_bytes = kl_layer_bwd_workspace_bytes(&c);
+  s->bwd_ws = s->alloc(s->bwd_ws_bytes, &st);
+  s->lm_ws_bytes = lm_ws;
+  s->lm_ws = s->alloc(lm_ws, &st);
+  s->loss = static_cast<float*>(s->alloc(sizeof(float), &st));
+  s->argmax = static_cast<int32_t*>(s->alloc(T * sizeof(int32_t), &st));
+  for (int k = 0; k < 2; ++k) {
+    for (int i = 0; i < 9; ++i) *gfield(s->gstage[k], i) = s->alloc(weight_elems(c, i) * 4, &st);
+    s->gstage[k].dtype = KL_F32;
+  }
+  s->dwlm_stage = static_cast<float*>(s->alloc(static_cast<size_t>(cfg->V) * c.H * 4, &st));
+  s->max_refs = 9 * L + 1;
+  s->partials = static_cast<double*>(s->alloc(static_cast<size_t>(s->max_refs) * SUMSQ_BLOCKS * 8, &st));
+  s->result = static_cast<float*>(s->alloc(4 * sizeof(float), &st));
+  s->refs = static_cast<GradRef*>(s->alloc(static_cast<size_t>(s->max_refs) * sizeof(GradRef), &st));
+  if (st != KL_OK) {
+    s->release();
+    delete s;
+    return st;
+  }
+  *out = s;
+  return KL_OK;
 }
 
 kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets, float clip_max_norm,
                         const kl_layer_grads* grads, void* dW_lm, kl_stream_result* result,
                         void* stream) {
-  (void)s; (void)X; (void)targets; (void)clip_max_norm; (void)grads; (void)dW_lm; (void)result; (void)stream;
-  return set_error(KL_ERR_UNSUPPORTED, "layer streaming not built yet");
+  if (!s || !X || !targets || !grads || !dW_lm || !result)
+    return set_error(KL_ERR_INVALID_ARG, "kl_stream_run: null argument");
+  if (!(clip_max_norm > 0.f)) return set_error(KL_ERR_INVALID_ARG, "kl_stream_run: clip_max_norm must be > 0");
+  int dev = -1;
+  KL_CUDA(cudaGetDevice(&dev));
+  if (dev != s->device) return set_error(KL_ERR_INVALID_ARG, "kl_stream_run: created on device %d, current %d", s->device, dev);
+  const kl_layer_cfg& c = s->cfg.layer;
+  const int L = s->cfg.n_layers;
+  const int T = c.B * c.S;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+
+  // where each gradient goes, and whether it needs staging
+  std::vector<kl_layer_grads> dst(grads, grads + L);
+  std::vector<GradRef> refs;
+  std::vector<bool> on_device(L);
+  for (int l = 0; l < L; ++l) {
+    if (dst[l].dtype != KL_F32) return set_error(KL_ERR_INVALID_ARG, "kl_stream_run: gradients must be fp32");
+    bool dev_all = true;
+    for (int i = 0; i < 9; ++i) {
+      void* p = *gfield(dst[l], i);
+      if (!p) return set_error(KL_ERR_INVALID_ARG, "kl_stream_run: layer %d gradient %d is null", l, i);
+      void* dp = device_visible(p);
+      if (!dp) return set_error(KL_ERR_INVALID_ARG, "kl_stream_run: layer %d gradient %d is not device-visible (pin it)", l, i);
+      if (!is_device_ptr(p)) dev_all = false;
+      refs.push_back({static_cast<float*>(dp), static_cast<int64_t>(weight_elems(c, i))});
+    }
+    on_device[l] = dev_all;
+  }
+  void* dwlm_dev = device_visible(dW_lm);
+  if (!dwlm_dev) return set_error(KL_ERR_INVALID_ARG, "kl_stream_run: dW_lm is not device-visible (pin it)");
+  const bool dwlm_on_device = is_device_ptr(dW_lm);
+  refs.push_back({static_cast<float*>(dwlm_dev), static_cast<int64_t>(s->cfg.V) * c.H});
+  KL_CUDA(cudaMemcpyAsync(s->refs, refs.data(), refs.size() * sizeof(GradRef), cudaMemcpyHostToDevice, cs));
+
+  const size_t es = dtype_size(c.dtype);
+  // lm-head weight upload (streamed mode), overlapped with the forward
+  if (!s->bulk) {
+    KL_CUDA(cudaMemcpyAsync(const_cast<void*>(s->lm_w), s->lm_host, static_cast<size_t>(s->cfg.V) * c.H * es,
+                            cudaMemcpyHostToDevice, s->copy));
+    KL_CUDA(cudaEventRecord(s->ev_lm, s->copy));
+    // the slots' contents may be stale (weights change between steps)
+    s->slot_layer[0] = s->slot_layer[1] = -1;
+    KL_CUDA(cudaEventRecord(s->ev_used[0], cs));
+    KL_CUDA(cudaEventRecord(s->ev_used[1], cs));
+  }
+  auto weights_for = [&](int l, int keep_slot, int* slot, kl_layer_weights* w) -> kl_status {
+    if (s->bulk) {
+      *w = s->layers[l];
+      *slot = -1;
+      return KL_OK;
+    }
+    KL_TRY(acquire(s, l, keep_slot, slot));
+    KL_CUDA(cudaStreamWaitEvent(cs, s->ev_loaded[*slot], 0));
+    *w = s->slot[*slot];
+    return KL_OK;
+  };
+
+  // ---------------- forward ----------------
+  int cur = -1;
+  for (int l = 0; l < L; ++l) {
+    kl_layer_weights w;
+    KL_TRY(weights_for(l, cur == 0 ? 1 : 0, &cur, &w));
+    if (!s->bulk && l + 1 < L) {
+      int nxt;
+      KL_TRY(acquire(s, l + 1, cur, &nxt));  // prefetch while layer l runs
+    }
+    const void* xin = l == 0 ? X : s->hidden[l - 1];
+    KL_TRY(kl_layer_forward(&c, &w, xin, s->hidden[l], &s->saved[l], nullptr, 0, cs));
+    if (!s->bulk) KL_CUDA(cudaEventRecord(s->ev_used[cur], cs));
+  }
+  // ---------------- lm-head ----------------
+  if (!s->bulk) KL_CUDA(cudaStreamWaitEvent(cs, s->ev_lm, 0));
+  kl_lmhead_cfg lc = {T, c.H, s->cfg.V, c.dtype, KL_F32};
+  float* dwlm_target = dwlm_on_device ? static_cast<float*>(dW_lm) : s->dwlm_stage;
+  KL_TRY(kl_lmhead_ce_argmax(&lc, s->hidden[L - 1], s->lm_w, targets, s->loss, s->argmax, nullptr, s->dx[0],
+                             dwlm_target, s->lm_ws, s->lm_ws_bytes, cs));
+  KL_TRY(sumsq(s, dwlm_target, static_cast<int64_t>(s->cfg.V) * c.H, 9 * L, cs));
+  if (!dwlm_on_device) {
+    KL_CUDA(cudaEventRecord(s->ev_gdone[0], cs));
+    KL_CUDA(cudaStreamWaitEvent(s->copy, s->ev_gdone[0], 0));
+    KL_CUDA(cudaMemcpyAsync(dW_lm, s->dwlm_stage, static_cast<size_t>(s->cfg.V) * c.H * 4, cudaMemcpyDeviceToHost,
+                            s->copy));
+  }
+  // ---------------- backward ----------------
+  int in = 0;
+  int stage_use = 0;
+  bool stage_busy[2] = {false, false};
+  for (int l = L - 1; l >= 0; --l) {
+    kl_layer_weights w;
+    KL_TRY(weights_for(l, cur, &cur, &w));
+    if (!s->bulk && l - 1 >= 0) {
+      int nxt;
+      KL_TRY(acquire(s, l - 1, cur, &nxt));
+    }
+    kl_layer_grads g;
+    int k = -1;
+    if (on_device[l]) {
+      g = dst[l];
+    } else {
+      k = stage_use++ & 1;
+      if (stage_busy[k]) KL_CUDA(cudaStreamWaitEvent(cs, s->ev_gfree[k], 0));
+      g = s->gstage[k];
+    }
+    KL_TRY(kl_layer_backward(&c, &w, &s->saved[l], s->dx[in], s->dx[in ^ 1], &g, s->bwd_ws, s->bwd_ws_bytes, cs));
+    in ^= 1;
+    for (int i = 0; i < 9; ++i)
+      KL_TRY(sumsq(s, static_cast<const float*>(*gfield(g, i)), static_cast<int64_t>(weight_elems(c, i)), 9 * l + i, cs));
+    if (!s->bulk) KL_CUDA(cudaEventRecord(s->ev_used[cur], cs));
+    if (k >= 0) {
+      KL_CUDA(cudaEventRecord(s->ev_gdone[k], cs));
+      KL_CUDA(cudaStreamWaitEvent(s->copy, s->ev_gdone[k], 0));
+      for (int i = 0; i < 9; ++i)
+        KL_CUDA(cudaMemcpyAsync(*gfield(dst[l], i), *gfield(g, i), weight_elems(c, i) * 4, cudaMemcpyDefault, s->copy));
+      KL_CUDA(cudaEventRecord(s->ev_gfree[k], s->copy));
+      stage_busy[k] = true;
+    }
+  }
+  // every copy-out must land before the clip scales the destinations
+  KL_CUDA(cudaEventRecord(s->ev_gdone[0], s->copy));
+  KL_CUDA(cudaStreamWaitEvent(cs, s->ev_gdone[0], 0));
+  {
+    ProfScope ps("clip_finalize", cs, 0.0, 8.0 * (9 * L + 1) * SUMSQ_BLOCKS);
+    clip_finalize_kernel<<<1, SUMSQ_THREADS, 0, cs>>>(s->partials, 9 * L + 1, s->loss, clip_max_norm, s->result);
+  }
+  KL_CUDA(cudaGetLastError());
+  {
+    double total = 0.0;
+    for (const GradRef& r : refs) total += static_cast<double>(r.n);
+    ProfScope ps("clip_scale", cs, 0.0, 8.0 * total);
+    dim3 grid(4 * num_sms(), 1);
+    grid.y = static_cast<unsigned>(refs.size() < 64 ? refs.size() : 64);
+    grid.x = static_cast<unsigned>(4 * num_sms() / grid.y + 1);
+    clip_scale_kernel<<<grid, 256, 0, cs>>>(s->refs, static_cast<int>(refs.size()), s->result);
+  }
+  KL_CUDA(cudaGetLastError());
+  float host_res[4] = {};
+  KL_CUDA(cudaMemcpyAsync(host_res, s->result, 3 * sizeof(float), cudaMemcpyDeviceToHost, cs));
+  KL_CUDA(cudaStreamSynchronize(cs));
+  result->loss = host_res[0];
+  result->total_norm = host_res[1];
+  result->clip_coef = host_res[2];
+  return KL_OK;
 }
 
-size_t kl_stream_device_bytes(const kl_stream* s) { (void)s; return 0; }
+size_t kl_stream_device_bytes(const kl_stream* s) { return s ? s->device_bytes : 0; }
 
-void kl_stream_destroy(kl_stream* s) { (void)s; }
-
+void kl_stream_destroy(kl_stream* s) {
+  if (!s) return;
+  cudaDeviceSynchronize();
+  s->release();
+  delete s;
 }
+
+}  // extern "C"

@@ -136,3 +136,54 @@ def run_lmhead(N, H, V, X_host, W_host, targets_host, dtype=KL_BF16, dw_dtype=No
     return {"loss": float(loss.item()), "argmax": arg.cpu().numpy().astype("int64"),
             "z": z.double().cpu().numpy(), "dz": dz.double().cpu().numpy(),
             "dX": dX.double().cpu().numpy(), "dW": dW.double().cpu().numpy()}
+
+
+def run_stream(cfg: LayerCfg, n_layers: int, V: int, layers_host: list, W_lm_host, X_host, targets_host,
+               clip: float, weights_on_device=False, grads_on_host=False, device="cuda", repeat=1):
+    """One (or `repeat`) layer-streaming training step(s) through kl_stream_*.
+
+    layers_host: per layer a dict of host arrays (synth names). Weights are
+    handed over as pinned host memory (streamed) or device memory (bulk).
+    Returns dict(result=(loss, norm, coef), grads=[{name: fp64 array}], dW_lm=array, device_bytes)."""
+    from . import (StreamCfg, kl_stream_create, kl_stream_destroy, kl_stream_device_bytes,
+                   kl_stream_run)
+
+    dt = cfg.dtype
+    keep = []
+
+    def place(a, dtype):
+        t = torch.as_tensor(a, dtype=torch.float64).to(dtype).contiguous()
+        t = t.to(device) if weights_on_device else t.pin_memory()
+        keep.append(t)
+        return t
+
+    hl = []
+    for lw in layers_host:
+        w = {n: place(lw[SYNTH_NAMES[n]], TORCH_DTYPE[dt]) for n in WEIGHT_FIELDS}
+        hl.append(weights_struct(w))
+    W = place(W_lm_host, TORCH_DTYPE[dt])
+    scfg = StreamCfg(cfg, n_layers, V)
+    h = kl_stream_create(scfg, hl, W.data_ptr())
+    try:
+        X = to_device(X_host, dt, device)
+        tgt = torch.as_tensor(targets_host, dtype=torch.int32).to(device)
+        gl, gs = [], []
+        for _ in range(n_layers):
+            g = {n: torch.empty(shp, dtype=torch.float32, device="cpu" if grads_on_host else device)
+                 for n, shp in weight_shapes(cfg).items()}
+            if grads_on_host:
+                g = {n: t.pin_memory() for n, t in g.items()}
+            gl.append(g)
+            gs.append(LayerGrads(*[g[n].data_ptr() for n in WEIGHT_FIELDS], KL_F32))
+        dW = torch.empty(V, cfg.H, dtype=torch.float32, device="cpu" if grads_on_host else device)
+        if grads_on_host:
+            dW = dW.pin_memory()
+        for _ in range(repeat):
+            res = kl_stream_run(h, X.data_ptr(), tgt.data_ptr(), clip, gs, dW.data_ptr())
+        torch.cuda.synchronize()
+        out = {"result": (res.loss, res.total_norm, res.clip_coef), "device_bytes": kl_stream_device_bytes(h),
+               "grads": [{SYNTH_NAMES[n]: g[n].double().cpu().numpy() for n in WEIGHT_FIELDS} for g in gl],
+               "dW_lm": dW.double().cpu().numpy()}
+    finally:
+        kl_stream_destroy(h)
+    return out
