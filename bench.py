@@ -1,16 +1,26 @@
-"""Benchmark: one Qwen3-32B-shaped decoder layer, forward + backward, bf16,
-on one GB300 (batch 1 x seq 2048, hidden 5120, 64 query / 8 KV heads of dim
-128, SwiGLU intermediate 25600, RoPE base 1e6, causal). Prints one JSON line.
+"""Benchmark of the GB300 Qwen3 layer path. Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload layer|attention|lmhead|stream]
 
-A step is one kl_layer_forward + kl_layer_backward over the whole batch.
+Workloads (Qwen3-32B dims: hidden 5120, 64 query / 8 KV heads of dim 128,
+SwiGLU intermediate 25600, RoPE base 1e6, causal; bf16):
+  layer      (default) one decoder layer forward + backward, batch 1 x seq 2048;
+             a step is kl_layer_forward + kl_layer_backward
+  attention  causal GQA attention forward + backward, batch 1 x seq 32768
+  lmhead     lm-head logits + single-launch CE/argmax + dX/dW, 4096 tokens,
+             vocab 151936
+  stream     8 layers streamed from pinned host memory, batch 2 x seq 4096,
+             lm-head CE, backward, global-norm clip at 1.0, gradients to
+             pinned host memory (one kl_stream_run per step)
+
 `value` is whole-job tokens/s with inputs resident in HBM; `e2e` is the same
-metric through the C ABI with pinned host buffers (H2D of X and dY and D2H of
-dX inside the timed region). The weights (975 MB) exceed L2 (129 MB), so no
-flush is needed between steps. N > 1 runs N independent replicas (weak
-scaling; the path needs no collective). `--impl reference` times the fp64
-CPU oracle on a bounded sample of the same workload.
+metric through the C ABI with each step's inputs copied from pinned host
+memory and its result read back inside the timed region. Every workload's
+inputs exceed L2 (129 MB), so no flush is needed between steps. N > 1 runs N
+independent replicas (weak scaling; the path needs no collective).
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+workload.
 """
 from __future__ import annotations
 
@@ -27,12 +37,20 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-WORKLOAD = dict(B=1, S=2048, H=5120, Hq=64, Hkv=8, d=128, I=25600, eps=1e-6, rope_base=1e6)
+QWEN = dict(H=5120, Hq=64, Hkv=8, d=128, I=25600, eps=1e-6, rope_base=1e6)
 METRIC = "layer fwd+bwd tokens/s (Qwen3-32B dims, bf16, 1 GB300); % of tensor-core peak"
-CONFIG = {"workload": "qwen3_32b_layer_fwd_bwd", "batch": 1, "seq_len": 2048, "hidden": 5120,
-          "heads_q": 64, "heads_kv": 8, "head_dim": 128, "intermediate": 25600, "rope_base": 1e6,
-          "causal": True, "l2": "inputs larger than L2 (975 MB of weights per step)"}
-CPU_SAMPLE_S = 1024  # tokens per oracle step (full layer dims)
+WORKLOADS = {
+    "layer": dict(B=1, S=2048, desc="qwen3_32b_layer_fwd_bwd"),
+    "attention": dict(B=1, S=32768, desc="gqa_attention_fwd_bwd_S32768"),
+    "lmhead": dict(N=4096, V=151936, desc="lmhead_ce_argmax_fwd_bwd_N4096_V151936"),
+    "stream": dict(B=2, S=4096, L=8, V=151936, clip=1.0, desc="stream_8_layers_T8192_ce_clip"),
+}
+METRICS = {
+    "layer": METRIC,
+    "attention": "causal GQA attention fwd+bwd tokens/s (seq 32768, 64/8 heads, d 128, bf16, 1 GB300)",
+    "lmhead": "lm-head CE+argmax fwd+bwd tokens/s (4096 tokens, vocab 151936, bf16, 1 GB300)",
+    "stream": "8-layer streamed training step tokens/s (batch 2 x 4096, bf16, 1 GB300)",
+}
 
 
 def _env_int(name, default):
@@ -50,6 +68,22 @@ def peaks():
                 "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "src": "measured"}
     except Exception:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+
+
+def traffic_record():
+    """DRAM bytes per launch of the dominant kernel from a committed ncu
+    capture, keyed by the source file it was taken from (null if it changed)."""
+    try:
+        import hashlib
+
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)
+        src = os.path.join(ROOT, rec["source"])
+        with open(src, "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+        return rec if digest == rec["source_sha256"] else None
+    except Exception:
+        return None
 
 
 class Clocks:
@@ -103,20 +137,6 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def build_inputs(torch, K, L, synth, device, seed=0):
-    cfg = L.make_cfg(**WORKLOAD, dtype=K.KL_BF16)
-    w = {}
-    for n, shp in L.weight_shapes(cfg).items():
-        if n.startswith("gamma"):
-            w[n] = synth.device_normal(shp, 0.02, 1.0, seed, f"layer0.{n}", torch.bfloat16, device)
-        else:
-            w[n] = synth.device_normal(shp, 0.02, 0.0, seed, f"layer0.{n}", torch.bfloat16, device)
-    T = WORKLOAD["B"] * WORKLOAD["S"]
-    X = synth.device_normal((T, WORKLOAD["H"]), 1.0, 0.0, seed, "X", torch.bfloat16, device)
-    dY = synth.device_normal((T, WORKLOAD["H"]), 1.0, 0.0, seed, "dY", torch.bfloat16, device)
-    return cfg, w, X, dY
-
-
 def read_profile(K):
     lib = K.load()
 
@@ -125,14 +145,177 @@ def read_profile(K):
                     ("flops", ctypes.c_double), ("bytes", ctypes.c_double)]
 
     arr = (Entry * 64)()
-    lib.kl_profile_read.restype = ctypes.c_int32
-    lib.kl_profile_read.argtypes = [ctypes.c_void_p, ctypes.c_int32]
     n = lib.kl_profile_read(ctypes.cast(arr, ctypes.c_void_p), 64)
     out = {}
     for i in range(max(n, 0)):
         e = arr[i]
         out[e.name.decode()] = {"launches": e.launches, "ms": e.ms, "flops": e.flops, "bytes": e.bytes}
     return out
+
+
+# ----------------------------------------------------------------------------
+# workloads: each returns (units_per_step, step(), e2e_step(), h2d, d2h, config)
+# ----------------------------------------------------------------------------
+
+def setup_layer(torch, K, L, synth, device, seed):
+    wl = WORKLOADS["layer"]
+    cfg = L.make_cfg(wl["B"], wl["S"], **QWEN, dtype=K.KL_BF16)
+    w = {}
+    for n, shp in L.weight_shapes(cfg).items():
+        w[n] = synth.device_normal(shp, 0.02, 1.0 if n.startswith("gamma") else 0.0, seed, f"layer0.{n}",
+                                   torch.bfloat16, device)
+    T = wl["B"] * wl["S"]
+    X = synth.device_normal((T, QWEN["H"]), 1.0, 0.0, seed, "X", torch.bfloat16, device)
+    dY = synth.device_normal((T, QWEN["H"]), 1.0, 0.0, seed, "dY", torch.bfloat16, device)
+    buf = L.LayerBuffers(cfg, device)
+    ws = L.weights_struct(w)
+    grads, gst = L.alloc_grads(cfg, device, K.KL_BF16)
+    Y, dX = torch.empty_like(X), torch.empty_like(X)
+    stream = torch.cuda.current_stream(device)
+
+    def run(x, dy, dx):
+        K.kl_layer_forward(cfg, ws, x.data_ptr(), Y.data_ptr(), buf.saved, buf.fwd_ws.data_ptr(),
+                           buf.fwd_ws.numel(), stream)
+        K.kl_layer_backward(cfg, ws, buf.saved, dy.data_ptr(), dx.data_ptr(), gst, buf.bwd_ws.data_ptr(),
+                            buf.bwd_ws.numel(), stream)
+
+    hX, hdY = X.cpu().pin_memory(), dY.cpu().pin_memory()
+    hdX = torch.empty_like(hX).pin_memory()
+    X2, dY2, dX2 = torch.empty_like(X), torch.empty_like(X), torch.empty_like(X)
+
+    def e2e():
+        X2.copy_(hX, non_blocking=True)
+        dY2.copy_(hdY, non_blocking=True)
+        run(X2, dY2, dX2)
+        hdX.copy_(dX2, non_blocking=True)
+
+    keep = (w, buf, grads, X, dY, Y, dX, hX, hdY, hdX, X2, dY2, dX2)
+    cfgd = {"workload": wl["desc"], "batch": wl["B"], "seq_len": wl["S"], "hidden": QWEN["H"],
+            "heads_q": QWEN["Hq"], "heads_kv": QWEN["Hkv"], "head_dim": QWEN["d"], "intermediate": QWEN["I"],
+            "rope_base": QWEN["rope_base"], "causal": True,
+            "l2": "inputs larger than L2 (975 MB of weights per step)"}
+    return T, (lambda: run(X, dY, dX)), e2e, 2 * X.numel() * 2, X.numel() * 2, cfgd, keep
+
+
+def setup_attention(torch, K, L, synth, device, seed):
+    wl = WORKLOADS["attention"]
+    B, S, Hq, Hkv, d = wl["B"], wl["S"], QWEN["Hq"], QWEN["Hkv"], QWEN["d"]
+    T = B * S
+    bf = torch.bfloat16
+    q = synth.device_normal((T, Hq * d), 1.0, 0.0, seed, "att.q", bf, device)
+    k = synth.device_normal((T, Hkv * d), 1.0, 0.0, seed, "att.k", bf, device)
+    v = synth.device_normal((T, Hkv * d), 1.0, 0.0, seed, "att.v", bf, device)
+    do = synth.device_normal((T, Hq * d), 1.0, 0.0, seed, "att.do", bf, device)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, S, dtype=torch.float32, device=device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(K.kl_attention_bwd_ws_bytes(B, S, Hq, Hkv, d), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def run(qq, kk, vv, dd):
+        K.kl_attention_fwd(B, S, Hq, Hkv, d, K.KL_BF16, qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), o.data_ptr(),
+                           lse.data_ptr(), stream)
+        K.kl_attention_bwd(B, S, Hq, Hkv, d, K.KL_BF16, qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), o.data_ptr(),
+                           lse.data_ptr(), dd.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), ws.data_ptr(),
+                           ws.numel(), stream)
+
+    hq, hk, hv, hdo = (t.cpu().pin_memory() for t in (q, k, v, do))
+    hdq = torch.empty_like(hq).pin_memory()
+    q2, k2, v2, do2 = (torch.empty_like(t) for t in (q, k, v, do))
+
+    def e2e():
+        for dst, src in ((q2, hq), (k2, hk), (v2, hv), (do2, hdo)):
+            dst.copy_(src, non_blocking=True)
+        run(q2, k2, v2, do2)
+        hdq.copy_(dq, non_blocking=True)
+
+    keep = (q, k, v, do, o, lse, dq, dk, dv, ws, hq, hk, hv, hdo, hdq, q2, k2, v2, do2)
+    cfgd = {"workload": wl["desc"], "batch": B, "seq_len": S, "heads_q": Hq, "heads_kv": Hkv, "head_dim": d,
+            "causal": True, "l2": "inputs larger than L2 (Q/K/V/dO 1.2 GB)"}
+    h2d = sum(t.numel() * 2 for t in (q, k, v, do))
+    return T, (lambda: run(q, k, v, do)), e2e, h2d, dq.numel() * 2, cfgd, keep
+
+
+def setup_lmhead(torch, K, L, synth, device, seed):
+    wl = WORKLOADS["lmhead"]
+    N, V, H = wl["N"], wl["V"], QWEN["H"]
+    bf = torch.bfloat16
+    X = synth.device_normal((N, H), 1.0, 0.0, seed, "lm.X", bf, device)
+    W = synth.device_normal((V, H), 0.02, 0.0, seed, "lm.W", bf, device)
+    tgt = synth.device_randint((N,), V, seed, "lm.targets", device)
+    cfg = L.lmhead_cfg(N, H, V, K.KL_BF16)
+    loss = torch.zeros(1, dtype=torch.float32, device=device)
+    arg = torch.empty(N, dtype=torch.int32, device=device)
+    dX = torch.empty_like(X)
+    dW = torch.empty_like(W)
+    ws = L.lmhead_ws(cfg, device)
+    stream = torch.cuda.current_stream(device)
+
+    def run(x, t):
+        K.kl_lmhead_ce_argmax(cfg, x.data_ptr(), W.data_ptr(), t.data_ptr(), loss.data_ptr(), arg.data_ptr(), 0,
+                              dX.data_ptr(), dW.data_ptr(), ws.data_ptr(), ws.numel(), stream)
+
+    hX, ht = X.cpu().pin_memory(), tgt.cpu().pin_memory()
+    hloss = torch.empty(1, dtype=torch.float32).pin_memory()
+    X2, t2 = torch.empty_like(X), torch.empty_like(tgt)
+
+    def e2e():
+        X2.copy_(hX, non_blocking=True)
+        t2.copy_(ht, non_blocking=True)
+        run(X2, t2)
+        hloss.copy_(loss, non_blocking=True)
+
+    keep = (X, W, tgt, loss, arg, dX, dW, ws, hX, ht, hloss, X2, t2)
+    cfgd = {"workload": wl["desc"], "tokens": N, "hidden": H, "vocab": V,
+            "l2": "inputs larger than L2 (W 1.56 GB, fp32 logits 2.49 GB)"}
+    return N, (lambda: run(X, tgt)), e2e, X.numel() * 2 + N * 4, 4, cfgd, keep
+
+
+def setup_stream(torch, K, L, synth, device, seed):
+    wl = WORKLOADS["stream"]
+    B, S, nl, V = wl["B"], wl["S"], wl["L"], wl["V"]
+    T, H = B * S, QWEN["H"]
+    cfg = L.make_cfg(B, S, **QWEN, dtype=K.KL_BF16)
+    bf = torch.bfloat16
+    hosts, structs = [], []
+    for li in range(nl):
+        w = {}
+        for n, shp in L.weight_shapes(cfg).items():
+            t = synth.device_normal(shp, 0.02, 1.0 if n.startswith("gamma") else 0.0, seed, f"l{li}.{n}", bf, device)
+            w[n] = t.cpu().pin_memory()
+        hosts.append(w)
+        structs.append(L.weights_struct(w))
+    W = synth.device_normal((V, H), 0.02, 0.0, seed, "lm.W", bf, device).cpu().pin_memory()
+    X = synth.device_normal((T, H), 1.0, 0.0, seed, "X", bf, device)
+    tgt = synth.device_randint((T,), V, seed, "lm.targets", device)
+    h = K.kl_stream_create(K.StreamCfg(cfg, nl, V), structs, W.data_ptr())
+    grads, gs = [], []
+    for _ in range(nl):
+        g = {n: torch.empty(shp, dtype=torch.float32).pin_memory() for n, shp in L.weight_shapes(cfg).items()}
+        grads.append(g)
+        gs.append(K.LayerGrads(*[g[n].data_ptr() for n in K.WEIGHT_FIELDS], K.KL_F32))
+    dW = torch.empty(V, H, dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream(device)
+
+    def run(x, t):
+        K.kl_stream_run(h, x.data_ptr(), t.data_ptr(), wl["clip"], gs, dW.data_ptr(), stream)
+
+    hX, ht = X.cpu().pin_memory(), tgt.cpu().pin_memory()
+    X2, t2 = torch.empty_like(X), torch.empty_like(tgt)
+
+    def e2e():
+        X2.copy_(hX, non_blocking=True)
+        t2.copy_(ht, non_blocking=True)
+        run(X2, t2)          # returns after the step (loss, norm, coef read back)
+
+    keep = (hosts, W, X, tgt, grads, dW, hX, ht, X2, t2, h)
+    cfgd = {"workload": wl["desc"], "layers": nl, "batch": B, "seq_len": S, "hidden": H, "vocab": V,
+            "clip_max_norm": wl["clip"], "weights": "pinned host, two device slots",
+            "grads": "fp32 to pinned host", "l2": "inputs larger than L2"}
+    return T, (lambda: run(X, tgt)), e2e, X.numel() * 2 + T * 4, 12, cfgd, keep
+
+
+SETUP = {"layer": setup_layer, "attention": setup_attention, "lmhead": setup_lmhead, "stream": setup_stream}
 
 
 def bench_ours(args, rank, world, local_rank, dist):
@@ -145,25 +328,10 @@ def bench_ours(args, rank, world, local_rank, dist):
     torch.cuda.set_device(local_rank)
     device = torch.device("cuda", local_rank)
     lib = K.load()
-    lib.kl_profile_enable.argtypes = [ctypes.c_int32]
-    lib.kl_launch_count.restype = ctypes.c_uint64
-    cfg, w, X, dY = build_inputs(torch, K, L, synth, device, seed=rank)
-    T = WORKLOAD["B"] * WORKLOAD["S"]
-    buf = L.LayerBuffers(cfg, device)
-    ws = L.weights_struct(w)
-    grads, gst = L.alloc_grads(cfg, device, K.KL_BF16)
-    Y = torch.empty_like(X)
-    dX = torch.empty_like(X)
+    units, step, e2e, h2d, d2h, cfgd, keep = SETUP[args.workload](torch, K, L, synth, device, seed=rank)
     stream = torch.cuda.current_stream(device)
-
-    def step(x_ptr, dy_ptr, dx_ptr):
-        K.kl_layer_forward(cfg, ws, x_ptr, Y.data_ptr(), buf.saved, buf.fwd_ws.data_ptr(), buf.fwd_ws.numel(),
-                           stream)
-        K.kl_layer_backward(cfg, ws, buf.saved, dy_ptr, dx_ptr, gst, buf.bwd_ws.data_ptr(), buf.bwd_ws.numel(),
-                            stream)
-
     for _ in range(args.warmup):
-        step(X.data_ptr(), dY.data_ptr(), dX.data_ptr())
+        step()
     torch.cuda.synchronize()
     K.kl_device_status(stream)
 
@@ -182,7 +350,7 @@ def bench_ours(args, rank, world, local_rank, dist):
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        step(X.data_ptr(), dY.data_ptr(), dX.data_ptr())
+        step()
     e1.record(stream)
     barrier()
     launches = lib.kl_launch_count() - n0
@@ -191,63 +359,112 @@ def bench_ours(args, rank, world, local_rank, dist):
     prof = read_profile(K)
     lib.kl_profile_enable(0)
 
-    # ---- end-to-end through the C ABI with pinned host buffers ----
-    hX = X.cpu().pin_memory()
-    hdY = dY.cpu().pin_memory()
-    hdX = torch.empty_like(hX).pin_memory()
-    dX2, X2, dY2 = torch.empty_like(X), torch.empty_like(X), torch.empty_like(X)
+    # ---- end to end through the C ABI with pinned host buffers ----
     barrier()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
     for _ in range(args.steps):
-        X2.copy_(hX, non_blocking=True)
-        dY2.copy_(hdY, non_blocking=True)
-        step(X2.data_ptr(), dY2.data_ptr(), dX2.data_ptr())
-        hdX.copy_(dX2, non_blocking=True)
+        e2e()
     f1.record(stream)
     barrier()
     ms_e2e = f0.elapsed_time(f1)
     K.kl_device_status(stream)
-
+    if args.workload == "stream":
+        K.kl_stream_destroy(keep[-1])
     if dist is not None:
         t = torch.tensor([ms, ms_e2e], device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms, ms_e2e = float(t[0]), float(t[1])
-    return dict(ms=ms, ms_e2e=ms_e2e, prof=prof, clocks=clk, launches=int(launches), T=T,
-                h2d=2 * X.numel() * X.element_size(), d2h=dX.numel() * dX.element_size())
+    return dict(ms=ms, ms_e2e=ms_e2e, prof=prof, clocks=clk, launches=int(launches), units=units, h2d=h2d,
+                d2h=d2h, config=cfgd)
 
 
-def oracle_sample(steps: int):
-    """Times the fp64 oracle's layer forward+backward at full layer dims on a
-    bounded token sample. Returns (tokens_per_s, seconds, cores, description)."""
+# ----------------------------------------------------------------------------
+# the oracle on a bounded sample of the workload (cpu_baseline, --impl reference)
+# ----------------------------------------------------------------------------
+
+def _oracle_weights(rng, H, Hq, Hkv, d, I):
+    Dq, Dkv = Hq * d, Hkv * d
+    n = lambda *s: 0.02 * rng.standard_normal(s)  # noqa: E731
+    return {"gamma1": 1 + n(H), "Wq": n(Dq, H), "Wk": n(Dkv, H), "Wv": n(Dkv, H), "Wo": n(H, Dq),
+            "gamma2": 1 + n(H), "Wg": n(I, H), "Wu": n(I, H), "Wd": n(H, I)}
+
+
+def oracle_sample(workload: str, steps: int):
+    """Times the fp64 oracle on a bounded sample of `workload`.
+    Returns (tokens_per_s, seconds_per_step, cores, description)."""
     import numpy as np
 
     import oracle as O
 
-    S = CPU_SAMPLE_S
-    W = WORKLOAD
-    cfg = O.LayerConfig(B=1, S=S, H=W["H"], Hq=W["Hq"], Hkv=W["Hkv"], d=W["d"], I=W["I"],
-                        eps=W["eps"], rope_base=W["rope_base"])
     rng = np.random.default_rng(0)
-    Dq, Dkv = W["Hq"] * W["d"], W["Hkv"] * W["d"]
-    w = {"gamma1": 1 + 0.02 * rng.standard_normal(W["H"]), "Wq": 0.02 * rng.standard_normal((Dq, W["H"])),
-         "Wk": 0.02 * rng.standard_normal((Dkv, W["H"])), "Wv": 0.02 * rng.standard_normal((Dkv, W["H"])),
-         "Wo": 0.02 * rng.standard_normal((W["H"], Dq)), "gamma2": 1 + 0.02 * rng.standard_normal(W["H"]),
-         "Wg": 0.02 * rng.standard_normal((W["I"], W["H"])), "Wu": 0.02 * rng.standard_normal((W["I"], W["H"])),
-         "Wd": 0.02 * rng.standard_normal((W["H"], W["I"]))}
-    X = rng.standard_normal((S, W["H"]))
-    dY = rng.standard_normal((S, W["H"]))
+    Q = QWEN
+    cores = os.cpu_count()
     times = []
+    if workload == "layer":
+        S = 1024
+        cfg = O.LayerConfig(B=1, S=S, H=Q["H"], Hq=Q["Hq"], Hkv=Q["Hkv"], d=Q["d"], I=Q["I"])
+        w = _oracle_weights(rng, Q["H"], Q["Hq"], Q["Hkv"], Q["d"], Q["I"])
+        X, dY = rng.standard_normal((S, Q["H"])), rng.standard_normal((S, Q["H"]))
+
+        def one():
+            Y, saved = O.layer_forward(cfg, w, X)
+            O.layer_backward(cfg, w, saved, dY)
+        units = S
+        desc = f"one full-dims layer fwd+bwd on {S} tokens (batch 1, seq {S})"
+    elif workload == "attention":
+        S = 2048
+        q = rng.standard_normal((S, Q["Hq"], Q["d"]))
+        k = rng.standard_normal((S, Q["Hkv"], Q["d"]))
+        v = rng.standard_normal((S, Q["Hkv"], Q["d"]))
+        do = rng.standard_normal((S, Q["Hq"], Q["d"]))
+
+        def one():
+            O.attention_fwd(q, k, v, 1, S)
+            O.attention_bwd(q, k, v, do, 1, S)
+        units = S
+        desc = (f"causal GQA attention fwd+bwd at seq {S} (64/8 heads, d 128); tokens/s at seq 32768 is "
+                f"this figure x {S}/32768 (quadratic cost)")
+    elif workload == "lmhead":
+        N, V = 256, WORKLOADS["lmhead"]["V"]
+        X = rng.standard_normal((N, Q["H"]))
+        W = 0.02 * rng.standard_normal((V, Q["H"]))
+        t = rng.integers(0, V, N)
+
+        def one():
+            O.lmhead_ce(X, W, t)
+        units = N
+        desc = f"lm-head CE+argmax fwd+bwd on {N} tokens, hidden 5120, vocab {V}"
+    else:   # stream: one layer + the head on a token sample, scaled to 8 layers
+        S = 256
+        cfg = O.LayerConfig(B=1, S=S, H=Q["H"], Hq=Q["Hq"], Hkv=Q["Hkv"], d=Q["d"], I=Q["I"])
+        w = _oracle_weights(rng, Q["H"], Q["Hq"], Q["Hkv"], Q["d"], Q["I"])
+        V = WORKLOADS["stream"]["V"]
+        X = rng.standard_normal((S, Q["H"]))
+        W = 0.02 * rng.standard_normal((V, Q["H"]))
+        t = rng.integers(0, V, S)
+        nl = WORKLOADS["stream"]["L"]
+
+        def one():
+            Y, saved = O.layer_forward(cfg, w, X)
+            t0 = time.perf_counter()
+            head = O.lmhead_ce(Y, W, t)
+            th = time.perf_counter() - t0
+            O.layer_backward(cfg, w, saved, head["dX"])
+            return th
+        units = S
+        desc = (f"one full-dims layer fwd+bwd plus the lm-head CE on {S} tokens; step time = "
+                f"{nl} x layer + head")
     for _ in range(max(1, steps)):
         t0 = time.perf_counter()
-        Y, saved = O.layer_forward(cfg, w, X)
-        O.layer_backward(cfg, w, saved, dY)
-        times.append(time.perf_counter() - t0)
+        th = one()
+        dt = time.perf_counter() - t0
+        if workload == "stream":
+            dt = nl * (dt - th) + th
+        times.append(dt)
     sec = statistics.median(times)
-    cores = os.cpu_count()
-    desc = (f"fp64 numpy oracle, one full-dims layer fwd+bwd on {S} tokens (batch 1, seq {S}) per step, "
-            f"median of {len(times)}; BLAS threads default to all {cores} host cores")
-    return S / sec, sec, cores, desc
+    desc = f"fp64 numpy oracle: {desc}; median of {len(times)}; BLAS threads default to all {cores} host cores"
+    return units / sec, sec, cores, desc
 
 
 def main():
@@ -256,23 +473,26 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="layer", choices=list(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.workload == "stream" and "--steps" not in sys.argv:
+        args.steps = 5
     world = _env_int("WORLD_SIZE", 1)
     rank = _env_int("RANK", 0)
     local_rank = _env_int("LOCAL_RANK", 0)
+    metric = METRICS[args.workload]
 
     if args.impl == "reference":
         if rank != 0:
             return
         steps = max(1, min(args.steps, 3))
-        for _ in range(min(args.warmup, 1)):
-            pass
-        tps, sec, cores, desc = oracle_sample(steps)
-        line = {"metric": METRIC, "value": tps, "unit": "tokens/s", "n_gpus": args.gpus, "steps": steps,
+        tps, sec, cores, desc = oracle_sample(args.workload, steps)
+        line = {"metric": metric, "value": tps, "unit": "tokens/s", "n_gpus": args.gpus, "steps": steps,
                 "warmup": 0, "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": CONFIG, "impl": "reference",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": {"workload": WORKLOADS[args.workload]["desc"]}, "impl": "reference",
                 "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                  "sample": desc},
                 "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -291,47 +511,58 @@ def main():
             dist.destroy_process_group()
         return
     pk = peaks()
-    tokens = r["T"] * args.steps * world
+    tokens = r["units"] * args.steps * world
     value = tokens / (r["ms"] / 1e3)
     e2e = tokens / (r["ms_e2e"] / 1e3)
+    prof = r["prof"]
+    total_ms = sum(v["ms"] for v in prof.values()) or 1.0
     kernels = {}
-    for name, e in sorted(r["prof"].items(), key=lambda kv: -kv[1]["ms"]):
+    for name, e in sorted(prof.items(), key=lambda kv: -kv[1]["ms"]):
         per = e["ms"] / e["launches"] / 1e3
         ent = {"launches": e["launches"], "ms_per_launch": round(e["ms"] / e["launches"], 4),
-               "share": round(e["ms"] / sum(v["ms"] for v in r["prof"].values()), 4)}
+               "share": round(e["ms"] / total_ms, 4)}
         if e["flops"] > 0:
             a = e["flops"] / e["launches"] / per / 1e12
             ent.update(achieved=round(a, 2), unit="TFLOP/s", frac=round(a / pk["bf16_tflops_sustained"], 4))
-        else:
+        elif e["bytes"] > 0:
             a = e["bytes"] / e["launches"] / per / 1e9
             ent.update(achieved=round(a, 1), unit="GB/s", frac=round(a / pk["hbm_gbs"], 4))
         kernels[name] = ent
-    dom = max(r["prof"].items(), key=lambda kv: kv[1]["ms"])
-    dname, d = dom
+    # roofline of the dominant kernel: labelled launches of one kernel are
+    # grouped (every "gemm.*" call site runs gemm_bf16_tc_kernel)
+    groups = {}
+    for name, e in prof.items():
+        key = "gemm_bf16_tc" if name.startswith("gemm.") or name == "gemm" else name
+        g = groups.setdefault(key, {"launches": 0, "ms": 0.0, "flops": 0.0, "bytes": 0.0})
+        for f in g:
+            g[f] += e[f]
+    dname, d = max(groups.items(), key=lambda kv: kv[1]["ms"])
     per = d["ms"] / d["launches"] / 1e3
+    trec = traffic_record()
+    traffic = trec["bytes_per_launch"].get(dname) if trec and args.workload in trec.get("workloads", []) else None
     if d["flops"] > 0:
         ach = d["flops"] / d["launches"] / per / 1e12
         roof = {"kernel": dname, "bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops_sustained"], 4), "traffic": None,
-                "peak_src": f"{pk['src']} bf16_tflops_sustained"}
+                "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops_sustained"], 4), "traffic": traffic,
+                "peak_src": f"{pk['src']} bf16_tflops_sustained (kernel timed inside the step)"}
     else:
         ach = d["bytes"] / d["launches"] / per / 1e9
         roof = {"kernel": dname, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"],
-                "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4), "traffic": None,
+                "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4), "traffic": traffic,
                 "peak_src": f"{pk['src']} hbm_gbs"}
-    total_flops = sum(e["flops"] for e in r["prof"].values()) / args.steps
+    total_flops = sum(e["flops"] for e in prof.values()) / args.steps
     agg_tflops = total_flops / (r["ms"] / args.steps / 1e3) / 1e12
-    line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+    line = {"metric": metric, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(r["ms"] / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": CONFIG | {"parallelism": f"replicas x{world}"},
+            "config": r["config"] | {"parallelism": f"replicas x{world}"},
             "tensor_frac_aggregate": round(agg_tflops / pk["bf16_tflops_sustained"], 4),
             "aggregate_tflops": round(agg_tflops, 2),
             "roofline": roof, "kernels": kernels, "gpu_launches": r["launches"], "clocks": r["clocks"],
             "e2e": {"value": round(e2e, 1), "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
                     "d2h_bytes_per_step": r["d2h"]}}
     if world == 1 and not args.no_cpu_baseline:
-        tps, sec, cores, desc = oracle_sample(1)
+        tps, sec, cores, desc = oracle_sample(args.workload, 1)
         line["cpu_baseline"] = {"value": round(tps, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": desc}
     print(json.dumps(line), flush=True)

@@ -58,9 +58,9 @@ namespace {
 
 bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-kl_status run_gemms(int dtype, GemmSpec* specs, int n, cudaStream_t st) {
-  if (dtype == KL_BF16) return gemm_bf16(specs, n, st);
-  for (int i = 0; i < n; ++i) KL_TRY(gemm_f32(specs[i], st));
+kl_status run_gemms(int dtype, GemmSpec* specs, int n, cudaStream_t st, const char* label) {
+  if (dtype == KL_BF16) return gemm_bf16(specs, n, st, label);
+  for (int i = 0; i < n; ++i) KL_TRY(gemm_f32(specs[i], st, label));
   return KL_OK;
 }
 
@@ -104,8 +104,8 @@ struct Dims {
 
 kl_status check_cfg(const kl_layer_cfg* c, Dims* o) {
   if (!c) return set_error(KL_ERR_INVALID_ARG, "null cfg");
-  if (c->B < 1 || c->S < 1 || c->H < 1 || c->Hq < 1 || c->Hkv < 1 || c->d < 2 || c->I < 1 ||
-      (c->d & 1) || c->Hq % c->Hkv || c->eps < 0.f || !(c->rope_base > 0.f))
+  if (c->B < 1 || c->S < 1 || c->H < 1 || c->Hq < 1 || c->Hkv < 1 || c->d < 8 || c->I < 1 ||
+      (c->d % 8) || c->Hq % c->Hkv || c->eps < 0.f || !(c->rope_base > 0.f))
     return set_error(KL_ERR_INVALID_ARG, "bad layer cfg (B %d S %d H %d Hq %d Hkv %d d %d I %d)",
                      c->B, c->S, c->H, c->Hq, c->Hkv, c->d, c->I);
   if (c->dtype != KL_BF16 && c->dtype != KL_F32)
@@ -285,25 +285,24 @@ kl_status kl_layer_forward(const kl_layer_cfg* cfg, const kl_layer_weights* w, c
     GemmSpec g[3] = {proj(T, D.Dq, H, s->h1, H, w->wq, H, s->q, D.Dq, dt),
                      proj(T, D.Dkv, H, s->h1, H, w->wk, H, s->k, D.Dkv, dt),
                      proj(T, D.Dkv, H, s->h1, H, w->wv, H, s->v, D.Dkv, dt)};
-    KL_TRY(run_gemms(dt, g, 3, st));
+    KL_TRY(run_gemms(dt, g, 3, st, "gemm.fwd_qkv"));
   }
-  KL_TRY(rope(D.B, D.S, D.Hq, D.d, cfg->rope_base, dt, s->q, 1, st));
-  KL_TRY(rope(D.B, D.S, D.Hkv, D.d, cfg->rope_base, dt, s->k, 1, st));
+  KL_TRY(rope_qk(D.B, D.S, D.Hq, D.Hkv, D.d, cfg->rope_base, dt, s->q, s->k, 1, st));
   KL_TRY(attention_fwd(D.B, D.S, D.Hq, D.Hkv, D.d, dt, s->q, s->k, s->v, s->o, s->lse, st));
   {
     GemmSpec g = proj(T, H, D.Dq, s->o, D.Dq, w->wo, D.Dq, s->x2, H, dt, X, dt);
-    KL_TRY(run_gemms(dt, &g, 1, st));
+    KL_TRY(run_gemms(dt, &g, 1, st, "gemm.fwd_o"));
   }
   KL_TRY(rmsnorm_fwd(T, H, dt, s->x2, w->gamma2, cfg->eps, s->h2, s->rstd2, st));
   {
     GemmSpec g[2] = {proj(T, I, H, s->h2, H, w->wg, H, s->g, I, dt),
                      proj(T, I, H, s->h2, H, w->wu, H, s->u, I, dt)};
-    KL_TRY(run_gemms(dt, g, 2, st));
+    KL_TRY(run_gemms(dt, g, 2, st, "gemm.fwd_gateup"));
   }
   KL_TRY(swiglu_fwd(static_cast<int64_t>(T) * I, dt, s->g, s->u, s->m, st));
   {
     GemmSpec g = proj(T, H, I, s->m, I, w->wd, I, Y, H, dt, s->x2, dt);
-    KL_TRY(run_gemms(dt, &g, 1, st));
+    KL_TRY(run_gemms(dt, &g, 1, st, "gemm.fwd_down"));
   }
   return KL_OK;
 }
@@ -336,7 +335,7 @@ kl_status kl_layer_backward(const kl_layer_cfg* cfg, const kl_layer_weights* w,
   // MLP: dm = dY Wd, dWd = dY^T m
   {
     GemmSpec g[2] = {dgrad(T, I, H, dY, w->wd, b.dm, dt), wgrad(H, I, T, dY, s->m, gr->wd, gdt)};
-    KL_TRY(run_gemms(dt, g, 2, st));
+    KL_TRY(run_gemms(dt, g, 2, st, "gemm.bwd_down"));
   }
   KL_TRY(swiglu_bwd(static_cast<int64_t>(T) * I, dt, b.dm, s->g, s->u, b.dg, b.du, st));
   {
@@ -345,7 +344,7 @@ kl_status kl_layer_backward(const kl_layer_cfg* cfg, const kl_layer_weights* w,
     dh.A[1] = b.du; dh.lda[1] = I; dh.B[1] = w->wu; dh.ldb[1] = H; dh.K[1] = I;
     GemmSpec g[3] = {dh, wgrad(I, H, T, b.dg, s->h2, gr->wg, gdt),
                      wgrad(I, H, T, b.du, s->h2, gr->wu, gdt)};
-    KL_TRY(run_gemms(dt, g, 3, st));
+    KL_TRY(run_gemms(dt, g, 3, st, "gemm.bwd_gateup"));
   }
   KL_TRY(rmsnorm_bwd(T, H, dt, b.dh2, KL_F32, s->x2, w->gamma2, s->rstd2, dY, b.dx2,
                      static_cast<float*>(gr->gamma2), b.norm, b.norm_bytes, st));
@@ -353,14 +352,13 @@ kl_status kl_layer_backward(const kl_layer_cfg* cfg, const kl_layer_weights* w,
   {
     GemmSpec g[2] = {dgrad(T, D.Dq, H, b.dx2, w->wo, b.dO, dt),
                      wgrad(H, D.Dq, T, b.dx2, s->o, gr->wo, gdt)};
-    KL_TRY(run_gemms(dt, g, 2, st));
+    KL_TRY(run_gemms(dt, g, 2, st, "gemm.bwd_o"));
   }
   float *dq_acc = nullptr, *dk_acc = nullptr, *dv_acc = nullptr;
   KL_TRY(attention_bwd_accum(D.B, D.S, D.Hq, D.Hkv, D.d, dt, s->q, s->k, s->v, s->o, s->lse, b.dO,
                              b.att, b.att_bytes, &dq_acc, &dk_acc, &dv_acc, st));
-  KL_TRY(rope_bwd_from_f32(D.B, D.S, D.Hq, D.d, cfg->rope_base, dt, dq_acc, b.dq, st));
-  KL_TRY(rope_bwd_from_f32(D.B, D.S, D.Hkv, D.d, cfg->rope_base, dt, dk_acc, b.dk, st));
-  KL_TRY(convert_f32(static_cast<int64_t>(T) * D.Dkv, dt, dv_acc, b.dv, st));
+  KL_TRY(rope_bwd_convert(D.B, D.S, D.Hq, D.Hkv, D.d, cfg->rope_base, dt, dq_acc, dk_acc, dv_acc, b.dq,
+                          b.dk, b.dv, st));
   {
     GemmSpec dh = dgrad(T, H, D.Dq, b.dq, w->wq, b.dh1, KL_F32);
     dh.nseg = 3;
@@ -369,7 +367,7 @@ kl_status kl_layer_backward(const kl_layer_cfg* cfg, const kl_layer_weights* w,
     GemmSpec g[4] = {dh, wgrad(D.Dq, H, T, b.dq, s->h1, gr->wq, gdt),
                      wgrad(D.Dkv, H, T, b.dk, s->h1, gr->wk, gdt),
                      wgrad(D.Dkv, H, T, b.dv, s->h1, gr->wv, gdt)};
-    KL_TRY(run_gemms(dt, g, 4, st));
+    KL_TRY(run_gemms(dt, g, 4, st, "gemm.bwd_qkv"));
   }
   KL_TRY(rmsnorm_bwd(T, H, dt, b.dh1, KL_F32, s->x, w->gamma1, s->rstd1, b.dx2, dX,
                      static_cast<float*>(gr->gamma1), b.norm, b.norm_bytes, st));
@@ -394,7 +392,8 @@ static kl_status check_lm(const kl_lmhead_cfg* c) {
 size_t kl_lmhead_workspace_bytes(const kl_lmhead_cfg* c) {
   if (check_lm(c) != KL_OK) return 0;
   const size_t NV = static_cast<size_t>(c->N) * c->V;
-  return align_up(NV * 4, 256) + align_up(NV * dtype_size(c->dtype), 256) + ce_ws(c->N);
+  return align_up(NV * 4, 256) + align_up(NV * dtype_size(c->dtype), 256) + ce_ws(c->N) +
+         align_up(static_cast<size_t>(c->N) * c->H * 4, 256);
 }
 
 kl_status kl_lmhead_ce_argmax(const kl_lmhead_cfg* c, const void* X, const void* W,
@@ -415,15 +414,17 @@ kl_status kl_lmhead_ce_argmax(const kl_lmhead_cfg* c, const void* X, const void*
   float* z = static_cast<float*>(cv.take(NV * 4));
   void* dz_ws = cv.take(NV * dtype_size(dt));
   void* ce = cv.take(ce_ws(N));
+  float* dx_acc = static_cast<float*>(cv.take(static_cast<size_t>(N) * H * 4));
   void* dz = dlogits ? dlogits : dz_ws;
   {
     GemmSpec g = proj(N, V, H, X, H, W, H, z, V, KL_F32);
-    KL_TRY(run_gemms(dt, &g, 1, st));
+    KL_TRY(run_gemms(dt, &g, 1, st, "gemm.lm_logits"));
   }
   KL_TRY(ce_argmax(N, V, z, targets, loss, argmax, dz, dt, ce, ce_ws(N), st));
   {
     GemmSpec g[2] = {dgrad(N, H, V, dz, W, dX, dt), wgrad(V, H, N, dz, X, dW, c->dw_dtype)};
-    KL_TRY(run_gemms(dt, g, 2, st));
+    g[0].acc_ws = dx_acc;   // K = V is long: split it, accumulate in fp32
+    KL_TRY(run_gemms(dt, g, 2, st, "gemm.lm_bwd"));
   }
   return KL_OK;
 }
@@ -458,7 +459,7 @@ kl_status kl_gemm(int32_t M, int32_t N, int32_t K, int32_t dtype, const void* A,
   s.a_mn = a_mn_major ? 1 : 0; s.b_mn = b_mn_major ? 1 : 0;
   s.C = C; s.ldc = ldc; s.c_dtype = c_dtype;
   s.R = R; s.ldr = ldr; s.r_dtype = r_dtype;
-  return run_gemms(dtype, &s, 1, static_cast<cudaStream_t>(stream));
+  return run_gemms(dtype, &s, 1, static_cast<cudaStream_t>(stream), "gemm");
 }
 
 kl_status kl_rmsnorm_fwd(int32_t rows, int32_t width, int32_t dtype, const void* x,

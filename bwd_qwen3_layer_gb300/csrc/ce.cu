@@ -28,6 +28,16 @@ constexpr int CLUSTER = 8;
 constexpr int THREADS = 512;
 constexpr int NWARP = THREADS / 32;
 
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// global memory into this CTA's shared memory, completing on mbarrier `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 struct Part {
   float m;
   float s;
@@ -54,6 +64,7 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS)
   __shared__ int red_i[NWARP];
   __shared__ Part part;
   __shared__ int is_last;
+  __shared__ __align__(8) uint64_t load_bar;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
   const int n = blockIdx.y;
@@ -66,9 +77,26 @@ __global__ void __cluster_dims__(CLUSTER, 1, 1) __launch_bounds__(THREADS)
   float m = -INFINITY;
   int mi = INT_MAX;
   if (VEC) {
+    // One bulk asynchronous copy of the whole tile (16-byte aligned, length a
+    // multiple of 16 bytes), completed on an mbarrier: the row is in flight at
+    // once instead of one vector per thread.
+    const uint32_t bar = smem_u32(&load_bar);
+    if (threadIdx.x == 0) {
+      mbar_init(bar, 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      if (len > 0) {
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(len) * 4u);
+        bulk_copy_g2s(smem_u32(sz), zr, static_cast<uint32_t>(len) * 4u, bar);
+      } else {
+        mbar_arrive(bar);
+      }
+    }
+    mbar_wait(bar, 0, err);
     for (int i = threadIdx.x * 4; i < len; i += THREADS * 4) {
-      const float4 a = __ldcs(reinterpret_cast<const float4*>(zr + i));
-      *reinterpret_cast<float4*>(sz + i) = a;
+      const float4 a = *reinterpret_cast<const float4*>(sz + i);
       better(m, mi, a.x, c0 + i);
       better(m, mi, a.y, c0 + i + 1);
       better(m, mi, a.z, c0 + i + 2);

@@ -139,13 +139,108 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(
     partial[static_cast<int64_t>(blockIdx.x) * width + j] = sacc[j];
 }
 
-__global__ void column_sum_kernel(int nrows, int width, const float* __restrict__ partial,
-                                  float* __restrict__ out) {
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= width) return;
+// RMSNorm backward, row-parallel form: one CTA covers a whole row (256
+// threads x 4-element chunks, up to 8 chunks each, so width <= 8192), keeps
+// its columns' gains and gain-gradient partial sums in registers across all
+// rows it visits, and reduces the row dot product with one barrier.
+constexpr int RB_MAXC = 8;
+
+__device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
+  const uint2 a = *reinterpret_cast<const uint2*>(p);
+  const float2 x0 = unpack_bf16x2(a.x), x1 = unpack_bf16x2(a.y);
+  v[0] = x0.x; v[1] = x0.y; v[2] = x1.x; v[3] = x1.y;
+}
+__device__ __forceinline__ void store4(float* p, const float (&v)[4]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* p, const float (&v)[4]) {
+  uint2 o;
+  o.x = pack_bf16x2(v[0], v[1]);
+  o.y = pack_bf16x2(v[2], v[3]);
+  *reinterpret_cast<uint2*>(p) = o;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) rmsnorm_bwd_rows_kernel(
+    int rows, int width, const float* __restrict__ dh, const T* __restrict__ x,
+    const T* __restrict__ gamma, const float* __restrict__ rstd, const T* __restrict__ resid,
+    T* __restrict__ dx, float* __restrict__ partial) {
+  __shared__ float red[2][8];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nchunk = width >> 2;
+  float g[RB_MAXC][4], acc[RB_MAXC][4];
+#pragma unroll
+  for (int k = 0; k < RB_MAXC; ++k) {
+    const int c = tid + 256 * k;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) g[k][e] = acc[k][e] = 0.f;
+    if (c < nchunk) load4(gamma + 4 * c, g[k]);
+  }
+  const float inv_w = 1.0f / static_cast<float>(width);
+  int buf = 0;
+  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+    const int64_t off = static_cast<int64_t>(row) * width;
+    const float r = rstd[row];
+    float dv[RB_MAXC][4], xv[RB_MAXC][4];
+    float dot = 0.f;
+#pragma unroll
+    for (int k = 0; k < RB_MAXC; ++k) {
+      const int c = tid + 256 * k;
+      if (c < nchunk) {
+        load4(dh + off + 4 * c, dv[k]);
+        load4(x + off + 4 * c, xv[k]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dot = fmaf(dv[k][e] * g[k][e], xv[k][e], dot);
+      }
+    }
+    dot = warp_sum(dot);
+    if (lane == 0) red[buf][warp] = dot;
+    __syncthreads();
+    dot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) dot += red[buf][w];
+    dot *= r * inv_w;
+    buf ^= 1;
+#pragma unroll
+    for (int k = 0; k < RB_MAXC; ++k) {
+      const int c = tid + 256 * k;
+      if (c < nchunk) {
+        float o[4], rv[4] = {0.f, 0.f, 0.f, 0.f};
+        if (resid) load4(resid + off + 4 * c, rv);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float n = xv[k][e] * r;
+          o[e] = r * (dv[k][e] * g[k][e] - n * dot) + rv[e];
+          acc[k][e] = fmaf(dv[k][e], n, acc[k][e]);
+        }
+        store4(dx + off + 4 * c, o);
+      }
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < RB_MAXC; ++k) {
+    const int c = tid + 256 * k;
+    if (c < nchunk) store4(partial + static_cast<int64_t>(blockIdx.x) * width + 4 * c, acc[k]);
+  }
+}
+
+// out[c] = sum over the partial rows (fixed order: deterministic).
+__global__ void __launch_bounds__(256) column_sum_kernel(int nrows, int width,
+                                                         const float* __restrict__ partial,
+                                                         float* __restrict__ out) {
+  __shared__ float red[4][64];
+  const int c = blockIdx.x * 64 + (threadIdx.x & 63);
+  const int grp = threadIdx.x >> 6;
   float s = 0.f;
-  for (int r = 0; r < nrows; ++r) s += partial[static_cast<int64_t>(r) * width + j];
-  out[j] = s;
+  if (c < width)
+    for (int r = grp; r < nrows; r += 4) s += partial[static_cast<int64_t>(r) * width + c];
+  red[grp][threadIdx.x & 63] = s;
+  __syncthreads();
+  if (grp == 0 && c < width) out[c] = (red[0][threadIdx.x] + red[1][threadIdx.x]) + (red[2][threadIdx.x] + red[3][threadIdx.x]);
 }
 
 int rmsnorm_bwd_grid(int rows) {
@@ -189,20 +284,78 @@ __global__ void rope_kernel(int S, int heads, int d, float base, T* __restrict__
   }
 }
 
+// Forward (dir = +1) or backward (dir = -1) rotation of q [T, hq, d] and k
+// [T, hk, d] in place, one CTA per token, VEC-wide vector accesses.
 template <typename T>
-__global__ void rope_bwd_f32_kernel(int S, int heads, int d, float base,
-                                    const float* __restrict__ src, T* __restrict__ dst) {
+__global__ void __launch_bounds__(128) rope_qk_kernel(int S, int hq, int hk, int d, float base,
+                                                      T* __restrict__ q, T* __restrict__ k,
+                                                      float dir) {
+  extern __shared__ float cs[];
+  const int t = blockIdx.x;
+  rope_table(t % S, d, base, dir, cs);
+  const int half = d / 2;
+  constexpr int V = Vec<T>::N;
+  const int groups = half / V;
+  const int items = (hq + hk) * groups;
+  for (int idx = threadIdx.x; idx < items; idx += blockDim.x) {
+    const int h = idx / groups, i0 = (idx - h * groups) * V;
+    T* p = h < hq ? q + (static_cast<int64_t>(t) * hq + h) * d
+                  : k + (static_cast<int64_t>(t) * hk + (h - hq)) * d;
+    float a[8], b[8];
+    Vec<T>::load(p + i0, a);
+    Vec<T>::load(p + half + i0, b);
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+      const float c = cs[i0 + e], sn = cs[half + i0 + e];
+      const float x = a[e], y = b[e];
+      a[e] = x * c - y * sn;
+      b[e] = x * sn + y * c;
+    }
+    Vec<T>::store(p + i0, a);
+    Vec<T>::store(p + half + i0, b);
+  }
+}
+
+// Attention-backward epilogue: fp32 accumulators -> dq, dk rotated back by
+// -angle, dv converted; one CTA per token, 4-wide vectors.
+template <typename T>
+__global__ void __launch_bounds__(128) rope_bwd_convert_kernel(
+    int S, int hq, int hk, int d, float base, const float* __restrict__ dq_acc,
+    const float* __restrict__ dk_acc, const float* __restrict__ dv_acc, T* __restrict__ dq,
+    T* __restrict__ dk, T* __restrict__ dv) {
   extern __shared__ float cs[];
   const int t = blockIdx.x;
   rope_table(t % S, d, base, -1.0f, cs);
   const int half = d / 2;
-  const int64_t off = static_cast<int64_t>(t) * heads * d;
-  for (int idx = threadIdx.x; idx < heads * half; idx += blockDim.x) {
-    const int hh = idx / half, i = idx - hh * half;
-    const float a = src[off + hh * d + i], b = src[off + hh * d + half + i];
-    const float c = cs[i], sn = cs[half + i];
-    st_f(dst + off + hh * d + i, a * c - b * sn);
-    st_f(dst + off + hh * d + half + i, a * sn + b * c);
+  const int groups = half / 4;
+  const int rot_items = (hq + hk) * groups;
+  const int items = rot_items + hk * (d / 4);
+  for (int idx = threadIdx.x; idx < items; idx += blockDim.x) {
+    if (idx < rot_items) {
+      const int h = idx / groups, i0 = (idx - h * groups) * 4;
+      const int64_t o = h < hq ? (static_cast<int64_t>(t) * hq + h) * d
+                               : (static_cast<int64_t>(t) * hk + (h - hq)) * d;
+      const float* src = h < hq ? dq_acc : dk_acc;
+      T* dst = h < hq ? dq : dk;
+      float a[4], b[4];
+      load4(src + o + i0, a);
+      load4(src + o + half + i0, b);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float c = cs[i0 + e], sn = cs[half + i0 + e];
+        const float x = a[e], y = b[e];
+        a[e] = x * c - y * sn;
+        b[e] = x * sn + y * c;
+      }
+      store4(dst + o + i0, a);
+      store4(dst + o + half + i0, b);
+    } else {
+      const int j = idx - rot_items;
+      const int64_t o = static_cast<int64_t>(t) * hk * d + static_cast<int64_t>(j) * 4;
+      float a[4];
+      load4(dv_acc + o, a);
+      store4(dv + o, a);
+    }
   }
 }
 
@@ -320,55 +473,91 @@ kl_status rmsnorm_bwd(int rows, int width, int dtype, const void* dh, int dh_dty
     return set_error(KL_ERR_UNSUPPORTED, "rmsnorm_bwd: width %d above 12288", width);
   if (!ws || ws_bytes < rmsnorm_bwd_ws(rows, width))
     return set_error(KL_ERR_NO_MEMORY, "rmsnorm_bwd: workspace too small");
+  if (dtype != KL_BF16 && dtype != KL_F32) return set_error(KL_ERR_INVALID_ARG, "rmsnorm_bwd: bad dtype %d", dtype);
+  if (dtype == KL_F32 && dh_dtype != KL_F32)
+    return set_error(KL_ERR_INVALID_ARG, "rmsnorm_bwd: fp32 mode needs fp32 dh");
   const int grid = rmsnorm_bwd_grid(rows);
   float* partial = static_cast<float*>(ws);
-  const size_t sm = width * sizeof(float);
+  const size_t es = dtype_size(dtype);
+  // row-parallel kernel: fp32 dh, width a multiple of 4 up to 8192, 16-byte aligned rows
+  const bool rows_form = dh_dtype == KL_F32 && width % 4 == 0 && width <= 256 * 4 * RB_MAXC &&
+                         al16(dh) && al16(x) && al16(dx) && al16(gamma) && (!resid || al16(resid)) &&
+                         (width * es) % 16 == 0;
   {
-  ProfScope ps("rmsnorm_bwd", st, 0.0,
-               1.0 * rows * width * (dtype_size(dh_dtype) + (resid ? 3.0 : 2.0) * dtype_size(dtype)) +
-                   4.0 * rows + 4.0 * grid * width);
-  if (dtype == KL_BF16) {
-    using T = __nv_bfloat16;
-    if (dh_dtype == KL_F32)
-      rmsnorm_bwd_kernel<T, float><<<grid, 256, sm, st>>>(rows, width, (const float*)dh, (const T*)x, (const T*)gamma, rstd, (const T*)resid, (T*)dx, partial);
-    else
-      rmsnorm_bwd_kernel<T, T><<<grid, 256, sm, st>>>(rows, width, (const T*)dh, (const T*)x, (const T*)gamma, rstd, (const T*)resid, (T*)dx, partial);
-  } else if (dtype == KL_F32) {
-    if (dh_dtype != KL_F32) return set_error(KL_ERR_INVALID_ARG, "rmsnorm_bwd: fp32 mode needs fp32 dh");
-    rmsnorm_bwd_kernel<float, float><<<grid, 256, sm, st>>>(rows, width, (const float*)dh, (const float*)x, (const float*)gamma, rstd, (const float*)resid, (float*)dx, partial);
-  } else {
-    return set_error(KL_ERR_INVALID_ARG, "rmsnorm_bwd: bad dtype %d", dtype);
-  }
+    ProfScope ps("rmsnorm_bwd", st, 0.0,
+                 1.0 * rows * width * (dtype_size(dh_dtype) + (resid ? 3.0 : 2.0) * es) + 4.0 * rows +
+                     4.0 * grid * width);
+    const size_t sm = width * sizeof(float);
+    if (dtype == KL_BF16) {
+      using T = __nv_bfloat16;
+      if (rows_form)
+        rmsnorm_bwd_rows_kernel<T><<<grid, 256, 0, st>>>(rows, width, (const float*)dh, (const T*)x, (const T*)gamma, rstd, (const T*)resid, (T*)dx, partial);
+      else if (dh_dtype == KL_F32)
+        rmsnorm_bwd_kernel<T, float><<<grid, 256, sm, st>>>(rows, width, (const float*)dh, (const T*)x, (const T*)gamma, rstd, (const T*)resid, (T*)dx, partial);
+      else
+        rmsnorm_bwd_kernel<T, T><<<grid, 256, sm, st>>>(rows, width, (const T*)dh, (const T*)x, (const T*)gamma, rstd, (const T*)resid, (T*)dx, partial);
+    } else {
+      if (rows_form)
+        rmsnorm_bwd_rows_kernel<float><<<grid, 256, 0, st>>>(rows, width, (const float*)dh, (const float*)x, (const float*)gamma, rstd, (const float*)resid, (float*)dx, partial);
+      else
+        rmsnorm_bwd_kernel<float, float><<<grid, 256, sm, st>>>(rows, width, (const float*)dh, (const float*)x, (const float*)gamma, rstd, (const float*)resid, (float*)dx, partial);
+    }
   }
   KL_CUDA(cudaGetLastError());
   ProfScope ps2("rmsnorm_bwd_colsum", st, 0.0, 4.0 * grid * width + 4.0 * width);
-  column_sum_kernel<<<(width + 255) / 256, 256, 0, st>>>(grid, width, partial, dgamma);
+  column_sum_kernel<<<(width + 63) / 64, 256, 0, st>>>(grid, width, partial, dgamma);
+  KL_CUDA(cudaGetLastError());
+  return KL_OK;
+}
+
+kl_status rope_qk(int B, int S, int hq, int hk, int d, float base, int dtype, void* q, void* k,
+                  int direction, cudaStream_t st) {
+  if (B < 1 || S < 1 || hq < 0 || hk < 0 || hq + hk < 1 || d < 2 || (d & 1) || !q ||
+      (hk > 0 && !k) || (direction != 1 && direction != -1))
+    return set_error(KL_ERR_INVALID_ARG, "rope: bad arguments");
+  if (dtype != KL_BF16 && dtype != KL_F32) return set_error(KL_ERR_INVALID_ARG, "rope: bad dtype");
+  const int T = B * S;
+  const size_t sm = d * sizeof(float);
+  const float dir = static_cast<float>(direction);
+  const int V = dtype == KL_BF16 ? 8 : 4;
+  const bool vec = (d / 2) % V == 0 && al16(q) && (hk == 0 || al16(k));
+  ProfScope ps("rope", st, 0.0, 2.0 * T * (hq + hk) * d * dtype_size(dtype));
+  if (vec) {
+    if (dtype == KL_BF16)
+      rope_qk_kernel<__nv_bfloat16><<<T, 128, sm, st>>>(S, hq, hk, d, base, (__nv_bfloat16*)q, (__nv_bfloat16*)k, dir);
+    else
+      rope_qk_kernel<float><<<T, 128, sm, st>>>(S, hq, hk, d, base, (float*)q, (float*)k, dir);
+  } else {
+    for (int w = 0; w < 2; ++w) {
+      void* x = w == 0 ? q : k;
+      const int heads = w == 0 ? hq : hk;
+      if (heads == 0) continue;
+      if (dtype == KL_BF16) rope_kernel<__nv_bfloat16><<<T, 128, sm, st>>>(S, heads, d, base, (__nv_bfloat16*)x, dir);
+      else rope_kernel<float><<<T, 128, sm, st>>>(S, heads, d, base, (float*)x, dir);
+    }
+  }
   KL_CUDA(cudaGetLastError());
   return KL_OK;
 }
 
 kl_status rope(int B, int S, int heads, int d, float base, int dtype, void* x, int direction,
                cudaStream_t st) {
-  if (B < 1 || S < 1 || heads < 1 || d < 2 || (d & 1) || !x || (direction != 1 && direction != -1))
-    return set_error(KL_ERR_INVALID_ARG, "rope: bad arguments");
-  const int T = B * S;
-  const size_t sm = d * sizeof(float);
-  const float dir = static_cast<float>(direction);
-  ProfScope ps("rope", st, 0.0, 2.0 * T * heads * d * dtype_size(dtype));
-  if (dtype == KL_BF16) rope_kernel<__nv_bfloat16><<<T, 128, sm, st>>>(S, heads, d, base, (__nv_bfloat16*)x, dir);
-  else if (dtype == KL_F32) rope_kernel<float><<<T, 128, sm, st>>>(S, heads, d, base, (float*)x, dir);
-  else return set_error(KL_ERR_INVALID_ARG, "rope: bad dtype");
-  KL_CUDA(cudaGetLastError());
-  return KL_OK;
+  return rope_qk(B, S, heads, 0, d, base, dtype, x, nullptr, direction, st);
 }
 
-kl_status rope_bwd_from_f32(int B, int S, int heads, int d, float base, int dtype,
-                            const float* src, void* dst, cudaStream_t st) {
+kl_status rope_bwd_convert(int B, int S, int hq, int hk, int d, float base, int dtype,
+                           const float* dq_acc, const float* dk_acc, const float* dv_acc, void* dq,
+                           void* dk, void* dv, cudaStream_t st) {
+  if (d % 8) return set_error(KL_ERR_UNSUPPORTED, "rope backward: head dim %d not a multiple of 8", d);
   const int T = B * S;
   const size_t sm = d * sizeof(float);
-  ProfScope ps("rope_bwd_f32", st, 0.0, 1.0 * T * heads * d * (4 + dtype_size(dtype)));
-  if (dtype == KL_BF16) rope_bwd_f32_kernel<__nv_bfloat16><<<T, 128, sm, st>>>(S, heads, d, base, src, (__nv_bfloat16*)dst);
-  else rope_bwd_f32_kernel<float><<<T, 128, sm, st>>>(S, heads, d, base, src, (float*)dst);
+  ProfScope ps("rope_bwd_convert", st, 0.0, 1.0 * T * (hq + 2 * hk) * d * (4 + dtype_size(dtype)));
+  if (dtype == KL_BF16)
+    rope_bwd_convert_kernel<__nv_bfloat16><<<T, 128, sm, st>>>(S, hq, hk, d, base, dq_acc, dk_acc, dv_acc,
+                                                               (__nv_bfloat16*)dq, (__nv_bfloat16*)dk, (__nv_bfloat16*)dv);
+  else
+    rope_bwd_convert_kernel<float><<<T, 128, sm, st>>>(S, hq, hk, d, base, dq_acc, dk_acc, dv_acc, (float*)dq,
+                                                       (float*)dk, (float*)dv);
   KL_CUDA(cudaGetLastError());
   return KL_OK;
 }

@@ -21,6 +21,7 @@
 #include <cudaTypedefs.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -38,19 +39,24 @@ constexpr uint32_t B_BYTES = BN * BK * 2;
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 2 * BN;
 constexpr int NUM_THREADS = 192;
-constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 256;
+constexpr int SCHED_Q = 8;                 // depth of the unit-id ring
+constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 512;
 
 struct GemmProb {
   int M, N;
   int nseg;
-  int kb[GEMM_MAX_SEG];
+  int kb[GEMM_MAX_SEG];   // k-blocks of each (A, B) segment
+  int kb_total;
+  int splits;             // work units per output tile (K split)
   int a_mn, b_mn;
   int m_tiles, n_tiles;
-  int tile_begin;
+  int n_fast;             // tile order: n fastest (1) or m fastest (0)
+  int unit_begin;         // first global work-unit index of this problem
   int tmap_base;
   void* C;
   int64_t ldc;
   int c_f32;
+  int atomic;             // fp32 output accumulated with red.add (split problems)
   int vec_ok;
   const void* R;
   int64_t ldr;
@@ -62,14 +68,42 @@ struct GemmParams {
   CUtensorMap tmB[GEMM_MAX_PROB * GEMM_MAX_SEG];
   GemmProb prob[GEMM_MAX_PROB];
   int nprob;
-  int total_tiles;
+  int total_units;
+  unsigned int* sched;    // [0] next unit to hand out, [1] CTAs finished
   uint32_t* err;
 };
 
-__device__ __forceinline__ int find_prob(const GemmParams& p, int tile) {
-  int pi = 0;
-  while (pi + 1 < p.nprob && tile >= p.prob[pi + 1].tile_begin) ++pi;
-  return pi;
+// A work unit: one K-range of one output tile of one problem.
+struct Unit {
+  int p;
+  int m0, n0;
+  int kb_lo, kb_hi;
+};
+
+__device__ __forceinline__ Unit decode_unit(const GemmParams& P, int u) {
+  int p = 0;
+  while (p + 1 < P.nprob && u >= P.prob[p + 1].unit_begin) ++p;
+  const GemmProb& pr = P.prob[p];
+  const int local = u - pr.unit_begin;
+  const int si = local % pr.splits;
+  const int tile = local / pr.splits;
+  Unit r;
+  r.p = p;
+  if (pr.n_fast) {
+    r.n0 = (tile % pr.n_tiles) * BN;
+    r.m0 = (tile / pr.n_tiles) * BM;
+  } else {
+    r.m0 = (tile % pr.m_tiles) * BM;
+    r.n0 = (tile / pr.m_tiles) * BN;
+  }
+  r.kb_lo = static_cast<int>(static_cast<int64_t>(si) * pr.kb_total / pr.splits);
+  r.kb_hi = static_cast<int>(static_cast<int64_t>(si + 1) * pr.kb_total / pr.splits);
+  return r;
+}
+
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
 }
 
 __device__ __forceinline__ void store_chunk(const GemmProb& pr, int row, int col0,
@@ -79,6 +113,16 @@ __device__ __forceinline__ void store_chunk(const GemmProb& pr, int row, int col
   for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
   const int ncols = min(32, pr.N - col0);
   const bool vec = pr.vec_ok && ncols == 32;
+  if (pr.atomic) {
+    float* c = static_cast<float*>(pr.C) + row * pr.ldc + col0;
+    if (vec) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) red_add_v4(c + j, f[j], f[j + 1], f[j + 2], f[j + 3]);
+    } else {
+      for (int j = 0; j < ncols; ++j) atomicAdd(c + j, f[j]);
+    }
+    return;
+  }
   if (pr.R) {
     if (pr.r_f32) {
       const float* r = static_cast<const float*>(pr.R) + row * pr.ldr + col0;
@@ -147,8 +191,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  auto qfull_bar = [&](int q) { return bar0 + 8u * (2 * STAGES + 5 + q); };
+  auto qempty_bar = [&](int q) { return bar0 + 8u * (2 * STAGES + 5 + SCHED_Q + q); };
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5 + 2 * SCHED_Q);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* qids = reinterpret_cast<volatile int*>(tmem_holder + 2);   // [SCHED_Q] unit ids
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -163,6 +210,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(tempty_bar(a), 4);
     }
     mbar_init(drain_bar, 1);
+    for (int q = 0; q < SCHED_Q; ++q) {
+      mbar_init(qfull_bar(q), 1);
+      mbar_init(qempty_bar(q), 5);   // the MMA thread and the 4 epilogue warps
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -176,7 +227,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t tmem_base = *tmem_holder;
 
   if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- scheduler + TMA producer ----------------
+    // Takes the next unit from the launch-wide counter, publishes its id to the
+    // MMA thread and the epilogue warps through a small shared ring, then loads
+    // every k-block of the unit. Id -1 ends the stream.
     for (int i = 0; i < p.nprob; ++i)
       for (int s = 0; s < p.prob[i].nseg; ++s) {
         tma_prefetch_desc(&p.tmA[p.prob[i].tmap_base + s]);
@@ -184,45 +238,62 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     int stage = 0;
     uint32_t phase = 0;
+    int q = 0;
+    uint32_t qphase = 0;
     long issued = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x) {
-      const int pi = find_prob(p, tile);
-      const GemmProb& pr = p.prob[pi];
-      const int local = tile - pr.tile_begin;
-      const int m0 = (local % pr.m_tiles) * BM;
-      const int n0 = (local / pr.m_tiles) * BN;
-      for (int s = 0; ok && s < pr.nseg; ++s) {
+    while (ok) {
+      int u = static_cast<int>(atomicAdd(&p.sched[0], 1u));
+      if (u >= p.total_units) u = -1;
+      if (*abort_flag || !mbar_wait(qempty_bar(q), qphase ^ 1u, p.err)) {
+        *abort_flag = 1;
+        break;
+      }
+      qids[q] = u;
+      mbar_arrive(qfull_bar(q));
+      if (++q == SCHED_Q) {
+        q = 0;
+        qphase ^= 1u;
+      }
+      if (u < 0) break;
+      const Unit un = decode_unit(p, u);
+      const GemmProb& pr = p.prob[un.p];
+      int s = 0, off = 0;
+      while (un.kb_lo >= off + pr.kb[s]) off += pr.kb[s++];
+      int kl = un.kb_lo - off;
+      for (int kbg = un.kb_lo; kbg < un.kb_hi; ++kbg, ++kl) {
+        if (kl == pr.kb[s]) {
+          ++s;
+          kl = 0;
+        }
         const CUtensorMap* ta = &p.tmA[pr.tmap_base + s];
         const CUtensorMap* tb = &p.tmB[pr.tmap_base + s];
-        for (int kb = 0; kb < pr.kb[s]; ++kb) {
-          if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u, p.err)) {
-            ok = false;
-            *abort_flag = 1;
-            break;
-          }
-          const uint32_t fb = full_bar(stage);
-          mbar_arrive_expect_tx(fb, STAGE_BYTES);
-          const uint32_t sa = sbase + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
-          const int k0 = kb * BK;
-          if (!pr.a_mn) {
-            tma_load_2d(sa, ta, k0, m0, fb);
-          } else {
-            tma_load_2d(sa, ta, m0, k0, fb);
-            tma_load_2d(sa + 8192, ta, m0 + 64, k0, fb);
-          }
-          if (!pr.b_mn) {
-            tma_load_2d(sb, tb, k0, n0, fb);
-          } else {
+        if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u, p.err)) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+        const uint32_t fb = full_bar(stage);
+        mbar_arrive_expect_tx(fb, STAGE_BYTES);
+        const uint32_t sa = sbase + stage * STAGE_BYTES;
+        const uint32_t sb = sa + A_BYTES;
+        const int k0 = kl * BK;
+        if (!pr.a_mn) {
+          tma_load_2d(sa, ta, k0, un.m0, fb);
+        } else {
+          tma_load_2d(sa, ta, un.m0, k0, fb);
+          tma_load_2d(sa + 8192, ta, un.m0 + 64, k0, fb);
+        }
+        if (!pr.b_mn) {
+          tma_load_2d(sb, tb, k0, un.n0, fb);
+        } else {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + 8192 * j, tb, n0 + 64 * j, k0, fb);
-          }
-          ++issued;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + 8192 * j, tb, un.n0 + 64 * j, k0, fb);
+        }
+        ++issued;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
     }
@@ -238,13 +309,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_wait(full_bar(stage), phase, p.err);
     }
   } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer ----------------
+    // ---------------- MMA issuer: one accumulation per unit ----------------
     int stage = 0;
     uint32_t phase = 0;
+    int q = 0;
+    uint32_t qphase = 0;
     int it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += gridDim.x, ++it) {
-      const GemmProb& pr = p.prob[find_prob(p, tile)];
+    while (ok) {
+      if (*abort_flag || !mbar_wait(qfull_bar(q), qphase, p.err)) {
+        *abort_flag = 1;
+        break;
+      }
+      const int u = qids[q];
+      mbar_arrive(qempty_bar(q));
+      if (++q == SCHED_Q) {
+        q = 0;
+        qphase ^= 1u;
+      }
+      if (u < 0) break;
+      const Unit un = decode_unit(p, u);
+      const GemmProb& pr = p.prob[un.p];
       const int acc = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
       if (*abort_flag || !mbar_wait(tempty_bar(acc), (use & 1u) ^ 1u, p.err)) {
@@ -255,46 +340,57 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
       const uint32_t idesc = idesc_bf16_f32(BM, BN, pr.a_mn, pr.b_mn);
       uint32_t accumulate = 0;
-      for (int s = 0; ok && s < pr.nseg; ++s) {
-        for (int kb = 0; kb < pr.kb[s]; ++kb) {
-          if (*abort_flag || !mbar_wait(full_bar(stage), phase, p.err)) {
-            ok = false;
-            *abort_flag = 1;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sa = sbase + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
+      for (int kbg = un.kb_lo; kbg < un.kb_hi; ++kbg) {
+        if (*abort_flag || !mbar_wait(full_bar(stage), phase, p.err)) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = sbase + stage * STAGE_BYTES;
+        const uint32_t sb = sa + A_BYTES;
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t ad = pr.a_mn ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
-                                        : smem_desc_sw128(sa + k * 32, 16, 1024);
-            const uint64_t bd = pr.b_mn ? smem_desc_sw128(sb + k * 2048, 8192, 1024)
-                                        : smem_desc_sw128(sb + k * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, idesc, accumulate);
-            accumulate = 1;
-          }
-          umma_commit(empty_bar(stage));
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
+        for (int k = 0; k < BK / 16; ++k) {
+          const uint64_t ad = pr.a_mn ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
+                                      : smem_desc_sw128(sa + k * 32, 16, 1024);
+          const uint64_t bd = pr.b_mn ? smem_desc_sw128(sb + k * 2048, 8192, 1024)
+                                      : smem_desc_sw128(sb + k * 32, 16, 1024);
+          umma_bf16(d_tmem, ad, bd, idesc, accumulate);
+          accumulate = 1;
+        }
+        umma_commit(empty_bar(stage));
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
         }
       }
       if (ok) umma_commit(tfull_bar(acc));
+      ++it;
     }
     // Every MMA issued must finish before TMEM is released.
     umma_commit(drain_bar);
     mbar_wait(drain_bar, 0, p.err);
   } else if (warp >= 2) {
-    // ---------------- epilogue ----------------
+    // ---------------- epilogue: one per unit ----------------
     const int quarter = warp & 3;
+    int q = 0;
+    uint32_t qphase = 0;
     int it = 0;
-    for (int tile = blockIdx.x; tile < p.total_tiles; tile += gridDim.x, ++it) {
-      const GemmProb& pr = p.prob[find_prob(p, tile)];
-      const int local = tile - pr.tile_begin;
-      const int m0 = (local % pr.m_tiles) * BM;
-      const int n0 = (local / pr.m_tiles) * BN;
+    while (true) {
+      if (*abort_flag || !mbar_wait(qfull_bar(q), qphase, p.err)) {
+        *abort_flag = 1;
+        break;
+      }
+      const int u = qids[q];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qempty_bar(q));
+      if (++q == SCHED_Q) {
+        q = 0;
+        qphase ^= 1u;
+      }
+      if (u < 0) break;
+      const Unit un = decode_unit(p, u);
+      const GemmProb& pr = p.prob[un.p];
       const int acc = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
       if (*abort_flag || !mbar_wait(tfull_bar(acc), use & 1u, p.err)) {
@@ -302,9 +398,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const int row = m0 + quarter * 32 + lane;
+      const int row = un.m0 + quarter * 32 + lane;
       for (int c = 0; c < BN / 32; ++c) {
-        const int col0 = n0 + c * 32;
+        const int col0 = un.n0 + c * 32;
         if (col0 >= pr.N) break;
         uint32_t v[32];
         tmem_ld_32x32b_x32(
@@ -316,14 +412,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty_bar(acc));
+      ++it;
     }
   }
 
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+  if (threadIdx.x == 0) {
+    // The last CTA to finish re-arms the launch's scheduler counters.
+    __threadfence();
+    const unsigned prev = atomicAdd(&p.sched[1], 1u);
+    if (prev == gridDim.x - 1) {
+      atomicExch(&p.sched[0], 0u);
+      atomicExch(&p.sched[1], 0u);
+      __threadfence();
+    }
+  }
+}
+
+// C = bf16(acc + R): finishes a problem that was accumulated in fp32.
+__global__ void gemm_finalize_kernel(int M, int N, const float* __restrict__ acc,
+                                     void* __restrict__ C, int64_t ldc, int c_f32,
+                                     const void* __restrict__ R, int64_t ldr, int r_f32) {
+  const int64_t total = static_cast<int64_t>(M) * N;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / N, c = i - r * N;
+    float v = acc[i];
+    if (R) v += r_f32 ? static_cast<const float*>(R)[r * ldr + c]
+                      : __bfloat162float(static_cast<const __nv_bfloat16*>(R)[r * ldr + c]);
+    if (c_f32) static_cast<float*>(C)[r * ldc + c] = v;
+    else static_cast<__nv_bfloat16*>(C)[r * ldc + c] = __float2bfloat16_rn(v);
   }
 }
 
@@ -430,15 +554,62 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(int M, int N, int nseg, G
 
 }  // namespace
 
-kl_status gemm_bf16(const GemmSpec* specs, int nspec, cudaStream_t st) {
+// K-split policy: problems with at least SPLIT_MIN_KB k-blocks whose result can
+// be accumulated in fp32 (fp32 output without addend, or a caller-provided
+// fp32 accumulator) are cut along K into units of at most ~UNIT_KB k-blocks,
+// so that no unit is long against a CTA's share of the launch.
+constexpr int SPLIT_MIN_KB = 256;
+constexpr int UNIT_KB = 256;
+
+// Scheduler counters: one pair per launch slot, reused round-robin; each launch
+// re-arms its pair when its last CTA exits.
+constexpr int SCHED_SLOTS = 64;
+__device__ unsigned int g_gemm_sched[SCHED_SLOTS][2];
+
+unsigned int* sched_slot_ptr() {
+  static unsigned int* base[64] = {};
+  static std::atomic<unsigned> seq{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!base[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_gemm_sched) != cudaSuccess) return nullptr;
+    base[dev] = static_cast<unsigned int*>(ptr);
+  }
+  return base[dev] + 2 * (seq.fetch_add(1) % SCHED_SLOTS);
+}
+
+kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const char* label) {
   if (nspec < 1 || nspec > GEMM_MAX_PROB) return set_error(KL_ERR_INVALID_ARG, "gemm: %d problems", nspec);
+  // Heavy units first: order the problems by k-blocks per unit, descending.
+  int order[GEMM_MAX_PROB];
+  int splits[GEMM_MAX_PROB];
+  int kbt[GEMM_MAX_PROB];
+  for (int i = 0; i < nspec; ++i) {
+    const GemmSpec& s = specs_in[i];
+    int kb = 0;
+    for (int g = 0; g < s.nseg && g < GEMM_MAX_SEG; ++g) kb += (s.K[g] + BK - 1) / BK;
+    const bool can_split = (s.c_dtype == KL_F32 && !s.R) || s.acc_ws;
+    splits[i] = (can_split && kb >= SPLIT_MIN_KB) ? (kb + UNIT_KB - 1) / UNIT_KB : 1;
+    kbt[i] = kb;
+    order[i] = i;
+  }
+  for (int a = 1; a < nspec; ++a)
+    for (int b = a; b > 0 && kbt[order[b]] / splits[order[b]] > kbt[order[b - 1]] / splits[order[b - 1]]; --b) {
+      const int t = order[b];
+      order[b] = order[b - 1];
+      order[b - 1] = t;
+    }
   GemmParams p;  // built on the host, passed by value into the launch
   memset(&p, 0, sizeof(p));
-  int tiles = 0, tm = 0;
+  int units = 0, tm = 0;
+  bool finalize[GEMM_MAX_PROB] = {};
+  double flops = 0.0, bytes = 0.0;
   for (int i = 0; i < nspec; ++i) {
-    const GemmSpec& s = specs[i];
+    const int oi = order[i];
+    const GemmSpec& s = specs_in[oi];
     if (s.M < 1 || s.N < 1 || s.nseg < 1 || s.nseg > GEMM_MAX_SEG || !s.C)
-      return set_error(KL_ERR_INVALID_ARG, "gemm: bad problem %d (M %d N %d nseg %d)", i, s.M, s.N, s.nseg);
+      return set_error(KL_ERR_INVALID_ARG, "gemm: bad problem %d (M %d N %d nseg %d)", oi, s.M, s.N, s.nseg);
     if (s.c_dtype != KL_BF16 && s.c_dtype != KL_F32)
       return set_error(KL_ERR_INVALID_ARG, "gemm: bad output dtype");
     GemmProb& pr = p.prob[i];
@@ -448,9 +619,10 @@ kl_status gemm_bf16(const GemmSpec* specs, int nspec, cudaStream_t st) {
     pr.a_mn = s.a_mn;
     pr.b_mn = s.b_mn;
     pr.tmap_base = tm;
+    double ksum = 0.0;
     for (int g = 0; g < s.nseg; ++g) {
       if (!s.A[g] || !s.B[g] || s.K[g] < 1)
-        return set_error(KL_ERR_INVALID_ARG, "gemm: problem %d segment %d: null operand or K < 1", i, g);
+        return set_error(KL_ERR_INVALID_ARG, "gemm: problem %d segment %d: null operand or K < 1", oi, g);
       if (!aligned16(s.A[g]) || !aligned16(s.B[g]) || (s.lda[g] % 8) || (s.ldb[g] % 8))
         return set_error(KL_ERR_INVALID_ARG,
                          "gemm: bf16 operands need 16-byte aligned bases and row strides that are multiples of 8");
@@ -459,24 +631,50 @@ kl_status gemm_bf16(const GemmSpec* specs, int nspec, cudaStream_t st) {
       if (!s.b_mn) KL_TRY(make_map(&p.tmB[tm + g], s.B[g], s.K[g], s.N, s.ldb[g], BN));
       else KL_TRY(make_map(&p.tmB[tm + g], s.B[g], s.N, s.K[g], s.ldb[g], 64));
       pr.kb[g] = (s.K[g] + BK - 1) / BK;
+      pr.kb_total += pr.kb[g];
+      ksum += s.K[g];
     }
     tm += s.nseg;
     pr.m_tiles = (s.M + BM - 1) / BM;
     pr.n_tiles = (s.N + BN - 1) / BN;
-    pr.tile_begin = tiles;
-    tiles += pr.m_tiles * pr.n_tiles;
-    pr.C = s.C;
-    pr.ldc = s.ldc;
-    pr.c_f32 = s.c_dtype == KL_F32;
-    pr.R = s.R;
-    pr.ldr = s.ldr;
-    pr.r_f32 = s.r_dtype == KL_F32;
-    const size_t ce = dtype_size(s.c_dtype), re = dtype_size(s.r_dtype);
-    pr.vec_ok = aligned16(s.C) && (s.ldc * ce) % 16 == 0 &&
-                (!s.R || (aligned16(s.R) && (s.ldr * re) % 16 == 0));
+    // keep the smaller operand resident in L2: walk its dimension fastest
+    pr.n_fast = s.N < s.M ? 1 : 0;
+    pr.splits = splits[oi] < pr.kb_total ? splits[oi] : pr.kb_total;
+    pr.atomic = pr.splits > 1;
+    pr.unit_begin = units;
+    units += pr.m_tiles * pr.n_tiles * pr.splits;
+    const bool direct_f32 = s.c_dtype == KL_F32 && !s.R;
+    if (pr.atomic && !direct_f32) {
+      // accumulate in the caller's fp32 workspace, finish with gemm_finalize_kernel
+      finalize[oi] = true;
+      pr.C = s.acc_ws;
+      pr.ldc = s.N;
+      pr.c_f32 = 1;
+      pr.R = nullptr;
+      pr.vec_ok = aligned16(s.acc_ws) && (s.N * 4) % 16 == 0;
+    } else {
+      pr.C = s.C;
+      pr.ldc = s.ldc;
+      pr.c_f32 = s.c_dtype == KL_F32;
+      pr.R = s.R;
+      pr.ldr = s.ldr;
+      pr.r_f32 = s.r_dtype == KL_F32;
+      const size_t ce = dtype_size(s.c_dtype), re = dtype_size(s.r_dtype);
+      pr.vec_ok = aligned16(s.C) && (s.ldc * ce) % 16 == 0 &&
+                  (!s.R || (aligned16(s.R) && (s.ldr * re) % 16 == 0));
+    }
+    if (pr.atomic) {
+      if (finalize[oi]) KL_CUDA(cudaMemsetAsync(pr.C, 0, static_cast<size_t>(s.M) * s.N * 4, st));
+      else KL_CUDA(cudaMemset2DAsync(pr.C, static_cast<size_t>(pr.ldc) * 4, 0, static_cast<size_t>(s.N) * 4, s.M, st));
+    }
+    flops += 2.0 * s.M * s.N * ksum;
+    bytes += 2.0 * (s.M + s.N) * ksum + static_cast<double>(s.M) * s.N * dtype_size(s.c_dtype) +
+             (s.R ? static_cast<double>(s.M) * s.N * dtype_size(s.r_dtype) : 0.0);
   }
   p.nprob = nspec;
-  p.total_tiles = tiles;
+  p.total_units = units;
+  p.sched = sched_slot_ptr();
+  if (!p.sched) return set_error(KL_ERR_CUDA, "gemm: scheduler counters unavailable");
   p.err = device_error_word();
   static uint64_t attr_done = 0;  // one bit per device ordinal
   int dev = 0;
@@ -486,23 +684,25 @@ kl_status gemm_bf16(const GemmSpec* specs, int nspec, cudaStream_t st) {
                                  static_cast<int>(SMEM_BYTES)));
     attr_done |= uint64_t(1) << dev;
   }
-  double flops = 0.0, bytes = 0.0;
-  for (int i = 0; i < nspec; ++i) {
-    const GemmSpec& s = specs[i];
-    double ksum = 0.0;
-    for (int g = 0; g < s.nseg; ++g) ksum += s.K[g];
-    flops += 2.0 * s.M * s.N * ksum;
-    bytes += 2.0 * (s.M + s.N) * ksum + static_cast<double>(s.M) * s.N * dtype_size(s.c_dtype) +
-             (s.R ? static_cast<double>(s.M) * s.N * dtype_size(s.r_dtype) : 0.0);
+  const int grid = units < num_sms() ? units : num_sms();
+  {
+    ProfScope ps(label, st, flops, bytes);
+    gemm_bf16_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(p);
   }
-  const int grid = tiles < num_sms() ? tiles : num_sms();
-  ProfScope ps("gemm_bf16_tc", st, flops, bytes);
-  gemm_bf16_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(p);
   KL_CUDA(cudaGetLastError());
+  for (int i = 0; i < nspec; ++i) {
+    if (!finalize[i]) continue;
+    const GemmSpec& s = specs_in[i];
+    const double n = static_cast<double>(s.M) * s.N;
+    ProfScope ps("gemm_finalize", st, 0.0, n * (4 + dtype_size(s.c_dtype) + (s.R ? dtype_size(s.r_dtype) : 0)));
+    gemm_finalize_kernel<<<4 * num_sms(), 256, 0, st>>>(s.M, s.N, s.acc_ws, s.C, s.ldc, s.c_dtype == KL_F32,
+                                                       s.R, s.ldr, s.r_dtype == KL_F32);
+    KL_CUDA(cudaGetLastError());
+  }
   return KL_OK;
 }
 
-kl_status gemm_f32(const GemmSpec& s, cudaStream_t st) {
+kl_status gemm_f32(const GemmSpec& s, cudaStream_t st, const char* label) {
   if (s.M < 1 || s.N < 1 || s.nseg < 1 || s.nseg > GEMM_MAX_SEG || !s.C)
     return set_error(KL_ERR_INVALID_ARG, "gemm f32: bad problem");
   if (s.c_dtype != KL_F32 || (s.R && s.r_dtype != KL_F32))
@@ -512,7 +712,7 @@ kl_status gemm_f32(const GemmSpec& s, cudaStream_t st) {
   dim3 grid((s.N + FT - 1) / FT, (s.M + FT - 1) / FT);
   double ksum = 0.0;
   for (int g = 0; g < s.nseg; ++g) ksum += s.K[g];
-  ProfScope ps("gemm_f32", st, 2.0 * s.M * s.N * ksum, 4.0 * ((s.M + s.N) * ksum + 1.0 * s.M * s.N));
+  ProfScope ps(label, st, 2.0 * s.M * s.N * ksum, 4.0 * ((s.M + s.N) * ksum + 1.0 * s.M * s.N));
   gemm_f32_kernel<<<grid, 256, 0, st>>>(s.M, s.N, s.nseg, s);
   KL_CUDA(cudaGetLastError());
   return KL_OK;

@@ -31,13 +31,16 @@ struct GemmSpec {
   const void* R = nullptr;  // optional addend, [M,N] with row stride ldr
   int64_t ldr = 0;
   int r_dtype = KL_BF16;
+  // Optional fp32 [M,N] scratch: lets a long-K problem with a bf16 output or
+  // an addend be split along K (accumulated here, then finished into C).
+  float* acc_ws = nullptr;
 };
 
 // bf16 operands on the tcgen05 tensor cores; up to GEMM_MAX_PROB independent
 // problems share one persistent launch.
-kl_status gemm_bf16(const GemmSpec* specs, int nspec, cudaStream_t st);
+kl_status gemm_bf16(const GemmSpec* specs, int nspec, cudaStream_t st, const char* label = "gemm");
 // fp32 operands on CUDA cores (one problem).
-kl_status gemm_f32(const GemmSpec& spec, cudaStream_t st);
+kl_status gemm_f32(const GemmSpec& spec, cudaStream_t st, const char* label = "gemm_f32");
 
 // ---------------------------------------------------------------------------
 // elementwise / normalisation kernels (elementwise.cu)
@@ -50,9 +53,14 @@ kl_status rmsnorm_bwd(int rows, int width, int dtype, const void* dh, int dh_dty
                       float* dgamma, void* ws, size_t ws_bytes, cudaStream_t st);
 kl_status rope(int B, int S, int heads, int d, float base, int dtype, void* x, int direction,
                cudaStream_t st);
-// Rotary backward of an fp32 accumulator src [B*S, heads, d] into dst (dtype).
-kl_status rope_bwd_from_f32(int B, int S, int heads, int d, float base, int dtype,
-                            const float* src, void* dst, cudaStream_t st);
+// q [T, hq, d] and k [T, hk, d] rotated in place in one launch (hk may be 0).
+kl_status rope_qk(int B, int S, int hq, int hk, int d, float base, int dtype, void* q, void* k,
+                  int direction, cudaStream_t st);
+// Attention-backward epilogue: fp32 accumulators of dq and dk rotated back by
+// the negative angle, dv converted, into dtype outputs (d a multiple of 8).
+kl_status rope_bwd_convert(int B, int S, int hq, int hk, int d, float base, int dtype,
+                           const float* dq_acc, const float* dk_acc, const float* dv_acc, void* dq,
+                           void* dk, void* dv, cudaStream_t st);
 kl_status convert_f32(int64_t n, int dtype, const float* src, void* dst, cudaStream_t st);
 kl_status swiglu_fwd(int64_t n, int dtype, const void* g, const void* u, void* m, cudaStream_t st);
 kl_status swiglu_bwd(int64_t n, int dtype, const void* dm, const void* g, const void* u, void* dg,

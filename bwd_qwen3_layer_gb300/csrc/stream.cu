@@ -11,10 +11,11 @@
 // layers are still resident; earlier ones are uploaded again), then the global
 // L2 norm of every weight gradient (deterministic two-stage reduction in
 // fp64) and the clip coefficient min(1, max_norm / (norm + 1e-6)), applied to
-// every gradient where it was delivered (device memory, or pinned host memory
-// through its device-visible address). Gradients bound for host memory are
-// computed into one of two device staging slots and copied out on the copy
-// stream while the next layer's backward runs.
+// every gradient where it was delivered. Gradients bound for device memory are
+// computed in place and scaled in place; gradients bound for pinned host memory
+// are computed into device buffers kept for the whole step, then written out
+// already scaled by one kernel through the destination's device-visible
+// address (the clip needs every gradient before any can be final).
 //
 // If the caller's layer weights are already device memory the driver runs in
 // "bulk" mode: no slots, no uploads, the same kernels in the same order. Its
@@ -34,21 +35,35 @@ constexpr int SUMSQ_THREADS = 256;
 constexpr double CLIP_EPS = 1e-6;
 
 struct GradRef {
-  float* p;
+  const float* src;
+  float* dst;
   int64_t n;
 };
 
 // partial[b] = sum of squares of p over the elements block b owns (fixed
-// assignment, fixed reduction order: deterministic).
+// assignment, fp32 within a thread over four interleaved accumulators, fp64
+// across threads and blocks in a fixed order: deterministic).
 __global__ void __launch_bounds__(SUMSQ_THREADS) sumsq_kernel(const float* __restrict__ p, int64_t n,
                                                               double* __restrict__ partial) {
   __shared__ double red[SUMSQ_THREADS / 32];
-  double acc = 0.0;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(SUMSQ_THREADS) + threadIdx.x; i < n;
-       i += static_cast<int64_t>(SUMSQ_BLOCKS) * SUMSQ_THREADS) {
-    const double v = p[i];
-    acc += v * v;
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  const int64_t stride = static_cast<int64_t>(SUMSQ_BLOCKS) * SUMSQ_THREADS;
+  const int64_t start = blockIdx.x * static_cast<int64_t>(SUMSQ_THREADS) + threadIdx.x;
+  if ((reinterpret_cast<uintptr_t>(p) & 15u) == 0) {
+    const int64_t n4 = n >> 2;
+    const float4* p4 = reinterpret_cast<const float4*>(p);
+    for (int64_t i = start; i < n4; i += stride) {
+      const float4 v = p4[i];
+      a0 = fmaf(v.x, v.x, a0);
+      a1 = fmaf(v.y, v.y, a1);
+      a2 = fmaf(v.z, v.z, a2);
+      a3 = fmaf(v.w, v.w, a3);
+    }
+    for (int64_t i = (n4 << 2) + start; i < n; i += stride) a0 = fmaf(p[i], p[i], a0);
+  } else {
+    for (int64_t i = start; i < n; i += stride) a0 = fmaf(p[i], p[i], a0);
   }
+  double acc = (static_cast<double>(a0) + a1) + (static_cast<double>(a2) + a3);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
@@ -83,17 +98,29 @@ __global__ void clip_finalize_kernel(const double* __restrict__ partial, int cou
   }
 }
 
-// Every listed gradient *= coef (skipped entirely when coef == 1).
-__global__ void clip_scale_kernel(const GradRef* __restrict__ refs, int count,
-                                  const float* __restrict__ result) {
+// dst = src * coef for every listed gradient (in place when src == dst, where
+// coef == 1 leaves nothing to do).
+__global__ void __launch_bounds__(256) clip_scale_kernel(const GradRef* __restrict__ refs, int count,
+                                                         const float* __restrict__ result) {
   const float coef = result[2];
-  if (coef == 1.0f) return;
   for (int r = blockIdx.y; r < count; r += gridDim.y) {
-    float* p = refs[r].p;
+    const float* src = refs[r].src;
+    float* dst = refs[r].dst;
     const int64_t n = refs[r].n;
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-      p[i] *= coef;
+    if (src == dst && coef == 1.0f) continue;
+    const int64_t start = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    if (((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15u) == 0) {
+      const int64_t n4 = n >> 2;
+      for (int64_t i = start; i < n4; i += stride) {
+        float4 v = reinterpret_cast<const float4*>(src)[i];
+        v.x *= coef; v.y *= coef; v.z *= coef; v.w *= coef;
+        reinterpret_cast<float4*>(dst)[i] = v;
+      }
+      for (int64_t i = (n4 << 2) + start; i < n; i += stride) dst[i] = src[i] * coef;
+    } else {
+      for (int64_t i = start; i < n; i += stride) dst[i] = src[i] * coef;
+    }
   }
 }
 
@@ -162,7 +189,6 @@ struct kl_stream {
   int slot_layer[2] = {-1, -1};
   cudaStream_t copy = nullptr;
   cudaEvent_t ev_loaded[2] = {}, ev_used[2] = {}, ev_lm = nullptr;
-  cudaEvent_t ev_gdone[2] = {}, ev_gfree[2] = {};
   const void* lm_w = nullptr;
   // activations and workspace
   std::vector<kl_layer_saved> saved;
@@ -174,9 +200,9 @@ struct kl_stream {
   size_t lm_ws_bytes = 0;
   float* loss = nullptr;
   int32_t* argmax = nullptr;
-  // gradient staging (host destinations) and the clip
-  kl_layer_grads gstage[2] = {};
-  float* dwlm_stage = nullptr;
+  // gradients bound for host memory are kept here until the clip is known
+  std::vector<kl_layer_grads> retain;   // allocated on first use
+  float* dwlm_retain = nullptr;
   double* partials = nullptr;
   float* result = nullptr;
   GradRef* refs = nullptr;
@@ -200,8 +226,6 @@ struct kl_stream {
     for (int i = 0; i < 2; ++i) {
       if (ev_loaded[i]) cudaEventDestroy(ev_loaded[i]);
       if (ev_used[i]) cudaEventDestroy(ev_used[i]);
-      if (ev_gdone[i]) cudaEventDestroy(ev_gdone[i]);
-      if (ev_gfree[i]) cudaEventDestroy(ev_gfree[i]);
     }
     if (ev_lm) cudaEventDestroy(ev_lm);
     if (copy) cudaStreamDestroy(copy);
@@ -243,6 +267,17 @@ kl_status sumsq(kl_stream* s, const float* p, int64_t n, int index, cudaStream_t
   return KL_OK;
 }
 
+kl_status make_stream_events(kl_stream* s) {
+  cudaError_t e = cudaStreamCreateWithFlags(&s->copy, cudaStreamNonBlocking);
+  for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
+    e = cudaEventCreateWithFlags(&s->ev_loaded[k], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->ev_used[k], cudaEventDisableTiming);
+  }
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->ev_lm, cudaEventDisableTiming);
+  if (e != cudaSuccess) return cuda_check(e, "kl_stream_create: stream/event");
+  return KL_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -276,30 +311,12 @@ kl_status kl_stream_create(const kl_stream_cfg* cfg, const kl_layer_weights* hos
   if (!s->bulk) {
     for (int k = 0; k < 2; ++k)
       for (int i = 0; i < 9; ++i) *wfield(s->slot[k], i) = s->alloc(weight_elems(c, i) * es, &st);
-    void* lm = s->alloc(static_cast<size_t>(cfg->V) * c.H * es, &st);
-    s->lm_w = lm;
-    if (st == KL_OK) {
-      cudaError_t e = cudaStreamCreateWithFlags(&s->copy, cudaStreamNonBlocking);
-      for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
-        e = cudaEventCreateWithFlags(&s->ev_loaded[k], cudaEventDisableTiming);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->ev_used[k], cudaEventDisableTiming);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->ev_gdone[k], cudaEventDisableTiming);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->ev_gfree[k], cudaEventDisableTiming);
-      }
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->ev_lm, cudaEventDisableTiming);
-      if (e != cudaSuccess) st = cuda_check(e, "kl_stream_create: stream/event");
-    }
+    s->lm_w = s->alloc(static_cast<size_t>(cfg->V) * c.H * es, &st);
+    if (st == KL_OK) st = make_stream_events(s);
   } else {
-    if (!is_device_ptr(host_lm_head)) st = set_error(KL_ERR_INVALID_ARG, "kl_stream_create: device layers need a device lm-head weight");
+    if (!is_device_ptr(host_lm_head))
+      st = set_error(KL_ERR_INVALID_ARG, "kl_stream_create: device layers need a device lm-head weight");
     s->lm_w = host_lm_head;
-    if (st == KL_OK) {
-      cudaError_t e = cudaStreamCreateWithFlags(&s->copy, cudaStreamNonBlocking);
-      for (int k = 0; k < 2 && e == cudaSuccess; ++k) {
-        e = cudaEventCreateWithFlags(&s->ev_gdone[k], cudaEventDisableTiming);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->ev_gfree[k], cudaEventDisableTiming);
-      }
-      if (e != cudaSuccess) st = cuda_check(e, "kl_stream_create: stream/event");
-    }
   }
   s->saved.resize(L);
   s->hidden.resize(L);
@@ -316,11 +333,6 @@ kl_status kl_stream_create(const kl_stream_cfg* cfg, const kl_layer_weights* hos
   s->lm_ws = s->alloc(lm_ws, &st);
   s->loss = static_cast<float*>(s->alloc(sizeof(float), &st));
   s->argmax = static_cast<int32_t*>(s->alloc(T * sizeof(int32_t), &st));
-  for (int k = 0; k < 2; ++k) {
-    for (int i = 0; i < 9; ++i) *gfield(s->gstage[k], i) = s->alloc(weight_elems(c, i) * 4, &st);
-    s->gstage[k].dtype = KL_F32;
-  }
-  s->dwlm_stage = static_cast<float*>(s->alloc(static_cast<size_t>(cfg->V) * c.H * 4, &st));
   s->max_refs = 9 * L + 1;
   s->partials = static_cast<double*>(s->alloc(static_cast<size_t>(s->max_refs) * SUMSQ_BLOCKS * 8, &st));
   s->result = static_cast<float*>(s->alloc(4 * sizeof(float), &st));
@@ -348,27 +360,50 @@ kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets, flo
   const int T = c.B * c.S;
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
 
-  // where each gradient goes, and whether it needs staging
+  // Where each gradient is computed (src) and where it must end up (dst).
   std::vector<kl_layer_grads> dst(grads, grads + L);
-  std::vector<GradRef> refs;
   std::vector<bool> on_device(L);
+  bool any_host = false;
   for (int l = 0; l < L; ++l) {
     if (dst[l].dtype != KL_F32) return set_error(KL_ERR_INVALID_ARG, "kl_stream_run: gradients must be fp32");
     bool dev_all = true;
     for (int i = 0; i < 9; ++i) {
       void* p = *gfield(dst[l], i);
       if (!p) return set_error(KL_ERR_INVALID_ARG, "kl_stream_run: layer %d gradient %d is null", l, i);
-      void* dp = device_visible(p);
-      if (!dp) return set_error(KL_ERR_INVALID_ARG, "kl_stream_run: layer %d gradient %d is not device-visible (pin it)", l, i);
+      if (!device_visible(p))
+        return set_error(KL_ERR_INVALID_ARG, "kl_stream_run: layer %d gradient %d is not device-visible (pin it)", l, i);
       if (!is_device_ptr(p)) dev_all = false;
-      refs.push_back({static_cast<float*>(dp), static_cast<int64_t>(weight_elems(c, i))});
     }
     on_device[l] = dev_all;
+    any_host = any_host || !dev_all;
   }
   void* dwlm_dev = device_visible(dW_lm);
   if (!dwlm_dev) return set_error(KL_ERR_INVALID_ARG, "kl_stream_run: dW_lm is not device-visible (pin it)");
   const bool dwlm_on_device = is_device_ptr(dW_lm);
-  refs.push_back({static_cast<float*>(dwlm_dev), static_cast<int64_t>(s->cfg.V) * c.H});
+  if ((any_host && s->retain.empty()) || (!dwlm_on_device && !s->dwlm_retain)) {
+    kl_status st = KL_OK;
+    if (any_host && s->retain.empty()) {
+      s->retain.resize(L);
+      for (int l = 0; l < L; ++l) {
+        for (int i = 0; i < 9; ++i) *gfield(s->retain[l], i) = s->alloc(weight_elems(c, i) * 4, &st);
+        s->retain[l].dtype = KL_F32;
+      }
+    }
+    if (!dwlm_on_device && !s->dwlm_retain)
+      s->dwlm_retain = static_cast<float*>(s->alloc(static_cast<size_t>(s->cfg.V) * c.H * 4, &st));
+    if (st != KL_OK) return st;
+  }
+  std::vector<kl_layer_grads> src(L);
+  std::vector<GradRef> refs;
+  for (int l = 0; l < L; ++l) {
+    src[l] = on_device[l] ? dst[l] : s->retain[l];
+    for (int i = 0; i < 9; ++i)
+      refs.push_back({static_cast<const float*>(*gfield(src[l], i)),
+                      static_cast<float*>(device_visible(*gfield(dst[l], i))),
+                      static_cast<int64_t>(weight_elems(c, i))});
+  }
+  float* dwlm_src = dwlm_on_device ? static_cast<float*>(dW_lm) : s->dwlm_retain;
+  refs.push_back({dwlm_src, static_cast<float*>(dwlm_dev), static_cast<int64_t>(s->cfg.V) * c.H});
   KL_CUDA(cudaMemcpyAsync(s->refs, refs.data(), refs.size() * sizeof(GradRef), cudaMemcpyHostToDevice, cs));
 
   const size_t es = dtype_size(c.dtype);
@@ -410,20 +445,11 @@ kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets, flo
   // ---------------- lm-head ----------------
   if (!s->bulk) KL_CUDA(cudaStreamWaitEvent(cs, s->ev_lm, 0));
   kl_lmhead_cfg lc = {T, c.H, s->cfg.V, c.dtype, KL_F32};
-  float* dwlm_target = dwlm_on_device ? static_cast<float*>(dW_lm) : s->dwlm_stage;
   KL_TRY(kl_lmhead_ce_argmax(&lc, s->hidden[L - 1], s->lm_w, targets, s->loss, s->argmax, nullptr, s->dx[0],
-                             dwlm_target, s->lm_ws, s->lm_ws_bytes, cs));
-  KL_TRY(sumsq(s, dwlm_target, static_cast<int64_t>(s->cfg.V) * c.H, 9 * L, cs));
-  if (!dwlm_on_device) {
-    KL_CUDA(cudaEventRecord(s->ev_gdone[0], cs));
-    KL_CUDA(cudaStreamWaitEvent(s->copy, s->ev_gdone[0], 0));
-    KL_CUDA(cudaMemcpyAsync(dW_lm, s->dwlm_stage, static_cast<size_t>(s->cfg.V) * c.H * 4, cudaMemcpyDeviceToHost,
-                            s->copy));
-  }
+                             dwlm_src, s->lm_ws, s->lm_ws_bytes, cs));
+  KL_TRY(sumsq(s, dwlm_src, static_cast<int64_t>(s->cfg.V) * c.H, 9 * L, cs));
   // ---------------- backward ----------------
   int in = 0;
-  int stage_use = 0;
-  bool stage_busy[2] = {false, false};
   for (int l = L - 1; l >= 0; --l) {
     kl_layer_weights w;
     KL_TRY(weights_for(l, cur, &cur, &w));
@@ -431,44 +457,25 @@ kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets, flo
       int nxt;
       KL_TRY(acquire(s, l - 1, cur, &nxt));
     }
-    kl_layer_grads g;
-    int k = -1;
-    if (on_device[l]) {
-      g = dst[l];
-    } else {
-      k = stage_use++ & 1;
-      if (stage_busy[k]) KL_CUDA(cudaStreamWaitEvent(cs, s->ev_gfree[k], 0));
-      g = s->gstage[k];
-    }
-    KL_TRY(kl_layer_backward(&c, &w, &s->saved[l], s->dx[in], s->dx[in ^ 1], &g, s->bwd_ws, s->bwd_ws_bytes, cs));
+    KL_TRY(kl_layer_backward(&c, &w, &s->saved[l], s->dx[in], s->dx[in ^ 1], &src[l], s->bwd_ws, s->bwd_ws_bytes, cs));
     in ^= 1;
     for (int i = 0; i < 9; ++i)
-      KL_TRY(sumsq(s, static_cast<const float*>(*gfield(g, i)), static_cast<int64_t>(weight_elems(c, i)), 9 * l + i, cs));
+      KL_TRY(sumsq(s, static_cast<const float*>(*gfield(src[l], i)), static_cast<int64_t>(weight_elems(c, i)),
+                   9 * l + i, cs));
     if (!s->bulk) KL_CUDA(cudaEventRecord(s->ev_used[cur], cs));
-    if (k >= 0) {
-      KL_CUDA(cudaEventRecord(s->ev_gdone[k], cs));
-      KL_CUDA(cudaStreamWaitEvent(s->copy, s->ev_gdone[k], 0));
-      for (int i = 0; i < 9; ++i)
-        KL_CUDA(cudaMemcpyAsync(*gfield(dst[l], i), *gfield(g, i), weight_elems(c, i) * 4, cudaMemcpyDefault, s->copy));
-      KL_CUDA(cudaEventRecord(s->ev_gfree[k], s->copy));
-      stage_busy[k] = true;
-    }
   }
-  // every copy-out must land before the clip scales the destinations
-  KL_CUDA(cudaEventRecord(s->ev_gdone[0], s->copy));
-  KL_CUDA(cudaStreamWaitEvent(cs, s->ev_gdone[0], 0));
+  // ---------------- global norm, clip, delivery ----------------
   {
     ProfScope ps("clip_finalize", cs, 0.0, 8.0 * (9 * L + 1) * SUMSQ_BLOCKS);
     clip_finalize_kernel<<<1, SUMSQ_THREADS, 0, cs>>>(s->partials, 9 * L + 1, s->loss, clip_max_norm, s->result);
   }
   KL_CUDA(cudaGetLastError());
   {
-    double total = 0.0;
-    for (const GradRef& r : refs) total += static_cast<double>(r.n);
-    ProfScope ps("clip_scale", cs, 0.0, 8.0 * total);
-    dim3 grid(4 * num_sms(), 1);
-    grid.y = static_cast<unsigned>(refs.size() < 64 ? refs.size() : 64);
-    grid.x = static_cast<unsigned>(4 * num_sms() / grid.y + 1);
+    double moved = 0.0;
+    for (const GradRef& r : refs) moved += 8.0 * static_cast<double>(r.n);
+    ProfScope ps("clip_scale", cs, 0.0, moved);
+    dim3 grid(1, static_cast<unsigned>(refs.size() < 64 ? refs.size() : 64));
+    grid.x = static_cast<unsigned>(8 * num_sms() / grid.y + 1);
     clip_scale_kernel<<<grid, 256, 0, cs>>>(s->refs, static_cast<int>(refs.size()), s->result);
   }
   KL_CUDA(cudaGetLastError());

@@ -314,8 +314,12 @@ KL_API kl_status kl_stream_create(const kl_stream_cfg* cfg, const kl_layer_weigh
  * backward in reverse re-streaming the weights, global-norm clip of every
  * weight gradient at clip_max_norm. X [T,H] and targets [T] are device.
  * grads[n_layers] and dW_lm [V,H]: destination of the clipped gradients, fp32,
- * device or host pinned memory (copies use cudaMemcpyDefault). *result is
- * written after the call returns; the call synchronises `stream`. */
+ * device memory or page-locked host memory (reached through its device-visible
+ * address). Gradients for device destinations are computed and scaled in
+ * place; gradients for host destinations are computed into device buffers the
+ * driver allocates on first use (fp32, every layer's gradients) and written
+ * out already clipped after the backward. *result is written before the call
+ * returns; the call synchronises `stream`. */
 KL_API kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets,
                         float clip_max_norm, const kl_layer_grads* grads, void* dW_lm,
                         kl_stream_result* result, void* stream);

@@ -86,3 +86,20 @@ def test_gemm_f32(kl, a_mn, b_mn):
     B32 = B.astype(np.float32).astype(np.float64)
     R32 = R.astype(np.float32).astype(np.float64)
     assert_rel(host(C), O.linear(A32, B32) + R32, 1e-6, "f32")
+
+
+@pytest.mark.parametrize("a_mn,b_mn,M,N,K", [(0, 0, 264, 520, 20480), (1, 1, 200, 136, 40960), (0, 1, 512, 256, 30720)])
+def test_gemm_bf16_long_k_split(kl, a_mn, b_mn, M, N, K):
+    """fp32 output without addend and K >= 16384: the launch cuts K into units
+    that different CTAs may own, summed with fp32 reductions."""
+    A, B, _ = _operands(M, N, K, 5)
+    a, lda = _store(A, a_mn, torch.bfloat16)
+    b, ldb = _store(B, b_mn, torch.bfloat16)
+    C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    for _ in range(2):   # the output is zeroed by the call itself
+        kl.kl_gemm(M, N, K, kl.KL_BF16, a.data_ptr(), lda, a_mn, b.data_ptr(), ldb, b_mn, C.data_ptr(), N,
+                   kl.KL_F32)
+        torch.cuda.synchronize()
+        # fp32 accumulation over K terms: rounding grows like sqrt(K) * 2^-24
+        tol = 2e-5 * max(1.0, (K / 8192) ** 0.5)
+        assert_rel(host(C), O.linear(A, B), tol, f"split C {M}x{N}x{K}")
