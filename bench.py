@@ -12,7 +12,7 @@ SwiGLU intermediate 25600, RoPE base 1e6, causal; bf16):
              vocab 151936
   stream     8 layers streamed from pinned host memory, batch 2 x seq 4096,
              lm-head CE, backward, global-norm clip at 1.0, gradients to
-             pinned host memory (one kl_stream_run per step)
+             device memory (one kl_stream_run per step)
 
 `value` is whole-job tokens/s with inputs resident in HBM; `e2e` is the same
 metric through the C ABI with each step's inputs copied from pinned host
@@ -291,10 +291,10 @@ def setup_stream(torch, K, L, synth, device, seed):
     h = K.kl_stream_create(K.StreamCfg(cfg, nl, V), structs, W.data_ptr())
     grads, gs = [], []
     for _ in range(nl):
-        g = {n: torch.empty(shp, dtype=torch.float32).pin_memory() for n, shp in L.weight_shapes(cfg).items()}
+        g = {n: torch.empty(shp, dtype=torch.float32, device=device) for n, shp in L.weight_shapes(cfg).items()}
         grads.append(g)
         gs.append(K.LayerGrads(*[g[n].data_ptr() for n in K.WEIGHT_FIELDS], K.KL_F32))
-    dW = torch.empty(V, H, dtype=torch.float32).pin_memory()
+    dW = torch.empty(V, H, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
 
     def run(x, t):
@@ -311,7 +311,7 @@ def setup_stream(torch, K, L, synth, device, seed):
     keep = (hosts, W, X, tgt, grads, dW, hX, ht, X2, t2, h)
     cfgd = {"workload": wl["desc"], "layers": nl, "batch": B, "seq_len": S, "hidden": H, "vocab": V,
             "clip_max_norm": wl["clip"], "weights": "pinned host, two device slots",
-            "grads": "fp32 to pinned host", "l2": "inputs larger than L2"}
+            "grads": "fp32, device", "l2": "inputs larger than L2"}
     return T, (lambda: run(X, tgt)), e2e, X.numel() * 2 + T * 4, 12, cfgd, keep
 
 

@@ -682,11 +682,7 @@ kl_status attention_fwd(int B, int S, int Hq, int Hkv, int d, int dtype, const v
   } else {
     if (!al16(q) || !al16(k) || !al16(v) || !al16(o))
       return set_error(KL_ERR_INVALID_ARG, "attention_fwd: bf16 buffers must be 16-byte aligned");
-    KL_TRY(set_smem_attrs());
-    dim3 grid((S + TB - 1) / TB, Hq, B);
-    fa_fwd_bf16_kernel<<<grid, 128, FWD_SMEM, st>>>(S, Hq, Hkv, (const __nv_bfloat16*)q,
-                                                   (const __nv_bfloat16*)k, (const __nv_bfloat16*)v,
-                                                   (__nv_bfloat16*)o, lse, scale * LOG2E);
+    KL_TRY(attention_fwd_tc(B, S, Hq, Hkv, q, k, v, o, lse, st));
   }
   KL_CUDA(cudaGetLastError());
   return KL_OK;

@@ -71,6 +71,9 @@ kl_status swiglu_bwd(int64_t n, int dtype, const void* dm, const void* g, const 
 // ---------------------------------------------------------------------------
 kl_status attention_fwd(int B, int S, int Hq, int Hkv, int d, int dtype, const void* q,
                         const void* k, const void* v, void* o, float* lse, cudaStream_t st);
+// bf16, head dim 128, on the tcgen05 tensor cores (attention_tc.cu).
+kl_status attention_fwd_tc(int B, int S, int Hq, int Hkv, const void* q, const void* k, const void* v,
+                           void* o, float* lse, cudaStream_t st);
 size_t attention_bwd_ws(int B, int S, int Hq, int Hkv, int d);
 // dq_out/dk_out/dv_out: fp32 accumulators [T,H*d] written by the kernel
 // (inside ws); the caller converts (with rotary backward) afterwards.

@@ -38,7 +38,10 @@ struct GradRef {
   const float* src;
   float* dst;
   int64_t n;
+  int64_t chunk_begin;   // first global 16384-element chunk of this tensor
 };
+
+constexpr int64_t SCALE_CHUNK = 16384;
 
 // partial[b] = sum of squares of p over the elements block b owns (fixed
 // assignment, fp32 within a thread over four interleaved accumulators, fp64
@@ -99,27 +102,32 @@ __global__ void clip_finalize_kernel(const double* __restrict__ partial, int cou
 }
 
 // dst = src * coef for every listed gradient (in place when src == dst, where
-// coef == 1 leaves nothing to do).
+// coef == 1 leaves nothing to do). The tensors are cut into chunks of
+// SCALE_CHUNK elements numbered across all of them; blocks stride over chunks.
 __global__ void __launch_bounds__(256) clip_scale_kernel(const GradRef* __restrict__ refs, int count,
+                                                         int64_t total_chunks,
                                                          const float* __restrict__ result) {
   const float coef = result[2];
-  for (int r = blockIdx.y; r < count; r += gridDim.y) {
+  int r = 0;
+  for (int64_t ch = blockIdx.x; ch < total_chunks; ch += gridDim.x) {
+    while (r + 1 < count && ch >= refs[r + 1].chunk_begin) ++r;
     const float* src = refs[r].src;
     float* dst = refs[r].dst;
-    const int64_t n = refs[r].n;
     if (src == dst && coef == 1.0f) continue;
-    const int64_t start = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    if (((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15u) == 0) {
-      const int64_t n4 = n >> 2;
-      for (int64_t i = start; i < n4; i += stride) {
-        float4 v = reinterpret_cast<const float4*>(src)[i];
+    const int64_t lo = (ch - refs[r].chunk_begin) * SCALE_CHUNK;
+    const int64_t hi = min(refs[r].n, lo + SCALE_CHUNK);
+    if (((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15u) == 0 && (lo & 3) == 0) {
+      const int64_t n4 = (hi - lo) >> 2;
+      const float4* s4 = reinterpret_cast<const float4*>(src + lo);
+      float4* d4 = reinterpret_cast<float4*>(dst + lo);
+      for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+        float4 v = s4[i];
         v.x *= coef; v.y *= coef; v.z *= coef; v.w *= coef;
-        reinterpret_cast<float4*>(dst)[i] = v;
+        d4[i] = v;
       }
-      for (int64_t i = (n4 << 2) + start; i < n; i += stride) dst[i] = src[i] * coef;
+      for (int64_t i = lo + (n4 << 2) + threadIdx.x; i < hi; i += blockDim.x) dst[i] = src[i] * coef;
     } else {
-      for (int64_t i = start; i < n; i += stride) dst[i] = src[i] * coef;
+      for (int64_t i = lo + threadIdx.x; i < hi; i += blockDim.x) dst[i] = src[i] * coef;
     }
   }
 }
@@ -400,10 +408,15 @@ kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets, flo
     for (int i = 0; i < 9; ++i)
       refs.push_back({static_cast<const float*>(*gfield(src[l], i)),
                       static_cast<float*>(device_visible(*gfield(dst[l], i))),
-                      static_cast<int64_t>(weight_elems(c, i))});
+                      static_cast<int64_t>(weight_elems(c, i)), 0});
   }
   float* dwlm_src = dwlm_on_device ? static_cast<float*>(dW_lm) : s->dwlm_retain;
-  refs.push_back({dwlm_src, static_cast<float*>(dwlm_dev), static_cast<int64_t>(s->cfg.V) * c.H});
+  refs.push_back({dwlm_src, static_cast<float*>(dwlm_dev), static_cast<int64_t>(s->cfg.V) * c.H, 0});
+  int64_t total_chunks = 0;
+  for (GradRef& r : refs) {
+    r.chunk_begin = total_chunks;
+    total_chunks += (r.n + SCALE_CHUNK - 1) / SCALE_CHUNK;
+  }
   KL_CUDA(cudaMemcpyAsync(s->refs, refs.data(), refs.size() * sizeof(GradRef), cudaMemcpyHostToDevice, cs));
 
   const size_t es = dtype_size(c.dtype);
@@ -474,9 +487,8 @@ kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets, flo
     double moved = 0.0;
     for (const GradRef& r : refs) moved += 8.0 * static_cast<double>(r.n);
     ProfScope ps("clip_scale", cs, 0.0, moved);
-    dim3 grid(1, static_cast<unsigned>(refs.size() < 64 ? refs.size() : 64));
-    grid.x = static_cast<unsigned>(8 * num_sms() / grid.y + 1);
-    clip_scale_kernel<<<grid, 256, 0, cs>>>(s->refs, static_cast<int>(refs.size()), s->result);
+    clip_scale_kernel<<<8 * num_sms(), 256, 0, cs>>>(s->refs, static_cast<int>(refs.size()), total_chunks,
+                                                     s->result);
   }
   KL_CUDA(cudaGetLastError());
   float host_res[4] = {};
