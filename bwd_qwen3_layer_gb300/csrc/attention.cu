@@ -733,22 +733,16 @@ kl_status attention_bwd_accum(int B, int S, int Hq, int Hkv, int d, int dtype, c
     if (!al16(q) || !al16(k) || !al16(v) || !al16(o) || !al16(dout))
       return set_error(KL_ERR_INVALID_ARG, "attention_bwd: bf16 buffers must be 16-byte aligned");
     KL_TRY(set_smem_attrs());
-    KL_CUDA(cudaMemsetAsync(dq, 0, T * Hq * d * 4, st));
     KL_CUDA(cudaMemsetAsync(dk, 0, T * Hkv * d * 4, st));
     KL_CUDA(cudaMemsetAsync(dv, 0, T * Hkv * d * 4, st));
     const int64_t rows = static_cast<int64_t>(T) * Hq;
     {
-    ProfScope ps("attn_bwd_pre_bf16", st, 0.0, 4.0 * T * Hq * d + 4.0 * T * Hq);
-    attn_bwd_pre_bf16_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
-        B, S, Hq, (const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, Dd);
+      ProfScope ps("attn_bwd_pre_bf16", st, 0.0, 4.0 * T * Hq * d + 4.0 * T * Hq);
+      attn_bwd_pre_bf16_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
+          B, S, Hq, (const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, Dd);
     }
     KL_CUDA(cudaGetLastError());
-    dim3 grid((S + TB - 1) / TB, Hq, B);
-    ProfScope ps("attn_bwd_bf16", st, bwd_flops,
-                 2.0 * T * (3.0 * Hq * d + 2.0 * Hkv * d) + 8.0 * T * Hq + 4.0 * T * (Hq + 2.0 * Hkv) * d);
-    fa_bwd_bf16_kernel<<<grid, 128, BWD_SMEM, st>>>(
-        S, Hq, Hkv, (const __nv_bfloat16*)q, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v,
-        (const __nv_bfloat16*)dout, lse, Dd, dq, dk, dv, scale * LOG2E, scale);
+    KL_TRY(attention_bwd_tc(B, S, Hq, Hkv, q, k, v, dout, lse, Dd, dq, dk, dv, st));
   }
   KL_CUDA(cudaGetLastError());
   return KL_OK;

@@ -53,6 +53,13 @@ struct FwdParams {
   uint32_t* err;
 };
 
+// 2^x with the hardware approximation (about 2 ulp; 0 for -inf).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -89,8 +96,8 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_kernel(const __grid_cons
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqb = (p.S + BQ - 1) / BQ;
-  const int qb = nqb - 1 - static_cast<int>(blockIdx.x);   // longest rows first
-  const int h = blockIdx.y, b = blockIdx.z;
+  const int qb = nqb - 1 - static_cast<int>(blockIdx.y);   // longest rows first (all heads)
+  const int h = blockIdx.x, b = blockIdx.z;
   const int j_kv = h * p.Hkv / p.Hq;
   const int q0 = qb * BQ;
   const int row0 = b * p.S;                    // first token row of this sequence
@@ -199,31 +206,40 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_kernel(const __grid_cons
     for (int j = 0; j < nkb; ++j) {
       const int s = j & 1;
       const uint32_t ph = (j >> 1) & 1;
-      if (*abort_flag || !mbar_wait(s_full(s), ph, p.err)) { ok = false; break; }
+      if (!mbar_wait_warp(s_full(s), ph, p.err, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const uint32_t sadr = tmem + lane_off + s * 128;
-      const bool diag = (j == nkb - 1);
-      // pass 1: row max of the scaled, masked scores
-      float mx = -INFINITY;
+      // the whole score row in registers: one TMEM round trip
+      uint32_t sv[BKV];
+      tmem_ld_32x32b_x32(sadr + 0, *reinterpret_cast<uint32_t(*)[32]>(sv + 0));
+      tmem_ld_32x32b_x32(sadr + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+      tmem_ld_32x32b_x32(sadr + 64, *reinterpret_cast<uint32_t(*)[32]>(sv + 64));
+      tmem_ld_32x32b_x32(sadr + 96, *reinterpret_cast<uint32_t(*)[32]>(sv + 96));
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_free(s));   // S[s] may be overwritten from here on
+      if (j == nkb - 1) {                      // diagonal tile: keys after the row are masked
+        const int lim = qrow - j * BKV;        // keys 0 .. lim are kept
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(sadr + c * 32, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int key = j * BKV + c * 32 + e;
-          float x = __uint_as_float(v[e]) * p.scale_log2;
-          if (diag && key > qrow) x = -INFINITY;
-          mx = fmaxf(mx, x);
-        }
+        for (int e = 0; e < BKV; ++e)
+          if (e > lim) sv[e] = __float_as_uint(-INFINITY);
       }
+      float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < BKV; e += 4) {
+        m0 = fmaxf(m0, __uint_as_float(sv[e]));
+        m1 = fmaxf(m1, __uint_as_float(sv[e + 1]));
+        m2 = fmaxf(m2, __uint_as_float(sv[e + 2]));
+        m3 = fmaxf(m3, __uint_as_float(sv[e + 3]));
+      }
+      const float mx = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * p.scale_log2;
       // raise the running max only when it grows by more than 2^8
       const bool raise = mx > m + 8.0f;
       const float m_new = raise ? mx : m;
-      const float alpha = raise ? exp2f(m - m_new) : 1.0f;
+      const float alpha = raise ? ex2_approx(m - m_new) : 1.0f;
       // O and the P buffer are stable once the previous P V product is done
-      if (j >= 1 && !mbar_wait(p_free, (j - 1) & 1, p.err)) { ok = false; break; }
+      if (j >= 1 && !mbar_wait_warp(p_free, (j - 1) & 1, p.err, abort_flag)) { ok = false; break; }
       if (j >= 1 && __any_sync(0xffffffffu, raise)) {
         tc_fence_after();
 #pragma unroll
@@ -237,23 +253,26 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_kernel(const __grid_cons
         }
         tmem_st_wait();
       }
-      // pass 2: probabilities, row sum, bf16 P into the swizzled K-major tile
-      float rs = 0.f;
+      // probabilities (one FFMA + one ex2 each), row sum, bf16 P into the
+      // swizzled K-major tile
+      const float neg = -m_new;
+      const float sc = p.scale_log2;
+      float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(sadr + c * 32, v);
-        tmem_ld_wait();
         uint32_t pk[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const int key = j * BKV + c * 32 + e;
-          const float x0 = __uint_as_float(v[e]) * p.scale_log2;
-          const float x1 = __uint_as_float(v[e + 1]) * p.scale_log2;
-          const float p0 = (diag && key > qrow) ? 0.f : exp2f(x0 - m_new);
-          const float p1 = (diag && key + 1 > qrow) ? 0.f : exp2f(x1 - m_new);
-          rs += p0 + p1;
+        for (int e = 0; e < 32; e += 4) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c * 32 + e]), sc, neg));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[c * 32 + e + 1]), sc, neg));
+          const float p2 = ex2_approx(fmaf(__uint_as_float(sv[c * 32 + e + 2]), sc, neg));
+          const float p3 = ex2_approx(fmaf(__uint_as_float(sv[c * 32 + e + 3]), sc, neg));
+          r0 += p0;
+          r1 += p1;
+          r2 += p2;
+          r3 += p3;
           pk[e >> 1] = pack_bf16x2(p0, p1);
+          pk[(e >> 1) + 1] = pack_bf16x2(p2, p3);
         }
         uint8_t* blk = prow + (c >> 1) * 16384;   // 64-key swizzle block
 #pragma unroll
@@ -263,18 +282,15 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_kernel(const __grid_cons
               make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
         }
       }
-      l = l * alpha + rs;
+      l = l * alpha + ((r0 + r1) + (r2 + r3));
       m = m_new;
       tc_fence_before();
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(s_free(s));
-        mbar_arrive(p_full);
-      }
+      if (lane == 0) mbar_arrive(p_full);
     }
     // O / l and lse once the last P V product is done
-    if (ok && mbar_wait(p_free, (nkb - 1) & 1, p.err)) {
+    if (ok && mbar_wait_warp(p_free, (nkb - 1) & 1, p.err, abort_flag)) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* orow = p.o + (static_cast<int64_t>(row0 + qrow) * p.Hq + h) * HD;
@@ -310,6 +326,480 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_kernel(const __grid_cons
   }
 }
 
+
+// ===========================================================================
+// Backward on the tensor cores. Two kernels, both recomputing P from lse:
+//   dK/dV: CTA = 128 keys of one query head; 64-query tiles from the diagonal
+//          on. S^T = K Q^T and dP^T = V dO^T (TMEM, double-buffered); thread =
+//          key row builds P^T and dS^T = P^T (dP^T - D) as bf16 in swizzled
+//          shared memory; dV += P^T dO and dK += dS^T Q accumulate in TMEM and
+//          are added at the end into the key/value head's fp32 accumulators
+//          (the head's query-head group adds into the same rows).
+//   dQ:    CTA = 128 queries of one head; 64-key tiles up to the diagonal.
+//          S = Q K^T and dP = dO V^T; thread = query row builds dS; dQ += dS K
+//          accumulates in TMEM and is written once (no atomics).
+// ===========================================================================
+constexpr uint32_t T64 = 64 * 128 * 2;   // 16 KB: a 64-row x 128-column bf16 tile (two 8 KB blocks)
+
+// K-major operand: R rows x 128 columns stored as two 64-column swizzle blocks
+// of R x 128 bytes; descriptor of k-step kk.
+__device__ __forceinline__ uint64_t desc_k128(uint32_t base, uint32_t block_bytes, int kk) {
+  return smem_desc_sw128(base + (kk >> 2) * block_bytes + (kk & 3) * 32, 16, 1024);
+}
+// K-major operand: R rows x 64 columns (one swizzle block).
+__device__ __forceinline__ uint64_t desc_k64(uint32_t base, int kk) {
+  return smem_desc_sw128(base + kk * 32, 16, 1024);
+}
+// MN-major view of a [K rows x 128 columns] tile (two 64-column blocks of
+// K x 128 bytes): N = the 128 columns, k-step kk = 16 rows.
+__device__ __forceinline__ uint64_t desc_mn128(uint32_t base, uint32_t block_bytes, int kk) {
+  return smem_desc_sw128(base + kk * 2048, block_bytes, 1024);
+}
+
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+struct BwdParams {
+  CUtensorMap tmQ, tmK, tmV, tmdO;   // box rows: see the kernels
+  const float* lse;                  // [B, Hq, S]
+  const float* Dd;                   // [B, Hq, S]
+  float* dq_acc;                     // [T, Hq*128]
+  float* dk_acc;                     // [T, Hkv*128]
+  float* dv_acc;                     // [T, Hkv*128]
+  int S, Hq, Hkv;
+  float scale_log2, scale;
+  uint32_t* err;
+};
+
+// ---------------------------------------------------------------------------
+// dK / dV
+// ---------------------------------------------------------------------------
+constexpr uint32_t KV_OFF_K = 0;
+constexpr uint32_t KV_OFF_V = KV_OFF_K + TILE_BYTES;
+constexpr uint32_t KV_OFF_Q = KV_OFF_V + TILE_BYTES;         // 2 stages of T64
+constexpr uint32_t KV_OFF_DO = KV_OFF_Q + 2 * T64;           // 2 stages of T64
+constexpr uint32_t PT_BYTES = 128 * 64 * 2;                   // 16 KB: 128 key rows x 64 queries
+constexpr uint32_t KV_OFF_P = KV_OFF_DO + 2 * T64;           // 2 buffers of P^T
+constexpr uint32_t KV_OFF_DS = KV_OFF_P + 2 * PT_BYTES;      // 2 buffers of dS^T
+constexpr uint32_t KV_OFF_BAR = KV_OFF_DS + 2 * PT_BYTES;
+constexpr size_t KV_SMEM = 1024 + KV_OFF_BAR + 256;
+
+__global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid_constant__ BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t bar = sb + KV_OFF_BAR;
+  const uint32_t kv_full = bar;
+  auto q_full = [&](int s) { return bar + 8 + 8 * s; };
+  auto q_free = [&](int s) { return bar + 24 + 8 * s; };
+  auto st_full = [&](int s) { return bar + 40 + 8 * s; };
+  auto st_free = [&](int s) { return bar + 56 + 8 * s; };
+  auto p_full = [&](int s) { return bar + 72 + 8 * s; };
+  auto p_free = [&](int s) { return bar + 88 + 8 * s; };
+  const uint32_t done = bar + 104;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + KV_OFF_BAR + 112);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + KV_OFF_BAR + 116);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kb = blockIdx.y;                 // key tiles near the start see the most queries
+  const int h = blockIdx.x, b = blockIdx.z;
+  const int jh = h * p.Hkv / p.Hq;
+  const int k0 = kb * BKV;
+  const int row0 = b * p.S;
+  const int nit = (p.S - k0 + 63) / 64;      // 64-query tiles from the diagonal to the end
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(q_full(s), 1);
+      mbar_init(q_free(s), 1);
+      mbar_init(st_full(s), 1);
+      mbar_init(st_free(s), 4);
+      mbar_init(p_full(s), 4);
+      mbar_init(p_free(s), 1);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA ----------------
+    mbar_arrive_expect_tx(kv_full, 2 * TILE_BYTES);
+    tma_load_2d(sb + KV_OFF_K, &p.tmK, jh * HD, row0 + k0, kv_full);
+    tma_load_2d(sb + KV_OFF_K + 16384, &p.tmK, jh * HD + 64, row0 + k0, kv_full);
+    tma_load_2d(sb + KV_OFF_V, &p.tmV, jh * HD, row0 + k0, kv_full);
+    tma_load_2d(sb + KV_OFF_V + 16384, &p.tmV, jh * HD + 64, row0 + k0, kv_full);
+    int issued = 0;
+    for (int it = 0; it < nit; ++it) {
+      const int s = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      if (*abort_flag || !mbar_wait(q_free(s), ph ^ 1u, p.err)) { *abort_flag = 1; break; }
+      const int qr = row0 + k0 + it * 64;
+      mbar_arrive_expect_tx(q_full(s), 2 * T64);
+      tma_load_2d(sb + KV_OFF_Q + s * T64, &p.tmQ, h * HD, qr, q_full(s));
+      tma_load_2d(sb + KV_OFF_Q + s * T64 + 8192, &p.tmQ, h * HD + 64, qr, q_full(s));
+      tma_load_2d(sb + KV_OFF_DO + s * T64, &p.tmdO, h * HD, qr, q_full(s));
+      tma_load_2d(sb + KV_OFF_DO + s * T64 + 8192, &p.tmdO, h * HD + 64, qr, q_full(s));
+      ++issued;
+    }
+    mbar_wait(kv_full, 0, p.err);
+    for (int it = (issued > 2 ? issued - 2 : 0); it < issued; ++it) mbar_wait(q_full(it & 1), (it >> 1) & 1, p.err);
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA ----------------
+    const uint32_t id_st = idesc_bf16_f32(128, 64, 0, 0);
+    const uint32_t id_gr = idesc_bf16_f32(128, 128, 0, 1);
+    bool ok = mbar_wait(kv_full, 0, p.err);
+    auto issue_grad = [&](int it) -> bool {
+      const int s = it & 1;
+      if (!mbar_wait(p_full(s), (it >> 1) & 1, p.err)) return false;
+      tc_fence_after();
+      const uint32_t sq = sb + KV_OFF_Q + s * T64, sdo = sb + KV_OFF_DO + s * T64;
+      for (int kk = 0; kk < 4; ++kk)
+        umma_bf16(tmem + 256, desc_k64(sb + KV_OFF_P + s * PT_BYTES, kk), desc_mn128(sdo, 8192, kk), id_gr,
+                  (it > 0 || kk > 0) ? 1u : 0u);
+      for (int kk = 0; kk < 4; ++kk)
+        umma_bf16(tmem + 384, desc_k64(sb + KV_OFF_DS + s * PT_BYTES, kk), desc_mn128(sq, 8192, kk), id_gr,
+                  (it > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(q_free(s));
+      umma_commit(p_free(s));
+      return true;
+    };
+    for (int it = 0; ok && it < nit; ++it) {
+      const int s = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      if (*abort_flag || !mbar_wait(q_full(s), ph, p.err) || (it >= 2 && !mbar_wait(st_free(s), ph ^ 1u, p.err))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sq = sb + KV_OFF_Q + s * T64, sdo = sb + KV_OFF_DO + s * T64;
+      for (int kk = 0; kk < HD / 16; ++kk)
+        umma_bf16(tmem + s * 64, desc_k128(sb + KV_OFF_K, 16384, kk), desc_k128(sq, 8192, kk), id_st, kk > 0);
+      for (int kk = 0; kk < HD / 16; ++kk)
+        umma_bf16(tmem + 128 + s * 64, desc_k128(sb + KV_OFF_V, 16384, kk), desc_k128(sdo, 8192, kk), id_st, kk > 0);
+      umma_commit(st_full(s));
+      if (it >= 1 && !issue_grad(it - 1)) ok = false;
+    }
+    if (ok && !issue_grad(nit - 1)) ok = false;
+    if (!ok) *abort_flag = 1;
+    umma_commit(done);
+    mbar_wait(done, 0, p.err);
+  } else if (warp >= 2) {
+    // ---------------- P^T, dS^T (thread = key row) and the final dK/dV ----------------
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int key = k0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const float* lrow = p.lse + (static_cast<int64_t>(b) * p.Hq + h) * p.S;
+    const float* drow = p.Dd + (static_cast<int64_t>(b) * p.Hq + h) * p.S;
+    const bool vec_stat = (p.S & 3) == 0;     // rows of lse / D are 16-byte aligned
+    bool ok = true;
+    for (int it = 0; it < nit; ++it) {
+      const int s = it & 1;
+      const uint32_t ph = (it >> 1) & 1;
+      const int q0 = k0 + it * 64;
+      if (!mbar_wait_warp(st_full(s), ph, p.err, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sv[64], dv[64];
+      tmem_ld_32x32b_x32(tmem + lane_off + s * 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
+      tmem_ld_32x32b_x32(tmem + lane_off + s * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+      tmem_ld_32x32b_x32(tmem + lane_off + 128 + s * 64, *reinterpret_cast<uint32_t(*)[32]>(dv));
+      tmem_ld_32x32b_x32(tmem + lane_off + 128 + s * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(dv + 32));
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(st_free(s));
+      if (it >= 2 && !mbar_wait_warp(p_free(s), ph ^ 1u, p.err, abort_flag)) { ok = false; break; }
+      const int lim = key - q0;              // queries q0 + c with c >= lim see this key
+      uint8_t* prow = smem + KV_OFF_P + s * PT_BYTES + r * 128;
+      uint8_t* drw = smem + KV_OFF_DS + s * PT_BYTES + r * 128;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        // lse (log2 units, +inf past the sequence end) and D of these 8 queries
+        float l8[8], d8[8];
+        const int qa = q0 + c8 * 8;
+        if (vec_stat && qa + 8 <= p.S) {
+          const float4 la = *reinterpret_cast<const float4*>(lrow + qa);
+          const float4 lb = *reinterpret_cast<const float4*>(lrow + qa + 4);
+          const float4 da = *reinterpret_cast<const float4*>(drow + qa);
+          const float4 db = *reinterpret_cast<const float4*>(drow + qa + 4);
+          l8[0] = la.x; l8[1] = la.y; l8[2] = la.z; l8[3] = la.w;
+          l8[4] = lb.x; l8[5] = lb.y; l8[6] = lb.z; l8[7] = lb.w;
+          d8[0] = da.x; d8[1] = da.y; d8[2] = da.z; d8[3] = da.w;
+          d8[4] = db.x; d8[5] = db.y; d8[6] = db.z; d8[7] = db.w;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) l8[e] *= LOG2E_F;
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const bool in = qa + e < p.S;
+            l8[e] = in ? lrow[qa + e] * LOG2E_F : INFINITY;
+            d8[e] = in ? drow[qa + e] : 0.f;
+          }
+        }
+        uint32_t pk[4], dk4[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const int c = c8 * 8 + e;
+          float p0 = ex2_approx(fmaf(__uint_as_float(sv[c]), p.scale_log2, -l8[e]));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), p.scale_log2, -l8[e + 1]));
+          if (c < lim) p0 = 0.f;
+          if (c + 1 < lim) p1 = 0.f;
+          const float d0 = p0 * (__uint_as_float(dv[c]) - d8[e]);
+          const float d1 = p1 * (__uint_as_float(dv[c + 1]) - d8[e + 1]);
+          pk[e >> 1] = pack_bf16x2(p0, p1);
+          dk4[e >> 1] = pack_bf16x2(d0, d1);
+        }
+        const int off = ((c8 ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(prow + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(drw + off) = make_uint4(dk4[0], dk4[1], dk4[2], dk4[3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full(s));
+    }
+    // The TMEM loads are warp-collective: every lane takes part; only rows
+    // inside the sequence add their results.
+    if (ok && mbar_wait_warp(done, 0, p.err, abort_flag)) {
+      tc_fence_after();
+      const bool in = key < p.S;
+      const int64_t o = (static_cast<int64_t>(row0 + (in ? key : 0)) * p.Hkv + jh) * HD;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem + lane_off + 256 + c * 32, v);
+        tmem_ld_wait();
+        if (in) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            red_add_v4(p.dv_acc + o + c * 32 + e, __uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                       __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+        }
+        tmem_ld_32x32b_x32(tmem + lane_off + 384 + c * 32, v);
+        tmem_ld_wait();
+        if (in) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            red_add_v4(p.dk_acc + o + c * 32 + e, __uint_as_float(v[e]) * p.scale,
+                       __uint_as_float(v[e + 1]) * p.scale, __uint_as_float(v[e + 2]) * p.scale,
+                       __uint_as_float(v[e + 3]) * p.scale);
+        }
+      }
+    } else {
+      *abort_flag = 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dQ
+// ---------------------------------------------------------------------------
+constexpr uint32_t DQ_OFF_Q = 0;
+constexpr uint32_t DQ_OFF_DO = DQ_OFF_Q + TILE_BYTES;
+constexpr uint32_t DQ_OFF_K = DQ_OFF_DO + TILE_BYTES;       // 2 stages of T64
+constexpr uint32_t DQ_OFF_V = DQ_OFF_K + 2 * T64;           // 2 stages of T64
+constexpr uint32_t DQ_OFF_DS = DQ_OFF_V + 2 * T64;          // 2 buffers: 128 rows x 64 keys bf16 (16 KB)
+constexpr uint32_t DQ_OFF_BAR = DQ_OFF_DS + 2 * 16384;
+constexpr size_t DQ_SMEM = 1024 + DQ_OFF_BAR + 256;
+
+__global__ void __launch_bounds__(THREADS, 1) fa_bwd_dq_tc_kernel(const __grid_constant__ BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t bar = sb + DQ_OFF_BAR;
+  const uint32_t q_full = bar;
+  auto kv_full = [&](int s) { return bar + 8 + 8 * s; };
+  auto kv_free = [&](int s) { return bar + 24 + 8 * s; };
+  auto sd_full = [&](int s) { return bar + 40 + 8 * s; };
+  auto sd_free = [&](int s) { return bar + 56 + 8 * s; };
+  auto ds_full = [&](int s) { return bar + 72 + 8 * s; };
+  auto ds_free = [&](int s) { return bar + 88 + 8 * s; };
+  const uint32_t done = bar + 104;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + DQ_OFF_BAR + 112);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + DQ_OFF_BAR + 116);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nqb = (p.S + BQ - 1) / BQ;
+  const int qb = nqb - 1 - static_cast<int>(blockIdx.y);   // longest rows first (all heads)
+  const int h = blockIdx.x, b = blockIdx.z;
+  const int jh = h * p.Hkv / p.Hq;
+  const int q0 = qb * BQ;
+  const int row0 = b * p.S;
+  const int nkb = (min(q0 + BQ, p.S) + 63) / 64;            // 64-key tiles up to the diagonal
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_free(s), 1);
+      mbar_init(sd_full(s), 1);
+      mbar_init(sd_free(s), 4);
+      mbar_init(ds_full(s), 4);
+      mbar_init(ds_free(s), 1);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0 && lane == 0) {
+    mbar_arrive_expect_tx(q_full, 2 * TILE_BYTES);
+    tma_load_2d(sb + DQ_OFF_Q, &p.tmQ, h * HD, row0 + q0, q_full);
+    tma_load_2d(sb + DQ_OFF_Q + 16384, &p.tmQ, h * HD + 64, row0 + q0, q_full);
+    tma_load_2d(sb + DQ_OFF_DO, &p.tmdO, h * HD, row0 + q0, q_full);
+    tma_load_2d(sb + DQ_OFF_DO + 16384, &p.tmdO, h * HD + 64, row0 + q0, q_full);
+    int issued = 0;
+    for (int j = 0; j < nkb; ++j) {
+      const int s = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (*abort_flag || !mbar_wait(kv_free(s), ph ^ 1u, p.err)) { *abort_flag = 1; break; }
+      const int kr = row0 + j * 64;
+      mbar_arrive_expect_tx(kv_full(s), 2 * T64);
+      tma_load_2d(sb + DQ_OFF_K + s * T64, &p.tmK, jh * HD, kr, kv_full(s));
+      tma_load_2d(sb + DQ_OFF_K + s * T64 + 8192, &p.tmK, jh * HD + 64, kr, kv_full(s));
+      tma_load_2d(sb + DQ_OFF_V + s * T64, &p.tmV, jh * HD, kr, kv_full(s));
+      tma_load_2d(sb + DQ_OFF_V + s * T64 + 8192, &p.tmV, jh * HD + 64, kr, kv_full(s));
+      ++issued;
+    }
+    mbar_wait(q_full, 0, p.err);
+    for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) mbar_wait(kv_full(j & 1), (j >> 1) & 1, p.err);
+  } else if (warp == 1 && lane == 0) {
+    const uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);
+    const uint32_t id_q = idesc_bf16_f32(128, 128, 0, 1);
+    bool ok = mbar_wait(q_full, 0, p.err);
+    auto issue_dq = [&](int j) -> bool {
+      const int s = j & 1;
+      if (!mbar_wait(ds_full(s), (j >> 1) & 1, p.err)) return false;
+      tc_fence_after();
+      for (int kk = 0; kk < 4; ++kk)
+        umma_bf16(tmem + 256, desc_k64(sb + DQ_OFF_DS + s * 16384, kk), desc_mn128(sb + DQ_OFF_K + s * T64, 8192, kk),
+                  id_q, (j > 0 || kk > 0) ? 1u : 0u);
+      umma_commit(kv_free(s));
+      umma_commit(ds_free(s));
+      return true;
+    };
+    for (int j = 0; ok && j < nkb; ++j) {
+      const int s = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (*abort_flag || !mbar_wait(kv_full(s), ph, p.err) || (j >= 2 && !mbar_wait(sd_free(s), ph ^ 1u, p.err))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      for (int kk = 0; kk < HD / 16; ++kk)
+        umma_bf16(tmem + s * 64, desc_k128(sb + DQ_OFF_Q, 16384, kk), desc_k128(sb + DQ_OFF_K + s * T64, 8192, kk), id_s,
+                  kk > 0);
+      for (int kk = 0; kk < HD / 16; ++kk)
+        umma_bf16(tmem + 128 + s * 64, desc_k128(sb + DQ_OFF_DO, 16384, kk),
+                  desc_k128(sb + DQ_OFF_V + s * T64, 8192, kk), id_s, kk > 0);
+      umma_commit(sd_full(s));
+      if (j >= 1 && !issue_dq(j - 1)) ok = false;
+    }
+    if (ok && !issue_dq(nkb - 1)) ok = false;
+    if (!ok) *abort_flag = 1;
+    umma_commit(done);
+    mbar_wait(done, 0, p.err);
+  } else if (warp >= 2) {
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int qrow = q0 + r;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const int64_t li = (static_cast<int64_t>(b) * p.Hq + h) * p.S + qrow;
+    const float l2 = qrow < p.S ? p.lse[li] * LOG2E_F : INFINITY;
+    const float Dq = qrow < p.S ? p.Dd[li] : 0.f;
+    bool ok = true;
+    for (int j = 0; j < nkb; ++j) {
+      const int s = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!mbar_wait_warp(sd_full(s), ph, p.err, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sv[64], dv[64];
+      tmem_ld_32x32b_x32(tmem + lane_off + s * 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
+      tmem_ld_32x32b_x32(tmem + lane_off + s * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
+      tmem_ld_32x32b_x32(tmem + lane_off + 128 + s * 64, *reinterpret_cast<uint32_t(*)[32]>(dv));
+      tmem_ld_32x32b_x32(tmem + lane_off + 128 + s * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(dv + 32));
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sd_free(s));
+      if (j >= 2 && !mbar_wait_warp(ds_free(s), ph ^ 1u, p.err, abort_flag)) { ok = false; break; }
+      const int lim = qrow - j * 64;          // keys j*64 + c with c <= lim are kept
+      uint8_t* drw = smem + DQ_OFF_DS + s * 16384 + r * 128;
+#pragma unroll
+      for (int c8 = 0; c8 < 8; ++c8) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const int c = c8 * 8 + e;
+          float p0 = ex2_approx(fmaf(__uint_as_float(sv[c]), p.scale_log2, -l2));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), p.scale_log2, -l2));
+          if (c > lim) p0 = 0.f;
+          if (c + 1 > lim) p1 = 0.f;
+          pk[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[c]) - Dq), p1 * (__uint_as_float(dv[c + 1]) - Dq));
+        }
+        *reinterpret_cast<uint4*>(drw + ((c8 ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_full(s));
+    }
+    if (ok && mbar_wait_warp(done, 0, p.err, abort_flag)) {
+      tc_fence_after();
+      float* orow = p.dq_acc + (static_cast<int64_t>(row0 + qrow) * p.Hq + h) * HD;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem + lane_off + 256 + c * 32, v);
+        tmem_ld_wait();
+        if (qrow < p.S) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(orow + c * 32 + e) =
+                make_float4(__uint_as_float(v[e]) * p.scale, __uint_as_float(v[e + 1]) * p.scale,
+                            __uint_as_float(v[e + 2]) * p.scale, __uint_as_float(v[e + 3]) * p.scale);
+        }
+      }
+    } else {
+      *abort_flag = 1;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -324,13 +814,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode() {
   return fn;
 }
 
-// [rows, cols] bf16 row-major, box 64 columns x 128 rows, 128-byte swizzle.
-kl_status map_rows(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows) {
+// [rows, cols] bf16 row-major, box 64 columns x box_rows rows, 128-byte swizzle.
+kl_status map_rows(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t box_rows = 128) {
   auto fn = encode();
   if (!fn) return set_error(KL_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, 128};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -364,8 +854,66 @@ kl_status attention_fwd_tc(int B, int S, int Hq, int Hkv, const void* q, const v
                                  static_cast<int>(SMEM_BYTES)));
     attr_done |= uint64_t(1) << dev;
   }
-  dim3 grid((S + BQ - 1) / BQ, Hq, B);
+  dim3 grid(Hq, (S + BQ - 1) / BQ, B);
   fa_fwd_tc_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(p);
+  KL_CUDA(cudaGetLastError());
+  return KL_OK;
+}
+
+}  // namespace kl
+
+namespace kl {
+
+kl_status attention_bwd_tc(int B, int S, int Hq, int Hkv, const void* q, const void* k, const void* v,
+                           const void* dout, const float* lse, const float* Dd, float* dq_acc, float* dk_acc,
+                           float* dv_acc, cudaStream_t st) {
+  const uint64_t T = static_cast<uint64_t>(B) * S;
+  static uint64_t attr_done = 0;
+  int dev = 0;
+  KL_CUDA(cudaGetDevice(&dev));
+  if (dev < 64 && !(attr_done >> dev & 1u)) {
+    KL_CUDA(cudaFuncSetAttribute(fa_bwd_dkdv_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(KV_SMEM)));
+    KL_CUDA(cudaFuncSetAttribute(fa_bwd_dq_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(DQ_SMEM)));
+    attr_done |= uint64_t(1) << dev;
+  }
+  BwdParams p;
+  memset(&p, 0, sizeof(p));
+  p.lse = lse;
+  p.Dd = Dd;
+  p.dq_acc = dq_acc;
+  p.dk_acc = dk_acc;
+  p.dv_acc = dv_acc;
+  p.S = S;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.scale_log2 = LOG2E_F / sqrtf(static_cast<float>(HD));
+  p.scale = 1.0f / sqrtf(static_cast<float>(HD));
+  p.err = device_error_word();
+  const double pairs = 0.5 * static_cast<double>(S) * (S + 1);
+  // dK / dV: K and V tiles of 128 rows, Q and dO tiles of 64 rows
+  KL_TRY(map_rows(&p.tmK, k, static_cast<uint64_t>(Hkv) * HD, T, 128));
+  KL_TRY(map_rows(&p.tmV, v, static_cast<uint64_t>(Hkv) * HD, T, 128));
+  KL_TRY(map_rows(&p.tmQ, q, static_cast<uint64_t>(Hq) * HD, T, 64));
+  KL_TRY(map_rows(&p.tmdO, dout, static_cast<uint64_t>(Hq) * HD, T, 64));
+  {
+    ProfScope ps("attn_bwd_dkdv_tc", st, 8.0 * B * Hq * HD * pairs, 0.0);
+    dim3 grid(Hq, (S + BKV - 1) / BKV, B);
+    fa_bwd_dkdv_tc_kernel<<<grid, THREADS, KV_SMEM, st>>>(p);
+  }
+  KL_CUDA(cudaGetLastError());
+  // dQ: Q and dO tiles of 128 rows, K and V tiles of 64 rows
+  KL_TRY(map_rows(&p.tmQ, q, static_cast<uint64_t>(Hq) * HD, T, 128));
+  KL_TRY(map_rows(&p.tmdO, dout, static_cast<uint64_t>(Hq) * HD, T, 128));
+  KL_TRY(map_rows(&p.tmK, k, static_cast<uint64_t>(Hkv) * HD, T, 64));
+  KL_TRY(map_rows(&p.tmV, v, static_cast<uint64_t>(Hkv) * HD, T, 64));
+  {
+    // only the dQ product is algorithmic work here; S and dP are recomputed
+    ProfScope ps("attn_bwd_dq_tc", st, 2.0 * B * Hq * HD * pairs, 0.0);
+    dim3 grid(Hq, (S + BQ - 1) / BQ, B);
+    fa_bwd_dq_tc_kernel<<<grid, THREADS, DQ_SMEM, st>>>(p);
+  }
   KL_CUDA(cudaGetLastError());
   return KL_OK;
 }

@@ -377,7 +377,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t qphase = 0;
     int it = 0;
     while (true) {
-      if (*abort_flag || !mbar_wait(qfull_bar(q), qphase, p.err)) {
+      if (!mbar_wait_warp(qfull_bar(q), qphase, p.err, abort_flag)) {
         *abort_flag = 1;
         break;
       }
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const GemmProb& pr = p.prob[un.p];
       const int acc = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
-      if (*abort_flag || !mbar_wait(tfull_bar(acc), use & 1u, p.err)) {
+      if (!mbar_wait_warp(tfull_bar(acc), use & 1u, p.err, abort_flag)) {
         *abort_flag = 1;
         break;
       }

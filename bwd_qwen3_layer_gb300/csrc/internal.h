@@ -74,6 +74,11 @@ kl_status attention_fwd(int B, int S, int Hq, int Hkv, int d, int dtype, const v
 // bf16, head dim 128, on the tcgen05 tensor cores (attention_tc.cu).
 kl_status attention_fwd_tc(int B, int S, int Hq, int Hkv, const void* q, const void* k, const void* v,
                            void* o, float* lse, cudaStream_t st);
+// Backward on the tcgen05 tensor cores: dq_acc fully written; dk_acc, dv_acc
+// accumulated (zeroed by the caller).
+kl_status attention_bwd_tc(int B, int S, int Hq, int Hkv, const void* q, const void* k, const void* v,
+                           const void* dout, const float* lse, const float* Dd, float* dq_acc, float* dk_acc,
+                           float* dv_acc, cudaStream_t st);
 size_t attention_bwd_ws(int B, int S, int Hq, int Hkv, int d);
 // dq_out/dk_out/dv_out: fp32 accumulators [T,H*d] written by the kernel
 // (inside ws); the caller converts (with rotary backward) afterwards.

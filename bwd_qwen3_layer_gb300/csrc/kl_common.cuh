@@ -115,6 +115,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
   return true;
 }
 
+// Warp-uniform form for roles whose next step is a warp-collective instruction
+// (tcgen05.ld / tcgen05.st): every lane calls it and every lane gets the same
+// answer, false if the abort flag is set or any lane's wait gave up.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint32_t* err,
+                                               volatile int* abort_flag) {
+  const bool ok = !*abort_flag && mbar_wait(bar, parity, err);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ----------------------------------------------------------------------------
 // TMA (tiled tensor copies global -> shared, completion on an mbarrier)
 // ----------------------------------------------------------------------------
