@@ -435,6 +435,399 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// 2-CTA form (cta_group::2): a cluster of two CTAs computes 256 x 256 tiles.
+// Each CTA stages its 128-row half of A and its 128-row half of B per k-block
+// (32 KB; 6 stages); the leader (rank 0) issues tcgen05.mma M=256 N=256, which
+// reads both CTAs' halves and leaves rows 0..127 of the tile in the leader's
+// TMEM and rows 128..255 in the follower's. Compared with one CTA on a 128 x 256
+// tile this halves the operand bytes each SM stages and reads per FLOP.
+//   leader  warp 0: scheduler (unit ids to both CTAs through DSMEM) + TMA
+//           warp 1: TMEM (both CTAs allocate together) + MMA issue
+//   follower warp 0: TMA of its halves, completing on the leader's barrier
+//   both    warps 2..5: epilogue of their own 128 rows
+// ---------------------------------------------------------------------------
+constexpr int STAGES2 = 6;
+constexpr uint32_t HALF_BYTES = 128 * BK * 2;            // 16 KB
+constexpr uint32_t STAGE2_BYTES = 2 * HALF_BYTES;        // A half + B half
+constexpr size_t SMEM2_BYTES = 1024 + STAGES2 * STAGE2_BYTES + 512;
+
+__device__ __forceinline__ uint32_t mapa_rank(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait with cluster-scope acquire (arrivals may come from the peer CTA).
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, uint32_t* err) {
+  if (mbar_try_wait_cl(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  uint32_t n = 0;
+  while (!mbar_try_wait_cl(bar, parity)) {
+    if ((++n & 255u) == 0 && global_timer_ns() - t0 > KL_WAIT_LIMIT_NS) {
+      record_error(err, KL_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
+}
+__device__ __forceinline__ bool mbar_wait_cl_warp(uint32_t bar, uint32_t parity, uint32_t* err,
+                                                  volatile int* abort_flag) {
+  const bool ok = !*abort_flag && mbar_wait_cl(bar, parity, err);
+  return __all_sync(0xffffffffu, ok);
+}
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, int32_t x, int32_t y,
+                                                 uint32_t leader_bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(leader_bar)
+      : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                               uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on `bar` (same offset) in both CTAs when this thread's MMAs complete.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_pair_local(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ Unit decode_unit2(const GemmParams& P, int u) {
+  int p = 0;
+  while (p + 1 < P.nprob && u >= P.prob[p + 1].unit_begin) ++p;
+  const GemmProb& pr = P.prob[p];
+  const int local = u - pr.unit_begin;
+  const int si = local % pr.splits;
+  const int tile = local / pr.splits;
+  Unit r;
+  r.p = p;
+  if (pr.n_fast) {
+    r.n0 = (tile % pr.n_tiles) * 256;
+    r.m0 = (tile / pr.n_tiles) * 256;
+  } else {
+    r.m0 = (tile % pr.m_tiles) * 256;
+    r.n0 = (tile / pr.m_tiles) * 256;
+  }
+  r.kb_lo = static_cast<int>(static_cast<int64_t>(si) * pr.kb_total / pr.splits);
+  r.kb_hi = static_cast<int>(static_cast<int64_t>(si + 1) * pr.kb_total / pr.splits);
+  return r;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    gemm_bf16_tc2_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES2 * STAGE2_BYTES);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES2 + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES2 + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES2 + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES2 + 4);
+  auto qfull_bar = [&](int q) { return bar0 + 8u * (2 * STAGES2 + 5 + q); };
+  auto qempty_bar = [&](int q) { return bar0 + 8u * (2 * STAGES2 + 5 + SCHED_Q + q); };
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES2 + 5 + 2 * SCHED_Q);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  volatile int* qids = reinterpret_cast<volatile int*>(tmem_holder + 2);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES2; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 8);   // 4 epilogue warps in each CTA
+    }
+    mbar_init(drain_bar, 1);
+    for (int q = 0; q < SCHED_Q; ++q) {
+      mbar_init(qfull_bar(q), 1);
+      mbar_init(qempty_bar(q), 10);  // leader MMA + 4 epilogue warps, follower TMA + 4 epilogue warps
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_holder)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();   // both CTAs' barriers exist before either signals the other
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const uint32_t leader_qempty0 = mapa_rank(qempty_bar(0), 0);
+  const uint32_t leader_tempty0 = mapa_rank(tempty_bar(0), 0);
+  const uint32_t leader_full0 = mapa_rank(full_bar(0), 0);
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- scheduler (leader) + TMA (both) ----------------
+    for (int i = 0; i < p.nprob; ++i)
+      for (int s = 0; s < p.prob[i].nseg; ++s) {
+        tma_prefetch_desc(&p.tmA[p.prob[i].tmap_base + s]);
+        tma_prefetch_desc(&p.tmB[p.prob[i].tmap_base + s]);
+      }
+    const uint32_t follower_qfull0 = mapa_rank(qfull_bar(0), 1);
+    const uint32_t follower_qids0 = mapa_rank(smem_u32(const_cast<int*>(qids)), 1);
+    int stage = 0;
+    uint32_t phase = 0;
+    int q = 0;
+    uint32_t qphase = 0;
+    long issued = 0;
+    bool ok = true;
+    while (ok) {
+      int u;
+      if (leader) {
+        u = static_cast<int>(atomicAdd(&p.sched[0], 1u));
+        if (u >= p.total_units) u = -1;
+        if (*abort_flag || !mbar_wait_cl(qempty_bar(q), qphase ^ 1u, p.err)) {
+          *abort_flag = 1;
+          break;
+        }
+        qids[q] = u;
+        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(follower_qids0 + 4u * q), "r"(u) : "memory");
+        mbar_arrive(qfull_bar(q));
+        mbar_arrive_cluster(follower_qfull0 + 8u * q);
+      } else {
+        if (*abort_flag || !mbar_wait_cl(qfull_bar(q), qphase, p.err)) {
+          *abort_flag = 1;
+          break;
+        }
+        u = qids[q];
+        mbar_arrive_cluster(leader_qempty0 + 8u * q);
+      }
+      if (++q == SCHED_Q) {
+        q = 0;
+        qphase ^= 1u;
+      }
+      if (u < 0) break;
+      const Unit un = decode_unit2(p, u);
+      const GemmProb& pr = p.prob[un.p];
+      const int mh = un.m0 + 128 * static_cast<int>(rank);   // this CTA's rows of A
+      const int nh = un.n0 + 128 * static_cast<int>(rank);   // this CTA's rows of B
+      int s = 0, off = 0;
+      while (un.kb_lo >= off + pr.kb[s]) off += pr.kb[s++];
+      int kl = un.kb_lo - off;
+      for (int kbg = un.kb_lo; kbg < un.kb_hi; ++kbg, ++kl) {
+        if (kl == pr.kb[s]) {
+          ++s;
+          kl = 0;
+        }
+        const CUtensorMap* ta = &p.tmA[pr.tmap_base + s];
+        const CUtensorMap* tb = &p.tmB[pr.tmap_base + s];
+        if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u, p.err)) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+        const uint32_t fb = leader_full0 + 8u * stage;
+        if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * STAGE2_BYTES);
+        const uint32_t sa = sbase + stage * STAGE2_BYTES;
+        const uint32_t sb = sa + HALF_BYTES;
+        const int k0 = kl * BK;
+        if (!pr.a_mn) {
+          tma_load_2d_pair(sa, ta, k0, mh, fb);
+        } else {
+          tma_load_2d_pair(sa, ta, mh, k0, fb);
+          tma_load_2d_pair(sa + 8192, ta, mh + 64, k0, fb);
+        }
+        if (!pr.b_mn) {
+          tma_load_2d_pair(sb, tb, k0, nh, fb);
+        } else {
+          tma_load_2d_pair(sb, tb, nh, k0, fb);
+          tma_load_2d_pair(sb + 8192, tb, nh + 64, k0, fb);
+        }
+        ++issued;
+        if (++stage == STAGES2) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (leader) {
+      // the leader's full barriers see both CTAs' copies: wait for the last ones
+      const long outstanding = issued < STAGES2 ? issued : STAGES2;
+      for (long i = 0; i < outstanding; ++i) {
+        if (stage == 0) {
+          stage = STAGES2 - 1;
+          phase ^= 1u;
+        } else {
+          --stage;
+        }
+        mbar_wait(full_bar(stage), phase, p.err);
+      }
+    }
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ---------------- MMA issuer (leader) ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    int q = 0;
+    uint32_t qphase = 0;
+    int it = 0;
+    bool ok = true;
+    while (ok) {
+      if (*abort_flag || !mbar_wait(qfull_bar(q), qphase, p.err)) {
+        *abort_flag = 1;
+        break;
+      }
+      const int u = qids[q];
+      mbar_arrive(qempty_bar(q));
+      if (++q == SCHED_Q) {
+        q = 0;
+        qphase ^= 1u;
+      }
+      if (u < 0) break;
+      const Unit un = decode_unit2(p, u);
+      const GemmProb& pr = p.prob[un.p];
+      const int acc = it & 1;
+      const uint32_t use = static_cast<uint32_t>(it >> 1);
+      if (*abort_flag || !mbar_wait_cl(tempty_bar(acc), (use & 1u) ^ 1u, p.err)) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 256);
+      const uint32_t idesc = idesc_bf16_f32(256, 256, pr.a_mn, pr.b_mn);
+      uint32_t accumulate = 0;
+      for (int kbg = un.kb_lo; kbg < un.kb_hi; ++kbg) {
+        if (*abort_flag || !mbar_wait(full_bar(stage), phase, p.err)) {
+          ok = false;
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = sbase + stage * STAGE2_BYTES;
+        const uint32_t sb = sa + HALF_BYTES;
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          const uint64_t ad = pr.a_mn ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
+                                      : smem_desc_sw128(sa + k * 32, 16, 1024);
+          const uint64_t bd = pr.b_mn ? smem_desc_sw128(sb + k * 2048, 8192, 1024)
+                                      : smem_desc_sw128(sb + k * 32, 16, 1024);
+          umma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
+          accumulate = 1;
+        }
+        umma_commit_pair(empty_bar(stage));
+        if (++stage == STAGES2) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (ok) umma_commit_pair(tfull_bar(acc));
+      ++it;
+    }
+    umma_commit_pair_local(drain_bar);
+    mbar_wait(drain_bar, 0, p.err);
+  } else if (warp >= 2) {
+    // ---------------- epilogue (both CTAs, own 128 rows) ----------------
+    const int quarter = warp & 3;
+    int q = 0;
+    uint32_t qphase = 0;
+    int it = 0;
+    while (true) {
+      if (!mbar_wait_cl_warp(qfull_bar(q), qphase, p.err, abort_flag)) {
+        *abort_flag = 1;
+        break;
+      }
+      const int u = qids[q];
+      __syncwarp();
+      if (lane == 0) {
+        if (leader) mbar_arrive(qempty_bar(q));
+        else mbar_arrive_cluster(leader_qempty0 + 8u * q);
+      }
+      if (++q == SCHED_Q) {
+        q = 0;
+        qphase ^= 1u;
+      }
+      if (u < 0) break;
+      const Unit un = decode_unit2(p, u);
+      const GemmProb& pr = p.prob[un.p];
+      const int acc = it & 1;
+      const uint32_t use = static_cast<uint32_t>(it >> 1);
+      if (!mbar_wait_cl_warp(tfull_bar(acc), use & 1u, p.err, abort_flag)) {
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int row = un.m0 + 128 * static_cast<int>(rank) + quarter * 32 + lane;
+      for (int c = 0; c < 256 / 32; ++c) {
+        const int col0 = un.n0 + c * 32;
+        if (col0 >= pr.N) break;
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(
+            tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * 256 + c * 32), v);
+        tmem_ld_wait();
+        if (row < pr.M) store_chunk(pr, row, col0, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(leader_tempty0 + 8u * acc);
+      ++it;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();   // neither CTA leaves while the other may still signal it
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
+  }
+  if (threadIdx.x == 0 && leader) {
+    __threadfence();
+    const unsigned prev = atomicAdd(&p.sched[1], 1u);
+    if (prev == gridDim.x / 2 - 1) {
+      atomicExch(&p.sched[0], 0u);
+      atomicExch(&p.sched[1], 0u);
+      __threadfence();
+    }
+  }
+}
+
 // C = bf16(acc + R): finishes a problem that was accumulated in fp32.
 __global__ void gemm_finalize_kernel(int M, int N, const float* __restrict__ acc,
                                      void* __restrict__ C, int64_t ldc, int c_f32,
@@ -558,6 +951,10 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(int M, int N, int nseg, G
 // be accumulated in fp32 (fp32 output without addend, or a caller-provided
 // fp32 accumulator) are cut along K into units of at most ~UNIT_KB k-blocks,
 // so that no unit is long against a CTA's share of the launch.
+// Tile shape: pairs of CTAs (cta_group::2) on 256 x 256 tiles, or single CTAs
+// on 128 x 256 tiles.
+constexpr bool USE_PAIR = true;
+constexpr int TILE_M = USE_PAIR ? 256 : BM;
 constexpr int SPLIT_MIN_KB = 256;
 constexpr int UNIT_KB = 256;
 
@@ -626,16 +1023,17 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
       if (!aligned16(s.A[g]) || !aligned16(s.B[g]) || (s.lda[g] % 8) || (s.ldb[g] % 8))
         return set_error(KL_ERR_INVALID_ARG,
                          "gemm: bf16 operands need 16-byte aligned bases and row strides that are multiples of 8");
+      // A: 128-row boxes in both forms; B: each CTA of a pair stages 128 rows
       if (!s.a_mn) KL_TRY(make_map(&p.tmA[tm + g], s.A[g], s.K[g], s.M, s.lda[g], BM));
       else KL_TRY(make_map(&p.tmA[tm + g], s.A[g], s.M, s.K[g], s.lda[g], 64));
-      if (!s.b_mn) KL_TRY(make_map(&p.tmB[tm + g], s.B[g], s.K[g], s.N, s.ldb[g], BN));
+      if (!s.b_mn) KL_TRY(make_map(&p.tmB[tm + g], s.B[g], s.K[g], s.N, s.ldb[g], USE_PAIR ? 128 : BN));
       else KL_TRY(make_map(&p.tmB[tm + g], s.B[g], s.N, s.K[g], s.ldb[g], 64));
       pr.kb[g] = (s.K[g] + BK - 1) / BK;
       pr.kb_total += pr.kb[g];
       ksum += s.K[g];
     }
     tm += s.nseg;
-    pr.m_tiles = (s.M + BM - 1) / BM;
+    pr.m_tiles = (s.M + TILE_M - 1) / TILE_M;
     pr.n_tiles = (s.N + BN - 1) / BN;
     // keep the smaller operand resident in L2: walk its dimension fastest
     pr.n_fast = s.N < s.M ? 1 : 0;
@@ -682,12 +1080,19 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
   if (dev < 64 && !(attr_done >> dev & 1u)) {
     KL_CUDA(cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(SMEM_BYTES)));
+    KL_CUDA(cudaFuncSetAttribute(gemm_bf16_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(SMEM2_BYTES)));
     attr_done |= uint64_t(1) << dev;
   }
-  const int grid = units < num_sms() ? units : num_sms();
   {
     ProfScope ps(label, st, flops, bytes);
-    gemm_bf16_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(p);
+    if (USE_PAIR) {
+      const int pairs = units < num_sms() / 2 ? units : num_sms() / 2;
+      gemm_bf16_tc2_kernel<<<2 * pairs, NUM_THREADS, SMEM2_BYTES, st>>>(p);
+    } else {
+      const int grid = units < num_sms() ? units : num_sms();
+      gemm_bf16_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(p);
+    }
   }
   KL_CUDA(cudaGetLastError());
   for (int i = 0; i < nspec; ++i) {
