@@ -14,6 +14,10 @@ namespace {
 template <typename T> struct Vec;
 template <> struct Vec<float> {
   static constexpr int N = 4;
+  static __device__ __forceinline__ void decode(const uint4& a, float (&f)[8]) {
+    f[0] = __uint_as_float(a.x); f[1] = __uint_as_float(a.y);
+    f[2] = __uint_as_float(a.z); f[3] = __uint_as_float(a.w);
+  }
   static __device__ __forceinline__ void load(const float* p, float (&f)[8]) {
     float4 a = *reinterpret_cast<const float4*>(p);
     f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
@@ -24,6 +28,12 @@ template <> struct Vec<float> {
 };
 template <> struct Vec<__nv_bfloat16> {
   static constexpr int N = 8;
+  static __device__ __forceinline__ void decode(const uint4& a, float (&f)[8]) {
+    const float2 x0 = unpack_bf16x2(a.x), x1 = unpack_bf16x2(a.y), x2 = unpack_bf16x2(a.z),
+                 x3 = unpack_bf16x2(a.w);
+    f[0] = x0.x; f[1] = x0.y; f[2] = x1.x; f[3] = x1.y;
+    f[4] = x2.x; f[5] = x2.y; f[6] = x3.x; f[7] = x3.y;
+  }
   static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&f)[8]) {
     uint4 a = *reinterpret_cast<const uint4*>(p);
     float2 x0 = unpack_bf16x2(a.x), x1 = unpack_bf16x2(a.y), x2 = unpack_bf16x2(a.z),
@@ -95,6 +105,59 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_kernel(int rows, int width,
     }
   } else {
     for (int j = lane; j < width; j += 32) st_f(hr + j, ld_f(gamma + j) * (ld_f(xr + j) * r));
+  }
+}
+
+// RMSNorm forward, row form: one 128-thread CTA per row, the row held in
+// registers as raw 16-byte vectors (NC per thread), so x is read from HBM
+// once; sum of squares by warp shuffles plus one barrier.
+constexpr int RF_THREADS = 128, RF_MAXC = 8;
+
+template <typename T, int NC>
+__global__ void __launch_bounds__(RF_THREADS) rmsnorm_fwd_row_kernel(int width, const T* __restrict__ x,
+                                                                     const T* __restrict__ gamma, float eps,
+                                                                     T* __restrict__ h,
+                                                                     float* __restrict__ rstd) {
+  __shared__ float red[RF_THREADS / 32];
+  constexpr int V = Vec<T>::N;
+  const int row = blockIdx.x, tid = threadIdx.x;
+  const int chunks = width / V;
+  const int64_t off = static_cast<int64_t>(row) * width;
+  uint4 raw[NC];
+#pragma unroll
+  for (int j = 0; j < NC; ++j) {
+    const int c = tid + j * RF_THREADS;
+    if (c < chunks) raw[j] = *reinterpret_cast<const uint4*>(x + off + c * V);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int j = 0; j < NC; ++j) {
+    if (tid + j * RF_THREADS < chunks) {
+      float f[8];
+      Vec<T>::decode(raw[j], f);
+#pragma unroll
+      for (int e = 0; e < V; ++e) ss = fmaf(f[e], f[e], ss);
+    }
+  }
+  ss = warp_sum(ss);
+  if ((tid & 31) == 0) red[tid >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < RF_THREADS / 32; ++w) tot += red[w];
+  const float r = 1.0f / sqrtf(tot / static_cast<float>(width) + eps);
+  if (tid == 0) rstd[row] = r;
+#pragma unroll
+  for (int j = 0; j < NC; ++j) {
+    const int c = tid + j * RF_THREADS;
+    if (c < chunks) {
+      float f[8], g[8];
+      Vec<T>::decode(raw[j], f);
+      Vec<T>::load(gamma + c * V, g);
+#pragma unroll
+      for (int e = 0; e < V; ++e) f[e] = g[e] * (f[e] * r);
+      Vec<T>::store(h + off + c * V, f);
+    }
   }
 }
 
@@ -228,6 +291,129 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_rows_kernel(
   }
 }
 
+// RMSNorm backward for bf16 activations with an fp32 incoming gradient, row
+// form with 8-element chunks: one 256-thread CTA per row at a time, two CTAs
+// resident per SM. Every load of a row (dh, x and the residual gradient) is
+// issued before the row's dot-product barrier; gains stay in registers as
+// packed bf16 and the gain-gradient partial sums as fp32 across the CTA's rows.
+constexpr int RW_THREADS = 256, RW_MAXC = 4;
+
+template <int NC>
+__global__ void __launch_bounds__(RW_THREADS, 2) rmsnorm_bwd_row8_kernel(
+    int rows, int width, const float* __restrict__ dh, const __nv_bfloat16* __restrict__ x,
+    const __nv_bfloat16* __restrict__ gamma, const float* __restrict__ rstd,
+    const __nv_bfloat16* __restrict__ resid, __nv_bfloat16* __restrict__ dx,
+    float* __restrict__ partial) {
+  using T = __nv_bfloat16;
+  __shared__ float red[2][RW_THREADS / 32];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int chunks = width >> 3;
+  uint4 graw[NC];
+  float acc[NC][8];
+#pragma unroll
+  for (int j = 0; j < NC; ++j) {
+    const int c = tid + j * RW_THREADS;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
+    if (c < chunks) graw[j] = *reinterpret_cast<const uint4*>(gamma + 8 * c);
+  }
+  const float inv_w = 1.0f / static_cast<float>(width);
+  int buf = 0;
+  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+    const int64_t off = static_cast<int64_t>(row) * width;
+    float4 d0[NC], d1[NC];
+    uint4 xraw[NC], rraw[NC];
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+      const int c = tid + j * RW_THREADS;
+      if (c < chunks) {
+        d0[j] = *reinterpret_cast<const float4*>(dh + off + 8 * c);
+        d1[j] = *reinterpret_cast<const float4*>(dh + off + 8 * c + 4);
+        xraw[j] = *reinterpret_cast<const uint4*>(x + off + 8 * c);
+        rraw[j] = resid ? *reinterpret_cast<const uint4*>(resid + off + 8 * c) : make_uint4(0, 0, 0, 0);
+      }
+    }
+    const float r = rstd[row];
+    float dot = 0.f;
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+      if (tid + j * RW_THREADS < chunks) {
+        float xv[8], g[8];
+        Vec<T>::decode(xraw[j], xv);
+        Vec<T>::decode(graw[j], g);
+        const float dv[8] = {d0[j].x, d0[j].y, d0[j].z, d0[j].w, d1[j].x, d1[j].y, d1[j].z, d1[j].w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) dot = fmaf(dv[e] * g[e], xv[e], dot);
+      }
+    }
+    dot = warp_sum(dot);
+    if (lane == 0) red[buf][warp] = dot;
+    __syncthreads();
+    dot = 0.f;
+#pragma unroll
+    for (int w = 0; w < RW_THREADS / 32; ++w) dot += red[buf][w];
+    dot *= r * inv_w;
+    buf ^= 1;
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+      const int c = tid + j * RW_THREADS;
+      if (c < chunks) {
+        float xv[8], g[8], rv[8], o[8];
+        Vec<T>::decode(xraw[j], xv);
+        Vec<T>::decode(graw[j], g);
+        Vec<T>::decode(rraw[j], rv);
+        const float dv[8] = {d0[j].x, d0[j].y, d0[j].z, d0[j].w, d1[j].x, d1[j].y, d1[j].z, d1[j].w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float n = xv[e] * r;
+          o[e] = r * (dv[e] * g[e] - n * dot) + rv[e];
+          acc[j][e] = fmaf(dv[e], n, acc[j][e]);
+        }
+        Vec<T>::store(dx + off + 8 * c, o);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < NC; ++j) {
+    const int c = tid + j * RW_THREADS;
+    if (c < chunks) {
+      float* p = partial + static_cast<int64_t>(blockIdx.x) * width + 8 * c;
+      *reinterpret_cast<float4*>(p) = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+      *reinterpret_cast<float4*>(p + 4) = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
+    }
+  }
+}
+
+// out[c] = sum over the partial rows, width a multiple of 4: a CTA takes 32
+// columns (8 float4 lanes) and splits the rows over 32 groups, then a fixed
+// tree over the groups (deterministic).
+__global__ void __launch_bounds__(256) column_sum4_kernel(int nrows, int width,
+                                                          const float* __restrict__ partial,
+                                                          float* __restrict__ out) {
+  __shared__ float4 red[32][8];
+  const int cg = threadIdx.x & 7, rg = threadIdx.x >> 3;
+  const int c = blockIdx.x * 32 + cg * 4;
+  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (c < width) {
+#pragma unroll 4
+    for (int r = rg; r < nrows; r += 32) {
+      const float4 v = *reinterpret_cast<const float4*>(partial + static_cast<int64_t>(r) * width + c);
+      s.x += v.x; s.y += v.y; s.z += v.z; s.w += v.w;
+    }
+  }
+  red[rg][cg] = s;
+  __syncthreads();
+  for (int k = 16; k > 0; k >>= 1) {
+    if (rg < k) {
+      const float4 o = red[rg + k][cg];
+      float4& m = red[rg][cg];
+      m.x += o.x; m.y += o.y; m.z += o.z; m.w += o.w;
+    }
+    __syncthreads();
+  }
+  if (rg == 0 && c < width) *reinterpret_cast<float4*>(out + c) = red[0][cg];
+}
+
 // out[c] = sum over the partial rows (fixed order: deterministic).
 __global__ void __launch_bounds__(256) column_sum_kernel(int nrows, int width,
                                                          const float* __restrict__ partial,
@@ -244,34 +430,56 @@ __global__ void __launch_bounds__(256) column_sum_kernel(int nrows, int width,
 }
 
 int rmsnorm_bwd_grid(int rows) {
-  const int want = (rows + 7) / 8;
+  const int want = rows;
   const int cap = 2 * num_sms();
   return want < cap ? want : cap;
 }
 
 // ---------------------------------------------------------------------------
-// RoPE: one CTA per token. The plane angles s * base^(-2i/d) are formed and
-// reduced in fp64 (exact enough at any position), cos/sin rounded to fp32
-// and kept in shared memory; every head of the token then uses them.
-// Plane i pairs element i with element i + d/2.
+// RoPE. Plane i pairs element i with element i + d/2 and turns it by the
+// angle s * base^(-2i/d). The inverse frequencies are formed on the host in
+// fp64 and passed by value; on the device the angle s * inv_freq is formed in
+// fp64 and reduced modulo 2 pi with a two-part constant (Cody and Waite's
+// reduction), so that only a remainder in [-pi, pi] goes to the fp32 sincosf.
+// The absolute error of cos/sin is then a few fp32 ulps of 1 at any position.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void rope_table(int s, int d, float base, float dir, float* cs) {
+constexpr int ROPE_MAX_HALF = 128;
+struct RopeFreq {
+  double inv[ROPE_MAX_HALF];
+};
+
+RopeFreq rope_freq(int d, float base) {
+  RopeFreq f;
+  for (int i = 0; i < ROPE_MAX_HALF; ++i)
+    f.inv[i] = i < d / 2 ? pow(static_cast<double>(base), -2.0 * i / d) : 0.0;
+  return f;
+}
+
+__device__ __forceinline__ void rope_cos_sin(int s, double inv, float dir, float* c, float* sn) {
+  const double two_pi_hi = 6.283185307179586;           // 2 pi rounded to double
+  const double two_pi_lo = 2.4492935982947064e-16;      // 2 pi - two_pi_hi
+  const double a = static_cast<double>(s) * inv;
+  const double k = rint(a * (1.0 / 6.283185307179586));
+  double r = fma(-k, two_pi_hi, a);
+  r = fma(-k, two_pi_lo, r);
+  float sf, cf;
+  sincosf(static_cast<float>(r), &sf, &cf);
+  *c = cf;
+  *sn = dir * sf;
+}
+
+// cos in cs[0, half), dir*sin in cs[half, d); the caller synchronises.
+__device__ __forceinline__ void rope_table(int s, int d, const RopeFreq& f, float dir, float* cs) {
   const int half = d / 2;
-  for (int i = threadIdx.x; i < half; i += blockDim.x) {
-    const double inv = pow(static_cast<double>(base), -2.0 * i / d);
-    double sn, c;
-    sincos(static_cast<double>(s) * inv, &sn, &c);
-    cs[i] = static_cast<float>(c);
-    cs[half + i] = dir * static_cast<float>(sn);
-  }
-  __syncthreads();
+  for (int i = threadIdx.x; i < half; i += blockDim.x) rope_cos_sin(s, f.inv[i], dir, &cs[i], &cs[half + i]);
 }
 
 template <typename T>
-__global__ void rope_kernel(int S, int heads, int d, float base, T* __restrict__ x, float dir) {
-  extern __shared__ float cs[];
+__global__ void rope_kernel(int S, int heads, int d, RopeFreq f, T* __restrict__ x, float dir) {
+  __shared__ float cs[2 * ROPE_MAX_HALF];
   const int t = blockIdx.x;
-  rope_table(t % S, d, base, dir, cs);
+  rope_table(t % S, d, f, dir, cs);
+  __syncthreads();
   const int half = d / 2;
   T* row = x + static_cast<int64_t>(t) * heads * d;
   for (int idx = threadIdx.x; idx < heads * half; idx += blockDim.x) {
@@ -285,76 +493,123 @@ __global__ void rope_kernel(int S, int heads, int d, float base, T* __restrict__
 }
 
 // Forward (dir = +1) or backward (dir = -1) rotation of q [T, hq, d] and k
-// [T, hk, d] in place, one CTA per token, VEC-wide vector accesses.
+// [T, hk, d] in place, one CTA per token. A work item is V consecutive planes
+// of one head (elements i0 .. i0+V-1 and their partners at +d/2); each thread
+// issues the loads of all its items before the angle table is formed, so the
+// table's arithmetic overlaps the memory latency.
+constexpr int RQ_THREADS = 128, RQ_ITEMS = 5;
+
 template <typename T>
-__global__ void __launch_bounds__(128) rope_qk_kernel(int S, int hq, int hk, int d, float base,
-                                                      T* __restrict__ q, T* __restrict__ k,
-                                                      float dir) {
-  extern __shared__ float cs[];
+__global__ void __launch_bounds__(RQ_THREADS) rope_qk_kernel(int S, int hq, int hk, int d, RopeFreq f,
+                                                             T* __restrict__ q, T* __restrict__ k,
+                                                             float dir) {
+  __shared__ float cs[2 * ROPE_MAX_HALF];
   const int t = blockIdx.x;
-  rope_table(t % S, d, base, dir, cs);
   const int half = d / 2;
   constexpr int V = Vec<T>::N;
   const int groups = half / V;
   const int items = (hq + hk) * groups;
-  for (int idx = threadIdx.x; idx < items; idx += blockDim.x) {
-    const int h = idx / groups, i0 = (idx - h * groups) * V;
-    T* p = h < hq ? q + (static_cast<int64_t>(t) * hq + h) * d
-                  : k + (static_cast<int64_t>(t) * hk + (h - hq)) * d;
-    float a[8], b[8];
-    Vec<T>::load(p + i0, a);
-    Vec<T>::load(p + half + i0, b);
+  for (int base = 0; base < items; base += RQ_THREADS * RQ_ITEMS) {
+    uint4 ra[RQ_ITEMS], rb[RQ_ITEMS];
 #pragma unroll
-    for (int e = 0; e < V; ++e) {
-      const float c = cs[i0 + e], sn = cs[half + i0 + e];
-      const float x = a[e], y = b[e];
-      a[e] = x * c - y * sn;
-      b[e] = x * sn + y * c;
+    for (int j = 0; j < RQ_ITEMS; ++j) {
+      const int idx = base + threadIdx.x + j * RQ_THREADS;
+      if (idx < items) {
+        const int h = idx / groups, i0 = (idx - h * groups) * V;
+        const T* p = h < hq ? q + (static_cast<int64_t>(t) * hq + h) * d
+                            : k + (static_cast<int64_t>(t) * hk + (h - hq)) * d;
+        ra[j] = *reinterpret_cast<const uint4*>(p + i0);
+        rb[j] = *reinterpret_cast<const uint4*>(p + half + i0);
+      }
     }
-    Vec<T>::store(p + i0, a);
-    Vec<T>::store(p + half + i0, b);
+    if (base == 0) {
+      rope_table(t % S, d, f, dir, cs);
+      __syncthreads();
+    }
+#pragma unroll
+    for (int j = 0; j < RQ_ITEMS; ++j) {
+      const int idx = base + threadIdx.x + j * RQ_THREADS;
+      if (idx < items) {
+        const int h = idx / groups, i0 = (idx - h * groups) * V;
+        T* p = h < hq ? q + (static_cast<int64_t>(t) * hq + h) * d
+                      : k + (static_cast<int64_t>(t) * hk + (h - hq)) * d;
+        float a[8], b[8];
+        Vec<T>::decode(ra[j], a);
+        Vec<T>::decode(rb[j], b);
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+          const float c = cs[i0 + e], sn = cs[half + i0 + e];
+          const float x = a[e], y = b[e];
+          a[e] = x * c - y * sn;
+          b[e] = x * sn + y * c;
+        }
+        Vec<T>::store(p + i0, a);
+        Vec<T>::store(p + half + i0, b);
+      }
+    }
   }
 }
 
-// Attention-backward epilogue: fp32 accumulators -> dq, dk rotated back by
-// -angle, dv converted; one CTA per token, 4-wide vectors.
+// Attention-backward epilogue: fp32 accumulators -> dq, dk turned back by
+// -angle, dv converted; one CTA per token. Items are 4-wide: a rotation item
+// reads planes i0..i0+3 and their partners, a dv item reads 4 elements; all
+// of a thread's loads are issued before the table is formed.
+constexpr int RC_THREADS = 256, RC_ITEMS = 6;
+
 template <typename T>
-__global__ void __launch_bounds__(128) rope_bwd_convert_kernel(
-    int S, int hq, int hk, int d, float base, const float* __restrict__ dq_acc,
+__global__ void __launch_bounds__(RC_THREADS) rope_bwd_convert_kernel(
+    int S, int hq, int hk, int d, RopeFreq f, const float* __restrict__ dq_acc,
     const float* __restrict__ dk_acc, const float* __restrict__ dv_acc, T* __restrict__ dq,
     T* __restrict__ dk, T* __restrict__ dv) {
-  extern __shared__ float cs[];
+  __shared__ float cs[2 * ROPE_MAX_HALF];
   const int t = blockIdx.x;
-  rope_table(t % S, d, base, -1.0f, cs);
   const int half = d / 2;
   const int groups = half / 4;
   const int rot_items = (hq + hk) * groups;
   const int items = rot_items + hk * (d / 4);
-  for (int idx = threadIdx.x; idx < items; idx += blockDim.x) {
-    if (idx < rot_items) {
-      const int h = idx / groups, i0 = (idx - h * groups) * 4;
-      const int64_t o = h < hq ? (static_cast<int64_t>(t) * hq + h) * d
-                               : (static_cast<int64_t>(t) * hk + (h - hq)) * d;
-      const float* src = h < hq ? dq_acc : dk_acc;
-      T* dst = h < hq ? dq : dk;
-      float a[4], b[4];
-      load4(src + o + i0, a);
-      load4(src + o + half + i0, b);
+  for (int base = 0; base < items; base += RC_THREADS * RC_ITEMS) {
+    float4 ra[RC_ITEMS], rb[RC_ITEMS];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float c = cs[i0 + e], sn = cs[half + i0 + e];
-        const float x = a[e], y = b[e];
-        a[e] = x * c - y * sn;
-        b[e] = x * sn + y * c;
+    for (int j = 0; j < RC_ITEMS; ++j) {
+      const int idx = base + threadIdx.x + j * RC_THREADS;
+      if (idx < rot_items) {
+        const int h = idx / groups, i0 = (idx - h * groups) * 4;
+        const float* src = h < hq ? dq_acc + (static_cast<int64_t>(t) * hq + h) * d
+                                  : dk_acc + (static_cast<int64_t>(t) * hk + (h - hq)) * d;
+        ra[j] = *reinterpret_cast<const float4*>(src + i0);
+        rb[j] = *reinterpret_cast<const float4*>(src + half + i0);
+      } else if (idx < items) {
+        const int64_t o = static_cast<int64_t>(t) * hk * d + static_cast<int64_t>(idx - rot_items) * 4;
+        ra[j] = *reinterpret_cast<const float4*>(dv_acc + o);
       }
-      store4(dst + o + i0, a);
-      store4(dst + o + half + i0, b);
-    } else {
-      const int j = idx - rot_items;
-      const int64_t o = static_cast<int64_t>(t) * hk * d + static_cast<int64_t>(j) * 4;
-      float a[4];
-      load4(dv_acc + o, a);
-      store4(dv + o, a);
+    }
+    if (base == 0) {
+      rope_table(t % S, d, f, -1.0f, cs);
+      __syncthreads();
+    }
+#pragma unroll
+    for (int j = 0; j < RC_ITEMS; ++j) {
+      const int idx = base + threadIdx.x + j * RC_THREADS;
+      if (idx < rot_items) {
+        const int h = idx / groups, i0 = (idx - h * groups) * 4;
+        T* dst = h < hq ? dq + (static_cast<int64_t>(t) * hq + h) * d
+                        : dk + (static_cast<int64_t>(t) * hk + (h - hq)) * d;
+        float a[4] = {ra[j].x, ra[j].y, ra[j].z, ra[j].w};
+        float b[4] = {rb[j].x, rb[j].y, rb[j].z, rb[j].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float c = cs[i0 + e], sn = cs[half + i0 + e];
+          const float x = a[e], y = b[e];
+          a[e] = x * c - y * sn;
+          b[e] = x * sn + y * c;
+        }
+        store4(dst + i0, a);
+        store4(dst + half + i0, b);
+      } else if (idx < items) {
+        const int64_t o = static_cast<int64_t>(t) * hk * d + static_cast<int64_t>(idx - rot_items) * 4;
+        const float a[4] = {ra[j].x, ra[j].y, ra[j].z, ra[j].w};
+        store4(dv + o, a);
+      }
     }
   }
 }
@@ -444,17 +699,33 @@ kl_status rmsnorm_fwd(int rows, int width, int dtype, const void* x, const void*
   const int grid = (rows + 7) / 8;
   ProfScope ps("rmsnorm_fwd", st, 0.0,
                2.0 * rows * width * dtype_size(dtype) + 4.0 * rows + 1.0 * width * dtype_size(dtype));
-  if (dtype == KL_BF16) {
+  if (dtype != KL_BF16 && dtype != KL_F32) return set_error(KL_ERR_INVALID_ARG, "rmsnorm_fwd: bad dtype %d", dtype);
+  const int V = dtype == KL_BF16 ? 8 : 4;
+  const bool vec = width % V == 0 && al16(x) && al16(gamma) && al16(h);
+  const int nc = (width / V + RF_THREADS - 1) / RF_THREADS;
+  if (vec && nc <= RF_MAXC) {
+    if (dtype == KL_BF16) {
+      using T = __nv_bfloat16;
+      switch (nc) {
+#define KL_RF_CASE(N) case N: rmsnorm_fwd_row_kernel<T, N><<<rows, RF_THREADS, 0, st>>>(width, (const T*)x, (const T*)gamma, eps, (T*)h, rstd); break;
+        KL_RF_CASE(1) KL_RF_CASE(2) KL_RF_CASE(3) KL_RF_CASE(4) KL_RF_CASE(5) KL_RF_CASE(6) KL_RF_CASE(7) KL_RF_CASE(8)
+#undef KL_RF_CASE
+      }
+    } else {
+      using T = float;
+      switch (nc) {
+#define KL_RF_CASE(N) case N: rmsnorm_fwd_row_kernel<T, N><<<rows, RF_THREADS, 0, st>>>(width, (const T*)x, (const T*)gamma, eps, (T*)h, rstd); break;
+        KL_RF_CASE(1) KL_RF_CASE(2) KL_RF_CASE(3) KL_RF_CASE(4) KL_RF_CASE(5) KL_RF_CASE(6) KL_RF_CASE(7) KL_RF_CASE(8)
+#undef KL_RF_CASE
+      }
+    }
+  } else if (dtype == KL_BF16) {
     using T = __nv_bfloat16;
-    const bool vec = width % 8 == 0 && al16(x) && al16(gamma) && al16(h);
     if (vec) rmsnorm_fwd_kernel<T, true><<<grid, 256, 0, st>>>(rows, width, (const T*)x, (const T*)gamma, eps, (T*)h, rstd);
     else rmsnorm_fwd_kernel<T, false><<<grid, 256, 0, st>>>(rows, width, (const T*)x, (const T*)gamma, eps, (T*)h, rstd);
-  } else if (dtype == KL_F32) {
-    const bool vec = width % 4 == 0 && al16(x) && al16(gamma) && al16(h);
+  } else {
     if (vec) rmsnorm_fwd_kernel<float, true><<<grid, 256, 0, st>>>(rows, width, (const float*)x, (const float*)gamma, eps, (float*)h, rstd);
     else rmsnorm_fwd_kernel<float, false><<<grid, 256, 0, st>>>(rows, width, (const float*)x, (const float*)gamma, eps, (float*)h, rstd);
-  } else {
-    return set_error(KL_ERR_INVALID_ARG, "rmsnorm_fwd: bad dtype %d", dtype);
   }
   KL_CUDA(cudaGetLastError());
   return KL_OK;
@@ -479,9 +750,12 @@ kl_status rmsnorm_bwd(int rows, int width, int dtype, const void* dh, int dh_dty
   const int grid = rmsnorm_bwd_grid(rows);
   float* partial = static_cast<float*>(ws);
   const size_t es = dtype_size(dtype);
-  // row-parallel kernel: fp32 dh, width a multiple of 4 up to 8192, 16-byte aligned rows
-  const bool rows_form = dh_dtype == KL_F32 && width % 4 == 0 && width <= 256 * 4 * RB_MAXC &&
-                         al16(dh) && al16(x) && al16(dx) && al16(gamma) && (!resid || al16(resid)) &&
+  const bool aligned = al16(dh) && al16(x) && al16(dx) && al16(gamma) && (!resid || al16(resid));
+  // bf16 row form: fp32 dh, width a multiple of 8 up to 8192
+  const int nc8 = (width / 8 + RW_THREADS - 1) / RW_THREADS;
+  const bool row8_form = dtype == KL_BF16 && dh_dtype == KL_F32 && width % 8 == 0 && nc8 <= RW_MAXC && aligned;
+  // generic row form: fp32 dh, width a multiple of 4 up to 8192, 16-byte aligned rows
+  const bool rows_form = dh_dtype == KL_F32 && width % 4 == 0 && width <= 256 * 4 * RB_MAXC && aligned &&
                          (width * es) % 16 == 0;
   {
     ProfScope ps("rmsnorm_bwd", st, 0.0,
@@ -490,7 +764,13 @@ kl_status rmsnorm_bwd(int rows, int width, int dtype, const void* dh, int dh_dty
     const size_t sm = width * sizeof(float);
     if (dtype == KL_BF16) {
       using T = __nv_bfloat16;
-      if (rows_form)
+      if (row8_form) {
+        switch (nc8) {
+#define KL_RW_CASE(N) case N: rmsnorm_bwd_row8_kernel<N><<<grid, RW_THREADS, 0, st>>>(rows, width, (const float*)dh, (const T*)x, (const T*)gamma, rstd, (const T*)resid, (T*)dx, partial); break;
+          KL_RW_CASE(1) KL_RW_CASE(2) KL_RW_CASE(3) KL_RW_CASE(4)
+#undef KL_RW_CASE
+        }
+      } else if (rows_form)
         rmsnorm_bwd_rows_kernel<T><<<grid, 256, 0, st>>>(rows, width, (const float*)dh, (const T*)x, (const T*)gamma, rstd, (const T*)resid, (T*)dx, partial);
       else if (dh_dtype == KL_F32)
         rmsnorm_bwd_kernel<T, float><<<grid, 256, sm, st>>>(rows, width, (const float*)dh, (const T*)x, (const T*)gamma, rstd, (const T*)resid, (T*)dx, partial);
@@ -505,7 +785,10 @@ kl_status rmsnorm_bwd(int rows, int width, int dtype, const void* dh, int dh_dty
   }
   KL_CUDA(cudaGetLastError());
   ProfScope ps2("rmsnorm_bwd_colsum", st, 0.0, 4.0 * grid * width + 4.0 * width);
-  column_sum_kernel<<<(width + 63) / 64, 256, 0, st>>>(grid, width, partial, dgamma);
+  if (width % 4 == 0 && al16(dgamma))
+    column_sum4_kernel<<<(width + 31) / 32, 256, 0, st>>>(grid, width, partial, dgamma);
+  else
+    column_sum_kernel<<<(width + 63) / 64, 256, 0, st>>>(grid, width, partial, dgamma);
   KL_CUDA(cudaGetLastError());
   return KL_OK;
 }
@@ -516,24 +799,25 @@ kl_status rope_qk(int B, int S, int hq, int hk, int d, float base, int dtype, vo
       (hk > 0 && !k) || (direction != 1 && direction != -1))
     return set_error(KL_ERR_INVALID_ARG, "rope: bad arguments");
   if (dtype != KL_BF16 && dtype != KL_F32) return set_error(KL_ERR_INVALID_ARG, "rope: bad dtype");
+  if (d / 2 > ROPE_MAX_HALF) return set_error(KL_ERR_UNSUPPORTED, "rope: head dim %d above %d", d, 2 * ROPE_MAX_HALF);
   const int T = B * S;
-  const size_t sm = d * sizeof(float);
   const float dir = static_cast<float>(direction);
+  const RopeFreq f = rope_freq(d, base);
   const int V = dtype == KL_BF16 ? 8 : 4;
   const bool vec = (d / 2) % V == 0 && al16(q) && (hk == 0 || al16(k));
   ProfScope ps("rope", st, 0.0, 2.0 * T * (hq + hk) * d * dtype_size(dtype));
   if (vec) {
     if (dtype == KL_BF16)
-      rope_qk_kernel<__nv_bfloat16><<<T, 128, sm, st>>>(S, hq, hk, d, base, (__nv_bfloat16*)q, (__nv_bfloat16*)k, dir);
+      rope_qk_kernel<__nv_bfloat16><<<T, RQ_THREADS, 0, st>>>(S, hq, hk, d, f, (__nv_bfloat16*)q, (__nv_bfloat16*)k, dir);
     else
-      rope_qk_kernel<float><<<T, 128, sm, st>>>(S, hq, hk, d, base, (float*)q, (float*)k, dir);
+      rope_qk_kernel<float><<<T, RQ_THREADS, 0, st>>>(S, hq, hk, d, f, (float*)q, (float*)k, dir);
   } else {
     for (int w = 0; w < 2; ++w) {
       void* x = w == 0 ? q : k;
       const int heads = w == 0 ? hq : hk;
       if (heads == 0) continue;
-      if (dtype == KL_BF16) rope_kernel<__nv_bfloat16><<<T, 128, sm, st>>>(S, heads, d, base, (__nv_bfloat16*)x, dir);
-      else rope_kernel<float><<<T, 128, sm, st>>>(S, heads, d, base, (float*)x, dir);
+      if (dtype == KL_BF16) rope_kernel<__nv_bfloat16><<<T, 128, 0, st>>>(S, heads, d, f, (__nv_bfloat16*)x, dir);
+      else rope_kernel<float><<<T, 128, 0, st>>>(S, heads, d, f, (float*)x, dir);
     }
   }
   KL_CUDA(cudaGetLastError());
@@ -549,15 +833,16 @@ kl_status rope_bwd_convert(int B, int S, int hq, int hk, int d, float base, int 
                            const float* dq_acc, const float* dk_acc, const float* dv_acc, void* dq,
                            void* dk, void* dv, cudaStream_t st) {
   if (d % 8) return set_error(KL_ERR_UNSUPPORTED, "rope backward: head dim %d not a multiple of 8", d);
+  if (d / 2 > ROPE_MAX_HALF) return set_error(KL_ERR_UNSUPPORTED, "rope backward: head dim %d above %d", d, 2 * ROPE_MAX_HALF);
   const int T = B * S;
-  const size_t sm = d * sizeof(float);
+  const RopeFreq f = rope_freq(d, base);
   ProfScope ps("rope_bwd_convert", st, 0.0, 1.0 * T * (hq + 2 * hk) * d * (4 + dtype_size(dtype)));
   if (dtype == KL_BF16)
-    rope_bwd_convert_kernel<__nv_bfloat16><<<T, 128, sm, st>>>(S, hq, hk, d, base, dq_acc, dk_acc, dv_acc,
-                                                               (__nv_bfloat16*)dq, (__nv_bfloat16*)dk, (__nv_bfloat16*)dv);
+    rope_bwd_convert_kernel<__nv_bfloat16><<<T, RC_THREADS, 0, st>>>(S, hq, hk, d, f, dq_acc, dk_acc, dv_acc,
+                                                                     (__nv_bfloat16*)dq, (__nv_bfloat16*)dk, (__nv_bfloat16*)dv);
   else
-    rope_bwd_convert_kernel<float><<<T, 128, sm, st>>>(S, hq, hk, d, base, dq_acc, dk_acc, dv_acc, (float*)dq,
-                                                       (float*)dk, (float*)dv);
+    rope_bwd_convert_kernel<float><<<T, RC_THREADS, 0, st>>>(S, hq, hk, d, f, dq_acc, dk_acc, dv_acc, (float*)dq,
+                                                             (float*)dk, (float*)dv);
   KL_CUDA(cudaGetLastError());
   return KL_OK;
 }

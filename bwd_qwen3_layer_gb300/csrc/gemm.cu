@@ -437,21 +437,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 
 // ---------------------------------------------------------------------------
-// 2-CTA form (cta_group::2): a cluster of two CTAs computes 256 x 256 tiles.
-// Each CTA stages its 128-row half of A and its 128-row half of B per k-block
-// (32 KB; 6 stages); the leader (rank 0) issues tcgen05.mma M=256 N=256, which
-// reads both CTAs' halves and leaves rows 0..127 of the tile in the leader's
-// TMEM and rows 128..255 in the follower's. Compared with one CTA on a 128 x 256
-// tile this halves the operand bytes each SM stages and reads per FLOP.
-//   leader  warp 0: scheduler (unit ids to both CTAs through DSMEM) + TMA
-//           warp 1: TMEM (both CTAs allocate together) + MMA issue
-//   follower warp 0: TMA of its halves, completing on the leader's barrier
-//   both    warps 2..5: epilogue of their own 128 rows
+// Pair form (cta_group::2): a CTA pair computes 256 x 256 tiles, and a cluster
+// holds NP pairs stacked along M (NP = 1 or 2), so one cluster tile is
+// (256*NP) x 256.
+//   Per k-block each CTA stages its 128-row half of A (16 KB) and its 128-row
+//   half of B (16 KB); 6 stages. The pair leader (even rank) issues
+//   tcgen05.mma M=256 N=256, which reads both CTAs' halves and leaves rows
+//   0..127 of the pair's tile in the leader's TMEM and rows 128..255 in the
+//   follower's.
+//   With NP = 2 both pairs need the same B tile: the CTAs of equal parity in
+//   the two pairs hold the same B half, so each loads one 64-row piece of it
+//   and multicasts the piece to itself and its counterpart. That cuts the
+//   bytes read from L2 per FLOP by a quarter. A stage is then written by both
+//   pairs, so its "empty" barrier waits for both pairs' MMA commits.
+//   rank 0   warp 0: scheduler (unit ids to every CTA through DSMEM) + TMA
+//   others   warp 0: TMA of their own halves, completing on their pair
+//                    leader's barrier
+//   leaders  warp 1: TMEM (both CTAs of a pair allocate together) + MMA issue
+//   all      warps 2..5: epilogue of their own 128 rows
 // ---------------------------------------------------------------------------
-constexpr int STAGES2 = 6;
+// k-blocks (of BK) per pipeline stage, and stages in the ring
+#ifndef KL_GEMM_KPS
+#define KL_GEMM_KPS 1
+#endif
+#ifndef KL_GEMM_PAIR_STAGES
+#define KL_GEMM_PAIR_STAGES (6 / KL_GEMM_KPS)
+#endif
+constexpr int KPS = KL_GEMM_KPS;
+constexpr int STAGES2 = KL_GEMM_PAIR_STAGES;
+// A and B tiles are issued by two producer threads in different warps (warp 0
+// and warp 6): one thread issuing every tensor copy of a stage serialises them.
+#ifndef KL_GEMM_SPLIT_PRODUCER
+#define KL_GEMM_SPLIT_PRODUCER 1
+#endif
+constexpr bool SPLIT_PRODUCER = KL_GEMM_SPLIT_PRODUCER != 0;
+constexpr int PAIR_THREADS = SPLIT_PRODUCER ? 224 : 192;
 constexpr uint32_t HALF_BYTES = 128 * BK * 2;            // 16 KB
-constexpr uint32_t STAGE2_BYTES = 2 * HALF_BYTES;        // A half + B half
+constexpr uint32_t KB2_BYTES = 2 * HALF_BYTES;           // one k-block: A half + B half
+constexpr uint32_t STAGE2_BYTES = KPS * KB2_BYTES;
 constexpr size_t SMEM2_BYTES = 1024 + STAGES2 * STAGE2_BYTES + 512;
+static_assert(SMEM2_BYTES <= 232448, "pair-kernel shared memory above the per-CTA limit");
 
 __device__ __forceinline__ uint32_t mapa_rank(uint32_t addr, uint32_t rank) {
   uint32_t r;
@@ -480,7 +505,7 @@ __device__ __forceinline__ bool mbar_try_wait_cl(uint32_t bar, uint32_t parity) 
       : "memory");
   return ok != 0;
 }
-// Bounded wait with cluster-scope acquire (arrivals may come from the peer CTA).
+// Bounded wait with cluster-scope acquire (arrivals may come from other CTAs).
 __device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, uint32_t* err) {
   if (mbar_try_wait_cl(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
@@ -498,12 +523,24 @@ __device__ __forceinline__ bool mbar_wait_cl_warp(uint32_t bar, uint32_t parity,
   const bool ok = !*abort_flag && mbar_wait_cl(bar, parity, err);
   return __all_sync(0xffffffffu, ok);
 }
+// Tile load into this CTA's shared memory, completing on the pair leader's barrier.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, int32_t x, int32_t y,
                                                  uint32_t leader_bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(tmap), "r"(x), "r"(y), "r"(leader_bar)
+      : "memory");
+}
+// The same tile into the same offset of every CTA in `mask`; each destination's
+// bytes complete on the barrier at `leader_bar`'s offset in that destination's
+// pair leader.
+__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void* tmap, int32_t x, int32_t y,
+                                                    uint32_t leader_bar, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      ".cta_group::2 [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(leader_bar), "h"(mask)
       : "memory");
 }
 __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
@@ -515,18 +552,20 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, 
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// Arrive on `bar` (same offset) in both CTAs when this thread's MMAs complete.
-__device__ __forceinline__ void umma_commit_pair(uint32_t bar) {
+// Arrive on `bar` (same offset) in every CTA of `mask` when this thread's MMAs complete.
+__device__ __forceinline__ void umma_commit_pair(uint32_t bar, uint16_t mask) {
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(static_cast<uint16_t>(3))
+      "h"(mask)
       : "memory");
 }
 __device__ __forceinline__ void umma_commit_pair_local(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ Unit decode_unit2(const GemmParams& P, int u) {
+// Unit decode for cluster tiles of (256*NP) x 256.
+template <int NP>
+__device__ __forceinline__ Unit decode_unit_cl(const GemmParams& P, int u) {
   int p = 0;
   while (p + 1 < P.nprob && u >= P.prob[p + 1].unit_begin) ++p;
   const GemmProb& pr = P.prob[p];
@@ -537,9 +576,9 @@ __device__ __forceinline__ Unit decode_unit2(const GemmParams& P, int u) {
   r.p = p;
   if (pr.n_fast) {
     r.n0 = (tile % pr.n_tiles) * 256;
-    r.m0 = (tile / pr.n_tiles) * 256;
+    r.m0 = (tile / pr.n_tiles) * (256 * NP);
   } else {
-    r.m0 = (tile % pr.m_tiles) * 256;
+    r.m0 = (tile % pr.m_tiles) * (256 * NP);
     r.n0 = (tile / pr.m_tiles) * 256;
   }
   r.kb_lo = static_cast<int>(static_cast<int64_t>(si) * pr.kb_total / pr.splits);
@@ -547,8 +586,12 @@ __device__ __forceinline__ Unit decode_unit2(const GemmParams& P, int u) {
   return r;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
-    gemm_bf16_tc2_kernel(const __grid_constant__ GemmParams p) {
+template <int NP>
+__global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __grid_constant__ GemmParams p) {
+  constexpr int CL = 2 * NP;                                   // CTAs per cluster
+  // consumers of each unit id: epilogue warps, producers (all but the
+  // scheduler's own, plus the B producers), MMA issuers
+  constexpr int QEMPTY_COUNT = 4 * CL + (CL - 1) + (SPLIT_PRODUCER ? CL : 0) + NP;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -569,21 +612,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
-  const bool leader = rank == 0;
+  const uint32_t pair = rank >> 1, peer = rank & 1u;
+  const bool pair_leader = peer == 0;
+  const uint32_t lead = rank & ~1u;                            // this pair's leader rank
+  const uint16_t pair_mask = static_cast<uint16_t>(3u << (2 * pair));
+  const uint16_t all_mask = static_cast<uint16_t>((1u << CL) - 1u);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES2; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), NP);   // one MMA commit from every pair that reads or writes the stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 8);   // 4 epilogue warps in each CTA
+      mbar_init(tempty_bar(a), 8);   // 4 epilogue warps in each CTA of the pair
     }
     mbar_init(drain_bar, 1);
     for (int q = 0; q < SCHED_Q; ++q) {
       mbar_init(qfull_bar(q), 1);
-      mbar_init(qempty_bar(q), 10);  // leader MMA + 4 epilogue warps, follower TMA + 4 epilogue warps
+      mbar_init(qempty_bar(q), QEMPTY_COUNT);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -596,22 +643,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();   // both CTAs' barriers exist before either signals the other
+  cluster_sync_all();   // every CTA's barriers exist before any CTA signals another
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const uint32_t leader_qempty0 = mapa_rank(qempty_bar(0), 0);
-  const uint32_t leader_tempty0 = mapa_rank(tempty_bar(0), 0);
-  const uint32_t leader_full0 = mapa_rank(full_bar(0), 0);
+  const uint32_t sched_qempty0 = mapa_rank(qempty_bar(0), 0);
+  const uint32_t lead_tempty0 = mapa_rank(tempty_bar(0), lead);
+  const uint32_t lead_full0 = mapa_rank(full_bar(0), lead);
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- scheduler (leader) + TMA (both) ----------------
+  const bool b_producer = SPLIT_PRODUCER && warp == 6;
+  if ((warp == 0 || b_producer) && lane == 0) {
+    // ---------------- scheduler (rank 0) + TMA (every CTA) ----------------
+    // warp 0: scheduler on rank 0, A tiles (and B tiles unless split);
+    // warp 6: B tiles when split.
     for (int i = 0; i < p.nprob; ++i)
       for (int s = 0; s < p.prob[i].nseg; ++s) {
         tma_prefetch_desc(&p.tmA[p.prob[i].tmap_base + s]);
         tma_prefetch_desc(&p.tmB[p.prob[i].tmap_base + s]);
       }
-    const uint32_t follower_qfull0 = mapa_rank(qfull_bar(0), 1);
-    const uint32_t follower_qids0 = mapa_rank(smem_u32(const_cast<int*>(qids)), 1);
     int stage = 0;
     uint32_t phase = 0;
     int q = 0;
@@ -620,7 +668,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     bool ok = true;
     while (ok) {
       int u;
-      if (leader) {
+      if (rank == 0 && !b_producer) {
         u = static_cast<int>(atomicAdd(&p.sched[0], 1u));
         if (u >= p.total_units) u = -1;
         if (*abort_flag || !mbar_wait_cl(qempty_bar(q), qphase ^ 1u, p.err)) {
@@ -628,57 +676,77 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         qids[q] = u;
-        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(follower_qids0 + 4u * q), "r"(u) : "memory");
         mbar_arrive(qfull_bar(q));
-        mbar_arrive_cluster(follower_qfull0 + 8u * q);
+#pragma unroll
+        for (int r = 1; r < CL; ++r) {
+          const uint32_t rq = mapa_rank(smem_u32(const_cast<int*>(qids)), r) + 4u * q;
+          asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(rq), "r"(u) : "memory");
+          mbar_arrive_cluster(mapa_rank(qfull_bar(q), r));
+        }
       } else {
         if (*abort_flag || !mbar_wait_cl(qfull_bar(q), qphase, p.err)) {
           *abort_flag = 1;
           break;
         }
         u = qids[q];
-        mbar_arrive_cluster(leader_qempty0 + 8u * q);
+        mbar_arrive_cluster(sched_qempty0 + 8u * q);
       }
       if (++q == SCHED_Q) {
         q = 0;
         qphase ^= 1u;
       }
       if (u < 0) break;
-      const Unit un = decode_unit2(p, u);
+      const Unit un = decode_unit_cl<NP>(p, u);
       const GemmProb& pr = p.prob[un.p];
-      const int mh = un.m0 + 128 * static_cast<int>(rank);   // this CTA's rows of A
-      const int nh = un.n0 + 128 * static_cast<int>(rank);   // this CTA's rows of B
+      const int mh = un.m0 + 256 * static_cast<int>(pair) + 128 * static_cast<int>(peer);   // this CTA's rows of A
+      const int nh = un.n0 + 128 * static_cast<int>(peer);                                   // this CTA's rows of B
       int s = 0, off = 0;
       while (un.kb_lo >= off + pr.kb[s]) off += pr.kb[s++];
       int kl = un.kb_lo - off;
-      for (int kbg = un.kb_lo; kbg < un.kb_hi; ++kbg, ++kl) {
-        if (kl == pr.kb[s]) {
-          ++s;
-          kl = 0;
-        }
-        const CUtensorMap* ta = &p.tmA[pr.tmap_base + s];
-        const CUtensorMap* tb = &p.tmB[pr.tmap_base + s];
-        if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u, p.err)) {
+      for (int kbg = un.kb_lo; kbg < un.kb_hi; kbg += KPS) {
+        const int nk = un.kb_hi - kbg < KPS ? un.kb_hi - kbg : KPS;
+        if (*abort_flag || !mbar_wait_cl(empty_bar(stage), phase ^ 1u, p.err)) {
           ok = false;
           *abort_flag = 1;
           break;
         }
-        const uint32_t fb = leader_full0 + 8u * stage;
-        if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * STAGE2_BYTES);
-        const uint32_t sa = sbase + stage * STAGE2_BYTES;
-        const uint32_t sb = sa + HALF_BYTES;
-        const int k0 = kl * BK;
-        if (!pr.a_mn) {
-          tma_load_2d_pair(sa, ta, k0, mh, fb);
-        } else {
-          tma_load_2d_pair(sa, ta, mh, k0, fb);
-          tma_load_2d_pair(sa + 8192, ta, mh + 64, k0, fb);
-        }
-        if (!pr.b_mn) {
-          tma_load_2d_pair(sb, tb, k0, nh, fb);
-        } else {
-          tma_load_2d_pair(sb, tb, nh, k0, fb);
-          tma_load_2d_pair(sb + 8192, tb, nh + 64, k0, fb);
+        const uint32_t fb = lead_full0 + 8u * stage;
+        if (pair_leader && !b_producer)
+          mbar_arrive_expect_tx(full_bar(stage), static_cast<uint32_t>(nk) * 2 * KB2_BYTES);
+        for (int j = 0; j < nk; ++j, ++kl) {
+          if (kl == pr.kb[s]) {
+            ++s;
+            kl = 0;
+          }
+          const CUtensorMap* ta = &p.tmA[pr.tmap_base + s];
+          const CUtensorMap* tb = &p.tmB[pr.tmap_base + s];
+          const uint32_t sa = sbase + stage * STAGE2_BYTES + j * KB2_BYTES;
+          const uint32_t sb = sa + HALF_BYTES;
+          const int k0 = kl * BK;
+          if (!b_producer) {
+            if (!pr.a_mn) {
+              tma_load_2d_pair(sa, ta, k0, mh, fb);
+            } else {
+              tma_load_2d_pair(sa, ta, mh, k0, fb);
+              tma_load_2d_pair(sa + 8192, ta, mh + 64, k0, fb);
+            }
+          }
+          if (SPLIT_PRODUCER && !b_producer) {
+            // B is issued by warp 6
+          } else if (NP == 1) {
+            if (!pr.b_mn) {
+              tma_load_2d_pair(sb, tb, k0, nh, fb);
+            } else {
+              tma_load_2d_pair(sb, tb, nh, k0, fb);
+              tma_load_2d_pair(sb + 8192, tb, nh + 64, k0, fb);
+            }
+          } else {
+            // piece `pair` of this CTA's B half, to this CTA and its counterpart in the other pair
+            const uint16_t mc = static_cast<uint16_t>((1u << rank) | (1u << (rank ^ 2u)));
+            const int nrow = nh + 64 * static_cast<int>(pair);
+            if (!pr.b_mn) tma_load_2d_pair_mc(sb + 8192u * pair, tb, k0, nrow, fb, mc);
+            else tma_load_2d_pair_mc(sb + 8192u * pair, tb, nrow, k0, fb, mc);
+          }
         }
         ++issued;
         if (++stage == STAGES2) {
@@ -687,8 +755,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         }
       }
     }
-    if (leader) {
-      // the leader's full barriers see both CTAs' copies: wait for the last ones
+    if (pair_leader && !b_producer) {
+      // the leader's full barriers see every copy into its pair: wait for the last ones
       const long outstanding = issued < STAGES2 ? issued : STAGES2;
       for (long i = 0; i < outstanding; ++i) {
         if (stage == 0) {
@@ -697,11 +765,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         } else {
           --stage;
         }
-        mbar_wait(full_bar(stage), phase, p.err);
+        mbar_wait_cl(full_bar(stage), phase, p.err);
       }
     }
-  } else if (warp == 1 && lane == 0 && leader) {
-    // ---------------- MMA issuer (leader) ----------------
+  } else if (warp == 1 && lane == 0 && pair_leader) {
+    // ---------------- MMA issuer (pair leaders) ----------------
     int stage = 0;
     uint32_t phase = 0;
     int q = 0;
@@ -709,18 +777,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     int it = 0;
     bool ok = true;
     while (ok) {
-      if (*abort_flag || !mbar_wait(qfull_bar(q), qphase, p.err)) {
+      if (*abort_flag || !mbar_wait_cl(qfull_bar(q), qphase, p.err)) {
         *abort_flag = 1;
         break;
       }
       const int u = qids[q];
-      mbar_arrive(qempty_bar(q));
+      mbar_arrive_cluster(sched_qempty0 + 8u * q);
       if (++q == SCHED_Q) {
         q = 0;
         qphase ^= 1u;
       }
       if (u < 0) break;
-      const Unit un = decode_unit2(p, u);
+      const Unit un = decode_unit_cl<NP>(p, u);
       const GemmProb& pr = p.prob[un.p];
       const int acc = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
@@ -732,37 +800,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 256);
       const uint32_t idesc = idesc_bf16_f32(256, 256, pr.a_mn, pr.b_mn);
       uint32_t accumulate = 0;
-      for (int kbg = un.kb_lo; kbg < un.kb_hi; ++kbg) {
-        if (*abort_flag || !mbar_wait(full_bar(stage), phase, p.err)) {
+      for (int kbg = un.kb_lo; kbg < un.kb_hi; kbg += KPS) {
+        const int nk = un.kb_hi - kbg < KPS ? un.kb_hi - kbg : KPS;
+        if (*abort_flag || !mbar_wait_cl(full_bar(stage), phase, p.err)) {
           ok = false;
           *abort_flag = 1;
           break;
         }
         tc_fence_after();
-        const uint32_t sa = sbase + stage * STAGE2_BYTES;
-        const uint32_t sb = sa + HALF_BYTES;
+        for (int j = 0; j < nk; ++j) {
+          const uint32_t sa = sbase + stage * STAGE2_BYTES + j * KB2_BYTES;
+          const uint32_t sb = sa + HALF_BYTES;
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
-          const uint64_t ad = pr.a_mn ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
-                                      : smem_desc_sw128(sa + k * 32, 16, 1024);
-          const uint64_t bd = pr.b_mn ? smem_desc_sw128(sb + k * 2048, 8192, 1024)
-                                      : smem_desc_sw128(sb + k * 32, 16, 1024);
-          umma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
-          accumulate = 1;
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = pr.a_mn ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
+                                        : smem_desc_sw128(sa + k * 32, 16, 1024);
+            const uint64_t bd = pr.b_mn ? smem_desc_sw128(sb + k * 2048, 8192, 1024)
+                                        : smem_desc_sw128(sb + k * 32, 16, 1024);
+            umma_bf16_pair(d_tmem, ad, bd, idesc, accumulate);
+            accumulate = 1;
+          }
         }
-        umma_commit_pair(empty_bar(stage));
+        umma_commit_pair(empty_bar(stage), all_mask);
         if (++stage == STAGES2) {
           stage = 0;
           phase ^= 1u;
         }
       }
-      if (ok) umma_commit_pair(tfull_bar(acc));
+      if (ok) umma_commit_pair(tfull_bar(acc), pair_mask);
       ++it;
     }
     umma_commit_pair_local(drain_bar);
     mbar_wait(drain_bar, 0, p.err);
-  } else if (warp >= 2) {
-    // ---------------- epilogue (both CTAs, own 128 rows) ----------------
+  } else if (warp >= 2 && warp <= 5) {
+    // ---------------- epilogue (every CTA, its own 128 rows) ----------------
     const int quarter = warp & 3;
     int q = 0;
     uint32_t qphase = 0;
@@ -774,16 +845,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       }
       const int u = qids[q];
       __syncwarp();
-      if (lane == 0) {
-        if (leader) mbar_arrive(qempty_bar(q));
-        else mbar_arrive_cluster(leader_qempty0 + 8u * q);
-      }
+      if (lane == 0) mbar_arrive_cluster(sched_qempty0 + 8u * q);
       if (++q == SCHED_Q) {
         q = 0;
         qphase ^= 1u;
       }
       if (u < 0) break;
-      const Unit un = decode_unit2(p, u);
+      const Unit un = decode_unit_cl<NP>(p, u);
       const GemmProb& pr = p.prob[un.p];
       const int acc = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
@@ -792,7 +860,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const int row = un.m0 + 128 * static_cast<int>(rank) + quarter * 32 + lane;
+      const int row = un.m0 + 256 * static_cast<int>(pair) + 128 * static_cast<int>(peer) + quarter * 32 + lane;
       for (int c = 0; c < 256 / 32; ++c) {
         const int col0 = un.n0 + c * 32;
         if (col0 >= pr.N) break;
@@ -804,23 +872,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(leader_tempty0 + 8u * acc);
+      if (lane == 0) mbar_arrive_cluster(lead_tempty0 + 8u * acc);
       ++it;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();   // neither CTA leaves while the other may still signal it
+  cluster_sync_all();   // no CTA leaves while another may still signal it
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(TMEM_COLS) : "memory");
   }
-  if (threadIdx.x == 0 && leader) {
+  if (threadIdx.x == 0 && rank == 0) {
     __threadfence();
     const unsigned prev = atomicAdd(&p.sched[1], 1u);
-    if (prev == gridDim.x / 2 - 1) {
+    if (prev == gridDim.x / CL - 1) {
       atomicExch(&p.sched[0], 0u);
       atomicExch(&p.sched[1], 0u);
       __threadfence();
@@ -951,10 +1019,17 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(int M, int N, int nseg, G
 // be accumulated in fp32 (fp32 output without addend, or a caller-provided
 // fp32 accumulator) are cut along K into units of at most ~UNIT_KB k-blocks,
 // so that no unit is long against a CTA's share of the launch.
-// Tile shape: pairs of CTAs (cta_group::2) on 256 x 256 tiles, or single CTAs
-// on 128 x 256 tiles.
+// Tile shape: pairs of CTAs (cta_group::2) on 256 x 256 tiles, clustered
+// GEMM_NP pairs deep along M with B multicast between the pairs; or single
+// CTAs on 128 x 256 tiles.
+#ifndef KL_GEMM_PAIRS_PER_CLUSTER
+#define KL_GEMM_PAIRS_PER_CLUSTER 1
+#endif
+constexpr int GEMM_NP = KL_GEMM_PAIRS_PER_CLUSTER;
+static_assert(GEMM_NP == 1 || GEMM_NP == 2, "pairs per cluster: 1 or 2");
+constexpr int GEMM_CL = 2 * GEMM_NP;
 constexpr bool USE_PAIR = true;
-constexpr int TILE_M = USE_PAIR ? 256 : BM;
+constexpr int TILE_M = USE_PAIR ? 256 * GEMM_NP : BM;
 constexpr int SPLIT_MIN_KB = 256;
 constexpr int UNIT_KB = 256;
 
@@ -974,6 +1049,22 @@ unsigned int* sched_slot_ptr() {
     base[dev] = static_cast<unsigned int*>(ptr);
   }
   return base[dev] + 2 * (seq.fetch_add(1) % SCHED_SLOTS);
+}
+
+// Clusters of the pair kernel that fit on the device at once (queried once per
+// device; the persistent grid is sized to it).
+int max_gemm_clusters(int dev, const cudaLaunchConfig_t& cfg_in) {
+  static int cached[64] = {};
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  cudaLaunchConfig_t cfg = cfg_in;
+  cfg.gridDim = dim3(GEMM_CL * (num_sms() / GEMM_CL));
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tcp_kernel<GEMM_NP>, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = num_sms() / GEMM_CL;
+  }
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
 }
 
 kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const char* label) {
@@ -1026,7 +1117,8 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
       // A: 128-row boxes in both forms; B: each CTA of a pair stages 128 rows
       if (!s.a_mn) KL_TRY(make_map(&p.tmA[tm + g], s.A[g], s.K[g], s.M, s.lda[g], BM));
       else KL_TRY(make_map(&p.tmA[tm + g], s.A[g], s.M, s.K[g], s.lda[g], 64));
-      if (!s.b_mn) KL_TRY(make_map(&p.tmB[tm + g], s.B[g], s.K[g], s.N, s.ldb[g], USE_PAIR ? 128 : BN));
+      if (!s.b_mn)
+        KL_TRY(make_map(&p.tmB[tm + g], s.B[g], s.K[g], s.N, s.ldb[g], USE_PAIR ? (GEMM_NP == 2 ? 64 : 128) : BN));
       else KL_TRY(make_map(&p.tmB[tm + g], s.B[g], s.N, s.K[g], s.ldb[g], 64));
       pr.kb[g] = (s.K[g] + BK - 1) / BK;
       pr.kb_total += pr.kb[g];
@@ -1080,15 +1172,28 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
   if (dev < 64 && !(attr_done >> dev & 1u)) {
     KL_CUDA(cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(SMEM_BYTES)));
-    KL_CUDA(cudaFuncSetAttribute(gemm_bf16_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    KL_CUDA(cudaFuncSetAttribute(gemm_bf16_tcp_kernel<GEMM_NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(SMEM2_BYTES)));
     attr_done |= uint64_t(1) << dev;
   }
   {
     ProfScope ps(label, st, flops, bytes);
     if (USE_PAIR) {
-      const int pairs = units < num_sms() / 2 ? units : num_sms() / 2;
-      gemm_bf16_tc2_kernel<<<2 * pairs, NUM_THREADS, SMEM2_BYTES, st>>>(p);
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = GEMM_CL;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.blockDim = dim3(PAIR_THREADS);
+      cfg.dynamicSmemBytes = SMEM2_BYTES;
+      cfg.stream = st;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      const int cap = max_gemm_clusters(dev, cfg);
+      const int clusters = units < cap ? units : cap;
+      cfg.gridDim = dim3(GEMM_CL * clusters);
+      KL_CUDA(cudaLaunchKernelEx(&cfg, gemm_bf16_tcp_kernel<GEMM_NP>, p));
     } else {
       const int grid = units < num_sms() ? units : num_sms();
       gemm_bf16_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(p);

@@ -12,6 +12,13 @@ Cases (T = 2048 tokens, hidden 5120, 64/8 heads of 128, intermediate 25600):
   attn_fwd      causal GQA attention forward, S = 2048
   attn_bwd      its backward
   ce            CE + argmax + dlogits on 4096 x 151936 fp32 logits
+  rmsnorm_fwd   RMSNorm forward, 2048 x 5120
+  rmsnorm_bwd   RMSNorm backward with fp32 dh and a residual gradient, 2048 x 5120
+  rope          in-place rotation of q [2048, 64, 128]
+  swiglu_fwd    m = silu(g) u over 2048 x 25600
+  swiglu_bwd    dg, du over 2048 x 25600
+  layer         one whole layer forward + backward (for the layer-internal
+                kernels; ~4 GB on the device)
 """
 from __future__ import annotations
 
@@ -88,6 +95,53 @@ def main():
         def run():
             K.kl_ce_argmax(N, V, z.data_ptr(), tgt.data_ptr(), loss.data_ptr(), arg.data_ptr(), dz.data_ptr(), bf,
                            ws.data_ptr(), ws.numel())
+    elif a.case in ("rmsnorm_fwd", "rmsnorm_bwd"):
+        x, gamma = _rand((T, H)), 1.0 + _rand((H,), 0.02)
+        h = torch.empty_like(x)
+        rstd = torch.empty(T, dtype=torch.float32, device="cuda")
+        K.kl_rmsnorm_fwd(T, H, bf, x.data_ptr(), gamma.data_ptr(), 1e-6, h.data_ptr(), rstd.data_ptr())
+        dh = torch.randn(T, H, device="cuda")
+        resid = _rand((T, H))
+        dx = torch.empty_like(x)
+        dgamma = torch.empty(H, dtype=torch.float32, device="cuda")
+        ws = torch.empty(K.kl_rmsnorm_bwd_ws_bytes(T, H), dtype=torch.uint8, device="cuda")
+
+        def run():
+            if a.case == "rmsnorm_fwd":
+                K.kl_rmsnorm_fwd(T, H, bf, x.data_ptr(), gamma.data_ptr(), 1e-6, h.data_ptr(), rstd.data_ptr())
+            else:
+                K.kl_rmsnorm_bwd(T, H, bf, dh.data_ptr(), K.KL_F32, x.data_ptr(), gamma.data_ptr(), rstd.data_ptr(),
+                                 resid.data_ptr(), dx.data_ptr(), dgamma.data_ptr(), ws.data_ptr(), ws.numel())
+    elif a.case == "rope":
+        q = _rand((T, HQ * D))
+
+        def run():
+            K.kl_rope(1, T, HQ, D, 1e6, bf, q.data_ptr(), 1)
+    elif a.case in ("swiglu_fwd", "swiglu_bwd"):
+        g, u, dm = _rand((T, I)), _rand((T, I)), _rand((T, I))
+        m, dg, du = torch.empty_like(g), torch.empty_like(g), torch.empty_like(g)
+
+        def run():
+            if a.case == "swiglu_fwd":
+                K.kl_swiglu_fwd(T * I, bf, g.data_ptr(), u.data_ptr(), m.data_ptr())
+            else:
+                K.kl_swiglu_bwd(T * I, bf, dm.data_ptr(), g.data_ptr(), u.data_ptr(), dg.data_ptr(), du.data_ptr())
+    elif a.case == "layer":
+        from . import layer as L
+        cfg = L.make_cfg(1, T, H, HQ, HKV, D, I, dtype=bf)
+        w = {n: (1.0 + _rand(shp, 0.02)) if n.startswith("gamma") else _rand(shp, 0.02)
+             for n, shp in L.weight_shapes(cfg).items()}
+        wst = L.weights_struct(w)
+        X, dY = _rand((T, H)), _rand((T, H))
+        Y, dX = torch.empty_like(X), torch.empty_like(X)
+        buf = L.LayerBuffers(cfg, "cuda")
+        grads, gst = L.alloc_grads(cfg, "cuda", bf)
+
+        def run():
+            K.kl_layer_forward(cfg, wst, X.data_ptr(), Y.data_ptr(), buf.saved, buf.fwd_ws.data_ptr(),
+                               buf.fwd_ws.numel())
+            K.kl_layer_backward(cfg, wst, buf.saved, dY.data_ptr(), dX.data_ptr(), gst, buf.bwd_ws.data_ptr(),
+                                buf.bwd_ws.numel())
     else:
         raise SystemExit(f"unknown case {a.case}")
     for _ in range(a.iters):
