@@ -30,17 +30,10 @@
 namespace kl {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;
-constexpr int STAGES = 4;
-constexpr uint32_t A_BYTES = BM * BK * 2;
-constexpr uint32_t B_BYTES = BN * BK * 2;
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr uint32_t TMEM_COLS = 2 * BN;
-constexpr int NUM_THREADS = 192;
+constexpr int BN = 256;                    // output tile columns
+constexpr int BK = 64;                     // k-block: one 128-byte swizzle atom of bf16
+constexpr uint32_t TMEM_COLS = 2 * BN;     // two fp32 accumulators
 constexpr int SCHED_Q = 8;                 // depth of the unit-id ring
-constexpr size_t SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 512;
 
 struct GemmProb {
   int M, N;
@@ -49,6 +42,7 @@ struct GemmProb {
   int kb_total;
   int splits;             // work units per output tile (K split)
   int a_mn, b_mn;
+  int a3d, b3d;           // MN-major operand staged by one 3-D copy (both 64-wide atoms)
   int m_tiles, n_tiles;
   int n_fast;             // tile order: n fastest (1) or m fastest (0)
   int unit_begin;         // first global work-unit index of this problem
@@ -79,27 +73,6 @@ struct Unit {
   int m0, n0;
   int kb_lo, kb_hi;
 };
-
-__device__ __forceinline__ Unit decode_unit(const GemmParams& P, int u) {
-  int p = 0;
-  while (p + 1 < P.nprob && u >= P.prob[p + 1].unit_begin) ++p;
-  const GemmProb& pr = P.prob[p];
-  const int local = u - pr.unit_begin;
-  const int si = local % pr.splits;
-  const int tile = local / pr.splits;
-  Unit r;
-  r.p = p;
-  if (pr.n_fast) {
-    r.n0 = (tile % pr.n_tiles) * BN;
-    r.m0 = (tile / pr.n_tiles) * BM;
-  } else {
-    r.m0 = (tile % pr.m_tiles) * BM;
-    r.n0 = (tile / pr.m_tiles) * BN;
-  }
-  r.kb_lo = static_cast<int>(static_cast<int64_t>(si) * pr.kb_total / pr.splits);
-  r.kb_hi = static_cast<int>(static_cast<int64_t>(si + 1) * pr.kb_total / pr.splits);
-  return r;
-}
 
 __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
@@ -177,264 +150,6 @@ __device__ __forceinline__ void store_chunk(const GemmProb& pr, int row, int col
     }
   }
 }
-
-__global__ void __launch_bounds__(NUM_THREADS, 1)
-    gemm_bf16_tc_kernel(const __grid_constant__ GemmParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t sbase = smem_u32(smem);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  const uint32_t bar0 = smem_u32(bars);
-  auto full_bar = [&](int s) { return bar0 + 8u * s; };
-  auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
-  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + a); };
-  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * STAGES + 2 + a); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-  auto qfull_bar = [&](int q) { return bar0 + 8u * (2 * STAGES + 5 + q); };
-  auto qempty_bar = [&](int q) { return bar0 + 8u * (2 * STAGES + 5 + SCHED_Q + q); };
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5 + 2 * SCHED_Q);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  volatile int* qids = reinterpret_cast<volatile int*>(tmem_holder + 2);   // [SCHED_Q] unit ids
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4);
-    }
-    mbar_init(drain_bar, 1);
-    for (int q = 0; q < SCHED_Q; ++q) {
-      mbar_init(qfull_bar(q), 1);
-      mbar_init(qempty_bar(q), 5);   // the MMA thread and the 4 epilogue warps
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_holder), TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_holder;
-
-  if (warp == 0 && lane == 0) {
-    // ---------------- scheduler + TMA producer ----------------
-    // Takes the next unit from the launch-wide counter, publishes its id to the
-    // MMA thread and the epilogue warps through a small shared ring, then loads
-    // every k-block of the unit. Id -1 ends the stream.
-    for (int i = 0; i < p.nprob; ++i)
-      for (int s = 0; s < p.prob[i].nseg; ++s) {
-        tma_prefetch_desc(&p.tmA[p.prob[i].tmap_base + s]);
-        tma_prefetch_desc(&p.tmB[p.prob[i].tmap_base + s]);
-      }
-    int stage = 0;
-    uint32_t phase = 0;
-    int q = 0;
-    uint32_t qphase = 0;
-    long issued = 0;
-    bool ok = true;
-    while (ok) {
-      int u = static_cast<int>(atomicAdd(&p.sched[0], 1u));
-      if (u >= p.total_units) u = -1;
-      if (*abort_flag || !mbar_wait(qempty_bar(q), qphase ^ 1u, p.err)) {
-        *abort_flag = 1;
-        break;
-      }
-      qids[q] = u;
-      mbar_arrive(qfull_bar(q));
-      if (++q == SCHED_Q) {
-        q = 0;
-        qphase ^= 1u;
-      }
-      if (u < 0) break;
-      const Unit un = decode_unit(p, u);
-      const GemmProb& pr = p.prob[un.p];
-      int s = 0, off = 0;
-      while (un.kb_lo >= off + pr.kb[s]) off += pr.kb[s++];
-      int kl = un.kb_lo - off;
-      for (int kbg = un.kb_lo; kbg < un.kb_hi; ++kbg, ++kl) {
-        if (kl == pr.kb[s]) {
-          ++s;
-          kl = 0;
-        }
-        const CUtensorMap* ta = &p.tmA[pr.tmap_base + s];
-        const CUtensorMap* tb = &p.tmB[pr.tmap_base + s];
-        if (*abort_flag || !mbar_wait(empty_bar(stage), phase ^ 1u, p.err)) {
-          ok = false;
-          *abort_flag = 1;
-          break;
-        }
-        const uint32_t fb = full_bar(stage);
-        mbar_arrive_expect_tx(fb, STAGE_BYTES);
-        const uint32_t sa = sbase + stage * STAGE_BYTES;
-        const uint32_t sb = sa + A_BYTES;
-        const int k0 = kl * BK;
-        if (!pr.a_mn) {
-          tma_load_2d(sa, ta, k0, un.m0, fb);
-        } else {
-          tma_load_2d(sa, ta, un.m0, k0, fb);
-          tma_load_2d(sa + 8192, ta, un.m0 + 64, k0, fb);
-        }
-        if (!pr.b_mn) {
-          tma_load_2d(sb, tb, k0, un.n0, fb);
-        } else {
-#pragma unroll
-          for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + 8192 * j, tb, un.n0 + 64 * j, k0, fb);
-        }
-        ++issued;
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-    }
-    // Wait (bounded) for the copies still in flight before the CTA can exit.
-    const long outstanding = issued < STAGES ? issued : STAGES;
-    for (long i = 0; i < outstanding; ++i) {
-      if (stage == 0) {
-        stage = STAGES - 1;
-        phase ^= 1u;
-      } else {
-        --stage;
-      }
-      mbar_wait(full_bar(stage), phase, p.err);
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer: one accumulation per unit ----------------
-    int stage = 0;
-    uint32_t phase = 0;
-    int q = 0;
-    uint32_t qphase = 0;
-    int it = 0;
-    bool ok = true;
-    while (ok) {
-      if (*abort_flag || !mbar_wait(qfull_bar(q), qphase, p.err)) {
-        *abort_flag = 1;
-        break;
-      }
-      const int u = qids[q];
-      mbar_arrive(qempty_bar(q));
-      if (++q == SCHED_Q) {
-        q = 0;
-        qphase ^= 1u;
-      }
-      if (u < 0) break;
-      const Unit un = decode_unit(p, u);
-      const GemmProb& pr = p.prob[un.p];
-      const int acc = it & 1;
-      const uint32_t use = static_cast<uint32_t>(it >> 1);
-      if (*abort_flag || !mbar_wait(tempty_bar(acc), (use & 1u) ^ 1u, p.err)) {
-        *abort_flag = 1;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-      const uint32_t idesc = idesc_bf16_f32(BM, BN, pr.a_mn, pr.b_mn);
-      uint32_t accumulate = 0;
-      for (int kbg = un.kb_lo; kbg < un.kb_hi; ++kbg) {
-        if (*abort_flag || !mbar_wait(full_bar(stage), phase, p.err)) {
-          ok = false;
-          *abort_flag = 1;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t sa = sbase + stage * STAGE_BYTES;
-        const uint32_t sb = sa + A_BYTES;
-#pragma unroll
-        for (int k = 0; k < BK / 16; ++k) {
-          const uint64_t ad = pr.a_mn ? smem_desc_sw128(sa + k * 2048, 8192, 1024)
-                                      : smem_desc_sw128(sa + k * 32, 16, 1024);
-          const uint64_t bd = pr.b_mn ? smem_desc_sw128(sb + k * 2048, 8192, 1024)
-                                      : smem_desc_sw128(sb + k * 32, 16, 1024);
-          umma_bf16(d_tmem, ad, bd, idesc, accumulate);
-          accumulate = 1;
-        }
-        umma_commit(empty_bar(stage));
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-      if (ok) umma_commit(tfull_bar(acc));
-      ++it;
-    }
-    // Every MMA issued must finish before TMEM is released.
-    umma_commit(drain_bar);
-    mbar_wait(drain_bar, 0, p.err);
-  } else if (warp >= 2) {
-    // ---------------- epilogue: one per unit ----------------
-    const int quarter = warp & 3;
-    int q = 0;
-    uint32_t qphase = 0;
-    int it = 0;
-    while (true) {
-      if (!mbar_wait_warp(qfull_bar(q), qphase, p.err, abort_flag)) {
-        *abort_flag = 1;
-        break;
-      }
-      const int u = qids[q];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(qempty_bar(q));
-      if (++q == SCHED_Q) {
-        q = 0;
-        qphase ^= 1u;
-      }
-      if (u < 0) break;
-      const Unit un = decode_unit(p, u);
-      const GemmProb& pr = p.prob[un.p];
-      const int acc = it & 1;
-      const uint32_t use = static_cast<uint32_t>(it >> 1);
-      if (!mbar_wait_warp(tfull_bar(acc), use & 1u, p.err, abort_flag)) {
-        *abort_flag = 1;
-        break;
-      }
-      tc_fence_after();
-      const int row = un.m0 + quarter * 32 + lane;
-      for (int c = 0; c < BN / 32; ++c) {
-        const int col0 = un.n0 + c * 32;
-        if (col0 >= pr.N) break;
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(
-            tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN + c * 32),
-            v);
-        tmem_ld_wait();
-        if (row < pr.M) store_chunk(pr, row, col0, v);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar(acc));
-      ++it;
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
-  }
-  if (threadIdx.x == 0) {
-    // The last CTA to finish re-arms the launch's scheduler counters.
-    __threadfence();
-    const unsigned prev = atomicAdd(&p.sched[1], 1u);
-    if (prev == gridDim.x - 1) {
-      atomicExch(&p.sched[0], 0u);
-      atomicExch(&p.sched[1], 0u);
-      __threadfence();
-    }
-  }
-}
-
 
 // ---------------------------------------------------------------------------
 // Pair form (cta_group::2): a CTA pair computes 256 x 256 tiles, and a cluster
@@ -523,6 +238,16 @@ __device__ __forceinline__ bool mbar_wait_cl_warp(uint32_t bar, uint32_t parity,
   const bool ok = !*abort_flag && mbar_wait_cl(bar, parity, err);
   return __all_sync(0xffffffffu, ok);
 }
+// One lane of a converged warp (the lowest), chosen by elect.sync. The issuing
+// roles run as whole warps so that descriptors, coordinates and barrier
+// addresses are warp-uniform values; only the elected lane issues.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
 // Tile load into this CTA's shared memory, completing on the pair leader's barrier.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, int32_t x, int32_t y,
                                                  uint32_t leader_bar) {
@@ -530,6 +255,16 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(tmap), "r"(x), "r"(y), "r"(leader_bar)
+      : "memory");
+}
+// Both 64-wide atoms of an MN-major half in one copy: 3-D map [MN/64][K][64],
+// box {64, 64, 2}, lands exactly as two 2-D {64, 64} copies 8 KB apart.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                                 uint32_t leader_bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(leader_bar)
       : "memory");
 }
 // The same tile into the same offset of every CTA in `mask`; each destination's
@@ -651,15 +386,17 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
   const uint32_t lead_full0 = mapa_rank(full_bar(0), lead);
 
   const bool b_producer = SPLIT_PRODUCER && warp == 6;
-  if ((warp == 0 || b_producer) && lane == 0) {
+  if (warp == 0 || b_producer) {
+    const bool el = elect_one();
     // ---------------- scheduler (rank 0) + TMA (every CTA) ----------------
     // warp 0: scheduler on rank 0, A tiles (and B tiles unless split);
     // warp 6: B tiles when split.
-    for (int i = 0; i < p.nprob; ++i)
-      for (int s = 0; s < p.prob[i].nseg; ++s) {
-        tma_prefetch_desc(&p.tmA[p.prob[i].tmap_base + s]);
-        tma_prefetch_desc(&p.tmB[p.prob[i].tmap_base + s]);
-      }
+    if (el)
+      for (int i = 0; i < p.nprob; ++i)
+        for (int s = 0; s < p.prob[i].nseg; ++s) {
+          tma_prefetch_desc(&p.tmA[p.prob[i].tmap_base + s]);
+          tma_prefetch_desc(&p.tmB[p.prob[i].tmap_base + s]);
+        }
     int stage = 0;
     uint32_t phase = 0;
     int q = 0;
@@ -667,29 +404,36 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
     long issued = 0;
     bool ok = true;
     while (ok) {
-      int u;
+      int u = 0;
       if (rank == 0 && !b_producer) {
-        u = static_cast<int>(atomicAdd(&p.sched[0], 1u));
-        if (u >= p.total_units) u = -1;
-        if (*abort_flag || !mbar_wait_cl(qempty_bar(q), qphase ^ 1u, p.err)) {
+        if (el) {
+          u = static_cast<int>(atomicAdd(&p.sched[0], 1u));
+          if (u >= p.total_units) u = -1;
+        }
+        u = __shfl_sync(0xffffffffu, u, 0);
+        if (!mbar_wait_cl_warp(qempty_bar(q), qphase ^ 1u, p.err, abort_flag)) {
           *abort_flag = 1;
           break;
         }
-        qids[q] = u;
-        mbar_arrive(qfull_bar(q));
+        if (el) {
+          qids[q] = u;
+          mbar_arrive(qfull_bar(q));
 #pragma unroll
-        for (int r = 1; r < CL; ++r) {
-          const uint32_t rq = mapa_rank(smem_u32(const_cast<int*>(qids)), r) + 4u * q;
-          asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(rq), "r"(u) : "memory");
-          mbar_arrive_cluster(mapa_rank(qfull_bar(q), r));
+          for (int r = 1; r < CL; ++r) {
+            const uint32_t rq = mapa_rank(smem_u32(const_cast<int*>(qids)), r) + 4u * q;
+            asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(rq), "r"(u) : "memory");
+            mbar_arrive_cluster(mapa_rank(qfull_bar(q), r));
+          }
         }
+        __syncwarp();
       } else {
-        if (*abort_flag || !mbar_wait_cl(qfull_bar(q), qphase, p.err)) {
+        if (!mbar_wait_cl_warp(qfull_bar(q), qphase, p.err, abort_flag)) {
           *abort_flag = 1;
           break;
         }
         u = qids[q];
-        mbar_arrive_cluster(sched_qempty0 + 8u * q);
+        __syncwarp();
+        if (el) mbar_arrive_cluster(sched_qempty0 + 8u * q);
       }
       if (++q == SCHED_Q) {
         q = 0;
@@ -705,13 +449,13 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
       int kl = un.kb_lo - off;
       for (int kbg = un.kb_lo; kbg < un.kb_hi; kbg += KPS) {
         const int nk = un.kb_hi - kbg < KPS ? un.kb_hi - kbg : KPS;
-        if (*abort_flag || !mbar_wait_cl(empty_bar(stage), phase ^ 1u, p.err)) {
+        if (!mbar_wait_cl_warp(empty_bar(stage), phase ^ 1u, p.err, abort_flag)) {
           ok = false;
           *abort_flag = 1;
           break;
         }
         const uint32_t fb = lead_full0 + 8u * stage;
-        if (pair_leader && !b_producer)
+        if (pair_leader && !b_producer && el)
           mbar_arrive_expect_tx(full_bar(stage), static_cast<uint32_t>(nk) * 2 * KB2_BYTES);
         for (int j = 0; j < nk; ++j, ++kl) {
           if (kl == pr.kb[s]) {
@@ -723,19 +467,25 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
           const uint32_t sa = sbase + stage * STAGE2_BYTES + j * KB2_BYTES;
           const uint32_t sb = sa + HALF_BYTES;
           const int k0 = kl * BK;
-          if (!b_producer) {
+          if (!el) {
+            // only the elected lane issues
+          } else if (!b_producer) {
             if (!pr.a_mn) {
               tma_load_2d_pair(sa, ta, k0, mh, fb);
+            } else if (pr.a3d) {
+              tma_load_3d_pair(sa, ta, 0, k0, mh >> 6, fb);
             } else {
               tma_load_2d_pair(sa, ta, mh, k0, fb);
               tma_load_2d_pair(sa + 8192, ta, mh + 64, k0, fb);
             }
           }
-          if (SPLIT_PRODUCER && !b_producer) {
-            // B is issued by warp 6
+          if (!el || (SPLIT_PRODUCER && !b_producer)) {
+            // B is issued by warp 6 (by its elected lane)
           } else if (NP == 1) {
             if (!pr.b_mn) {
               tma_load_2d_pair(sb, tb, k0, nh, fb);
+            } else if (pr.b3d) {
+              tma_load_3d_pair(sb, tb, 0, k0, nh >> 6, fb);
             } else {
               tma_load_2d_pair(sb, tb, nh, k0, fb);
               tma_load_2d_pair(sb + 8192, tb, nh + 64, k0, fb);
@@ -768,8 +518,9 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
         mbar_wait_cl(full_bar(stage), phase, p.err);
       }
     }
-  } else if (warp == 1 && lane == 0 && pair_leader) {
-    // ---------------- MMA issuer (pair leaders) ----------------
+  } else if (warp == 1 && pair_leader) {
+    // ---------------- MMA issuer (pair leaders; one elected lane issues) ----------------
+    const bool el = elect_one();
     int stage = 0;
     uint32_t phase = 0;
     int q = 0;
@@ -777,12 +528,13 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
     int it = 0;
     bool ok = true;
     while (ok) {
-      if (*abort_flag || !mbar_wait_cl(qfull_bar(q), qphase, p.err)) {
+      if (!mbar_wait_cl_warp(qfull_bar(q), qphase, p.err, abort_flag)) {
         *abort_flag = 1;
         break;
       }
       const int u = qids[q];
-      mbar_arrive_cluster(sched_qempty0 + 8u * q);
+      __syncwarp();
+      if (el) mbar_arrive_cluster(sched_qempty0 + 8u * q);
       if (++q == SCHED_Q) {
         q = 0;
         qphase ^= 1u;
@@ -792,7 +544,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
       const GemmProb& pr = p.prob[un.p];
       const int acc = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
-      if (*abort_flag || !mbar_wait_cl(tempty_bar(acc), (use & 1u) ^ 1u, p.err)) {
+      if (!mbar_wait_cl_warp(tempty_bar(acc), (use & 1u) ^ 1u, p.err, abort_flag)) {
         *abort_flag = 1;
         break;
       }
@@ -802,12 +554,13 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
       uint32_t accumulate = 0;
       for (int kbg = un.kb_lo; kbg < un.kb_hi; kbg += KPS) {
         const int nk = un.kb_hi - kbg < KPS ? un.kb_hi - kbg : KPS;
-        if (*abort_flag || !mbar_wait_cl(full_bar(stage), phase, p.err)) {
+        if (!mbar_wait_cl_warp(full_bar(stage), phase, p.err, abort_flag)) {
           ok = false;
           *abort_flag = 1;
           break;
         }
         tc_fence_after();
+        if (el) {
         for (int j = 0; j < nk; ++j) {
           const uint32_t sa = sbase + stage * STAGE2_BYTES + j * KB2_BYTES;
           const uint32_t sb = sa + HALF_BYTES;
@@ -822,15 +575,19 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
           }
         }
         umma_commit_pair(empty_bar(stage), all_mask);
+        }
+        __syncwarp();
         if (++stage == STAGES2) {
           stage = 0;
           phase ^= 1u;
         }
       }
-      if (ok) umma_commit_pair(tfull_bar(acc), pair_mask);
+      if (ok && el) umma_commit_pair(tfull_bar(acc), pair_mask);
+      __syncwarp();
       ++it;
     }
-    umma_commit_pair_local(drain_bar);
+    if (el) umma_commit_pair_local(drain_bar);
+    __syncwarp();
     mbar_wait(drain_bar, 0, p.err);
   } else if (warp >= 2 && warp <= 5) {
     // ---------------- epilogue (every CTA, its own 128 rows) ----------------
@@ -949,6 +706,22 @@ kl_status make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t out
   return KL_OK;
 }
 
+// MN-major bf16 operand as a 3-D map: dims {64, K, MN/64} with strides
+// {ld, 64} elements, box {64, 64, 2}, 128-byte swizzle. Needs MN % 64 == 0
+// (every element addressed lies inside the MN x K operand); returns false if
+// the encoder refuses the map (the caller then uses 2-D maps).
+bool make_map_mn3(CUtensorMap* m, const void* ptr, uint64_t mn, uint64_t k, int64_t ld) {
+  auto fn = encode_fn();
+  if (!fn || mn % 64 != 0) return false;
+  cuuint64_t dims[3] = {64, k, mn / 64};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, 128};
+  cuuint32_t box[3] = {64, 64, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // ---------------------------------------------------------------------------
@@ -1028,8 +801,7 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(int M, int N, int nseg, G
 constexpr int GEMM_NP = KL_GEMM_PAIRS_PER_CLUSTER;
 static_assert(GEMM_NP == 1 || GEMM_NP == 2, "pairs per cluster: 1 or 2");
 constexpr int GEMM_CL = 2 * GEMM_NP;
-constexpr bool USE_PAIR = true;
-constexpr int TILE_M = USE_PAIR ? 256 * GEMM_NP : BM;
+constexpr int TILE_M = 256 * GEMM_NP;
 constexpr int SPLIT_MIN_KB = 256;
 constexpr int UNIT_KB = 256;
 
@@ -1115,14 +887,27 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
         return set_error(KL_ERR_INVALID_ARG,
                          "gemm: bf16 operands need 16-byte aligned bases and row strides that are multiples of 8");
       // A: 128-row boxes in both forms; B: each CTA of a pair stages 128 rows
-      if (!s.a_mn) KL_TRY(make_map(&p.tmA[tm + g], s.A[g], s.K[g], s.M, s.lda[g], BM));
+      if (!s.a_mn) KL_TRY(make_map(&p.tmA[tm + g], s.A[g], s.K[g], s.M, s.lda[g], 128));
       else KL_TRY(make_map(&p.tmA[tm + g], s.A[g], s.M, s.K[g], s.lda[g], 64));
       if (!s.b_mn)
-        KL_TRY(make_map(&p.tmB[tm + g], s.B[g], s.K[g], s.N, s.ldb[g], USE_PAIR ? (GEMM_NP == 2 ? 64 : 128) : BN));
+        KL_TRY(make_map(&p.tmB[tm + g], s.B[g], s.K[g], s.N, s.ldb[g], GEMM_NP == 2 ? 64 : 128));
       else KL_TRY(make_map(&p.tmB[tm + g], s.B[g], s.N, s.K[g], s.ldb[g], 64));
       pr.kb[g] = (s.K[g] + BK - 1) / BK;
       pr.kb_total += pr.kb[g];
       ksum += s.K[g];
+    }
+    // MN-major operands: one 3-D copy per half instead of two 2-D copies
+    {
+      CUtensorMap a3[GEMM_MAX_SEG], b3[GEMM_MAX_SEG];
+      bool ok_a = s.a_mn != 0, ok_b = s.b_mn != 0 && GEMM_NP == 1;
+      for (int g = 0; g < s.nseg; ++g) {
+        if (ok_a) ok_a = make_map_mn3(&a3[g], s.A[g], s.M, s.K[g], s.lda[g]);
+        if (ok_b) ok_b = make_map_mn3(&b3[g], s.B[g], s.N, s.K[g], s.ldb[g]);
+      }
+      for (int g = 0; ok_a && g < s.nseg; ++g) p.tmA[tm + g] = a3[g];
+      for (int g = 0; ok_b && g < s.nseg; ++g) p.tmB[tm + g] = b3[g];
+      pr.a3d = ok_a;
+      pr.b3d = ok_b;
     }
     tm += s.nseg;
     pr.m_tiles = (s.M + TILE_M - 1) / TILE_M;
@@ -1170,15 +955,13 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
   int dev = 0;
   KL_CUDA(cudaGetDevice(&dev));
   if (dev < 64 && !(attr_done >> dev & 1u)) {
-    KL_CUDA(cudaFuncSetAttribute(gemm_bf16_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(SMEM_BYTES)));
     KL_CUDA(cudaFuncSetAttribute(gemm_bf16_tcp_kernel<GEMM_NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(SMEM2_BYTES)));
     attr_done |= uint64_t(1) << dev;
   }
   {
     ProfScope ps(label, st, flops, bytes);
-    if (USE_PAIR) {
+    {
       cudaLaunchConfig_t cfg = {};
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1194,9 +977,6 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
       const int clusters = units < cap ? units : cap;
       cfg.gridDim = dim3(GEMM_CL * clusters);
       KL_CUDA(cudaLaunchKernelEx(&cfg, gemm_bf16_tcp_kernel<GEMM_NP>, p));
-    } else {
-      const int grid = units < num_sms() ? units : num_sms();
-      gemm_bf16_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(p);
     }
   }
   KL_CUDA(cudaGetLastError());
