@@ -128,70 +128,88 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- TMA ----------------
-    tma_prefetch_desc(&p.tmQ);
-    tma_prefetch_desc(&p.tmK);
-    tma_prefetch_desc(&p.tmV);
-    mbar_arrive_expect_tx(q_full, TILE_BYTES);
-    tma_load_2d(sb + OFF_Q, &p.tmQ, h * HD, row0 + q0, q_full);
-    tma_load_2d(sb + OFF_Q + 16384, &p.tmQ, h * HD + 64, row0 + q0, q_full);
+  if (warp == 0) {
+    // ---------------- TMA (whole warp; the elected lane issues) ----------------
+    const bool el = elect_one();
+    if (el) {
+      tma_prefetch_desc(&p.tmQ);
+      tma_prefetch_desc(&p.tmK);
+      tma_prefetch_desc(&p.tmV);
+      mbar_arrive_expect_tx(q_full, TILE_BYTES);
+      tma_load_2d(sb + OFF_Q, &p.tmQ, h * HD, row0 + q0, q_full);
+      tma_load_2d(sb + OFF_Q + 16384, &p.tmQ, h * HD + 64, row0 + q0, q_full);
+    }
+    __syncwarp();
     int issued_k = 0, issued_v = 0;
     for (int j = 0; j < nkb; ++j) {
       const int s = j & 1;
       const uint32_t ph = (j >> 1) & 1;
-      if (*abort_flag || !mbar_wait(k_empty(s), ph ^ 1u, p.err)) { *abort_flag = 1; break; }
-      mbar_arrive_expect_tx(k_full(s), TILE_BYTES);
-      tma_load_2d(sb + OFF_K + s * TILE_BYTES, &p.tmK, j_kv * HD, row0 + j * BKV, k_full(s));
-      tma_load_2d(sb + OFF_K + s * TILE_BYTES + 16384, &p.tmK, j_kv * HD + 64, row0 + j * BKV, k_full(s));
+      if (!mbar_wait_warp(k_empty(s), ph ^ 1u, p.err, abort_flag)) { *abort_flag = 1; break; }
+      if (el) {
+        mbar_arrive_expect_tx(k_full(s), TILE_BYTES);
+        tma_load_2d(sb + OFF_K + s * TILE_BYTES, &p.tmK, j_kv * HD, row0 + j * BKV, k_full(s));
+        tma_load_2d(sb + OFF_K + s * TILE_BYTES + 16384, &p.tmK, j_kv * HD + 64, row0 + j * BKV, k_full(s));
+      }
+      __syncwarp();
       ++issued_k;
-      if (*abort_flag || !mbar_wait(v_empty(s), ph ^ 1u, p.err)) { *abort_flag = 1; break; }
-      mbar_arrive_expect_tx(v_full(s), TILE_BYTES);
-      tma_load_2d(sb + OFF_V + s * TILE_BYTES, &p.tmV, j_kv * HD, row0 + j * BKV, v_full(s));
-      tma_load_2d(sb + OFF_V + s * TILE_BYTES + 16384, &p.tmV, j_kv * HD + 64, row0 + j * BKV, v_full(s));
+      if (!mbar_wait_warp(v_empty(s), ph ^ 1u, p.err, abort_flag)) { *abort_flag = 1; break; }
+      if (el) {
+        mbar_arrive_expect_tx(v_full(s), TILE_BYTES);
+        tma_load_2d(sb + OFF_V + s * TILE_BYTES, &p.tmV, j_kv * HD, row0 + j * BKV, v_full(s));
+        tma_load_2d(sb + OFF_V + s * TILE_BYTES + 16384, &p.tmV, j_kv * HD + 64, row0 + j * BKV, v_full(s));
+      }
+      __syncwarp();
       ++issued_v;
     }
     // copies still in flight must land before exit
     mbar_wait(q_full, 0, p.err);
     for (int j = (issued_k > 2 ? issued_k - 2 : 0); j < issued_k; ++j) mbar_wait(k_full(j & 1), (j >> 1) & 1, p.err);
     for (int j = (issued_v > 2 ? issued_v - 2 : 0); j < issued_v; ++j) mbar_wait(v_full(j & 1), (j >> 1) & 1, p.err);
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA ----------------
+  } else if (warp == 1) {
+    // ---------------- MMA (whole warp; the elected lane issues) ----------------
+    const bool el = elect_one();
     const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
     const uint32_t idesc_pv = idesc_bf16_f32(128, 128, 0, 1);
-    bool ok = mbar_wait(q_full, 0, p.err);
+    bool ok = mbar_wait_warp(q_full, 0, p.err, abort_flag);
     auto issue_pv = [&](int j) -> bool {
       const int s = j & 1;
       const uint32_t ph = (j >> 1) & 1;
-      if (!mbar_wait(p_full, j & 1, p.err)) return false;
-      if (!mbar_wait(v_full(s), ph, p.err)) return false;
+      if (!mbar_wait_warp(p_full, j & 1, p.err, abort_flag)) return false;
+      if (!mbar_wait_warp(v_full(s), ph, p.err, abort_flag)) return false;
       tc_fence_after();
-      for (int kk = 0; kk < BKV / 16; ++kk)
-        umma_bf16(tmem + 256, desc_kmajor(sb + OFF_P, kk), desc_mnmajor(sb + OFF_V + s * TILE_BYTES, kk),
-                  idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-      umma_commit(v_empty(s));
-      umma_commit(p_free);
+      if (el) {
+        for (int kk = 0; kk < BKV / 16; ++kk)
+          umma_bf16(tmem + 256, desc_kmajor(sb + OFF_P, kk), desc_mnmajor(sb + OFF_V + s * TILE_BYTES, kk),
+                    idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(v_empty(s));
+        umma_commit(p_free);
+      }
+      __syncwarp();
       return true;
     };
     for (int j = 0; ok && j < nkb; ++j) {
       const int s = j & 1;
       const uint32_t ph = (j >> 1) & 1;
-      if (*abort_flag || !mbar_wait(k_full(s), ph, p.err) ||
-          (j >= 2 && !mbar_wait(s_free(s), ph ^ 1u, p.err))) {
+      if (!mbar_wait_warp(k_full(s), ph, p.err, abort_flag) ||
+          (j >= 2 && !mbar_wait_warp(s_free(s), ph ^ 1u, p.err, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t d = tmem + s * 128;
-      for (int kk = 0; kk < HD / 16; ++kk)
-        umma_bf16(d, desc_kmajor(sb + OFF_Q, kk), desc_kmajor(sb + OFF_K + s * TILE_BYTES, kk), idesc_s, kk > 0);
-      umma_commit(k_empty(s));
-      umma_commit(s_full(s));
+      if (el) {
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16(d, desc_kmajor(sb + OFF_Q, kk), desc_kmajor(sb + OFF_K + s * TILE_BYTES, kk), idesc_s, kk > 0);
+        umma_commit(k_empty(s));
+        umma_commit(s_full(s));
+      }
+      __syncwarp();
       if (j >= 1 && !issue_pv(j - 1)) ok = false;
     }
     if (ok && !issue_pv(nkb - 1)) ok = false;
     if (!ok) *abort_flag = 1;
-    umma_commit(drain);
+    if (el) umma_commit(drain);
+    __syncwarp();
     mbar_wait(drain, 0, p.err);
   } else if (warp >= 2) {
     // ---------------- softmax / correction / epilogue ----------------
@@ -383,7 +401,8 @@ constexpr uint32_t KV_OFF_DO = KV_OFF_Q + 2 * T64;           // 2 stages of T64
 constexpr uint32_t PT_BYTES = 128 * 64 * 2;                   // 16 KB: 128 key rows x 64 queries
 constexpr uint32_t KV_OFF_P = KV_OFF_DO + 2 * T64;           // 2 buffers of P^T
 constexpr uint32_t KV_OFF_DS = KV_OFF_P + 2 * PT_BYTES;      // 2 buffers of dS^T
-constexpr uint32_t KV_OFF_BAR = KV_OFF_DS + 2 * PT_BYTES;
+constexpr uint32_t KV_OFF_STAT = KV_OFF_DS + 2 * PT_BYTES;  // 2 stages: lse[64], D[64] (fp32)
+constexpr uint32_t KV_OFF_BAR = KV_OFF_STAT + 2 * 512;
 constexpr size_t KV_SMEM = 1024 + KV_OFF_BAR + 256;
 
 __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid_constant__ BwdParams p) {
@@ -410,6 +429,9 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid
   const int k0 = kb * BKV;
   const int row0 = b * p.S;
   const int nit = (p.S - k0 + 63) / 64;      // 64-query tiles from the diagonal to the end
+  // lse / D rows staged in shared memory by bulk copies when they are 16-byte aligned
+  const bool stat_smem = (p.S & 3) == 0 && (reinterpret_cast<uintptr_t>(p.lse) & 15u) == 0 &&
+                         (reinterpret_cast<uintptr_t>(p.Dd) & 15u) == 0;
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
@@ -434,67 +456,92 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- TMA ----------------
-    mbar_arrive_expect_tx(kv_full, 2 * TILE_BYTES);
-    tma_load_2d(sb + KV_OFF_K, &p.tmK, jh * HD, row0 + k0, kv_full);
-    tma_load_2d(sb + KV_OFF_K + 16384, &p.tmK, jh * HD + 64, row0 + k0, kv_full);
-    tma_load_2d(sb + KV_OFF_V, &p.tmV, jh * HD, row0 + k0, kv_full);
-    tma_load_2d(sb + KV_OFF_V + 16384, &p.tmV, jh * HD + 64, row0 + k0, kv_full);
+  if (warp == 0) {
+    // ---------------- TMA (whole warp; the elected lane issues) ----------------
+    const bool el = elect_one();
+    if (el) {
+      mbar_arrive_expect_tx(kv_full, 2 * TILE_BYTES);
+      tma_load_2d(sb + KV_OFF_K, &p.tmK, jh * HD, row0 + k0, kv_full);
+      tma_load_2d(sb + KV_OFF_K + 16384, &p.tmK, jh * HD + 64, row0 + k0, kv_full);
+      tma_load_2d(sb + KV_OFF_V, &p.tmV, jh * HD, row0 + k0, kv_full);
+      tma_load_2d(sb + KV_OFF_V + 16384, &p.tmV, jh * HD + 64, row0 + k0, kv_full);
+    }
+    __syncwarp();
     int issued = 0;
     for (int it = 0; it < nit; ++it) {
       const int s = it & 1;
       const uint32_t ph = (it >> 1) & 1;
-      if (*abort_flag || !mbar_wait(q_free(s), ph ^ 1u, p.err)) { *abort_flag = 1; break; }
+      if (!mbar_wait_warp(q_free(s), ph ^ 1u, p.err, abort_flag)) { *abort_flag = 1; break; }
       const int qr = row0 + k0 + it * 64;
-      mbar_arrive_expect_tx(q_full(s), 2 * T64);
-      tma_load_2d(sb + KV_OFF_Q + s * T64, &p.tmQ, h * HD, qr, q_full(s));
-      tma_load_2d(sb + KV_OFF_Q + s * T64 + 8192, &p.tmQ, h * HD + 64, qr, q_full(s));
-      tma_load_2d(sb + KV_OFF_DO + s * T64, &p.tmdO, h * HD, qr, q_full(s));
-      tma_load_2d(sb + KV_OFF_DO + s * T64 + 8192, &p.tmdO, h * HD + 64, qr, q_full(s));
+      if (el) {
+        // lse and D of the tile's queries (those inside the sequence) ride with Q and dO
+        const int nq = p.S - (k0 + it * 64) < 64 ? p.S - (k0 + it * 64) : 64;
+        const uint32_t stat_bytes = stat_smem ? static_cast<uint32_t>(nq) * 4u : 0u;
+        mbar_arrive_expect_tx(q_full(s), 2 * T64 + 2 * stat_bytes);
+        if (stat_smem) {
+          const int64_t so = (static_cast<int64_t>(b) * p.Hq + h) * p.S + k0 + it * 64;
+          bulk_copy_g2s(sb + KV_OFF_STAT + s * 512, p.lse + so, stat_bytes, q_full(s));
+          bulk_copy_g2s(sb + KV_OFF_STAT + s * 512 + 256, p.Dd + so, stat_bytes, q_full(s));
+        }
+        tma_load_2d(sb + KV_OFF_Q + s * T64, &p.tmQ, h * HD, qr, q_full(s));
+        tma_load_2d(sb + KV_OFF_Q + s * T64 + 8192, &p.tmQ, h * HD + 64, qr, q_full(s));
+        tma_load_2d(sb + KV_OFF_DO + s * T64, &p.tmdO, h * HD, qr, q_full(s));
+        tma_load_2d(sb + KV_OFF_DO + s * T64 + 8192, &p.tmdO, h * HD + 64, qr, q_full(s));
+      }
+      __syncwarp();
       ++issued;
     }
     mbar_wait(kv_full, 0, p.err);
     for (int it = (issued > 2 ? issued - 2 : 0); it < issued; ++it) mbar_wait(q_full(it & 1), (it >> 1) & 1, p.err);
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA ----------------
+  } else if (warp == 1) {
+    // ---------------- MMA (whole warp; the elected lane issues) ----------------
+    const bool el = elect_one();
     const uint32_t id_st = idesc_bf16_f32(128, 64, 0, 0);
     const uint32_t id_gr = idesc_bf16_f32(128, 128, 0, 1);
-    bool ok = mbar_wait(kv_full, 0, p.err);
+    bool ok = mbar_wait_warp(kv_full, 0, p.err, abort_flag);
     auto issue_grad = [&](int it) -> bool {
       const int s = it & 1;
-      if (!mbar_wait(p_full(s), (it >> 1) & 1, p.err)) return false;
+      if (!mbar_wait_warp(p_full(s), (it >> 1) & 1, p.err, abort_flag)) return false;
       tc_fence_after();
       const uint32_t sq = sb + KV_OFF_Q + s * T64, sdo = sb + KV_OFF_DO + s * T64;
-      for (int kk = 0; kk < 4; ++kk)
-        umma_bf16(tmem + 256, desc_k64(sb + KV_OFF_P + s * PT_BYTES, kk), desc_mn128(sdo, 8192, kk), id_gr,
-                  (it > 0 || kk > 0) ? 1u : 0u);
-      for (int kk = 0; kk < 4; ++kk)
-        umma_bf16(tmem + 384, desc_k64(sb + KV_OFF_DS + s * PT_BYTES, kk), desc_mn128(sq, 8192, kk), id_gr,
-                  (it > 0 || kk > 0) ? 1u : 0u);
-      umma_commit(q_free(s));
-      umma_commit(p_free(s));
+      if (el) {
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16(tmem + 256, desc_k64(sb + KV_OFF_P + s * PT_BYTES, kk), desc_mn128(sdo, 8192, kk), id_gr,
+                    (it > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16(tmem + 384, desc_k64(sb + KV_OFF_DS + s * PT_BYTES, kk), desc_mn128(sq, 8192, kk), id_gr,
+                    (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(q_free(s));
+        umma_commit(p_free(s));
+      }
+      __syncwarp();
       return true;
     };
     for (int it = 0; ok && it < nit; ++it) {
       const int s = it & 1;
       const uint32_t ph = (it >> 1) & 1;
-      if (*abort_flag || !mbar_wait(q_full(s), ph, p.err) || (it >= 2 && !mbar_wait(st_free(s), ph ^ 1u, p.err))) {
+      if (!mbar_wait_warp(q_full(s), ph, p.err, abort_flag) ||
+          (it >= 2 && !mbar_wait_warp(st_free(s), ph ^ 1u, p.err, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t sq = sb + KV_OFF_Q + s * T64, sdo = sb + KV_OFF_DO + s * T64;
-      for (int kk = 0; kk < HD / 16; ++kk)
-        umma_bf16(tmem + s * 64, desc_k128(sb + KV_OFF_K, 16384, kk), desc_k128(sq, 8192, kk), id_st, kk > 0);
-      for (int kk = 0; kk < HD / 16; ++kk)
-        umma_bf16(tmem + 128 + s * 64, desc_k128(sb + KV_OFF_V, 16384, kk), desc_k128(sdo, 8192, kk), id_st, kk > 0);
-      umma_commit(st_full(s));
+      if (el) {
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16(tmem + s * 64, desc_k128(sb + KV_OFF_K, 16384, kk), desc_k128(sq, 8192, kk), id_st, kk > 0);
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16(tmem + 128 + s * 64, desc_k128(sb + KV_OFF_V, 16384, kk), desc_k128(sdo, 8192, kk), id_st,
+                    kk > 0);
+        umma_commit(st_full(s));
+      }
+      __syncwarp();
       if (it >= 1 && !issue_grad(it - 1)) ok = false;
     }
     if (ok && !issue_grad(nit - 1)) ok = false;
     if (!ok) *abort_flag = 1;
-    umma_commit(done);
+    if (el) umma_commit(done);
+    __syncwarp();
     mbar_wait(done, 0, p.err);
   } else if (warp >= 2) {
     // ---------------- P^T, dS^T (thread = key row) and the final dK/dV ----------------
@@ -525,12 +572,26 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid
       const int lim = key - q0;              // queries q0 + c with c >= lim see this key
       uint8_t* prow = smem + KV_OFF_P + s * PT_BYTES + r * 128;
       uint8_t* drw = smem + KV_OFF_DS + s * PT_BYTES + r * 128;
+      // the stage's lse / D copies completed with its Q / dO (q_full), before S^T
+      if (stat_smem && !mbar_wait_warp(q_full(s), ph, p.err, abort_flag)) { ok = false; break; }
+      const float* sl = reinterpret_cast<const float*>(smem + KV_OFF_STAT + s * 512);
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
         // lse (log2 units, +inf past the sequence end) and D of these 8 queries
         float l8[8], d8[8];
         const int qa = q0 + c8 * 8;
-        if (vec_stat && qa + 8 <= p.S) {
+        if (stat_smem && qa + 8 <= p.S) {
+          const float4 la = *reinterpret_cast<const float4*>(sl + c8 * 8);
+          const float4 lb = *reinterpret_cast<const float4*>(sl + c8 * 8 + 4);
+          const float4 da = *reinterpret_cast<const float4*>(sl + 64 + c8 * 8);
+          const float4 db = *reinterpret_cast<const float4*>(sl + 64 + c8 * 8 + 4);
+          l8[0] = la.x; l8[1] = la.y; l8[2] = la.z; l8[3] = la.w;
+          l8[4] = lb.x; l8[5] = lb.y; l8[6] = lb.z; l8[7] = lb.w;
+          d8[0] = da.x; d8[1] = da.y; d8[2] = da.z; d8[3] = da.w;
+          d8[4] = db.x; d8[5] = db.y; d8[6] = db.z; d8[7] = db.w;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) l8[e] *= LOG2E_F;
+        } else if (vec_stat && qa + 8 <= p.S) {
           const float4 la = *reinterpret_cast<const float4*>(lrow + qa);
           const float4 lb = *reinterpret_cast<const float4*>(lrow + qa + 4);
           const float4 da = *reinterpret_cast<const float4*>(drow + qa);
@@ -670,62 +731,80 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dq_tc_kernel(const __grid_c
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == 0 && lane == 0) {
-    mbar_arrive_expect_tx(q_full, 2 * TILE_BYTES);
-    tma_load_2d(sb + DQ_OFF_Q, &p.tmQ, h * HD, row0 + q0, q_full);
-    tma_load_2d(sb + DQ_OFF_Q + 16384, &p.tmQ, h * HD + 64, row0 + q0, q_full);
-    tma_load_2d(sb + DQ_OFF_DO, &p.tmdO, h * HD, row0 + q0, q_full);
-    tma_load_2d(sb + DQ_OFF_DO + 16384, &p.tmdO, h * HD + 64, row0 + q0, q_full);
+  if (warp == 0) {
+    // ---------------- TMA (whole warp; the elected lane issues) ----------------
+    const bool el = elect_one();
+    if (el) {
+      mbar_arrive_expect_tx(q_full, 2 * TILE_BYTES);
+      tma_load_2d(sb + DQ_OFF_Q, &p.tmQ, h * HD, row0 + q0, q_full);
+      tma_load_2d(sb + DQ_OFF_Q + 16384, &p.tmQ, h * HD + 64, row0 + q0, q_full);
+      tma_load_2d(sb + DQ_OFF_DO, &p.tmdO, h * HD, row0 + q0, q_full);
+      tma_load_2d(sb + DQ_OFF_DO + 16384, &p.tmdO, h * HD + 64, row0 + q0, q_full);
+    }
+    __syncwarp();
     int issued = 0;
     for (int j = 0; j < nkb; ++j) {
       const int s = j & 1;
       const uint32_t ph = (j >> 1) & 1;
-      if (*abort_flag || !mbar_wait(kv_free(s), ph ^ 1u, p.err)) { *abort_flag = 1; break; }
+      if (!mbar_wait_warp(kv_free(s), ph ^ 1u, p.err, abort_flag)) { *abort_flag = 1; break; }
       const int kr = row0 + j * 64;
-      mbar_arrive_expect_tx(kv_full(s), 2 * T64);
-      tma_load_2d(sb + DQ_OFF_K + s * T64, &p.tmK, jh * HD, kr, kv_full(s));
-      tma_load_2d(sb + DQ_OFF_K + s * T64 + 8192, &p.tmK, jh * HD + 64, kr, kv_full(s));
-      tma_load_2d(sb + DQ_OFF_V + s * T64, &p.tmV, jh * HD, kr, kv_full(s));
-      tma_load_2d(sb + DQ_OFF_V + s * T64 + 8192, &p.tmV, jh * HD + 64, kr, kv_full(s));
+      if (el) {
+        mbar_arrive_expect_tx(kv_full(s), 2 * T64);
+        tma_load_2d(sb + DQ_OFF_K + s * T64, &p.tmK, jh * HD, kr, kv_full(s));
+        tma_load_2d(sb + DQ_OFF_K + s * T64 + 8192, &p.tmK, jh * HD + 64, kr, kv_full(s));
+        tma_load_2d(sb + DQ_OFF_V + s * T64, &p.tmV, jh * HD, kr, kv_full(s));
+        tma_load_2d(sb + DQ_OFF_V + s * T64 + 8192, &p.tmV, jh * HD + 64, kr, kv_full(s));
+      }
+      __syncwarp();
       ++issued;
     }
     mbar_wait(q_full, 0, p.err);
     for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) mbar_wait(kv_full(j & 1), (j >> 1) & 1, p.err);
-  } else if (warp == 1 && lane == 0) {
+  } else if (warp == 1) {
+    // ---------------- MMA (whole warp; the elected lane issues) ----------------
+    const bool el = elect_one();
     const uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);
     const uint32_t id_q = idesc_bf16_f32(128, 128, 0, 1);
-    bool ok = mbar_wait(q_full, 0, p.err);
+    bool ok = mbar_wait_warp(q_full, 0, p.err, abort_flag);
     auto issue_dq = [&](int j) -> bool {
       const int s = j & 1;
-      if (!mbar_wait(ds_full(s), (j >> 1) & 1, p.err)) return false;
+      if (!mbar_wait_warp(ds_full(s), (j >> 1) & 1, p.err, abort_flag)) return false;
       tc_fence_after();
-      for (int kk = 0; kk < 4; ++kk)
-        umma_bf16(tmem + 256, desc_k64(sb + DQ_OFF_DS + s * 16384, kk), desc_mn128(sb + DQ_OFF_K + s * T64, 8192, kk),
-                  id_q, (j > 0 || kk > 0) ? 1u : 0u);
-      umma_commit(kv_free(s));
-      umma_commit(ds_free(s));
+      if (el) {
+        for (int kk = 0; kk < 4; ++kk)
+          umma_bf16(tmem + 256, desc_k64(sb + DQ_OFF_DS + s * 16384, kk),
+                    desc_mn128(sb + DQ_OFF_K + s * T64, 8192, kk), id_q, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(kv_free(s));
+        umma_commit(ds_free(s));
+      }
+      __syncwarp();
       return true;
     };
     for (int j = 0; ok && j < nkb; ++j) {
       const int s = j & 1;
       const uint32_t ph = (j >> 1) & 1;
-      if (*abort_flag || !mbar_wait(kv_full(s), ph, p.err) || (j >= 2 && !mbar_wait(sd_free(s), ph ^ 1u, p.err))) {
+      if (!mbar_wait_warp(kv_full(s), ph, p.err, abort_flag) ||
+          (j >= 2 && !mbar_wait_warp(sd_free(s), ph ^ 1u, p.err, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      for (int kk = 0; kk < HD / 16; ++kk)
-        umma_bf16(tmem + s * 64, desc_k128(sb + DQ_OFF_Q, 16384, kk), desc_k128(sb + DQ_OFF_K + s * T64, 8192, kk), id_s,
-                  kk > 0);
-      for (int kk = 0; kk < HD / 16; ++kk)
-        umma_bf16(tmem + 128 + s * 64, desc_k128(sb + DQ_OFF_DO, 16384, kk),
-                  desc_k128(sb + DQ_OFF_V + s * T64, 8192, kk), id_s, kk > 0);
-      umma_commit(sd_full(s));
+      if (el) {
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16(tmem + s * 64, desc_k128(sb + DQ_OFF_Q, 16384, kk), desc_k128(sb + DQ_OFF_K + s * T64, 8192, kk),
+                    id_s, kk > 0);
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_bf16(tmem + 128 + s * 64, desc_k128(sb + DQ_OFF_DO, 16384, kk),
+                    desc_k128(sb + DQ_OFF_V + s * T64, 8192, kk), id_s, kk > 0);
+        umma_commit(sd_full(s));
+      }
+      __syncwarp();
       if (j >= 1 && !issue_dq(j - 1)) ok = false;
     }
     if (ok && !issue_dq(nkb - 1)) ok = false;
     if (!ok) *abort_flag = 1;
-    umma_commit(done);
+    if (el) umma_commit(done);
+    __syncwarp();
     mbar_wait(done, 0, p.err);
   } else if (warp >= 2) {
     const int quarter = warp & 3;

@@ -28,16 +28,6 @@ constexpr int CLUSTER = 8;
 constexpr int THREADS = 512;
 constexpr int NWARP = THREADS / 32;
 
-// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
-// global memory into this CTA's shared memory, completing on mbarrier `bar`.
-__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
-                                              uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 struct Part {
   float m;
   float s;

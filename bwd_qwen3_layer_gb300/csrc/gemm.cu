@@ -238,16 +238,6 @@ __device__ __forceinline__ bool mbar_wait_cl_warp(uint32_t bar, uint32_t parity,
   const bool ok = !*abort_flag && mbar_wait_cl(bar, parity, err);
   return __all_sync(0xffffffffu, ok);
 }
-// One lane of a converged warp (the lowest), chosen by elect.sync. The issuing
-// roles run as whole warps so that descriptors, coordinates and barrier
-// addresses are warp-uniform values; only the elected lane issues.
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(pred));
-  return pred != 0;
-}
 // Tile load into this CTA's shared memory, completing on the pair leader's barrier.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap, int32_t x, int32_t y,
                                                  uint32_t leader_bar) {

@@ -124,9 +124,30 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, ui
   return __all_sync(0xffffffffu, ok);
 }
 
+// One lane of a converged warp (the lowest), chosen by elect.sync. Roles that
+// issue TMA copies or tcgen05 MMAs run as whole warps, so descriptors,
+// coordinates and barrier addresses are warp-uniform values; only the elected
+// lane issues.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
 // ----------------------------------------------------------------------------
 // TMA (tiled tensor copies global -> shared, completion on an mbarrier)
 // ----------------------------------------------------------------------------
+// Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
+// global memory into this CTA's shared memory, completing on mbarrier `bar`.
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int32_t x, int32_t y,
                                             uint32_t bar) {
   asm volatile(

@@ -87,6 +87,7 @@ ATT_CASES = [
     (1, 1, 64, 2, 2, 128),      # exactly one tile, MHA
     (1, 1, 1, 4, 1, 128),       # a single token: O = v0
     (1, 1, 1000, 16, 2, 128),   # longer, GQA 8:1
+    (1, 1, 331, 8, 1, 128),     # length not a multiple of 4: lse / D read from global memory
     (0, 1, 32, 4, 2, 16),       # tiny fp32 workload
     (0, 2, 19, 6, 3, 40),
 ]
