@@ -396,14 +396,16 @@ struct BwdParams {
 // ---------------------------------------------------------------------------
 constexpr uint32_t KV_OFF_K = 0;
 constexpr uint32_t KV_OFF_V = KV_OFF_K + TILE_BYTES;
-constexpr uint32_t KV_OFF_Q = KV_OFF_V + TILE_BYTES;         // 2 stages of T64
-constexpr uint32_t KV_OFF_DO = KV_OFF_Q + 2 * T64;           // 2 stages of T64
+constexpr int KV_QS = 3;                                      // stages of the Q / dO / lse / D ring
+constexpr uint32_t KV_OFF_Q = KV_OFF_V + TILE_BYTES;         // KV_QS stages of T64
+constexpr uint32_t KV_OFF_DO = KV_OFF_Q + KV_QS * T64;       // KV_QS stages of T64
 constexpr uint32_t PT_BYTES = 128 * 64 * 2;                   // 16 KB: 128 key rows x 64 queries
-constexpr uint32_t KV_OFF_P = KV_OFF_DO + 2 * T64;           // 2 buffers of P^T
+constexpr uint32_t KV_OFF_P = KV_OFF_DO + KV_QS * T64;       // 2 buffers of P^T
 constexpr uint32_t KV_OFF_DS = KV_OFF_P + 2 * PT_BYTES;      // 2 buffers of dS^T
-constexpr uint32_t KV_OFF_STAT = KV_OFF_DS + 2 * PT_BYTES;  // 2 stages: lse[64], D[64] (fp32)
-constexpr uint32_t KV_OFF_BAR = KV_OFF_STAT + 2 * 512;
+constexpr uint32_t KV_OFF_STAT = KV_OFF_DS + 2 * PT_BYTES;  // KV_QS stages: lse[64], D[64] (fp32)
+constexpr uint32_t KV_OFF_BAR = KV_OFF_STAT + KV_QS * 512;
 constexpr size_t KV_SMEM = 1024 + KV_OFF_BAR + 256;
+static_assert(KV_SMEM <= 232448, "dK/dV shared memory above the per-CTA limit");
 
 __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -412,15 +414,15 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid
   const uint32_t sb = smem_u32(smem);
   const uint32_t bar = sb + KV_OFF_BAR;
   const uint32_t kv_full = bar;
-  auto q_full = [&](int s) { return bar + 8 + 8 * s; };
-  auto q_free = [&](int s) { return bar + 24 + 8 * s; };
-  auto st_full = [&](int s) { return bar + 40 + 8 * s; };
-  auto st_free = [&](int s) { return bar + 56 + 8 * s; };
-  auto p_full = [&](int s) { return bar + 72 + 8 * s; };
-  auto p_free = [&](int s) { return bar + 88 + 8 * s; };
-  const uint32_t done = bar + 104;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + KV_OFF_BAR + 112);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + KV_OFF_BAR + 116);
+  auto q_full = [&](int s) { return bar + 8 + 8 * s; };              // KV_QS of each ring barrier
+  auto q_free = [&](int s) { return bar + 32 + 8 * s; };
+  auto st_full = [&](int s) { return bar + 56 + 8 * s; };             // 2 of each TMEM / P barrier
+  auto st_free = [&](int s) { return bar + 72 + 8 * s; };
+  auto p_full = [&](int s) { return bar + 88 + 8 * s; };
+  auto p_free = [&](int s) { return bar + 104 + 8 * s; };
+  const uint32_t done = bar + 120;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + KV_OFF_BAR + 128);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + KV_OFF_BAR + 132);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kb = blockIdx.y;                 // key tiles near the start see the most queries
@@ -435,9 +437,11 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < KV_QS; ++s) {
       mbar_init(q_full(s), 1);
       mbar_init(q_free(s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(st_full(s), 1);
       mbar_init(st_free(s), 4);
       mbar_init(p_full(s), 4);
@@ -469,8 +473,8 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid
     __syncwarp();
     int issued = 0;
     for (int it = 0; it < nit; ++it) {
-      const int s = it & 1;
-      const uint32_t ph = (it >> 1) & 1;
+      const int s = it % KV_QS;
+      const uint32_t ph = (it / KV_QS) & 1;
       if (!mbar_wait_warp(q_free(s), ph ^ 1u, p.err, abort_flag)) { *abort_flag = 1; break; }
       const int qr = row0 + k0 + it * 64;
       if (el) {
@@ -492,7 +496,8 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid
       ++issued;
     }
     mbar_wait(kv_full, 0, p.err);
-    for (int it = (issued > 2 ? issued - 2 : 0); it < issued; ++it) mbar_wait(q_full(it & 1), (it >> 1) & 1, p.err);
+    for (int it = (issued > KV_QS ? issued - KV_QS : 0); it < issued; ++it)
+      mbar_wait(q_full(it % KV_QS), (it / KV_QS) & 1, p.err);
   } else if (warp == 1) {
     // ---------------- MMA (whole warp; the elected lane issues) ----------------
     const bool el = elect_one();
@@ -500,10 +505,10 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid
     const uint32_t id_gr = idesc_bf16_f32(128, 128, 0, 1);
     bool ok = mbar_wait_warp(kv_full, 0, p.err, abort_flag);
     auto issue_grad = [&](int it) -> bool {
-      const int s = it & 1;
+      const int s = it & 1, qs = it % KV_QS;
       if (!mbar_wait_warp(p_full(s), (it >> 1) & 1, p.err, abort_flag)) return false;
       tc_fence_after();
-      const uint32_t sq = sb + KV_OFF_Q + s * T64, sdo = sb + KV_OFF_DO + s * T64;
+      const uint32_t sq = sb + KV_OFF_Q + qs * T64, sdo = sb + KV_OFF_DO + qs * T64;
       if (el) {
         for (int kk = 0; kk < 4; ++kk)
           umma_bf16(tmem + 256, desc_k64(sb + KV_OFF_P + s * PT_BYTES, kk), desc_mn128(sdo, 8192, kk), id_gr,
@@ -511,22 +516,22 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid
         for (int kk = 0; kk < 4; ++kk)
           umma_bf16(tmem + 384, desc_k64(sb + KV_OFF_DS + s * PT_BYTES, kk), desc_mn128(sq, 8192, kk), id_gr,
                     (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(q_free(s));
+        umma_commit(q_free(qs));
         umma_commit(p_free(s));
       }
       __syncwarp();
       return true;
     };
     for (int it = 0; ok && it < nit; ++it) {
-      const int s = it & 1;
+      const int s = it & 1, qs = it % KV_QS;
       const uint32_t ph = (it >> 1) & 1;
-      if (!mbar_wait_warp(q_full(s), ph, p.err, abort_flag) ||
+      if (!mbar_wait_warp(q_full(qs), (it / KV_QS) & 1, p.err, abort_flag) ||
           (it >= 2 && !mbar_wait_warp(st_free(s), ph ^ 1u, p.err, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t sq = sb + KV_OFF_Q + s * T64, sdo = sb + KV_OFF_DO + s * T64;
+      const uint32_t sq = sb + KV_OFF_Q + qs * T64, sdo = sb + KV_OFF_DO + qs * T64;
       if (el) {
         for (int kk = 0; kk < HD / 16; ++kk)
           umma_bf16(tmem + s * 64, desc_k128(sb + KV_OFF_K, 16384, kk), desc_k128(sq, 8192, kk), id_st, kk > 0);
@@ -573,8 +578,11 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid
       uint8_t* prow = smem + KV_OFF_P + s * PT_BYTES + r * 128;
       uint8_t* drw = smem + KV_OFF_DS + s * PT_BYTES + r * 128;
       // the stage's lse / D copies completed with its Q / dO (q_full), before S^T
-      if (stat_smem && !mbar_wait_warp(q_full(s), ph, p.err, abort_flag)) { ok = false; break; }
-      const float* sl = reinterpret_cast<const float*>(smem + KV_OFF_STAT + s * 512);
+      if (stat_smem && !mbar_wait_warp(q_full(it % KV_QS), (it / KV_QS) & 1, p.err, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const float* sl = reinterpret_cast<const float*>(smem + KV_OFF_STAT + (it % KV_QS) * 512);
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
         // lse (log2 units, +inf past the sequence end) and D of these 8 queries
@@ -676,11 +684,13 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid
 // ---------------------------------------------------------------------------
 constexpr uint32_t DQ_OFF_Q = 0;
 constexpr uint32_t DQ_OFF_DO = DQ_OFF_Q + TILE_BYTES;
-constexpr uint32_t DQ_OFF_K = DQ_OFF_DO + TILE_BYTES;       // 2 stages of T64
-constexpr uint32_t DQ_OFF_V = DQ_OFF_K + 2 * T64;           // 2 stages of T64
-constexpr uint32_t DQ_OFF_DS = DQ_OFF_V + 2 * T64;          // 2 buffers: 128 rows x 64 keys bf16 (16 KB)
+constexpr int DQ_KS = 4;                                     // stages of the K / V ring
+constexpr uint32_t DQ_OFF_K = DQ_OFF_DO + TILE_BYTES;       // DQ_KS stages of T64
+constexpr uint32_t DQ_OFF_V = DQ_OFF_K + DQ_KS * T64;       // DQ_KS stages of T64
+constexpr uint32_t DQ_OFF_DS = DQ_OFF_V + DQ_KS * T64;      // 2 buffers: 128 rows x 64 keys bf16 (16 KB)
 constexpr uint32_t DQ_OFF_BAR = DQ_OFF_DS + 2 * 16384;
 constexpr size_t DQ_SMEM = 1024 + DQ_OFF_BAR + 256;
+static_assert(DQ_SMEM <= 232448, "dQ shared memory above the per-CTA limit");
 
 __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dq_tc_kernel(const __grid_constant__ BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -689,15 +699,15 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dq_tc_kernel(const __grid_c
   const uint32_t sb = smem_u32(smem);
   const uint32_t bar = sb + DQ_OFF_BAR;
   const uint32_t q_full = bar;
-  auto kv_full = [&](int s) { return bar + 8 + 8 * s; };
-  auto kv_free = [&](int s) { return bar + 24 + 8 * s; };
-  auto sd_full = [&](int s) { return bar + 40 + 8 * s; };
-  auto sd_free = [&](int s) { return bar + 56 + 8 * s; };
-  auto ds_full = [&](int s) { return bar + 72 + 8 * s; };
-  auto ds_free = [&](int s) { return bar + 88 + 8 * s; };
-  const uint32_t done = bar + 104;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + DQ_OFF_BAR + 112);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + DQ_OFF_BAR + 116);
+  auto kv_full = [&](int s) { return bar + 8 + 8 * s; };             // DQ_KS of each ring barrier
+  auto kv_free = [&](int s) { return bar + 40 + 8 * s; };
+  auto sd_full = [&](int s) { return bar + 72 + 8 * s; };            // 2 of each TMEM / dS barrier
+  auto sd_free = [&](int s) { return bar + 88 + 8 * s; };
+  auto ds_full = [&](int s) { return bar + 104 + 8 * s; };
+  auto ds_free = [&](int s) { return bar + 120 + 8 * s; };
+  const uint32_t done = bar + 136;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + DQ_OFF_BAR + 144);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + DQ_OFF_BAR + 148);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqb = (p.S + BQ - 1) / BQ;
@@ -710,9 +720,11 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dq_tc_kernel(const __grid_c
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < DQ_KS; ++s) {
       mbar_init(kv_full(s), 1);
       mbar_init(kv_free(s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(sd_full(s), 1);
       mbar_init(sd_free(s), 4);
       mbar_init(ds_full(s), 4);
@@ -744,8 +756,8 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dq_tc_kernel(const __grid_c
     __syncwarp();
     int issued = 0;
     for (int j = 0; j < nkb; ++j) {
-      const int s = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
+      const int s = j % DQ_KS;
+      const uint32_t ph = (j / DQ_KS) & 1;
       if (!mbar_wait_warp(kv_free(s), ph ^ 1u, p.err, abort_flag)) { *abort_flag = 1; break; }
       const int kr = row0 + j * 64;
       if (el) {
@@ -759,7 +771,8 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dq_tc_kernel(const __grid_c
       ++issued;
     }
     mbar_wait(q_full, 0, p.err);
-    for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) mbar_wait(kv_full(j & 1), (j >> 1) & 1, p.err);
+    for (int j = (issued > DQ_KS ? issued - DQ_KS : 0); j < issued; ++j)
+      mbar_wait(kv_full(j % DQ_KS), (j / DQ_KS) & 1, p.err);
   } else if (warp == 1) {
     // ---------------- MMA (whole warp; the elected lane issues) ----------------
     const bool el = elect_one();
@@ -767,23 +780,23 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dq_tc_kernel(const __grid_c
     const uint32_t id_q = idesc_bf16_f32(128, 128, 0, 1);
     bool ok = mbar_wait_warp(q_full, 0, p.err, abort_flag);
     auto issue_dq = [&](int j) -> bool {
-      const int s = j & 1;
+      const int s = j & 1, ks = j % DQ_KS;
       if (!mbar_wait_warp(ds_full(s), (j >> 1) & 1, p.err, abort_flag)) return false;
       tc_fence_after();
       if (el) {
         for (int kk = 0; kk < 4; ++kk)
           umma_bf16(tmem + 256, desc_k64(sb + DQ_OFF_DS + s * 16384, kk),
-                    desc_mn128(sb + DQ_OFF_K + s * T64, 8192, kk), id_q, (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(kv_free(s));
+                    desc_mn128(sb + DQ_OFF_K + ks * T64, 8192, kk), id_q, (j > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(kv_free(ks));
         umma_commit(ds_free(s));
       }
       __syncwarp();
       return true;
     };
     for (int j = 0; ok && j < nkb; ++j) {
-      const int s = j & 1;
+      const int s = j & 1, ks = j % DQ_KS;
       const uint32_t ph = (j >> 1) & 1;
-      if (!mbar_wait_warp(kv_full(s), ph, p.err, abort_flag) ||
+      if (!mbar_wait_warp(kv_full(ks), (j / DQ_KS) & 1, p.err, abort_flag) ||
           (j >= 2 && !mbar_wait_warp(sd_free(s), ph ^ 1u, p.err, abort_flag))) {
         ok = false;
         break;
@@ -791,11 +804,11 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dq_tc_kernel(const __grid_c
       tc_fence_after();
       if (el) {
         for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16(tmem + s * 64, desc_k128(sb + DQ_OFF_Q, 16384, kk), desc_k128(sb + DQ_OFF_K + s * T64, 8192, kk),
+          umma_bf16(tmem + s * 64, desc_k128(sb + DQ_OFF_Q, 16384, kk), desc_k128(sb + DQ_OFF_K + ks * T64, 8192, kk),
                     id_s, kk > 0);
         for (int kk = 0; kk < HD / 16; ++kk)
           umma_bf16(tmem + 128 + s * 64, desc_k128(sb + DQ_OFF_DO, 16384, kk),
-                    desc_k128(sb + DQ_OFF_V + s * T64, 8192, kk), id_s, kk > 0);
+                    desc_k128(sb + DQ_OFF_V + ks * T64, 8192, kk), id_s, kk > 0);
         umma_commit(sd_full(s));
       }
       __syncwarp();
