@@ -295,8 +295,11 @@ __device__ __forceinline__ Unit decode_unit_cl(const GemmParams& P, int u) {
   while (p + 1 < P.nprob && u >= P.prob[p + 1].unit_begin) ++p;
   const GemmProb& pr = P.prob[p];
   const int local = u - pr.unit_begin;
-  const int si = local % pr.splits;
-  const int tile = local / pr.splits;
+  // K splits are the slowest index: the units in flight share one K range, so
+  // the operand slices they stream stay resident in L2
+  const int ntile = pr.m_tiles * pr.n_tiles;
+  const int si = local / ntile;
+  const int tile = local - si * ntile;
   Unit r;
   r.p = p;
   if (pr.n_fast) {
