@@ -3,14 +3,15 @@
 // (y = x W^T), its input gradient (dx = dy W) and its weight gradient
 // (dW = dy^T x), and the lm-head products.
 //
-// bf16 path: one persistent, warp-specialised tcgen05 kernel.
-//   warp 0      TMA producer: 128x64 A tile and 256x64 B tile per stage,
-//               128-byte swizzle, 4-stage mbarrier ring.
-//   warp 1      allocates 512 TMEM columns (two 128x256 fp32 accumulators)
-//               and one elected lane issues tcgen05.mma (M=128, N=256, K=16).
-//   warps 2..5  epilogue: tcgen05.ld the accumulator lane quarter they own,
-//               add the optional residual, convert, store; then release the
-//               accumulator so the MMA warp can start the tile after next.
+// bf16 path: one persistent, warp-specialised tcgen05 kernel on CTA pairs
+// (cta_group::2, 256 x 256 output tiles; the pair form is described above the
+// kernel). Per k-block of 64 each CTA stages a 128 x 64 half of A and of B with
+// 128-byte swizzle in a 6-stage mbarrier ring; tcgen05.mma M=256 N=256 K=16
+// accumulates in TMEM (two 256-column fp32 accumulators per CTA, so one tile's
+// epilogue overlaps the next tile's main loop); four epilogue warps read their
+// TMEM lane quarter (tcgen05.ld 32x32b.x32), add the optional residual,
+// convert and store. Work units (a tile, or a K range of a tile for long fp32
+// outputs) are handed out by a global atomic counter, heaviest problems first.
 // Operands may be K-major or MN-major (the transpose bits of the instruction
 // descriptor), so dX and dW need no transposed copies. Up to four problems
 // share one launch (for example the q/k/v projections, or a dX and a dW
@@ -152,24 +153,18 @@ __device__ __forceinline__ void store_chunk(const GemmProb& pr, int row, int col
 }
 
 // ---------------------------------------------------------------------------
-// Pair form (cta_group::2): a CTA pair computes 256 x 256 tiles, and a cluster
-// holds NP pairs stacked along M (NP = 1 or 2), so one cluster tile is
-// (256*NP) x 256.
+// Pair form (cta_group::2): a cluster of two CTAs computes 256 x 256 tiles.
 //   Per k-block each CTA stages its 128-row half of A (16 KB) and its 128-row
-//   half of B (16 KB); 6 stages. The pair leader (even rank) issues
-//   tcgen05.mma M=256 N=256, which reads both CTAs' halves and leaves rows
-//   0..127 of the pair's tile in the leader's TMEM and rows 128..255 in the
-//   follower's.
-//   With NP = 2 both pairs need the same B tile: the CTAs of equal parity in
-//   the two pairs hold the same B half, so each loads one 64-row piece of it
-//   and multicasts the piece to itself and its counterpart. That cuts the
-//   bytes read from L2 per FLOP by a quarter. A stage is then written by both
-//   pairs, so its "empty" barrier waits for both pairs' MMA commits.
-//   rank 0   warp 0: scheduler (unit ids to every CTA through DSMEM) + TMA
-//   others   warp 0: TMA of their own halves, completing on their pair
-//                    leader's barrier
-//   leaders  warp 1: TMEM (both CTAs of a pair allocate together) + MMA issue
-//   all      warps 2..5: epilogue of their own 128 rows
+//   half of B (16 KB); 6 stages. The leader (rank 0) issues tcgen05.mma
+//   M=256 N=256, which reads both CTAs' halves and leaves rows 0..127 of the
+//   tile in the leader's TMEM and rows 128..255 in the follower's.
+//   leader    warp 0: scheduler (unit ids to both CTAs through DSMEM) + A copies
+//   follower  warp 0: A copies, completing on the leader's barrier
+//   both      warp 6: B copies (two producer threads: one thread issuing every
+//                     tensor copy of a stage serialises them)
+//   leader    warp 1: TMEM (both CTAs allocate together) + MMA issue
+//   both      warps 2..5: epilogue of their own 128 rows
+// The issuing roles run as whole warps; one elected lane issues.
 // ---------------------------------------------------------------------------
 // k-blocks (of BK) per pipeline stage, and stages in the ring
 #ifndef KL_GEMM_KPS
@@ -257,17 +252,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
       "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(leader_bar)
       : "memory");
 }
-// The same tile into the same offset of every CTA in `mask`; each destination's
-// bytes complete on the barrier at `leader_bar`'s offset in that destination's
-// pair leader.
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void* tmap, int32_t x, int32_t y,
-                                                    uint32_t leader_bar, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".cta_group::2 [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-      "l"(tmap), "r"(x), "r"(y), "r"(leader_bar), "h"(mask)
-      : "memory");
-}
 __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                                uint32_t accumulate) {
   asm volatile(
@@ -288,8 +272,7 @@ __device__ __forceinline__ void umma_commit_pair_local(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// Unit decode for cluster tiles of (256*NP) x 256.
-template <int NP>
+// Unit decode for 256 x 256 tiles.
 __device__ __forceinline__ Unit decode_unit_cl(const GemmParams& P, int u) {
   int p = 0;
   while (p + 1 < P.nprob && u >= P.prob[p + 1].unit_begin) ++p;
@@ -304,9 +287,9 @@ __device__ __forceinline__ Unit decode_unit_cl(const GemmParams& P, int u) {
   r.p = p;
   if (pr.n_fast) {
     r.n0 = (tile % pr.n_tiles) * 256;
-    r.m0 = (tile / pr.n_tiles) * (256 * NP);
+    r.m0 = (tile / pr.n_tiles) * 256;
   } else {
-    r.m0 = (tile % pr.m_tiles) * (256 * NP);
+    r.m0 = (tile % pr.m_tiles) * 256;
     r.n0 = (tile / pr.m_tiles) * 256;
   }
   r.kb_lo = static_cast<int>(static_cast<int64_t>(si) * pr.kb_total / pr.splits);
@@ -314,12 +297,11 @@ __device__ __forceinline__ Unit decode_unit_cl(const GemmParams& P, int u) {
   return r;
 }
 
-template <int NP>
 __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __grid_constant__ GemmParams p) {
-  constexpr int CL = 2 * NP;                                   // CTAs per cluster
+  constexpr int CL = 2;                                        // CTAs per cluster
   // consumers of each unit id: epilogue warps, producers (all but the
-  // scheduler's own, plus the B producers), MMA issuers
-  constexpr int QEMPTY_COUNT = 4 * CL + (CL - 1) + (SPLIT_PRODUCER ? CL : 0) + NP;
+  // scheduler's own, plus the B producers), the MMA issuer
+  constexpr int QEMPTY_COUNT = 4 * CL + (CL - 1) + (SPLIT_PRODUCER ? CL : 0) + 1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -340,16 +322,14 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
-  const uint32_t pair = rank >> 1, peer = rank & 1u;
+  const uint32_t peer = rank;                                  // 0: leader, 1: follower
   const bool pair_leader = peer == 0;
-  const uint32_t lead = rank & ~1u;                            // this pair's leader rank
-  const uint16_t pair_mask = static_cast<uint16_t>(3u << (2 * pair));
-  const uint16_t all_mask = static_cast<uint16_t>((1u << CL) - 1u);
+  const uint16_t pair_mask = 3u;                               // both CTAs of the pair
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES2; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), NP);   // one MMA commit from every pair that reads or writes the stage
+      mbar_init(empty_bar(s), 1);    // the MMA commit (multicast to both CTAs)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -375,8 +355,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const uint32_t sched_qempty0 = mapa_rank(qempty_bar(0), 0);
-  const uint32_t lead_tempty0 = mapa_rank(tempty_bar(0), lead);
-  const uint32_t lead_full0 = mapa_rank(full_bar(0), lead);
+  const uint32_t lead_tempty0 = mapa_rank(tempty_bar(0), 0);
+  const uint32_t lead_full0 = mapa_rank(full_bar(0), 0);
 
   const bool b_producer = SPLIT_PRODUCER && warp == 6;
   if (warp == 0 || b_producer) {
@@ -433,9 +413,9 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
         qphase ^= 1u;
       }
       if (u < 0) break;
-      const Unit un = decode_unit_cl<NP>(p, u);
+      const Unit un = decode_unit_cl(p, u);
       const GemmProb& pr = p.prob[un.p];
-      const int mh = un.m0 + 256 * static_cast<int>(pair) + 128 * static_cast<int>(peer);   // this CTA's rows of A
+      const int mh = un.m0 + 128 * static_cast<int>(peer);   // this CTA's rows of A
       const int nh = un.n0 + 128 * static_cast<int>(peer);                                   // this CTA's rows of B
       int s = 0, off = 0;
       while (un.kb_lo >= off + pr.kb[s]) off += pr.kb[s++];
@@ -474,21 +454,13 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
           }
           if (!el || (SPLIT_PRODUCER && !b_producer)) {
             // B is issued by warp 6 (by its elected lane)
-          } else if (NP == 1) {
-            if (!pr.b_mn) {
-              tma_load_2d_pair(sb, tb, k0, nh, fb);
-            } else if (pr.b3d) {
-              tma_load_3d_pair(sb, tb, 0, k0, nh >> 6, fb);
-            } else {
-              tma_load_2d_pair(sb, tb, nh, k0, fb);
-              tma_load_2d_pair(sb + 8192, tb, nh + 64, k0, fb);
-            }
+          } else if (!pr.b_mn) {
+            tma_load_2d_pair(sb, tb, k0, nh, fb);
+          } else if (pr.b3d) {
+            tma_load_3d_pair(sb, tb, 0, k0, nh >> 6, fb);
           } else {
-            // piece `pair` of this CTA's B half, to this CTA and its counterpart in the other pair
-            const uint16_t mc = static_cast<uint16_t>((1u << rank) | (1u << (rank ^ 2u)));
-            const int nrow = nh + 64 * static_cast<int>(pair);
-            if (!pr.b_mn) tma_load_2d_pair_mc(sb + 8192u * pair, tb, k0, nrow, fb, mc);
-            else tma_load_2d_pair_mc(sb + 8192u * pair, tb, nrow, k0, fb, mc);
+            tma_load_2d_pair(sb, tb, nh, k0, fb);
+            tma_load_2d_pair(sb + 8192, tb, nh + 64, k0, fb);
           }
         }
         ++issued;
@@ -533,7 +505,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
         qphase ^= 1u;
       }
       if (u < 0) break;
-      const Unit un = decode_unit_cl<NP>(p, u);
+      const Unit un = decode_unit_cl(p, u);
       const GemmProb& pr = p.prob[un.p];
       const int acc = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
@@ -567,7 +539,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
             accumulate = 1;
           }
         }
-        umma_commit_pair(empty_bar(stage), all_mask);
+        umma_commit_pair(empty_bar(stage), pair_mask);
         }
         __syncwarp();
         if (++stage == STAGES2) {
@@ -601,7 +573,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
         qphase ^= 1u;
       }
       if (u < 0) break;
-      const Unit un = decode_unit_cl<NP>(p, u);
+      const Unit un = decode_unit_cl(p, u);
       const GemmProb& pr = p.prob[un.p];
       const int acc = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
@@ -610,7 +582,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
         break;
       }
       tc_fence_after();
-      const int row = un.m0 + 256 * static_cast<int>(pair) + 128 * static_cast<int>(peer) + quarter * 32 + lane;
+      const int row = un.m0 + 128 * static_cast<int>(peer) + quarter * 32 + lane;
       for (int c = 0; c < 256 / 32; ++c) {
         const int col0 = un.n0 + c * 32;
         if (col0 >= pr.N) break;
@@ -785,16 +757,9 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(int M, int N, int nseg, G
 // be accumulated in fp32 (fp32 output without addend, or a caller-provided
 // fp32 accumulator) are cut along K into units of at most ~UNIT_KB k-blocks,
 // so that no unit is long against a CTA's share of the launch.
-// Tile shape: pairs of CTAs (cta_group::2) on 256 x 256 tiles, clustered
-// GEMM_NP pairs deep along M with B multicast between the pairs; or single
-// CTAs on 128 x 256 tiles.
-#ifndef KL_GEMM_PAIRS_PER_CLUSTER
-#define KL_GEMM_PAIRS_PER_CLUSTER 1
-#endif
-constexpr int GEMM_NP = KL_GEMM_PAIRS_PER_CLUSTER;
-static_assert(GEMM_NP == 1 || GEMM_NP == 2, "pairs per cluster: 1 or 2");
-constexpr int GEMM_CL = 2 * GEMM_NP;
-constexpr int TILE_M = 256 * GEMM_NP;
+// Tile shape: pairs of CTAs (cta_group::2) on 256 x 256 tiles.
+constexpr int GEMM_CL = 2;
+constexpr int TILE_M = 256;
 constexpr int SPLIT_MIN_KB = 256;
 constexpr int UNIT_KB = 256;
 
@@ -824,7 +789,7 @@ int max_gemm_clusters(int dev, const cudaLaunchConfig_t& cfg_in) {
   cudaLaunchConfig_t cfg = cfg_in;
   cfg.gridDim = dim3(GEMM_CL * (num_sms() / GEMM_CL));
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tcp_kernel<GEMM_NP>, &cfg) != cudaSuccess || n < 1) {
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_bf16_tcp_kernel, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
     n = num_sms() / GEMM_CL;
   }
@@ -883,7 +848,7 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
       if (!s.a_mn) KL_TRY(make_map(&p.tmA[tm + g], s.A[g], s.K[g], s.M, s.lda[g], 128));
       else KL_TRY(make_map(&p.tmA[tm + g], s.A[g], s.M, s.K[g], s.lda[g], 64));
       if (!s.b_mn)
-        KL_TRY(make_map(&p.tmB[tm + g], s.B[g], s.K[g], s.N, s.ldb[g], GEMM_NP == 2 ? 64 : 128));
+        KL_TRY(make_map(&p.tmB[tm + g], s.B[g], s.K[g], s.N, s.ldb[g], 128));
       else KL_TRY(make_map(&p.tmB[tm + g], s.B[g], s.N, s.K[g], s.ldb[g], 64));
       pr.kb[g] = (s.K[g] + BK - 1) / BK;
       pr.kb_total += pr.kb[g];
@@ -892,7 +857,7 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
     // MN-major operands: one 3-D copy per half instead of two 2-D copies
     {
       CUtensorMap a3[GEMM_MAX_SEG], b3[GEMM_MAX_SEG];
-      bool ok_a = s.a_mn != 0, ok_b = s.b_mn != 0 && GEMM_NP == 1;
+      bool ok_a = s.a_mn != 0, ok_b = s.b_mn != 0;
       for (int g = 0; g < s.nseg; ++g) {
         if (ok_a) ok_a = make_map_mn3(&a3[g], s.A[g], s.M, s.K[g], s.lda[g]);
         if (ok_b) ok_b = make_map_mn3(&b3[g], s.B[g], s.N, s.K[g], s.ldb[g]);
@@ -948,7 +913,7 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
   int dev = 0;
   KL_CUDA(cudaGetDevice(&dev));
   if (dev < 64 && !(attr_done >> dev & 1u)) {
-    KL_CUDA(cudaFuncSetAttribute(gemm_bf16_tcp_kernel<GEMM_NP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    KL_CUDA(cudaFuncSetAttribute(gemm_bf16_tcp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(SMEM2_BYTES)));
     attr_done |= uint64_t(1) << dev;
   }
@@ -969,7 +934,7 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
       const int cap = max_gemm_clusters(dev, cfg);
       const int clusters = units < cap ? units : cap;
       cfg.gridDim = dim3(GEMM_CL * clusters);
-      KL_CUDA(cudaLaunchKernelEx(&cfg, gemm_bf16_tcp_kernel<GEMM_NP>, p));
+      KL_CUDA(cudaLaunchKernelEx(&cfg, gemm_bf16_tcp_kernel, p));
     }
   }
   KL_CUDA(cudaGetLastError());
