@@ -294,12 +294,20 @@ kl_status kl_layer_forward(const kl_layer_cfg* cfg, const kl_layer_weights* w, c
     KL_TRY(run_gemms(dt, &g, 1, st, "gemm.fwd_o"));
   }
   KL_TRY(rmsnorm_fwd(T, H, dt, s->x2, w->gamma2, cfg->eps, s->h2, s->rstd2, st));
-  {
+  if (dt == KL_BF16) {
+    // g and u of the same 128 columns in one tile; m = silu(g) u in the epilogue
+    GemmSpec g = proj(T, I, H, s->h2, H, w->wg, H, s->g, I, dt);
+    g.epi = GEMM_EPI_SWIGLU;
+    g.B2 = w->wu;
+    g.C2 = s->u;
+    g.C3 = s->m;
+    KL_TRY(run_gemms(dt, &g, 1, st, "gemm.fwd_gateup"));
+  } else {
     GemmSpec g[2] = {proj(T, I, H, s->h2, H, w->wg, H, s->g, I, dt),
                      proj(T, I, H, s->h2, H, w->wu, H, s->u, I, dt)};
     KL_TRY(run_gemms(dt, g, 2, st, "gemm.fwd_gateup"));
+    KL_TRY(swiglu_fwd(static_cast<int64_t>(T) * I, dt, s->g, s->u, s->m, st));
   }
-  KL_TRY(swiglu_fwd(static_cast<int64_t>(T) * I, dt, s->g, s->u, s->m, st));
   {
     GemmSpec g = proj(T, H, I, s->m, I, w->wd, I, Y, H, dt, s->x2, dt);
     KL_TRY(run_gemms(dt, &g, 1, st, "gemm.fwd_down"));
@@ -332,12 +340,19 @@ kl_status kl_layer_backward(const kl_layer_cfg* cfg, const kl_layer_weights* w,
   carve_bwd(D, c, &b);
   const int T = D.T, H = D.H, I = D.I, dt = D.dt, gdt = gr->dtype;
 
-  // MLP: dm = dY Wd, dWd = dY^T m
+  // MLP: dm = dY Wd (bf16: dg, du formed from it in the epilogue), dWd = dY^T m
   {
     GemmSpec g[2] = {dgrad(T, I, H, dY, w->wd, b.dm, dt), wgrad(H, I, T, dY, s->m, gr->wd, gdt)};
+    if (dt == KL_BF16) {
+      g[0].epi = GEMM_EPI_SWIGLU_BWD;
+      g[0].C = b.dg;
+      g[0].C2 = b.du;
+      g[0].X1 = s->g;
+      g[0].X2 = s->u;
+    }
     KL_TRY(run_gemms(dt, g, 2, st, "gemm.bwd_down"));
   }
-  KL_TRY(swiglu_bwd(static_cast<int64_t>(T) * I, dt, b.dm, s->g, s->u, b.dg, b.du, st));
+  if (dt != KL_BF16) KL_TRY(swiglu_bwd(static_cast<int64_t>(T) * I, dt, b.dm, s->g, s->u, b.dg, b.du, st));
   {
     GemmSpec dh = dgrad(T, H, I, b.dg, w->wg, b.dh2, KL_F32);
     dh.nseg = 2;
@@ -348,15 +363,23 @@ kl_status kl_layer_backward(const kl_layer_cfg* cfg, const kl_layer_weights* w,
   }
   KL_TRY(rmsnorm_bwd(T, H, dt, b.dh2, KL_F32, s->x2, w->gamma2, s->rstd2, dY, b.dx2,
                      static_cast<float*>(gr->gamma2), b.norm, b.norm_bytes, st));
-  // attention block: dO = dx2 Wo, dWo = dx2^T o
+  // attention block: dO = dx2 Wo (bf16: D = rowsum(dO * O) per head from the
+  // epilogue, straight into the attention workspace), dWo = dx2^T o
+  const bool d_ready = dt == KL_BF16;
   {
     GemmSpec g[2] = {dgrad(T, D.Dq, H, b.dx2, w->wo, b.dO, dt),
                      wgrad(H, D.Dq, T, b.dx2, s->o, gr->wo, gdt)};
+    if (d_ready) {
+      g[0].epi = GEMM_EPI_ROWDOT;
+      g[0].X1 = s->o;
+      g[0].dot_out = attention_bwd_d_rows(b.att);
+      g[0].dot_S = D.S;
+    }
     KL_TRY(run_gemms(dt, g, 2, st, "gemm.bwd_o"));
   }
   float *dq_acc = nullptr, *dk_acc = nullptr, *dv_acc = nullptr;
   KL_TRY(attention_bwd_accum(D.B, D.S, D.Hq, D.Hkv, D.d, dt, s->q, s->k, s->v, s->o, s->lse, b.dO,
-                             b.att, b.att_bytes, &dq_acc, &dk_acc, &dv_acc, st));
+                             b.att, b.att_bytes, &dq_acc, &dk_acc, &dv_acc, st, d_ready));
   KL_TRY(rope_bwd_convert(D.B, D.S, D.Hq, D.Hkv, D.d, cfg->rope_base, dt, dq_acc, dk_acc, dv_acc, b.dq,
                           b.dk, b.dv, st));
   {

@@ -697,7 +697,8 @@ size_t attention_bwd_ws(int B, int S, int Hq, int Hkv, int d) {
 kl_status attention_bwd_accum(int B, int S, int Hq, int Hkv, int d, int dtype, const void* q,
                               const void* k, const void* v, const void* o, const float* lse,
                               const void* dout, void* ws, size_t ws_bytes, float** dq_acc,
-                              float** dk_acc, float** dv_acc, cudaStream_t st) {
+                              float** dk_acc, float** dv_acc, cudaStream_t st,
+                              bool d_ready) {
   KL_TRY(check_args(B, S, Hq, Hkv, d, dtype));
   if (!q || !k || !v || !o || !lse || !dout)
     return set_error(KL_ERR_INVALID_ARG, "attention_bwd: null pointer");
@@ -736,12 +737,12 @@ kl_status attention_bwd_accum(int B, int S, int Hq, int Hkv, int d, int dtype, c
     KL_CUDA(cudaMemsetAsync(dk, 0, T * Hkv * d * 4, st));
     KL_CUDA(cudaMemsetAsync(dv, 0, T * Hkv * d * 4, st));
     const int64_t rows = static_cast<int64_t>(T) * Hq;
-    {
+    if (!d_ready) {
       ProfScope ps("attn_bwd_pre_bf16", st, 0.0, 4.0 * T * Hq * d + 4.0 * T * Hq);
       attn_bwd_pre_bf16_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
           B, S, Hq, (const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, Dd);
+      KL_CUDA(cudaGetLastError());
     }
-    KL_CUDA(cudaGetLastError());
     KL_TRY(attention_bwd_tc(B, S, Hq, Hkv, q, k, v, dout, lse, Dd, dq, dk, dv, st));
   }
   KL_CUDA(cudaGetLastError());

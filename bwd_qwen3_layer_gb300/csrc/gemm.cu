@@ -56,6 +56,15 @@ struct GemmProb {
   const void* R;
   int64_t ldr;
   int r_f32;
+  int epi;                // GEMM_EPI_*
+  int n_step;             // output columns per tile: 256, or 128 for GEMM_EPI_SWIGLU
+  int nmaps;              // tensor-map slots used (segments, or 2 B maps for GEMM_EPI_SWIGLU)
+  void* C2;
+  void* C3;
+  const void* X1;
+  const void* X2;
+  float* dot_out;
+  int dot_S;
 };
 
 struct GemmParams {
@@ -150,6 +159,134 @@ __device__ __forceinline__ void store_chunk(const GemmProb& pr, int row, int col
       for (int j = 0; j < ncols; ++j) c[j] = __float2bfloat16_rn(f[j]);
     }
   }
+}
+
+__device__ __forceinline__ float sigmoid_f(float g) { return 1.0f / (1.0f + expf(-g)); }
+
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16* p, bool vec, int ncols, float (&f)[32]) {
+  if (vec) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) {
+      const uint4 a = *reinterpret_cast<const uint4*>(p + j);
+      const float2 x0 = unpack_bf16x2(a.x), x1 = unpack_bf16x2(a.y), x2 = unpack_bf16x2(a.z),
+                   x3 = unpack_bf16x2(a.w);
+      f[j] = x0.x; f[j + 1] = x0.y; f[j + 2] = x1.x; f[j + 3] = x1.y;
+      f[j + 4] = x2.x; f[j + 5] = x2.y; f[j + 6] = x3.x; f[j + 7] = x3.y;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) f[j] = j < ncols ? __bfloat162float(p[j]) : 0.f;
+  }
+}
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, bool vec, int ncols, const float (&f)[32]) {
+  if (vec) {
+#pragma unroll
+    for (int j = 0; j < 32; j += 8) {
+      uint4 o;
+      o.x = pack_bf16x2(f[j], f[j + 1]);
+      o.y = pack_bf16x2(f[j + 2], f[j + 3]);
+      o.z = pack_bf16x2(f[j + 4], f[j + 5]);
+      o.w = pack_bf16x2(f[j + 6], f[j + 7]);
+      *reinterpret_cast<uint4*>(p + j) = o;
+    }
+  } else {
+    for (int j = 0; j < ncols; ++j) p[j] = __float2bfloat16_rn(f[j]);
+  }
+}
+
+// GEMM_EPI_SWIGLU: 32 columns of g and of u (fp32 accumulators) -> g, u, m.
+__device__ __forceinline__ void store_swiglu(const GemmProb& pr, int row, int col0, const uint32_t (&vg)[32],
+                                             const uint32_t (&vu)[32]) {
+  const int ncols = min(32, pr.N - col0);
+  const bool vec = pr.vec_ok && ncols == 32;
+  const int64_t o = static_cast<int64_t>(row) * pr.ldc + col0;
+  float g[32], u[32], m[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    g[j] = __uint_as_float(vg[j]);
+    u[j] = __uint_as_float(vu[j]);
+    m[j] = g[j] * sigmoid_f(g[j]) * u[j];
+  }
+  store_bf16x32(static_cast<__nv_bfloat16*>(pr.C) + o, vec, ncols, g);
+  store_bf16x32(static_cast<__nv_bfloat16*>(pr.C2) + o, vec, ncols, u);
+  store_bf16x32(static_cast<__nv_bfloat16*>(pr.C3) + o, vec, ncols, m);
+}
+
+// GEMM_EPI_SWIGLU_BWD: the saved g, u of one 32-column chunk, as raw bf16
+// (loaded a chunk ahead so the epilogue does not wait on HBM for each chunk).
+struct GluRaw {
+  uint4 g[4], u[4];
+};
+__device__ __forceinline__ void glu_load(const GemmProb& pr, int row, int col0, GluRaw& r) {
+  const int ncols = min(32, pr.N - col0);
+  if (row >= pr.M || ncols <= 0) return;
+  const int64_t o = static_cast<int64_t>(row) * pr.ldc + col0;
+  const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(pr.X1) + o;
+  const __nv_bfloat16* u = static_cast<const __nv_bfloat16*>(pr.X2) + o;
+  if (pr.vec_ok && ncols == 32) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      r.g[j] = *reinterpret_cast<const uint4*>(g + 8 * j);
+      r.u[j] = *reinterpret_cast<const uint4*>(u + 8 * j);
+    }
+  } else {
+    __nv_bfloat16 tg[32], tu[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      tg[j] = j < ncols ? g[j] : __float2bfloat16_rn(0.f);
+      tu[j] = j < ncols ? u[j] : __float2bfloat16_rn(0.f);
+    }
+    memcpy(r.g, tg, sizeof(tg));
+    memcpy(r.u, tu, sizeof(tu));
+  }
+}
+// 32 columns of dm (fp32) with the saved g, u -> dg = dm u s (1 + g (1 - s)), du = dm g s.
+__device__ __forceinline__ void store_swiglu_bwd(const GemmProb& pr, int row, int col0, const uint32_t (&v)[32],
+                                                 const GluRaw& r) {
+  const int ncols = min(32, pr.N - col0);
+  const bool vec = pr.vec_ok && ncols == 32;
+  const int64_t o = static_cast<int64_t>(row) * pr.ldc + col0;
+  float g[32], u[32];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t gw[4] = {r.g[j].x, r.g[j].y, r.g[j].z, r.g[j].w};
+    const uint32_t uw[4] = {r.u[j].x, r.u[j].y, r.u[j].z, r.u[j].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 gf = unpack_bf16x2(gw[e]), uf = unpack_bf16x2(uw[e]);
+      g[8 * j + 2 * e] = gf.x;
+      g[8 * j + 2 * e + 1] = gf.y;
+      u[8 * j + 2 * e] = uf.x;
+      u[8 * j + 2 * e + 1] = uf.y;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float dm = __uint_as_float(v[j]);
+    const float sg = sigmoid_f(g[j]);
+    const float dg = dm * u[j] * sg * (1.0f + g[j] * (1.0f - sg));
+    u[j] = dm * g[j] * sg;   // du
+    g[j] = dg;
+  }
+  store_bf16x32(static_cast<__nv_bfloat16*>(pr.C) + o, vec, ncols, g);
+  store_bf16x32(static_cast<__nv_bfloat16*>(pr.C2) + o, vec, ncols, u);
+}
+
+// GEMM_EPI_ROWDOT: sum over 32 columns of bf16(product) * X1.
+__device__ __forceinline__ float chunk_rowdot(const GemmProb& pr, int row, int col0, const uint32_t (&v)[32]) {
+  const int ncols = min(32, pr.N - col0);
+  const bool vec = pr.vec_ok && ncols == 32;
+  float x[32];
+  load_bf16x32(static_cast<const __nv_bfloat16*>(pr.X1) + static_cast<int64_t>(row) * pr.ldc + col0, vec, ncols, x);
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; j += 4) {
+    a0 = fmaf(__bfloat162float(__float2bfloat16_rn(__uint_as_float(v[j]))), x[j], a0);
+    a1 = fmaf(__bfloat162float(__float2bfloat16_rn(__uint_as_float(v[j + 1]))), x[j + 1], a1);
+    a2 = fmaf(__bfloat162float(__float2bfloat16_rn(__uint_as_float(v[j + 2]))), x[j + 2], a2);
+    a3 = fmaf(__bfloat162float(__float2bfloat16_rn(__uint_as_float(v[j + 3]))), x[j + 3], a3);
+  }
+  return (a0 + a1) + (a2 + a3);
 }
 
 // ---------------------------------------------------------------------------
@@ -286,11 +423,11 @@ __device__ __forceinline__ Unit decode_unit_cl(const GemmParams& P, int u) {
   Unit r;
   r.p = p;
   if (pr.n_fast) {
-    r.n0 = (tile % pr.n_tiles) * 256;
+    r.n0 = (tile % pr.n_tiles) * pr.n_step;
     r.m0 = (tile / pr.n_tiles) * 256;
   } else {
     r.m0 = (tile % pr.m_tiles) * 256;
-    r.n0 = (tile / pr.m_tiles) * 256;
+    r.n0 = (tile / pr.m_tiles) * pr.n_step;
   }
   r.kb_lo = static_cast<int>(static_cast<int64_t>(si) * pr.kb_total / pr.splits);
   r.kb_hi = static_cast<int>(static_cast<int64_t>(si + 1) * pr.kb_total / pr.splits);
@@ -366,7 +503,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
     // warp 6: B tiles when split.
     if (el)
       for (int i = 0; i < p.nprob; ++i)
-        for (int s = 0; s < p.prob[i].nseg; ++s) {
+        for (int s = 0; s < p.prob[i].nmaps; ++s) {
           tma_prefetch_desc(&p.tmA[p.prob[i].tmap_base + s]);
           tma_prefetch_desc(&p.tmB[p.prob[i].tmap_base + s]);
         }
@@ -416,7 +553,10 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
       const Unit un = decode_unit_cl(p, u);
       const GemmProb& pr = p.prob[un.p];
       const int mh = un.m0 + 128 * static_cast<int>(peer);   // this CTA's rows of A
-      const int nh = un.n0 + 128 * static_cast<int>(peer);                                   // this CTA's rows of B
+      // this CTA's rows of B: its half of the tile's 256 columns, or (SwiGLU) the
+      // tile's 128 columns of the gate (leader) or up (follower) weights
+      const bool glu = pr.epi == GEMM_EPI_SWIGLU;
+      const int nh = glu ? un.n0 : un.n0 + 128 * static_cast<int>(peer);
       int s = 0, off = 0;
       while (un.kb_lo >= off + pr.kb[s]) off += pr.kb[s++];
       int kl = un.kb_lo - off;
@@ -436,7 +576,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
             kl = 0;
           }
           const CUtensorMap* ta = &p.tmA[pr.tmap_base + s];
-          const CUtensorMap* tb = &p.tmB[pr.tmap_base + s];
+          const CUtensorMap* tb = &p.tmB[pr.tmap_base + (glu ? static_cast<int>(peer) : s)];
           const uint32_t sa = sbase + stage * STAGE2_BYTES + j * KB2_BYTES;
           const uint32_t sb = sa + HALF_BYTES;
           const int k0 = kl * BK;
@@ -577,20 +717,53 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
       const GemmProb& pr = p.prob[un.p];
       const int acc = it & 1;
       const uint32_t use = static_cast<uint32_t>(it >> 1);
+      const int row = un.m0 + 128 * static_cast<int>(peer) + quarter * 32 + lane;
+      GluRaw glu_next;
+      if (pr.epi == GEMM_EPI_SWIGLU_BWD) glu_load(pr, row, un.n0, glu_next);   // overlaps the wait below
       if (!mbar_wait_cl_warp(tfull_bar(acc), use & 1u, p.err, abort_flag)) {
         *abort_flag = 1;
         break;
       }
       tc_fence_after();
-      const int row = un.m0 + 128 * static_cast<int>(peer) + quarter * 32 + lane;
-      for (int c = 0; c < 256 / 32; ++c) {
-        const int col0 = un.n0 + c * 32;
-        if (col0 >= pr.N) break;
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(
-            tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * 256 + c * 32), v);
-        tmem_ld_wait();
-        if (row < pr.M) store_chunk(pr, row, col0, v);
+      const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * 256);
+      if (pr.epi == GEMM_EPI_SWIGLU) {
+        // columns 0..127 of the accumulator are g, 128..255 are u, of the same 128 outputs
+        for (int c = 0; c < 4; ++c) {
+          const int col0 = un.n0 + c * 32;
+          if (col0 >= pr.N) break;
+          uint32_t vg[32], vu[32];
+          tmem_ld_32x32b_x32(tacc + c * 32, vg);
+          tmem_ld_32x32b_x32(tacc + 128 + c * 32, vu);
+          tmem_ld_wait();
+          if (row < pr.M) store_swiglu(pr, row, col0, vg, vu);
+        }
+      } else {
+        float dot = 0.f;
+        for (int c = 0; c < 256 / 32; ++c) {
+          const int col0 = un.n0 + c * 32;
+          if (col0 >= pr.N) break;
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tacc + c * 32, v);
+          tmem_ld_wait();
+          if (pr.epi == GEMM_EPI_SWIGLU_BWD) {
+            const GluRaw cur = glu_next;
+            if (c + 1 < 256 / 32) glu_load(pr, row, col0 + 32, glu_next);   // next chunk in flight
+            if (row < pr.M) store_swiglu_bwd(pr, row, col0, v, cur);
+          } else if (row < pr.M) {
+            {
+              store_chunk(pr, row, col0, v);
+              if (pr.epi == GEMM_EPI_ROWDOT) {
+                dot += chunk_rowdot(pr, row, col0, v);
+                if ((c & 3) == 3) {   // the 128 columns of one head are done
+                  const int heads = pr.N >> 7, h = (col0 - 96) >> 7;
+                  const int b = row / pr.dot_S, t = row - b * pr.dot_S;
+                  pr.dot_out[(static_cast<int64_t>(b) * heads + h) * pr.dot_S + t] = dot;
+                  dot = 0.f;
+                }
+              }
+            }
+          }
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -807,7 +980,7 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
     const GemmSpec& s = specs_in[i];
     int kb = 0;
     for (int g = 0; g < s.nseg && g < GEMM_MAX_SEG; ++g) kb += (s.K[g] + BK - 1) / BK;
-    const bool can_split = (s.c_dtype == KL_F32 && !s.R) || s.acc_ws;
+    const bool can_split = s.epi == GEMM_EPI_STORE && ((s.c_dtype == KL_F32 && !s.R) || s.acc_ws);
     splits[i] = (can_split && kb >= SPLIT_MIN_KB) ? (kb + UNIT_KB - 1) / UNIT_KB : 1;
     kbt[i] = kb;
     order[i] = i;
@@ -830,6 +1003,18 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
       return set_error(KL_ERR_INVALID_ARG, "gemm: bad problem %d (M %d N %d nseg %d)", oi, s.M, s.N, s.nseg);
     if (s.c_dtype != KL_BF16 && s.c_dtype != KL_F32)
       return set_error(KL_ERR_INVALID_ARG, "gemm: bad output dtype");
+    const bool glu = s.epi == GEMM_EPI_SWIGLU;
+    if (s.epi != GEMM_EPI_STORE) {
+      const bool pairs_ok = s.epi != GEMM_EPI_SWIGLU || (s.B2 && aligned16(s.B2) && !s.b_mn && s.C2 && s.C3);
+      const bool bwd_ok = s.epi != GEMM_EPI_SWIGLU_BWD || (s.X1 && s.X2 && s.C2);
+      const bool dot_ok = s.epi != GEMM_EPI_ROWDOT || (s.X1 && s.dot_out && s.dot_S > 0 && s.M % s.dot_S == 0 &&
+                                                       s.N % 128 == 0);
+      if (s.epi > GEMM_EPI_ROWDOT || s.c_dtype != KL_BF16 || s.R || s.nseg != 1 || s.acc_ws || !pairs_ok ||
+          !bwd_ok || !dot_ok)
+        return set_error(KL_ERR_INVALID_ARG, "gemm: problem %d: bad epilogue variant %d", oi, s.epi);
+    }
+    if (tm + (glu ? 2 : s.nseg) > GEMM_MAX_PROB * GEMM_MAX_SEG)
+      return set_error(KL_ERR_INVALID_ARG, "gemm: too many operand maps in one launch");
     GemmProb& pr = p.prob[i];
     pr.M = s.M;
     pr.N = s.N;
@@ -837,6 +1022,15 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
     pr.a_mn = s.a_mn;
     pr.b_mn = s.b_mn;
     pr.tmap_base = tm;
+    pr.epi = s.epi;
+    pr.n_step = glu ? 128 : BN;
+    pr.nmaps = glu ? 2 : s.nseg;
+    pr.C2 = s.C2;
+    pr.C3 = s.C3;
+    pr.X1 = s.X1;
+    pr.X2 = s.X2;
+    pr.dot_out = s.dot_out;
+    pr.dot_S = s.dot_S;
     double ksum = 0.0;
     for (int g = 0; g < s.nseg; ++g) {
       if (!s.A[g] || !s.B[g] || s.K[g] < 1)
@@ -854,6 +1048,12 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
       pr.kb_total += pr.kb[g];
       ksum += s.K[g];
     }
+    if (glu) {
+      // leader stages gate rows, follower up rows, of the same 128 outputs
+      if (s.ldb[0] % 8) return set_error(KL_ERR_INVALID_ARG, "gemm: up weights row stride");
+      KL_TRY(make_map(&p.tmB[tm + 1], s.B2, s.K[0], s.N, s.ldb[0], 128));
+      p.tmA[tm + 1] = p.tmA[tm];
+    }
     // MN-major operands: one 3-D copy per half instead of two 2-D copies
     {
       CUtensorMap a3[GEMM_MAX_SEG], b3[GEMM_MAX_SEG];
@@ -867,9 +1067,9 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
       pr.a3d = ok_a;
       pr.b3d = ok_b;
     }
-    tm += s.nseg;
+    tm += pr.nmaps;
     pr.m_tiles = (s.M + TILE_M - 1) / TILE_M;
-    pr.n_tiles = (s.N + BN - 1) / BN;
+    pr.n_tiles = (s.N + pr.n_step - 1) / pr.n_step;
     // keep the smaller operand resident in L2: walk its dimension fastest
     pr.n_fast = s.N < s.M ? 1 : 0;
     pr.splits = splits[oi] < pr.kb_total ? splits[oi] : pr.kb_total;
@@ -894,14 +1094,18 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
       pr.r_f32 = s.r_dtype == KL_F32;
       const size_t ce = dtype_size(s.c_dtype), re = dtype_size(s.r_dtype);
       pr.vec_ok = aligned16(s.C) && (s.ldc * ce) % 16 == 0 &&
-                  (!s.R || (aligned16(s.R) && (s.ldr * re) % 16 == 0));
+                  (!s.R || (aligned16(s.R) && (s.ldr * re) % 16 == 0)) &&
+                  (!s.C2 || aligned16(s.C2)) && (!s.C3 || aligned16(s.C3)) && (!s.X1 || aligned16(s.X1)) &&
+                  (!s.X2 || aligned16(s.X2));
     }
     if (pr.atomic) {
       if (finalize[oi]) KL_CUDA(cudaMemsetAsync(pr.C, 0, static_cast<size_t>(s.M) * s.N * 4, st));
       else KL_CUDA(cudaMemset2DAsync(pr.C, static_cast<size_t>(pr.ldc) * 4, 0, static_cast<size_t>(s.N) * 4, s.M, st));
     }
-    flops += 2.0 * s.M * s.N * ksum;
-    bytes += 2.0 * (s.M + s.N) * ksum + static_cast<double>(s.M) * s.N * dtype_size(s.c_dtype) +
+    const double nmul = glu ? 2.0 : 1.0;   // SwiGLU: a gate and an up product
+    const double extra = glu ? 2.0 : s.epi == GEMM_EPI_SWIGLU_BWD ? 3.0 : s.epi == GEMM_EPI_ROWDOT ? 1.0 : 0.0;
+    flops += 2.0 * s.M * s.N * nmul * ksum;
+    bytes += 2.0 * (s.M + nmul * s.N) * ksum + static_cast<double>(s.M) * s.N * dtype_size(s.c_dtype) * (1.0 + extra) +
              (s.R ? static_cast<double>(s.M) * s.N * dtype_size(s.r_dtype) : 0.0);
   }
   p.nprob = nspec;

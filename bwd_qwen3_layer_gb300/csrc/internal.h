@@ -34,7 +34,31 @@ struct GemmSpec {
   // Optional fp32 [M,N] scratch: lets a long-K problem with a bf16 output or
   // an addend be split along K (accumulated here, then finished into C).
   float* acc_ws = nullptr;
+  // Epilogue variant (bf16 operands and outputs, one segment, no addend, no K
+  // split); every extra tensor is [M, N] with row stride ldc:
+  //   GEMM_EPI_SWIGLU      B = gate weights, B2 = up weights ([N, K] both):
+  //                        C = g, C2 = u, C3 = m = silu(g) * u, m formed from
+  //                        the fp32 accumulators.
+  //   GEMM_EPI_SWIGLU_BWD  the product is dm; X1 = g, X2 = u;
+  //                        C = dg = dm u s (1 + g (1 - s)), C2 = du = dm g s,
+  //                        s = sigmoid(g).
+  //   GEMM_EPI_ROWDOT      C = the product (bf16, as usual); X1 = O; and
+  //                        dot_out[(b * N/128 + h) * dot_S + t] = sum over the
+  //                        128 columns of head h of bf16(C) * O for token row
+  //                        b * dot_S + t (N a multiple of 128).
+  int epi = 0;
+  const void* B2 = nullptr;
+  void* C2 = nullptr;
+  void* C3 = nullptr;
+  const void* X1 = nullptr;
+  const void* X2 = nullptr;
+  float* dot_out = nullptr;
+  int dot_S = 0;
 };
+constexpr int GEMM_EPI_STORE = 0;
+constexpr int GEMM_EPI_SWIGLU = 1;
+constexpr int GEMM_EPI_SWIGLU_BWD = 2;
+constexpr int GEMM_EPI_ROWDOT = 3;
 
 // bf16 operands on the tcgen05 tensor cores; up to GEMM_MAX_PROB independent
 // problems share one persistent launch.
@@ -81,11 +105,15 @@ kl_status attention_bwd_tc(int B, int S, int Hq, int Hkv, const void* q, const v
                            float* dv_acc, cudaStream_t st);
 size_t attention_bwd_ws(int B, int S, int Hq, int Hkv, int d);
 // dq_out/dk_out/dv_out: fp32 accumulators [T,H*d] written by the kernel
-// (inside ws); the caller converts (with rotary backward) afterwards.
+// (inside ws); the caller converts (with rotary backward) afterwards. The
+// workspace starts with D = rowsum(dO * O) as fp32 [B, Hq, S]; d_ready (bf16)
+// means the caller has already written it there (attention_bwd_d_rows).
+inline float* attention_bwd_d_rows(void* ws) { return static_cast<float*>(ws); }
 kl_status attention_bwd_accum(int B, int S, int Hq, int Hkv, int d, int dtype, const void* q,
                               const void* k, const void* v, const void* o, const float* lse,
                               const void* dout, void* ws, size_t ws_bytes, float** dq_acc,
-                              float** dk_acc, float** dv_acc, cudaStream_t st);
+                              float** dk_acc, float** dv_acc, cudaStream_t st,
+                              bool d_ready = false);
 
 // ---------------------------------------------------------------------------
 // cross entropy (ce.cu)
