@@ -163,6 +163,8 @@ struct BwdWs {
   size_t att_bytes;
   void* norm;
   size_t norm_bytes;
+  void* tail;             // fp32 scratch balancing the GEMM launches' last rounds (bf16)
+  size_t tail_bytes;
 };
 
 void carve_bwd(const Dims& D, Carver& c, BwdWs* w) {
@@ -181,6 +183,8 @@ void carve_bwd(const Dims& D, Carver& c, BwdWs* w) {
   w->att = c.take(w->att_bytes);
   w->norm_bytes = rmsnorm_bwd_ws(D.T, D.H);
   w->norm = c.take(w->norm_bytes);
+  w->tail_bytes = D.dt == KL_BF16 ? gemm_tail_ws_bytes() : 0;
+  w->tail = w->tail_bytes ? c.take(w->tail_bytes) : nullptr;
 }
 
 kl_status check_ptrs(std::initializer_list<const void*> ptrs, const char* what) {
@@ -255,7 +259,7 @@ kl_status kl_layer_saved_carve(const kl_layer_cfg* cfg, void* base, size_t bytes
 size_t kl_layer_fwd_workspace_bytes(const kl_layer_cfg* cfg) {
   Dims D;
   if (check_cfg(cfg, &D) != KL_OK) return 0;
-  return 256;
+  return D.dt == KL_BF16 ? gemm_tail_ws_bytes() : 256;
 }
 
 size_t kl_layer_bwd_workspace_bytes(const kl_layer_cfg* cfg) {
@@ -267,10 +271,17 @@ size_t kl_layer_bwd_workspace_bytes(const kl_layer_cfg* cfg) {
   return c.off;
 }
 
+// Gives every spec of a launch the fp32 scratch that balances its last round.
+void with_tail(GemmSpec* g, int n, void* ws, size_t bytes) {
+  if (!ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return;
+  for (int i = 0; i < n; ++i) {
+    g[i].tail_ws = static_cast<float*>(ws);
+    g[i].tail_ws_bytes = bytes;
+  }
+}
+
 kl_status kl_layer_forward(const kl_layer_cfg* cfg, const kl_layer_weights* w, const void* X,
                            void* Y, kl_layer_saved* s, void* ws, size_t ws_bytes, void* stream) {
-  (void)ws;
-  (void)ws_bytes;
   Dims D;
   KL_TRY(check_cfg(cfg, &D));
   if (!w || !s) return set_error(KL_ERR_INVALID_ARG, "layer_forward: null weights or saved");
@@ -285,12 +296,14 @@ kl_status kl_layer_forward(const kl_layer_cfg* cfg, const kl_layer_weights* w, c
     GemmSpec g[3] = {proj(T, D.Dq, H, s->h1, H, w->wq, H, s->q, D.Dq, dt),
                      proj(T, D.Dkv, H, s->h1, H, w->wk, H, s->k, D.Dkv, dt),
                      proj(T, D.Dkv, H, s->h1, H, w->wv, H, s->v, D.Dkv, dt)};
+    with_tail(g, 3, ws, ws_bytes);
     KL_TRY(run_gemms(dt, g, 3, st, "gemm.fwd_qkv"));
   }
   KL_TRY(rope_qk(D.B, D.S, D.Hq, D.Hkv, D.d, cfg->rope_base, dt, s->q, s->k, 1, st));
   KL_TRY(attention_fwd(D.B, D.S, D.Hq, D.Hkv, D.d, dt, s->q, s->k, s->v, s->o, s->lse, st));
   {
     GemmSpec g = proj(T, H, D.Dq, s->o, D.Dq, w->wo, D.Dq, s->x2, H, dt, X, dt);
+    with_tail(&g, 1, ws, ws_bytes);
     KL_TRY(run_gemms(dt, &g, 1, st, "gemm.fwd_o"));
   }
   KL_TRY(rmsnorm_fwd(T, H, dt, s->x2, w->gamma2, cfg->eps, s->h2, s->rstd2, st));
@@ -310,6 +323,7 @@ kl_status kl_layer_forward(const kl_layer_cfg* cfg, const kl_layer_weights* w, c
   }
   {
     GemmSpec g = proj(T, H, I, s->m, I, w->wd, I, Y, H, dt, s->x2, dt);
+    with_tail(&g, 1, ws, ws_bytes);
     KL_TRY(run_gemms(dt, &g, 1, st, "gemm.fwd_down"));
   }
   return KL_OK;
@@ -350,6 +364,7 @@ kl_status kl_layer_backward(const kl_layer_cfg* cfg, const kl_layer_weights* w,
       g[0].X1 = s->g;
       g[0].X2 = s->u;
     }
+    with_tail(g, 2, b.tail, b.tail_bytes);
     KL_TRY(run_gemms(dt, g, 2, st, "gemm.bwd_down"));
   }
   if (dt != KL_BF16) KL_TRY(swiglu_bwd(static_cast<int64_t>(T) * I, dt, b.dm, s->g, s->u, b.dg, b.du, st));
@@ -359,6 +374,7 @@ kl_status kl_layer_backward(const kl_layer_cfg* cfg, const kl_layer_weights* w,
     dh.A[1] = b.du; dh.lda[1] = I; dh.B[1] = w->wu; dh.ldb[1] = H; dh.K[1] = I;
     GemmSpec g[3] = {dh, wgrad(I, H, T, b.dg, s->h2, gr->wg, gdt),
                      wgrad(I, H, T, b.du, s->h2, gr->wu, gdt)};
+    with_tail(g, 3, b.tail, b.tail_bytes);
     KL_TRY(run_gemms(dt, g, 3, st, "gemm.bwd_gateup"));
   }
   KL_TRY(rmsnorm_bwd(T, H, dt, b.dh2, KL_F32, s->x2, w->gamma2, s->rstd2, dY, b.dx2,
@@ -375,6 +391,7 @@ kl_status kl_layer_backward(const kl_layer_cfg* cfg, const kl_layer_weights* w,
       g[0].dot_out = attention_bwd_d_rows(b.att);
       g[0].dot_S = D.S;
     }
+    with_tail(g, 2, b.tail, b.tail_bytes);
     KL_TRY(run_gemms(dt, g, 2, st, "gemm.bwd_o"));
   }
   float *dq_acc = nullptr, *dk_acc = nullptr, *dv_acc = nullptr;
@@ -390,6 +407,7 @@ kl_status kl_layer_backward(const kl_layer_cfg* cfg, const kl_layer_weights* w,
     GemmSpec g[4] = {dh, wgrad(D.Dq, H, T, b.dq, s->h1, gr->wq, gdt),
                      wgrad(D.Dkv, H, T, b.dk, s->h1, gr->wk, gdt),
                      wgrad(D.Dkv, H, T, b.dv, s->h1, gr->wv, gdt)};
+    with_tail(g, 4, b.tail, b.tail_bytes);
     KL_TRY(run_gemms(dt, g, 4, st, "gemm.bwd_qkv"));
   }
   KL_TRY(rmsnorm_bwd(T, H, dt, b.dh1, KL_F32, s->x, w->gamma1, s->rstd1, b.dx2, dX,
@@ -416,7 +434,7 @@ size_t kl_lmhead_workspace_bytes(const kl_lmhead_cfg* c) {
   if (check_lm(c) != KL_OK) return 0;
   const size_t NV = static_cast<size_t>(c->N) * c->V;
   return align_up(NV * 4, 256) + align_up(NV * dtype_size(c->dtype), 256) + ce_ws(c->N) +
-         align_up(static_cast<size_t>(c->N) * c->H * 4, 256);
+         align_up(static_cast<size_t>(c->N) * c->H * 4, 256) + (c->dtype == KL_BF16 ? gemm_tail_ws_bytes() : 0);
 }
 
 kl_status kl_lmhead_ce_argmax(const kl_lmhead_cfg* c, const void* X, const void* W,
@@ -438,15 +456,19 @@ kl_status kl_lmhead_ce_argmax(const kl_lmhead_cfg* c, const void* X, const void*
   void* dz_ws = cv.take(NV * dtype_size(dt));
   void* ce = cv.take(ce_ws(N));
   float* dx_acc = static_cast<float*>(cv.take(static_cast<size_t>(N) * H * 4));
+  const size_t tail_bytes = dt == KL_BF16 ? gemm_tail_ws_bytes() : 0;
+  void* tail = tail_bytes ? cv.take(tail_bytes) : nullptr;
   void* dz = dlogits ? dlogits : dz_ws;
   {
     GemmSpec g = proj(N, V, H, X, H, W, H, z, V, KL_F32);
+    with_tail(&g, 1, tail, tail_bytes);
     KL_TRY(run_gemms(dt, &g, 1, st, "gemm.lm_logits"));
   }
   KL_TRY(ce_argmax(N, V, z, targets, loss, argmax, dz, dt, ce, ce_ws(N), st));
   {
     GemmSpec g[2] = {dgrad(N, H, V, dz, W, dX, dt), wgrad(V, H, N, dz, X, dW, c->dw_dtype)};
     g[0].acc_ws = dx_acc;   // K = V is long: split it, accumulate in fp32
+    with_tail(g, 2, tail, tail_bytes);
     KL_TRY(run_gemms(dt, g, 2, st, "gemm.lm_bwd"));
   }
   return KL_OK;

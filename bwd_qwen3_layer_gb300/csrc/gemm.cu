@@ -65,6 +65,9 @@ struct GemmProb {
   const void* X2;
   float* dot_out;
   int dot_S;
+  int whole_tiles;        // tiles computed whole; the rest (tail) are split along K
+  int tail_tiles, tail_splits;
+  float* tail_acc;        // [tail_tiles][256][256] fp32
 };
 
 struct GemmParams {
@@ -82,6 +85,7 @@ struct Unit {
   int p;
   int m0, n0;
   int kb_lo, kb_hi;
+  int tail;               // index among the problem's split tail tiles, or -1
 };
 
 __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
@@ -418,10 +422,22 @@ __device__ __forceinline__ Unit decode_unit_cl(const GemmParams& P, int u) {
   // K splits are the slowest index: the units in flight share one K range, so
   // the operand slices they stream stay resident in L2
   const int ntile = pr.m_tiles * pr.n_tiles;
-  const int si = local / ntile;
-  const int tile = local - si * ntile;
+  int si, tile, nsplit;
   Unit r;
   r.p = p;
+  r.tail = -1;
+  if (pr.tail_splits > 1 && local >= pr.whole_tiles) {
+    // last-round tiles, split along K (split-major as well)
+    const int t = local - pr.whole_tiles;
+    si = t / pr.tail_tiles;
+    r.tail = t - si * pr.tail_tiles;
+    tile = pr.whole_tiles + r.tail;
+    nsplit = pr.tail_splits;
+  } else {
+    si = local / ntile;
+    tile = local - si * ntile;
+    nsplit = pr.splits;
+  }
   if (pr.n_fast) {
     r.n0 = (tile % pr.n_tiles) * pr.n_step;
     r.m0 = (tile / pr.n_tiles) * 256;
@@ -429,8 +445,8 @@ __device__ __forceinline__ Unit decode_unit_cl(const GemmParams& P, int u) {
     r.m0 = (tile % pr.m_tiles) * 256;
     r.n0 = (tile / pr.m_tiles) * pr.n_step;
   }
-  r.kb_lo = static_cast<int>(static_cast<int64_t>(si) * pr.kb_total / pr.splits);
-  r.kb_hi = static_cast<int>(static_cast<int64_t>(si + 1) * pr.kb_total / pr.splits);
+  r.kb_lo = static_cast<int>(static_cast<int64_t>(si) * pr.kb_total / nsplit);
+  r.kb_hi = static_cast<int>(static_cast<int64_t>(si + 1) * pr.kb_total / nsplit);
   return r;
 }
 
@@ -750,7 +766,14 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
             if (c + 1 < 256 / 32) glu_load(pr, row, col0 + 32, glu_next);   // next chunk in flight
             if (row < pr.M) store_swiglu_bwd(pr, row, col0, v, cur);
           } else if (row < pr.M) {
-            {
+            if (un.tail >= 0) {
+              // a K-range of a last-round tile: accumulate into the compact fp32 scratch
+              float* a = pr.tail_acc + (static_cast<int64_t>(un.tail) * 256 + (row - un.m0)) * 256 + (col0 - un.n0);
+#pragma unroll
+              for (int j = 0; j < 32; j += 4)
+                red_add_v4(a + j, __uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                           __uint_as_float(v[j + 3]));
+            } else {
               store_chunk(pr, row, col0, v);
               if (pr.epi == GEMM_EPI_ROWDOT) {
                 dot += chunk_rowdot(pr, row, col0, v);
@@ -788,6 +811,46 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
       atomicExch(&p.sched[1], 0u);
       __threadfence();
     }
+  }
+}
+
+// Finishes the split last-round tiles of one problem: C = acc + R, converted.
+struct TailFin {
+  int M, N, m_tiles, n_tiles, n_fast, whole;
+  const float* acc;
+  void* C;
+  int64_t ldc;
+  int c_f32;
+  const void* R;
+  int64_t ldr;
+  int r_f32;
+};
+__global__ void __launch_bounds__(256) gemm_tail_finalize_kernel(const TailFin f) {
+  const int t = blockIdx.x;                      // tail tile
+  const int tile = f.whole + t;
+  int m0, n0;
+  if (f.n_fast) {
+    n0 = (tile % f.n_tiles) * 256;
+    m0 = (tile / f.n_tiles) * 256;
+  } else {
+    m0 = (tile % f.m_tiles) * 256;
+    n0 = (tile / f.m_tiles) * 256;
+  }
+  const int r = blockIdx.y * 4 + (threadIdx.x >> 6);  // 4 rows per block, 64 threads x 4 columns per row
+  const int c = (threadIdx.x & 63) * 4;
+  const int row = m0 + r;
+  if (row >= f.M) return;
+  const float4 a = *reinterpret_cast<const float4*>(f.acc + (static_cast<int64_t>(t) * 256 + r) * 256 + c);
+  const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int col = n0 + c + e;
+    if (col >= f.N) break;
+    float v = av[e];
+    if (f.R) v += f.r_f32 ? static_cast<const float*>(f.R)[row * f.ldr + col]
+                          : __bfloat162float(static_cast<const __nv_bfloat16*>(f.R)[row * f.ldr + col]);
+    if (f.c_f32) static_cast<float*>(f.C)[row * f.ldc + col] = v;
+    else static_cast<__nv_bfloat16*>(f.C)[row * f.ldc + col] = __float2bfloat16_rn(v);
   }
 }
 
@@ -1108,11 +1171,6 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
     bytes += 2.0 * (s.M + nmul * s.N) * ksum + static_cast<double>(s.M) * s.N * dtype_size(s.c_dtype) * (1.0 + extra) +
              (s.R ? static_cast<double>(s.M) * s.N * dtype_size(s.r_dtype) : 0.0);
   }
-  p.nprob = nspec;
-  p.total_units = units;
-  p.sched = sched_slot_ptr();
-  if (!p.sched) return set_error(KL_ERR_CUDA, "gemm: scheduler counters unavailable");
-  p.err = device_error_word();
   static uint64_t attr_done = 0;  // one bit per device ordinal
   int dev = 0;
   KL_CUDA(cudaGetDevice(&dev));
@@ -1121,25 +1179,69 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
                                  static_cast<int>(SMEM2_BYTES)));
     attr_done |= uint64_t(1) << dev;
   }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = GEMM_CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(PAIR_THREADS);
+  cfg.dynamicSmemBytes = SMEM2_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int cap = max_gemm_clusters(dev, cfg);
+  // Last round: if the units leave some CTA pairs idle in the last round, split
+  // the last problem's last tiles along K so that the round's work spreads
+  // over every pair (accumulated in tail_ws, finished below).
+  int tail_prob = -1;
+  {
+    const int lp = nspec - 1;
+    GemmProb& pr = p.prob[lp];
+    const GemmSpec& s = specs_in[order[lp]];
+    const int tiles = pr.m_tiles * pr.n_tiles;
+    const int rem = units % cap;
+    if (units > cap && rem > 0 && s.tail_ws && pr.splits == 1 && pr.epi == GEMM_EPI_STORE && rem <= tiles &&
+        pr.n_step == 256 && (reinterpret_cast<uintptr_t>(s.tail_ws) & 15u) == 0) {
+      int ts = cap / rem;
+      const int max_ts = pr.kb_total / 8;            // at least 8 k-blocks per piece
+      if (ts > max_ts) ts = max_ts;
+      const size_t need = static_cast<size_t>(rem) * 256 * 256 * 4;
+      if (ts >= 2 && need <= s.tail_ws_bytes) {
+        pr.whole_tiles = tiles - rem;
+        pr.tail_tiles = rem;
+        pr.tail_splits = ts;
+        pr.tail_acc = s.tail_ws;
+        units += rem * (ts - 1);
+        tail_prob = lp;
+        KL_CUDA(cudaMemsetAsync(s.tail_ws, 0, need, st));
+      }
+    }
+  }
+  p.nprob = nspec;
+  p.total_units = units;
+  p.sched = sched_slot_ptr();
+  if (!p.sched) return set_error(KL_ERR_CUDA, "gemm: scheduler counters unavailable");
+  p.err = device_error_word();
   {
     ProfScope ps(label, st, flops, bytes);
-    {
-      cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = GEMM_CL;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.blockDim = dim3(PAIR_THREADS);
-      cfg.dynamicSmemBytes = SMEM2_BYTES;
-      cfg.stream = st;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      const int cap = max_gemm_clusters(dev, cfg);
-      const int clusters = units < cap ? units : cap;
-      cfg.gridDim = dim3(GEMM_CL * clusters);
-      KL_CUDA(cudaLaunchKernelEx(&cfg, gemm_bf16_tcp_kernel, p));
-    }
+    const int clusters = units < cap ? units : cap;
+    cfg.gridDim = dim3(GEMM_CL * clusters);
+    KL_CUDA(cudaLaunchKernelEx(&cfg, gemm_bf16_tcp_kernel, p));
+  }
+  KL_CUDA(cudaGetLastError());
+  if (tail_prob >= 0) {
+    const GemmProb& pr = p.prob[tail_prob];
+    const GemmSpec& s = specs_in[order[tail_prob]];
+    TailFin f;
+    f.M = pr.M; f.N = pr.N; f.m_tiles = pr.m_tiles; f.n_tiles = pr.n_tiles; f.n_fast = pr.n_fast;
+    f.whole = pr.whole_tiles; f.acc = pr.tail_acc;
+    f.C = s.C; f.ldc = s.ldc; f.c_f32 = s.c_dtype == KL_F32;
+    f.R = s.R; f.ldr = s.ldr; f.r_f32 = s.r_dtype == KL_F32;
+    const double n = static_cast<double>(pr.tail_tiles) * 256 * 256;
+    ProfScope ps("gemm_tail_finalize", st, 0.0, n * (4 + dtype_size(s.c_dtype) + (s.R ? dtype_size(s.r_dtype) : 0)));
+    gemm_tail_finalize_kernel<<<dim3(pr.tail_tiles, 64), 256, 0, st>>>(f);
+    KL_CUDA(cudaGetLastError());
   }
   KL_CUDA(cudaGetLastError());
   for (int i = 0; i < nspec; ++i) {
@@ -1153,6 +1255,8 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
   }
   return KL_OK;
 }
+
+size_t gemm_tail_ws_bytes() { return align_up(static_cast<size_t>(num_sms() / GEMM_CL) * 256 * 256 * 4, 256); }
 
 kl_status gemm_f32(const GemmSpec& s, cudaStream_t st, const char* label) {
   if (s.M < 1 || s.N < 1 || s.nseg < 1 || s.nseg > GEMM_MAX_SEG || !s.C)

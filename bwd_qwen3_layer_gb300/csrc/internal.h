@@ -46,6 +46,13 @@ struct GemmSpec {
   //                        dot_out[(b * N/128 + h) * dot_S + t] = sum over the
   //                        128 columns of head h of bf16(C) * O for token row
   //                        b * dot_S + t (N a multiple of 128).
+  // Optional compact fp32 scratch for the last round of the launch: when the
+  // launch's work leaves its last round of CTA pairs partly idle, the last
+  // tiles of the last problem (in execution order) are split along K,
+  // accumulated here ([tiles][256][256] fp32) and finished after the launch
+  // (residual added, converted). Plain-store problems only.
+  float* tail_ws = nullptr;
+  size_t tail_ws_bytes = 0;
   int epi = 0;
   const void* B2 = nullptr;
   void* C2 = nullptr;
@@ -55,6 +62,9 @@ struct GemmSpec {
   float* dot_out = nullptr;
   int dot_S = 0;
 };
+// Bytes of tail_ws that let every launch split its last round (at most one
+// 256 x 256 fp32 tile per CTA pair of the device).
+size_t gemm_tail_ws_bytes();
 constexpr int GEMM_EPI_STORE = 0;
 constexpr int GEMM_EPI_SWIGLU = 1;
 constexpr int GEMM_EPI_SWIGLU_BWD = 2;

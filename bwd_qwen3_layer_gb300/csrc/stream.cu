@@ -452,7 +452,8 @@ kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets, flo
       KL_TRY(acquire(s, l + 1, cur, &nxt));  // prefetch while layer l runs
     }
     const void* xin = l == 0 ? X : s->hidden[l - 1];
-    KL_TRY(kl_layer_forward(&c, &w, xin, s->hidden[l], &s->saved[l], nullptr, 0, cs));
+    // the backward workspace is idle during the forward pass: it serves as the forward's
+    KL_TRY(kl_layer_forward(&c, &w, xin, s->hidden[l], &s->saved[l], s->bwd_ws, s->bwd_ws_bytes, cs));
     if (!s->bulk) KL_CUDA(cudaEventRecord(s->ev_used[cur], cs));
   }
   // ---------------- lm-head ----------------

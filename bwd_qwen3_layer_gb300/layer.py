@@ -6,7 +6,7 @@ from __future__ import annotations
 import torch
 
 from . import (KL_BF16, KL_F32, LayerCfg, LayerGrads, LayerWeights, LmheadCfg, WEIGHT_FIELDS,
-               kl_layer_bwd_workspace_bytes, kl_layer_saved_bytes, kl_layer_saved_carve,
+               kl_layer_bwd_workspace_bytes, kl_layer_fwd_workspace_bytes, kl_layer_saved_bytes, kl_layer_saved_carve,
                kl_lmhead_workspace_bytes)
 
 TORCH_DTYPE = {KL_F32: torch.float32, KL_BF16: torch.bfloat16}
@@ -45,7 +45,7 @@ class LayerBuffers:
         nb = kl_layer_saved_bytes(cfg)
         self.saved_mem = torch.empty(nb, dtype=torch.uint8, device=device)
         self.saved = kl_layer_saved_carve(cfg, self.saved_mem.data_ptr(), nb)
-        self.fwd_ws = torch.empty(256, dtype=torch.uint8, device=device)
+        self.fwd_ws = torch.empty(max(256, kl_layer_fwd_workspace_bytes(cfg)), dtype=torch.uint8, device=device)
         nb = kl_layer_bwd_workspace_bytes(cfg)
         self.bwd_ws = torch.empty(nb, dtype=torch.uint8, device=device)
 

@@ -159,7 +159,9 @@ KL_API size_t kl_layer_saved_bytes(const kl_layer_cfg* cfg);
 KL_API kl_status kl_layer_saved_carve(const kl_layer_cfg* cfg, void* base, size_t bytes,
                                kl_layer_saved* out);
 /* Workspace bytes of the forward and the backward (device, caller-owned,
- * 256-byte aligned; contents undefined between calls). */
+ * 256-byte aligned; contents undefined between calls). The forward's
+ * workspace is optional (ws may be NULL): with it, the projections' last
+ * round of tiles is split along K over every CTA pair. */
 KL_API size_t kl_layer_fwd_workspace_bytes(const kl_layer_cfg* cfg);
 KL_API size_t kl_layer_bwd_workspace_bytes(const kl_layer_cfg* cfg);
 
