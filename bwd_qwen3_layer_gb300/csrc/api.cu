@@ -156,6 +156,9 @@ void carve_saved(const Dims& D, Carver& c, kl_layer_saved* s) {
   s->m = c.take(T * D.I * es);
 }
 
+// The rotary (cos, sin) table [S][d/2] used by the fused q/k projection and dQ epilogues.
+size_t rope_table_bytes(const Dims& D) { return align_up(static_cast<size_t>(D.S) * (D.d / 2) * 8, 256); }
+
 struct BwdWs {
   void *dm, *dg, *du, *dx2, *dO, *dq, *dk, *dv;
   float *dh2, *dh1;
@@ -165,6 +168,7 @@ struct BwdWs {
   size_t norm_bytes;
   void* tail;             // fp32 scratch balancing the GEMM launches' last rounds (bf16)
   size_t tail_bytes;
+  float2* rope;           // rotary (cos, sin) table [S][d/2] for the fused dQ rotation (bf16)
 };
 
 void carve_bwd(const Dims& D, Carver& c, BwdWs* w) {
@@ -185,6 +189,7 @@ void carve_bwd(const Dims& D, Carver& c, BwdWs* w) {
   w->norm = c.take(w->norm_bytes);
   w->tail_bytes = D.dt == KL_BF16 ? gemm_tail_ws_bytes() : 0;
   w->tail = w->tail_bytes ? c.take(w->tail_bytes) : nullptr;
+  w->rope = D.dt == KL_BF16 ? static_cast<float2*>(c.take(rope_table_bytes(D))) : nullptr;
 }
 
 kl_status check_ptrs(std::initializer_list<const void*> ptrs, const char* what) {
@@ -259,7 +264,7 @@ kl_status kl_layer_saved_carve(const kl_layer_cfg* cfg, void* base, size_t bytes
 size_t kl_layer_fwd_workspace_bytes(const kl_layer_cfg* cfg) {
   Dims D;
   if (check_cfg(cfg, &D) != KL_OK) return 0;
-  return D.dt == KL_BF16 ? gemm_tail_ws_bytes() : 256;
+  return D.dt == KL_BF16 ? gemm_tail_ws_bytes() + rope_table_bytes(D) : 256;
 }
 
 size_t kl_layer_bwd_workspace_bytes(const kl_layer_cfg* cfg) {
@@ -290,20 +295,33 @@ kl_status kl_layer_forward(const kl_layer_cfg* cfg, const kl_layer_weights* w, c
                      s->g, s->u, s->m}, "layer_forward buffers"));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int T = D.T, H = D.H, I = D.I, dt = D.dt;
+  // bf16 with the full workspace: tail scratch + rotary table, rotation fused into q/k
+  const bool fused = dt == KL_BF16 && ws && ws_bytes >= kl_layer_fwd_workspace_bytes(cfg) &&
+                     (reinterpret_cast<uintptr_t>(ws) & 255u) == 0;
+  const size_t tail_bytes = fused ? gemm_tail_ws_bytes() : 0;
+  float2* rope_tab = fused ? reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + tail_bytes) : nullptr;
   s->x = X;
   KL_TRY(rmsnorm_fwd(T, H, dt, X, w->gamma1, cfg->eps, s->h1, s->rstd1, st));
+  if (fused) KL_TRY(rope_cs_table(D.S, D.d, cfg->rope_base, rope_tab, st));
   {
     GemmSpec g[3] = {proj(T, D.Dq, H, s->h1, H, w->wq, H, s->q, D.Dq, dt),
                      proj(T, D.Dkv, H, s->h1, H, w->wk, H, s->k, D.Dkv, dt),
                      proj(T, D.Dkv, H, s->h1, H, w->wv, H, s->v, D.Dkv, dt)};
-    with_tail(g, 3, ws, ws_bytes);
+    if (fused) {
+      with_tail(g, 3, ws, tail_bytes);
+      for (int i = 0; i < 2; ++i) {   // q and k leave the epilogue rotated
+        g[i].epi = GEMM_EPI_ROPE;
+        g[i].rope_cs = rope_tab;
+        g[i].rope_S = D.S;
+      }
+    }
     KL_TRY(run_gemms(dt, g, 3, st, "gemm.fwd_qkv"));
   }
-  KL_TRY(rope_qk(D.B, D.S, D.Hq, D.Hkv, D.d, cfg->rope_base, dt, s->q, s->k, 1, st));
+  if (!fused) KL_TRY(rope_qk(D.B, D.S, D.Hq, D.Hkv, D.d, cfg->rope_base, dt, s->q, s->k, 1, st));
   KL_TRY(attention_fwd(D.B, D.S, D.Hq, D.Hkv, D.d, dt, s->q, s->k, s->v, s->o, s->lse, st));
   {
     GemmSpec g = proj(T, H, D.Dq, s->o, D.Dq, w->wo, D.Dq, s->x2, H, dt, X, dt);
-    with_tail(&g, 1, ws, ws_bytes);
+    if (fused) with_tail(&g, 1, ws, tail_bytes);
     KL_TRY(run_gemms(dt, &g, 1, st, "gemm.fwd_o"));
   }
   KL_TRY(rmsnorm_fwd(T, H, dt, s->x2, w->gamma2, cfg->eps, s->h2, s->rstd2, st));
@@ -323,7 +341,7 @@ kl_status kl_layer_forward(const kl_layer_cfg* cfg, const kl_layer_weights* w, c
   }
   {
     GemmSpec g = proj(T, H, I, s->m, I, w->wd, I, Y, H, dt, s->x2, dt);
-    with_tail(&g, 1, ws, ws_bytes);
+    if (fused) with_tail(&g, 1, ws, tail_bytes);
     KL_TRY(run_gemms(dt, &g, 1, st, "gemm.fwd_down"));
   }
   return KL_OK;
@@ -395,10 +413,14 @@ kl_status kl_layer_backward(const kl_layer_cfg* cfg, const kl_layer_weights* w,
     KL_TRY(run_gemms(dt, g, 2, st, "gemm.bwd_o"));
   }
   float *dq_acc = nullptr, *dk_acc = nullptr, *dv_acc = nullptr;
+  // bf16: dQ leaves the attention kernel rotated back and converted; dK, dV (summed
+  // over each kv head's query heads) are finished below
+  if (b.rope) KL_TRY(rope_cs_table(D.S, D.d, cfg->rope_base, b.rope, st));
   KL_TRY(attention_bwd_accum(D.B, D.S, D.Hq, D.Hkv, D.d, dt, s->q, s->k, s->v, s->o, s->lse, b.dO,
-                             b.att, b.att_bytes, &dq_acc, &dk_acc, &dv_acc, st, d_ready));
-  KL_TRY(rope_bwd_convert(D.B, D.S, D.Hq, D.Hkv, D.d, cfg->rope_base, dt, dq_acc, dk_acc, dv_acc, b.dq,
-                          b.dk, b.dv, st));
+                             b.att, b.att_bytes, &dq_acc, &dk_acc, &dv_acc, st, d_ready,
+                             b.rope ? b.dq : nullptr, b.rope));
+  KL_TRY(rope_bwd_convert(D.B, D.S, dq_acc ? D.Hq : 0, D.Hkv, D.d, cfg->rope_base, dt, dq_acc, dk_acc, dv_acc,
+                          b.dq, b.dk, b.dv, st));
   {
     GemmSpec dh = dgrad(T, H, D.Dq, b.dq, w->wq, b.dh1, KL_F32);
     dh.nseg = 3;
@@ -558,9 +580,9 @@ kl_status kl_attention_bwd(int32_t B, int32_t S, int32_t Hq, int32_t Hkv, int32_
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float *dq_acc = nullptr, *dk_acc = nullptr, *dv_acc = nullptr;
   KL_TRY(attention_bwd_accum(B, S, Hq, Hkv, d, dtype, q, k, v, o, lse, dout, ws, ws_bytes, &dq_acc,
-                             &dk_acc, &dv_acc, st));
+                             &dk_acc, &dv_acc, st, false, dtype == KL_BF16 ? dq : nullptr));
   const int64_t T = static_cast<int64_t>(B) * S;
-  KL_TRY(convert_f32(T * Hq * d, dtype, dq_acc, dq, st));
+  if (dq_acc) KL_TRY(convert_f32(T * Hq * d, dtype, dq_acc, dq, st));
   KL_TRY(convert_f32(T * Hkv * d, dtype, dk_acc, dk, st));
   KL_TRY(convert_f32(T * Hkv * d, dtype, dv_acc, dv, st));
   return KL_OK;

@@ -698,7 +698,7 @@ kl_status attention_bwd_accum(int B, int S, int Hq, int Hkv, int d, int dtype, c
                               const void* k, const void* v, const void* o, const float* lse,
                               const void* dout, void* ws, size_t ws_bytes, float** dq_acc,
                               float** dk_acc, float** dv_acc, cudaStream_t st,
-                              bool d_ready) {
+                              bool d_ready, void* dq_out, const float2* rope_cs) {
   KL_TRY(check_args(B, S, Hq, Hkv, d, dtype));
   if (!q || !k || !v || !o || !lse || !dout)
     return set_error(KL_ERR_INVALID_ARG, "attention_bwd: null pointer");
@@ -743,7 +743,9 @@ kl_status attention_bwd_accum(int B, int S, int Hq, int Hkv, int d, int dtype, c
           B, S, Hq, (const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, Dd);
       KL_CUDA(cudaGetLastError());
     }
-    KL_TRY(attention_bwd_tc(B, S, Hq, Hkv, q, k, v, dout, lse, Dd, dq, dk, dv, st));
+    if (dq_out && !al16(dq_out)) return set_error(KL_ERR_INVALID_ARG, "attention_bwd: dq not 16-byte aligned");
+    KL_TRY(attention_bwd_tc(B, S, Hq, Hkv, q, k, v, dout, lse, Dd, dq, dk, dv, st, dq_out, rope_cs));
+    if (dq_out) *dq_acc = nullptr;
   }
   KL_CUDA(cudaGetLastError());
   return KL_OK;

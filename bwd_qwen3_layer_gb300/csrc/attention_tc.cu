@@ -383,7 +383,9 @@ struct BwdParams {
   CUtensorMap tmQ, tmK, tmV, tmdO;   // box rows: see the kernels
   const float* lse;                  // [B, Hq, S]
   const float* Dd;                   // [B, Hq, S]
-  float* dq_acc;                     // [T, Hq*128]
+  float* dq_acc;                     // [T, Hq*128] fp32 (when dq_out is null)
+  __nv_bfloat16* dq_out;             // [T, Hq*128] bf16 final dQ, or null
+  const float2* rope_cs;             // [S][64] cos/sin: dQ turned back by -angle (with dq_out), or null
   float* dk_acc;                     // [T, Hkv*128]
   float* dv_acc;                     // [T, Hkv*128]
   int S, Hq, Hkv;
@@ -863,7 +865,60 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dq_tc_kernel(const __grid_c
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full(s));
     }
-    if (ok && mbar_wait_warp(done, 0, p.err, abort_flag)) {
+    // the query's rotary cos/sin (planes 0..31) are fetched before the wait for the last MMA
+    const float2* cs = p.rope_cs ? p.rope_cs + static_cast<int64_t>(qrow < p.S ? qrow : 0) * 64 : nullptr;
+    float4 csn[16];
+    if (cs) {
+#pragma unroll
+      for (int e = 0; e < 16; ++e) csn[e] = reinterpret_cast<const float4*>(cs)[e];
+    }
+    const bool fin = ok && mbar_wait_warp(done, 0, p.err, abort_flag);
+    if (fin && p.dq_out) {
+      // bf16 dQ, turned back by the rotary angle of the query's position when a table is given
+      tc_fence_after();
+      __nv_bfloat16* orow = p.dq_out + (static_cast<int64_t>(row0 + qrow) * p.Hq + h) * HD;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t va[32], vb[32];   // planes 32c .. 32c+31 and their partners at +64
+        tmem_ld_32x32b_x32(tmem + lane_off + 256 + c * 32, va);
+        tmem_ld_32x32b_x32(tmem + lane_off + 256 + 64 + c * 32, vb);
+        tmem_ld_wait();
+        float4 csc[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) csc[e] = csn[e];
+        if (cs && c == 0) {   // planes 32..63 in flight while planes 0..31 are turned
+#pragma unroll
+          for (int e = 0; e < 16; ++e) csn[e] = reinterpret_cast<const float4*>(cs)[16 + e];
+        }
+        if (qrow < p.S) {
+          float xa[32], xb[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float x = __uint_as_float(va[e]) * p.scale, y = __uint_as_float(vb[e]) * p.scale;
+            if (cs) {
+              const float4 q4 = csc[e >> 1];
+              const float tc = (e & 1) ? q4.z : q4.x, ts = (e & 1) ? q4.w : q4.y;
+              xa[e] = x * tc + y * ts;
+              xb[e] = y * tc - x * ts;
+            } else {
+              xa[e] = x;
+              xb[e] = y;
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 wa, wb;
+            wa.x = pack_bf16x2(xa[e], xa[e + 1]); wa.y = pack_bf16x2(xa[e + 2], xa[e + 3]);
+            wa.z = pack_bf16x2(xa[e + 4], xa[e + 5]); wa.w = pack_bf16x2(xa[e + 6], xa[e + 7]);
+            wb.x = pack_bf16x2(xb[e], xb[e + 1]); wb.y = pack_bf16x2(xb[e + 2], xb[e + 3]);
+            wb.z = pack_bf16x2(xb[e + 4], xb[e + 5]); wb.w = pack_bf16x2(xb[e + 6], xb[e + 7]);
+            *reinterpret_cast<uint4*>(orow + c * 32 + e) = wa;
+            *reinterpret_cast<uint4*>(orow + 64 + c * 32 + e) = wb;
+          }
+        }
+      }
+    } else if (fin) {
+      // fp32 accumulator
       tc_fence_after();
       float* orow = p.dq_acc + (static_cast<int64_t>(row0 + qrow) * p.Hq + h) * HD;
 #pragma unroll
@@ -958,7 +1013,7 @@ namespace kl {
 
 kl_status attention_bwd_tc(int B, int S, int Hq, int Hkv, const void* q, const void* k, const void* v,
                            const void* dout, const float* lse, const float* Dd, float* dq_acc, float* dk_acc,
-                           float* dv_acc, cudaStream_t st) {
+                           float* dv_acc, cudaStream_t st, void* dq_out, const float2* rope_cs) {
   const uint64_t T = static_cast<uint64_t>(B) * S;
   static uint64_t attr_done = 0;
   int dev = 0;
@@ -975,6 +1030,8 @@ kl_status attention_bwd_tc(int B, int S, int Hq, int Hkv, const void* q, const v
   p.lse = lse;
   p.Dd = Dd;
   p.dq_acc = dq_acc;
+  p.dq_out = static_cast<__nv_bfloat16*>(dq_out);
+  p.rope_cs = dq_out ? rope_cs : nullptr;
   p.dk_acc = dk_acc;
   p.dv_acc = dv_acc;
   p.S = S;

@@ -474,6 +474,19 @@ __device__ __forceinline__ void rope_table(int s, int d, const RopeFreq& f, floa
   for (int i = threadIdx.x; i < half; i += blockDim.x) rope_cos_sin(s, f.inv[i], dir, &cs[i], &cs[half + i]);
 }
 
+// The (cos, sin) table of every position and plane: consumed by the fused
+// rotary epilogues of the q/k projection and of the attention dQ kernel.
+__global__ void rope_cs_kernel(int S, int half, RopeFreq f, float2* __restrict__ cs) {
+  const int64_t n = static_cast<int64_t>(S) * half;
+  for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
+       idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int s = static_cast<int>(idx / half), i = static_cast<int>(idx - static_cast<int64_t>(s) * half);
+    float c, sn;
+    rope_cos_sin(s, f.inv[i], 1.0f, &c, &sn);
+    cs[idx] = make_float2(c, sn);
+  }
+}
+
 template <typename T>
 __global__ void rope_kernel(int S, int heads, int d, RopeFreq f, T* __restrict__ x, float dir) {
   __shared__ float cs[2 * ROPE_MAX_HALF];
@@ -820,6 +833,17 @@ kl_status rope_qk(int B, int S, int hq, int hk, int d, float base, int dtype, vo
       else rope_kernel<float><<<T, 128, 0, st>>>(S, heads, d, f, (float*)x, dir);
     }
   }
+  KL_CUDA(cudaGetLastError());
+  return KL_OK;
+}
+
+kl_status rope_cs_table(int S, int d, float base, float2* cs, cudaStream_t st) {
+  if (S < 1 || d < 2 || (d & 1) || d / 2 > ROPE_MAX_HALF || !cs)
+    return set_error(KL_ERR_INVALID_ARG, "rope table: bad arguments");
+  const RopeFreq f = rope_freq(d, base);
+  const int64_t n = static_cast<int64_t>(S) * (d / 2);
+  ProfScope ps("rope_table", st, 0.0, 8.0 * n);
+  rope_cs_kernel<<<ew_grid(n), 256, 0, st>>>(S, d / 2, f, cs);
   KL_CUDA(cudaGetLastError());
   return KL_OK;
 }

@@ -65,6 +65,8 @@ struct GemmProb {
   const void* X2;
   float* dot_out;
   int dot_S;
+  const float2* rope_cs;  // GEMM_EPI_ROPE: [rope_S][64] cos/sin
+  int rope_S;
   int whole_tiles;        // tiles computed whole; the rest (tail) are split along K
   int tail_tiles, tail_splits;
   float* tail_acc;        // [tail_tiles][256][256] fp32
@@ -274,6 +276,23 @@ __device__ __forceinline__ void store_swiglu_bwd(const GemmProb& pr, int row, in
   }
   store_bf16x32(static_cast<__nv_bfloat16*>(pr.C) + o, vec, ncols, g);
   store_bf16x32(static_cast<__nv_bfloat16*>(pr.C2) + o, vec, ncols, u);
+}
+
+// GEMM_EPI_ROPE: planes 0..31 of a 32-column chunk (va) and their partners 64
+// columns on (vb), turned by the angles cs[0..31] of the row's position.
+__device__ __forceinline__ void store_rope(const GemmProb& pr, int row, int colA, const uint32_t (&va)[32],
+                                           const uint32_t (&vb)[32], const float2* cs) {
+  float xa[32], xb[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float2 t = cs[j];
+    const float x = __uint_as_float(va[j]), y = __uint_as_float(vb[j]);
+    xa[j] = x * t.x - y * t.y;
+    xb[j] = x * t.y + y * t.x;
+  }
+  __nv_bfloat16* c = static_cast<__nv_bfloat16*>(pr.C) + static_cast<int64_t>(row) * pr.ldc + colA;
+  store_bf16x32(c, pr.vec_ok, 32, xa);
+  store_bf16x32(c + 64, pr.vec_ok, 32, xb);
 }
 
 // GEMM_EPI_ROWDOT: sum over 32 columns of bf16(product) * X1.
@@ -753,6 +772,20 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
           tmem_ld_wait();
           if (row < pr.M) store_swiglu(pr, row, col0, vg, vu);
         }
+      } else if (pr.epi == GEMM_EPI_ROPE) {
+        // two heads of 128 columns; plane i pairs column i with i + 64 of its head
+        const float2* cs = pr.rope_cs + static_cast<int64_t>((row < pr.M ? row : 0) % pr.rope_S) * 64;
+        for (int hl = 0; hl < 2; ++hl) {
+          for (int c = 0; c < 2; ++c) {
+            const int colA = un.n0 + 128 * hl + 32 * c;
+            if (colA >= pr.N) break;
+            uint32_t va[32], vb[32];
+            tmem_ld_32x32b_x32(tacc + 128 * hl + 32 * c, va);
+            tmem_ld_32x32b_x32(tacc + 128 * hl + 64 + 32 * c, vb);
+            tmem_ld_wait();
+            if (row < pr.M) store_rope(pr, row, colA, va, vb, cs + 32 * c);
+          }
+        }
       } else {
         float dot = 0.f;
         for (int c = 0; c < 256 / 32; ++c) {
@@ -1072,8 +1105,10 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
       const bool bwd_ok = s.epi != GEMM_EPI_SWIGLU_BWD || (s.X1 && s.X2 && s.C2);
       const bool dot_ok = s.epi != GEMM_EPI_ROWDOT || (s.X1 && s.dot_out && s.dot_S > 0 && s.M % s.dot_S == 0 &&
                                                        s.N % 128 == 0);
-      if (s.epi > GEMM_EPI_ROWDOT || s.c_dtype != KL_BF16 || s.R || s.nseg != 1 || s.acc_ws || !pairs_ok ||
-          !bwd_ok || !dot_ok)
+      const bool rope_ok = s.epi != GEMM_EPI_ROPE || (s.rope_cs && s.rope_S > 0 && s.N % 128 == 0 &&
+                                                      aligned16(s.C) && s.ldc % 8 == 0);
+      if (s.epi > GEMM_EPI_ROPE || s.c_dtype != KL_BF16 || s.R || s.nseg != 1 || s.acc_ws || !pairs_ok ||
+          !bwd_ok || !dot_ok || !rope_ok)
         return set_error(KL_ERR_INVALID_ARG, "gemm: problem %d: bad epilogue variant %d", oi, s.epi);
     }
     if (tm + (glu ? 2 : s.nseg) > GEMM_MAX_PROB * GEMM_MAX_SEG)
@@ -1094,6 +1129,8 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
     pr.X2 = s.X2;
     pr.dot_out = s.dot_out;
     pr.dot_S = s.dot_S;
+    pr.rope_cs = s.rope_cs;
+    pr.rope_S = s.rope_S;
     double ksum = 0.0;
     for (int g = 0; g < s.nseg; ++g) {
       if (!s.A[g] || !s.B[g] || s.K[g] < 1)

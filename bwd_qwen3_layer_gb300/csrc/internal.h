@@ -61,6 +61,10 @@ struct GemmSpec {
   const void* X2 = nullptr;
   float* dot_out = nullptr;
   int dot_S = 0;
+  // GEMM_EPI_ROPE: columns are heads of 128; the pair (i, i + 64) of each head
+  // is turned by the angle of token row % rope_S, cos/sin from rope_cs[pos][64].
+  const float2* rope_cs = nullptr;
+  int rope_S = 0;
 };
 // Bytes of tail_ws that let every launch split its last round (at most one
 // 256 x 256 fp32 tile per CTA pair of the device).
@@ -69,6 +73,7 @@ constexpr int GEMM_EPI_STORE = 0;
 constexpr int GEMM_EPI_SWIGLU = 1;
 constexpr int GEMM_EPI_SWIGLU_BWD = 2;
 constexpr int GEMM_EPI_ROWDOT = 3;
+constexpr int GEMM_EPI_ROPE = 4;
 
 // bf16 operands on the tcgen05 tensor cores; up to GEMM_MAX_PROB independent
 // problems share one persistent launch.
@@ -87,6 +92,8 @@ kl_status rmsnorm_bwd(int rows, int width, int dtype, const void* dh, int dh_dty
                       float* dgamma, void* ws, size_t ws_bytes, cudaStream_t st);
 kl_status rope(int B, int S, int heads, int d, float base, int dtype, void* x, int direction,
                cudaStream_t st);
+// cs[s * d/2 + i] = (cos, sin) of the angle s * base^(-2i/d), s < S (d/2 <= 128).
+kl_status rope_cs_table(int S, int d, float base, float2* cs, cudaStream_t st);
 // q [T, hq, d] and k [T, hk, d] rotated in place in one launch (hk may be 0).
 kl_status rope_qk(int B, int S, int hq, int hk, int d, float base, int dtype, void* q, void* k,
                   int direction, cudaStream_t st);
@@ -112,10 +119,14 @@ kl_status attention_fwd_tc(int B, int S, int Hq, int Hkv, const void* q, const v
 // accumulated (zeroed by the caller).
 kl_status attention_bwd_tc(int B, int S, int Hq, int Hkv, const void* q, const void* k, const void* v,
                            const void* dout, const float* lse, const float* Dd, float* dq_acc, float* dk_acc,
-                           float* dv_acc, cudaStream_t st);
+                           float* dv_acc, cudaStream_t st,
+                           void* dq_out = nullptr, const float2* rope_cs = nullptr);
 size_t attention_bwd_ws(int B, int S, int Hq, int Hkv, int d);
 // dq_out/dk_out/dv_out: fp32 accumulators [T,H*d] written by the kernel
-// (inside ws); the caller converts (with rotary backward) afterwards. The
+// (inside ws); the caller converts (with rotary backward) afterwards. With
+// dq_out (bf16, tensor-core path) dQ is written there directly instead, turned
+// back by the rotary angles of rope_cs ([S][d/2] cos/sin) when that is given,
+// and *dq_acc is null. The
 // workspace starts with D = rowsum(dO * O) as fp32 [B, Hq, S]; d_ready (bf16)
 // means the caller has already written it there (attention_bwd_d_rows).
 inline float* attention_bwd_d_rows(void* ws) { return static_cast<float*>(ws); }
@@ -123,7 +134,8 @@ kl_status attention_bwd_accum(int B, int S, int Hq, int Hkv, int d, int dtype, c
                               const void* k, const void* v, const void* o, const float* lse,
                               const void* dout, void* ws, size_t ws_bytes, float** dq_acc,
                               float** dk_acc, float** dv_acc, cudaStream_t st,
-                              bool d_ready = false);
+                              bool d_ready = false, void* dq_out = nullptr,
+                              const float2* rope_cs = nullptr);
 
 // ---------------------------------------------------------------------------
 // cross entropy (ce.cu)
