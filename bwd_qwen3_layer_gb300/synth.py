@@ -148,9 +148,14 @@ def layer_weight_shapes(H: int, Hq: int, Hkv: int, d: int, I: int) -> dict:
 
 
 def layer_weights(seed: int, H: int, Hq: int, Hkv: int, d: int, I: int,
-                  bf16: bool = False, prefix: str = "layer0") -> dict:
+                  bf16: bool = False, prefix: str = "layer0", qk_norm: bool = False) -> dict:
+    """Projection weights N(0, 0.02) [out, in]; norm gains 1 + N(0, 0.02);
+    with qk_norm also the per-head q/k gains gamma_q, gamma_k of length d."""
     out = {}
-    for name, shape in layer_weight_shapes(H, Hq, Hkv, d, I).items():
+    shapes = layer_weight_shapes(H, Hq, Hkv, d, I)
+    if qk_norm:
+        shapes = dict(shapes, gamma_q=(d,), gamma_k=(d,))
+    for name, shape in shapes.items():
         if name.startswith("gamma"):
             w = normal(seed, f"{prefix}.{name}", shape, std=0.02, mean=1.0)
         else:

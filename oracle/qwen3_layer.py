@@ -28,6 +28,12 @@ class LayerConfig:
     I: int
     eps: float = 1e-6
     rope_base: float = 1e6
+    # Options beyond the pages' layer (whose "10 of 10 tensors" count implies
+    # neither): Qwen3's per-head RMSNorm of q and k before the rotation (gains
+    # gamma_q, gamma_k of length d shared by all heads), and rotary planes of
+    # adjacent pairs (2i, 2i+1) instead of (i, i + d/2).
+    qk_norm: bool = False
+    rope_interleaved: bool = False
 
     @property
     def T(self) -> int:
@@ -91,25 +97,33 @@ def rope_angles(S: int, d: int, base: float) -> np.ndarray:
     return np.arange(S, dtype=np.float64)[:, None] * freq[None, :]
 
 
-def _rope_rotate(x: np.ndarray, B: int, S: int, base: float, sign: float) -> np.ndarray:
+def _rope_rotate(x: np.ndarray, B: int, S: int, base: float, sign: float,
+                 interleaved: bool = False) -> np.ndarray:
     x = np.asarray(x, np.float64)
     T, nh, d = x.shape
     assert T == B * S
     ang = sign * rope_angles(S, d, base)                      # [S, d/2]
     c = np.tile(np.cos(ang), (B, 1))[:, None, :]              # [T, 1, d/2]
     s = np.tile(np.sin(ang), (B, 1))[:, None, :]
-    a, b = x[..., : d // 2], x[..., d // 2:]
+    if interleaved:                                           # plane i = (x_2i, x_2i+1)
+        a, b = x[..., 0::2], x[..., 1::2]
+        y = np.empty_like(x)
+        y[..., 0::2] = a * c - b * s
+        y[..., 1::2] = a * s + b * c
+        return y
+    a, b = x[..., : d // 2], x[..., d // 2:]                  # plane i = (x_i, x_i+d/2)
     return np.concatenate([a * c - b * s, a * s + b * c], axis=-1)
 
 
-def rope_fwd(x: np.ndarray, B: int, S: int, base: float) -> np.ndarray:
-    """Rotate each (x_i, x_{i+d/2}) plane by +angle[s, i]; x is [T, heads, d]."""
-    return _rope_rotate(x, B, S, base, +1.0)
+def rope_fwd(x: np.ndarray, B: int, S: int, base: float, interleaved: bool = False) -> np.ndarray:
+    """Rotate each plane by +angle[s, i]; x is [T, heads, d]. Plane i is
+    (x_i, x_{i+d/2}), or (x_{2i}, x_{2i+1}) when interleaved."""
+    return _rope_rotate(x, B, S, base, +1.0, interleaved)
 
 
-def rope_bwd(dy: np.ndarray, B: int, S: int, base: float) -> np.ndarray:
+def rope_bwd(dy: np.ndarray, B: int, S: int, base: float, interleaved: bool = False) -> np.ndarray:
     """Gradient of rope_fwd: the rotation is orthogonal, so rotate by -angle."""
-    return _rope_rotate(dy, B, S, base, -1.0)
+    return _rope_rotate(dy, B, S, base, -1.0, interleaved)
 
 
 # ----------------------------------------------------------------------------
@@ -259,8 +273,15 @@ def layer_forward(cfg: LayerConfig, w: dict, X: np.ndarray):
     q = linear(h1, w["Wq"]).reshape(T, Hq, d)
     k = linear(h1, w["Wk"]).reshape(T, Hkv, d)
     v = linear(h1, w["Wv"]).reshape(T, Hkv, d)
-    qr = rope_fwd(q, cfg.B, cfg.S, cfg.rope_base)
-    kr = rope_fwd(k, cfg.B, cfg.S, cfg.rope_base)
+    extra = {}
+    if cfg.qk_norm:
+        # each head's d features normalised like the pre-norm RMSNorm, one gain per feature
+        qn, rstd_q = rmsnorm_fwd(q, w["gamma_q"], cfg.eps)
+        kn, rstd_k = rmsnorm_fwd(k, w["gamma_k"], cfg.eps)
+        extra = dict(q_pre=q.reshape(T, Hq * d), k_pre=k.reshape(T, Hkv * d), rstd_q=rstd_q, rstd_k=rstd_k)
+        q, k = qn, kn
+    qr = rope_fwd(q, cfg.B, cfg.S, cfg.rope_base, cfg.rope_interleaved)
+    kr = rope_fwd(k, cfg.B, cfg.S, cfg.rope_base, cfg.rope_interleaved)
     O, lse = attention_fwd(qr, kr, v, cfg.B, cfg.S)
     O2 = O.reshape(T, Hq * d)
     x2 = X + linear(O2, w["Wo"])
@@ -270,13 +291,14 @@ def layer_forward(cfg: LayerConfig, w: dict, X: np.ndarray):
     m = swiglu_fwd(g, u)
     Y = x2 + linear(m, w["Wd"])
     saved = dict(X=X, h1=h1, rstd1=rstd1, q=qr, k=kr, v=v, o=O2, lse=lse,
-                 x2=x2, h2=h2, rstd2=rstd2, g=g, u=u, m=m)
+                 x2=x2, h2=h2, rstd2=rstd2, g=g, u=u, m=m, **extra)
     return Y, saved
 
 
 def layer_backward(cfg: LayerConfig, w: dict, saved: dict, dY: np.ndarray):
     """Backward of layer_forward. Returns (dX, grads) with grads keyed like the
-    weights: gamma1, Wq, Wk, Wv, Wo, gamma2, Wg, Wu, Wd."""
+    weights: gamma1, Wq, Wk, Wv, Wo, gamma2, Wg, Wu, Wd (and gamma_q, gamma_k
+    with qk_norm)."""
     T, Hq, Hkv, d = cfg.T, cfg.Hq, cfg.Hkv, cfg.d
     dY = np.asarray(dY, np.float64)
     s = saved
@@ -293,8 +315,14 @@ def layer_backward(cfg: LayerConfig, w: dict, saved: dict, dY: np.ndarray):
     dO = (dx2 @ w["Wo"]).reshape(T, Hq, d)
     dWo = dx2.T @ s["o"]
     dqr, dkr, dv = attention_bwd(s["q"], s["k"], s["v"], dO, cfg.B, cfg.S)
-    dq = rope_bwd(dqr, cfg.B, cfg.S, cfg.rope_base).reshape(T, Hq * d)
-    dk = rope_bwd(dkr, cfg.B, cfg.S, cfg.rope_base).reshape(T, Hkv * d)
+    dq = rope_bwd(dqr, cfg.B, cfg.S, cfg.rope_base, cfg.rope_interleaved)
+    dk = rope_bwd(dkr, cfg.B, cfg.S, cfg.rope_base, cfg.rope_interleaved)
+    qk_grads = {}
+    if cfg.qk_norm:
+        dq, qk_grads["gamma_q"] = rmsnorm_bwd(dq, s["q_pre"].reshape(T, Hq, d), w["gamma_q"], s["rstd_q"])
+        dk, qk_grads["gamma_k"] = rmsnorm_bwd(dk, s["k_pre"].reshape(T, Hkv, d), w["gamma_k"], s["rstd_k"])
+    dq = dq.reshape(T, Hq * d)
+    dk = dk.reshape(T, Hkv * d)
     dv = dv.reshape(T, Hkv * d)
     dh1 = dq @ w["Wq"] + dk @ w["Wk"] + dv @ w["Wv"]
     dWq = dq.T @ s["h1"]
@@ -303,7 +331,7 @@ def layer_backward(cfg: LayerConfig, w: dict, saved: dict, dY: np.ndarray):
     dX_n, dgamma1 = rmsnorm_bwd(dh1, s["X"], w["gamma1"], s["rstd1"])
     dX = dx2 + dX_n
     grads = dict(gamma1=dgamma1, Wq=dWq, Wk=dWk, Wv=dWv, Wo=dWo,
-                 gamma2=dgamma2, Wg=dWg, Wu=dWu, Wd=dWd)
+                 gamma2=dgamma2, Wg=dWg, Wu=dWu, Wd=dWd, **qk_grads)
     inter = dict(dm=dm, dg=dg, du=du, dh2=dh2, dx2=dx2, dO=dO.reshape(T, Hq * d),
                  dq=dq, dk=dk, dv=dv, dh1=dh1)
     return dX, grads, inter

@@ -104,8 +104,8 @@ def test_ce_fd():
         assert _close(fd, np.sum(r["dW"] * v))
 
 
-def _layer_fd_check(cfg, seed, ndir=2):
-    w = synth.layer_weights(seed, cfg.H, cfg.Hq, cfg.Hkv, cfg.d, cfg.I)
+def _layer_fd_check(cfg, seed, ndir=2, h=1e-5, h_for=None):
+    w = synth.layer_weights(seed, cfg.H, cfg.Hq, cfg.Hkv, cfg.d, cfg.I, qk_norm=cfg.qk_norm)
     inp = synth.layer_inputs(seed, cfg.T, cfg.H)
     X, dY = inp["X"], inp["dY"]
     Y, saved = O.layer_forward(cfg, w, X)
@@ -116,15 +116,16 @@ def _layer_fd_check(cfg, seed, ndir=2):
 
     for _ in range(ndir):
         v = _rand(*X.shape)
-        assert _close(_fd_dir(L_x, X, v, h=1e-5), np.sum(dX * v), rtol=2e-6)
-    for name in synth.LAYER_WEIGHT_NAMES:
+        assert _close(_fd_dir(L_x, X, v, h=h), np.sum(dX * v), rtol=2e-6)
+    assert set(grads) == set(w)
+    for name in w:
         def L_w(t, name=name):
             ww = dict(w)
             ww[name] = t
             return np.sum(O.layer_forward(cfg, ww, X)[0] * dY)
         for _ in range(ndir):
             v = _rand(*w[name].shape)
-            fd = _fd_dir(L_w, w[name], v, h=1e-5)
+            fd = _fd_dir(L_w, w[name], v, h=(h_for or {}).get(name, h))
             assert _close(fd, np.sum(grads[name] * v), rtol=2e-6), name
     return grads
 
@@ -132,6 +133,18 @@ def _layer_fd_check(cfg, seed, ndir=2):
 def test_layer_fd_tiny():
     cfg = O.LayerConfig(B=2, S=3, H=8, Hq=4, Hkv=2, d=4, I=12, eps=1e-6, rope_base=1e4)
     _layer_fd_check(cfg, seed=7, ndir=3)
+
+
+@pytest.mark.parametrize("qk_norm,interleaved", [(True, False), (False, True), (True, True)])
+def test_layer_fd_qk_norm_and_interleaved_rope(qk_norm, interleaved):
+    """The per-head q/k RMSNorm (gains gamma_q, gamma_k) and the interleaved
+    rotary pairing: every gradient, dX and both new gains, against FD."""
+    cfg = O.LayerConfig(B=2, S=3, H=8, Hq=4, Hkv=2, d=4, I=12, eps=1e-6, rope_base=1e4,
+                        qk_norm=qk_norm, rope_interleaved=interleaved)
+    # the per-head norm of small q / k (projection weights N(0, 0.02)) curves the
+    # loss sharply along Wq, Wk: a smaller step keeps the O(h^2) error below 2e-6
+    grads = _layer_fd_check(cfg, seed=11, ndir=3, h_for={"Wq": 1e-6, "Wk": 1e-6})
+    assert ("gamma_q" in grads) == qk_norm
 
 
 def test_layer_fd_config_tiny_fp32_dims():
@@ -345,6 +358,55 @@ def test_rope_plane_angles():
             assert math.isclose(y[s, i + d // 2], math.sin(a), abs_tol=1e-14)
             others = np.delete(y[s], [i, i + d // 2])
             assert np.all(others == 0.0)
+
+
+def test_rope_interleaved_is_permuted_half():
+    """Pairs (2i, 2i+1) with angle i are the rotate-half pairs (i, i+d/2) after
+    moving element 2i to i and 2i+1 to i+d/2."""
+    B, S, d = 2, 6, 8
+    x = _rand(B * S, 3, d)
+    perm = np.concatenate([np.arange(0, d, 2), np.arange(1, d, 2)])   # half-layout index -> interleaved index
+    inv = np.argsort(perm)
+    for fn in (O.rope_fwd, O.rope_bwd):
+        y_int = fn(x, B, S, 1e4, interleaved=True)
+        y_half = fn(x[..., perm], B, S, 1e4)[..., inv]
+        np.testing.assert_allclose(y_int, y_half, rtol=0, atol=1e-15)
+    # and it is not the rotate-half map itself
+    assert not np.allclose(O.rope_fwd(x, B, S, 1e4, interleaved=True), O.rope_fwd(x, B, S, 1e4))
+
+
+def test_rope_interleaved_relative_offset():
+    S, d = 10, 8
+    q, k = _rand(d), _rand(d)
+    Q = O.rope_fwd(np.tile(q, (S, 1))[:, None, :], 1, S, 1e4, interleaved=True)[:, 0]
+    K = O.rope_fwd(np.tile(k, (S, 1))[:, None, :], 1, S, 1e4, interleaved=True)[:, 0]
+    for off in range(0, 4):
+        vals = [np.dot(Q[m], K[m - off]) for m in range(off, S)]
+        np.testing.assert_allclose(vals, vals[0], rtol=1e-12)
+
+
+def test_qk_norm_closed_forms():
+    """With unit gains each head's normalised q (before the rotation, seen at
+    position 0 where the rotation is the identity) has RMS 1/sqrt(1 + eps/mean(q^2));
+    with eps = 0 the layer output is invariant to scaling Wq and Wk."""
+    cfg = O.LayerConfig(B=1, S=3, H=8, Hq=2, Hkv=1, d=4, I=6, eps=1e-3, qk_norm=True)
+    w = synth.layer_weights(2, cfg.H, cfg.Hq, cfg.Hkv, cfg.d, cfg.I, qk_norm=True)
+    w["gamma_q"] = np.ones(cfg.d)
+    w["gamma_k"] = np.ones(cfg.d)
+    X = synth.layer_inputs(2, cfg.T, cfg.H)["X"]
+    _, s = O.layer_forward(cfg, w, X)
+    qpre = s["q_pre"].reshape(cfg.T, cfg.Hq, cfg.d)
+    rms = np.sqrt(np.mean(s["q"][0] ** 2, axis=-1))
+    want = 1.0 / np.sqrt(1.0 + cfg.eps / np.mean(qpre[0] ** 2, axis=-1))
+    np.testing.assert_allclose(rms, want, rtol=1e-13)
+    cfg0 = O.LayerConfig(B=1, S=3, H=8, Hq=2, Hkv=1, d=4, I=6, eps=0.0, qk_norm=True)
+    Y0, _ = O.layer_forward(cfg0, w, X)
+    w2 = dict(w, Wq=3.0 * w["Wq"], Wk=0.25 * w["Wk"])
+    Y1, _ = O.layer_forward(cfg0, w2, X)
+    np.testing.assert_allclose(Y1, Y0, rtol=1e-12, atol=1e-14)
+    # without the norm the same scaling changes the output
+    cfg1 = O.LayerConfig(B=1, S=3, H=8, Hq=2, Hkv=1, d=4, I=6, eps=0.0)
+    assert not np.allclose(O.layer_forward(cfg1, w2, X)[0], O.layer_forward(cfg1, w, X)[0])
 
 
 # ----------------------------------------------------------------------------
