@@ -33,15 +33,18 @@ _i32, _i64, _f32, _vp, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, cty
 
 class LayerCfg(ctypes.Structure):
     _fields_ = [("B", _i32), ("S", _i32), ("H", _i32), ("Hq", _i32), ("Hkv", _i32), ("d", _i32),
-                ("I", _i32), ("eps", _f32), ("rope_base", _f32), ("dtype", _i32)]
+                ("I", _i32), ("eps", _f32), ("rope_base", _f32), ("dtype", _i32),
+                ("qk_norm", _i32), ("rope_interleaved", _i32)]
 
 
 WEIGHT_FIELDS = ("gamma1", "wq", "wk", "wv", "wo", "gamma2", "wg", "wu", "wd")
-SAVED_FIELDS = ("x", "h1", "rstd1", "q", "k", "v", "o", "lse", "x2", "h2", "rstd2", "g", "u", "m")
+QK_WEIGHT_FIELDS = ("gamma_q", "gamma_k")   # read only with cfg.qk_norm
+SAVED_FIELDS = ("x", "h1", "rstd1", "q", "k", "v", "o", "lse", "x2", "h2", "rstd2", "g", "u", "m",
+                "q_pre", "k_pre", "rstd_q", "rstd_k")
 
 
 class LayerWeights(ctypes.Structure):
-    _fields_ = [(n, _vp) for n in WEIGHT_FIELDS]
+    _fields_ = [(n, _vp) for n in WEIGHT_FIELDS + QK_WEIGHT_FIELDS]
 
 
 class LayerSaved(ctypes.Structure):
@@ -49,7 +52,7 @@ class LayerSaved(ctypes.Structure):
 
 
 class LayerGrads(ctypes.Structure):
-    _fields_ = [(n, _vp) for n in WEIGHT_FIELDS] + [("dtype", _i32)]
+    _fields_ = [(n, _vp) for n in WEIGHT_FIELDS] + [("dtype", _i32)] + [(n, _vp) for n in QK_WEIGHT_FIELDS]
 
 
 class LmheadCfg(ctypes.Structure):

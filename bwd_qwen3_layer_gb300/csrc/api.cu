@@ -100,6 +100,7 @@ struct Dims {
   int B, S, T, H, Hq, Hkv, d, I, Dq, Dkv;
   int dt;
   size_t es;
+  int qk_norm, inter;   // layer options: per-head q/k RMSNorm, interleaved rotary planes
 };
 
 kl_status check_cfg(const kl_layer_cfg* c, Dims* o) {
@@ -120,10 +121,14 @@ kl_status check_cfg(const kl_layer_cfg* c, Dims* o) {
     return set_error(KL_ERR_UNSUPPORTED, "fp32 layer needs head dim <= 256");
   }
   if (c->H * 4 > 48 * 1024) return set_error(KL_ERR_UNSUPPORTED, "hidden width above 12288");
+  if ((c->qk_norm != 0 && c->qk_norm != 1) || (c->rope_interleaved != 0 && c->rope_interleaved != 1))
+    return set_error(KL_ERR_INVALID_ARG, "qk_norm and rope_interleaved are 0 or 1");
   o->B = c->B; o->S = c->S; o->T = static_cast<int>(T); o->H = c->H; o->Hq = c->Hq;
   o->Hkv = c->Hkv; o->d = c->d; o->I = c->I; o->Dq = c->Hq * c->d; o->Dkv = c->Hkv * c->d;
   o->dt = c->dtype;
   o->es = dtype_size(c->dtype);
+  o->qk_norm = c->qk_norm;
+  o->inter = c->rope_interleaved;
   return KL_OK;
 }
 
@@ -154,6 +159,15 @@ void carve_saved(const Dims& D, Carver& c, kl_layer_saved* s) {
   s->g = c.take(T * D.I * es);
   s->u = c.take(T * D.I * es);
   s->m = c.take(T * D.I * es);
+  if (D.qk_norm) {
+    s->q_pre = c.take(T * D.Dq * es);
+    s->k_pre = c.take(T * D.Dkv * es);
+    s->rstd_q = static_cast<float*>(c.take(T * D.Hq * 4));
+    s->rstd_k = static_cast<float*>(c.take(T * D.Hkv * 4));
+  } else {
+    s->q_pre = s->k_pre = nullptr;
+    s->rstd_q = s->rstd_k = nullptr;
+  }
 }
 
 // The rotary (cos, sin) table [S][d/2] used by the fused q/k projection and dQ epilogues.
@@ -169,6 +183,8 @@ struct BwdWs {
   void* tail;             // fp32 scratch balancing the GEMM launches' last rounds (bf16)
   size_t tail_bytes;
   float2* rope;           // rotary (cos, sin) table [S][d/2] for the fused dQ rotation (bf16)
+  void *qk_q, *qk_k;      // gain-gradient partials of the per-head q / k norms (qk_norm)
+  size_t qk_q_bytes, qk_k_bytes;
 };
 
 void carve_bwd(const Dims& D, Carver& c, BwdWs* w) {
@@ -190,6 +206,10 @@ void carve_bwd(const Dims& D, Carver& c, BwdWs* w) {
   w->tail_bytes = D.dt == KL_BF16 ? gemm_tail_ws_bytes() : 0;
   w->tail = w->tail_bytes ? c.take(w->tail_bytes) : nullptr;
   w->rope = D.dt == KL_BF16 ? static_cast<float2*>(c.take(rope_table_bytes(D))) : nullptr;
+  w->qk_q_bytes = D.qk_norm ? qk_rope_bwd_ws(D.T * D.Hq, D.d) : 0;
+  w->qk_k_bytes = D.qk_norm ? qk_rope_bwd_ws(D.T * D.Hkv, D.d) : 0;
+  w->qk_q = D.qk_norm ? c.take(w->qk_q_bytes) : nullptr;
+  w->qk_k = D.qk_norm ? c.take(w->qk_k_bytes) : nullptr;
 }
 
 kl_status check_ptrs(std::initializer_list<const void*> ptrs, const char* what) {
@@ -295,21 +315,30 @@ kl_status kl_layer_forward(const kl_layer_cfg* cfg, const kl_layer_weights* w, c
                      s->g, s->u, s->m}, "layer_forward buffers"));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int T = D.T, H = D.H, I = D.I, dt = D.dt;
-  // bf16 with the full workspace: tail scratch + rotary table, rotation fused into q/k
+  if (D.qk_norm) {
+    KL_TRY(check_ptrs({w->gamma_q, w->gamma_k}, "layer_forward q/k norm gains"));
+    KL_TRY(check_ptrs({s->q_pre, s->k_pre, s->rstd_q, s->rstd_k}, "layer_forward q/k norm buffers"));
+  }
+  // bf16 with the full workspace: tail scratch + rotary table (the rotation fused
+  // into the q/k projection's epilogue when neither layer option is on)
   const bool fused = dt == KL_BF16 && ws && ws_bytes >= kl_layer_fwd_workspace_bytes(cfg) &&
                      (reinterpret_cast<uintptr_t>(ws) & 255u) == 0;
+  const bool options = D.qk_norm || D.inter;
   const size_t tail_bytes = fused ? gemm_tail_ws_bytes() : 0;
   float2* rope_tab = fused ? reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + tail_bytes) : nullptr;
   s->x = X;
   KL_TRY(rmsnorm_fwd(T, H, dt, X, w->gamma1, cfg->eps, s->h1, s->rstd1, st));
   if (fused) KL_TRY(rope_cs_table(D.S, D.d, cfg->rope_base, rope_tab, st));
   {
-    GemmSpec g[3] = {proj(T, D.Dq, H, s->h1, H, w->wq, H, s->q, D.Dq, dt),
-                     proj(T, D.Dkv, H, s->h1, H, w->wk, H, s->k, D.Dkv, dt),
+    // with the q/k norm the projections land in q_pre / k_pre first
+    void* qdst = D.qk_norm ? s->q_pre : s->q;
+    void* kdst = D.qk_norm ? s->k_pre : s->k;
+    GemmSpec g[3] = {proj(T, D.Dq, H, s->h1, H, w->wq, H, qdst, D.Dq, dt),
+                     proj(T, D.Dkv, H, s->h1, H, w->wk, H, kdst, D.Dkv, dt),
                      proj(T, D.Dkv, H, s->h1, H, w->wv, H, s->v, D.Dkv, dt)};
     if (fused) {
       with_tail(g, 3, ws, tail_bytes);
-      for (int i = 0; i < 2; ++i) {   // q and k leave the epilogue rotated
+      for (int i = 0; i < 2 && !options; ++i) {   // q and k leave the epilogue rotated
         g[i].epi = GEMM_EPI_ROPE;
         g[i].rope_cs = rope_tab;
         g[i].rope_S = D.S;
@@ -317,7 +346,17 @@ kl_status kl_layer_forward(const kl_layer_cfg* cfg, const kl_layer_weights* w, c
     }
     KL_TRY(run_gemms(dt, g, 3, st, "gemm.fwd_qkv"));
   }
-  if (!fused) KL_TRY(rope_qk(D.B, D.S, D.Hq, D.Hkv, D.d, cfg->rope_base, dt, s->q, s->k, 1, st));
+  if (options) {
+    // optional per-head norm, then the rotation (pairs of either layout)
+    const void* qsrc = D.qk_norm ? s->q_pre : s->q;
+    const void* ksrc = D.qk_norm ? s->k_pre : s->k;
+    KL_TRY(qk_rope_fwd(T, D.Hq, D.S, D.d, dt, qsrc, w->gamma_q, cfg->eps, D.qk_norm, D.inter, cfg->rope_base,
+                       rope_tab, s->q, s->rstd_q, st));
+    KL_TRY(qk_rope_fwd(T, D.Hkv, D.S, D.d, dt, ksrc, w->gamma_k, cfg->eps, D.qk_norm, D.inter, cfg->rope_base,
+                       rope_tab, s->k, s->rstd_k, st));
+  } else if (!fused) {
+    KL_TRY(rope_qk(D.B, D.S, D.Hq, D.Hkv, D.d, cfg->rope_base, dt, s->q, s->k, 1, st));
+  }
   KL_TRY(attention_fwd(D.B, D.S, D.Hq, D.Hkv, D.d, dt, s->q, s->k, s->v, s->o, s->lse, st));
   {
     GemmSpec g = proj(T, H, D.Dq, s->o, D.Dq, w->wo, D.Dq, s->x2, H, dt, X, dt);
@@ -360,6 +399,10 @@ kl_status kl_layer_backward(const kl_layer_cfg* cfg, const kl_layer_weights* w,
                      gr->wu, gr->wd}, "layer_backward outputs"));
   if (gr->dtype != KL_F32 && gr->dtype != KL_BF16)
     return set_error(KL_ERR_INVALID_ARG, "layer_backward: bad gradient dtype");
+  if (D.qk_norm) {
+    KL_TRY(check_ptrs({w->gamma_q, w->gamma_k, gr->gamma_q, gr->gamma_k}, "layer_backward q/k norm gains"));
+    KL_TRY(check_ptrs({s->q_pre, s->k_pre, s->rstd_q, s->rstd_k}, "layer_backward q/k norm saved"));
+  }
   if (D.dt == KL_F32 && gr->dtype != KL_F32)
     return set_error(KL_ERR_UNSUPPORTED, "layer_backward: fp32 layer needs fp32 gradients");
   const size_t need = kl_layer_bwd_workspace_bytes(cfg);
@@ -413,14 +456,29 @@ kl_status kl_layer_backward(const kl_layer_cfg* cfg, const kl_layer_weights* w,
     KL_TRY(run_gemms(dt, g, 2, st, "gemm.bwd_o"));
   }
   float *dq_acc = nullptr, *dk_acc = nullptr, *dv_acc = nullptr;
-  // bf16: dQ leaves the attention kernel rotated back and converted; dK, dV (summed
-  // over each kv head's query heads) are finished below
   if (b.rope) KL_TRY(rope_cs_table(D.S, D.d, cfg->rope_base, b.rope, st));
-  KL_TRY(attention_bwd_accum(D.B, D.S, D.Hq, D.Hkv, D.d, dt, s->q, s->k, s->v, s->o, s->lse, b.dO,
-                             b.att, b.att_bytes, &dq_acc, &dk_acc, &dv_acc, st, d_ready,
-                             b.rope ? b.dq : nullptr, b.rope));
-  KL_TRY(rope_bwd_convert(D.B, D.S, dq_acc ? D.Hq : 0, D.Hkv, D.d, cfg->rope_base, dt, dq_acc, dk_acc, dv_acc,
-                          b.dq, b.dk, b.dv, st));
+  if (!D.qk_norm && !D.inter) {
+    // bf16: dQ leaves the attention kernel rotated back and converted; dK, dV (summed
+    // over each kv head's query heads) are finished below
+    KL_TRY(attention_bwd_accum(D.B, D.S, D.Hq, D.Hkv, D.d, dt, s->q, s->k, s->v, s->o, s->lse, b.dO,
+                               b.att, b.att_bytes, &dq_acc, &dk_acc, &dv_acc, st, d_ready,
+                               b.rope ? b.dq : nullptr, b.rope));
+    KL_TRY(rope_bwd_convert(D.B, D.S, dq_acc ? D.Hq : 0, D.Hkv, D.d, cfg->rope_base, dt, dq_acc, dk_acc, dv_acc,
+                            b.dq, b.dk, b.dv, st));
+  } else {
+    // layer options: dQ (bf16, still rotated, in b.dq) or its fp32 accumulator, then the
+    // rotation back and the per-head norm backward for q and k; dV converted
+    KL_TRY(attention_bwd_accum(D.B, D.S, D.Hq, D.Hkv, D.d, dt, s->q, s->k, s->v, s->o, s->lse, b.dO,
+                               b.att, b.att_bytes, &dq_acc, &dk_acc, &dv_acc, st, d_ready,
+                               dt == KL_BF16 ? b.dq : nullptr, nullptr));
+    const void* dqr = dq_acc ? static_cast<const void*>(dq_acc) : b.dq;
+    KL_TRY(qk_rope_bwd(T, D.Hq, D.S, D.d, dt, dqr, dq_acc ? KL_F32 : KL_BF16, s->q_pre, w->gamma_q, s->rstd_q,
+                       D.qk_norm, D.inter, cfg->rope_base, b.rope, b.dq, static_cast<float*>(gr->gamma_q), b.qk_q,
+                       b.qk_q_bytes, st));
+    KL_TRY(qk_rope_bwd(T, D.Hkv, D.S, D.d, dt, dk_acc, KL_F32, s->k_pre, w->gamma_k, s->rstd_k, D.qk_norm, D.inter,
+                       cfg->rope_base, b.rope, b.dk, static_cast<float*>(gr->gamma_k), b.qk_k, b.qk_k_bytes, st));
+    KL_TRY(convert_f32(static_cast<int64_t>(T) * D.Dkv, dt, dv_acc, b.dv, st));
+  }
   {
     GemmSpec dh = dgrad(T, H, D.Dq, b.dq, w->wq, b.dh1, KL_F32);
     dh.nseg = 3;

@@ -627,6 +627,145 @@ __global__ void __launch_bounds__(RC_THREADS) rope_bwd_convert_kernel(
   }
 }
 
+// ---------------------------------------------------------------------------
+// q / k heads with the options: an optional RMSNorm over each head's d
+// features (gain g[d]) followed by the rotary turn, planes (i, i+d/2) or
+// interleaved (2i, 2i+1). One warp per (token, head) row; lane l owns planes
+// l, l+32, ... (d/2 <= 128, so at most 4 planes per lane). Each element is read
+// and written by the same lane only, so input and output may be one buffer.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void plane_idx(int i, int d, int inter, int& ia, int& ib) {
+  ia = inter ? 2 * i : i;
+  ib = inter ? 2 * i + 1 : i + d / 2;
+}
+__device__ __forceinline__ float2 plane_cs(int pos, int i, int half, const RopeFreq& f, const float2* tab) {
+  if (tab) return tab[static_cast<int64_t>(pos) * half + i];
+  float c, sn;
+  rope_cos_sin(pos, f.inv[i], 1.0f, &c, &sn);
+  return make_float2(c, sn);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) qk_rope_fwd_kernel(int rows, int heads, int S, int d, const T* pre,
+                                                          const T* __restrict__ gamma, float eps, int norm, int inter,
+                                                          RopeFreq f, const float2* __restrict__ tab,
+                                                          T* out, float* __restrict__ rstd) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + warp;
+  if (row >= rows) return;
+  const int pos = (row / heads) % S, half = d / 2;
+  const T* x = pre + static_cast<int64_t>(row) * d;
+  T* y = out + static_cast<int64_t>(row) * d;
+  float r = 1.0f;
+  if (norm) {
+    float ss = 0.f;
+    for (int j = lane; j < d; j += 32) {
+      const float v = ld_f(x + j);
+      ss = fmaf(v, v, ss);
+    }
+    ss = warp_sum(ss);
+    r = 1.0f / sqrtf(ss / static_cast<float>(d) + eps);
+    if (lane == 0) rstd[row] = r;
+  }
+  for (int i = lane; i < half; i += 32) {
+    int ia, ib;
+    plane_idx(i, d, inter, ia, ib);
+    float a = ld_f(x + ia) * r, b = ld_f(x + ib) * r;
+    if (norm) {
+      a *= ld_f(gamma + ia);
+      b *= ld_f(gamma + ib);
+    }
+    const float2 cs = plane_cs(pos, i, half, f, tab);
+    st_f(y + ia, a * cs.x - b * cs.y);
+    st_f(y + ib, a * cs.y + b * cs.x);
+  }
+}
+
+// Backward: dy (gradient after the rotation, element type TD, scaled by
+// dy_scale) turned back, then the RMSNorm backward
+//   n = x r, dn = dy g, dx = r (dn - n mean(dn n)),  dg += dy n
+// (without the norm dx = dy). Gain gradients: per-CTA partial rows
+// partial[blockIdx.x][d], summed afterwards in a fixed order.
+constexpr int QK_MAXP = 4;   // planes per lane (d/2 <= 128)
+
+template <typename T, typename TD>
+__global__ void __launch_bounds__(256) qk_rope_bwd_kernel(int rows, int heads, int S, int d, const TD* dyr,
+                                                          float dy_scale, const T* __restrict__ pre,
+                                                          const T* __restrict__ gamma, const float* __restrict__ rstd,
+                                                          int norm, int inter, RopeFreq f,
+                                                          const float2* __restrict__ tab, T* dx,
+                                                          float* __restrict__ partial) {
+  __shared__ float sacc[8][256];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = d / 2;
+  float acc_a[QK_MAXP], acc_b[QK_MAXP];
+#pragma unroll
+  for (int t = 0; t < QK_MAXP; ++t) acc_a[t] = acc_b[t] = 0.f;
+  for (int row = blockIdx.x * 8 + warp; row < rows; row += gridDim.x * 8) {
+    const int pos = (row / heads) % S;
+    const int64_t o = static_cast<int64_t>(row) * d;
+    float da[QK_MAXP], db[QK_MAXP], na[QK_MAXP], nb[QK_MAXP];
+    const float r = norm ? rstd[row] : 1.0f;
+    float dot = 0.f;
+#pragma unroll
+    for (int t = 0; t < QK_MAXP; ++t) {
+      const int i = lane + 32 * t;
+      da[t] = db[t] = na[t] = nb[t] = 0.f;
+      if (i < half) {
+        int ia, ib;
+        plane_idx(i, d, inter, ia, ib);
+        const float ya = ld_f(dyr + o + ia) * dy_scale, yb = ld_f(dyr + o + ib) * dy_scale;
+        const float2 cs = plane_cs(pos, i, half, f, tab);
+        da[t] = ya * cs.x + yb * cs.y;       // turned back by -angle
+        db[t] = yb * cs.x - ya * cs.y;
+        if (norm) {
+          na[t] = ld_f(pre + o + ia) * r;
+          nb[t] = ld_f(pre + o + ib) * r;
+          dot = fmaf(da[t] * ld_f(gamma + ia), na[t], dot);
+          dot = fmaf(db[t] * ld_f(gamma + ib), nb[t], dot);
+        }
+      }
+    }
+    if (norm) dot = warp_sum(dot) / static_cast<float>(d);
+#pragma unroll
+    for (int t = 0; t < QK_MAXP; ++t) {
+      const int i = lane + 32 * t;
+      if (i < half) {
+        int ia, ib;
+        plane_idx(i, d, inter, ia, ib);
+        if (norm) {
+          const float ga = ld_f(gamma + ia), gb = ld_f(gamma + ib);
+          st_f(dx + o + ia, r * (da[t] * ga - na[t] * dot));
+          st_f(dx + o + ib, r * (db[t] * gb - nb[t] * dot));
+          acc_a[t] = fmaf(da[t], na[t], acc_a[t]);
+          acc_b[t] = fmaf(db[t], nb[t], acc_b[t]);
+        } else {
+          st_f(dx + o + ia, da[t]);
+          st_f(dx + o + ib, db[t]);
+        }
+      }
+    }
+  }
+  if (!norm) return;
+  // gain-gradient partial of this CTA: warps' rows summed in a fixed order
+#pragma unroll
+  for (int t = 0; t < QK_MAXP; ++t) {
+    const int i = lane + 32 * t;
+    if (i < half) {
+      int ia, ib;
+      plane_idx(i, d, inter, ia, ib);
+      sacc[warp][ia] = acc_a[t];
+      sacc[warp][ib] = acc_b[t];
+    }
+  }
+  __syncthreads();
+  for (int j = threadIdx.x; j < d; j += blockDim.x) {
+    float v = 0.f;
+    for (int w = 0; w < 8; ++w) v += sacc[w][j];
+    partial[static_cast<int64_t>(blockIdx.x) * d + j] = v;
+  }
+}
+
 template <typename T>
 __global__ void convert_kernel(int64_t n, const float* __restrict__ src, T* __restrict__ dst) {
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
@@ -868,6 +1007,66 @@ kl_status rope_bwd_convert(int B, int S, int hq, int hk, int d, float base, int 
     rope_bwd_convert_kernel<float><<<T, RC_THREADS, 0, st>>>(S, hq, hk, d, f, dq_acc, dk_acc, dv_acc, (float*)dq,
                                                              (float*)dk, (float*)dv);
   KL_CUDA(cudaGetLastError());
+  return KL_OK;
+}
+
+int qk_bwd_grid(int rows) {
+  const int want = (rows + 7) / 8, cap = 2 * num_sms();
+  return want < cap ? want : cap;
+}
+
+size_t qk_rope_bwd_ws(int rows, int d) { return align_up(static_cast<size_t>(qk_bwd_grid(rows)) * d * 4, 256); }
+
+kl_status qk_rope_fwd(int T, int heads, int S, int d, int dtype, const void* pre, const void* gamma, float eps,
+                      int norm, int inter, float base, const float2* tab, void* out, float* rstd, cudaStream_t st) {
+  if (T < 1 || heads < 1 || d < 2 || (d & 1) || d / 2 > ROPE_MAX_HALF || !pre || !out || (norm && (!gamma || !rstd)))
+    return set_error(KL_ERR_INVALID_ARG, "q/k rotary: bad arguments");
+  const int rows = T * heads;
+  const RopeFreq f = rope_freq(d, base);
+  ProfScope ps("qk_rope_fwd", st, 0.0, 2.0 * rows * d * dtype_size(dtype));
+  const int grid = (rows + 7) / 8;
+  if (dtype == KL_BF16)
+    qk_rope_fwd_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(rows, heads, S, d, (const __nv_bfloat16*)pre,
+                                                           (const __nv_bfloat16*)gamma, eps, norm, inter, f, tab,
+                                                           (__nv_bfloat16*)out, rstd);
+  else
+    qk_rope_fwd_kernel<float><<<grid, 256, 0, st>>>(rows, heads, S, d, (const float*)pre, (const float*)gamma, eps,
+                                                   norm, inter, f, tab, (float*)out, rstd);
+  KL_CUDA(cudaGetLastError());
+  return KL_OK;
+}
+
+kl_status qk_rope_bwd(int T, int heads, int S, int d, int dtype, const void* dyr, int dy_dtype, const void* pre,
+                      const void* gamma, const float* rstd, int norm, int inter, float base, const float2* tab,
+                      void* dx, float* dgamma, void* ws, size_t ws_bytes, cudaStream_t st) {
+  if (T < 1 || heads < 1 || d < 2 || (d & 1) || d / 2 > ROPE_MAX_HALF || d > 256 || !dyr || !dx ||
+      (norm && (!pre || !gamma || !rstd || !dgamma)))
+    return set_error(KL_ERR_INVALID_ARG, "q/k rotary backward: bad arguments");
+  const int rows = T * heads;
+  if (norm && (!ws || ws_bytes < qk_rope_bwd_ws(rows, d)))
+    return set_error(KL_ERR_NO_MEMORY, "q/k rotary backward: workspace too small");
+  const RopeFreq f = rope_freq(d, base);
+  const int grid = qk_bwd_grid(rows);
+  float* partial = static_cast<float*>(ws);
+  {
+    ProfScope ps("qk_rope_bwd", st, 0.0, 1.0 * rows * d * (dtype_size(dy_dtype) + (norm ? 2.0 : 1.0) * dtype_size(dtype)));
+#define KL_QKB(T_, TD_)                                                                                         \
+  qk_rope_bwd_kernel<T_, TD_><<<grid, 256, 0, st>>>(rows, heads, S, d, (const TD_*)dyr, 1.0f, (const T_*)pre,  \
+                                                    (const T_*)gamma, rstd, norm, inter, f, tab, (T_*)dx, partial)
+    if (dtype == KL_BF16) {
+      if (dy_dtype == KL_BF16) KL_QKB(__nv_bfloat16, __nv_bfloat16);
+      else KL_QKB(__nv_bfloat16, float);
+    } else {
+      KL_QKB(float, float);
+    }
+#undef KL_QKB
+  }
+  KL_CUDA(cudaGetLastError());
+  if (norm) {
+    ProfScope ps2("qk_rope_bwd_colsum", st, 0.0, 4.0 * grid * d);
+    column_sum_kernel<<<(d + 63) / 64, 256, 0, st>>>(grid, d, partial, dgamma);
+    KL_CUDA(cudaGetLastError());
+  }
   return KL_OK;
 }
 

@@ -92,6 +92,17 @@ kl_status rmsnorm_bwd(int rows, int width, int dtype, const void* dh, int dh_dty
                       float* dgamma, void* ws, size_t ws_bytes, cudaStream_t st);
 kl_status rope(int B, int S, int heads, int d, float base, int dtype, void* x, int direction,
                cudaStream_t st);
+// q / k heads with the layer options: rows [T*heads, d] of `pre` -> optional
+// RMSNorm over each row (gain gamma[d], rstd[row] saved) -> rotary turn, planes
+// (i, i+d/2) or interleaved (2i, 2i+1); cos/sin from tab ([S][d/2]) or formed.
+kl_status qk_rope_fwd(int T, int heads, int S, int d, int dtype, const void* pre, const void* gamma, float eps,
+                      int norm, int inter, float base, const float2* tab, void* out, float* rstd, cudaStream_t st);
+// Its backward: dyr (gradient after the rotation, dy_dtype) -> dx (dtype);
+// with the norm also dgamma (fp32 [d], overwritten). Workspace: qk_rope_bwd_ws.
+size_t qk_rope_bwd_ws(int rows, int d);
+kl_status qk_rope_bwd(int T, int heads, int S, int d, int dtype, const void* dyr, int dy_dtype, const void* pre,
+                      const void* gamma, const float* rstd, int norm, int inter, float base, const float2* tab,
+                      void* dx, float* dgamma, void* ws, size_t ws_bytes, cudaStream_t st);
 // cs[s * d/2 + i] = (cos, sin) of the angle s * base^(-2i/d), s < S (d/2 <= 128).
 kl_status rope_cs_table(int S, int d, float base, float2* cs, cudaStream_t st);
 // q [T, hq, d] and k [T, hk, d] rotated in place in one launch (hk may be 0).

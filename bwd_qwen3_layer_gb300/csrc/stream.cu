@@ -144,16 +144,21 @@ size_t weight_elems(const kl_layer_cfg& c, int which) {
     case 5: return H;          // gamma2
     case 6: return I * H;      // wg
     case 7: return I * H;      // wu
-    default: return H * I;     // wd
+    case 8: return H * I;      // wd
+    default: return static_cast<size_t>(c.d);   // gamma_q, gamma_k
   }
 }
 
+// Weight tensors of one layer: the nine of the pages' layer, plus the two
+// per-head q/k norm gains with cfg.qk_norm.
+int n_weights(const kl_layer_cfg& c) { return c.qk_norm ? 11 : 9; }
+
 const void** wfield(kl_layer_weights& w, int i) {
-  const void** f[9] = {&w.gamma1, &w.wq, &w.wk, &w.wv, &w.wo, &w.gamma2, &w.wg, &w.wu, &w.wd};
+  const void** f[11] = {&w.gamma1, &w.wq, &w.wk, &w.wv, &w.wo, &w.gamma2, &w.wg, &w.wu, &w.wd, &w.gamma_q, &w.gamma_k};
   return f[i];
 }
 void** gfield(kl_layer_grads& g, int i) {
-  void** f[9] = {&g.gamma1, &g.wq, &g.wk, &g.wv, &g.wo, &g.gamma2, &g.wg, &g.wu, &g.wd};
+  void** f[11] = {&g.gamma1, &g.wq, &g.wk, &g.wv, &g.wo, &g.gamma2, &g.wg, &g.wu, &g.wd, &g.gamma_q, &g.gamma_k};
   return f[i];
 }
 
@@ -246,7 +251,7 @@ kl_status upload_layer(kl_stream* s, int layer, int slot) {
   const kl_layer_cfg& c = s->cfg.layer;
   const size_t es = dtype_size(c.dtype);
   KL_CUDA(cudaStreamWaitEvent(s->copy, s->ev_used[slot], 0));
-  for (int i = 0; i < 9; ++i)
+  for (int i = 0; i < n_weights(c); ++i)
     KL_CUDA(cudaMemcpyAsync(const_cast<void*>(*wfield(s->slot[slot], i)), *wfield(s->layers[layer], i),
                             weight_elems(c, i) * es, cudaMemcpyHostToDevice, s->copy));
   KL_CUDA(cudaEventRecord(s->ev_loaded[slot], s->copy));
@@ -303,7 +308,7 @@ kl_status kl_stream_create(const kl_stream_cfg* cfg, const kl_layer_weights* hos
   const size_t lm_ws = kl_lmhead_workspace_bytes(&lc);
   if (lm_ws == 0) return KL_ERR_UNSUPPORTED;
   for (int l = 0; l < cfg->n_layers; ++l)
-    for (int i = 0; i < 9; ++i)
+    for (int i = 0; i < n_weights(c); ++i)
       if (!*wfield(const_cast<kl_layer_weights&>(host_layers[l]), i))
         return set_error(KL_ERR_INVALID_ARG, "kl_stream_create: layer %d weight %d is null", l, i);
 
@@ -318,7 +323,7 @@ kl_status kl_stream_create(const kl_stream_cfg* cfg, const kl_layer_weights* hos
   const size_t T = static_cast<size_t>(c.B) * c.S, es = dtype_size(c.dtype);
   if (!s->bulk) {
     for (int k = 0; k < 2; ++k)
-      for (int i = 0; i < 9; ++i) *wfield(s->slot[k], i) = s->alloc(weight_elems(c, i) * es, &st);
+      for (int i = 0; i < n_weights(c); ++i) *wfield(s->slot[k], i) = s->alloc(weight_elems(c, i) * es, &st);
     s->lm_w = s->alloc(static_cast<size_t>(cfg->V) * c.H * es, &st);
     if (st == KL_OK) st = make_stream_events(s);
   } else {
@@ -341,7 +346,7 @@ kl_status kl_stream_create(const kl_stream_cfg* cfg, const kl_layer_weights* hos
   s->lm_ws = s->alloc(lm_ws, &st);
   s->loss = static_cast<float*>(s->alloc(sizeof(float), &st));
   s->argmax = static_cast<int32_t*>(s->alloc(T * sizeof(int32_t), &st));
-  s->max_refs = 9 * L + 1;
+  s->max_refs = n_weights(c) * L + 1;
   s->partials = static_cast<double*>(s->alloc(static_cast<size_t>(s->max_refs) * SUMSQ_BLOCKS * 8, &st));
   s->result = static_cast<float*>(s->alloc(4 * sizeof(float), &st));
   s->refs = static_cast<GradRef*>(s->alloc(static_cast<size_t>(s->max_refs) * sizeof(GradRef), &st));
@@ -375,7 +380,7 @@ kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets, flo
   for (int l = 0; l < L; ++l) {
     if (dst[l].dtype != KL_F32) return set_error(KL_ERR_INVALID_ARG, "kl_stream_run: gradients must be fp32");
     bool dev_all = true;
-    for (int i = 0; i < 9; ++i) {
+    for (int i = 0; i < n_weights(c); ++i) {
       void* p = *gfield(dst[l], i);
       if (!p) return set_error(KL_ERR_INVALID_ARG, "kl_stream_run: layer %d gradient %d is null", l, i);
       if (!device_visible(p))
@@ -393,7 +398,7 @@ kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets, flo
     if (any_host && s->retain.empty()) {
       s->retain.resize(L);
       for (int l = 0; l < L; ++l) {
-        for (int i = 0; i < 9; ++i) *gfield(s->retain[l], i) = s->alloc(weight_elems(c, i) * 4, &st);
+        for (int i = 0; i < n_weights(c); ++i) *gfield(s->retain[l], i) = s->alloc(weight_elems(c, i) * 4, &st);
         s->retain[l].dtype = KL_F32;
       }
     }
@@ -405,7 +410,7 @@ kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets, flo
   std::vector<GradRef> refs;
   for (int l = 0; l < L; ++l) {
     src[l] = on_device[l] ? dst[l] : s->retain[l];
-    for (int i = 0; i < 9; ++i)
+    for (int i = 0; i < n_weights(c); ++i)
       refs.push_back({static_cast<const float*>(*gfield(src[l], i)),
                       static_cast<float*>(device_visible(*gfield(dst[l], i))),
                       static_cast<int64_t>(weight_elems(c, i)), 0});
@@ -461,7 +466,7 @@ kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets, flo
   kl_lmhead_cfg lc = {T, c.H, s->cfg.V, c.dtype, KL_F32};
   KL_TRY(kl_lmhead_ce_argmax(&lc, s->hidden[L - 1], s->lm_w, targets, s->loss, s->argmax, nullptr, s->dx[0],
                              dwlm_src, s->lm_ws, s->lm_ws_bytes, cs));
-  KL_TRY(sumsq(s, dwlm_src, static_cast<int64_t>(s->cfg.V) * c.H, 9 * L, cs));
+  KL_TRY(sumsq(s, dwlm_src, static_cast<int64_t>(s->cfg.V) * c.H, n_weights(c) * L, cs));
   // ---------------- backward ----------------
   int in = 0;
   for (int l = L - 1; l >= 0; --l) {
@@ -473,15 +478,16 @@ kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets, flo
     }
     KL_TRY(kl_layer_backward(&c, &w, &s->saved[l], s->dx[in], s->dx[in ^ 1], &src[l], s->bwd_ws, s->bwd_ws_bytes, cs));
     in ^= 1;
-    for (int i = 0; i < 9; ++i)
+    for (int i = 0; i < n_weights(c); ++i)
       KL_TRY(sumsq(s, static_cast<const float*>(*gfield(src[l], i)), static_cast<int64_t>(weight_elems(c, i)),
-                   9 * l + i, cs));
+                   n_weights(c) * l + i, cs));
     if (!s->bulk) KL_CUDA(cudaEventRecord(s->ev_used[cur], cs));
   }
   // ---------------- global norm, clip, delivery ----------------
   {
-    ProfScope ps("clip_finalize", cs, 0.0, 8.0 * (9 * L + 1) * SUMSQ_BLOCKS);
-    clip_finalize_kernel<<<1, SUMSQ_THREADS, 0, cs>>>(s->partials, 9 * L + 1, s->loss, clip_max_norm, s->result);
+    const int nref = n_weights(c) * L + 1;
+    ProfScope ps("clip_finalize", cs, 0.0, 8.0 * nref * SUMSQ_BLOCKS);
+    clip_finalize_kernel<<<1, SUMSQ_THREADS, 0, cs>>>(s->partials, nref, s->loss, clip_max_norm, s->result);
   }
   KL_CUDA(cudaGetLastError());
   {

@@ -5,27 +5,36 @@ from __future__ import annotations
 
 import torch
 
-from . import (KL_BF16, KL_F32, LayerCfg, LayerGrads, LayerWeights, LmheadCfg, WEIGHT_FIELDS,
+from . import (KL_BF16, KL_F32, LayerCfg, LayerGrads, LayerWeights, LmheadCfg, QK_WEIGHT_FIELDS, WEIGHT_FIELDS,
                kl_layer_bwd_workspace_bytes, kl_layer_fwd_workspace_bytes, kl_layer_saved_bytes, kl_layer_saved_carve,
                kl_lmhead_workspace_bytes)
 
 TORCH_DTYPE = {KL_F32: torch.float32, KL_BF16: torch.bfloat16}
 SYNTH_NAMES = {"gamma1": "gamma1", "wq": "Wq", "wk": "Wk", "wv": "Wv", "wo": "Wo",
-               "gamma2": "gamma2", "wg": "Wg", "wu": "Wu", "wd": "Wd"}
+               "gamma2": "gamma2", "wg": "Wg", "wu": "Wu", "wd": "Wd",
+               "gamma_q": "gamma_q", "gamma_k": "gamma_k"}
 
 
-def make_cfg(B, S, H, Hq, Hkv, d, I, eps=1e-6, rope_base=1e6, dtype=KL_BF16) -> LayerCfg:
-    return LayerCfg(B, S, H, Hq, Hkv, d, I, eps, rope_base, dtype)
+def make_cfg(B, S, H, Hq, Hkv, d, I, eps=1e-6, rope_base=1e6, dtype=KL_BF16, qk_norm=False,
+             rope_interleaved=False) -> LayerCfg:
+    return LayerCfg(B, S, H, Hq, Hkv, d, I, eps, rope_base, dtype, int(qk_norm), int(rope_interleaved))
+
+
+def weight_fields(cfg: LayerCfg) -> tuple:
+    return WEIGHT_FIELDS + (QK_WEIGHT_FIELDS if cfg.qk_norm else ())
 
 
 def weight_shapes(cfg: LayerCfg) -> dict:
     H, Dq, Dkv, I = cfg.H, cfg.Hq * cfg.d, cfg.Hkv * cfg.d, cfg.I
-    return {"gamma1": (H,), "wq": (Dq, H), "wk": (Dkv, H), "wv": (Dkv, H), "wo": (H, Dq),
-            "gamma2": (H,), "wg": (I, H), "wu": (I, H), "wd": (H, I)}
+    shapes = {"gamma1": (H,), "wq": (Dq, H), "wk": (Dkv, H), "wv": (Dkv, H), "wo": (H, Dq),
+              "gamma2": (H,), "wg": (I, H), "wu": (I, H), "wd": (H, I)}
+    if cfg.qk_norm:
+        shapes.update(gamma_q=(cfg.d,), gamma_k=(cfg.d,))
+    return shapes
 
 
 def weights_struct(w: dict) -> LayerWeights:
-    return LayerWeights(*[w[n].data_ptr() for n in WEIGHT_FIELDS])
+    return LayerWeights(*[w[n].data_ptr() if n in w else None for n in WEIGHT_FIELDS + QK_WEIGHT_FIELDS])
 
 
 def alloc_grads(cfg: LayerCfg, device, dtype: int) -> tuple:
@@ -33,7 +42,8 @@ def alloc_grads(cfg: LayerCfg, device, dtype: int) -> tuple:
     for n, shp in weight_shapes(cfg).items():
         dt = torch.float32 if n.startswith("gamma") else TORCH_DTYPE[dtype]
         g[n] = torch.empty(shp, dtype=dt, device=device)
-    st = LayerGrads(*[g[n].data_ptr() for n in WEIGHT_FIELDS], dtype)
+    st = LayerGrads(*[g[n].data_ptr() for n in WEIGHT_FIELDS], dtype,
+                    *[g[n].data_ptr() if n in g else None for n in QK_WEIGHT_FIELDS])
     return g, st
 
 
@@ -85,7 +95,7 @@ def run_layer(cfg: LayerCfg, w_host: dict, X_host, dY_host, device="cuda", grad_
 
     dt = cfg.dtype
     gdt = dt if grad_dtype is None else grad_dtype
-    w = {n: to_device(w_host[SYNTH_NAMES[n]], dt, device) for n in WEIGHT_FIELDS}
+    w = {n: to_device(w_host[SYNTH_NAMES[n]], dt, device) for n in weight_fields(cfg)}
     T = cfg.B * cfg.S
     X = to_device(X_host, dt, device)
     dY = to_device(dY_host, dt, device)
@@ -100,7 +110,7 @@ def run_layer(cfg: LayerCfg, w_host: dict, X_host, dY_host, device="cuda", grad_
                       buf.bwd_ws.numel())
     torch.cuda.synchronize()
     out = {"Y": Y.double().cpu().numpy(), "dX": dX.double().cpu().numpy()}
-    for n in WEIGHT_FIELDS:
+    for n in weight_fields(cfg):
         out["d" + SYNTH_NAMES[n]] = grads[n].double().cpu().numpy()
     Dq, Dkv = cfg.Hq * cfg.d, cfg.Hkv * cfg.d
     sdt = TORCH_DTYPE[dt]
@@ -109,6 +119,9 @@ def run_layer(cfg: LayerCfg, w_host: dict, X_host, dY_host, device="cuda", grad_
               "lse": ((cfg.B, cfg.Hq, cfg.S), torch.float32), "x2": ((T, cfg.H), sdt),
               "h2": ((T, cfg.H), sdt), "rstd2": ((T,), torch.float32), "g": ((T, cfg.I), sdt),
               "u": ((T, cfg.I), sdt), "m": ((T, cfg.I), sdt)}
+    if cfg.qk_norm:
+        shapes.update(q_pre=((T, Dq), sdt), k_pre=((T, Dkv), sdt), rstd_q=((T, cfg.Hq), torch.float32),
+                      rstd_k=((T, cfg.Hkv), torch.float32))
     out["saved"] = {k: buf.view(k, s, d).double().cpu().numpy() for k, (s, d) in shapes.items()}
     if keep:
         out["_keep"] = (w, X, dY, Y, dX, buf, grads)
@@ -159,7 +172,7 @@ def run_stream(cfg: LayerCfg, n_layers: int, V: int, layers_host: list, W_lm_hos
 
     hl = []
     for lw in layers_host:
-        w = {n: place(lw[SYNTH_NAMES[n]], TORCH_DTYPE[dt]) for n in WEIGHT_FIELDS}
+        w = {n: place(lw[SYNTH_NAMES[n]], TORCH_DTYPE[dt]) for n in weight_fields(cfg)}
         hl.append(weights_struct(w))
     W = place(W_lm_host, TORCH_DTYPE[dt])
     scfg = StreamCfg(cfg, n_layers, V)
@@ -174,7 +187,8 @@ def run_stream(cfg: LayerCfg, n_layers: int, V: int, layers_host: list, W_lm_hos
             if grads_on_host:
                 g = {n: t.pin_memory() for n, t in g.items()}
             gl.append(g)
-            gs.append(LayerGrads(*[g[n].data_ptr() for n in WEIGHT_FIELDS], KL_F32))
+            gs.append(LayerGrads(*[g[n].data_ptr() for n in WEIGHT_FIELDS], KL_F32,
+                                 *[g[n].data_ptr() if n in g else None for n in QK_WEIGHT_FIELDS]))
         dW = torch.empty(V, cfg.H, dtype=torch.float32, device="cpu" if grads_on_host else device)
         if grads_on_host:
             dW = dW.pin_memory()
@@ -182,7 +196,7 @@ def run_stream(cfg: LayerCfg, n_layers: int, V: int, layers_host: list, W_lm_hos
             res = kl_stream_run(h, X.data_ptr(), tgt.data_ptr(), clip, gs, dW.data_ptr())
         torch.cuda.synchronize()
         out = {"result": (res.loss, res.total_norm, res.clip_coef), "device_bytes": kl_stream_device_bytes(h),
-               "grads": [{SYNTH_NAMES[n]: g[n].double().cpu().numpy() for n in WEIGHT_FIELDS} for g in gl],
+               "grads": [{SYNTH_NAMES[n]: g[n].double().cpu().numpy() for n in weight_fields(cfg)} for g in gl],
                "dW_lm": dW.double().cpu().numpy()}
     finally:
         kl_stream_destroy(h)

@@ -116,12 +116,19 @@ typedef struct kl_layer_cfg {
   float eps;           /* RMSNorm epsilon                                   */
   float rope_base;     /* rotary base                                       */
   int32_t dtype;       /* kl_dtype of weights, activations and arithmetic  */
+  /* Options beyond the pages' layer (0 = off): */
+  int32_t qk_norm;     /* 1: RMSNorm over each q and k head (gains gamma_q,
+                          gamma_k of length d shared by the heads), before
+                          the rotation, as in Qwen3 checkpoints              */
+  int32_t rope_interleaved; /* 1: rotary planes (2i, 2i+1); 0: (i, i+d/2)   */
 } kl_layer_cfg;
 
-/* Device pointers, dtype = cfg.dtype. gamma*: [H]. wq [Hq*d, H],
- * wk/wv [Hkv*d, H], wo [H, Hq*d], wg/wu [I, H], wd [H, I]. */
+/* Device pointers, dtype = cfg.dtype. gamma1/gamma2: [H]. wq [Hq*d, H],
+ * wk/wv [Hkv*d, H], wo [H, Hq*d], wg/wu [I, H], wd [H, I]; gamma_q/gamma_k
+ * [d] (read only when cfg.qk_norm, may be NULL otherwise). */
 typedef struct kl_layer_weights {
   const void *gamma1, *wq, *wk, *wv, *wo, *gamma2, *wg, *wu, *wd;
+  const void *gamma_q, *gamma_k;
 } kl_layer_weights;
 
 /* Activations the forward saves for the backward (device, caller-owned).
@@ -142,6 +149,11 @@ typedef struct kl_layer_saved {
   void* g;             /* [T,I] gate projection                            */
   void* u;             /* [T,I] up projection                              */
   void* m;             /* [T,I] silu(g) * u                                */
+  /* cfg.qk_norm only (NULL otherwise): */
+  void* q_pre;         /* [T,Hq*d]  query projection before its norm        */
+  void* k_pre;         /* [T,Hkv*d] key projection before its norm          */
+  float* rstd_q;       /* [T,Hq]  per-head 1/sqrt(mean(q^2)+eps)            */
+  float* rstd_k;       /* [T,Hkv]                                           */
 } kl_layer_saved;
 
 /* Gradients written by the backward (device, caller-owned). Projection
@@ -151,6 +163,7 @@ typedef struct kl_layer_saved {
 typedef struct kl_layer_grads {
   void *gamma1, *wq, *wk, *wv, *wo, *gamma2, *wg, *wu, *wd;
   int32_t dtype;
+  void *gamma_q, *gamma_k;  /* fp32 [d], cfg.qk_norm only (may be NULL otherwise) */
 } kl_layer_grads;
 
 /* Bytes of one buffer holding every saved activation, and a carve of such a
@@ -305,7 +318,8 @@ typedef struct kl_stream_result {
 } kl_stream_result;
 
 /* host_layers[n_layers]: HOST pointers (pinned or pageable) to each layer's
- * weights in cfg.layer.dtype; host_lm_head [V,H] host. The driver keeps the
+ * weights in cfg.layer.dtype (gamma_q/gamma_k too when cfg.layer.qk_norm,
+ * else they are ignored); host_lm_head [V,H] host. The driver keeps the
  * pointers (no copy of the weights); they must stay valid until destroy.
  * Allocates two device weight slots, the lm-head weight, saved activations
  * for every layer and workspace on the current device. */

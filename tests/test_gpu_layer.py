@@ -14,12 +14,12 @@ pytestmark = pytest.mark.gpu
 GRAD_NAMES = ("gamma1", "Wq", "Wk", "Wv", "Wo", "gamma2", "Wg", "Wu", "Wd")
 
 
-def _run_both(kl, B, S, H, Hq, Hkv, d, I, dt, seed, grad_dtype=None, w=None):
+def _run_both(kl, B, S, H, Hq, Hkv, d, I, dt, seed, grad_dtype=None, w=None, qk_norm=False, inter=False):
     bf = dt == kl.KL_BF16
-    cfg = L.make_cfg(B, S, H, Hq, Hkv, d, I, dtype=dt)
-    ocfg = O.LayerConfig(B=B, S=S, H=H, Hq=Hq, Hkv=Hkv, d=d, I=I)
+    cfg = L.make_cfg(B, S, H, Hq, Hkv, d, I, dtype=dt, qk_norm=qk_norm, rope_interleaved=inter)
+    ocfg = O.LayerConfig(B=B, S=S, H=H, Hq=Hq, Hkv=Hkv, d=d, I=I, qk_norm=qk_norm, rope_interleaved=inter)
     if w is None:
-        w = synth.layer_weights(seed, H, Hq, Hkv, d, I, bf16=bf)
+        w = synth.layer_weights(seed, H, Hq, Hkv, d, I, bf16=bf, qk_norm=qk_norm)
     inp = synth.layer_inputs(seed, B * S, H, bf16=bf)
     if not bf:   # fp32 mode: both sides see the fp32-representable values
         w = {k: v.astype(np.float32).astype(np.float64) for k, v in w.items()}
@@ -49,6 +49,39 @@ def test_bf16_layer(kl, B, S, H, Hq, Hkv, I):
     for n in GRAD_NAMES:
         assert_rel(got["d" + n], grads[n], TOL_BF16, "d" + n)
     for k in ("q", "k", "v", "o", "x2", "g", "u", "m"):
+        assert_rel(got["saved"][k], saved[k].reshape(got["saved"][k].shape), TOL_BF16, k)
+
+
+OPTION_CASES = [(True, False), (False, True), (True, True)]
+
+
+@pytest.mark.parametrize("qk_norm,inter", OPTION_CASES)
+def test_tiny_fp32_layer_options(kl, qk_norm, inter):
+    """Per-head q/k RMSNorm and/or interleaved rotary planes, fp32, tiny workload."""
+    got, Y, dX, grads, saved, _, _ = _run_both(kl, 1, 32, 64, 4, 2, 16, 172, kl.KL_F32, 1, qk_norm=qk_norm,
+                                               inter=inter)
+    assert_rel(got["Y"], Y, TOL_F32, "Y")
+    assert_rel(got["dX"], dX, TOL_F32, "dX")
+    names = GRAD_NAMES + (("gamma_q", "gamma_k") if qk_norm else ())
+    for n in names:
+        assert_rel(got["d" + n], grads[n], TOL_F32, "d" + n)
+    keys = ("q", "k") + (("q_pre", "k_pre", "rstd_q", "rstd_k") if qk_norm else ())
+    for k in keys:
+        assert_rel(got["saved"][k], saved[k].reshape(got["saved"][k].shape), TOL_F32, k)
+
+
+@pytest.mark.parametrize("qk_norm,inter", OPTION_CASES)
+@pytest.mark.parametrize("B,S,H,Hq,Hkv,I", [(2, 200, 512, 8, 2, 1376), (1, 333, 640, 8, 1, 1000)])
+def test_bf16_layer_options(kl, qk_norm, inter, B, S, H, Hq, Hkv, I):
+    got, Y, dX, grads, saved, _, _ = _run_both(kl, B, S, H, Hq, Hkv, 128, I, kl.KL_BF16, 7, qk_norm=qk_norm,
+                                               inter=inter)
+    assert_rel(got["Y"], Y, TOL_BF16, "Y")
+    assert_rel(got["dX"], dX, TOL_BF16, "dX")
+    names = GRAD_NAMES + (("gamma_q", "gamma_k") if qk_norm else ())
+    for n in names:
+        assert_rel(got["d" + n], grads[n], TOL_BF16, "d" + n)
+    keys = ("q", "k", "v", "o") + (("q_pre", "k_pre", "rstd_q", "rstd_k") if qk_norm else ())
+    for k in keys:
         assert_rel(got["saved"][k], saved[k].reshape(got["saved"][k].shape), TOL_BF16, k)
 
 

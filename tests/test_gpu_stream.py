@@ -15,8 +15,9 @@ from _parity import TOL_BF16, TOL_F32, assert_rel
 pytestmark = pytest.mark.gpu
 
 
-def _inputs(n_layers, B, S, H, Hq, Hkv, d, I, V, seed, bf16):
-    layers = [synth.layer_weights(seed, H, Hq, Hkv, d, I, bf16=bf16, prefix=f"l{i}") for i in range(n_layers)]
+def _inputs(n_layers, B, S, H, Hq, Hkv, d, I, V, seed, bf16, qk_norm=False):
+    layers = [synth.layer_weights(seed, H, Hq, Hkv, d, I, bf16=bf16, prefix=f"l{i}", qk_norm=qk_norm)
+              for i in range(n_layers)]
     X = synth.normal(seed, "X", (B * S, H))
     W = synth.normal(seed, "lm.W", (V, H), std=0.02)
     if bf16:
@@ -57,6 +58,22 @@ def test_stream_matches_oracle_with_active_clip(kl, dt):
     got = L.run_stream(cfg, nl, V, layers, W, X, tgt, clip)
     _compare(got, ref, tol, ltol)
     assert got["result"][2] < 0.51
+
+
+def test_stream_with_layer_options(kl):
+    """Per-head q/k norms (their gains streamed with the layer, their gradients
+    in the global norm) and interleaved rotary planes, bf16, clip active."""
+    dims = dict(B=2, S=64, H=256, Hq=4, Hkv=2, d=128, I=512)
+    V, nl = 1024, 2
+    layers, X, W, tgt = _inputs(nl, **dims, V=V, seed=4, bf16=True, qk_norm=True)
+    ocfg = O.LayerConfig(**dims, qk_norm=True, rope_interleaved=True)
+    free = O.stack_fwd_bwd(ocfg, layers, W, X, tgt, max_norm=1e9)
+    clip = 0.5 * free["total_norm"]
+    ref = O.stack_fwd_bwd(ocfg, layers, W, X, tgt, max_norm=clip)
+    assert "gamma_q" in ref["grads"][0]
+    cfg = L.make_cfg(**dims, dtype=1, qk_norm=True, rope_interleaved=True)
+    got = L.run_stream(cfg, nl, V, layers, W, X, tgt, clip)
+    _compare(got, ref, TOL_BF16, 1e-3)
 
 
 def test_streamed_equals_bulk(kl):
