@@ -1,7 +1,7 @@
 """Benchmark of the GB300 Qwen3 layer path. Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload layer|attention|lmhead|stream]
+                  [--workload layer|attention|lmhead|stream|stream_recompute|stream_fwd64]
 
 Workloads (Qwen3-32B dims: hidden 5120, 64 query / 8 KV heads of dim 128,
 SwiGLU intermediate 25600, RoPE base 1e6, causal; bf16):
@@ -13,6 +13,16 @@ SwiGLU intermediate 25600, RoPE base 1e6, causal; bf16):
   stream     8 layers streamed from pinned host memory, batch 2 x seq 4096,
              lm-head CE, backward, global-norm clip at 1.0, gradients to
              device memory (one kl_stream_run per step)
+  stream_recompute
+             the same step keeping only each layer's input between forward
+             and backward (the layer's forward runs again before its backward)
+  stream_fwd64
+             64 layers forward only (kl_stream_forward), batch 1 x seq 2048,
+             weights streamed from pinned host memory; reports the driver's
+             device memory (independent of depth)
+The stream workloads also time the same call with every layer's weights
+already in device memory ("bulk": no uploads) to show how much of the host
+link the compute hides.
 
 `value` is whole-job tokens/s with inputs resident in HBM; `e2e` is the same
 metric through the C ABI with each step's inputs copied from pinned host
@@ -43,13 +53,19 @@ WORKLOADS = {
     "layer": dict(B=1, S=2048, desc="qwen3_32b_layer_fwd_bwd"),
     "attention": dict(B=1, S=32768, desc="gqa_attention_fwd_bwd_S32768"),
     "lmhead": dict(N=4096, V=151936, desc="lmhead_ce_argmax_fwd_bwd_N4096_V151936"),
-    "stream": dict(B=2, S=4096, L=8, V=151936, clip=1.0, desc="stream_8_layers_T8192_ce_clip"),
+    "stream": dict(B=2, S=4096, L=8, V=151936, clip=1.0, mode=0, desc="stream_8_layers_T8192_ce_clip"),
+    "stream_recompute": dict(B=2, S=4096, L=8, V=151936, clip=1.0, mode=1,
+                             desc="stream_8_layers_T8192_ce_clip_recompute"),
+    "stream_fwd64": dict(B=1, S=2048, L=64, distinct=4, mode=2, desc="stream_forward_64_layers_T2048"),
 }
 METRICS = {
     "layer": METRIC,
     "attention": "causal GQA attention fwd+bwd tokens/s (seq 32768, 64/8 heads, d 128, bf16, 1 GB300)",
     "lmhead": "lm-head CE+argmax fwd+bwd tokens/s (4096 tokens, vocab 151936, bf16, 1 GB300)",
     "stream": "8-layer streamed training step tokens/s (batch 2 x 4096, bf16, 1 GB300)",
+    "stream_recompute": "8-layer streamed training step with activation recompute tokens/s (batch 2 x 4096, bf16, "
+                        "1 GB300)",
+    "stream_fwd64": "64-layer streamed forward tokens/s (batch 1 x 2048, bf16, 1 GB300)",
 }
 
 
@@ -271,51 +287,108 @@ def setup_lmhead(torch, K, L, synth, device, seed):
     return N, (lambda: run(X, tgt)), e2e, X.numel() * 2 + N * 4, 4, cfgd, keep
 
 
-def setup_stream(torch, K, L, synth, device, seed):
-    wl = WORKLOADS["stream"]
-    B, S, nl, V = wl["B"], wl["S"], wl["L"], wl["V"]
+def setup_stream(torch, K, L, synth, device, seed, name="stream"):
+    wl = WORKLOADS[name]
+    B, S, nl, mode = wl["B"], wl["S"], wl["L"], wl["mode"]
+    train = mode != K.KL_STREAM_FORWARD
+    V = wl.get("V", 0)
     T, H = B * S, QWEN["H"]
     cfg = L.make_cfg(B, S, **QWEN, dtype=K.KL_BF16)
     bf = torch.bfloat16
-    hosts, structs = [], []
-    for li in range(nl):
+    distinct = wl.get("distinct", nl)   # host weight sets; layer l uses set l % distinct
+    hosts = []
+    for li in range(distinct):
         w = {}
         for n, shp in L.weight_shapes(cfg).items():
             t = synth.device_normal(shp, 0.02, 1.0 if n.startswith("gamma") else 0.0, seed, f"l{li}.{n}", bf, device)
             w[n] = t.cpu().pin_memory()
         hosts.append(w)
-        structs.append(L.weights_struct(w))
-    W = synth.device_normal((V, H), 0.02, 0.0, seed, "lm.W", bf, device).cpu().pin_memory()
+    structs = [L.weights_struct(hosts[li % distinct]) for li in range(nl)]
+    W = synth.device_normal((V, H), 0.02, 0.0, seed, "lm.W", bf, device).cpu().pin_memory() if train else None
     X = synth.device_normal((T, H), 1.0, 0.0, seed, "X", bf, device)
-    tgt = synth.device_randint((T,), V, seed, "lm.targets", device)
-    h = K.kl_stream_create(K.StreamCfg(cfg, nl, V), structs, W.data_ptr())
+    tgt = synth.device_randint((T,), V, seed, "lm.targets", device) if train else None
+    Y = torch.empty_like(X)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info(device)[0]
+    h = K.kl_stream_create(K.StreamCfg(cfg, nl, V, mode), structs, W.data_ptr() if train else None)
+    free1 = torch.cuda.mem_get_info(device)[0]
     grads, gs = [], []
-    for _ in range(nl):
-        g = {n: torch.empty(shp, dtype=torch.float32, device=device) for n, shp in L.weight_shapes(cfg).items()}
-        grads.append(g)
-        gs.append(K.LayerGrads(*[g[n].data_ptr() for n in K.WEIGHT_FIELDS], K.KL_F32))
-    dW = torch.empty(V, H, dtype=torch.float32, device=device)
+    if train:
+        for _ in range(nl):
+            g = {n: torch.empty(shp, dtype=torch.float32, device=device) for n, shp in L.weight_shapes(cfg).items()}
+            grads.append(g)
+            gs.append(K.LayerGrads(*[g[n].data_ptr() for n in K.WEIGHT_FIELDS], K.KL_F32))
+    dW = torch.empty(V, H, dtype=torch.float32, device=device) if train else None
     stream = torch.cuda.current_stream(device)
 
-    def run(x, t):
-        K.kl_stream_run(h, x.data_ptr(), t.data_ptr(), wl["clip"], gs, dW.data_ptr(), stream)
+    def run(handle, x, t):
+        if train:
+            K.kl_stream_run(handle, x.data_ptr(), t.data_ptr(), wl["clip"], gs, dW.data_ptr(), stream)
+        else:
+            K.kl_stream_forward(handle, x.data_ptr(), Y.data_ptr(), stream)
 
-    hX, ht = X.cpu().pin_memory(), tgt.cpu().pin_memory()
-    X2, t2 = torch.empty_like(X), torch.empty_like(tgt)
+    hX = X.cpu().pin_memory()
+    ht = tgt.cpu().pin_memory() if train else None
+    hY = torch.empty_like(hX).pin_memory()
+    X2 = torch.empty_like(X)
+    t2 = torch.empty_like(tgt) if train else None
 
     def e2e():
         X2.copy_(hX, non_blocking=True)
-        t2.copy_(ht, non_blocking=True)
-        run(X2, t2)          # returns after the step (loss, norm, coef read back)
+        if train:
+            t2.copy_(ht, non_blocking=True)
+        run(h, X2, t2)       # returns after the step (training: loss, norm, coef read back)
+        if not train:
+            hY.copy_(Y, non_blocking=True)
 
-    keep = (hosts, W, X, tgt, grads, dW, hX, ht, X2, t2, h)
-    cfgd = {"workload": wl["desc"], "layers": nl, "batch": B, "seq_len": S, "hidden": H, "vocab": V,
-            "clip_max_norm": wl["clip"], "weights": "pinned host, two device slots",
-            "grads": "fp32, device", "l2": "inputs larger than L2"}
-    return T, (lambda: run(X, tgt)), e2e, X.numel() * 2 + T * 4, 12, cfgd, keep
+    layer_bytes = sum(t.numel() * t.element_size() for t in hosts[0].values())
+    weight_h2d = nl * layer_bytes * (2 if train else 1) + (V * H * 2 if train else 0)
+
+    def after(args):
+        """Destroys the streamed driver, then times the same call with every
+        layer's weights already in device memory (bulk: no uploads)."""
+        dev_bytes = K.kl_stream_device_bytes(h)
+        K.kl_stream_destroy(h)
+        dev_sets = [{n: t.to(device) for n, t in w.items()} for w in hosts]
+        dstructs = [L.weights_struct(dev_sets[li % distinct]) for li in range(nl)]
+        Wd = W.to(device) if train else None
+        hb = K.kl_stream_create(K.StreamCfg(cfg, nl, V, mode), dstructs, Wd.data_ptr() if train else None)
+        try:
+            for _ in range(args.warmup):
+                run(hb, X, tgt)
+            torch.cuda.synchronize()
+            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b0.record(stream)
+            for _ in range(args.steps):
+                run(hb, X, tgt)
+            b1.record(stream)
+            torch.cuda.synchronize()
+            ms_bulk = b0.elapsed_time(b1) / args.steps
+        finally:
+            K.kl_stream_destroy(hb)
+        del dev_sets, Wd
+        return {"driver_device_bytes": dev_bytes, "device_bytes_at_create": free0 - free1,
+                "weight_h2d_bytes_per_step": weight_h2d, "ms_per_step_bulk": round(ms_bulk, 3)}
+
+    keep = {"objs": (hosts, W, X, tgt, grads, dW, Y, hX, ht, hY, X2, t2), "after": after}
+    cfgd = {"workload": wl["desc"], "layers": nl, "batch": B, "seq_len": S, "hidden": H,
+            "weights": "pinned host, two device slots", "l2": "inputs larger than L2"}
+    if distinct < nl:
+        cfgd["host_weight_sets"] = f"{distinct} distinct sets, layer l uses set l mod {distinct}; every layer " \
+                                   "is uploaded on its own"
+    if train:
+        cfgd.update(vocab=V, clip_max_norm=wl["clip"], grads="fp32, device",
+                    activations="inputs only, layer forward recomputed" if mode == K.KL_STREAM_RECOMPUTE
+                    else "every layer's saved set")
+        return T, (lambda: run(h, X, tgt)), e2e, X.numel() * 2 + T * 4, 12, cfgd, keep
+    cfgd.update(activations="one layer's working set")
+    return T, (lambda: run(h, X, tgt)), e2e, X.numel() * 2, Y.numel() * 2, cfgd, keep
 
 
-SETUP = {"layer": setup_layer, "attention": setup_attention, "lmhead": setup_lmhead, "stream": setup_stream}
+SETUP = {"layer": setup_layer, "attention": setup_attention, "lmhead": setup_lmhead,
+         "stream": lambda *a, **k: setup_stream(*a, **k, name="stream"),
+         "stream_recompute": lambda *a, **k: setup_stream(*a, **k, name="stream_recompute"),
+         "stream_fwd64": lambda *a, **k: setup_stream(*a, **k, name="stream_fwd64")}
 
 
 def bench_ours(args, rank, world, local_rank, dist):
@@ -369,14 +442,17 @@ def bench_ours(args, rank, world, local_rank, dist):
     barrier()
     ms_e2e = f0.elapsed_time(f1)
     K.kl_device_status(stream)
-    if args.workload == "stream":
-        K.kl_stream_destroy(keep[-1])
+    extra = None
+    if isinstance(keep, dict) and "after" in keep:
+        extra = keep["after"](args)
+        extra["link_hidden"] = round(extra["ms_per_step_bulk"] / (ms / args.steps), 4)
+        extra["weight_h2d_gbs"] = round(extra["weight_h2d_bytes_per_step"] / (ms / args.steps) / 1e6, 1)
     if dist is not None:
         t = torch.tensor([ms, ms_e2e], device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms, ms_e2e = float(t[0]), float(t[1])
     return dict(ms=ms, ms_e2e=ms_e2e, prof=prof, clocks=clk, launches=int(launches), units=units, h2d=h2d,
-                d2h=d2h, config=cfgd)
+                d2h=d2h, config=cfgd, extra=extra)
 
 
 # ----------------------------------------------------------------------------
@@ -435,7 +511,21 @@ def oracle_sample(workload: str, steps: int):
             O.lmhead_ce(X, W, t)
         units = N
         desc = f"lm-head CE+argmax fwd+bwd on {N} tokens, hidden 5120, vocab {V}"
-    else:   # stream: one layer + the head on a token sample, scaled to 8 layers
+    elif workload == "stream_fwd64":   # one layer forward on a token sample, scaled to 64 layers
+        S = 512
+        cfg = O.LayerConfig(B=1, S=S, H=Q["H"], Hq=Q["Hq"], Hkv=Q["Hkv"], d=Q["d"], I=Q["I"])
+        w = _oracle_weights(rng, Q["H"], Q["Hq"], Q["Hkv"], Q["d"], Q["I"])
+        X = rng.standard_normal((S, Q["H"]))
+        nl = WORKLOADS["stream_fwd64"]["L"]
+
+        def one():
+            O.layer_forward(cfg, w, X)
+            return 0.0
+        units = S
+        desc = (f"one full-dims layer forward on {S} tokens (batch 1, seq {S}); step time = {nl} x layer; "
+                f"tokens/s at seq 2048 is below this (attention grows with the sequence)")
+    else:   # stream, stream_recompute: one layer + the head on a token sample, scaled to 8 layers
+        # (recompute changes where activations live, not what is computed)
         S = 256
         cfg = O.LayerConfig(B=1, S=S, H=Q["H"], Hq=Q["Hq"], Hkv=Q["Hkv"], d=Q["d"], I=Q["I"])
         w = _oracle_weights(rng, Q["H"], Q["Hq"], Q["Hkv"], Q["d"], Q["I"])
@@ -459,7 +549,7 @@ def oracle_sample(workload: str, steps: int):
         t0 = time.perf_counter()
         th = one()
         dt = time.perf_counter() - t0
-        if workload == "stream":
+        if workload.startswith("stream"):
             dt = nl * (dt - th) + th
         times.append(dt)
     sec = statistics.median(times)
@@ -477,7 +567,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
-    if args.workload == "stream" and "--steps" not in sys.argv:
+    if args.workload.startswith("stream") and "--steps" not in sys.argv:
         args.steps = 5
     world = _env_int("WORLD_SIZE", 1)
     rank = _env_int("RANK", 0)
@@ -561,6 +651,8 @@ def main():
             "roofline": roof, "kernels": kernels, "gpu_launches": r["launches"], "clocks": r["clocks"],
             "e2e": {"value": round(e2e, 1), "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
                     "d2h_bytes_per_step": r["d2h"]}}
+    if r["extra"] is not None:
+        line["stream"] = r["extra"]
     if world == 1 and not args.no_cpu_baseline:
         tps, sec, cores, desc = oracle_sample(args.workload, 1)
         line["cpu_baseline"] = {"value": round(tps, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",

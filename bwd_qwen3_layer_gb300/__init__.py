@@ -59,8 +59,13 @@ class LmheadCfg(ctypes.Structure):
     _fields_ = [("N", _i32), ("H", _i32), ("V", _i32), ("dtype", _i32), ("dw_dtype", _i32)]
 
 
+KL_STREAM_SAVE_ALL = 0
+KL_STREAM_RECOMPUTE = 1
+KL_STREAM_FORWARD = 2
+
+
 class StreamCfg(ctypes.Structure):
-    _fields_ = [("layer", LayerCfg), ("n_layers", _i32), ("V", _i32)]
+    _fields_ = [("layer", LayerCfg), ("n_layers", _i32), ("V", _i32), ("mode", _i32)]
 
 
 class StreamResult(ctypes.Structure):
@@ -99,6 +104,7 @@ _SIGNATURES = {
                                         _vp, _vp, _vp, _vp, _sz, _vp]),
     "kl_stream_create": (ctypes.c_int, [_P(StreamCfg), _P(LayerWeights), _vp, _P(_vp)]),
     "kl_stream_run": (ctypes.c_int, [_vp, _vp, _vp, _f32, _P(LayerGrads), _vp, _P(StreamResult), _vp]),
+    "kl_stream_forward": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
     "kl_stream_device_bytes": (_sz, [_vp]),
     "kl_stream_destroy": (None, [_vp]),
     "kl_profile_enable": (ctypes.c_int, [_i32]),
@@ -287,6 +293,10 @@ def kl_stream_run(handle: int, X: int, targets: int, clip_max_norm: float, grads
     check(load().kl_stream_run(handle, X, targets, clip_max_norm, arr, dW_lm, ctypes.byref(res),
                                _stream(stream)))
     return res
+
+
+def kl_stream_forward(handle: int, X: int, Y: int, stream=None) -> None:
+    check(load().kl_stream_forward(handle, X, Y, _stream(stream)))
 
 
 def kl_stream_device_bytes(handle: int) -> int:

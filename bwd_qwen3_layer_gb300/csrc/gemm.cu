@@ -69,7 +69,7 @@ struct GemmProb {
   int rope_S;
   int whole_tiles;        // tiles computed whole; the rest (tail) are split along K
   int tail_tiles, tail_splits;
-  float* tail_acc;        // [tail_tiles][256][256] fp32
+  float* tail_acc;        // [tail_splits][tail_tiles][256][256] fp32, one slice per K range
 };
 
 struct GemmParams {
@@ -87,7 +87,7 @@ struct Unit {
   int p;
   int m0, n0;
   int kb_lo, kb_hi;
-  int tail;               // index among the problem's split tail tiles, or -1
+  int tail;               // scratch slice of a split last-round tile (split * tail_tiles + tile), or -1
 };
 
 __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
@@ -449,8 +449,8 @@ __device__ __forceinline__ Unit decode_unit_cl(const GemmParams& P, int u) {
     // last-round tiles, split along K (split-major as well)
     const int t = local - pr.whole_tiles;
     si = t / pr.tail_tiles;
-    r.tail = t - si * pr.tail_tiles;
-    tile = pr.whole_tiles + r.tail;
+    r.tail = t;
+    tile = pr.whole_tiles + (t - si * pr.tail_tiles);
     nsplit = pr.tail_splits;
   } else {
     si = local / ntile;
@@ -800,12 +800,13 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
             if (row < pr.M) store_swiglu_bwd(pr, row, col0, v, cur);
           } else if (row < pr.M) {
             if (un.tail >= 0) {
-              // a K-range of a last-round tile: accumulate into the compact fp32 scratch
-              float* a = pr.tail_acc + (static_cast<int64_t>(un.tail) * 256 + (row - un.m0)) * 256 + (col0 - un.n0);
+              // a K range of a last-round tile: its own fp32 scratch slice (summed in a fixed order later)
+              float4* a = reinterpret_cast<float4*>(pr.tail_acc + (static_cast<int64_t>(un.tail) * 256 + (row - un.m0)) *
+                                                                      256 + (col0 - un.n0));
 #pragma unroll
               for (int j = 0; j < 32; j += 4)
-                red_add_v4(a + j, __uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
-                           __uint_as_float(v[j + 3]));
+                a[j / 4] = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                                       __uint_as_float(v[j + 3]));
             } else {
               store_chunk(pr, row, col0, v);
               if (pr.epi == GEMM_EPI_ROWDOT) {
@@ -847,9 +848,10 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
   }
 }
 
-// Finishes the split last-round tiles of one problem: C = acc + R, converted.
+// Finishes the split last-round tiles of one problem: C = (sum of the K-range
+// slices, in split order) + R, converted. Deterministic: no atomics anywhere.
 struct TailFin {
-  int M, N, m_tiles, n_tiles, n_fast, whole;
+  int M, N, m_tiles, n_tiles, n_fast, whole, tiles, splits;
   const float* acc;
   void* C;
   int64_t ldc;
@@ -873,7 +875,12 @@ __global__ void __launch_bounds__(256) gemm_tail_finalize_kernel(const TailFin f
   const int c = (threadIdx.x & 63) * 4;
   const int row = m0 + r;
   if (row >= f.M) return;
-  const float4 a = *reinterpret_cast<const float4*>(f.acc + (static_cast<int64_t>(t) * 256 + r) * 256 + c);
+  float4 a = *reinterpret_cast<const float4*>(f.acc + (static_cast<int64_t>(t) * 256 + r) * 256 + c);
+  for (int sp = 1; sp < f.splits; ++sp) {
+    const float4 b =
+        *reinterpret_cast<const float4*>(f.acc + (static_cast<int64_t>(sp * f.tiles + t) * 256 + r) * 256 + c);
+    a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+  }
   const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
@@ -1230,7 +1237,8 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
   const int cap = max_gemm_clusters(dev, cfg);
   // Last round: if the units leave some CTA pairs idle in the last round, split
   // the last problem's last tiles along K so that the round's work spreads
-  // over every pair (accumulated in tail_ws, finished below).
+  // over every pair (each K range stored to its own slice of tail_ws, the
+  // slices summed in split order below).
   int tail_prob = -1;
   {
     const int lp = nspec - 1;
@@ -1243,7 +1251,7 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
       int ts = cap / rem;
       const int max_ts = pr.kb_total / 8;            // at least 8 k-blocks per piece
       if (ts > max_ts) ts = max_ts;
-      const size_t need = static_cast<size_t>(rem) * 256 * 256 * 4;
+      const size_t need = static_cast<size_t>(ts) * rem * 256 * 256 * 4;   // ts * rem <= cap slices
       if (ts >= 2 && need <= s.tail_ws_bytes) {
         pr.whole_tiles = tiles - rem;
         pr.tail_tiles = rem;
@@ -1251,7 +1259,6 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
         pr.tail_acc = s.tail_ws;
         units += rem * (ts - 1);
         tail_prob = lp;
-        KL_CUDA(cudaMemsetAsync(s.tail_ws, 0, need, st));
       }
     }
   }
@@ -1272,11 +1279,12 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
     const GemmSpec& s = specs_in[order[tail_prob]];
     TailFin f;
     f.M = pr.M; f.N = pr.N; f.m_tiles = pr.m_tiles; f.n_tiles = pr.n_tiles; f.n_fast = pr.n_fast;
-    f.whole = pr.whole_tiles; f.acc = pr.tail_acc;
+    f.whole = pr.whole_tiles; f.tiles = pr.tail_tiles; f.splits = pr.tail_splits; f.acc = pr.tail_acc;
     f.C = s.C; f.ldc = s.ldc; f.c_f32 = s.c_dtype == KL_F32;
     f.R = s.R; f.ldr = s.ldr; f.r_f32 = s.r_dtype == KL_F32;
     const double n = static_cast<double>(pr.tail_tiles) * 256 * 256;
-    ProfScope ps("gemm_tail_finalize", st, 0.0, n * (4 + dtype_size(s.c_dtype) + (s.R ? dtype_size(s.r_dtype) : 0)));
+    ProfScope ps("gemm_tail_finalize", st, 0.0,
+                 n * (4.0 * pr.tail_splits + dtype_size(s.c_dtype) + (s.R ? dtype_size(s.r_dtype) : 0)));
     gemm_tail_finalize_kernel<<<dim3(pr.tail_tiles, 64), 256, 0, st>>>(f);
     KL_CUDA(cudaGetLastError());
   }

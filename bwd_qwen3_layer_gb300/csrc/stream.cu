@@ -20,6 +20,15 @@
 // If the caller's layer weights are already device memory the driver runs in
 // "bulk" mode: no slots, no uploads, the same kernels in the same order. Its
 // results are what the streamed mode is compared with.
+//
+// Modes. SAVE_ALL keeps every layer's saved activations from the forward to
+// the backward. RECOMPUTE keeps only each layer's input (the previous layer's
+// output) and runs the layer's forward again, into one shared saved set, right
+// before its backward, with the weights already resident for the backward (the
+// last layer's set is still intact after the forward and is not recomputed);
+// the price is one more layer forward per layer but the last. FORWARD holds
+// only what a forward needs: two weight slots, one layer's working set, two
+// hidden buffers; device memory does not grow with depth.
 #include <string.h>
 
 #include <vector>
@@ -193,6 +202,7 @@ struct kl_stream {
   kl_stream_cfg cfg;
   int device = 0;
   bool bulk = false;
+  int mode = KL_STREAM_SAVE_ALL;
   std::vector<kl_layer_weights> layers;  // as given (host, or device in bulk mode)
   const void* lm_host = nullptr;
   std::vector<void*> allocs;
@@ -204,11 +214,11 @@ struct kl_stream {
   cudaEvent_t ev_loaded[2] = {}, ev_used[2] = {}, ev_lm = nullptr;
   const void* lm_w = nullptr;
   // activations and workspace
-  std::vector<kl_layer_saved> saved;
-  std::vector<void*> hidden;   // output of layer l
+  std::vector<kl_layer_saved> saved;   // one per layer (SAVE_ALL) or one shared set
+  std::vector<void*> hidden;   // output of layer l (two alternating buffers with FORWARD)
   void* dx[2] = {};
-  void* bwd_ws = nullptr;
-  size_t bwd_ws_bytes = 0;
+  void* ws = nullptr;          // layer workspace (the backward's, which the forward reuses)
+  size_t ws_bytes = 0;
   void* lm_ws = nullptr;
   size_t lm_ws_bytes = 0;
   float* loss = nullptr;
@@ -233,6 +243,9 @@ struct kl_stream {
     device_bytes += align_up(bytes, 256);
     return p;
   }
+  kl_layer_saved* saved_for(int l) { return &saved[mode == KL_STREAM_SAVE_ALL ? l : 0]; }
+  void* hidden_of(int l) { return hidden[mode == KL_STREAM_FORWARD ? (l & 1) : l]; }
+
   void release() {
     for (void* p : allocs) cudaFree(p);
     allocs.clear();
@@ -291,22 +304,76 @@ kl_status make_stream_events(kl_stream* s) {
   return KL_OK;
 }
 
+// The weights of layer l for the compute stream: the caller's (bulk) or a
+// slot, uploaded if it is not resident (never into keep_slot), the compute
+// stream made to wait for the upload.
+kl_status weights_for(kl_stream* s, int l, int keep_slot, int* slot, kl_layer_weights* w, cudaStream_t cs) {
+  if (s->bulk) {
+    *w = s->layers[l];
+    *slot = -1;
+    return KL_OK;
+  }
+  KL_TRY(acquire(s, l, keep_slot, slot));
+  KL_CUDA(cudaStreamWaitEvent(cs, s->ev_loaded[*slot], 0));
+  *w = s->slot[*slot];
+  return KL_OK;
+}
+
+// Start of a pass: the slots' contents may be stale (weights change between
+// calls), and nothing of this pass has used them yet.
+kl_status begin_pass(kl_stream* s, cudaStream_t cs) {
+  if (s->bulk) return KL_OK;
+  s->slot_layer[0] = s->slot_layer[1] = -1;
+  KL_CUDA(cudaEventRecord(s->ev_used[0], cs));
+  KL_CUDA(cudaEventRecord(s->ev_used[1], cs));
+  return KL_OK;
+}
+
+// Forward through every layer: layer l reads X (l = 0) or the previous
+// layer's output, writes hidden_of(l) (`last` for the last layer when given),
+// with layer l + 1's weights uploaded while layer l runs. *cur receives the
+// slot holding the last layer.
+kl_status forward_layers(kl_stream* s, const void* X, void* last, cudaStream_t cs, int* cur_out) {
+  const kl_layer_cfg& c = s->cfg.layer;
+  const int L = s->cfg.n_layers;
+  int cur = -1;
+  for (int l = 0; l < L; ++l) {
+    kl_layer_weights w;
+    KL_TRY(weights_for(s, l, cur == 0 ? 1 : 0, &cur, &w, cs));
+    if (!s->bulk && l + 1 < L) {
+      int nxt;
+      KL_TRY(acquire(s, l + 1, cur, &nxt));  // prefetch while layer l runs
+    }
+    const void* xin = l == 0 ? X : s->hidden_of(l - 1);
+    void* out = (l == L - 1 && last) ? last : s->hidden_of(l);
+    KL_TRY(kl_layer_forward(&c, &w, xin, out, s->saved_for(l), s->ws, s->ws_bytes, cs));
+    if (!s->bulk) KL_CUDA(cudaEventRecord(s->ev_used[cur], cs));
+  }
+  *cur_out = cur;
+  return KL_OK;
+}
+
 }  // namespace
 
 extern "C" {
 
 kl_status kl_stream_create(const kl_stream_cfg* cfg, const kl_layer_weights* host_layers,
                            const void* host_lm_head, kl_stream** out) {
-  if (!cfg || !host_layers || !host_lm_head || !out)
-    return set_error(KL_ERR_INVALID_ARG, "kl_stream_create: null argument");
+  if (!cfg || !host_layers || !out) return set_error(KL_ERR_INVALID_ARG, "kl_stream_create: null argument");
   *out = nullptr;
-  if (cfg->n_layers < 1 || cfg->V < 1) return set_error(KL_ERR_INVALID_ARG, "kl_stream_create: bad n_layers or V");
+  const int mode = cfg->mode;
+  if (mode != KL_STREAM_SAVE_ALL && mode != KL_STREAM_RECOMPUTE && mode != KL_STREAM_FORWARD)
+    return set_error(KL_ERR_INVALID_ARG, "kl_stream_create: bad mode %d", mode);
+  const bool train = mode != KL_STREAM_FORWARD;
+  if (train && !host_lm_head) return set_error(KL_ERR_INVALID_ARG, "kl_stream_create: null lm-head weight");
+  if (cfg->n_layers < 1 || (train && cfg->V < 1))
+    return set_error(KL_ERR_INVALID_ARG, "kl_stream_create: bad n_layers or V");
   const kl_layer_cfg& c = cfg->layer;
   const size_t saved_bytes = kl_layer_saved_bytes(&c);
   if (saved_bytes == 0) return KL_ERR_INVALID_ARG;  // message set by the size query's checks
-  kl_lmhead_cfg lc = {c.B * c.S, c.H, cfg->V, c.dtype, KL_F32};
-  const size_t lm_ws = kl_lmhead_workspace_bytes(&lc);
-  if (lm_ws == 0) return KL_ERR_UNSUPPORTED;
+  kl_lmhead_cfg lc = {c.B * c.S, c.H, train ? cfg->V : 1, c.dtype, KL_F32};
+  const size_t lm_ws = train ? kl_lmhead_workspace_bytes(&lc) : 0;
+  if (train && lm_ws == 0) return KL_ERR_UNSUPPORTED;
   for (int l = 0; l < cfg->n_layers; ++l)
     for (int i = 0; i < n_weights(c); ++i)
       if (!*wfield(const_cast<kl_layer_weights&>(host_layers[l]), i))
@@ -317,6 +384,7 @@ kl_status kl_stream_create(const kl_stream_cfg* cfg, const kl_layer_weights* hos
   KL_CUDA(cudaGetDevice(&s->device));
   s->layers.assign(host_layers, host_layers + cfg->n_layers);
   s->lm_host = host_lm_head;
+  s->mode = mode;
   s->bulk = is_device_ptr(host_layers[0].wq);
   kl_status st = KL_OK;
   const int L = cfg->n_layers;
@@ -324,32 +392,34 @@ kl_status kl_stream_create(const kl_stream_cfg* cfg, const kl_layer_weights* hos
   if (!s->bulk) {
     for (int k = 0; k < 2; ++k)
       for (int i = 0; i < n_weights(c); ++i) *wfield(s->slot[k], i) = s->alloc(weight_elems(c, i) * es, &st);
-    s->lm_w = s->alloc(static_cast<size_t>(cfg->V) * c.H * es, &st);
+    if (train) s->lm_w = s->alloc(static_cast<size_t>(cfg->V) * c.H * es, &st);
     if (st == KL_OK) st = make_stream_events(s);
   } else {
-    if (!is_device_ptr(host_lm_head))
+    if (train && !is_device_ptr(host_lm_head))
       st = set_error(KL_ERR_INVALID_ARG, "kl_stream_create: device layers need a device lm-head weight");
     s->lm_w = host_lm_head;
   }
-  s->saved.resize(L);
-  s->hidden.resize(L);
-  for (int l = 0; l < L && st == KL_OK; ++l) {
+  s->saved.resize(mode == KL_STREAM_SAVE_ALL ? L : 1);
+  s->hidden.resize(mode == KL_STREAM_FORWARD ? 2 : L);
+  for (size_t i = 0; i < s->saved.size() && st == KL_OK; ++i) {
     void* mem = s->alloc(saved_bytes, &st);
-    if (st == KL_OK) st = kl_layer_saved_carve(&c, mem, saved_bytes, &s->saved[l]);
-    s->hidden[l] = s->alloc(T * c.H * es, &st);
+    if (st == KL_OK) st = kl_layer_saved_carve(&c, mem, saved_bytes, &s->saved[i]);
   }
-  s->dx[0] = s->alloc(T * c.H * es, &st);
-  s->dx[1] = s->alloc(T * c.H * es, &st);
-  s->bwd_ws_bytes = kl_layer_bwd_workspace_bytes(&c);
-  s->bwd_ws = s->alloc(s->bwd_ws_bytes, &st);
-  s->lm_ws_bytes = lm_ws;
-  s->lm_ws = s->alloc(lm_ws, &st);
-  s->loss = static_cast<float*>(s->alloc(sizeof(float), &st));
-  s->argmax = static_cast<int32_t*>(s->alloc(T * sizeof(int32_t), &st));
-  s->max_refs = n_weights(c) * L + 1;
-  s->partials = static_cast<double*>(s->alloc(static_cast<size_t>(s->max_refs) * SUMSQ_BLOCKS * 8, &st));
-  s->result = static_cast<float*>(s->alloc(4 * sizeof(float), &st));
-  s->refs = static_cast<GradRef*>(s->alloc(static_cast<size_t>(s->max_refs) * sizeof(GradRef), &st));
+  for (size_t i = 0; i < s->hidden.size(); ++i) s->hidden[i] = s->alloc(T * c.H * es, &st);
+  s->ws_bytes = train ? kl_layer_bwd_workspace_bytes(&c) : kl_layer_fwd_workspace_bytes(&c);
+  s->ws = s->alloc(s->ws_bytes, &st);
+  if (train) {
+    s->dx[0] = s->alloc(T * c.H * es, &st);
+    s->dx[1] = s->alloc(T * c.H * es, &st);
+    s->lm_ws_bytes = lm_ws;
+    s->lm_ws = s->alloc(lm_ws, &st);
+    s->loss = static_cast<float*>(s->alloc(sizeof(float), &st));
+    s->argmax = static_cast<int32_t*>(s->alloc(T * sizeof(int32_t), &st));
+    s->max_refs = n_weights(c) * L + 1;
+    s->partials = static_cast<double*>(s->alloc(static_cast<size_t>(s->max_refs) * SUMSQ_BLOCKS * 8, &st));
+    s->result = static_cast<float*>(s->alloc(4 * sizeof(float), &st));
+    s->refs = static_cast<GradRef*>(s->alloc(static_cast<size_t>(s->max_refs) * sizeof(GradRef), &st));
+  }
   if (st != KL_OK) {
     s->release();
     delete s;
@@ -365,6 +435,8 @@ kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets, flo
   if (!s || !X || !targets || !grads || !dW_lm || !result)
     return set_error(KL_ERR_INVALID_ARG, "kl_stream_run: null argument");
   if (!(clip_max_norm > 0.f)) return set_error(KL_ERR_INVALID_ARG, "kl_stream_run: clip_max_norm must be > 0");
+  if (s->mode == KL_STREAM_FORWARD)
+    return set_error(KL_ERR_INVALID_ARG, "kl_stream_run: the driver was created forward-only");
   int dev = -1;
   KL_CUDA(cudaGetDevice(&dev));
   if (dev != s->device) return set_error(KL_ERR_INVALID_ARG, "kl_stream_run: created on device %d, current %d", s->device, dev);
@@ -430,37 +502,12 @@ kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets, flo
     KL_CUDA(cudaMemcpyAsync(const_cast<void*>(s->lm_w), s->lm_host, static_cast<size_t>(s->cfg.V) * c.H * es,
                             cudaMemcpyHostToDevice, s->copy));
     KL_CUDA(cudaEventRecord(s->ev_lm, s->copy));
-    // the slots' contents may be stale (weights change between steps)
-    s->slot_layer[0] = s->slot_layer[1] = -1;
-    KL_CUDA(cudaEventRecord(s->ev_used[0], cs));
-    KL_CUDA(cudaEventRecord(s->ev_used[1], cs));
   }
-  auto weights_for = [&](int l, int keep_slot, int* slot, kl_layer_weights* w) -> kl_status {
-    if (s->bulk) {
-      *w = s->layers[l];
-      *slot = -1;
-      return KL_OK;
-    }
-    KL_TRY(acquire(s, l, keep_slot, slot));
-    KL_CUDA(cudaStreamWaitEvent(cs, s->ev_loaded[*slot], 0));
-    *w = s->slot[*slot];
-    return KL_OK;
-  };
+  KL_TRY(begin_pass(s, cs));
 
   // ---------------- forward ----------------
   int cur = -1;
-  for (int l = 0; l < L; ++l) {
-    kl_layer_weights w;
-    KL_TRY(weights_for(l, cur == 0 ? 1 : 0, &cur, &w));
-    if (!s->bulk && l + 1 < L) {
-      int nxt;
-      KL_TRY(acquire(s, l + 1, cur, &nxt));  // prefetch while layer l runs
-    }
-    const void* xin = l == 0 ? X : s->hidden[l - 1];
-    // the backward workspace is idle during the forward pass: it serves as the forward's
-    KL_TRY(kl_layer_forward(&c, &w, xin, s->hidden[l], &s->saved[l], s->bwd_ws, s->bwd_ws_bytes, cs));
-    if (!s->bulk) KL_CUDA(cudaEventRecord(s->ev_used[cur], cs));
-  }
+  KL_TRY(forward_layers(s, X, nullptr, cs, &cur));
   // ---------------- lm-head ----------------
   if (!s->bulk) KL_CUDA(cudaStreamWaitEvent(cs, s->ev_lm, 0));
   kl_lmhead_cfg lc = {T, c.H, s->cfg.V, c.dtype, KL_F32};
@@ -471,12 +518,15 @@ kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets, flo
   int in = 0;
   for (int l = L - 1; l >= 0; --l) {
     kl_layer_weights w;
-    KL_TRY(weights_for(l, cur, &cur, &w));
+    KL_TRY(weights_for(s, l, cur, &cur, &w, cs));
     if (!s->bulk && l - 1 >= 0) {
       int nxt;
       KL_TRY(acquire(s, l - 1, cur, &nxt));
     }
-    KL_TRY(kl_layer_backward(&c, &w, &s->saved[l], s->dx[in], s->dx[in ^ 1], &src[l], s->bwd_ws, s->bwd_ws_bytes, cs));
+    kl_layer_saved* sv = s->saved_for(l);
+    if (s->mode == KL_STREAM_RECOMPUTE && l != L - 1)   // the layer's activations again, from its input
+      KL_TRY(kl_layer_forward(&c, &w, l == 0 ? X : s->hidden[l - 1], s->hidden[l], sv, s->ws, s->ws_bytes, cs));
+    KL_TRY(kl_layer_backward(&c, &w, sv, s->dx[in], s->dx[in ^ 1], &src[l], s->ws, s->ws_bytes, cs));
     in ^= 1;
     for (int i = 0; i < n_weights(c); ++i)
       KL_TRY(sumsq(s, static_cast<const float*>(*gfield(src[l], i)), static_cast<int64_t>(weight_elems(c, i)),
@@ -504,6 +554,20 @@ kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets, flo
   result->loss = host_res[0];
   result->total_norm = host_res[1];
   result->clip_coef = host_res[2];
+  return KL_OK;
+}
+
+kl_status kl_stream_forward(kl_stream* s, const void* X, void* Y, void* stream) {
+  if (!s || !X || !Y) return set_error(KL_ERR_INVALID_ARG, "kl_stream_forward: null argument");
+  int dev = -1;
+  KL_CUDA(cudaGetDevice(&dev));
+  if (dev != s->device)
+    return set_error(KL_ERR_INVALID_ARG, "kl_stream_forward: created on device %d, current %d", s->device, dev);
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  KL_TRY(begin_pass(s, cs));
+  int cur = -1;
+  KL_TRY(forward_layers(s, X, Y, cs, &cur));
+  KL_CUDA(cudaStreamSynchronize(cs));
   return KL_OK;
 }
 

@@ -151,31 +151,38 @@ def run_lmhead(N, H, V, X_host, W_host, targets_host, dtype=KL_BF16, dw_dtype=No
             "dX": dX.double().cpu().numpy(), "dW": dW.double().cpu().numpy()}
 
 
+def _stream_weights(cfg: LayerCfg, layers_host: list, weights_on_device: bool, device, keep: list) -> list:
+    """LayerWeights structs over pinned host (streamed) or device (bulk) copies
+    of each layer's host arrays (synth names); the tensors are kept in `keep`."""
+    dt = TORCH_DTYPE[cfg.dtype]
+    hl = []
+    for lw in layers_host:
+        w = {}
+        for n in weight_fields(cfg):
+            t = torch.as_tensor(lw[SYNTH_NAMES[n]], dtype=torch.float64).to(dt).contiguous()
+            w[n] = t.to(device) if weights_on_device else t.pin_memory()
+        keep.append(w)
+        hl.append(weights_struct(w))
+    return hl
+
+
 def run_stream(cfg: LayerCfg, n_layers: int, V: int, layers_host: list, W_lm_host, X_host, targets_host,
-               clip: float, weights_on_device=False, grads_on_host=False, device="cuda", repeat=1):
+               clip: float, weights_on_device=False, grads_on_host=False, device="cuda", repeat=1, mode=0):
     """One (or `repeat`) layer-streaming training step(s) through kl_stream_*.
 
     layers_host: per layer a dict of host arrays (synth names). Weights are
     handed over as pinned host memory (streamed) or device memory (bulk).
+    mode: KL_STREAM_SAVE_ALL (0) or KL_STREAM_RECOMPUTE (1).
     Returns dict(result=(loss, norm, coef), grads=[{name: fp64 array}], dW_lm=array, device_bytes)."""
     from . import (StreamCfg, kl_stream_create, kl_stream_destroy, kl_stream_device_bytes,
                    kl_stream_run)
 
     dt = cfg.dtype
     keep = []
-
-    def place(a, dtype):
-        t = torch.as_tensor(a, dtype=torch.float64).to(dtype).contiguous()
-        t = t.to(device) if weights_on_device else t.pin_memory()
-        keep.append(t)
-        return t
-
-    hl = []
-    for lw in layers_host:
-        w = {n: place(lw[SYNTH_NAMES[n]], TORCH_DTYPE[dt]) for n in weight_fields(cfg)}
-        hl.append(weights_struct(w))
-    W = place(W_lm_host, TORCH_DTYPE[dt])
-    scfg = StreamCfg(cfg, n_layers, V)
+    hl = _stream_weights(cfg, layers_host, weights_on_device, device, keep)
+    W = torch.as_tensor(W_lm_host, dtype=torch.float64).to(TORCH_DTYPE[dt]).contiguous()
+    W = W.to(device) if weights_on_device else W.pin_memory()
+    scfg = StreamCfg(cfg, n_layers, V, mode)
     h = kl_stream_create(scfg, hl, W.data_ptr())
     try:
         X = to_device(X_host, dt, device)
@@ -198,6 +205,32 @@ def run_stream(cfg: LayerCfg, n_layers: int, V: int, layers_host: list, W_lm_hos
         out = {"result": (res.loss, res.total_norm, res.clip_coef), "device_bytes": kl_stream_device_bytes(h),
                "grads": [{SYNTH_NAMES[n]: g[n].double().cpu().numpy() for n in weight_fields(cfg)} for g in gl],
                "dW_lm": dW.double().cpu().numpy()}
+    finally:
+        kl_stream_destroy(h)
+    return out
+
+
+def run_stream_forward(cfg: LayerCfg, layers_host: list, X_host, weights_on_device=False, device="cuda",
+                       mode=2, repeat=1, W_lm_host=None, V=0):
+    """Forward only through every layer with kl_stream_forward (weights
+    streamed from pinned host memory, or bulk from device memory). A training
+    mode (SAVE_ALL, RECOMPUTE) also needs the lm-head weight W_lm_host [V, H].
+    Returns dict(Y=fp64 array [T, H], device_bytes)."""
+    from . import StreamCfg, kl_stream_create, kl_stream_destroy, kl_stream_device_bytes, kl_stream_forward
+
+    keep = []
+    hl = _stream_weights(cfg, layers_host, weights_on_device, device, keep)
+    W = None
+    if W_lm_host is not None:
+        W = torch.as_tensor(W_lm_host, dtype=torch.float64).to(TORCH_DTYPE[cfg.dtype]).contiguous()
+        W = W.to(device) if weights_on_device else W.pin_memory()
+    h = kl_stream_create(StreamCfg(cfg, len(layers_host), V, mode), hl, None if W is None else W.data_ptr())
+    try:
+        X = to_device(X_host, cfg.dtype, device)
+        Y = torch.empty_like(X)
+        for _ in range(repeat):
+            kl_stream_forward(h, X.data_ptr(), Y.data_ptr())
+        out = {"Y": Y.double().cpu().numpy(), "device_bytes": kl_stream_device_bytes(h)}
     finally:
         kl_stream_destroy(h)
     return out

@@ -305,10 +305,25 @@ KL_API kl_status kl_attention_bwd(int32_t B, int32_t S, int32_t Hq, int32_t Hkv,
 
 typedef struct kl_stream kl_stream;
 
+/* What the driver keeps between a layer's forward and its backward. */
+enum {
+  KL_STREAM_SAVE_ALL = 0,   /* every layer's saved activations stay resident    */
+  KL_STREAM_RECOMPUTE = 1,  /* only each layer's input stays resident; the layer's
+                               forward is run again (same slot, same weights)
+                               right before its backward. Device memory for
+                               activations: one layer's saved set + T x H per
+                               layer, independent of depth otherwise          */
+  KL_STREAM_FORWARD = 2     /* forward only (kl_stream_forward): two weight
+                               slots, one layer's working set and two hidden
+                               buffers: device memory independent of depth;
+                               no lm-head weight, kl_stream_run refused       */
+};
+
 typedef struct kl_stream_cfg {
   kl_layer_cfg layer;  /* dims of every layer; dtype must be KL_BF16 or F32 */
   int32_t n_layers;
-  int32_t V;           /* lm-head vocabulary                               */
+  int32_t V;           /* lm-head vocabulary (ignored by KL_STREAM_FORWARD) */
+  int32_t mode;        /* KL_STREAM_SAVE_ALL, _RECOMPUTE or _FORWARD         */
 } kl_stream_cfg;
 
 typedef struct kl_stream_result {
@@ -319,10 +334,12 @@ typedef struct kl_stream_result {
 
 /* host_layers[n_layers]: HOST pointers (pinned or pageable) to each layer's
  * weights in cfg.layer.dtype (gamma_q/gamma_k too when cfg.layer.qk_norm,
- * else they are ignored); host_lm_head [V,H] host. The driver keeps the
- * pointers (no copy of the weights); they must stay valid until destroy.
- * Allocates two device weight slots, the lm-head weight, saved activations
- * for every layer and workspace on the current device. */
+ * else they are ignored); host_lm_head [V,H] host (may be null with
+ * KL_STREAM_FORWARD). The driver keeps the pointers (no copy of the weights);
+ * they must stay valid until destroy. Device-memory layer weights select the
+ * bulk mode (no slots, no uploads, same kernels in the same order).
+ * Allocates on the current device: two weight slots, the lm-head weight,
+ * saved activations (per cfg->mode) and workspace. */
 KL_API kl_status kl_stream_create(const kl_stream_cfg* cfg, const kl_layer_weights* host_layers,
                            const void* host_lm_head, kl_stream** out);
 /* One training step: streams layer weights in (copy stream, double-buffered),
@@ -339,7 +356,13 @@ KL_API kl_status kl_stream_create(const kl_stream_cfg* cfg, const kl_layer_weigh
 KL_API kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets,
                         float clip_max_norm, const kl_layer_grads* grads, void* dW_lm,
                         kl_stream_result* result, void* stream);
-/* Peak device bytes the driver allocated (weights slots + activations + ws). */
+/* Forward only, in any mode: X [T,H] device -> Y [T,H] device (cfg.layer.dtype),
+ * the hidden state after the last layer, streaming every layer's weights as
+ * kl_stream_run's forward does (the lm-head is not applied). Synchronises
+ * `stream` before returning. X and Y must not overlap the driver's buffers. */
+KL_API kl_status kl_stream_forward(kl_stream* s, const void* X, void* Y, void* stream);
+/* Device bytes the driver allocated (weight slots + activations + workspace;
+ * the retained gradient buffers once a run delivered to host memory). */
 KL_API size_t kl_stream_device_bytes(const kl_stream* s);
 KL_API void kl_stream_destroy(kl_stream* s);
 

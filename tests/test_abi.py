@@ -112,3 +112,17 @@ def test_gemm_host_checks(lib):
     # leading dimension smaller than the contiguous extent
     assert lib.kl_gemm(16, 16, 64, K.KL_BF16, 0x1000, 32, 0, 0x1000, 64, 0, 0x1000, 16, K.KL_BF16, None, 0, 0,
                        None) == K.KL_ERR_INVALID_ARG
+
+
+def test_stream_host_checks(lib):
+    layer = _cfg(S=64, H=256, Hq=4, Hkv=2, I=512)
+    w = (K.LayerWeights * 1)(K.LayerWeights(*([0x1000] * 9), None, None))
+    out = ctypes.c_void_p()
+    bad_mode = K.StreamCfg(layer, 1, 1024, 7)
+    assert lib.kl_stream_create(ctypes.byref(bad_mode), w, 0x1000, ctypes.byref(out)) == K.KL_ERR_INVALID_ARG
+    # a training driver needs the lm-head weight; a forward-only one does not
+    train = K.StreamCfg(layer, 1, 1024, K.KL_STREAM_RECOMPUTE)
+    assert lib.kl_stream_create(ctypes.byref(train), w, None, ctypes.byref(out)) == K.KL_ERR_INVALID_ARG
+    no_layers = K.StreamCfg(layer, 0, 0, K.KL_STREAM_FORWARD)
+    assert lib.kl_stream_create(ctypes.byref(no_layers), w, None, ctypes.byref(out)) == K.KL_ERR_INVALID_ARG
+    assert lib.kl_stream_forward(None, 0x1000, 0x1000, None) == K.KL_ERR_INVALID_ARG
