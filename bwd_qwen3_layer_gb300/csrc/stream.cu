@@ -329,11 +329,25 @@ kl_status begin_pass(kl_stream* s, cudaStream_t cs) {
   return KL_OK;
 }
 
+// One of `pieces` equal pieces of the lm-head weight's upload on the copy
+// stream; the last piece records ev_lm.
+kl_status upload_lm_piece(kl_stream* s, int piece, int pieces) {
+  const size_t bytes = static_cast<size_t>(s->cfg.V) * s->cfg.layer.H * dtype_size(s->cfg.layer.dtype);
+  const size_t lo = bytes * piece / pieces, hi = bytes * (piece + 1) / pieces;
+  if (hi > lo)
+    KL_CUDA(cudaMemcpyAsync(static_cast<uint8_t*>(const_cast<void*>(s->lm_w)) + lo,
+                            static_cast<const uint8_t*>(s->lm_host) + lo, hi - lo, cudaMemcpyHostToDevice, s->copy));
+  if (piece == pieces - 1) KL_CUDA(cudaEventRecord(s->ev_lm, s->copy));
+  return KL_OK;
+}
+
 // Forward through every layer: layer l reads X (l = 0) or the previous
 // layer's output, writes hidden_of(l) (`last` for the last layer when given),
-// with layer l + 1's weights uploaded while layer l runs. *cur receives the
-// slot holding the last layer.
-kl_status forward_layers(kl_stream* s, const void* X, void* last, cudaStream_t cs, int* cur_out) {
+// with layer l + 1's weights uploaded while layer l runs. With `with_lm` the
+// lm-head weight's upload is cut into one piece per layer, each queued behind
+// that layer's prefetch, so that no layer's weights wait for the whole head.
+// *cur receives the slot holding the last layer.
+kl_status forward_layers(kl_stream* s, const void* X, void* last, cudaStream_t cs, int* cur_out, bool with_lm) {
   const kl_layer_cfg& c = s->cfg.layer;
   const int L = s->cfg.n_layers;
   int cur = -1;
@@ -344,6 +358,7 @@ kl_status forward_layers(kl_stream* s, const void* X, void* last, cudaStream_t c
       int nxt;
       KL_TRY(acquire(s, l + 1, cur, &nxt));  // prefetch while layer l runs
     }
+    if (!s->bulk && with_lm) KL_TRY(upload_lm_piece(s, l, L));
     const void* xin = l == 0 ? X : s->hidden_of(l - 1);
     void* out = (l == L - 1 && last) ? last : s->hidden_of(l);
     KL_TRY(kl_layer_forward(&c, &w, xin, out, s->saved_for(l), s->ws, s->ws_bytes, cs));
@@ -496,18 +511,11 @@ kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets, flo
   }
   KL_CUDA(cudaMemcpyAsync(s->refs, refs.data(), refs.size() * sizeof(GradRef), cudaMemcpyHostToDevice, cs));
 
-  const size_t es = dtype_size(c.dtype);
-  // lm-head weight upload (streamed mode), overlapped with the forward
-  if (!s->bulk) {
-    KL_CUDA(cudaMemcpyAsync(const_cast<void*>(s->lm_w), s->lm_host, static_cast<size_t>(s->cfg.V) * c.H * es,
-                            cudaMemcpyHostToDevice, s->copy));
-    KL_CUDA(cudaEventRecord(s->ev_lm, s->copy));
-  }
   KL_TRY(begin_pass(s, cs));
 
-  // ---------------- forward ----------------
+  // ---------------- forward (the lm-head weight uploaded alongside) ----------------
   int cur = -1;
-  KL_TRY(forward_layers(s, X, nullptr, cs, &cur));
+  KL_TRY(forward_layers(s, X, nullptr, cs, &cur, true));
   // ---------------- lm-head ----------------
   if (!s->bulk) KL_CUDA(cudaStreamWaitEvent(cs, s->ev_lm, 0));
   kl_lmhead_cfg lc = {T, c.H, s->cfg.V, c.dtype, KL_F32};
@@ -566,7 +574,7 @@ kl_status kl_stream_forward(kl_stream* s, const void* X, void* Y, void* stream) 
   cudaStream_t cs = static_cast<cudaStream_t>(stream);
   KL_TRY(begin_pass(s, cs));
   int cur = -1;
-  KL_TRY(forward_layers(s, X, Y, cs, &cur));
+  KL_TRY(forward_layers(s, X, Y, cs, &cur, false));
   KL_CUDA(cudaStreamSynchronize(cs));
   return KL_OK;
 }
