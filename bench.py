@@ -413,12 +413,12 @@ def bench_ours(args, rank, world, local_rank, dist):
             dist.barrier()
         torch.cuda.synchronize()
 
-    # ---- device-resident timed region (profiler on: per-kernel events) ----
+    # ---- device-resident timed region (no per-launch events: consecutive
+    # kernels may overlap their prologue with the predecessor's tail) ----
     clocks = Clocks(local_rank)
     barrier()
     clocks.start()
     time.sleep(0.25)
-    lib.kl_profile_enable(1)
     n0 = lib.kl_launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -429,6 +429,18 @@ def bench_ours(args, rank, world, local_rank, dist):
     launches = lib.kl_launch_count() - n0
     clk = clocks.stop()
     ms = e0.elapsed_time(e1)
+
+    # ---- the same steps again with the launch profiler on (CUDA events
+    # around every launch): per-kernel times and roofline fractions ----
+    barrier()
+    lib.kl_profile_enable(1)
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    for _ in range(args.steps):
+        step()
+    p1.record(stream)
+    barrier()
+    ms_prof = p0.elapsed_time(p1)
     prof = read_profile(K)
     lib.kl_profile_enable(0)
 
@@ -451,8 +463,8 @@ def bench_ours(args, rank, world, local_rank, dist):
         t = torch.tensor([ms, ms_e2e], device=device)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms, ms_e2e = float(t[0]), float(t[1])
-    return dict(ms=ms, ms_e2e=ms_e2e, prof=prof, clocks=clk, launches=int(launches), units=units, h2d=h2d,
-                d2h=d2h, config=cfgd, extra=extra)
+    return dict(ms=ms, ms_e2e=ms_e2e, ms_prof=ms_prof, prof=prof, clocks=clk, launches=int(launches), units=units,
+                h2d=h2d, d2h=d2h, config=cfgd, extra=extra)
 
 
 # ----------------------------------------------------------------------------
@@ -640,6 +652,8 @@ def main():
         roof = {"kernel": dname, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4), "traffic": traffic,
                 "peak_src": f"{pk['src']} hbm_gbs"}
+    roof["timed"] = (f"per-launch CUDA events over a second timed region of the same {args.steps} steps "
+                     f"({r['ms_prof'] / args.steps:.4f} ms per step with the events)")
     total_flops = sum(e["flops"] for e in prof.values()) / args.steps
     agg_tflops = total_flops / (r["ms"] / args.steps / 1e3) / 1e12
     line = {"metric": metric, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,

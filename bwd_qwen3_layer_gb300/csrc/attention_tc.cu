@@ -75,6 +75,7 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t base, int kk) {
 }
 
 __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_kernel(const __grid_constant__ FwdParams p) {
+  pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -410,6 +411,7 @@ constexpr size_t KV_SMEM = 1024 + KV_OFF_BAR + 256;
 static_assert(KV_SMEM <= 232448, "dK/dV shared memory above the per-CTA limit");
 
 __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid_constant__ BwdParams p) {
+  pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -695,6 +697,7 @@ constexpr size_t DQ_SMEM = 1024 + DQ_OFF_BAR + 256;
 static_assert(DQ_SMEM <= 232448, "dQ shared memory above the per-CTA limit");
 
 __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dq_tc_kernel(const __grid_constant__ BwdParams p) {
+  pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1002,7 +1005,7 @@ kl_status attention_fwd_tc(int B, int S, int Hq, int Hkv, const void* q, const v
     attr_done |= uint64_t(1) << dev;
   }
   dim3 grid(Hq, (S + BQ - 1) / BQ, B);
-  fa_fwd_tc_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(p);
+  launch_pdl(fa_fwd_tc_kernel, grid, THREADS, SMEM_BYTES, st, p);
   KL_CUDA(cudaGetLastError());
   return KL_OK;
 }
@@ -1049,7 +1052,7 @@ kl_status attention_bwd_tc(int B, int S, int Hq, int Hkv, const void* q, const v
   {
     ProfScope ps("attn_bwd_dkdv_tc", st, 8.0 * B * Hq * HD * pairs, 0.0);
     dim3 grid(Hq, (S + BKV - 1) / BKV, B);
-    fa_bwd_dkdv_tc_kernel<<<grid, THREADS, KV_SMEM, st>>>(p);
+    launch_pdl(fa_bwd_dkdv_tc_kernel, grid, THREADS, KV_SMEM, st, p);
   }
   KL_CUDA(cudaGetLastError());
   // dQ: Q and dO tiles of 128 rows, K and V tiles of 64 rows
@@ -1061,7 +1064,7 @@ kl_status attention_bwd_tc(int B, int S, int Hq, int Hkv, const void* q, const v
     // only the dQ product is algorithmic work here; S and dP are recomputed
     ProfScope ps("attn_bwd_dq_tc", st, 2.0 * B * Hq * HD * pairs, 0.0);
     dim3 grid(Hq, (S + BQ - 1) / BQ, B);
-    fa_bwd_dq_tc_kernel<<<grid, THREADS, DQ_SMEM, st>>>(p);
+    launch_pdl(fa_bwd_dq_tc_kernel, grid, THREADS, DQ_SMEM, st, p);
   }
   KL_CUDA(cudaGetLastError());
   return KL_OK;

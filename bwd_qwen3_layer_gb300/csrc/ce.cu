@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(THREADS)
                      int32_t* __restrict__ argmax, void* __restrict__ dz, int dz_f32, float invN,
                      unsigned int* __restrict__ counter, float* __restrict__ loss,
                      uint32_t* __restrict__ err) {
+  pdl_enter();
   extern __shared__ __align__(16) float sz[];
   __shared__ float red_m[NWARP];
   __shared__ float red_s[NWARP];
@@ -256,17 +257,19 @@ kl_status ce_argmax(int N, int V, const float* z, const int32_t* targets, float*
   auto launch = [&](auto kernel) -> kl_status {
     KL_CUDA(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = CLUSTER;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_enter
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = grid;
     cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     KL_CUDA(cudaLaunchKernelEx(&cfg, kernel, N, V, slice, z, targets, loss_rows, argmax, dz, f32, invN, counter, loss,
                                device_error_word()));
     return KL_OK;

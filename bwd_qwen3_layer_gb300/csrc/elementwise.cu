@@ -71,6 +71,7 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_kernel(int rows, int width,
                                                           const T* __restrict__ gamma, float eps,
                                                           T* __restrict__ h,
                                                           float* __restrict__ rstd) {
+  pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * 8 + warp;
   if (row >= rows) return;
@@ -118,6 +119,7 @@ __global__ void __launch_bounds__(RF_THREADS) rmsnorm_fwd_row_kernel(int width, 
                                                                      const T* __restrict__ gamma, float eps,
                                                                      T* __restrict__ h,
                                                                      float* __restrict__ rstd) {
+  pdl_enter();
   __shared__ float red[RF_THREADS / 32];
   constexpr int V = Vec<T>::N;
   const int row = blockIdx.x, tid = threadIdx.x;
@@ -172,6 +174,7 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(
     int rows, int width, const TD* __restrict__ dh, const T* __restrict__ x,
     const T* __restrict__ gamma, const float* __restrict__ rstd, const T* __restrict__ resid,
     T* __restrict__ dx, float* __restrict__ partial) {
+  pdl_enter();
   extern __shared__ float sacc[];
   for (int j = threadIdx.x; j < width; j += blockDim.x) sacc[j] = 0.f;
   __syncthreads();
@@ -232,6 +235,7 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_rows_kernel(
     int rows, int width, const float* __restrict__ dh, const T* __restrict__ x,
     const T* __restrict__ gamma, const float* __restrict__ rstd, const T* __restrict__ resid,
     T* __restrict__ dx, float* __restrict__ partial) {
+  pdl_enter();
   __shared__ float red[2][8];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nchunk = width >> 2;
@@ -304,6 +308,7 @@ __global__ void __launch_bounds__(RW_THREADS, 2) rmsnorm_bwd_row8_kernel(
     const __nv_bfloat16* __restrict__ gamma, const float* __restrict__ rstd,
     const __nv_bfloat16* __restrict__ resid, __nv_bfloat16* __restrict__ dx,
     float* __restrict__ partial) {
+  pdl_enter();
   using T = __nv_bfloat16;
   __shared__ float red[2][RW_THREADS / 32];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -390,6 +395,7 @@ __global__ void __launch_bounds__(RW_THREADS, 2) rmsnorm_bwd_row8_kernel(
 __global__ void __launch_bounds__(256) column_sum4_kernel(int nrows, int width,
                                                           const float* __restrict__ partial,
                                                           float* __restrict__ out) {
+  pdl_enter();
   __shared__ float4 red[32][8];
   const int cg = threadIdx.x & 7, rg = threadIdx.x >> 3;
   const int c = blockIdx.x * 32 + cg * 4;
@@ -418,6 +424,7 @@ __global__ void __launch_bounds__(256) column_sum4_kernel(int nrows, int width,
 __global__ void __launch_bounds__(256) column_sum_kernel(int nrows, int width,
                                                          const float* __restrict__ partial,
                                                          float* __restrict__ out) {
+  pdl_enter();
   __shared__ float red[4][64];
   const int c = blockIdx.x * 64 + (threadIdx.x & 63);
   const int grp = threadIdx.x >> 6;
@@ -477,6 +484,7 @@ __device__ __forceinline__ void rope_table(int s, int d, const RopeFreq& f, floa
 // The (cos, sin) table of every position and plane: consumed by the fused
 // rotary epilogues of the q/k projection and of the attention dQ kernel.
 __global__ void rope_cs_kernel(int S, int half, RopeFreq f, float2* __restrict__ cs) {
+  pdl_enter();
   const int64_t n = static_cast<int64_t>(S) * half;
   for (int64_t idx = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; idx < n;
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -489,6 +497,7 @@ __global__ void rope_cs_kernel(int S, int half, RopeFreq f, float2* __restrict__
 
 template <typename T>
 __global__ void rope_kernel(int S, int heads, int d, RopeFreq f, T* __restrict__ x, float dir) {
+  pdl_enter();
   __shared__ float cs[2 * ROPE_MAX_HALF];
   const int t = blockIdx.x;
   rope_table(t % S, d, f, dir, cs);
@@ -516,6 +525,7 @@ template <typename T>
 __global__ void __launch_bounds__(RQ_THREADS) rope_qk_kernel(int S, int hq, int hk, int d, RopeFreq f,
                                                              T* __restrict__ q, T* __restrict__ k,
                                                              float dir) {
+  pdl_enter();
   __shared__ float cs[2 * ROPE_MAX_HALF];
   const int t = blockIdx.x;
   const int half = d / 2;
@@ -574,6 +584,7 @@ __global__ void __launch_bounds__(RC_THREADS) rope_bwd_convert_kernel(
     int S, int hq, int hk, int d, RopeFreq f, const float* __restrict__ dq_acc,
     const float* __restrict__ dk_acc, const float* __restrict__ dv_acc, T* __restrict__ dq,
     T* __restrict__ dk, T* __restrict__ dv) {
+  pdl_enter();
   __shared__ float cs[2 * ROPE_MAX_HALF];
   const int t = blockIdx.x;
   const int half = d / 2;
@@ -650,6 +661,7 @@ __global__ void __launch_bounds__(256) qk_rope_fwd_kernel(int rows, int heads, i
                                                           const T* __restrict__ gamma, float eps, int norm, int inter,
                                                           RopeFreq f, const float2* __restrict__ tab,
                                                           T* out, float* __restrict__ rstd) {
+  pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * 8 + warp;
   if (row >= rows) return;
@@ -695,6 +707,7 @@ __global__ void __launch_bounds__(256) qk_rope_bwd_kernel(int rows, int heads, i
                                                           int norm, int inter, RopeFreq f,
                                                           const float2* __restrict__ tab, T* dx,
                                                           float* __restrict__ partial) {
+  pdl_enter();
   __shared__ float sacc[8][256];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int half = d / 2;
@@ -768,6 +781,7 @@ __global__ void __launch_bounds__(256) qk_rope_bwd_kernel(int rows, int heads, i
 
 template <typename T>
 __global__ void convert_kernel(int64_t n, const float* __restrict__ src, T* __restrict__ dst) {
+  pdl_enter();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
     st_f(dst + i, src[i]);
@@ -781,6 +795,7 @@ __device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + expf
 template <typename T, bool VEC>
 __global__ void swiglu_fwd_kernel(int64_t n, const T* __restrict__ g, const T* __restrict__ u,
                                   T* __restrict__ m) {
+  pdl_enter();
   constexpr int V = Vec<T>::N;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   if (VEC) {
@@ -805,6 +820,7 @@ template <typename T, bool VEC>
 __global__ void swiglu_bwd_kernel(int64_t n, const T* __restrict__ dm, const T* __restrict__ g,
                                   const T* __restrict__ u, T* __restrict__ dg,
                                   T* __restrict__ du) {
+  pdl_enter();
   constexpr int V = Vec<T>::N;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   if (VEC) {
@@ -859,25 +875,25 @@ kl_status rmsnorm_fwd(int rows, int width, int dtype, const void* x, const void*
     if (dtype == KL_BF16) {
       using T = __nv_bfloat16;
       switch (nc) {
-#define KL_RF_CASE(N) case N: rmsnorm_fwd_row_kernel<T, N><<<rows, RF_THREADS, 0, st>>>(width, (const T*)x, (const T*)gamma, eps, (T*)h, rstd); break;
+#define KL_RF_CASE(N) case N: launch_pdl(rmsnorm_fwd_row_kernel<T, N>, rows, RF_THREADS, 0, st, width, (const T*)x, (const T*)gamma, eps, (T*)h, rstd); break;
         KL_RF_CASE(1) KL_RF_CASE(2) KL_RF_CASE(3) KL_RF_CASE(4) KL_RF_CASE(5) KL_RF_CASE(6) KL_RF_CASE(7) KL_RF_CASE(8)
 #undef KL_RF_CASE
       }
     } else {
       using T = float;
       switch (nc) {
-#define KL_RF_CASE(N) case N: rmsnorm_fwd_row_kernel<T, N><<<rows, RF_THREADS, 0, st>>>(width, (const T*)x, (const T*)gamma, eps, (T*)h, rstd); break;
+#define KL_RF_CASE(N) case N: launch_pdl(rmsnorm_fwd_row_kernel<T, N>, rows, RF_THREADS, 0, st, width, (const T*)x, (const T*)gamma, eps, (T*)h, rstd); break;
         KL_RF_CASE(1) KL_RF_CASE(2) KL_RF_CASE(3) KL_RF_CASE(4) KL_RF_CASE(5) KL_RF_CASE(6) KL_RF_CASE(7) KL_RF_CASE(8)
 #undef KL_RF_CASE
       }
     }
   } else if (dtype == KL_BF16) {
     using T = __nv_bfloat16;
-    if (vec) rmsnorm_fwd_kernel<T, true><<<grid, 256, 0, st>>>(rows, width, (const T*)x, (const T*)gamma, eps, (T*)h, rstd);
-    else rmsnorm_fwd_kernel<T, false><<<grid, 256, 0, st>>>(rows, width, (const T*)x, (const T*)gamma, eps, (T*)h, rstd);
+    if (vec) launch_pdl(rmsnorm_fwd_kernel<T, true>, grid, 256, 0, st, rows, width, (const T*)x, (const T*)gamma, eps, (T*)h, rstd);
+    else launch_pdl(rmsnorm_fwd_kernel<T, false>, grid, 256, 0, st, rows, width, (const T*)x, (const T*)gamma, eps, (T*)h, rstd);
   } else {
-    if (vec) rmsnorm_fwd_kernel<float, true><<<grid, 256, 0, st>>>(rows, width, (const float*)x, (const float*)gamma, eps, (float*)h, rstd);
-    else rmsnorm_fwd_kernel<float, false><<<grid, 256, 0, st>>>(rows, width, (const float*)x, (const float*)gamma, eps, (float*)h, rstd);
+    if (vec) launch_pdl(rmsnorm_fwd_kernel<float, true>, grid, 256, 0, st, rows, width, (const float*)x, (const float*)gamma, eps, (float*)h, rstd);
+    else launch_pdl(rmsnorm_fwd_kernel<float, false>, grid, 256, 0, st, rows, width, (const float*)x, (const float*)gamma, eps, (float*)h, rstd);
   }
   KL_CUDA(cudaGetLastError());
   return KL_OK;
@@ -918,29 +934,29 @@ kl_status rmsnorm_bwd(int rows, int width, int dtype, const void* dh, int dh_dty
       using T = __nv_bfloat16;
       if (row8_form) {
         switch (nc8) {
-#define KL_RW_CASE(N) case N: rmsnorm_bwd_row8_kernel<N><<<grid, RW_THREADS, 0, st>>>(rows, width, (const float*)dh, (const T*)x, (const T*)gamma, rstd, (const T*)resid, (T*)dx, partial); break;
+#define KL_RW_CASE(N) case N: launch_pdl(rmsnorm_bwd_row8_kernel<N>, grid, RW_THREADS, 0, st, rows, width, (const float*)dh, (const T*)x, (const T*)gamma, rstd, (const T*)resid, (T*)dx, partial); break;
           KL_RW_CASE(1) KL_RW_CASE(2) KL_RW_CASE(3) KL_RW_CASE(4)
 #undef KL_RW_CASE
         }
       } else if (rows_form)
-        rmsnorm_bwd_rows_kernel<T><<<grid, 256, 0, st>>>(rows, width, (const float*)dh, (const T*)x, (const T*)gamma, rstd, (const T*)resid, (T*)dx, partial);
+        launch_pdl(rmsnorm_bwd_rows_kernel<T>, grid, 256, 0, st, rows, width, (const float*)dh, (const T*)x, (const T*)gamma, rstd, (const T*)resid, (T*)dx, partial);
       else if (dh_dtype == KL_F32)
-        rmsnorm_bwd_kernel<T, float><<<grid, 256, sm, st>>>(rows, width, (const float*)dh, (const T*)x, (const T*)gamma, rstd, (const T*)resid, (T*)dx, partial);
+        launch_pdl(rmsnorm_bwd_kernel<T, float>, grid, 256, sm, st, rows, width, (const float*)dh, (const T*)x, (const T*)gamma, rstd, (const T*)resid, (T*)dx, partial);
       else
-        rmsnorm_bwd_kernel<T, T><<<grid, 256, sm, st>>>(rows, width, (const T*)dh, (const T*)x, (const T*)gamma, rstd, (const T*)resid, (T*)dx, partial);
+        launch_pdl(rmsnorm_bwd_kernel<T, T>, grid, 256, sm, st, rows, width, (const T*)dh, (const T*)x, (const T*)gamma, rstd, (const T*)resid, (T*)dx, partial);
     } else {
       if (rows_form)
-        rmsnorm_bwd_rows_kernel<float><<<grid, 256, 0, st>>>(rows, width, (const float*)dh, (const float*)x, (const float*)gamma, rstd, (const float*)resid, (float*)dx, partial);
+        launch_pdl(rmsnorm_bwd_rows_kernel<float>, grid, 256, 0, st, rows, width, (const float*)dh, (const float*)x, (const float*)gamma, rstd, (const float*)resid, (float*)dx, partial);
       else
-        rmsnorm_bwd_kernel<float, float><<<grid, 256, sm, st>>>(rows, width, (const float*)dh, (const float*)x, (const float*)gamma, rstd, (const float*)resid, (float*)dx, partial);
+        launch_pdl(rmsnorm_bwd_kernel<float, float>, grid, 256, sm, st, rows, width, (const float*)dh, (const float*)x, (const float*)gamma, rstd, (const float*)resid, (float*)dx, partial);
     }
   }
   KL_CUDA(cudaGetLastError());
   ProfScope ps2("rmsnorm_bwd_colsum", st, 0.0, 4.0 * grid * width + 4.0 * width);
   if (width % 4 == 0 && al16(dgamma))
-    column_sum4_kernel<<<(width + 31) / 32, 256, 0, st>>>(grid, width, partial, dgamma);
+    launch_pdl(column_sum4_kernel, (width + 31) / 32, 256, 0, st, grid, width, partial, dgamma);
   else
-    column_sum_kernel<<<(width + 63) / 64, 256, 0, st>>>(grid, width, partial, dgamma);
+    launch_pdl(column_sum_kernel, (width + 63) / 64, 256, 0, st, grid, width, partial, dgamma);
   KL_CUDA(cudaGetLastError());
   return KL_OK;
 }
@@ -960,16 +976,16 @@ kl_status rope_qk(int B, int S, int hq, int hk, int d, float base, int dtype, vo
   ProfScope ps("rope", st, 0.0, 2.0 * T * (hq + hk) * d * dtype_size(dtype));
   if (vec) {
     if (dtype == KL_BF16)
-      rope_qk_kernel<__nv_bfloat16><<<T, RQ_THREADS, 0, st>>>(S, hq, hk, d, f, (__nv_bfloat16*)q, (__nv_bfloat16*)k, dir);
+      launch_pdl(rope_qk_kernel<__nv_bfloat16>, T, RQ_THREADS, 0, st, S, hq, hk, d, f, (__nv_bfloat16*)q, (__nv_bfloat16*)k, dir);
     else
-      rope_qk_kernel<float><<<T, RQ_THREADS, 0, st>>>(S, hq, hk, d, f, (float*)q, (float*)k, dir);
+      launch_pdl(rope_qk_kernel<float>, T, RQ_THREADS, 0, st, S, hq, hk, d, f, (float*)q, (float*)k, dir);
   } else {
     for (int w = 0; w < 2; ++w) {
       void* x = w == 0 ? q : k;
       const int heads = w == 0 ? hq : hk;
       if (heads == 0) continue;
-      if (dtype == KL_BF16) rope_kernel<__nv_bfloat16><<<T, 128, 0, st>>>(S, heads, d, f, (__nv_bfloat16*)x, dir);
-      else rope_kernel<float><<<T, 128, 0, st>>>(S, heads, d, f, (float*)x, dir);
+      if (dtype == KL_BF16) launch_pdl(rope_kernel<__nv_bfloat16>, T, 128, 0, st, S, heads, d, f, (__nv_bfloat16*)x, dir);
+      else launch_pdl(rope_kernel<float>, T, 128, 0, st, S, heads, d, f, (float*)x, dir);
     }
   }
   KL_CUDA(cudaGetLastError());
@@ -982,7 +998,7 @@ kl_status rope_cs_table(int S, int d, float base, float2* cs, cudaStream_t st) {
   const RopeFreq f = rope_freq(d, base);
   const int64_t n = static_cast<int64_t>(S) * (d / 2);
   ProfScope ps("rope_table", st, 0.0, 8.0 * n);
-  rope_cs_kernel<<<ew_grid(n), 256, 0, st>>>(S, d / 2, f, cs);
+  launch_pdl(rope_cs_kernel, ew_grid(n), 256, 0, st, S, d / 2, f, cs);
   KL_CUDA(cudaGetLastError());
   return KL_OK;
 }
@@ -1001,10 +1017,10 @@ kl_status rope_bwd_convert(int B, int S, int hq, int hk, int d, float base, int 
   const RopeFreq f = rope_freq(d, base);
   ProfScope ps("rope_bwd_convert", st, 0.0, 1.0 * T * (hq + 2 * hk) * d * (4 + dtype_size(dtype)));
   if (dtype == KL_BF16)
-    rope_bwd_convert_kernel<__nv_bfloat16><<<T, RC_THREADS, 0, st>>>(S, hq, hk, d, f, dq_acc, dk_acc, dv_acc,
+    launch_pdl(rope_bwd_convert_kernel<__nv_bfloat16>, T, RC_THREADS, 0, st, S, hq, hk, d, f, dq_acc, dk_acc, dv_acc,
                                                                      (__nv_bfloat16*)dq, (__nv_bfloat16*)dk, (__nv_bfloat16*)dv);
   else
-    rope_bwd_convert_kernel<float><<<T, RC_THREADS, 0, st>>>(S, hq, hk, d, f, dq_acc, dk_acc, dv_acc, (float*)dq,
+    launch_pdl(rope_bwd_convert_kernel<float>, T, RC_THREADS, 0, st, S, hq, hk, d, f, dq_acc, dk_acc, dv_acc, (float*)dq,
                                                              (float*)dk, (float*)dv);
   KL_CUDA(cudaGetLastError());
   return KL_OK;
@@ -1026,11 +1042,11 @@ kl_status qk_rope_fwd(int T, int heads, int S, int d, int dtype, const void* pre
   ProfScope ps("qk_rope_fwd", st, 0.0, 2.0 * rows * d * dtype_size(dtype));
   const int grid = (rows + 7) / 8;
   if (dtype == KL_BF16)
-    qk_rope_fwd_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(rows, heads, S, d, (const __nv_bfloat16*)pre,
+    launch_pdl(qk_rope_fwd_kernel<__nv_bfloat16>, grid, 256, 0, st, rows, heads, S, d, (const __nv_bfloat16*)pre,
                                                            (const __nv_bfloat16*)gamma, eps, norm, inter, f, tab,
                                                            (__nv_bfloat16*)out, rstd);
   else
-    qk_rope_fwd_kernel<float><<<grid, 256, 0, st>>>(rows, heads, S, d, (const float*)pre, (const float*)gamma, eps,
+    launch_pdl(qk_rope_fwd_kernel<float>, grid, 256, 0, st, rows, heads, S, d, (const float*)pre, (const float*)gamma, eps,
                                                    norm, inter, f, tab, (float*)out, rstd);
   KL_CUDA(cudaGetLastError());
   return KL_OK;
@@ -1051,7 +1067,7 @@ kl_status qk_rope_bwd(int T, int heads, int S, int d, int dtype, const void* dyr
   {
     ProfScope ps("qk_rope_bwd", st, 0.0, 1.0 * rows * d * (dtype_size(dy_dtype) + (norm ? 2.0 : 1.0) * dtype_size(dtype)));
 #define KL_QKB(T_, TD_)                                                                                         \
-  qk_rope_bwd_kernel<T_, TD_><<<grid, 256, 0, st>>>(rows, heads, S, d, (const TD_*)dyr, 1.0f, (const T_*)pre,  \
+  launch_pdl(qk_rope_bwd_kernel<T_, TD_>, grid, 256, 0, st, rows, heads, S, d, (const TD_*)dyr, 1.0f, (const T_*)pre,  \
                                                     (const T_*)gamma, rstd, norm, inter, f, tab, (T_*)dx, partial)
     if (dtype == KL_BF16) {
       if (dy_dtype == KL_BF16) KL_QKB(__nv_bfloat16, __nv_bfloat16);
@@ -1064,7 +1080,7 @@ kl_status qk_rope_bwd(int T, int heads, int S, int d, int dtype, const void* dyr
   KL_CUDA(cudaGetLastError());
   if (norm) {
     ProfScope ps2("qk_rope_bwd_colsum", st, 0.0, 4.0 * grid * d);
-    column_sum_kernel<<<(d + 63) / 64, 256, 0, st>>>(grid, d, partial, dgamma);
+    launch_pdl(column_sum_kernel, (d + 63) / 64, 256, 0, st, grid, d, partial, dgamma);
     KL_CUDA(cudaGetLastError());
   }
   return KL_OK;
@@ -1072,8 +1088,8 @@ kl_status qk_rope_bwd(int T, int heads, int S, int d, int dtype, const void* dyr
 
 kl_status convert_f32(int64_t n, int dtype, const float* src, void* dst, cudaStream_t st) {
   ProfScope ps("convert_f32", st, 0.0, 1.0 * n * (4 + dtype_size(dtype)));
-  if (dtype == KL_BF16) convert_kernel<__nv_bfloat16><<<ew_grid(n), 256, 0, st>>>(n, src, (__nv_bfloat16*)dst);
-  else convert_kernel<float><<<ew_grid(n), 256, 0, st>>>(n, src, (float*)dst);
+  if (dtype == KL_BF16) launch_pdl(convert_kernel<__nv_bfloat16>, ew_grid(n), 256, 0, st, n, src, (__nv_bfloat16*)dst);
+  else launch_pdl(convert_kernel<float>, ew_grid(n), 256, 0, st, n, src, (float*)dst);
   KL_CUDA(cudaGetLastError());
   return KL_OK;
 }
@@ -1084,14 +1100,14 @@ kl_status swiglu_fwd(int64_t n, int dtype, const void* g, const void* u, void* m
   if (dtype == KL_BF16) {
     using T = __nv_bfloat16;
     if (n % 8 == 0 && al16(g) && al16(u) && al16(m))
-      swiglu_fwd_kernel<T, true><<<ew_grid(n / 8), 256, 0, st>>>(n, (const T*)g, (const T*)u, (T*)m);
+      launch_pdl(swiglu_fwd_kernel<T, true>, ew_grid(n / 8), 256, 0, st, n, (const T*)g, (const T*)u, (T*)m);
     else
-      swiglu_fwd_kernel<T, false><<<ew_grid(n), 256, 0, st>>>(n, (const T*)g, (const T*)u, (T*)m);
+      launch_pdl(swiglu_fwd_kernel<T, false>, ew_grid(n), 256, 0, st, n, (const T*)g, (const T*)u, (T*)m);
   } else if (dtype == KL_F32) {
     if (n % 4 == 0 && al16(g) && al16(u) && al16(m))
-      swiglu_fwd_kernel<float, true><<<ew_grid(n / 4), 256, 0, st>>>(n, (const float*)g, (const float*)u, (float*)m);
+      launch_pdl(swiglu_fwd_kernel<float, true>, ew_grid(n / 4), 256, 0, st, n, (const float*)g, (const float*)u, (float*)m);
     else
-      swiglu_fwd_kernel<float, false><<<ew_grid(n), 256, 0, st>>>(n, (const float*)g, (const float*)u, (float*)m);
+      launch_pdl(swiglu_fwd_kernel<float, false>, ew_grid(n), 256, 0, st, n, (const float*)g, (const float*)u, (float*)m);
   } else {
     return set_error(KL_ERR_INVALID_ARG, "swiglu_fwd: bad dtype");
   }
@@ -1106,14 +1122,14 @@ kl_status swiglu_bwd(int64_t n, int dtype, const void* dm, const void* g, const 
   if (dtype == KL_BF16) {
     using T = __nv_bfloat16;
     if (n % 8 == 0 && al16(dm) && al16(g) && al16(u) && al16(dg) && al16(du))
-      swiglu_bwd_kernel<T, true><<<ew_grid(n / 8), 256, 0, st>>>(n, (const T*)dm, (const T*)g, (const T*)u, (T*)dg, (T*)du);
+      launch_pdl(swiglu_bwd_kernel<T, true>, ew_grid(n / 8), 256, 0, st, n, (const T*)dm, (const T*)g, (const T*)u, (T*)dg, (T*)du);
     else
-      swiglu_bwd_kernel<T, false><<<ew_grid(n), 256, 0, st>>>(n, (const T*)dm, (const T*)g, (const T*)u, (T*)dg, (T*)du);
+      launch_pdl(swiglu_bwd_kernel<T, false>, ew_grid(n), 256, 0, st, n, (const T*)dm, (const T*)g, (const T*)u, (T*)dg, (T*)du);
   } else if (dtype == KL_F32) {
     if (n % 4 == 0 && al16(dm) && al16(g) && al16(u) && al16(dg) && al16(du))
-      swiglu_bwd_kernel<float, true><<<ew_grid(n / 4), 256, 0, st>>>(n, (const float*)dm, (const float*)g, (const float*)u, (float*)dg, (float*)du);
+      launch_pdl(swiglu_bwd_kernel<float, true>, ew_grid(n / 4), 256, 0, st, n, (const float*)dm, (const float*)g, (const float*)u, (float*)dg, (float*)du);
     else
-      swiglu_bwd_kernel<float, false><<<ew_grid(n), 256, 0, st>>>(n, (const float*)dm, (const float*)g, (const float*)u, (float*)dg, (float*)du);
+      launch_pdl(swiglu_bwd_kernel<float, false>, ew_grid(n), 256, 0, st, n, (const float*)dm, (const float*)g, (const float*)u, (float*)dg, (float*)du);
   } else {
     return set_error(KL_ERR_INVALID_ARG, "swiglu_bwd: bad dtype");
   }

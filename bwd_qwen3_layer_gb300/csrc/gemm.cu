@@ -470,6 +470,7 @@ __device__ __forceinline__ Unit decode_unit_cl(const GemmParams& P, int u) {
 }
 
 __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __grid_constant__ GemmParams p) {
+  pdl_enter();
   constexpr int CL = 2;                                        // CTAs per cluster
   // consumers of each unit id: epilogue warps, producers (all but the
   // scheduler's own, plus the B producers), the MMA issuer
@@ -861,6 +862,7 @@ struct TailFin {
   int r_f32;
 };
 __global__ void __launch_bounds__(256) gemm_tail_finalize_kernel(const TailFin f) {
+  pdl_enter();
   const int t = blockIdx.x;                      // tail tile
   const int tile = f.whole + t;
   int m0, n0;
@@ -898,6 +900,7 @@ __global__ void __launch_bounds__(256) gemm_tail_finalize_kernel(const TailFin f
 __global__ void gemm_finalize_kernel(int M, int N, const float* __restrict__ acc,
                                      void* __restrict__ C, int64_t ldc, int c_f32,
                                      const void* __restrict__ R, int64_t ldr, int r_f32) {
+  pdl_enter();
   const int64_t total = static_cast<int64_t>(M) * N;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -972,6 +975,7 @@ constexpr int FT = 64;   // tile edge
 constexpr int FK = 16;   // k step
 
 __global__ void __launch_bounds__(256) gemm_f32_kernel(int M, int N, int nseg, GemmSpec spec) {
+  pdl_enter();
   __shared__ float As[FK][FT + 1];
   __shared__ float Bs[FK][FT + 1];
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
@@ -1224,11 +1228,13 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
     attr_done |= uint64_t(1) << dev;
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = GEMM_CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_enter
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(PAIR_THREADS);
   cfg.dynamicSmemBytes = SMEM2_BYTES;
   cfg.stream = st;
@@ -1271,6 +1277,7 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
     ProfScope ps(label, st, flops, bytes);
     const int clusters = units < cap ? units : cap;
     cfg.gridDim = dim3(GEMM_CL * clusters);
+    cfg.numAttrs = 2;   // the occupancy query above used the cluster attribute alone
     KL_CUDA(cudaLaunchKernelEx(&cfg, gemm_bf16_tcp_kernel, p));
   }
   KL_CUDA(cudaGetLastError());
@@ -1285,7 +1292,7 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
     const double n = static_cast<double>(pr.tail_tiles) * 256 * 256;
     ProfScope ps("gemm_tail_finalize", st, 0.0,
                  n * (4.0 * pr.tail_splits + dtype_size(s.c_dtype) + (s.R ? dtype_size(s.r_dtype) : 0)));
-    gemm_tail_finalize_kernel<<<dim3(pr.tail_tiles, 64), 256, 0, st>>>(f);
+    launch_pdl(gemm_tail_finalize_kernel, dim3(pr.tail_tiles, 64), 256, 0, st, f);
     KL_CUDA(cudaGetLastError());
   }
   KL_CUDA(cudaGetLastError());
@@ -1294,7 +1301,7 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
     const GemmSpec& s = specs_in[i];
     const double n = static_cast<double>(s.M) * s.N;
     ProfScope ps("gemm_finalize", st, 0.0, n * (4 + dtype_size(s.c_dtype) + (s.R ? dtype_size(s.r_dtype) : 0)));
-    gemm_finalize_kernel<<<4 * num_sms(), 256, 0, st>>>(s.M, s.N, s.acc_ws, s.C, s.ldc, s.c_dtype == KL_F32,
+    launch_pdl(gemm_finalize_kernel, 4 * num_sms(), 256, 0, st, s.M, s.N, s.acc_ws, s.C, s.ldc, s.c_dtype == KL_F32,
                                                        s.R, s.ldr, s.r_dtype == KL_F32);
     KL_CUDA(cudaGetLastError());
   }
@@ -1314,7 +1321,7 @@ kl_status gemm_f32(const GemmSpec& s, cudaStream_t st, const char* label) {
   double ksum = 0.0;
   for (int g = 0; g < s.nseg; ++g) ksum += s.K[g];
   ProfScope ps(label, st, 2.0 * s.M * s.N * ksum, 4.0 * ((s.M + s.N) * ksum + 1.0 * s.M * s.N));
-  gemm_f32_kernel<<<grid, 256, 0, st>>>(s.M, s.N, s.nseg, s);
+  launch_pdl(gemm_f32_kernel, grid, 256, 0, st, s.M, s.N, s.nseg, s);
   KL_CUDA(cudaGetLastError());
   return KL_OK;
 }

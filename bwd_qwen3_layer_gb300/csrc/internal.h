@@ -2,6 +2,8 @@
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include <utility>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -155,6 +157,27 @@ size_t ce_ws(int N);
 kl_status ce_argmax(int N, int V, const float* z, const int32_t* targets, float* loss,
                     int32_t* argmax, void* dz, int dz_dtype, void* ws, size_t ws_bytes,
                     cudaStream_t st);
+
+// Launches `kern` on `st` with programmatic stream serialization: the grid may
+// be scheduled while the stream's previous kernel drains; the kernel itself
+// waits for that kernel's completion first thing (pdl_enter). Arguments are
+// converted to the kernel's parameter types. Launch errors are also left for
+// cudaGetLastError.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // Counts a kernel launch and, while profiling is on, brackets it with CUDA
 // events on `st` (construct immediately before the launch; the destructor

@@ -124,6 +124,18 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, ui
   return __all_sync(0xffffffffu, ok);
 }
 
+// Programmatic dependent launch. Every kernel of the library is launched
+// with programmatic stream serialization (launch_pdl), so it may become
+// resident while its predecessor on the stream is still finishing; its first
+// statement is pdl_enter(): wait until the predecessor grid has completed and
+// its memory is visible (before any global-memory access, read or write),
+// then allow the successor grid to begin launching. Without the launch
+// attribute both instructions are no-ops.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // One lane of a converged warp (the lowest), chosen by elect.sync. Roles that
 // issue TMA copies or tcgen05 MMAs run as whole warps, so descriptors,
 // coordinates and barrier addresses are warp-uniform values; only the elected

@@ -57,6 +57,7 @@ constexpr int64_t SCALE_CHUNK = 16384;
 // across threads and blocks in a fixed order: deterministic).
 __global__ void __launch_bounds__(SUMSQ_THREADS) sumsq_kernel(const float* __restrict__ p, int64_t n,
                                                               double* __restrict__ partial) {
+  pdl_enter();
   __shared__ double red[SUMSQ_THREADS / 32];
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
   const int64_t stride = static_cast<int64_t>(SUMSQ_BLOCKS) * SUMSQ_THREADS;
@@ -91,6 +92,7 @@ __global__ void __launch_bounds__(SUMSQ_THREADS) sumsq_kernel(const float* __res
 __global__ void clip_finalize_kernel(const double* __restrict__ partial, int count,
                                      const float* __restrict__ loss, float max_norm,
                                      float* __restrict__ result) {
+  pdl_enter();
   __shared__ double red[SUMSQ_THREADS / 32];
   double acc = 0.0;
   for (int i = threadIdx.x; i < count * SUMSQ_BLOCKS; i += blockDim.x) acc += partial[i];
@@ -116,6 +118,7 @@ __global__ void clip_finalize_kernel(const double* __restrict__ partial, int cou
 __global__ void __launch_bounds__(256) clip_scale_kernel(const GradRef* __restrict__ refs, int count,
                                                          int64_t total_chunks,
                                                          const float* __restrict__ result) {
+  pdl_enter();
   const float coef = result[2];
   int r = 0;
   for (int64_t ch = blockIdx.x; ch < total_chunks; ch += gridDim.x) {
@@ -288,7 +291,7 @@ kl_status acquire(kl_stream* s, int layer, int keep_slot, int* slot_out) {
 
 kl_status sumsq(kl_stream* s, const float* p, int64_t n, int index, cudaStream_t st) {
   ProfScope ps("grad_sumsq", st, 0.0, 4.0 * n);
-  sumsq_kernel<<<SUMSQ_BLOCKS, SUMSQ_THREADS, 0, st>>>(p, n, s->partials + static_cast<int64_t>(index) * SUMSQ_BLOCKS);
+  launch_pdl(sumsq_kernel, SUMSQ_BLOCKS, SUMSQ_THREADS, 0, st, p, n, s->partials + static_cast<int64_t>(index) * SUMSQ_BLOCKS);
   KL_CUDA(cudaGetLastError());
   return KL_OK;
 }
@@ -545,14 +548,14 @@ kl_status kl_stream_run(kl_stream* s, const void* X, const int32_t* targets, flo
   {
     const int nref = n_weights(c) * L + 1;
     ProfScope ps("clip_finalize", cs, 0.0, 8.0 * nref * SUMSQ_BLOCKS);
-    clip_finalize_kernel<<<1, SUMSQ_THREADS, 0, cs>>>(s->partials, nref, s->loss, clip_max_norm, s->result);
+    launch_pdl(clip_finalize_kernel, 1, SUMSQ_THREADS, 0, cs, s->partials, nref, s->loss, clip_max_norm, s->result);
   }
   KL_CUDA(cudaGetLastError());
   {
     double moved = 0.0;
     for (const GradRef& r : refs) moved += 8.0 * static_cast<double>(r.n);
     ProfScope ps("clip_scale", cs, 0.0, moved);
-    clip_scale_kernel<<<8 * num_sms(), 256, 0, cs>>>(s->refs, static_cast<int>(refs.size()), total_chunks,
+    launch_pdl(clip_scale_kernel, 8 * num_sms(), 256, 0, cs, s->refs, static_cast<int>(refs.size()), total_chunks,
                                                      s->result);
   }
   KL_CUDA(cudaGetLastError());
