@@ -117,9 +117,12 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_
 
 // Warp-uniform form for roles whose next step is a warp-collective instruction
 // (tcgen05.ld / tcgen05.st): every lane calls it and every lane gets the same
-// answer, false if the abort flag is set or any lane's wait gave up.
+// answer, false if the abort flag is set or any lane's wait gave up. A phase
+// that is already complete is taken without looking at the abort flag (a role
+// whose partner aborted stops at its next wait that would block).
 __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, uint32_t* err,
                                                volatile int* abort_flag) {
+  if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
   const bool ok = !*abort_flag && mbar_wait(bar, parity, err);
   return __all_sync(0xffffffffu, ok);
 }
