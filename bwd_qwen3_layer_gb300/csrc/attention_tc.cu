@@ -33,6 +33,11 @@ constexpr int BQ = 128;       // query rows per CTA
 constexpr int BKV = 128;      // keys per tile
 constexpr uint32_t TILE_BYTES = 128 * 128 * 2;   // 32 KB: two 16 KB swizzle blocks of 64 columns
 constexpr int THREADS = 192;
+// Backward kernels: TMA warp, MMA warp and 8 elementwise warps, two per TMEM
+// lane quarter, each taking 32 of a step's 64 columns (one warp per scheduler
+// left the exp / multiply / store chain of a step unhidden).
+constexpr int BWD_THREADS = 320;
+constexpr int BWD_EW = 8;                     // elementwise warps
 constexpr float LOG2E_F = 1.4426950408889634f;
 constexpr float LN2_F = 0.6931471805599453f;
 
@@ -410,7 +415,7 @@ constexpr uint32_t KV_OFF_BAR = KV_OFF_STAT + KV_QS * 512;
 constexpr size_t KV_SMEM = 1024 + KV_OFF_BAR + 256;
 static_assert(KV_SMEM <= 232448, "dK/dV shared memory above the per-CTA limit");
 
-__global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid_constant__ BwdParams p) {
   pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -447,8 +452,8 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(st_full(s), 1);
-      mbar_init(st_free(s), 4);
-      mbar_init(p_full(s), 4);
+      mbar_init(st_free(s), BWD_EW);
+      mbar_init(p_full(s), BWD_EW);
       mbar_init(p_free(s), 1);
     }
     mbar_init(done, 1);
@@ -503,58 +508,84 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid
     for (int it = (issued > KV_QS ? issued - KV_QS : 0); it < issued; ++it)
       mbar_wait(q_full(it % KV_QS), (it / KV_QS) & 1, p.err);
   } else if (warp == 1) {
-    // ---------------- MMA (whole warp; the elected lane issues) ----------------
+    // ---------------- MMA (the elected lane issues) ----------------
+    // S^T / dP^T of step j go out as soon as their TMEM buffer (j & 1) is free
+    // (the elementwise warps have loaded step j - 2) and the step's Q / dO have
+    // landed; the gradient products of step j go out as soon as its P^T / dS^T
+    // are written. One ordered issue stream would hold S^T(j) behind the
+    // gradients of step j - 2 and leave the elementwise warps waiting.
     const bool el = elect_one();
     const uint32_t id_st = idesc_bf16_f32(128, 64, 0, 0);
     const uint32_t id_gr = idesc_bf16_f32(128, 128, 0, 1);
     bool ok = mbar_wait_warp(kv_full, 0, p.err, abort_flag);
-    auto issue_grad = [&](int it) -> bool {
-      const int s = it & 1, qs = it % KV_QS;
-      if (!mbar_wait_warp(p_full(s), (it >> 1) & 1, p.err, abort_flag)) return false;
-      tc_fence_after();
-      const uint32_t sq = sb + KV_OFF_Q + qs * T64, sdo = sb + KV_OFF_DO + qs * T64;
-      if (el) {
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16(tmem + 256, desc_k64(sb + KV_OFF_P + s * PT_BYTES, kk), desc_mn128(sdo, 8192, kk), id_gr,
-                    (it > 0 || kk > 0) ? 1u : 0u);
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16(tmem + 384, desc_k64(sb + KV_OFF_DS + s * PT_BYTES, kk), desc_mn128(sq, 8192, kk), id_gr,
-                    (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(q_free(qs));
-        umma_commit(p_free(s));
+    if (el && ok) {
+      int ns = 0, ng = 0;          // next step whose S^T / dP^T, whose gradients, go out
+      uint32_t idle = 0;
+      uint64_t since = 0;
+      while (ng < nit) {
+        bool prog = false;
+        if (ng < ns && mbar_test_wait(p_full(ng & 1), (ng >> 1) & 1)) {
+          tc_fence_after();
+          const int sg = ng & 1, qs = ng % KV_QS;
+          const uint32_t sq = sb + KV_OFF_Q + qs * T64, sdo = sb + KV_OFF_DO + qs * T64;
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem + 256, desc_k64(sb + KV_OFF_P + sg * PT_BYTES, kk), desc_mn128(sdo, 8192, kk), id_gr,
+                      (ng > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem + 384, desc_k64(sb + KV_OFF_DS + sg * PT_BYTES, kk), desc_mn128(sq, 8192, kk), id_gr,
+                      (ng > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(q_free(qs));
+          umma_commit(p_free(sg));
+          ++ng;
+          prog = true;
+        }
+        if (ns < nit && mbar_test_wait(q_full(ns % KV_QS), (ns / KV_QS) & 1) &&
+            (ns < 2 || mbar_test_wait(st_free(ns & 1), ((ns >> 1) & 1) ^ 1u))) {
+          tc_fence_after();
+          const int ss = ns & 1, qs = ns % KV_QS;
+          const uint32_t sq = sb + KV_OFF_Q + qs * T64, sdo = sb + KV_OFF_DO + qs * T64;
+          for (int kk = 0; kk < HD / 16; ++kk)
+            umma_bf16(tmem + ss * 64, desc_k128(sb + KV_OFF_K, 16384, kk), desc_k128(sq, 8192, kk), id_st, kk > 0);
+          for (int kk = 0; kk < HD / 16; ++kk)
+            umma_bf16(tmem + 128 + ss * 64, desc_k128(sb + KV_OFF_V, 16384, kk), desc_k128(sdo, 8192, kk), id_st,
+                      kk > 0);
+          umma_commit(st_full(ss));
+          ++ns;
+          prog = true;
+        }
+        if (prog) {
+          idle = 0;
+          since = 0;
+          continue;
+        }
+        // nothing ready: keep polling, bounded (the other roles stop on the abort flag)
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        if ((++idle & 1023u) == 0) {
+          const uint64_t now = global_timer_ns();
+          if (since == 0) {
+            since = now;
+          } else if (now - since > KL_WAIT_LIMIT_NS) {
+            record_error(p.err, KL_DEVERR_TIMEOUT);
+            ok = false;
+            break;
+          }
+        }
       }
-      __syncwarp();
-      return true;
-    };
-    for (int it = 0; ok && it < nit; ++it) {
-      const int s = it & 1, qs = it % KV_QS;
-      const uint32_t ph = (it >> 1) & 1;
-      if (!mbar_wait_warp(q_full(qs), (it / KV_QS) & 1, p.err, abort_flag) ||
-          (it >= 2 && !mbar_wait_warp(st_free(s), ph ^ 1u, p.err, abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t sq = sb + KV_OFF_Q + qs * T64, sdo = sb + KV_OFF_DO + qs * T64;
-      if (el) {
-        for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16(tmem + s * 64, desc_k128(sb + KV_OFF_K, 16384, kk), desc_k128(sq, 8192, kk), id_st, kk > 0);
-        for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16(tmem + 128 + s * 64, desc_k128(sb + KV_OFF_V, 16384, kk), desc_k128(sdo, 8192, kk), id_st,
-                    kk > 0);
-        umma_commit(st_full(s));
-      }
-      __syncwarp();
-      if (it >= 1 && !issue_grad(it - 1)) ok = false;
     }
-    if (ok && !issue_grad(nit - 1)) ok = false;
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, __ffs(__ballot_sync(0xffffffffu, el)) - 1) != 0;
     if (!ok) *abort_flag = 1;
     if (el) umma_commit(done);
     __syncwarp();
     mbar_wait(done, 0, p.err);
   } else if (warp >= 2) {
     // ---------------- P^T, dS^T (thread = key row) and the final dK/dV ----------------
+    // warp 2 + 4 * half + i: lane quarter (warp & 3), queries 32 * half .. + 31 of a step
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int col0 = half * 32;
     const int r = quarter * 32 + lane;
     const int key = k0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -568,11 +599,9 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid
       const int q0 = k0 + it * 64;
       if (!mbar_wait_warp(st_full(s), ph, p.err, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sv[64], dv[64];
-      tmem_ld_32x32b_x32(tmem + lane_off + s * 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
-      tmem_ld_32x32b_x32(tmem + lane_off + s * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-      tmem_ld_32x32b_x32(tmem + lane_off + 128 + s * 64, *reinterpret_cast<uint32_t(*)[32]>(dv));
-      tmem_ld_32x32b_x32(tmem + lane_off + 128 + s * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(dv + 32));
+      uint32_t sv[32], dv[32];
+      tmem_ld_32x32b_x32(tmem + lane_off + s * 64 + col0, sv);
+      tmem_ld_32x32b_x32(tmem + lane_off + 128 + s * 64 + col0, dv);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
@@ -588,7 +617,8 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid
       }
       const float* sl = reinterpret_cast<const float*>(smem + KV_OFF_STAT + (it % KV_QS) * 512);
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
+      for (int c8l = 0; c8l < 4; ++c8l) {
+        const int c8 = half * 4 + c8l;
         // lse (log2 units, +inf past the sequence end) and D of these 8 queries
         float l8[8], d8[8];
         const int qa = q0 + c8 * 8;
@@ -625,13 +655,13 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid
         uint32_t pk[4], dk4[4];
 #pragma unroll
         for (int e = 0; e < 8; e += 2) {
-          const int c = c8 * 8 + e;
-          float p0 = ex2_approx(fmaf(__uint_as_float(sv[c]), p.scale_log2, -l8[e]));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), p.scale_log2, -l8[e + 1]));
+          const int c = c8 * 8 + e, cl = c8l * 8 + e;   // step column, column within this warp's half
+          float p0 = ex2_approx(fmaf(__uint_as_float(sv[cl]), p.scale_log2, -l8[e]));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sv[cl + 1]), p.scale_log2, -l8[e + 1]));
           if (c < lim) p0 = 0.f;
           if (c + 1 < lim) p1 = 0.f;
-          const float d0 = p0 * (__uint_as_float(dv[c]) - d8[e]);
-          const float d1 = p1 * (__uint_as_float(dv[c + 1]) - d8[e + 1]);
+          const float d0 = p0 * (__uint_as_float(dv[cl]) - d8[e]);
+          const float d1 = p1 * (__uint_as_float(dv[cl + 1]) - d8[e + 1]);
           pk[e >> 1] = pack_bf16x2(p0, p1);
           dk4[e >> 1] = pack_bf16x2(d0, d1);
         }
@@ -650,7 +680,8 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid
       const bool in = key < p.S;
       const int64_t o = (static_cast<int64_t>(row0 + (in ? key : 0)) * p.Hkv + jh) * HD;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = half * 2 + cc;   // this warp's 64 of the 128 head columns
         uint32_t v[32];
         tmem_ld_32x32b_x32(tmem + lane_off + 256 + c * 32, v);
         tmem_ld_wait();
@@ -696,7 +727,7 @@ constexpr uint32_t DQ_OFF_BAR = DQ_OFF_DS + 2 * 16384;
 constexpr size_t DQ_SMEM = 1024 + DQ_OFF_BAR + 256;
 static_assert(DQ_SMEM <= 232448, "dQ shared memory above the per-CTA limit");
 
-__global__ void __launch_bounds__(THREADS, 1) fa_bwd_dq_tc_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dq_tc_kernel(const __grid_constant__ BwdParams p) {
   pdl_enter();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -731,8 +762,8 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dq_tc_kernel(const __grid_c
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(sd_full(s), 1);
-      mbar_init(sd_free(s), 4);
-      mbar_init(ds_full(s), 4);
+      mbar_init(sd_free(s), BWD_EW);
+      mbar_init(ds_full(s), BWD_EW);
       mbar_init(ds_free(s), 1);
     }
     mbar_init(done, 1);
@@ -779,53 +810,77 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dq_tc_kernel(const __grid_c
     for (int j = (issued > DQ_KS ? issued - DQ_KS : 0); j < issued; ++j)
       mbar_wait(kv_full(j % DQ_KS), (j / DQ_KS) & 1, p.err);
   } else if (warp == 1) {
-    // ---------------- MMA (whole warp; the elected lane issues) ----------------
+    // ---------------- MMA (the elected lane issues) ----------------
+    // S / dP of step j go out as soon as their TMEM buffer (j & 1) is free and
+    // the step's K / V have landed; dQ += dS K of step j as soon as its dS is
+    // written (see the dK / dV kernel for why the two streams are not ordered).
     const bool el = elect_one();
     const uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);
     const uint32_t id_q = idesc_bf16_f32(128, 128, 0, 1);
     bool ok = mbar_wait_warp(q_full, 0, p.err, abort_flag);
-    auto issue_dq = [&](int j) -> bool {
-      const int s = j & 1, ks = j % DQ_KS;
-      if (!mbar_wait_warp(ds_full(s), (j >> 1) & 1, p.err, abort_flag)) return false;
-      tc_fence_after();
-      if (el) {
-        for (int kk = 0; kk < 4; ++kk)
-          umma_bf16(tmem + 256, desc_k64(sb + DQ_OFF_DS + s * 16384, kk),
-                    desc_mn128(sb + DQ_OFF_K + ks * T64, 8192, kk), id_q, (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(kv_free(ks));
-        umma_commit(ds_free(s));
+    if (el && ok) {
+      int ns = 0, ng = 0;          // next step whose S / dP, whose dQ product, goes out
+      uint32_t idle = 0;
+      uint64_t since = 0;
+      while (ng < nkb) {
+        bool prog = false;
+        if (ng < ns && mbar_test_wait(ds_full(ng & 1), (ng >> 1) & 1)) {
+          tc_fence_after();
+          const int sg = ng & 1, ks = ng % DQ_KS;
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem + 256, desc_k64(sb + DQ_OFF_DS + sg * 16384, kk),
+                      desc_mn128(sb + DQ_OFF_K + ks * T64, 8192, kk), id_q, (ng > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(kv_free(ks));
+          umma_commit(ds_free(sg));
+          ++ng;
+          prog = true;
+        }
+        if (ns < nkb && mbar_test_wait(kv_full(ns % DQ_KS), (ns / DQ_KS) & 1) &&
+            (ns < 2 || mbar_test_wait(sd_free(ns & 1), ((ns >> 1) & 1) ^ 1u))) {
+          tc_fence_after();
+          const int ss = ns & 1, ks = ns % DQ_KS;
+          for (int kk = 0; kk < HD / 16; ++kk)
+            umma_bf16(tmem + ss * 64, desc_k128(sb + DQ_OFF_Q, 16384, kk),
+                      desc_k128(sb + DQ_OFF_K + ks * T64, 8192, kk), id_s, kk > 0);
+          for (int kk = 0; kk < HD / 16; ++kk)
+            umma_bf16(tmem + 128 + ss * 64, desc_k128(sb + DQ_OFF_DO, 16384, kk),
+                      desc_k128(sb + DQ_OFF_V + ks * T64, 8192, kk), id_s, kk > 0);
+          umma_commit(sd_full(ss));
+          ++ns;
+          prog = true;
+        }
+        if (prog) {
+          idle = 0;
+          since = 0;
+          continue;
+        }
+        if (*abort_flag) {
+          ok = false;
+          break;
+        }
+        if ((++idle & 1023u) == 0) {
+          const uint64_t now = global_timer_ns();
+          if (since == 0) {
+            since = now;
+          } else if (now - since > KL_WAIT_LIMIT_NS) {
+            record_error(p.err, KL_DEVERR_TIMEOUT);
+            ok = false;
+            break;
+          }
+        }
       }
-      __syncwarp();
-      return true;
-    };
-    for (int j = 0; ok && j < nkb; ++j) {
-      const int s = j & 1, ks = j % DQ_KS;
-      const uint32_t ph = (j >> 1) & 1;
-      if (!mbar_wait_warp(kv_full(ks), (j / DQ_KS) & 1, p.err, abort_flag) ||
-          (j >= 2 && !mbar_wait_warp(sd_free(s), ph ^ 1u, p.err, abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      if (el) {
-        for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16(tmem + s * 64, desc_k128(sb + DQ_OFF_Q, 16384, kk), desc_k128(sb + DQ_OFF_K + ks * T64, 8192, kk),
-                    id_s, kk > 0);
-        for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16(tmem + 128 + s * 64, desc_k128(sb + DQ_OFF_DO, 16384, kk),
-                    desc_k128(sb + DQ_OFF_V + ks * T64, 8192, kk), id_s, kk > 0);
-        umma_commit(sd_full(s));
-      }
-      __syncwarp();
-      if (j >= 1 && !issue_dq(j - 1)) ok = false;
     }
-    if (ok && !issue_dq(nkb - 1)) ok = false;
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, __ffs(__ballot_sync(0xffffffffu, el)) - 1) != 0;
     if (!ok) *abort_flag = 1;
     if (el) umma_commit(done);
     __syncwarp();
     mbar_wait(done, 0, p.err);
   } else if (warp >= 2) {
+    // warp 2 + 4 * half + i: lane quarter (warp & 3), keys 32 * half .. + 31 of a step,
+    // and at the end rotary planes 32 * half .. + 31 (with their partners at +64)
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int col0 = half * 32;
     const int r = quarter * 32 + lane;
     const int qrow = q0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -838,11 +893,9 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dq_tc_kernel(const __grid_c
       const uint32_t ph = (j >> 1) & 1;
       if (!mbar_wait_warp(sd_full(s), ph, p.err, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sv[64], dv[64];
-      tmem_ld_32x32b_x32(tmem + lane_off + s * 64, *reinterpret_cast<uint32_t(*)[32]>(sv));
-      tmem_ld_32x32b_x32(tmem + lane_off + s * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(sv + 32));
-      tmem_ld_32x32b_x32(tmem + lane_off + 128 + s * 64, *reinterpret_cast<uint32_t(*)[32]>(dv));
-      tmem_ld_32x32b_x32(tmem + lane_off + 128 + s * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(dv + 32));
+      uint32_t sv[32], dv[32];
+      tmem_ld_32x32b_x32(tmem + lane_off + s * 64 + col0, sv);
+      tmem_ld_32x32b_x32(tmem + lane_off + 128 + s * 64 + col0, dv);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
@@ -851,16 +904,17 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dq_tc_kernel(const __grid_c
       const int lim = qrow - j * 64;          // keys j*64 + c with c <= lim are kept
       uint8_t* drw = smem + DQ_OFF_DS + s * 16384 + r * 128;
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
+      for (int c8l = 0; c8l < 4; ++c8l) {
+        const int c8 = half * 4 + c8l;
         uint32_t pk[4];
 #pragma unroll
         for (int e = 0; e < 8; e += 2) {
-          const int c = c8 * 8 + e;
-          float p0 = ex2_approx(fmaf(__uint_as_float(sv[c]), p.scale_log2, -l2));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sv[c + 1]), p.scale_log2, -l2));
+          const int c = c8 * 8 + e, cl = c8l * 8 + e;   // step column, column within this warp's half
+          float p0 = ex2_approx(fmaf(__uint_as_float(sv[cl]), p.scale_log2, -l2));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sv[cl + 1]), p.scale_log2, -l2));
           if (c > lim) p0 = 0.f;
           if (c + 1 > lim) p1 = 0.f;
-          pk[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[c]) - Dq), p1 * (__uint_as_float(dv[c + 1]) - Dq));
+          pk[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[cl]) - Dq), p1 * (__uint_as_float(dv[cl + 1]) - Dq));
         }
         *reinterpret_cast<uint4*>(drw + ((c8 ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
@@ -868,31 +922,24 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dq_tc_kernel(const __grid_c
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full(s));
     }
-    // the query's rotary cos/sin (planes 0..31) are fetched before the wait for the last MMA
+    // the query's rotary cos/sin of this warp's planes are fetched before the wait for the last MMA
     const float2* cs = p.rope_cs ? p.rope_cs + static_cast<int64_t>(qrow < p.S ? qrow : 0) * 64 : nullptr;
-    float4 csn[16];
+    float4 csc[16];
     if (cs) {
 #pragma unroll
-      for (int e = 0; e < 16; ++e) csn[e] = reinterpret_cast<const float4*>(cs)[e];
+      for (int e = 0; e < 16; ++e) csc[e] = reinterpret_cast<const float4*>(cs)[16 * half + e];
     }
     const bool fin = ok && mbar_wait_warp(done, 0, p.err, abort_flag);
     if (fin && p.dq_out) {
       // bf16 dQ, turned back by the rotary angle of the query's position when a table is given
       tc_fence_after();
       __nv_bfloat16* orow = p.dq_out + (static_cast<int64_t>(row0 + qrow) * p.Hq + h) * HD;
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      {
+        const int c = half;
         uint32_t va[32], vb[32];   // planes 32c .. 32c+31 and their partners at +64
         tmem_ld_32x32b_x32(tmem + lane_off + 256 + c * 32, va);
         tmem_ld_32x32b_x32(tmem + lane_off + 256 + 64 + c * 32, vb);
         tmem_ld_wait();
-        float4 csc[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) csc[e] = csn[e];
-        if (cs && c == 0) {   // planes 32..63 in flight while planes 0..31 are turned
-#pragma unroll
-          for (int e = 0; e < 16; ++e) csn[e] = reinterpret_cast<const float4*>(cs)[16 + e];
-        }
         if (qrow < p.S) {
           float xa[32], xb[32];
 #pragma unroll
@@ -925,7 +972,8 @@ __global__ void __launch_bounds__(THREADS, 1) fa_bwd_dq_tc_kernel(const __grid_c
       tc_fence_after();
       float* orow = p.dq_acc + (static_cast<int64_t>(row0 + qrow) * p.Hq + h) * HD;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = half * 2 + cc;
         uint32_t v[32];
         tmem_ld_32x32b_x32(tmem + lane_off + 256 + c * 32, v);
         tmem_ld_wait();
@@ -1052,7 +1100,7 @@ kl_status attention_bwd_tc(int B, int S, int Hq, int Hkv, const void* q, const v
   {
     ProfScope ps("attn_bwd_dkdv_tc", st, 8.0 * B * Hq * HD * pairs, 0.0);
     dim3 grid(Hq, (S + BKV - 1) / BKV, B);
-    launch_pdl(fa_bwd_dkdv_tc_kernel, grid, THREADS, KV_SMEM, st, p);
+    launch_pdl(fa_bwd_dkdv_tc_kernel, grid, BWD_THREADS, KV_SMEM, st, p);
   }
   KL_CUDA(cudaGetLastError());
   // dQ: Q and dO tiles of 128 rows, K and V tiles of 64 rows
@@ -1064,7 +1112,7 @@ kl_status attention_bwd_tc(int B, int S, int Hq, int Hkv, const void* q, const v
     // only the dQ product is algorithmic work here; S and dP are recomputed
     ProfScope ps("attn_bwd_dq_tc", st, 2.0 * B * Hq * HD * pairs, 0.0);
     dim3 grid(Hq, (S + BQ - 1) / BQ, B);
-    launch_pdl(fa_bwd_dq_tc_kernel, grid, THREADS, DQ_SMEM, st, p);
+    launch_pdl(fa_bwd_dq_tc_kernel, grid, BWD_THREADS, DQ_SMEM, st, p);
   }
   KL_CUDA(cudaGetLastError());
   return KL_OK;
