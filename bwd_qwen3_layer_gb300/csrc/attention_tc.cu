@@ -21,6 +21,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "internal.h"
 #include "kl_common.cuh"
@@ -616,6 +617,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
         break;
       }
       const float* sl = reinterpret_cast<const float*>(smem + KV_OFF_STAT + (it % KV_QS) * 512);
+      // the causal mask only reaches the steps at the diagonal: the others take the unmasked body
+      auto step = [&](auto masked) {
+      constexpr bool MASK = decltype(masked)::value;
 #pragma unroll
       for (int c8l = 0; c8l < 4; ++c8l) {
         const int c8 = half * 4 + c8l;
@@ -658,8 +662,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
           const int c = c8 * 8 + e, cl = c8l * 8 + e;   // step column, column within this warp's half
           float p0 = ex2_approx(fmaf(__uint_as_float(sv[cl]), p.scale_log2, -l8[e]));
           float p1 = ex2_approx(fmaf(__uint_as_float(sv[cl + 1]), p.scale_log2, -l8[e + 1]));
-          if (c < lim) p0 = 0.f;
-          if (c + 1 < lim) p1 = 0.f;
+          if (MASK && c < lim) p0 = 0.f;
+          if (MASK && c + 1 < lim) p1 = 0.f;
           const float d0 = p0 * (__uint_as_float(dv[cl]) - d8[e]);
           const float d1 = p1 * (__uint_as_float(dv[cl + 1]) - d8[e + 1]);
           pk[e >> 1] = pack_bf16x2(p0, p1);
@@ -669,6 +673,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
         *reinterpret_cast<uint4*>(prow + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         *reinterpret_cast<uint4*>(drw + off) = make_uint4(dk4[0], dk4[1], dk4[2], dk4[3]);
       }
+      };
+      if (__any_sync(0xffffffffu, lim > col0)) step(std::true_type{});
+      else step(std::false_type{});
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full(s));
@@ -903,6 +910,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dq_tc_kernel(const __gr
       if (j >= 2 && !mbar_wait_warp(ds_free(s), ph ^ 1u, p.err, abort_flag)) { ok = false; break; }
       const int lim = qrow - j * 64;          // keys j*64 + c with c <= lim are kept
       uint8_t* drw = smem + DQ_OFF_DS + s * 16384 + r * 128;
+      auto step = [&](auto masked) {
+      constexpr bool MASK = decltype(masked)::value;
 #pragma unroll
       for (int c8l = 0; c8l < 4; ++c8l) {
         const int c8 = half * 4 + c8l;
@@ -912,12 +921,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dq_tc_kernel(const __gr
           const int c = c8 * 8 + e, cl = c8l * 8 + e;   // step column, column within this warp's half
           float p0 = ex2_approx(fmaf(__uint_as_float(sv[cl]), p.scale_log2, -l2));
           float p1 = ex2_approx(fmaf(__uint_as_float(sv[cl + 1]), p.scale_log2, -l2));
-          if (c > lim) p0 = 0.f;
-          if (c + 1 > lim) p1 = 0.f;
+          if (MASK && c > lim) p0 = 0.f;
+          if (MASK && c + 1 > lim) p1 = 0.f;
           pk[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[cl]) - Dq), p1 * (__uint_as_float(dv[cl + 1]) - Dq));
         }
         *reinterpret_cast<uint4*>(drw + ((c8 ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
+      };
+      // keys j*64 + c with c > lim are masked: only the steps at the diagonal have any
+      if (__any_sync(0xffffffffu, lim < col0 + 31)) step(std::true_type{});
+      else step(std::false_type{});
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full(s));
