@@ -403,36 +403,45 @@ struct BwdParams {
 // ---------------------------------------------------------------------------
 // dK / dV
 // ---------------------------------------------------------------------------
+// Four Q / dO stages let the scores of a step go out two steps ahead of its
+// gradients; they fit because P^T / dS^T are single-buffered (each elementwise
+// warp holds a step's packed values in registers until the previous step's
+// gradient products have released the buffer) and because the dynamic shared
+// memory is taken as 1024-byte aligned (checked at entry) instead of carrying
+// alignment slack.
 constexpr uint32_t KV_OFF_K = 0;
 constexpr uint32_t KV_OFF_V = KV_OFF_K + TILE_BYTES;
-constexpr int KV_QS = 3;                                      // stages of the Q / dO / lse / D ring
+constexpr int KV_QS = 4;                                      // stages of the Q / dO / lse / D ring
 constexpr uint32_t KV_OFF_Q = KV_OFF_V + TILE_BYTES;         // KV_QS stages of T64
 constexpr uint32_t KV_OFF_DO = KV_OFF_Q + KV_QS * T64;       // KV_QS stages of T64
 constexpr uint32_t PT_BYTES = 128 * 64 * 2;                   // 16 KB: 128 key rows x 64 queries
-constexpr uint32_t KV_OFF_P = KV_OFF_DO + KV_QS * T64;       // 2 buffers of P^T
-constexpr uint32_t KV_OFF_DS = KV_OFF_P + 2 * PT_BYTES;      // 2 buffers of dS^T
-constexpr uint32_t KV_OFF_STAT = KV_OFF_DS + 2 * PT_BYTES;  // KV_QS stages: lse[64], D[64] (fp32)
+constexpr uint32_t KV_OFF_P = KV_OFF_DO + KV_QS * T64;       // P^T
+constexpr uint32_t KV_OFF_DS = KV_OFF_P + PT_BYTES;          // dS^T
+constexpr uint32_t KV_OFF_STAT = KV_OFF_DS + PT_BYTES;      // KV_QS stages: lse[64], D[64] (fp32)
 constexpr uint32_t KV_OFF_BAR = KV_OFF_STAT + KV_QS * 512;
-constexpr size_t KV_SMEM = 1024 + KV_OFF_BAR + 256;
+constexpr size_t KV_SMEM = KV_OFF_BAR + 256;
 static_assert(KV_SMEM <= 232448, "dK/dV shared memory above the per-CTA limit");
 
 __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid_constant__ BwdParams p) {
   pdl_enter();
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  extern __shared__ __align__(1024) uint8_t kv_smem_raw[];
+  if (smem_u32(kv_smem_raw) & 1023u) {   // the layout has no alignment slack (CTA-uniform exit)
+    if (threadIdx.x == 0) record_error(p.err, KL_DEVERR_SMEM);
+    return;
+  }
+  uint8_t* smem = kv_smem_raw;
   const uint32_t sb = smem_u32(smem);
   const uint32_t bar = sb + KV_OFF_BAR;
   const uint32_t kv_full = bar;
   auto q_full = [&](int s) { return bar + 8 + 8 * s; };              // KV_QS of each ring barrier
-  auto q_free = [&](int s) { return bar + 32 + 8 * s; };
-  auto st_full = [&](int s) { return bar + 56 + 8 * s; };             // 2 of each TMEM / P barrier
-  auto st_free = [&](int s) { return bar + 72 + 8 * s; };
-  auto p_full = [&](int s) { return bar + 88 + 8 * s; };
-  auto p_free = [&](int s) { return bar + 104 + 8 * s; };
-  const uint32_t done = bar + 120;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + KV_OFF_BAR + 128);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + KV_OFF_BAR + 132);
+  auto q_free = [&](int s) { return bar + 8 + 8 * KV_QS + 8 * s; };
+  auto st_full = [&](int s) { return bar + 8 + 16 * KV_QS + 8 * s; }; // 2 of each TMEM barrier
+  auto st_free = [&](int s) { return bar + 24 + 16 * KV_QS + 8 * s; };
+  const uint32_t p_full = bar + 40 + 16 * KV_QS;                      // the single P^T / dS^T buffer
+  const uint32_t p_free = bar + 48 + 16 * KV_QS;
+  const uint32_t done = bar + 56 + 16 * KV_QS;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + KV_OFF_BAR + 64 + 16 * KV_QS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + KV_OFF_BAR + 68 + 16 * KV_QS);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kb = blockIdx.y;                 // key tiles near the start see the most queries
@@ -454,9 +463,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
     for (int s = 0; s < 2; ++s) {
       mbar_init(st_full(s), 1);
       mbar_init(st_free(s), BWD_EW);
-      mbar_init(p_full(s), BWD_EW);
-      mbar_init(p_free(s), 1);
     }
+    mbar_init(p_full, BWD_EW);
+    mbar_init(p_free, 1);
     mbar_init(done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -525,18 +534,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
       uint64_t since = 0;
       while (ng < nit) {
         bool prog = false;
-        if (ng < ns && mbar_test_wait(p_full(ng & 1), (ng >> 1) & 1)) {
+        if (ng < ns && mbar_test_wait(p_full, ng & 1)) {
           tc_fence_after();
-          const int sg = ng & 1, qs = ng % KV_QS;
+          const int qs = ng % KV_QS;
           const uint32_t sq = sb + KV_OFF_Q + qs * T64, sdo = sb + KV_OFF_DO + qs * T64;
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + 256, desc_k64(sb + KV_OFF_P + sg * PT_BYTES, kk), desc_mn128(sdo, 8192, kk), id_gr,
+            umma_bf16(tmem + 256, desc_k64(sb + KV_OFF_P, kk), desc_mn128(sdo, 8192, kk), id_gr,
                       (ng > 0 || kk > 0) ? 1u : 0u);
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + 384, desc_k64(sb + KV_OFF_DS + sg * PT_BYTES, kk), desc_mn128(sq, 8192, kk), id_gr,
+            umma_bf16(tmem + 384, desc_k64(sb + KV_OFF_DS, kk), desc_mn128(sq, 8192, kk), id_gr,
                       (ng > 0 || kk > 0) ? 1u : 0u);
           umma_commit(q_free(qs));
-          umma_commit(p_free(sg));
+          umma_commit(p_free);
           ++ng;
           prog = true;
         }
@@ -607,10 +616,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(st_free(s));
-      if (it >= 2 && !mbar_wait_warp(p_free(s), ph ^ 1u, p.err, abort_flag)) { ok = false; break; }
       const int lim = key - q0;              // queries q0 + c with c >= lim see this key
-      uint8_t* prow = smem + KV_OFF_P + s * PT_BYTES + r * 128;
-      uint8_t* drw = smem + KV_OFF_DS + s * PT_BYTES + r * 128;
+      uint8_t* prow = smem + KV_OFF_P + r * 128;
+      uint8_t* drw = smem + KV_OFF_DS + r * 128;
+      uint4 pst[4], dst[4];                  // this warp's 4 chunks of the row, until the buffer is free
       // the stage's lse / D copies completed with its Q / dO (q_full), before S^T
       if (stat_smem && !mbar_wait_warp(q_full(it % KV_QS), (it / KV_QS) & 1, p.err, abort_flag)) {
         ok = false;
@@ -669,16 +678,23 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
           pk[e >> 1] = pack_bf16x2(p0, p1);
           dk4[e >> 1] = pack_bf16x2(d0, d1);
         }
-        const int off = ((c8 ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(prow + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        *reinterpret_cast<uint4*>(drw + off) = make_uint4(dk4[0], dk4[1], dk4[2], dk4[3]);
+        pst[c8l] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        dst[c8l] = make_uint4(dk4[0], dk4[1], dk4[2], dk4[3]);
       }
       };
       if (__any_sync(0xffffffffu, lim > col0)) step(std::true_type{});
       else step(std::false_type{});
+      // the buffer is free once the previous step's gradient products completed
+      if (it >= 1 && !mbar_wait_warp(p_free, (it - 1) & 1, p.err, abort_flag)) { ok = false; break; }
+#pragma unroll
+      for (int c8l = 0; c8l < 4; ++c8l) {
+        const int off = (((half * 4 + c8l) ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(prow + off) = pst[c8l];
+        *reinterpret_cast<uint4*>(drw + off) = dst[c8l];
+      }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full(s));
+      if (lane == 0) mbar_arrive(p_full);
     }
     // The TMEM loads are warp-collective: every lane takes part; only rows
     // inside the sequence add their results.
@@ -1113,7 +1129,7 @@ kl_status attention_bwd_tc(int B, int S, int Hq, int Hkv, const void* q, const v
   {
     ProfScope ps("attn_bwd_dkdv_tc", st, 8.0 * B * Hq * HD * pairs, 0.0);
     dim3 grid(Hq, (S + BKV - 1) / BKV, B);
-    launch_pdl(fa_bwd_dkdv_tc_kernel, grid, BWD_THREADS, KV_SMEM, st, p);
+    launch_pdl(fa_bwd_dkdv_tc_kernel, grid, BWD_THREADS, KV_SMEM, st, p);   // shared memory checked in-kernel
   }
   KL_CUDA(cudaGetLastError());
   // dQ: Q and dO tiles of 128 rows, K and V tiles of 64 rows

@@ -75,6 +75,8 @@ typedef enum kl_dtype { KL_F32 = 0, KL_BF16 = 1 } kl_dtype;
 /* Device error word bits, reported by kl_device_status(). */
 #define KL_DEVERR_TIMEOUT 0x1u      /* a pipeline wait gave up */
 #define KL_DEVERR_TARGET 0x2u       /* a CE target id was outside [0, V) */
+#define KL_DEVERR_SMEM 0x4u         /* a kernel found its shared memory misaligned
+                                       and returned without doing its work */
 
 KL_API const char* kl_version(void);
 KL_API const char* kl_status_str(kl_status s);
