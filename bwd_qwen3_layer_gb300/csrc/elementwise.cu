@@ -125,11 +125,14 @@ __global__ void __launch_bounds__(RF_THREADS) rmsnorm_fwd_row_kernel(int width, 
   const int row = blockIdx.x, tid = threadIdx.x;
   const int chunks = width / V;
   const int64_t off = static_cast<int64_t>(row) * width;
-  uint4 raw[NC];
+  uint4 raw[NC], graw[NC];   // the row and the gains, both in flight before the reduction
 #pragma unroll
   for (int j = 0; j < NC; ++j) {
     const int c = tid + j * RF_THREADS;
-    if (c < chunks) raw[j] = *reinterpret_cast<const uint4*>(x + off + c * V);
+    if (c < chunks) {
+      raw[j] = *reinterpret_cast<const uint4*>(x + off + c * V);
+      graw[j] = *reinterpret_cast<const uint4*>(gamma + c * V);
+    }
   }
   float ss = 0.f;
 #pragma unroll
@@ -155,7 +158,7 @@ __global__ void __launch_bounds__(RF_THREADS) rmsnorm_fwd_row_kernel(int width, 
     if (c < chunks) {
       float f[8], g[8];
       Vec<T>::decode(raw[j], f);
-      Vec<T>::load(gamma + c * V, g);
+      Vec<T>::decode(graw[j], g);
 #pragma unroll
       for (int e = 0; e < V; ++e) f[e] = g[e] * (f[e] * r);
       Vec<T>::store(h + off + c * V, f);

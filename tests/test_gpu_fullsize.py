@@ -57,6 +57,29 @@ def test_qwen3_layer_T2048_full_parity(kl):
         assert_rel(got["d" + n], g, TOL_BF16, "d" + n)
 
 
+def test_qwen3_layer_T2048_forward_bit_reproducible(kl):
+    """At full size the q/k/v, O and down projections split their last round of
+    tiles along K; the pieces are summed in a fixed order whichever CTA lands
+    last, so the whole forward (every saved tensor and Y) repeats bit for bit."""
+    B, S = 1, 2048
+    cfg = L.make_cfg(B, S, **QWEN, dtype=kl.KL_BF16)
+    w = {n: _dev_normal(shp, 0.02, 1.0 if n.startswith("gamma") else 0.0, f"rep.{n}")
+         for n, shp in L.weight_shapes(cfg).items()}
+    X = _dev_normal((B * S, QWEN["H"]), 1.0, 0.0, "rep.X")
+    ws = L.weights_struct(w)
+    buf = L.LayerBuffers(cfg, "cuda")
+    outs = []
+    for _ in range(2):
+        Y = torch.empty_like(X)
+        kl.kl_layer_forward(cfg, ws, X.data_ptr(), Y.data_ptr(), buf.saved, buf.fwd_ws.data_ptr(),
+                            buf.fwd_ws.numel())
+        torch.cuda.synchronize()
+        outs.append((Y.clone(), buf.saved_mem.clone()))
+    kl.kl_device_status()
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1], outs[1][1])
+
+
 def test_attention_S32768_sampled_and_invariants(kl):
     B, S, Hq, Hkv, d = 1, 32768, 64, 8, 128
     T = B * S
