@@ -50,3 +50,11 @@ from .qwen3_layer import (  # noqa: F401
     swiglu_fwd,
 )
 from .stack import stack_fwd_bwd, clip_coefficient  # noqa: F401
+from .paged import (  # noqa: F401,E402
+    gather,
+    layer_forward_paged,
+    paged_attention,
+    paged_write,
+    positions,
+    rope_at,
+)
