@@ -68,6 +68,10 @@ class StreamCfg(ctypes.Structure):
     _fields_ = [("layer", LayerCfg), ("n_layers", _i32), ("V", _i32), ("mode", _i32)]
 
 
+class PagedCfg(ctypes.Structure):
+    _fields_ = [("B", _i32), ("n_new", _i32), ("block_size", _i32), ("max_blocks", _i32), ("n_blocks", _i32)]
+
+
 class StreamResult(ctypes.Structure):
     _fields_ = [("loss", _f32), ("total_norm", _f32), ("clip_coef", _f32)]
 
@@ -107,6 +111,13 @@ _SIGNATURES = {
     "kl_stream_forward": (ctypes.c_int, [_vp, _vp, _vp, _vp]),
     "kl_stream_device_bytes": (_sz, [_vp]),
     "kl_stream_destroy": (None, [_vp]),
+    "kl_paged_kv_write": (ctypes.c_int, [_P(PagedCfg), _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "kl_paged_attention_ws_bytes": (_sz, [_P(PagedCfg), _i32, _i32, _i32]),
+    "kl_paged_attention": (ctypes.c_int, [_P(PagedCfg), _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                          _vp, _sz, _vp]),
+    "kl_layer_forward_paged_ws_bytes": (_sz, [_P(LayerCfg), _P(PagedCfg)]),
+    "kl_layer_forward_paged": (ctypes.c_int, [_P(LayerCfg), _P(PagedCfg), _P(LayerWeights), _vp, _vp, _vp, _vp,
+                                              _vp, _vp, _vp, _sz, _vp]),
     "kl_profile_enable": (ctypes.c_int, [_i32]),
     "kl_profile_read": (_i32, [_vp, _i32]),
     "kl_launch_count": (ctypes.c_uint64, []),
@@ -271,6 +282,31 @@ def kl_attention_bwd(B, S, Hq, Hkv, d, dtype, q, k, v, o, lse, dout, dq, dk, dv,
                      stream=None) -> None:
     check(load().kl_attention_bwd(B, S, Hq, Hkv, d, dtype, q, k, v, o, lse, dout, dq, dk, dv, ws, ws_bytes,
                                   _stream(stream)))
+
+
+def kl_paged_kv_write(pc: PagedCfg, Hkv, d, dtype, k_new, v_new, table, ctx, k_pool, v_pool, stream=None) -> None:
+    check(load().kl_paged_kv_write(ctypes.byref(pc), Hkv, d, dtype, k_new, v_new, table, ctx, k_pool, v_pool,
+                                   _stream(stream)))
+
+
+def kl_paged_attention_ws_bytes(pc: PagedCfg, Hq, Hkv, d) -> int:
+    return load().kl_paged_attention_ws_bytes(ctypes.byref(pc), Hq, Hkv, d)
+
+
+def kl_paged_attention(pc: PagedCfg, Hq, Hkv, d, dtype, q, k_pool, v_pool, table, ctx, o, lse, ws, ws_bytes,
+                       stream=None) -> None:
+    check(load().kl_paged_attention(ctypes.byref(pc), Hq, Hkv, d, dtype, q, k_pool, v_pool, table, ctx, o, lse, ws,
+                                    ws_bytes, _stream(stream)))
+
+
+def kl_layer_forward_paged_ws_bytes(cfg: LayerCfg, pc: PagedCfg) -> int:
+    return load().kl_layer_forward_paged_ws_bytes(ctypes.byref(cfg), ctypes.byref(pc))
+
+
+def kl_layer_forward_paged(cfg: LayerCfg, pc: PagedCfg, w: LayerWeights, X, Y, k_pool, v_pool, table, ctx, ws,
+                           ws_bytes, stream=None) -> None:
+    check(load().kl_layer_forward_paged(ctypes.byref(cfg), ctypes.byref(pc), ctypes.byref(w), X, Y, k_pool, v_pool,
+                                        table, ctx, ws, ws_bytes, _stream(stream)))
 
 
 def kl_device_status(stream=None) -> int:

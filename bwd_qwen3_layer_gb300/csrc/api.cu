@@ -212,6 +212,41 @@ void carve_bwd(const Dims& D, Carver& c, BwdWs* w) {
   w->qk_k = D.qk_norm ? c.take(w->qk_k_bytes) : nullptr;
 }
 
+// Workspace of the paged-cache layer forward: the step's activations (T = B *
+// n_new rows), the attention split partials and the GEMMs' last-round scratch.
+struct PagedWs {
+  void *h1, *q_pre, *k_pre, *v, *q, *k, *o, *x2, *h2, *g, *u, *m;
+  float *rstd1, *rstd2, *rstd_q, *rstd_k;
+  void* att;
+  size_t att_bytes;
+  void* tail;
+  size_t tail_bytes;
+};
+
+void carve_paged(const Dims& D, const kl_paged_cfg& pc, Carver& c, PagedWs* w) {
+  const size_t T = D.T, es = D.es;
+  w->h1 = c.take(T * D.H * es);
+  w->rstd1 = static_cast<float*>(c.take(T * 4));
+  w->q_pre = c.take(T * D.Dq * es);
+  w->k_pre = c.take(T * D.Dkv * es);
+  w->v = c.take(T * D.Dkv * es);
+  w->q = c.take(T * D.Dq * es);
+  w->k = c.take(T * D.Dkv * es);
+  w->rstd_q = static_cast<float*>(c.take(T * D.Hq * 4));
+  w->rstd_k = static_cast<float*>(c.take(T * D.Hkv * 4));
+  w->o = c.take(T * D.Dq * es);
+  w->x2 = c.take(T * D.H * es);
+  w->h2 = c.take(T * D.H * es);
+  w->rstd2 = static_cast<float*>(c.take(T * 4));
+  w->g = c.take(T * D.I * es);
+  w->u = c.take(T * D.I * es);
+  w->m = c.take(T * D.I * es);
+  w->att_bytes = paged_attention_ws(pc, D.Hq, D.Hkv);
+  w->att = w->att_bytes ? c.take(w->att_bytes) : nullptr;
+  w->tail_bytes = gemm_tail_ws_bytes();
+  w->tail = c.take(w->tail_bytes);
+}
+
 kl_status check_ptrs(std::initializer_list<const void*> ptrs, const char* what) {
   for (const void* p : ptrs) {
     if (!p) return set_error(KL_ERR_INVALID_ARG, "%s: null pointer", what);
@@ -646,4 +681,93 @@ kl_status kl_attention_bwd(int32_t B, int32_t S, int32_t Hq, int32_t Hkv, int32_
   return KL_OK;
 }
 
+size_t kl_paged_attention_ws_bytes(const kl_paged_cfg* pc, int32_t Hq, int32_t Hkv, int32_t d) {
+  if (paged_check(pc, Hq, Hkv, d, KL_BF16) != KL_OK) return 0;
+  return paged_attention_ws(*pc, Hq, Hkv);
+}
+
+kl_status kl_paged_kv_write(const kl_paged_cfg* pc, int32_t Hkv, int32_t d, int32_t dtype, const void* k_new,
+                            const void* v_new, const int32_t* table, const int32_t* ctx, void* k_pool, void* v_pool,
+                            void* stream) {
+  KL_TRY(paged_check(pc, Hkv, Hkv, d, dtype));
+  return paged_kv_write(*pc, Hkv, k_new, v_new, table, ctx, k_pool, v_pool, static_cast<cudaStream_t>(stream));
+}
+
+kl_status kl_paged_attention(const kl_paged_cfg* pc, int32_t Hq, int32_t Hkv, int32_t d, int32_t dtype,
+                             const void* q, const void* k_pool, const void* v_pool, const int32_t* table,
+                             const int32_t* ctx, void* o, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  KL_TRY(paged_check(pc, Hq, Hkv, d, dtype));
+  return paged_attention(*pc, Hq, Hkv, q, k_pool, v_pool, table, ctx, o, lse, ws, ws_bytes,
+                         static_cast<cudaStream_t>(stream));
+}
+
+size_t kl_layer_forward_paged_ws_bytes(const kl_layer_cfg* cfg, const kl_paged_cfg* pc) {
+  Dims D;
+  if (check_cfg(cfg, &D) != KL_OK || paged_check(pc, D.Hq, D.Hkv, D.d, D.dt) != KL_OK) return 0;
+  if (cfg->B != pc->B || cfg->S != pc->n_new) return 0;
+  Carver c(nullptr);
+  PagedWs w;
+  carve_paged(D, *pc, c, &w);
+  return c.off;
+}
+
+kl_status kl_layer_forward_paged(const kl_layer_cfg* cfg, const kl_paged_cfg* pc, const kl_layer_weights* w,
+                                 const void* X, void* Y, void* k_pool, void* v_pool, const int32_t* table,
+                                 const int32_t* ctx, void* ws, size_t ws_bytes, void* stream) {
+  Dims D;
+  KL_TRY(check_cfg(cfg, &D));
+  KL_TRY(paged_check(pc, D.Hq, D.Hkv, D.d, D.dt));
+  if (cfg->B != pc->B || cfg->S != pc->n_new)
+    return set_error(KL_ERR_INVALID_ARG, "layer_forward_paged: cfg B, S must be the step's B, n_new");
+  if (!w) return set_error(KL_ERR_INVALID_ARG, "layer_forward_paged: null weights");
+  KL_TRY(check_ptrs({w->gamma1, w->wq, w->wk, w->wv, w->wo, w->gamma2, w->wg, w->wu, w->wd},
+                    "layer_forward_paged weights"));
+  if (D.qk_norm) KL_TRY(check_ptrs({w->gamma_q, w->gamma_k}, "layer_forward_paged q/k norm gains"));
+  KL_TRY(check_ptrs({X, Y, k_pool, v_pool, table, ctx}, "layer_forward_paged buffers"));
+  const size_t need = kl_layer_forward_paged_ws_bytes(cfg, pc);
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u))
+    return set_error(KL_ERR_NO_MEMORY, "layer_forward_paged: workspace too small or not 256-byte aligned");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Carver c(ws);
+  PagedWs b;
+  carve_paged(D, *pc, c, &b);
+  const int T = D.T, H = D.H, I = D.I, dt = D.dt;
+  KL_TRY(rmsnorm_fwd(T, H, dt, X, w->gamma1, cfg->eps, b.h1, b.rstd1, st));
+  {
+    GemmSpec g[3] = {proj(T, D.Dq, H, b.h1, H, w->wq, H, b.q_pre, D.Dq, dt),
+                     proj(T, D.Dkv, H, b.h1, H, w->wk, H, b.k_pre, D.Dkv, dt),
+                     proj(T, D.Dkv, H, b.h1, H, w->wv, H, b.v, D.Dkv, dt)};
+    with_tail(g, 3, b.tail, b.tail_bytes);
+    KL_TRY(run_gemms(dt, g, 3, st, "gemm.paged_qkv"));
+  }
+  // optional per-head norm, then the rotation at the tokens' absolute positions ctx[b] + i
+  KL_TRY(qk_rope_fwd(T, D.Hq, D.S, D.d, dt, b.q_pre, w->gamma_q, cfg->eps, D.qk_norm, D.inter, cfg->rope_base,
+                     nullptr, b.q, b.rstd_q, st, ctx));
+  KL_TRY(qk_rope_fwd(T, D.Hkv, D.S, D.d, dt, b.k_pre, w->gamma_k, cfg->eps, D.qk_norm, D.inter, cfg->rope_base,
+                     nullptr, b.k, b.rstd_k, st, ctx));
+  KL_TRY(paged_kv_write(*pc, D.Hkv, b.k, b.v, table, ctx, k_pool, v_pool, st));
+  KL_TRY(paged_attention(*pc, D.Hq, D.Hkv, b.q, k_pool, v_pool, table, ctx, b.o, nullptr, b.att, b.att_bytes, st));
+  {
+    GemmSpec g = proj(T, H, D.Dq, b.o, D.Dq, w->wo, D.Dq, b.x2, H, dt, X, dt);
+    with_tail(&g, 1, b.tail, b.tail_bytes);
+    KL_TRY(run_gemms(dt, &g, 1, st, "gemm.paged_o"));
+  }
+  KL_TRY(rmsnorm_fwd(T, H, dt, b.x2, w->gamma2, cfg->eps, b.h2, b.rstd2, st));
+  {
+    GemmSpec g = proj(T, I, H, b.h2, H, w->wg, H, b.g, I, dt);
+    g.epi = GEMM_EPI_SWIGLU;
+    g.B2 = w->wu;
+    g.C2 = b.u;
+    g.C3 = b.m;
+    KL_TRY(run_gemms(dt, &g, 1, st, "gemm.paged_gateup"));
+  }
+  {
+    GemmSpec g = proj(T, H, I, b.m, I, w->wd, I, Y, H, dt, b.x2, dt);
+    with_tail(&g, 1, b.tail, b.tail_bytes);
+    KL_TRY(run_gemms(dt, &g, 1, st, "gemm.paged_down"));
+  }
+  return KL_OK;
+}
+
 }  // extern "C"
+

@@ -663,12 +663,16 @@ template <typename T>
 __global__ void __launch_bounds__(256) qk_rope_fwd_kernel(int rows, int heads, int S, int d, const T* pre,
                                                           const T* __restrict__ gamma, float eps, int norm, int inter,
                                                           RopeFreq f, const float2* __restrict__ tab,
-                                                          T* out, float* __restrict__ rstd) {
+                                                          T* out, float* __restrict__ rstd,
+                                                          const int32_t* __restrict__ pos_off) {
   pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int row = blockIdx.x * 8 + warp;
   if (row >= rows) return;
-  const int pos = (row / heads) % S, half = d / 2;
+  // position of the row's token: its index in the sequence, plus the sequence's
+  // offset when the tokens continue a cached prefix
+  const int tok = row / heads;
+  const int pos = tok % S + (pos_off ? pos_off[tok / S] : 0), half = d / 2;
   const T* x = pre + static_cast<int64_t>(row) * d;
   T* y = out + static_cast<int64_t>(row) * d;
   float r = 1.0f;
@@ -1037,8 +1041,10 @@ int qk_bwd_grid(int rows) {
 size_t qk_rope_bwd_ws(int rows, int d) { return align_up(static_cast<size_t>(qk_bwd_grid(rows)) * d * 4, 256); }
 
 kl_status qk_rope_fwd(int T, int heads, int S, int d, int dtype, const void* pre, const void* gamma, float eps,
-                      int norm, int inter, float base, const float2* tab, void* out, float* rstd, cudaStream_t st) {
-  if (T < 1 || heads < 1 || d < 2 || (d & 1) || d / 2 > ROPE_MAX_HALF || !pre || !out || (norm && (!gamma || !rstd)))
+                      int norm, int inter, float base, const float2* tab, void* out, float* rstd, cudaStream_t st,
+                      const int32_t* pos_off) {
+  if (T < 1 || heads < 1 || d < 2 || (d & 1) || d / 2 > ROPE_MAX_HALF || !pre || !out || (norm && (!gamma || !rstd)) ||
+      (pos_off && tab))
     return set_error(KL_ERR_INVALID_ARG, "q/k rotary: bad arguments");
   const int rows = T * heads;
   const RopeFreq f = rope_freq(d, base);
@@ -1047,10 +1053,10 @@ kl_status qk_rope_fwd(int T, int heads, int S, int d, int dtype, const void* pre
   if (dtype == KL_BF16)
     launch_pdl(qk_rope_fwd_kernel<__nv_bfloat16>, grid, 256, 0, st, rows, heads, S, d, (const __nv_bfloat16*)pre,
                                                            (const __nv_bfloat16*)gamma, eps, norm, inter, f, tab,
-                                                           (__nv_bfloat16*)out, rstd);
+                                                           (__nv_bfloat16*)out, rstd, pos_off);
   else
     launch_pdl(qk_rope_fwd_kernel<float>, grid, 256, 0, st, rows, heads, S, d, (const float*)pre, (const float*)gamma, eps,
-                                                   norm, inter, f, tab, (float*)out, rstd);
+                                                   norm, inter, f, tab, (float*)out, rstd, pos_off);
   KL_CUDA(cudaGetLastError());
   return KL_OK;
 }

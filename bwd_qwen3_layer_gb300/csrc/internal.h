@@ -98,7 +98,8 @@ kl_status rope(int B, int S, int heads, int d, float base, int dtype, void* x, i
 // RMSNorm over each row (gain gamma[d], rstd[row] saved) -> rotary turn, planes
 // (i, i+d/2) or interleaved (2i, 2i+1); cos/sin from tab ([S][d/2]) or formed.
 kl_status qk_rope_fwd(int T, int heads, int S, int d, int dtype, const void* pre, const void* gamma, float eps,
-                      int norm, int inter, float base, const float2* tab, void* out, float* rstd, cudaStream_t st);
+                      int norm, int inter, float base, const float2* tab, void* out, float* rstd, cudaStream_t st,
+                      const int32_t* pos_off = nullptr);
 // Its backward: dyr (gradient after the rotation, dy_dtype) -> dx (dtype);
 // with the norm also dgamma (fp32 [d], overwritten). Workspace: qk_rope_bwd_ws.
 size_t qk_rope_bwd_ws(int rows, int d);
@@ -116,6 +117,15 @@ kl_status rope_bwd_convert(int B, int S, int hq, int hk, int d, float base, int 
                            const float* dq_acc, const float* dk_acc, const float* dv_acc, void* dq,
                            void* dk, void* dv, cudaStream_t st);
 kl_status convert_f32(int64_t n, int dtype, const float* src, void* dst, cudaStream_t st);
+
+// paged.cu: the forward path with a paged key/value cache (bf16, d = 128)
+kl_status paged_check(const kl_paged_cfg* pc, int Hq, int Hkv, int d, int dtype);
+size_t paged_attention_ws(const kl_paged_cfg& pc, int Hq, int Hkv);
+kl_status paged_kv_write(const kl_paged_cfg& pc, int Hkv, const void* k_new, const void* v_new, const int32_t* table,
+                         const int32_t* ctx, void* kp, void* vp, cudaStream_t st);
+kl_status paged_attention(const kl_paged_cfg& pc, int Hq, int Hkv, const void* q, const void* kp, const void* vp,
+                          const int32_t* table, const int32_t* ctx, void* o, float* lse, void* ws, size_t ws_bytes,
+                          cudaStream_t st);
 kl_status swiglu_fwd(int64_t n, int dtype, const void* g, const void* u, void* m, cudaStream_t st);
 kl_status swiglu_bwd(int64_t n, int dtype, const void* dm, const void* g, const void* u, void* dg,
                      void* du, cudaStream_t st);

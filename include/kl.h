@@ -77,6 +77,9 @@ typedef enum kl_dtype { KL_F32 = 0, KL_BF16 = 1 } kl_dtype;
 #define KL_DEVERR_TARGET 0x2u       /* a CE target id was outside [0, V) */
 #define KL_DEVERR_SMEM 0x4u         /* a kernel found its shared memory misaligned
                                        and returned without doing its work */
+#define KL_DEVERR_PAGE 0x8u         /* a paged-cache position past its block-table row,
+                                       or a table entry outside the pool (the access
+                                       was skipped)                                   */
 
 KL_API const char* kl_version(void);
 KL_API const char* kl_status_str(kl_status s);
@@ -367,6 +370,63 @@ KL_API kl_status kl_stream_forward(kl_stream* s, const void* X, void* Y, void* s
  * the retained gradient buffers once a run delivered to host memory). */
 KL_API size_t kl_stream_device_bytes(const kl_stream* s);
 KL_API void kl_stream_destroy(kl_stream* s);
+
+/* ------------------------------------------------------------------------ */
+/* Forward with a paged key/value cache ("From-scratch GPU LLM training",    */
+/* "What is built": a GPU forward path with a paged key-value cache;         */
+/* "KYNETRA FOUNDRY", paged-KV paragraph: fixed-size token blocks anywhere   */
+/* in a global pool, a per-sequence block table mapping logical positions to */
+/* physical blocks, keys and values gathered through it)                     */
+/* ------------------------------------------------------------------------ */
+
+/* A step feeds n_new new tokens to each of B sequences (n_new = 1: decode).
+ * Sequence b already holds ctx[b] tokens in the cache, so its new token i
+ * sits at absolute position ctx[b] + i: the rotary angle and the causal
+ * limit use that position. A pool (one for keys, one for values, per layer)
+ * is [n_blocks][block_size][Hkv * d] in the layer dtype; position p of
+ * sequence b lives in block table[b * max_blocks + p / block_size], slot
+ * p % block_size. The caller owns pools and tables and assigns the blocks.
+ * This path is bf16 with head dim 128 and at most 64 query rows per kv head
+ * and step ((Hq / Hkv) * n_new <= 64). A position past its table row or a
+ * table entry outside [0, n_blocks) is skipped and reported by
+ * kl_device_status (KL_DEVERR_PAGE). */
+typedef struct kl_paged_cfg {
+  int32_t B;           /* sequences in the step                              */
+  int32_t n_new;       /* new tokens per sequence                            */
+  int32_t block_size;  /* tokens per cache block                             */
+  int32_t max_blocks;  /* length of each block-table row                     */
+  int32_t n_blocks;    /* blocks in each pool                                */
+} kl_paged_cfg;
+
+/* The new tokens' keys and values (k_new, v_new [B*n_new, Hkv*d] device,
+ * rows b * n_new + i) into their cache slots. table [B*max_blocks] and ctx
+ * [B] are device int32. */
+KL_API kl_status kl_paged_kv_write(const kl_paged_cfg* pc, int32_t Hkv, int32_t d, int32_t dtype,
+                                   const void* k_new, const void* v_new, const int32_t* table,
+                                   const int32_t* ctx, void* k_pool, void* v_pool, void* stream);
+/* Workspace for kl_paged_attention (0 when the step needs no context split). */
+KL_API size_t kl_paged_attention_ws_bytes(const kl_paged_cfg* pc, int32_t Hq, int32_t Hkv, int32_t d);
+/* Causal GQA attention of the new queries q [B*n_new, Hq*d] (after the
+ * rotation) over each sequence's cache, positions 0 .. ctx[b] + n_new - 1:
+ * the new tokens' keys and values must already be written. Query i of
+ * sequence b sees keys at positions <= ctx[b] + i; scale 1/sqrt(d); query
+ * head h reads kv head floor(h * Hkv / Hq). o [B*n_new, Hq*d] device; lse
+ * [B, Hq, n_new] fp32 device (natural log) or NULL. */
+KL_API kl_status kl_paged_attention(const kl_paged_cfg* pc, int32_t Hq, int32_t Hkv, int32_t d, int32_t dtype,
+                                    const void* q, const void* k_pool, const void* v_pool,
+                                    const int32_t* table, const int32_t* ctx, void* o, float* lse,
+                                    void* ws, size_t ws_bytes, void* stream);
+/* Workspace for kl_layer_forward_paged. */
+KL_API size_t kl_layer_forward_paged_ws_bytes(const kl_layer_cfg* cfg, const kl_paged_cfg* pc);
+/* The layer forward of kl_layer_forward for the step's new tokens against a
+ * paged cache: X, Y [B*n_new, H] device with cfg->B == pc->B and cfg->S ==
+ * pc->n_new (so T = B*S rows, as everywhere); q and k are rotated at their
+ * absolute positions, the new keys and values are written into the layer's
+ * pools, then attention reads the cache. Nothing is saved for a backward. */
+KL_API kl_status kl_layer_forward_paged(const kl_layer_cfg* cfg, const kl_paged_cfg* pc,
+                                        const kl_layer_weights* w, const void* X, void* Y, void* k_pool,
+                                        void* v_pool, const int32_t* table, const int32_t* ctx, void* ws,
+                                        size_t ws_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -126,3 +126,19 @@ def test_stream_host_checks(lib):
     no_layers = K.StreamCfg(layer, 0, 0, K.KL_STREAM_FORWARD)
     assert lib.kl_stream_create(ctypes.byref(no_layers), w, None, ctypes.byref(out)) == K.KL_ERR_INVALID_ARG
     assert lib.kl_stream_forward(None, 0x1000, 0x1000, None) == K.KL_ERR_INVALID_ARG
+
+
+def test_paged_host_checks(lib):
+    pc = K.PagedCfg(4, 1, 16, 8, 64)
+    assert K.kl_paged_attention_ws_bytes(pc, 64, 8, 128) >= 0
+    assert K.kl_paged_attention_ws_bytes(pc, 64, 8, 64) == 0            # head dim 128 only
+    assert K.kl_paged_attention_ws_bytes(K.PagedCfg(4, 9, 16, 8, 64), 64, 8, 128) == 0   # 8 x 9 > 64 rows
+    assert K.kl_paged_attention_ws_bytes(K.PagedCfg(0, 1, 16, 8, 64), 64, 8, 128) == 0
+    # null pointers are refused before any CUDA call
+    assert lib.kl_paged_attention(ctypes.byref(pc), 64, 8, 128, K.KL_BF16, None, None, None, None, None, None,
+                                  None, None, 0, None) == K.KL_ERR_INVALID_ARG
+    assert lib.kl_paged_kv_write(ctypes.byref(pc), 8, 128, K.KL_F32, None, None, None, None, None, None,
+                                 None) == K.KL_ERR_UNSUPPORTED
+    layer = _cfg(B=4, S=1)
+    assert K.kl_layer_forward_paged_ws_bytes(layer, pc) > 0
+    assert K.kl_layer_forward_paged_ws_bytes(_cfg(B=4, S=2), pc) == 0    # S must be the step's n_new
