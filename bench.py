@@ -1,7 +1,7 @@
 """Benchmark of the GB300 Qwen3 layer path. Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload layer|attention|lmhead|stream|stream_recompute|stream_fwd64]
+                  [--workload layer|attention|lmhead|stream|stream_recompute|stream_fwd64|decode]
 
 Workloads (Qwen3-32B dims: hidden 5120, 64 query / 8 KV heads of dim 128,
 SwiGLU intermediate 25600, RoPE base 1e6, causal; bf16):
@@ -20,6 +20,11 @@ SwiGLU intermediate 25600, RoPE base 1e6, causal; bf16):
              64 layers forward only (kl_stream_forward), batch 1 x seq 2048,
              weights streamed from pinned host memory; reports the driver's
              device memory (independent of depth)
+  decode     one layer's forward for one new token of each of 64 sequences
+             whose keys and values (context 4096) sit in a paged cache
+             (kl_layer_forward_paged, block size 16, blocks shuffled over
+             the pool); bound by HBM: the layer's weights and the context's
+             keys and values are read once per step
 The stream workloads also time the same call with every layer's weights
 already in device memory ("bulk": no uploads) to show how much of the host
 link the compute hides.
@@ -57,6 +62,7 @@ WORKLOADS = {
     "stream_recompute": dict(B=2, S=4096, L=8, V=151936, clip=1.0, mode=1,
                              desc="stream_8_layers_T8192_ce_clip_recompute"),
     "stream_fwd64": dict(B=1, S=2048, L=64, distinct=4, mode=2, desc="stream_forward_64_layers_T2048"),
+    "decode": dict(B=64, ctx=4096, block=16, desc="decode_layer_B64_ctx4096_paged"),
 }
 METRICS = {
     "layer": METRIC,
@@ -66,6 +72,7 @@ METRICS = {
     "stream_recompute": "8-layer streamed training step with activation recompute tokens/s (batch 2 x 4096, bf16, "
                         "1 GB300)",
     "stream_fwd64": "64-layer streamed forward tokens/s (batch 1 x 2048, bf16, 1 GB300)",
+    "decode": "one-layer decode tokens/s, paged KV cache (64 sequences x context 4096, Qwen3-32B dims, bf16, 1 GB300)",
 }
 
 
@@ -385,10 +392,58 @@ def setup_stream(torch, K, L, synth, device, seed, name="stream"):
     return T, (lambda: run(h, X, tgt)), e2e, X.numel() * 2, Y.numel() * 2, cfgd, keep
 
 
+def setup_decode(torch, K, L, synth, device, seed):
+    wl = WORKLOADS["decode"]
+    B, ctx, bs = wl["B"], wl["ctx"], wl["block"]
+    H = QWEN["H"]
+    cfg = L.make_cfg(B, 1, **QWEN, dtype=K.KL_BF16)
+    w = {}
+    for n, shp in L.weight_shapes(cfg).items():
+        w[n] = synth.device_normal(shp, 0.02, 1.0 if n.startswith("gamma") else 0.0, seed, f"dec.{n}", torch.bfloat16,
+                                   device)
+    max_blocks = (ctx + 1 + bs - 1) // bs
+    n_blocks = B * max_blocks
+    kv_w = QWEN["Hkv"] * QWEN["d"]
+    kp = synth.device_normal((n_blocks, bs, kv_w), 1.0, 0.0, seed, "dec.kpool", torch.bfloat16, device)
+    vp = synth.device_normal((n_blocks, bs, kv_w), 1.0, 0.0, seed, "dec.vpool", torch.bfloat16, device)
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    table = torch.randperm(n_blocks, generator=gen).to(torch.int32).reshape(B, max_blocks).to(device)
+    ctx_t = torch.full((B,), ctx, dtype=torch.int32, device=device)
+    X = synth.device_normal((B, H), 1.0, 0.0, seed, "dec.X", torch.bfloat16, device)
+    Y = torch.empty_like(X)
+    pc = K.PagedCfg(B, 1, bs, max_blocks, n_blocks)
+    ws = torch.empty(K.kl_layer_forward_paged_ws_bytes(cfg, pc), dtype=torch.uint8, device=device)
+    wst = L.weights_struct(w)
+    stream = torch.cuda.current_stream(device)
+
+    def run(x, y):
+        K.kl_layer_forward_paged(cfg, pc, wst, x.data_ptr(), y.data_ptr(), kp.data_ptr(), vp.data_ptr(),
+                                 table.data_ptr(), ctx_t.data_ptr(), ws.data_ptr(), ws.numel(), stream)
+
+    hX = X.cpu().pin_memory()
+    hY = torch.empty_like(hX).pin_memory()
+    X2, Y2 = torch.empty_like(X), torch.empty_like(X)
+
+    def e2e():
+        X2.copy_(hX, non_blocking=True)
+        run(X2, Y2)
+        hY.copy_(Y2, non_blocking=True)
+
+    weight_bytes = sum(t.numel() * t.element_size() for t in w.values())
+    kv_bytes = 2 * B * (ctx + 1) * kv_w * 2
+    keep = (w, kp, vp, table, ctx_t, X, Y, ws, hX, hY, X2, Y2)
+    cfgd = {"workload": wl["desc"], "sequences": B, "context": ctx, "new_tokens_per_sequence": 1,
+            "block_size": bs, "hidden": H, "heads_q": QWEN["Hq"], "heads_kv": QWEN["Hkv"], "head_dim": QWEN["d"],
+            "intermediate": QWEN["I"], "l2": "inputs larger than L2 (975 MB weights + 1.07 GB cache per step)",
+            "hbm_bytes_per_step": weight_bytes + kv_bytes + 4 * B * H * 2, "roofline_bytes": True}
+    return B, (lambda: run(X, Y)), e2e, X.numel() * 2, Y.numel() * 2, cfgd, keep
+
+
 SETUP = {"layer": setup_layer, "attention": setup_attention, "lmhead": setup_lmhead,
          "stream": lambda *a, **k: setup_stream(*a, **k, name="stream"),
          "stream_recompute": lambda *a, **k: setup_stream(*a, **k, name="stream_recompute"),
-         "stream_fwd64": lambda *a, **k: setup_stream(*a, **k, name="stream_fwd64")}
+         "stream_fwd64": lambda *a, **k: setup_stream(*a, **k, name="stream_fwd64"),
+         "decode": setup_decode}
 
 
 def bench_ours(args, rank, world, local_rank, dist):
@@ -523,6 +578,21 @@ def oracle_sample(workload: str, steps: int):
             O.lmhead_ce(X, W, t)
         units = N
         desc = f"lm-head CE+argmax fwd+bwd on {N} tokens, hidden 5120, vocab {V}"
+    elif workload == "decode":
+        Bs, ctx, bs = 8, WORKLOADS["decode"]["ctx"], WORKLOADS["decode"]["block"]
+        cfg = O.LayerConfig(B=Bs, S=1, H=Q["H"], Hq=Q["Hq"], Hkv=Q["Hkv"], d=Q["d"], I=Q["I"])
+        w = _oracle_weights(rng, Q["H"], Q["Hq"], Q["Hkv"], Q["d"], Q["I"])
+        maxb = (ctx + 1 + bs - 1) // bs
+        table = rng.permutation(Bs * maxb).reshape(Bs, maxb)
+        kp = rng.standard_normal((Bs * maxb, bs, Q["Hkv"], Q["d"]))
+        vp = rng.standard_normal((Bs * maxb, bs, Q["Hkv"], Q["d"]))
+        X = rng.standard_normal((Bs, Q["H"]))
+        ctxa = np.full(Bs, ctx)
+
+        def one():
+            O.layer_forward_paged(cfg, w, X, kp, vp, table, ctxa, 1)
+        units = Bs
+        desc = f"one full-dims layer's paged decode step for {Bs} sequences at context {ctx}"
     elif workload == "stream_fwd64":   # one layer forward on a token sample, scaled to 64 layers
         S = 512
         cfg = O.LayerConfig(B=1, S=S, H=Q["H"], Hq=Q["Hq"], Hkv=Q["Hkv"], d=Q["d"], I=Q["I"])
@@ -642,7 +712,16 @@ def main():
     per = d["ms"] / d["launches"] / 1e3
     trec = traffic_record()
     traffic = trec["bytes_per_launch"].get(dname) if trec and args.workload in trec.get("workloads", []) else None
-    if d["flops"] > 0:
+    if r["config"].get("roofline_bytes"):
+        # bandwidth-bound workload: the dominant kernel group against HBM, plus the whole step
+        ach = d["bytes"] / d["launches"] / per / 1e9
+        step_gbs = r["config"]["hbm_bytes_per_step"] / (r["ms"] / args.steps / 1e3) / 1e9
+        roof = {"kernel": dname, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4), "traffic": traffic,
+                "peak_src": f"{pk['src']} hbm_gbs",
+                "step": {"bytes": r["config"]["hbm_bytes_per_step"], "achieved": round(step_gbs, 1),
+                         "frac": round(step_gbs / pk["hbm_gbs"], 4)}}
+    elif d["flops"] > 0:
         ach = d["flops"] / d["launches"] / per / 1e12
         roof = {"kernel": dname, "bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops_sustained"],
                 "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops_sustained"], 4), "traffic": traffic,

@@ -1250,10 +1250,11 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   const int cap = max_gemm_clusters(dev, cfg);
-  // Last round: if the units leave some CTA pairs idle in the last round, split
-  // the last problem's last tiles along K so that the round's work spreads
-  // over every pair (each K range stored to its own slice of tail_ws, the
-  // slices summed in split order below).
+  // Last round: if the units leave some CTA pairs idle in the last round (or
+  // in the only one: a skinny problem such as a decode step's projections),
+  // split the last problem's last tiles along K so that the round's work
+  // spreads over every pair (each K range stored to its own slice of tail_ws,
+  // the slices summed in split order below).
   int tail_prob = -1;
   {
     const int lp = nspec - 1;
@@ -1261,7 +1262,7 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
     const GemmSpec& s = specs_in[order[lp]];
     const int tiles = pr.m_tiles * pr.n_tiles;
     const int rem = units % cap;
-    if (units > cap && rem > 0 && s.tail_ws && pr.splits == 1 && pr.epi == GEMM_EPI_STORE && rem <= tiles &&
+    if (rem > 0 && s.tail_ws && pr.splits == 1 && pr.epi == GEMM_EPI_STORE && rem <= tiles &&
         pr.n_step == 256 && (reinterpret_cast<uintptr_t>(s.tail_ws) & 15u) == 0) {
       int ts = cap / rem;
       const int max_ts = pr.kb_total / 8;            // at least 8 k-blocks per piece

@@ -19,6 +19,8 @@ Cases (T = 2048 tokens, hidden 5120, 64/8 heads of 128, intermediate 25600):
   swiglu_bwd    dg, du over 2048 x 25600
   layer         one whole layer forward + backward (for the layer-internal
                 kernels; ~4 GB on the device)
+  paged_attn    decode attention over a paged cache: 64 sequences x context
+                4096, one new token each, block size 16 (~1.1 GB of cache)
 """
 from __future__ import annotations
 
@@ -126,6 +128,23 @@ def main():
                 K.kl_swiglu_fwd(T * I, bf, g.data_ptr(), u.data_ptr(), m.data_ptr())
             else:
                 K.kl_swiglu_bwd(T * I, bf, dm.data_ptr(), g.data_ptr(), u.data_ptr(), dg.data_ptr(), du.data_ptr())
+    elif a.case == "paged_attn":
+        B, ctx, bs = 64, 4096, 16
+        max_blocks = (ctx + 1 + bs - 1) // bs
+        n_blocks = B * max_blocks
+        kp = _rand((n_blocks, bs, HKV * D))
+        vp = _rand((n_blocks, bs, HKV * D))
+        table = torch.randperm(n_blocks, device="cuda").to(torch.int32).reshape(B, max_blocks)
+        ctx_t = torch.full((B,), ctx, dtype=torch.int32, device="cuda")
+        q = _rand((B, HQ * D))
+        o = torch.empty_like(q)
+        pc = K.PagedCfg(B, 1, bs, max_blocks, n_blocks)
+        nb = K.kl_paged_attention_ws_bytes(pc, HQ, HKV, D)
+        ws = torch.empty(max(nb, 256), dtype=torch.uint8, device="cuda")
+
+        def run():
+            K.kl_paged_attention(pc, HQ, HKV, D, bf, q.data_ptr(), kp.data_ptr(), vp.data_ptr(), table.data_ptr(),
+                                 ctx_t.data_ptr(), o.data_ptr(), 0, ws.data_ptr(), nb)
     elif a.case == "layer":
         from . import layer as L
         cfg = L.make_cfg(1, T, H, HQ, HKV, D, I, dtype=bf)

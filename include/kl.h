@@ -389,7 +389,8 @@ KL_API void kl_stream_destroy(kl_stream* s);
  * This path is bf16 with head dim 128 and at most 64 query rows per kv head
  * and step ((Hq / Hkv) * n_new <= 64). A position past its table row or a
  * table entry outside [0, n_blocks) is skipped and reported by
- * kl_device_status (KL_DEVERR_PAGE). */
+ * kl_device_status (KL_DEVERR_PAGE). Pool rows (n_blocks * block_size * Hkv)
+ * must stay below 2^31. */
 typedef struct kl_paged_cfg {
   int32_t B;           /* sequences in the step                              */
   int32_t n_new;       /* new tokens per sequence                            */
@@ -404,7 +405,9 @@ typedef struct kl_paged_cfg {
 KL_API kl_status kl_paged_kv_write(const kl_paged_cfg* pc, int32_t Hkv, int32_t d, int32_t dtype,
                                    const void* k_new, const void* v_new, const int32_t* table,
                                    const int32_t* ctx, void* k_pool, void* v_pool, void* stream);
-/* Workspace for kl_paged_attention (0 when the step needs no context split). */
+/* Workspace for kl_paged_attention: the partial results of (sequence, kv
+ * head) items whose keys are shared out between several CTAs; 0 when none is.
+ * It depends on the device's SM count. */
 KL_API size_t kl_paged_attention_ws_bytes(const kl_paged_cfg* pc, int32_t Hq, int32_t Hkv, int32_t d);
 /* Causal GQA attention of the new queries q [B*n_new, Hq*d] (after the
  * rotation) over each sequence's cache, positions 0 .. ctx[b] + n_new - 1:

@@ -46,6 +46,10 @@ def _case(seed, B, n_new, Hq, Hkv, bs, ctx, extra_blocks=3):
     (64, 1, 8, 1, 16, [40] * 64),            # many sequences: no context split
     (1, 1, 64, 8, 32, [2000]),               # one long sequence: context split + combine
     (2, 2, 4, 2, 8, [0, 1]),                 # tiny contexts
+    (2, 8, 8, 1, 16, [100, 3]),              # 64 rows per kv head: four row groups
+    (6, 1, 16, 2, 16, [0, 1, 63, 64, 65, 1000]),   # ragged around the 64-key tile edge
+    (40, 1, 64, 8, 16, [700] * 40),          # runs of several tiles cut items into pieces
+    (3, 3, 12, 4, 5, [7, 0, 190]),           # block size 5, three new tokens, 9 rows
 ])
 def test_paged_attention_matches_oracle(kl, B, n_new, Hq, Hkv, bs, ctx):
     table, kp, vp, q, max_blocks, n_blocks = _case(11, B, n_new, Hq, Hkv, bs, ctx)
