@@ -96,6 +96,9 @@ _SIGNATURES = {
     "kl_ce_argmax_noalloc": (ctypes.c_int, [_i32, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _vp]),
     "kl_gemm": (ctypes.c_int, [_i32, _i32, _i32, _i32, _vp, _i64, _i32, _vp, _i64, _i32, _vp, _i64, _i32,
                                _vp, _i64, _i32, _vp]),
+    "kl_gemm_scratch_bytes": (_sz, []),
+    "kl_gemm_ex": (ctypes.c_int, [_i32, _i32, _i32, _i32, _vp, _i64, _i32, _vp, _i64, _i32, _vp, _i64, _i32,
+                                  _vp, _i64, _i32, _vp, _sz, _vp]),
     "kl_rmsnorm_fwd": (ctypes.c_int, [_i32, _i32, _i32, _vp, _vp, _f32, _vp, _vp, _vp]),
     "kl_rmsnorm_bwd_ws_bytes": (_sz, [_i32, _i32]),
     "kl_rmsnorm_bwd": (ctypes.c_int, [_i32, _i32, _i32, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -242,6 +245,17 @@ def kl_gemm(M, N, K, dtype, A, lda, a_mn, B, ldb, b_mn, C, ldc, c_dtype, R=0, ld
             stream=None) -> None:
     check(load().kl_gemm(M, N, K, dtype, A, lda, a_mn, B, ldb, b_mn, C, ldc, c_dtype, R, ldr, r_dtype,
                          _stream(stream)))
+
+
+def kl_gemm_scratch_bytes() -> int:
+    return load().kl_gemm_scratch_bytes()
+
+
+def kl_gemm_ex(M, N, K, dtype, A, lda, a_mn, B, ldb, b_mn, C, ldc, c_dtype, R=0, ldr=0, r_dtype=KL_BF16,
+               ws=0, ws_bytes=0, stream=None) -> None:
+    """kl_gemm with a device scratch (last-round K split, few-rows kernel)."""
+    check(load().kl_gemm_ex(M, N, K, dtype, A, lda, a_mn, B, ldb, b_mn, C, ldc, c_dtype, R, ldr, r_dtype, ws,
+                            ws_bytes, _stream(stream)))
 
 
 def kl_rmsnorm_fwd(rows, width, dtype, x, gamma, eps, h, rstd, stream=None) -> None:

@@ -406,6 +406,7 @@ kl_status kl_layer_forward(const kl_layer_cfg* cfg, const kl_layer_weights* w, c
     g.B2 = w->wu;
     g.C2 = s->u;
     g.C3 = s->m;
+    if (fused) with_tail(&g, 1, ws, tail_bytes);   // scratch of the few-rows kernel
     KL_TRY(run_gemms(dt, &g, 1, st, "gemm.fwd_gateup"));
   } else {
     GemmSpec g[2] = {proj(T, I, H, s->h2, H, w->wg, H, s->g, I, dt),
@@ -606,6 +607,16 @@ kl_status kl_gemm(int32_t M, int32_t N, int32_t K, int32_t dtype, const void* A,
                   int32_t a_mn_major, const void* B, int64_t ldb, int32_t b_mn_major, void* C,
                   int64_t ldc, int32_t c_dtype, const void* R, int64_t ldr, int32_t r_dtype,
                   void* stream) {
+  return kl_gemm_ex(M, N, K, dtype, A, lda, a_mn_major, B, ldb, b_mn_major, C, ldc, c_dtype, R, ldr, r_dtype,
+                    nullptr, 0, stream);
+}
+
+size_t kl_gemm_scratch_bytes(void) { return gemm_tail_ws_bytes(); }
+
+kl_status kl_gemm_ex(int32_t M, int32_t N, int32_t K, int32_t dtype, const void* A, int64_t lda,
+                     int32_t a_mn_major, const void* B, int64_t ldb, int32_t b_mn_major, void* C,
+                     int64_t ldc, int32_t c_dtype, const void* R, int64_t ldr, int32_t r_dtype, void* ws,
+                     size_t ws_bytes, void* stream) {
   if (M < 1 || N < 1 || K < 1 || !A || !B || !C) return set_error(KL_ERR_INVALID_ARG, "gemm: bad arguments");
   if ((dtype != KL_F32 && dtype != KL_BF16) || (c_dtype != KL_F32 && c_dtype != KL_BF16) ||
       (R && r_dtype != KL_F32 && r_dtype != KL_BF16))
@@ -619,6 +630,7 @@ kl_status kl_gemm(int32_t M, int32_t N, int32_t K, int32_t dtype, const void* A,
   s.a_mn = a_mn_major ? 1 : 0; s.b_mn = b_mn_major ? 1 : 0;
   s.C = C; s.ldc = ldc; s.c_dtype = c_dtype;
   s.R = R; s.ldr = ldr; s.r_dtype = r_dtype;
+  if (ws_bytes >= gemm_tail_ws_bytes()) with_tail(&s, 1, ws, ws_bytes);
   return run_gemms(dtype, &s, 1, static_cast<cudaStream_t>(stream), "gemm");
 }
 
@@ -759,6 +771,7 @@ kl_status kl_layer_forward_paged(const kl_layer_cfg* cfg, const kl_paged_cfg* pc
     g.B2 = w->wu;
     g.C2 = b.u;
     g.C3 = b.m;
+    with_tail(&g, 1, b.tail, b.tail_bytes);
     KL_TRY(run_gemms(dt, &g, 1, st, "gemm.paged_gateup"));
   }
   {

@@ -1088,6 +1088,7 @@ int max_gemm_clusters(int dev, const cudaLaunchConfig_t& cfg_in) {
 
 kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const char* label) {
   if (nspec < 1 || nspec > GEMM_MAX_PROB) return set_error(KL_ERR_INVALID_ARG, "gemm: %d problems", nspec);
+  if (gemm_skinny_fits(specs_in, nspec)) return gemm_skinny(specs_in, nspec, st, label);
   // Heavy units first: order the problems by k-blocks per unit, descending.
   int order[GEMM_MAX_PROB];
   int splits[GEMM_MAX_PROB];

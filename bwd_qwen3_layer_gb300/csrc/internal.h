@@ -80,6 +80,11 @@ constexpr int GEMM_EPI_ROPE = 4;
 // bf16 operands on the tcgen05 tensor cores; up to GEMM_MAX_PROB independent
 // problems share one persistent launch.
 kl_status gemm_bf16(const GemmSpec* specs, int nspec, cudaStream_t st, const char* label = "gemm");
+// Few-row GEMMs (every problem M <= 128, K-major operands, plain store or
+// SwiGLU): the weights stream once over one CTA per SM. gemm_bf16 routes here
+// when gemm_skinny_fits (it also needs the problems' tail_ws as scratch).
+bool gemm_skinny_fits(const GemmSpec* specs, int nspec);
+kl_status gemm_skinny(const GemmSpec* specs, int nspec, cudaStream_t st, const char* label);
 // fp32 operands on CUDA cores (one problem).
 kl_status gemm_f32(const GemmSpec& spec, cudaStream_t st, const char* label = "gemm_f32");
 

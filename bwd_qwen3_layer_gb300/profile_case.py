@@ -21,6 +21,9 @@ Cases (T = 2048 tokens, hidden 5120, 64/8 heads of 128, intermediate 25600):
                 kernels; ~4 GB on the device)
   paged_attn    decode attention over a paged cache: 64 sequences x context
                 4096, one new token each, block size 16 (~1.1 GB of cache)
+  down_few_rows the decode step's down projection: 64 rows x 25600 against
+                5120 x 25600 weights (262 MB) plus the residual, through
+                kl_gemm_ex with its scratch (the few-rows kernel)
 """
 from __future__ import annotations
 
@@ -145,6 +148,18 @@ def main():
         def run():
             K.kl_paged_attention(pc, HQ, HKV, D, bf, q.data_ptr(), kp.data_ptr(), vp.data_ptr(), table.data_ptr(),
                                  ctx_t.data_ptr(), o.data_ptr(), 0, ws.data_ptr(), nb)
+    elif a.case == "down_few_rows":
+        M, N, Kd = 64, H, I
+        A = _rand((M, Kd))
+        Bw = _rand((N, Kd), 0.02)
+        R = _rand((M, N))
+        C = torch.empty_like(R)
+        nb = K.kl_gemm_scratch_bytes()
+        ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+
+        def run():
+            K.kl_gemm_ex(M, N, Kd, bf, A.data_ptr(), Kd, 0, Bw.data_ptr(), Kd, 0, C.data_ptr(), N, bf, R.data_ptr(),
+                         N, bf, ws=ws.data_ptr(), ws_bytes=nb)
     elif a.case == "layer":
         from . import layer as L
         cfg = L.make_cfg(1, T, H, HQ, HKV, D, I, dtype=bf)

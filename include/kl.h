@@ -269,6 +269,20 @@ KL_API kl_status kl_gemm(int32_t M, int32_t N, int32_t K, int32_t dtype,
                   const void* B, int64_t ldb, int32_t b_mn_major,
                   void* C, int64_t ldc, int32_t c_dtype,
                   const void* R, int64_t ldr, int32_t r_dtype, void* stream);
+/* kl_gemm with an fp32 device scratch (ws, 256-byte aligned; ws_bytes of at
+ * least kl_gemm_scratch_bytes(), else it is not used). With it a KL_BF16
+ * product may (a) split its last round of tiles along K when that round would
+ * leave CTA pairs idle, and (b) when M <= 128 with both operands K-major, run
+ * on the few-rows kernel (the weights streamed once over one CTA per SM,
+ * K-range pieces summed in a fixed order). Results are deterministic either
+ * way. The scratch's content is not kept between calls. */
+KL_API size_t kl_gemm_scratch_bytes(void);
+KL_API kl_status kl_gemm_ex(int32_t M, int32_t N, int32_t K, int32_t dtype,
+                  const void* A, int64_t lda, int32_t a_mn_major,
+                  const void* B, int64_t ldb, int32_t b_mn_major,
+                  void* C, int64_t ldc, int32_t c_dtype,
+                  const void* R, int64_t ldr, int32_t r_dtype,
+                  void* ws, size_t ws_bytes, void* stream);
 
 /* h = gamma * x * rstd, rstd = 1/sqrt(mean(x^2)+eps); x,h [rows,width]. */
 KL_API kl_status kl_rmsnorm_fwd(int32_t rows, int32_t width, int32_t dtype, const void* x,

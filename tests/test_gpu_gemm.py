@@ -103,3 +103,62 @@ def test_gemm_bf16_long_k_split(kl, a_mn, b_mn, M, N, K):
         # fp32 accumulation over K terms: rounding grows like sqrt(K) * 2^-24
         tol = 2e-5 * max(1.0, (K / 8192) ** 0.5)
         assert_rel(host(C), O.linear(A, B), tol, f"split C {M}x{N}x{K}")
+
+
+# few rows (M <= 128, K-major operands) with a scratch: the weights-streaming
+# kernel, including tiles whose K range is shared out between CTAs and summed
+# from pieces (N ragged on the 128-row tiles, K ragged on the 64-wide blocks)
+FEW_ROWS = [(1, 200, 72), (5, 300, 8192), (17, 520, 264), (33, 136, 40), (64, 1344, 2560), (128, 264, 4104)]
+
+
+@pytest.mark.parametrize("M,N,K", FEW_ROWS)
+@pytest.mark.parametrize("out", ["f32", "bf16+R"])
+def test_gemm_few_rows_with_scratch(kl, M, N, K, out):
+    A, B, R = _operands(M, N, K, 5)
+    a, b = dev(A, torch.bfloat16), dev(B, torch.bfloat16)
+    nb = kl.kl_gemm_scratch_bytes()
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    ref = O.linear(A, B)
+    if out == "f32":
+        C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+        kl.kl_gemm_ex(M, N, K, kl.KL_BF16, a.data_ptr(), K, 0, b.data_ptr(), K, 0, C.data_ptr(), N, kl.KL_F32,
+                      ws=ws.data_ptr(), ws_bytes=nb)
+        tol = 1e-5
+    else:
+        r = dev(R, torch.bfloat16)
+        C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        kl.kl_gemm_ex(M, N, K, kl.KL_BF16, a.data_ptr(), K, 0, b.data_ptr(), K, 0, C.data_ptr(), N, kl.KL_BF16,
+                      r.data_ptr(), N, kl.KL_BF16, ws=ws.data_ptr(), ws_bytes=nb)
+        ref = ref + R
+        tol = 4e-3
+    torch.cuda.synchronize()
+    kl.kl_device_status()
+    assert_rel(host(C), ref, tol, f"C {M}x{N}x{K} {out}")
+    # the pieces are summed in a fixed order: a second call repeats every bit
+    C2 = torch.empty_like(C)
+    if out == "f32":
+        kl.kl_gemm_ex(M, N, K, kl.KL_BF16, a.data_ptr(), K, 0, b.data_ptr(), K, 0, C2.data_ptr(), N, kl.KL_F32,
+                      ws=ws.data_ptr(), ws_bytes=nb)
+    else:
+        kl.kl_gemm_ex(M, N, K, kl.KL_BF16, a.data_ptr(), K, 0, b.data_ptr(), K, 0, C2.data_ptr(), N, kl.KL_BF16,
+                      r.data_ptr(), N, kl.KL_BF16, ws=ws.data_ptr(), ws_bytes=nb)
+    torch.cuda.synchronize()
+    assert torch.equal(C, C2)
+
+
+def test_gemm_few_rows_strided_operands(kl):
+    """Leading dimensions wider than K and N (views into larger buffers)."""
+    M, N, K = 24, 392, 1000
+    A, B, R = _operands(M, N, K, 6)
+    abuf = torch.zeros((M, K + 24), dtype=torch.bfloat16, device="cuda")
+    bbuf = torch.zeros((N, K + 8), dtype=torch.bfloat16, device="cuda")
+    abuf[:, :K] = dev(A, torch.bfloat16)
+    bbuf[:, :K] = dev(B, torch.bfloat16)
+    C = torch.zeros((M, N + 40), dtype=torch.float32, device="cuda")
+    nb = kl.kl_gemm_scratch_bytes()
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    kl.kl_gemm_ex(M, N, K, kl.KL_BF16, abuf.data_ptr(), K + 24, 0, bbuf.data_ptr(), K + 8, 0, C.data_ptr(), N + 40,
+                  kl.KL_F32, ws=ws.data_ptr(), ws_bytes=nb)
+    torch.cuda.synchronize()
+    assert_rel(host(C[:, :N]), O.linear(A, B), 1e-5, "C strided")
+    assert torch.count_nonzero(C[:, N:]) == 0          # nothing written past N
