@@ -93,20 +93,24 @@ def peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
 
 
-def traffic_record():
-    """DRAM bytes per launch of the dominant kernel from a committed ncu
-    capture, keyed by the source file it was taken from (null if it changed)."""
+def traffic_record(workload, group):
+    """DRAM bytes per launch of a kernel group on a workload, from a committed
+    ncu capture (profiles/traffic.json), or None when there is no record or the
+    source file of the kernel has changed since the counters were taken."""
     try:
         import hashlib
 
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            rec = json.load(f)
-        src = os.path.join(ROOT, rec["source"])
-        with open(src, "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()
-        return rec if digest == rec["source_sha256"] else None
+            recs = json.load(f)["records"]
+        for rec in recs:
+            if rec["workload"] != workload or rec["group"] != group:
+                continue
+            with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+                digest = hashlib.sha256(f.read()).hexdigest()
+            return rec["bytes_per_launch"] if digest == rec["source_sha256"] else None
     except Exception:
         return None
+    return None
 
 
 class Clocks:
@@ -710,8 +714,7 @@ def main():
             g[f] += e[f]
     dname, d = max(groups.items(), key=lambda kv: kv[1]["ms"])
     per = d["ms"] / d["launches"] / 1e3
-    trec = traffic_record()
-    traffic = trec["bytes_per_launch"].get(dname) if trec and args.workload in trec.get("workloads", []) else None
+    traffic = traffic_record(args.workload, dname)
     if r["config"].get("roofline_bytes"):
         # bandwidth-bound workload: the dominant kernel group against HBM, plus the whole step
         ach = d["bytes"] / d["launches"] / per / 1e9
