@@ -64,7 +64,7 @@ struct SkParams {
   CUtensorMap tmB2[SK_MAXP];  // up weights (SwiGLU)
   SkProb prob[SK_MAXP];
   int nprob, W, P, stages, mpad, glu, stage_bytes;
-  float* pieces;              // [2 * grid][1 + glu][mpad][128] fp32
+  float* pieces;              // [2 * grid][1 + glu][mpad / 4][128][4] fp32 (16-byte granules, row fastest)
   unsigned int* cnt;          // [tiles][4] arrival counters (zero between launches)
   uint32_t* err;
 };
@@ -309,12 +309,16 @@ __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid
         if (whole) {
           sk_store_final(pr, p.glu, n, 32 * c, g, uu);
         } else {
+          // granule (m / 4, r) holds tokens m .. m+3 of row r: a warp writes 512 contiguous bytes
+          float4* pg = reinterpret_cast<float4*>(piece) + static_cast<size_t>(8 * c) * SK_BN + r;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int m = 32 * c + j;
-            if (m >= pr.M) continue;
-            piece[static_cast<size_t>(m) * SK_BN + r] = g[j];
-            if (p.glu) piece[(static_cast<size_t>(p.mpad) + m) * SK_BN + r] = uu[j];
+          for (int q4 = 0; q4 < 8; ++q4)
+            pg[q4 * SK_BN] = make_float4(g[4 * q4], g[4 * q4 + 1], g[4 * q4 + 2], g[4 * q4 + 3]);
+          if (p.glu) {
+            float4* pu = pg + static_cast<size_t>(p.mpad / 4) * SK_BN;
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4)
+              pu[q4 * SK_BN] = make_float4(uu[4 * q4], uu[4 * q4 + 1], uu[4 * q4 + 2], uu[4 * q4 + 3]);
           }
         }
       }
@@ -338,16 +342,29 @@ __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid
             for (int j = 0; j < 32; ++j) g[j] = uu[j] = 0.f;
             for (int c = first; c <= last; ++c) {
               // CTA c's piece of this tile: its first segment unless the tile began before c's run.
-              // Rows mc .. mc+31 lie inside the piece (mpad is a multiple of 32); rows past M
-              // hold no data and their sums are never stored.
+              // Tokens mc .. mc+31 lie inside the piece (mpad is a multiple of 32; every CTA
+              // writes all mpad tokens, those past M as zeros, never stored).
               const int slot = 2 * c + ((c == first && c * p.P != tfu) ? 1 : 0);
-              const float* pc = p.pieces + static_cast<size_t>(slot) * piece_floats + static_cast<size_t>(mc) * SK_BN + r;
+              const float4* pc = reinterpret_cast<const float4*>(p.pieces + static_cast<size_t>(slot) * piece_floats) +
+                                 static_cast<size_t>(mc / 4) * SK_BN + r;
 #pragma unroll
-              for (int j = 0; j < 32; ++j) g[j] += __ldcg(pc + j * SK_BN);
+              for (int q4 = 0; q4 < 8; ++q4) {
+                const float4 v = __ldcg(pc + q4 * SK_BN);
+                g[4 * q4] += v.x;
+                g[4 * q4 + 1] += v.y;
+                g[4 * q4 + 2] += v.z;
+                g[4 * q4 + 3] += v.w;
+              }
               if (p.glu) {
-                const float* pu = pc + static_cast<size_t>(p.mpad) * SK_BN;
+                const float4* pu = pc + static_cast<size_t>(p.mpad / 4) * SK_BN;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) uu[j] += __ldcg(pu + j * SK_BN);
+                for (int q4 = 0; q4 < 8; ++q4) {
+                  const float4 v = __ldcg(pu + q4 * SK_BN);
+                  uu[4 * q4] += v.x;
+                  uu[4 * q4 + 1] += v.y;
+                  uu[4 * q4 + 2] += v.z;
+                  uu[4 * q4 + 3] += v.w;
+                }
               }
             }
             sk_store_final(pr, p.glu, n, mc, g, uu);
