@@ -112,6 +112,15 @@ def test_gemm_host_checks(lib):
     # leading dimension smaller than the contiguous extent
     assert lib.kl_gemm(16, 16, 64, K.KL_BF16, 0x1000, 32, 0, 0x1000, 64, 0, 0x1000, 16, K.KL_BF16, None, 0, 0,
                        None) == K.KL_ERR_INVALID_ARG
+    # the scratch-taking form: same checks; its scratch size is whole 256-byte blocks
+    nb = lib.kl_gemm_scratch_bytes()
+    assert nb > 0 and nb % 256 == 0
+    assert lib.kl_gemm_ex(0, 8, 8, K.KL_BF16, 0x1000, 8, 0, 0x1000, 8, 0, 0x1000, 8, K.KL_BF16, None, 0, 0,
+                          0x1000, nb, None) == K.KL_ERR_INVALID_ARG
+    assert lib.kl_gemm_ex(16, 16, 64, K.KL_BF16, 0x1000, 64, 0, 0x1000, 64, 0, 0x1000, 8, K.KL_BF16, None, 0, 0,
+                          0x1000, nb, None) == K.KL_ERR_INVALID_ARG      # ldc < N
+    assert lib.kl_gemm_ex(16, 16, 64, 7, 0x1000, 64, 0, 0x1000, 64, 0, 0x1000, 16, K.KL_BF16, None, 0, 0,
+                          0x1000, nb, None) == K.KL_ERR_INVALID_ARG      # unknown dtype
 
 
 def test_stream_host_checks(lib):
@@ -133,6 +142,8 @@ def test_paged_host_checks(lib):
     assert K.kl_paged_attention_ws_bytes(pc, 64, 8, 128) >= 0
     assert K.kl_paged_attention_ws_bytes(pc, 64, 8, 64) == 0            # head dim 128 only
     assert K.kl_paged_attention_ws_bytes(K.PagedCfg(4, 9, 16, 8, 64), 64, 8, 128) == 0   # 8 x 9 > 64 rows
+    # pool rows past 32-bit indexing are refused
+    assert K.kl_paged_attention_ws_bytes(K.PagedCfg(4, 1, 16, 8, 1 << 28), 64, 8, 128) == 0
     assert K.kl_paged_attention_ws_bytes(K.PagedCfg(0, 1, 16, 8, 64), 64, 8, 128) == 0
     # null pointers are refused before any CUDA call
     assert lib.kl_paged_attention(ctypes.byref(pc), 64, 8, 128, K.KL_BF16, None, None, None, None, None, None,
