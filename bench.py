@@ -450,6 +450,24 @@ SETUP = {"layer": setup_layer, "attention": setup_attention, "lmhead": setup_lmh
          "decode": setup_decode}
 
 
+def max_over_ranks(vals, dist, device):
+    """Each rank's timings, reduced to the maximum over ranks: the slowest
+    rank sets the job's time. Without a process group, the values as given."""
+    if dist is None:
+        return [float(v) for v in vals]
+    import torch
+
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_throughput(units_per_rank_step, steps, world, ms):
+    """Units that all ranks processed per second of the job's time (weak
+    scaling: every rank handles its own units_per_rank_step each step)."""
+    return units_per_rank_step * steps * world / (ms / 1e3)
+
+
 def bench_ours(args, rank, world, local_rank, dist):
     import torch
 
@@ -518,10 +536,7 @@ def bench_ours(args, rank, world, local_rank, dist):
         extra = keep["after"](args)
         extra["link_hidden"] = round(extra["ms_per_step_bulk"] / (ms / args.steps), 4)
         extra["weight_h2d_gbs"] = round(extra["weight_h2d_bytes_per_step"] / (ms / args.steps) / 1e6, 1)
-    if dist is not None:
-        t = torch.tensor([ms, ms_e2e], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_e2e = float(t[0]), float(t[1])
+    ms, ms_e2e = max_over_ranks([ms, ms_e2e], dist, device)
     return dict(ms=ms, ms_e2e=ms_e2e, ms_prof=ms_prof, prof=prof, clocks=clk, launches=int(launches), units=units,
                 h2d=h2d, d2h=d2h, config=cfgd, extra=extra)
 
@@ -687,9 +702,8 @@ def main():
             dist.destroy_process_group()
         return
     pk = peaks()
-    tokens = r["units"] * args.steps * world
-    value = tokens / (r["ms"] / 1e3)
-    e2e = tokens / (r["ms_e2e"] / 1e3)
+    value = job_throughput(r["units"], args.steps, world, r["ms"])
+    e2e = job_throughput(r["units"], args.steps, world, r["ms_e2e"])
     prof = r["prof"]
     total_ms = sum(v["ms"] for v in prof.values()) or 1.0
     kernels = {}
