@@ -1360,23 +1360,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dq_tc_kernel(const __gr
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
 // [rows, cols] bf16 row-major, box 64 columns x box_rows rows, 128-byte swizzle.
 kl_status map_rows(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t box_rows = 128) {
-  auto fn = encode();
+  auto fn = tensor_map_encoder();
   if (!fn) return set_error(KL_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};

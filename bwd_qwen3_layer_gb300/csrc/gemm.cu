@@ -925,25 +925,11 @@ __global__ void gemm_finalize_kernel(int M, int N, const float* __restrict__ acc
 // ---------------------------------------------------------------------------
 // host: tensor maps
 // ---------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
 // 2-D bf16 map: inner extent `inner` (contiguous), `outer` rows with row
 // stride ld elements, box 64 x box_outer, 128-byte swizzle, zero fill.
 kl_status make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, int64_t ld,
                    uint32_t box_outer) {
-  auto fn = encode_fn();
+  auto fn = tensor_map_encoder();
   if (!fn) return set_error(KL_ERR_CUDA, "cuTensorMapEncodeTiled unavailable");
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
@@ -964,7 +950,7 @@ kl_status make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t out
 // (every element addressed lies inside the MN x K operand); returns false if
 // the encoder refuses the map (the caller then uses 2-D maps).
 bool make_map_mn3(CUtensorMap* m, const void* ptr, uint64_t mn, uint64_t k, int64_t ld) {
-  auto fn = encode_fn();
+  auto fn = tensor_map_encoder();
   if (!fn || mn % 64 != 0) return false;
   cuuint64_t dims[3] = {64, k, mn / 64};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(ld) * 2, 128};
@@ -1317,6 +1303,20 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
     KL_CUDA(cudaGetLastError());
   }
   return KL_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
 }
 
 size_t gemm_tail_ws_bytes() { return align_up(static_cast<size_t>(num_sms() / GEMM_CL) * 256 * 256 * 4, 256); }

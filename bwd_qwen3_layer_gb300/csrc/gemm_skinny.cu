@@ -403,24 +403,10 @@ unsigned int* skinny_cnt_slot() {
   return base[dev] + static_cast<size_t>(seq.fetch_add(1) % SK_CNT_SLOTS) * SK_CNT_TILES * 4;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 sk_encode() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-  });
-  return fn;
-}
-
 // K-major bf16 operand [rows][K] (row stride ld elements), box {64, box_rows},
 // 128-byte swizzle, zero fill outside.
 bool sk_map(CUtensorMap* m, const void* ptr, int K, int rows, int64_t ld, int box_rows) {
-  auto fn = sk_encode();
+  auto fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};

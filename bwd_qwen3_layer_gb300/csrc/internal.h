@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <utility>
 #include <stddef.h>
@@ -71,6 +72,10 @@ struct GemmSpec {
 // Bytes of tail_ws that let every launch split its last round (at most one
 // 256 x 256 fp32 tile per CTA pair of the device).
 size_t gemm_tail_ws_bytes();
+
+// The driver's cuTensorMapEncodeTiled (looked up once through the runtime), or
+// null if the driver has none; every TMA tensor map of the library is made with it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 constexpr int GEMM_EPI_STORE = 0;
 constexpr int GEMM_EPI_SWIGLU = 1;
 constexpr int GEMM_EPI_SWIGLU_BWD = 2;
