@@ -73,6 +73,7 @@ GemmSpec proj(int M, int N, int K, const void* A, int64_t lda, const void* B, in
   s.a_mn = 0; s.b_mn = 0;
   s.C = C; s.ldc = ldc; s.c_dtype = c_dtype;
   s.R = R; s.ldr = ldc; s.r_dtype = r_dtype;
+  s.b_const = 1;   // every caller passes a layer weight as B
   return s;
 }
 

@@ -64,6 +64,7 @@ struct SkParams {
   CUtensorMap tmB2[SK_MAXP];  // up weights (SwiGLU)
   SkProb prob[SK_MAXP];
   int nprob, W, P, stages, mpad, glu, stage_bytes;
+  int b_early;                // the weights may be copied before the dependency wait
   float* pieces;              // [2 * grid][1 + glu][mpad / 4][128][4] fp32 (16-byte granules, row fastest)
   unsigned int* cnt;          // [tiles][4] arrival counters (zero between launches)
   uint32_t* err;
@@ -131,7 +132,8 @@ __device__ __forceinline__ void sk_store_final(const SkProb& pr, int glu, int n,
 }
 
 __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid_constant__ SkParams p) {
-  pdl_enter();
+  // No global access before the dependency wait except the weights' first
+  // copies (warp 0 below): no earlier kernel writes them.
   extern __shared__ uint8_t sk_smem[];
   __shared__ __align__(8) uint64_t bars[2 * SK_MAX_STAGES + 5];
   __shared__ uint32_t tmem_holder;
@@ -183,10 +185,30 @@ __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid
         if (p.glu) tma_prefetch_desc(&p.tmB2[i]);
       }
     const uint32_t tx = static_cast<uint32_t>(nacc * SK_W_BYTES + p.mpad * SK_BK * 2);
-    int stage = 0;
-    uint32_t phase = 0;
-    int issued = 0;
-    for (int u = u0; u < u1; ++u) {
+    // the first stages' weights go out before the wait for the preceding kernel
+    // (their stages are free: the ring is fresh); their activation rows after it
+    const int pre = p.b_early ? min(S, u1 - u0) : 0;
+    if (el)
+      for (int i = 0; i < pre; ++i) {
+        const SkUnit un = sk_decode(p, u0 + i);
+        const uint32_t s = sbase + i * p.stage_bytes;
+        mbar_arrive_expect_tx(full_bar(i), tx);
+        tma_load_2d(s, &p.tmB[un.p], un.kbi * SK_BK, un.tile * SK_BN, full_bar(i));
+        if (p.glu) tma_load_2d(s + SK_W_BYTES, &p.tmB2[un.p], un.kbi * SK_BK, un.tile * SK_BN, full_bar(i));
+      }
+    __syncwarp();
+    pdl_wait();
+    pdl_launch_dependents();
+    if (el)
+      for (int i = 0; i < pre; ++i) {
+        const SkUnit un = sk_decode(p, u0 + i);
+        tma_load_2d(sbase + i * p.stage_bytes + nacc * SK_W_BYTES, &p.tmA[un.p], un.kbi * SK_BK, 0, full_bar(i));
+      }
+    __syncwarp();
+    int stage = pre % S;
+    uint32_t phase = pre == S ? 1u : 0u;
+    int issued = pre;
+    for (int u = u0 + pre; u < u1; ++u) {
       if (!mbar_wait_warp(empty_bar(stage), phase ^ 1u, p.err, &abort_flag)) {
         abort_flag = 1;
         break;
@@ -220,6 +242,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
+    pdl_wait();
     const bool el = elect_one();
     const uint32_t idesc = idesc_bf16_f32(SK_BN, p.mpad, 0, 0);
     int stage = 0;
@@ -273,6 +296,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid
     mbar_wait(drain_bar, 0, p.err);
   } else {
     // ---------------- epilogue: warp w owns TMEM lanes (rows) 32 (w % 4) .. +31 ----------------
+    pdl_wait();
     const int q = warp & 3;
     const int r = 32 * q + lane;                 // row of the weight tile
     const size_t piece_floats = static_cast<size_t>(nacc) * p.mpad * SK_BN;
@@ -517,6 +541,8 @@ kl_status gemm_skinny(const GemmSpec* specs, int nspec, cudaStream_t st, const c
   p.mpad = pl.mpad;
   p.glu = pl.glu;
   p.stage_bytes = pl.stage_bytes;
+  p.b_early = 1;
+  for (int i = 0; i < nspec; ++i) p.b_early &= specs[i].b_const ? 1 : 0;
   p.pieces = specs[0].tail_ws;
   p.cnt = skinny_cnt_slot();
   p.err = device_error_word();

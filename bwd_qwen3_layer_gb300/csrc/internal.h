@@ -56,6 +56,10 @@ struct GemmSpec {
   // (residual added, converted). Plain-store problems only.
   float* tail_ws = nullptr;
   size_t tail_ws_bytes = 0;
+  // B (and B2) are constant weights that no kernel of this library launched
+  // before the GEMM writes: the few-rows kernel may then start copying them
+  // before it waits for its predecessor on the stream.
+  int b_const = 0;
   int epi = 0;
   const void* B2 = nullptr;
   void* C2 = nullptr;

@@ -150,6 +150,12 @@ __device__ __forceinline__ void pdl_enter() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+// The two halves, for a kernel that first touches memory no earlier kernel
+// writes (e.g. constant weights) and only then waits.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 // One lane of a converged warp (the lowest), chosen by elect.sync. Roles that
 // issue TMA copies or tcgen05 MMAs run as whole warps, so descriptors,
