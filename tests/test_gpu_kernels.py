@@ -90,6 +90,8 @@ ATT_CASES = [
     (1, 1, 331, 8, 1, 128),     # length not a multiple of 4: lse / D read from global memory
     (0, 1, 32, 4, 2, 16),       # tiny fp32 workload
     (0, 2, 19, 6, 3, 40),
+    (1, 2, 700, 64, 8, 128),    # more (head, query-tile) items than SMs: the persistent forward, ragged, B = 2
+    (1, 3, 130, 64, 8, 128),    # persistent forward with three sequences of two query tiles each
 ]
 
 
