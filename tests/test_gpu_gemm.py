@@ -162,3 +162,23 @@ def test_gemm_few_rows_strided_operands(kl):
     torch.cuda.synchronize()
     assert_rel(host(C[:, :N]), O.linear(A, B), 1e-5, "C strided")
     assert torch.count_nonzero(C[:, N:]) == 0          # nothing written past N
+
+
+def test_gemm_few_rows_counter_slots_rearm(kl):
+    """Forty launches in a row cycle the shared-tile arrival counters' slots more
+    than twice: each counter must be back at zero when its slot comes round again,
+    so every launch gives the same bits (shapes with tiles shared between CTAs)."""
+    M, N, K = 64, 1344, 2560
+    A, B, _ = _operands(M, N, K, 7)
+    a, b = dev(A, torch.bfloat16), dev(B, torch.bfloat16)
+    nb = kl.kl_gemm_scratch_bytes()
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    outs = [torch.empty((M, N), dtype=torch.float32, device="cuda") for _ in range(40)]
+    for C in outs:
+        kl.kl_gemm_ex(M, N, K, kl.KL_BF16, a.data_ptr(), K, 0, b.data_ptr(), K, 0, C.data_ptr(), N, kl.KL_F32,
+                      ws=ws.data_ptr(), ws_bytes=nb)
+    torch.cuda.synchronize()
+    kl.kl_device_status()
+    assert_rel(host(outs[0]), O.linear(A, B), 1e-5, "first")
+    for C in outs[1:]:
+        assert torch.equal(C, outs[0])
