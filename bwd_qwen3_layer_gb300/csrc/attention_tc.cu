@@ -26,7 +26,6 @@
 #include <math.h>
 #include <string.h>
 
-#include <mutex>
 #include <type_traits>
 
 #include "internal.h"

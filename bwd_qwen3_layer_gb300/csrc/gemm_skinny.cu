@@ -12,6 +12,9 @@
 //   * Work units are (weight tile, 64-wide k-block); the W units, tile-major,
 //     are dealt in equal runs of P to one CTA per SM (stream-K), so every SM
 //     streams the same bytes whatever N and K are.
+//   * Weights that no earlier kernel writes (GemmSpec::b_const) start
+//     streaming before the wait for the preceding kernel: the first ring
+//     stages' weight tiles are copied, then the wait, then their activations.
 //   * A tile held whole by one CTA is written by it. A tile shared by two or
 //     more CTAs leaves one fp32 piece per CTA; per 32-row quarter of the
 //     tile, the warp that brings its arrival counter to the number of pieces
@@ -27,7 +30,6 @@
 #include <string.h>
 
 #include <atomic>
-#include <mutex>
 
 #include "internal.h"
 #include "kl_common.cuh"
