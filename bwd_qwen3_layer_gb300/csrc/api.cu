@@ -753,12 +753,10 @@ kl_status kl_layer_forward_paged(const kl_layer_cfg* cfg, const kl_paged_cfg* pc
     with_tail(g, 3, b.tail, b.tail_bytes);
     KL_TRY(run_gemms(dt, g, 3, st, "gemm.paged_qkv"));
   }
-  // optional per-head norm, then the rotation at the tokens' absolute positions ctx[b] + i
-  KL_TRY(qk_rope_fwd(T, D.Hq, D.S, D.d, dt, b.q_pre, w->gamma_q, cfg->eps, D.qk_norm, D.inter, cfg->rope_base,
-                     nullptr, b.q, b.rstd_q, st, ctx));
-  KL_TRY(qk_rope_fwd(T, D.Hkv, D.S, D.d, dt, b.k_pre, w->gamma_k, cfg->eps, D.qk_norm, D.inter, cfg->rope_base,
-                     nullptr, b.k, b.rstd_k, st, ctx));
-  KL_TRY(paged_kv_write(*pc, D.Hkv, b.k, b.v, table, ctx, k_pool, v_pool, st));
+  // optional per-head norm, the rotation at the tokens' absolute positions ctx[b] + i, and the new keys
+  // and values written into their cache slots: one launch
+  KL_TRY(paged_qkv_rope(*pc, D.Hq, D.Hkv, D.d, b.q_pre, b.k_pre, b.v, w->gamma_q, w->gamma_k, cfg->eps, D.qk_norm,
+                        D.inter, cfg->rope_base, table, ctx, b.q, k_pool, v_pool, st));
   KL_TRY(paged_attention(*pc, D.Hq, D.Hkv, b.q, k_pool, v_pool, table, ctx, b.o, nullptr, b.att, b.att_bytes, st));
   {
     GemmSpec g = proj(T, H, D.Dq, b.o, D.Dq, w->wo, D.Dq, b.x2, H, dt, X, dt);

@@ -700,6 +700,74 @@ __global__ void __launch_bounds__(256) qk_rope_fwd_kernel(int rows, int heads, i
   }
 }
 
+// A step over a paged key/value cache, in one launch: every new token's q
+// heads rotated (after the optional per-head norm) into q_out, its k heads
+// rotated the same way straight into their cache slots, and its v heads copied
+// to theirs. Token i of sequence b sits at position ctx[b] + i; its slot is
+// block table[b][pos / bs], row pos % bs. One warp per (token, head) row, the
+// q heads first; a position past its table row or a table entry outside the
+// pool is skipped and recorded (KL_DEVERR_PAGE), a negative position skipped.
+__global__ void __launch_bounds__(256) paged_qkv_rope_kernel(
+    int T, int n_new, int Hq, int Hkv, int d, const __nv_bfloat16* __restrict__ q_pre,
+    const __nv_bfloat16* __restrict__ k_pre, const __nv_bfloat16* __restrict__ v, const __nv_bfloat16* __restrict__ gq,
+    const __nv_bfloat16* __restrict__ gk, float eps, int norm, int inter, RopeFreq f, const int32_t* __restrict__ table,
+    const int32_t* __restrict__ ctx, int bs, int max_blocks, int n_blocks, __nv_bfloat16* __restrict__ q_out,
+    __nv_bfloat16* __restrict__ k_pool, __nv_bfloat16* __restrict__ v_pool, uint32_t* err) {
+  pdl_enter();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int heads = Hq + Hkv;
+  const int row = blockIdx.x * 8 + warp;
+  if (row >= T * heads) return;
+  const int tok = row / heads, hh = row - tok * heads;
+  const int b = tok / n_new, pos = ctx[b] + (tok - b * n_new), half = d / 2;
+  const __nv_bfloat16* x;
+  __nv_bfloat16* y;
+  const __nv_bfloat16* g;
+  if (hh < Hq) {
+    x = q_pre + (static_cast<int64_t>(tok) * Hq + hh) * d;
+    y = q_out + (static_cast<int64_t>(tok) * Hq + hh) * d;
+    g = gq;
+  } else {
+    const int h = hh - Hq;
+    if (pos < 0) return;
+    const int lb = pos / bs;
+    const int blk = lb < max_blocks ? table[b * max_blocks + lb] : -1;
+    if (blk < 0 || blk >= n_blocks) {
+      if (lane == 0) record_error(err, KL_DEVERR_PAGE);
+      return;
+    }
+    const int64_t dst = ((static_cast<int64_t>(blk) * bs + (pos - lb * bs)) * Hkv + h) * d;
+    const int64_t src = (static_cast<int64_t>(tok) * Hkv + h) * d;
+    x = k_pre + src;
+    y = k_pool + dst;
+    g = gk;
+    for (int j = lane * 4; j < d; j += 128)   // the value row, unchanged
+      *reinterpret_cast<uint2*>(v_pool + dst + j) = *reinterpret_cast<const uint2*>(v + src + j);
+  }
+  float r = 1.0f;
+  if (norm) {
+    float ss = 0.f;
+    for (int j = lane; j < d; j += 32) {
+      const float vv = ld_f(x + j);
+      ss = fmaf(vv, vv, ss);
+    }
+    ss = warp_sum(ss);
+    r = 1.0f / sqrtf(ss / static_cast<float>(d) + eps);
+  }
+  for (int i = lane; i < half; i += 32) {
+    int ia, ib;
+    plane_idx(i, d, inter, ia, ib);
+    float a = ld_f(x + ia) * r, bb = ld_f(x + ib) * r;
+    if (norm) {
+      a *= ld_f(g + ia);
+      bb *= ld_f(g + ib);
+    }
+    const float2 cs = plane_cs(pos, i, half, f, nullptr);
+    st_f(y + ia, a * cs.x - bb * cs.y);
+    st_f(y + ib, a * cs.y + bb * cs.x);
+  }
+}
+
 // Backward: dy (gradient after the rotation, element type TD, scaled by
 // dy_scale) turned back, then the RMSNorm backward
 //   n = x r, dn = dy g, dx = r (dn - n mean(dn n)),  dg += dy n
@@ -1057,6 +1125,26 @@ kl_status qk_rope_fwd(int T, int heads, int S, int d, int dtype, const void* pre
   else
     launch_pdl(qk_rope_fwd_kernel<float>, grid, 256, 0, st, rows, heads, S, d, (const float*)pre, (const float*)gamma, eps,
                                                    norm, inter, f, tab, (float*)out, rstd, pos_off);
+  KL_CUDA(cudaGetLastError());
+  return KL_OK;
+}
+
+kl_status paged_qkv_rope(const kl_paged_cfg& pc, int Hq, int Hkv, int d, const void* q_pre, const void* k_pre,
+                         const void* v, const void* gamma_q, const void* gamma_k, float eps, int norm, int inter,
+                         float base, const int32_t* table, const int32_t* ctx, void* q_out, void* k_pool, void* v_pool,
+                         cudaStream_t st) {
+  if (d != 128 || !q_pre || !k_pre || !v || !table || !ctx || !q_out || !k_pool || !v_pool ||
+      (norm && (!gamma_q || !gamma_k)))
+    return set_error(KL_ERR_INVALID_ARG, "paged q/k/v rotation: bad arguments");
+  const int T = pc.B * pc.n_new, rows = T * (Hq + Hkv);
+  const RopeFreq f = rope_freq(d, base);
+  ProfScope ps("paged_qkv_rope", st, 0.0, 2.0 * 2 * T * (Hq + 2 * Hkv) * d);
+  launch_pdl(paged_qkv_rope_kernel, (rows + 7) / 8, 256, 0, st, T, pc.n_new, Hq, Hkv, d,
+             static_cast<const __nv_bfloat16*>(q_pre), static_cast<const __nv_bfloat16*>(k_pre),
+             static_cast<const __nv_bfloat16*>(v), static_cast<const __nv_bfloat16*>(gamma_q),
+             static_cast<const __nv_bfloat16*>(gamma_k), eps, norm, inter, f, table, ctx, pc.block_size,
+             pc.max_blocks, pc.n_blocks, static_cast<__nv_bfloat16*>(q_out), static_cast<__nv_bfloat16*>(k_pool),
+             static_cast<__nv_bfloat16*>(v_pool), device_error_word());
   KL_CUDA(cudaGetLastError());
   return KL_OK;
 }

@@ -135,6 +135,12 @@ kl_status convert_f32(int64_t n, int dtype, const float* src, void* dst, cudaStr
 // paged.cu: the forward path with a paged key/value cache (bf16, d = 128)
 kl_status paged_check(const kl_paged_cfg* pc, int Hq, int Hkv, int d, int dtype);
 size_t paged_attention_ws(const kl_paged_cfg& pc, int Hq, int Hkv);
+// One launch for a paged step's rotations and cache writes: q rotated into
+// q_out, k rotated into its cache slots, v copied into its (bf16, d = 128).
+kl_status paged_qkv_rope(const kl_paged_cfg& pc, int Hq, int Hkv, int d, const void* q_pre, const void* k_pre,
+                         const void* v, const void* gamma_q, const void* gamma_k, float eps, int norm, int inter,
+                         float base, const int32_t* table, const int32_t* ctx, void* q_out, void* k_pool, void* v_pool,
+                         cudaStream_t st);
 kl_status paged_kv_write(const kl_paged_cfg& pc, int Hkv, const void* k_new, const void* v_new, const int32_t* table,
                          const int32_t* ctx, void* kp, void* vp, cudaStream_t st);
 kl_status paged_attention(const kl_paged_cfg& pc, int Hq, int Hkv, const void* q, const void* kp, const void* vp,
