@@ -161,3 +161,30 @@ def test_table_entry_outside_the_pool_is_reported(kl):
     with pytest.raises(kl.KLError):
         kl.kl_device_status()
     kl.kl_device_status()                 # the word was cleared by the read
+
+
+def test_layer_step_with_a_table_entry_outside_the_pool_is_reported(kl):
+    """The paged layer step's rotation/cache-write launch meets a new token whose
+    block-table entry is outside the pool: the write is skipped and the device
+    error word says why (the rest of the step still runs)."""
+    B, n_new, H, Hq, Hkv, I, bs = 2, 1, 256, 4, 2, 512, 16
+    ctx = [5, 20]
+    cfg = L.make_cfg(B, n_new, H, Hq, Hkv, D, I, dtype=kl.KL_BF16)
+    w = synth.layer_weights(51, H, Hq, Hkv, D, I, bf16=True)
+    X = synth.layer_inputs(51, B * n_new, H, bf16=True)["X"]
+    table, kp, vp, _, max_blocks, n_blocks = _case(52, B, n_new, Hq, Hkv, bs, ctx)
+    table = table.copy()
+    table[1, 20 // bs] = n_blocks + 3      # sequence 1's new token (position 20) has no valid block
+    pc = kl.PagedCfg(B, n_new, bs, max_blocks, n_blocks)
+    w_dev = {n: L.to_device(w[L.SYNTH_NAMES[n]], kl.KL_BF16, "cuda") for n in L.weight_fields(cfg)}
+    kd, vd = _dev(kp), _dev(vp)
+    Xd, td, cd = L.to_device(X, kl.KL_BF16, "cuda"), _dev(table, torch.int32), _dev(ctx, torch.int32)
+    ws = torch.empty(kl.kl_layer_forward_paged_ws_bytes(cfg, pc), dtype=torch.uint8, device="cuda")
+    Y = torch.empty_like(Xd)
+    kl.kl_layer_forward_paged(cfg, pc, L.weights_struct(w_dev), Xd.data_ptr(), Y.data_ptr(), kd.data_ptr(),
+                              vd.data_ptr(), td.data_ptr(), cd.data_ptr(), ws.data_ptr(), ws.numel())
+    torch.cuda.synchronize()
+    with pytest.raises(kl.KLError) as e:
+        kl.kl_device_status()
+    assert e.value.status == kl.KL_ERR_DEVICE
+    kl.kl_device_status()                 # the word was cleared by the read
