@@ -523,3 +523,95 @@ def test_layer_sequences_independent():
     Ya, _ = O.layer_forward(cfg1, w, X[:4])
     Yb, _ = O.layer_forward(cfg1, w, X[4:])
     np.testing.assert_allclose(Y2, np.concatenate([Ya, Yb]), rtol=1e-13, atol=1e-14)
+
+
+# ----------------------------------------------------------------------------
+# the layer's wiring ("KYNETRA FOUNDRY", pre-norm decoder paragraph): RMSNorm
+# of the layer input -> attention -> residual onto the layer input (x2); then
+# RMSNorm of x2 -> SwiGLU MLP -> residual onto x2. Every expected value below
+# is assembled from the separately pinned pieces (rmsnorm_fwd, linear,
+# rope_fwd, attention_fwd, swiglu_fwd), never from layer_forward itself.
+# ----------------------------------------------------------------------------
+
+_WCFG = O.LayerConfig(B=2, S=5, H=16, Hq=4, Hkv=2, d=4, I=24)
+
+
+def _wiring_weights(seed):
+    w = synth.layer_weights(seed, _WCFG.H, _WCFG.Hq, _WCFG.Hkv, _WCFG.d, _WCFG.I)
+    # projections scaled so each branch moves the residual stream by O(1):
+    # reading the wrong tensor then changes every output by far more than rounding
+    return {k: (v if k.startswith("gamma") else 15.0 * v) for k, v in w.items()}
+
+
+def _attention_branch(cfg, w, X):
+    h1, _ = O.rmsnorm_fwd(X, w["gamma1"], cfg.eps)
+    q = O.rope_fwd(O.linear(h1, w["Wq"]).reshape(cfg.T, cfg.Hq, cfg.d), cfg.B, cfg.S, cfg.rope_base)
+    k = O.rope_fwd(O.linear(h1, w["Wk"]).reshape(cfg.T, cfg.Hkv, cfg.d), cfg.B, cfg.S, cfg.rope_base)
+    v = O.linear(h1, w["Wv"]).reshape(cfg.T, cfg.Hkv, cfg.d)
+    o, _ = O.attention_fwd(q, k, v, cfg.B, cfg.S)
+    return O.linear(o.reshape(cfg.T, cfg.Hq * cfg.d), w["Wo"])
+
+
+def _mlp_branch(cfg, w, x):
+    h2, _ = O.rmsnorm_fwd(x, w["gamma2"], cfg.eps)
+    return O.linear(O.swiglu_fwd(O.linear(h2, w["Wg"]), O.linear(h2, w["Wu"])), w["Wd"])
+
+
+def _wiring_checks(fwd):
+    """The three wiring properties of a layer forward `fwd(cfg, w, X) -> (Y, saved)`;
+    returns the names of those that fail."""
+    cfg = _WCFG
+    w = _wiring_weights(21)
+    X = synth.layer_inputs(21, cfg.T, cfg.H)["X"]
+    failed = []
+
+    def close(a, b):
+        return np.allclose(a, b, rtol=1e-12, atol=1e-12)
+
+    # (i) no MLP contribution (Wd = 0): Y is the layer input plus the attention branch
+    Y0, _ = fwd(cfg, dict(w, Wd=np.zeros_like(w["Wd"])), X)
+    if not close(Y0, X + _attention_branch(cfg, w, X)):
+        failed.append("attention residual")
+    # (ii) no attention contribution (Wo = 0): Y is the input plus the MLP of its own norm
+    Y1, _ = fwd(cfg, dict(w, Wo=np.zeros_like(w["Wo"])), X)
+    if not close(Y1, X + _mlp_branch(cfg, w, X)):
+        failed.append("mlp residual")
+    # (iii) both branches: the MLP normalises the attention half's output x2 (taken
+    # from run (i), which (i) ties to the pieces) and its residual lands on x2
+    Y, saved = fwd(cfg, w, X)
+    if not (close(Y, Y0 + _mlp_branch(cfg, w, Y0))
+            and close(saved["x2"], Y0)
+            and close(saved["h2"], O.rmsnorm_fwd(Y0, w["gamma2"], cfg.eps)[0])):
+        failed.append("mlp reads x2")
+    # and the second norm sees the attention branch at all: a change of Wo moves h2
+    _, saved2 = fwd(cfg, dict(w, Wo=1.5 * w["Wo"]), X)
+    if np.allclose(saved2["h2"], saved["h2"], rtol=1e-3, atol=1e-3):
+        failed.append("h2 independent of Wo")
+    return failed
+
+
+def _miswired_forward(kind):
+    """A layer forward assembled from the pinned pieces with one plausible
+    wiring mistake, to show that _wiring_checks can tell it from the oracle."""
+    def fwd(cfg, w, X):
+        h1, _ = O.rmsnorm_fwd(X, w["gamma1"], cfg.eps)
+        x2 = (h1 if kind == "attention residual onto h1" else X) + _attention_branch(cfg, w, X)
+        norm_in = X if kind == "mlp norm reads X" else x2
+        h2, _ = O.rmsnorm_fwd(norm_in, w["gamma2"], cfg.eps)
+        mlp = O.linear(O.swiglu_fwd(O.linear(h2, w["Wg"]), O.linear(h2, w["Wu"])), w["Wd"])
+        Y = (X if kind == "mlp residual onto X" else x2) + mlp
+        return Y, {"x2": x2, "h2": h2}
+    return fwd
+
+
+def test_layer_wiring_from_pinned_pieces():
+    """The oracle's layer_forward meets all three wiring properties."""
+    assert _wiring_checks(O.layer_forward) == []
+
+
+@pytest.mark.parametrize("kind", ["mlp norm reads X", "mlp residual onto X", "attention residual onto h1"])
+def test_layer_wiring_checks_catch_miswiring(kind):
+    """Each plausible miswiring of the second half (or of the first residual)
+    fails at least one wiring check, while the correctly wired assembly passes."""
+    assert _wiring_checks(_miswired_forward("correct")) == []
+    assert _wiring_checks(_miswired_forward(kind)) != []
