@@ -167,8 +167,11 @@ __global__ void __launch_bounds__(RF_THREADS) rmsnorm_fwd_row_kernel(int width, 
 }
 
 // ---------------------------------------------------------------------------
-// RMSNorm backward: one warp per row; the gain gradient is accumulated per
-// CTA in shared memory and written as a partial row, reduced afterwards.
+// RMSNorm backward, any width: one CTA per row at a time, thread t owning
+// columns t, t + 256, ... . The gain gradient of a column is summed in shared
+// memory by its owning thread alone, in row order (no atomics, so the partial
+// rows and the gain gradient are the same on every run), and written as one
+// partial row per CTA, reduced afterwards in CTA order.
 //   n = x*rstd, dn = dh*gamma, dx = resid + rstd*(dn - n*mean(dn*n)),
 //   dgamma += dh*n.
 // ---------------------------------------------------------------------------
@@ -179,32 +182,37 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(
     T* __restrict__ dx, float* __restrict__ partial) {
   pdl_enter();
   extern __shared__ float sacc[];
-  for (int j = threadIdx.x; j < width; j += blockDim.x) sacc[j] = 0.f;
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ float red[2][8];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int j = tid; j < width; j += 256) sacc[j] = 0.f;
   const float inv_w = 1.0f / static_cast<float>(width);
-  for (int row = blockIdx.x * 8 + warp; row < rows; row += gridDim.x * 8) {
+  int buf = 0;
+  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
     const int64_t off = static_cast<int64_t>(row) * width;
     const float r = rstd[row];
     float dot = 0.f;
-    for (int j = lane; j < width; j += 32) {
+    for (int j = tid; j < width; j += 256) {
       const float n = ld_f(x + off + j) * r;
-      const float g = ld_f(dh + off + j);
-      dot = fmaf(g * ld_f(gamma + j), n, dot);
+      dot = fmaf(ld_f(dh + off + j) * ld_f(gamma + j), n, dot);
     }
-    dot = warp_sum(dot) * inv_w;
-    for (int j = lane; j < width; j += 32) {
+    dot = warp_sum(dot);
+    if (lane == 0) red[buf][warp] = dot;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) tot += red[buf][w];
+    tot *= inv_w;
+    buf ^= 1;   // the next row's partial sums go to the other buffer: one barrier per row
+    for (int j = tid; j < width; j += 256) {
       const float n = ld_f(x + off + j) * r;
       const float g = ld_f(dh + off + j);
-      const float dn = g * ld_f(gamma + j);
-      float v = r * (dn - n * dot);
+      float v = r * (g * ld_f(gamma + j) - n * tot);
       if (resid) v += ld_f(resid + off + j);
       st_f(dx + off + j, v);
-      atomicAdd(&sacc[j], g * n);
+      sacc[j] += g * n;
     }
   }
-  __syncthreads();
-  for (int j = threadIdx.x; j < width; j += blockDim.x)
+  for (int j = tid; j < width; j += 256)
     partial[static_cast<int64_t>(blockIdx.x) * width + j] = sacc[j];
 }
 

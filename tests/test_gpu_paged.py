@@ -66,7 +66,7 @@ def test_paged_attention_matches_oracle(kl, B, n_new, Hq, Hkv, bs, ctx):
     torch.cuda.synchronize()
     kl.kl_device_status()
     assert_rel(o.double().cpu().numpy(), Oref, TOL_BF16, "O")
-    np.testing.assert_allclose(lse.double().cpu().numpy(), lse_ref, rtol=0, atol=2e-2)
+    np.testing.assert_allclose(lse.double().cpu().numpy(), lse_ref, rtol=0, atol=2e-3)
 
 
 def test_paged_kv_write_is_exact(kl):
