@@ -117,25 +117,43 @@ def traffic_record(workload, group):
 
 
 class Clocks:
-    """nvidia-smi sampler for the timed region (every 200 ms)."""
+    """nvidia-smi sampler (every 20 ms, read-only query). mark() brackets the
+    timed region by wall clock; stop() reports the samples taken inside it."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 20
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
         self.f = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
             self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    @staticmethod
+    def _stamp(text):
+        """nvidia-smi's local-time stamp 'YYYY/MM/DD HH:MM:SS.mmm' as epoch seconds."""
+        try:
+            whole, _, frac = text.strip().partition(".")
+            return time.mktime(time.strptime(whole, "%Y/%m/%d %H:%M:%S")) + float("0." + (frac or "0"))
+        except ValueError:
+            return None
 
     def stop(self):
         if self.proc is None:
@@ -149,22 +167,25 @@ class Clocks:
         self.f.seek(0)
         rows = [r.split(",") for r in self.f.read().strip().splitlines() if r.strip()]
         os.unlink(self.f.name)
-        sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        parsed = []
         for r in rows:
             r = [x.strip() for x in r]
-            if len(r) < 9:
+            if len(r) < 10:
                 continue
             try:
-                sm.append(float(r[1]))
-                mx = float(r[2])
+                parsed.append((self._stamp(r[0]), float(r[2]), float(r[3]),
+                               [n for n, v in zip(names, r[6:10]) if v.lower().startswith("active")]))
             except ValueError:
                 continue
-            for n, v in zip(names, r[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        inside = [p for p in parsed if p[0] is not None and self.t0 is not None and self.t1 is not None
+                  and self.t0 - 0.01 <= p[0] <= self.t1 + 0.01]
+        use = inside or parsed            # a region shorter than one period: every sample
+        sm = [p[1] for p in use]
+        reasons = sorted({n for p in use for n in p[3]})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": use[-1][2] if use else None,
+                "reasons": reasons, "samples": len(sm), "samples_in_timed_region": len(inside),
+                "period_ms": self.PERIOD_MS}
 
 
 def read_profile(K):
@@ -532,11 +553,13 @@ def bench_ours(args, rank, world, local_rank, dist):
     time.sleep(0.25)
     n0 = lib.kl_launch_count()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks.mark(True)
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     barrier()
+    clocks.mark(False)
     launches = lib.kl_launch_count() - n0
     clk = clocks.stop()
     ms = e0.elapsed_time(e1)
@@ -702,6 +725,107 @@ def oracle_sample(workload: str, steps: int):
     return units / sec, sec, cores, desc
 
 
+def pick_tensor_peak(pk, region_ms):
+    """The tensor-core denominator for kernels timed in a region of region_ms:
+    the burst GEMM figure for a short region (the board has not yet reached its
+    power cap), the sustained one for a region of half a second or more."""
+    if region_ms < 500.0:
+        return pk["bf16_tflops"], f"{pk['src']} bf16_tflops (burst: timed region {region_ms / 1e3:.2f} s < 0.5 s)"
+    return (pk["bf16_tflops_sustained"],
+            f"{pk['src']} bf16_tflops_sustained (timed region {region_ms / 1e3:.2f} s >= 0.5 s)")
+
+
+def summarize(r, workload, steps, world, pk):
+    """Throughput, per-kernel roofline figures and the dominant kernel's
+    roofline of one bench_ours result."""
+    value = job_throughput(r["units"], steps, world, r["ms"])
+    e2e = job_throughput(r["units"], steps, world, r["ms_e2e"])
+    tpk, tsrc = pick_tensor_peak(pk, r["ms_prof"])
+    prof = r["prof"]
+    total_ms = sum(v["ms"] for v in prof.values()) or 1.0
+    kernels, above = {}, []
+    for name, e in sorted(prof.items(), key=lambda kv: -kv[1]["ms"]):
+        per = e["ms"] / e["launches"] / 1e3
+        ent = {"launches": e["launches"], "ms_per_launch": round(e["ms"] / e["launches"], 4),
+               "share": round(e["ms"] / total_ms, 4)}
+        if e["flops"] > 0:
+            a = e["flops"] / e["launches"] / per / 1e12
+            ent.update(achieved=round(a, 2), unit="TFLOP/s", frac=round(a / tpk, 4))
+        elif e["bytes"] > 0:
+            a = e["bytes"] / e["launches"] / per / 1e9
+            ent.update(achieved=round(a, 1), unit="GB/s", frac=round(a / pk["hbm_gbs"], 4))
+        if ent.get("frac", 0.0) > 1.0:
+            above.append(name)
+        kernels[name] = ent
+    # roofline of the dominant kernel: labelled launches of one kernel are
+    # grouped (every "gemm.*" call site runs gemm_bf16_tc_kernel)
+    groups = {}
+    for name, e in prof.items():
+        key = "gemm_bf16_tc" if name.startswith("gemm.") or name == "gemm" else name
+        g = groups.setdefault(key, {"launches": 0, "ms": 0.0, "flops": 0.0, "bytes": 0.0})
+        for f in g:
+            g[f] += e[f]
+    dname, d = max(groups.items(), key=lambda kv: kv[1]["ms"])
+    per = d["ms"] / d["launches"] / 1e3
+    traffic = traffic_record(workload, dname)
+    if r["config"].get("roofline_bytes"):
+        # bandwidth-bound workload: the dominant kernel group against HBM, plus the whole step
+        ach = d["bytes"] / d["launches"] / per / 1e9
+        step_gbs = r["config"]["hbm_bytes_per_step"] / (r["ms"] / steps / 1e3) / 1e9
+        roof = {"kernel": dname, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4), "traffic": traffic,
+                "peak_src": f"{pk['src']} hbm_gbs",
+                "step": {"bytes": r["config"]["hbm_bytes_per_step"], "achieved": round(step_gbs, 1),
+                         "frac": round(step_gbs / pk["hbm_gbs"], 4)}}
+    elif d["flops"] > 0:
+        ach = d["flops"] / d["launches"] / per / 1e12
+        roof = {"kernel": dname, "bound": "tensor", "achieved": round(ach, 2), "peak": tpk,
+                "unit": "TFLOP/s", "frac": round(ach / tpk, 4), "traffic": traffic, "peak_src": tsrc,
+                "frac_burst": round(ach / pk["bf16_tflops"], 4),
+                "frac_sustained": round(ach / pk["bf16_tflops_sustained"], 4)}
+    else:
+        ach = d["bytes"] / d["launches"] / per / 1e9
+        roof = {"kernel": dname, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4), "traffic": traffic,
+                "peak_src": f"{pk['src']} hbm_gbs"}
+    roof["timed"] = (f"per-launch CUDA events over a second timed region of the same {steps} steps "
+                     f"({r['ms_prof'] / steps:.4f} ms per step with the events)")
+    total_flops = sum(e["flops"] for e in prof.values()) / steps
+    agg_tflops = total_flops / (r["ms"] / steps / 1e3) / 1e12
+    out = {"value": round(value, 1), "unit": "tokens/s", "ms_per_step": round(r["ms"] / steps, 4)}
+    if total_flops > 0:
+        bpk, bsrc = pick_tensor_peak(pk, r["ms"])
+        out.update(tensor_frac_aggregate=round(agg_tflops / bpk, 4), aggregate_tflops=round(agg_tflops, 2),
+                   aggregate_peak_src=bsrc)
+    out.update(roofline=roof, kernels=kernels, kernels_frac_above_1=above, gpu_launches=r["launches"],
+               clocks=r["clocks"],
+               e2e={"value": round(e2e, 1), "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
+                    "d2h_bytes_per_step": r["d2h"]})
+    if r["extra"] is not None:
+        out["stream"] = r["extra"]
+    return out
+
+
+EXTRAS = {"attention": (5, 3), "lmhead": (10, 3), "stream": (3, 3), "decode": (20, 3)}
+
+
+def measure_extras(args, pk):
+    """Short runs of the long-context attention, lm-head, 8-layer stream and
+    paged decode workloads in the same process, each with its own timed
+    region, per-kernel figures and clock record (steps, warm-up per EXTRAS)."""
+    out = {}
+    for wl, (steps, warm) in EXTRAS.items():
+        a = argparse.Namespace(**vars(args))
+        a.workload, a.steps, a.warmup = wl, steps, warm
+        t0 = time.time()
+        r = bench_ours(a, 0, 1, 0, None)
+        ent = {"metric": METRICS[wl], "steps": steps, "warmup": warm} | summarize(r, wl, steps, 1, pk)
+        ent["config"] = r["config"]
+        ent["wall_s"] = round(time.time() - t0, 1)
+        out[wl] = ent
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -710,6 +834,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="layer", choices=list(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="layer workload: skip the short runs of the other workloads")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.workload.startswith("stream") and "--steps" not in sys.argv:
@@ -746,69 +872,14 @@ def main():
             dist.destroy_process_group()
         return
     pk = peaks()
-    value = job_throughput(r["units"], args.steps, world, r["ms"])
-    e2e = job_throughput(r["units"], args.steps, world, r["ms_e2e"])
-    prof = r["prof"]
-    total_ms = sum(v["ms"] for v in prof.values()) or 1.0
-    kernels = {}
-    for name, e in sorted(prof.items(), key=lambda kv: -kv[1]["ms"]):
-        per = e["ms"] / e["launches"] / 1e3
-        ent = {"launches": e["launches"], "ms_per_launch": round(e["ms"] / e["launches"], 4),
-               "share": round(e["ms"] / total_ms, 4)}
-        if e["flops"] > 0:
-            a = e["flops"] / e["launches"] / per / 1e12
-            ent.update(achieved=round(a, 2), unit="TFLOP/s", frac=round(a / pk["bf16_tflops_sustained"], 4))
-        elif e["bytes"] > 0:
-            a = e["bytes"] / e["launches"] / per / 1e9
-            ent.update(achieved=round(a, 1), unit="GB/s", frac=round(a / pk["hbm_gbs"], 4))
-        kernels[name] = ent
-    # roofline of the dominant kernel: labelled launches of one kernel are
-    # grouped (every "gemm.*" call site runs gemm_bf16_tc_kernel)
-    groups = {}
-    for name, e in prof.items():
-        key = "gemm_bf16_tc" if name.startswith("gemm.") or name == "gemm" else name
-        g = groups.setdefault(key, {"launches": 0, "ms": 0.0, "flops": 0.0, "bytes": 0.0})
-        for f in g:
-            g[f] += e[f]
-    dname, d = max(groups.items(), key=lambda kv: kv[1]["ms"])
-    per = d["ms"] / d["launches"] / 1e3
-    traffic = traffic_record(args.workload, dname)
-    if r["config"].get("roofline_bytes"):
-        # bandwidth-bound workload: the dominant kernel group against HBM, plus the whole step
-        ach = d["bytes"] / d["launches"] / per / 1e9
-        step_gbs = r["config"]["hbm_bytes_per_step"] / (r["ms"] / args.steps / 1e3) / 1e9
-        roof = {"kernel": dname, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"],
-                "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4), "traffic": traffic,
-                "peak_src": f"{pk['src']} hbm_gbs",
-                "step": {"bytes": r["config"]["hbm_bytes_per_step"], "achieved": round(step_gbs, 1),
-                         "frac": round(step_gbs / pk["hbm_gbs"], 4)}}
-    elif d["flops"] > 0:
-        ach = d["flops"] / d["launches"] / per / 1e12
-        roof = {"kernel": dname, "bound": "tensor", "achieved": round(ach, 2), "peak": pk["bf16_tflops_sustained"],
-                "unit": "TFLOP/s", "frac": round(ach / pk["bf16_tflops_sustained"], 4), "traffic": traffic,
-                "peak_src": f"{pk['src']} bf16_tflops_sustained (kernel timed inside the step)"}
-    else:
-        ach = d["bytes"] / d["launches"] / per / 1e9
-        roof = {"kernel": dname, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"],
-                "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4), "traffic": traffic,
-                "peak_src": f"{pk['src']} hbm_gbs"}
-    roof["timed"] = (f"per-launch CUDA events over a second timed region of the same {args.steps} steps "
-                     f"({r['ms_prof'] / args.steps:.4f} ms per step with the events)")
-    total_flops = sum(e["flops"] for e in prof.values()) / args.steps
-    agg_tflops = total_flops / (r["ms"] / args.steps / 1e3) / 1e12
-    line = {"metric": metric, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": round(r["ms"] / args.steps, 4), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": r["config"] | {"parallelism": f"replicas x{world}"},
-            "tensor_frac_aggregate": round(agg_tflops / pk["bf16_tflops_sustained"], 4),
-            "aggregate_tflops": round(agg_tflops, 2),
-            "roofline": roof, "kernels": kernels, "gpu_launches": r["launches"], "clocks": r["clocks"],
-            "e2e": {"value": round(e2e, 1), "unit": "tokens/s", "h2d_bytes_per_step": r["h2d"],
-                    "d2h_bytes_per_step": r["d2h"]}}
-    if r["extra"] is not None:
-        line["stream"] = r["extra"]
+    line = {"metric": metric} | summarize(r, args.workload, args.steps, world, pk)
+    line.update({"n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic"})
+    line["config"] = r["config"] | {"parallelism": f"replicas x{world}"}
+    if world == 1 and args.workload == "layer" and not args.no_extra:
+        line["workloads"] = measure_extras(args, pk)
     if world == 1 and not args.no_cpu_baseline:
-        tps, sec, cores, desc = oracle_sample(args.workload, 1)
+        tps, sec, cores, desc = oracle_sample(args.workload, 3)
         line["cpu_baseline"] = {"value": round(tps, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
                                 "sample": desc}
     print(json.dumps(line), flush=True)
