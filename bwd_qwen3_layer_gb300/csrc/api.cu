@@ -287,7 +287,12 @@ kl_status kl_device_status(void* stream, uint32_t* bits) {
   const uint32_t zero = 0;
   KL_CUDA(cudaMemcpyToSymbol(g_device_error_word, &zero, sizeof(zero)));
   if (bits) *bits = v;
-  if (v & KL_DEVERR_TIMEOUT) return set_error(KL_ERR_TIMEOUT, "a kernel wait timed out (bits 0x%x)", v);
+  if (v & KL_DEVERR_TIMEOUT) {
+    // a few-rows GEMM that gave up may have left arrival counts behind
+    const kl_status rs = skinny_cnt_reset();
+    if (rs != KL_OK) return rs;
+    return set_error(KL_ERR_TIMEOUT, "a kernel wait timed out (bits 0x%x)", v);
+  }
   if (v) return set_error(KL_ERR_DEVICE, "a kernel rejected its input (bits 0x%x)", v);
   return KL_OK;
 }

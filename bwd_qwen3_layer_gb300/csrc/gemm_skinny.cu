@@ -413,7 +413,10 @@ __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid
 
 // Arrival counters, one slot per launch, reused round-robin; each counter is
 // re-armed by the warp that finishes its rows, so a slot is all zeros again
-// once its launch has ended.
+// once its launch has ended. A launch that gave up on a wait can leave counts
+// behind; it has also set the sticky timeout bit of the device error word, and
+// skinny_cnt_reset() (called when kl_device_status reads that bit) clears every
+// slot before the next launch.
 __device__ unsigned int g_skinny_cnt[SK_CNT_SLOTS][SK_CNT_TILES * 4];
 
 unsigned int* skinny_cnt_slot() {
@@ -488,6 +491,13 @@ bool skinny_plan(const GemmSpec* s, int n, SkPlan* pl) {
 }
 
 }  // namespace
+
+kl_status skinny_cnt_reset() {
+  void* ptr = nullptr;
+  KL_CUDA(cudaGetSymbolAddress(&ptr, g_skinny_cnt));
+  KL_CUDA(cudaMemset(ptr, 0, sizeof(g_skinny_cnt)));
+  return KL_OK;
+}
 
 bool gemm_skinny_fits(const GemmSpec* specs, int nspec) {
   SkPlan pl;

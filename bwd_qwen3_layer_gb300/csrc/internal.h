@@ -94,6 +94,9 @@ kl_status gemm_bf16(const GemmSpec* specs, int nspec, cudaStream_t st, const cha
 // when gemm_skinny_fits (it also needs the problems' tail_ws as scratch).
 bool gemm_skinny_fits(const GemmSpec* specs, int nspec);
 kl_status gemm_skinny(const GemmSpec* specs, int nspec, cudaStream_t st, const char* label);
+// Zeroes the few-rows GEMM's arrival counters on the current device
+// (synchronous; used after a launch reported a timeout).
+kl_status skinny_cnt_reset();
 // fp32 operands on CUDA cores (one problem).
 kl_status gemm_f32(const GemmSpec& spec, cudaStream_t st, const char* label = "gemm_f32");
 
