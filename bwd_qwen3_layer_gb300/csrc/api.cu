@@ -504,22 +504,26 @@ kl_status kl_layer_backward(const kl_layer_cfg* cfg, const kl_layer_weights* w,
     // over each kv head's query heads) are finished below
     KL_TRY(attention_bwd_accum(D.B, D.S, D.Hq, D.Hkv, D.d, dt, s->q, s->k, s->v, s->o, s->lse, b.dO,
                                b.att, b.att_bytes, &dq_acc, &dk_acc, &dv_acc, st, d_ready,
-                               b.rope ? b.dq : nullptr, b.rope));
-    KL_TRY(rope_bwd_convert(D.B, D.S, dq_acc ? D.Hq : 0, D.Hkv, D.d, cfg->rope_base, dt, dq_acc, dk_acc, dv_acc,
-                            b.dq, b.dk, b.dv, st));
+                               b.rope ? b.dq : nullptr, b.rope, b.dk, b.dv));
+    if (dk_acc)   // fp32: the accumulators are rotated back and stored here
+      KL_TRY(rope_bwd_convert(D.B, D.S, dq_acc ? D.Hq : 0, D.Hkv, D.d, cfg->rope_base, dt, dq_acc, dk_acc, dv_acc,
+                              b.dq, b.dk, b.dv, st));
   } else {
     // layer options: dQ (bf16, still rotated, in b.dq) or its fp32 accumulator, then the
     // rotation back and the per-head norm backward for q and k; dV converted
     KL_TRY(attention_bwd_accum(D.B, D.S, D.Hq, D.Hkv, D.d, dt, s->q, s->k, s->v, s->o, s->lse, b.dO,
                                b.att, b.att_bytes, &dq_acc, &dk_acc, &dv_acc, st, d_ready,
-                               dt == KL_BF16 ? b.dq : nullptr, nullptr));
+                               dt == KL_BF16 ? b.dq : nullptr, nullptr, b.dk, b.dv));
+    // bf16: dQ and dK (still rotated) are read from and rewritten in place in b.dq, b.dk
     const void* dqr = dq_acc ? static_cast<const void*>(dq_acc) : b.dq;
     KL_TRY(qk_rope_bwd(T, D.Hq, D.S, D.d, dt, dqr, dq_acc ? KL_F32 : KL_BF16, s->q_pre, w->gamma_q, s->rstd_q,
                        D.qk_norm, D.inter, cfg->rope_base, b.rope, b.dq, static_cast<float*>(gr->gamma_q), b.qk_q,
                        b.qk_q_bytes, st));
-    KL_TRY(qk_rope_bwd(T, D.Hkv, D.S, D.d, dt, dk_acc, KL_F32, s->k_pre, w->gamma_k, s->rstd_k, D.qk_norm, D.inter,
-                       cfg->rope_base, b.rope, b.dk, static_cast<float*>(gr->gamma_k), b.qk_k, b.qk_k_bytes, st));
-    KL_TRY(convert_f32(static_cast<int64_t>(T) * D.Dkv, dt, dv_acc, b.dv, st));
+    const void* dkr = dk_acc ? static_cast<const void*>(dk_acc) : b.dk;
+    KL_TRY(qk_rope_bwd(T, D.Hkv, D.S, D.d, dt, dkr, dk_acc ? KL_F32 : KL_BF16, s->k_pre, w->gamma_k, s->rstd_k,
+                       D.qk_norm, D.inter, cfg->rope_base, b.rope, b.dk, static_cast<float*>(gr->gamma_k), b.qk_k,
+                       b.qk_k_bytes, st));
+    if (dv_acc) KL_TRY(convert_f32(static_cast<int64_t>(T) * D.Dkv, dt, dv_acc, b.dv, st));
   }
   {
     GemmSpec dh = dgrad(T, H, D.Dq, b.dq, w->wq, b.dh1, KL_F32);
@@ -556,7 +560,7 @@ size_t kl_lmhead_workspace_bytes(const kl_lmhead_cfg* c) {
   if (check_lm(c) != KL_OK) return 0;
   const size_t NV = static_cast<size_t>(c->N) * c->V;
   return align_up(NV * 4, 256) + align_up(NV * dtype_size(c->dtype), 256) + ce_ws(c->N) +
-         align_up(static_cast<size_t>(c->N) * c->H * 4, 256) + (c->dtype == KL_BF16 ? gemm_tail_ws_bytes() : 0);
+         (c->dtype == KL_BF16 ? gemm_tail_ws_bytes() : 0);
 }
 
 kl_status kl_lmhead_ce_argmax(const kl_lmhead_cfg* c, const void* X, const void* W,
@@ -577,7 +581,6 @@ kl_status kl_lmhead_ce_argmax(const kl_lmhead_cfg* c, const void* X, const void*
   float* z = static_cast<float*>(cv.take(NV * 4));
   void* dz_ws = cv.take(NV * dtype_size(dt));
   void* ce = cv.take(ce_ws(N));
-  float* dx_acc = static_cast<float*>(cv.take(static_cast<size_t>(N) * H * 4));
   const size_t tail_bytes = dt == KL_BF16 ? gemm_tail_ws_bytes() : 0;
   void* tail = tail_bytes ? cv.take(tail_bytes) : nullptr;
   void* dz = dlogits ? dlogits : dz_ws;
@@ -589,7 +592,6 @@ kl_status kl_lmhead_ce_argmax(const kl_lmhead_cfg* c, const void* X, const void*
   KL_TRY(ce_argmax(N, V, z, targets, loss, argmax, dz, dt, ce, ce_ws(N), st));
   {
     GemmSpec g[2] = {dgrad(N, H, V, dz, W, dX, dt), wgrad(V, H, N, dz, X, dW, c->dw_dtype)};
-    g[0].acc_ws = dx_acc;   // K = V is long: split it, accumulate in fp32
     with_tail(g, 2, tail, tail_bytes);
     KL_TRY(run_gemms(dt, g, 2, st, "gemm.lm_bwd"));
   }
@@ -690,12 +692,14 @@ kl_status kl_attention_bwd(int32_t B, int32_t S, int32_t Hq, int32_t Hkv, int32_
   if (!dq || !dk || !dv) return set_error(KL_ERR_INVALID_ARG, "attention_bwd: null output");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   float *dq_acc = nullptr, *dk_acc = nullptr, *dv_acc = nullptr;
+  const bool bf = dtype == KL_BF16;
   KL_TRY(attention_bwd_accum(B, S, Hq, Hkv, d, dtype, q, k, v, o, lse, dout, ws, ws_bytes, &dq_acc,
-                             &dk_acc, &dv_acc, st, false, dtype == KL_BF16 ? dq : nullptr));
+                             &dk_acc, &dv_acc, st, false, bf ? dq : nullptr, nullptr, bf ? dk : nullptr,
+                             bf ? dv : nullptr));
   const int64_t T = static_cast<int64_t>(B) * S;
   if (dq_acc) KL_TRY(convert_f32(T * Hq * d, dtype, dq_acc, dq, st));
-  KL_TRY(convert_f32(T * Hkv * d, dtype, dk_acc, dk, st));
-  KL_TRY(convert_f32(T * Hkv * d, dtype, dv_acc, dv, st));
+  if (dk_acc) KL_TRY(convert_f32(T * Hkv * d, dtype, dk_acc, dk, st));
+  if (dv_acc) KL_TRY(convert_f32(T * Hkv * d, dtype, dv_acc, dv, st));
   return KL_OK;
 }
 

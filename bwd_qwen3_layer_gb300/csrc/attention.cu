@@ -265,7 +265,8 @@ kl_status attention_bwd_accum(int B, int S, int Hq, int Hkv, int d, int dtype, c
                               const void* k, const void* v, const void* o, const float* lse,
                               const void* dout, void* ws, size_t ws_bytes, float** dq_acc,
                               float** dk_acc, float** dv_acc, cudaStream_t st,
-                              bool d_ready, void* dq_out, const float2* rope_cs) {
+                              bool d_ready, void* dq_out, const float2* rope_cs, void* dk_out,
+                              void* dv_out) {
   KL_TRY(check_args(B, S, Hq, Hkv, d, dtype));
   if (!q || !k || !v || !o || !lse || !dout)
     return set_error(KL_ERR_INVALID_ARG, "attention_bwd: null pointer");
@@ -300,8 +301,7 @@ kl_status attention_bwd_accum(int B, int S, int Hq, int Hkv, int d, int dtype, c
   } else {
     if (!al16(q) || !al16(k) || !al16(v) || !al16(o) || !al16(dout))
       return set_error(KL_ERR_INVALID_ARG, "attention_bwd: bf16 buffers must be 16-byte aligned");
-    KL_CUDA(cudaMemsetAsync(dk, 0, T * Hkv * d * 4, st));
-    KL_CUDA(cudaMemsetAsync(dv, 0, T * Hkv * d * 4, st));
+    if (!dq_out || !dk_out || !dv_out) return set_error(KL_ERR_INVALID_ARG, "attention_bwd: null output");
     const int64_t rows = static_cast<int64_t>(T) * Hq;
     if (!d_ready) {
       ProfScope ps("attn_bwd_pre_bf16", st, 0.0, 4.0 * T * Hq * d + 4.0 * T * Hq);
@@ -309,9 +309,9 @@ kl_status attention_bwd_accum(int B, int S, int Hq, int Hkv, int d, int dtype, c
           B, S, Hq, (const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, Dd);
       KL_CUDA(cudaGetLastError());
     }
-    if (dq_out && !al16(dq_out)) return set_error(KL_ERR_INVALID_ARG, "attention_bwd: dq not 16-byte aligned");
-    KL_TRY(attention_bwd_tc(B, S, Hq, Hkv, q, k, v, dout, lse, Dd, dq, dk, dv, st, dq_out, rope_cs));
-    if (dq_out) *dq_acc = nullptr;
+    if (!al16(dq_out)) return set_error(KL_ERR_INVALID_ARG, "attention_bwd: dq not 16-byte aligned");
+    KL_TRY(attention_bwd_tc(B, S, Hq, Hkv, q, k, v, dout, lse, Dd, nullptr, dq_out, dk_out, dv_out, rope_cs, st));
+    *dq_acc = *dk_acc = *dv_acc = nullptr;
   }
   KL_CUDA(cudaGetLastError());
   return KL_OK;

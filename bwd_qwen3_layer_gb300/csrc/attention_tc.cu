@@ -24,6 +24,7 @@
 // Every wait is bounded; a timeout records KL_DEVERR_TIMEOUT and unwinds.
 #include <cudaTypedefs.h>
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <type_traits>
@@ -713,28 +714,36 @@ __device__ __forceinline__ uint64_t desc_mn128(uint32_t base, uint32_t block_byt
   return smem_desc_sw128(base + kk * 2048, block_bytes, 1024);
 }
 
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-
 struct BwdParams {
   CUtensorMap tmQ, tmK, tmV, tmdO;   // box rows: see the kernels
   const float* lse;                  // [B, Hq, S]
   const float* Dd;                   // [B, Hq, S]
   float* dq_acc;                     // [T, Hq*128] fp32 (when dq_out is null)
   __nv_bfloat16* dq_out;             // [T, Hq*128] bf16 final dQ, or null
-  const float2* rope_cs;             // [S][64] cos/sin: dQ turned back by -angle (with dq_out), or null
-  float* dk_acc;                     // [T, Hkv*128]
-  float* dv_acc;                     // [T, Hkv*128]
+  __nv_bfloat16* dk_out;             // [T, Hkv*128] bf16 final dK
+  __nv_bfloat16* dv_out;             // [T, Hkv*128] bf16 final dV
+  const float2* rope_cs;             // [S][64] cos/sin: dQ (with dq_out) and dK turned back by -angle, or null
   int S, Hq, Hkv;
+  int nsplit;                        // CTAs (one cluster) sharing a kv head's key tile; heads split between them
   float scale_log2, scale;
   uint32_t* err;
 };
 
 // ---------------------------------------------------------------------------
-// dK / dV
+// dK / dV, one CTA per (kv head, 128-key tile) walking its query-head group
 // ---------------------------------------------------------------------------
+// The kv head's K and V tiles are loaded once; the CTA then steps through
+// 64-query tiles of every query head of its share of the group (each head from
+// the diagonal to the end of the sequence) with dV and dK accumulating in TMEM
+// across all of them. When the group is split over a cluster of nsplit CTAs
+// (short sequences: the causal work per key tile is uneven and few tiles
+// exist), the CTAs' partial sums meet in distributed shared memory: CTA o owns
+// head-dim columns [W o, W o + W) and [64 + W o, ...) (W = 64 / nsplit, so a
+// rotary plane's two columns stay together) and adds the nsplit partials of
+// those columns in rank order. dK (times the softmax scale, turned back by the
+// key position's rotary angle when a table is given) and dV are written once,
+// as bf16: no atomics, and the same bits on every run.
+//
 // Four Q / dO stages let the scores of a step go out two steps ahead of its
 // gradients; they fit because P^T / dS^T are single-buffered (each elementwise
 // warp holds a step's packed values in registers until the previous step's
@@ -752,13 +761,126 @@ constexpr uint32_t KV_OFF_DS = KV_OFF_P + PT_BYTES;          // dS^T
 constexpr uint32_t KV_OFF_STAT = KV_OFF_DS + PT_BYTES;      // KV_QS stages: lse[64], D[64] (fp32)
 constexpr uint32_t KV_OFF_BAR = KV_OFF_STAT + KV_QS * 512;
 constexpr size_t KV_SMEM = KV_OFF_BAR + 256;
+// The partial-sum exchange reuses K, V and the Q / dO ring: nsplit slots of
+// 128 rows x 4W fp32 (dV low, dV high, dK low, dK high columns) = 128 KB.
+constexpr uint32_t KV_OFF_XCH = 0;
+constexpr uint32_t KV_XCH_BYTES = 128 * 256 * 4;
+static_assert(KV_XCH_BYTES <= KV_OFF_P, "exchange slots overlap the P^T buffer");
 static_assert(KV_SMEM <= 232448, "dK/dV shared memory above the per-CTA limit");
+
+// Writes one key row's finished dV or dK columns [c0, c0 + W) and [64 + c0, ...)
+// as bf16 (dK: times the scale, turned back by the key position's rotary angle).
+template <int W>
+__device__ __forceinline__ void dkdv_store_row(__nv_bfloat16* row, int c0, const float (&lo)[W],
+                                               const float (&hi)[W], bool is_k, float scale,
+                                               const float2* cs) {
+  float a[W], bb[W];
+#pragma unroll
+  for (int e = 0; e < W; ++e) {
+    if (is_k) {
+      const float x = lo[e] * scale, y = hi[e] * scale;
+      if (cs) {
+        const float2 t = cs[c0 + e];
+        a[e] = x * t.x + y * t.y;
+        bb[e] = y * t.x - x * t.y;
+      } else {
+        a[e] = x;
+        bb[e] = y;
+      }
+    } else {
+      a[e] = lo[e];
+      bb[e] = hi[e];
+    }
+  }
+#pragma unroll
+  for (int e = 0; e < W; e += 8) {
+    uint4 wa, wb;
+    wa.x = pack_bf16x2(a[e], a[e + 1]); wa.y = pack_bf16x2(a[e + 2], a[e + 3]);
+    wa.z = pack_bf16x2(a[e + 4], a[e + 5]); wa.w = pack_bf16x2(a[e + 6], a[e + 7]);
+    wb.x = pack_bf16x2(bb[e], bb[e + 1]); wb.y = pack_bf16x2(bb[e + 2], bb[e + 3]);
+    wb.z = pack_bf16x2(bb[e + 4], bb[e + 5]); wb.w = pack_bf16x2(bb[e + 6], bb[e + 7]);
+    *reinterpret_cast<uint4*>(row + c0 + e) = wa;
+    *reinterpret_cast<uint4*>(row + 64 + c0 + e) = wb;
+  }
+}
+
+// TMEM columns [col, col + W) of this warp's 32 lanes (W = 16, 32 or 64).
+template <int W>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[W]) {
+  if constexpr (W == 16) {
+    uint32_t r[16];
+    tmem_ld_32x32b_x16(taddr, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
+  } else {
+#pragma unroll
+    for (int c = 0; c < W; c += 32) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(taddr + c, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[c + e] = __uint_as_float(r[e]);
+    }
+  }
+}
+
+// The end of the dK/dV kernel for one elementwise thread: key row r (TMEM lane),
+// matrix is_k (dK at TMEM column 384, else dV at 256). With a cluster, the
+// thread first sends its row's columns of every owner to that owner's slot
+// `rank` (between the two cluster barriers the caller places around it), then
+// adds its own columns' slots in rank order.
+template <int W>
+__device__ __forceinline__ void dkdv_send(uint32_t tmem_row, uint32_t sb, int r, bool is_k, int nsplit,
+                                          uint32_t rank) {
+  const uint32_t slot_bytes = 128u * 16u * W;
+  for (int o = 0; o < nsplit; ++o) {
+    float lo[W], hi[W];
+    tmem_ld_cols<W>(tmem_row + W * o, lo);
+    tmem_ld_cols<W>(tmem_row + 64 + W * o, hi);
+    // row r of slot `rank`: 4W floats (dV lo, dV hi, dK lo, dK hi), 16-byte granules XOR-swizzled by row
+    const uint32_t rowb = sb + KV_OFF_XCH + rank * slot_bytes + static_cast<uint32_t>(r) * 16u * W;
+    const uint32_t dst = mapa_shared(rowb, static_cast<uint32_t>(o));
+#pragma unroll
+    for (int g = 0; g < W / 4; ++g) {
+      const int ga = (is_k ? W / 2 : 0) + g, gb = (is_k ? W / 2 : 0) + W / 4 + g;
+      st_cluster_v4(dst + ((ga ^ (r & 7)) << 4), lo[4 * g], lo[4 * g + 1], lo[4 * g + 2], lo[4 * g + 3]);
+      st_cluster_v4(dst + ((gb ^ (r & 7)) << 4), hi[4 * g], hi[4 * g + 1], hi[4 * g + 2], hi[4 * g + 3]);
+    }
+  }
+}
+
+template <int W>
+__device__ __forceinline__ void dkdv_reduce_store(const uint8_t* smem, int r, bool is_k, int nsplit, uint32_t rank,
+                                                  __nv_bfloat16* row, float scale, const float2* cs) {
+  const uint32_t slot_bytes = 128u * 16u * W;
+  float lo[W], hi[W];
+#pragma unroll
+  for (int e = 0; e < W; ++e) lo[e] = hi[e] = 0.f;
+  for (int s = 0; s < nsplit; ++s) {
+    const uint8_t* rowp = smem + KV_OFF_XCH + s * slot_bytes + static_cast<uint32_t>(r) * 16u * W;
+#pragma unroll
+    for (int g = 0; g < W / 4; ++g) {
+      const int ga = (is_k ? W / 2 : 0) + g, gb = (is_k ? W / 2 : 0) + W / 4 + g;
+      const float4 a = *reinterpret_cast<const float4*>(rowp + ((ga ^ (r & 7)) << 4));
+      const float4 b = *reinterpret_cast<const float4*>(rowp + ((gb ^ (r & 7)) << 4));
+      lo[4 * g] += a.x; lo[4 * g + 1] += a.y; lo[4 * g + 2] += a.z; lo[4 * g + 3] += a.w;
+      hi[4 * g] += b.x; hi[4 * g + 1] += b.y; hi[4 * g + 2] += b.z; hi[4 * g + 3] += b.w;
+    }
+  }
+  if (row) dkdv_store_row<W>(row, W * static_cast<int>(rank), lo, hi, is_k, scale, cs);
+}
 
 __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid_constant__ BwdParams p) {
   pdl_enter();
   extern __shared__ __align__(1024) uint8_t kv_smem_raw[];
+  const int nsplit = p.nsplit;
   if (smem_u32(kv_smem_raw) & 1023u) {   // the layout has no alignment slack (CTA-uniform exit)
     if (threadIdx.x == 0) record_error(p.err, KL_DEVERR_SMEM);
+    if (nsplit > 1) {                    // the cluster's barriers still see every thread
+      cluster_sync_all();
+      cluster_sync_all();
+    }
     return;
   }
   uint8_t* smem = kv_smem_raw;
@@ -777,11 +899,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kb = blockIdx.y;                 // key tiles near the start see the most queries
-  const int h = blockIdx.x, b = blockIdx.z;
-  const int jh = h * p.Hkv / p.Hq;
+  const int jh = static_cast<int>(blockIdx.x) / nsplit, b = blockIdx.z;
+  const uint32_t rank = nsplit > 1 ? cluster_ctarank() : 0u;
+  const int G = p.Hq / p.Hkv;                // query heads of the kv head
+  const int gh = G / nsplit;                 // of them, this CTA's
+  const int h_first = jh * G + static_cast<int>(rank) * gh;
   const int k0 = kb * BKV;
   const int row0 = b * p.S;
-  const int nit = (p.S - k0 + 63) / 64;      // 64-query tiles from the diagonal to the end
+  const int nit = (p.S - k0 + 63) / 64;      // 64-query tiles from the diagonal to the end, per head
+  const int nsteps = gh * nit;               // step g: head h_first + g / nit, query tile g % nit
   // lse / D rows staged in shared memory by bulk copies when they are 16-byte aligned
   const bool stat_smem = (p.S & 3) == 0 && (reinterpret_cast<uintptr_t>(p.lse) & 15u) == 0 &&
                          (reinterpret_cast<uintptr_t>(p.Dd) & 15u) == 0;
@@ -810,6 +936,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  bool fin = false;                          // elementwise warps: every MMA of the CTA completed
 
   if (warp == 0) {
     // ---------------- TMA (whole warp; the elected lane issues) ----------------
@@ -823,18 +950,20 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
     }
     __syncwarp();
     int issued = 0;
-    for (int it = 0; it < nit; ++it) {
-      const int s = it % KV_QS;
-      const uint32_t ph = (it / KV_QS) & 1;
+    for (int g = 0; g < nsteps; ++g) {
+      const int s = g % KV_QS;
+      const uint32_t ph = (g / KV_QS) & 1;
       if (!mbar_wait_warp(q_free(s), ph ^ 1u, p.err, abort_flag)) { *abort_flag = 1; break; }
-      const int qr = row0 + k0 + it * 64;
+      const int h = h_first + g / nit;
+      const int q0 = k0 + (g % nit) * 64;
+      const int qr = row0 + q0;
       if (el) {
         // lse and D of the tile's queries (those inside the sequence) ride with Q and dO
-        const int nq = p.S - (k0 + it * 64) < 64 ? p.S - (k0 + it * 64) : 64;
+        const int nq = p.S - q0 < 64 ? p.S - q0 : 64;
         const uint32_t stat_bytes = stat_smem ? static_cast<uint32_t>(nq) * 4u : 0u;
         mbar_arrive_expect_tx(q_full(s), 2 * T64 + 2 * stat_bytes);
         if (stat_smem) {
-          const int64_t so = (static_cast<int64_t>(b) * p.Hq + h) * p.S + k0 + it * 64;
+          const int64_t so = (static_cast<int64_t>(b) * p.Hq + h) * p.S + q0;
           bulk_copy_g2s(sb + KV_OFF_STAT + s * 512, p.lse + so, stat_bytes, q_full(s));
           bulk_copy_g2s(sb + KV_OFF_STAT + s * 512 + 256, p.Dd + so, stat_bytes, q_full(s));
         }
@@ -847,8 +976,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
       ++issued;
     }
     mbar_wait(kv_full, 0, p.err);
-    for (int it = (issued > KV_QS ? issued - KV_QS : 0); it < issued; ++it)
-      mbar_wait(q_full(it % KV_QS), (it / KV_QS) & 1, p.err);
+    for (int g = (issued > KV_QS ? issued - KV_QS : 0); g < issued; ++g)
+      mbar_wait(q_full(g % KV_QS), (g / KV_QS) & 1, p.err);
   } else if (warp == 1) {
     // ---------------- MMA (the elected lane issues) ----------------
     // S^T / dP^T of step j go out as soon as their TMEM buffer (j & 1) is free
@@ -864,7 +993,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
       int ns = 0, ng = 0;          // next step whose S^T / dP^T, whose gradients, go out
       uint32_t idle = 0;
       uint64_t since = 0;
-      while (ng < nit) {
+      while (ng < nsteps) {
         bool prog = false;
         if (ng < ns && mbar_test_wait(p_full, ng & 1)) {
           tc_fence_after();
@@ -881,7 +1010,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
           ++ng;
           prog = true;
         }
-        if (ns < nit && mbar_test_wait(q_full(ns % KV_QS), (ns / KV_QS) & 1) &&
+        if (ns < nsteps && mbar_test_wait(q_full(ns % KV_QS), (ns / KV_QS) & 1) &&
             (ns < 2 || mbar_test_wait(st_free(ns & 1), ((ns >> 1) & 1) ^ 1u))) {
           tc_fence_after();
           const int ss = ns & 1, qs = ns % KV_QS;
@@ -923,7 +1052,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
     __syncwarp();
     mbar_wait(done, 0, p.err);
   } else if (warp >= 2) {
-    // ---------------- P^T, dS^T (thread = key row) and the final dK/dV ----------------
+    // ---------------- P^T, dS^T (thread = key row) ----------------
     // warp 2 + 4 * half + i: lane quarter (warp & 3), queries 32 * half .. + 31 of a step
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
@@ -931,14 +1060,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
     const int r = quarter * 32 + lane;
     const int key = k0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const float* lrow = p.lse + (static_cast<int64_t>(b) * p.Hq + h) * p.S;
-    const float* drow = p.Dd + (static_cast<int64_t>(b) * p.Hq + h) * p.S;
     const bool vec_stat = (p.S & 3) == 0;     // rows of lse / D are 16-byte aligned
     bool ok = true;
-    for (int it = 0; it < nit; ++it) {
-      const int s = it & 1;
-      const uint32_t ph = (it >> 1) & 1;
-      const int q0 = k0 + it * 64;
+    for (int g = 0; g < nsteps; ++g) {
+      const int s = g & 1;
+      const uint32_t ph = (g >> 1) & 1;
+      const int h = h_first + g / nit;
+      const int q0 = k0 + (g % nit) * 64;
+      const float* lrow = p.lse + (static_cast<int64_t>(b) * p.Hq + h) * p.S;
+      const float* drow = p.Dd + (static_cast<int64_t>(b) * p.Hq + h) * p.S;
       if (!mbar_wait_warp(st_full(s), ph, p.err, abort_flag)) { ok = false; break; }
       tc_fence_after();
       uint32_t sv[32], dv[32];
@@ -953,11 +1083,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
       uint8_t* drw = smem + KV_OFF_DS + r * 128;
       uint4 pst[4], dst[4];                  // this warp's 4 chunks of the row, until the buffer is free
       // the stage's lse / D copies completed with its Q / dO (q_full), before S^T
-      if (stat_smem && !mbar_wait_warp(q_full(it % KV_QS), (it / KV_QS) & 1, p.err, abort_flag)) {
+      if (stat_smem && !mbar_wait_warp(q_full(g % KV_QS), (g / KV_QS) & 1, p.err, abort_flag)) {
         ok = false;
         break;
       }
-      const float* sl = reinterpret_cast<const float*>(smem + KV_OFF_STAT + (it % KV_QS) * 512);
+      const float* sl = reinterpret_cast<const float*>(smem + KV_OFF_STAT + (g % KV_QS) * 512);
       // the causal mask only reaches the steps at the diagonal: the others take the unmasked body
       auto step = [&](auto masked) {
       constexpr bool MASK = decltype(masked)::value;
@@ -1017,7 +1147,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
       if (__any_sync(0xffffffffu, lim > col0)) step(std::true_type{});
       else step(std::false_type{});
       // the buffer is free once the previous step's gradient products completed
-      if (it >= 1 && !mbar_wait_warp(p_free, (it - 1) & 1, p.err, abort_flag)) { ok = false; break; }
+      if (g >= 1 && !mbar_wait_warp(p_free, (g - 1) & 1, p.err, abort_flag)) { ok = false; break; }
 #pragma unroll
       for (int c8l = 0; c8l < 4; ++c8l) {
         const int off = (((half * 4 + c8l) ^ (r & 7)) << 4);
@@ -1028,36 +1158,48 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
-    // The TMEM loads are warp-collective: every lane takes part; only rows
-    // inside the sequence add their results.
-    if (ok && mbar_wait_warp(done, 0, p.err, abort_flag)) {
-      tc_fence_after();
-      const bool in = key < p.S;
-      const int64_t o = (static_cast<int64_t>(row0 + (in ? key : 0)) * p.Hkv + jh) * HD;
+    fin = ok && mbar_wait_warp(done, 0, p.err, abort_flag);
+    if (!fin) *abort_flag = 1;
+    if (fin) tc_fence_after();
+  }
+
+  // ---------------- dK, dV: written once, as bf16 ----------------
+  // Elementwise warp 2 + 4 * half + i: key row r = its TMEM lane; half 0 finishes
+  // dV, half 1 dK. The TMEM loads are warp-collective: every lane takes part,
+  // only rows inside the sequence store.
+  const int quarter = warp & 3;
+  const int r = quarter * 32 + lane;
+  const int key = k0 + r;
+  const bool is_k = warp >= 6;
+  const uint32_t tmem_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + (is_k ? 384u : 256u);
+  __nv_bfloat16* orow = nullptr;
+  const float2* cs = nullptr;
+  if (warp >= 2 && key < p.S) {
+    orow = (is_k ? p.dk_out : p.dv_out) + (static_cast<int64_t>(row0 + key) * p.Hkv + jh) * HD;
+    if (is_k && p.rope_cs) cs = p.rope_cs + static_cast<int64_t>(key) * 64;
+  }
+  if (nsplit == 1) {
+    if (fin) {
+      float lo[32], hi[32];
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = half * 2 + cc;   // this warp's 64 of the 128 head columns
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + 256 + c * 32, v);
-        tmem_ld_wait();
-        if (in) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            red_add_v4(p.dv_acc + o + c * 32 + e, __uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                       __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
-        }
-        tmem_ld_32x32b_x32(tmem + lane_off + 384 + c * 32, v);
-        tmem_ld_wait();
-        if (in) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            red_add_v4(p.dk_acc + o + c * 32 + e, __uint_as_float(v[e]) * p.scale,
-                       __uint_as_float(v[e + 1]) * p.scale, __uint_as_float(v[e + 2]) * p.scale,
-                       __uint_as_float(v[e + 3]) * p.scale);
-        }
+      for (int c = 0; c < 64; c += 32) {
+        tmem_ld_cols<32>(tmem_row + c, lo);
+        tmem_ld_cols<32>(tmem_row + 64 + c, hi);
+        if (orow) dkdv_store_row<32>(orow, c, lo, hi, is_k, p.scale, cs);
       }
-    } else {
-      *abort_flag = 1;
+    }
+  } else {
+    // every CTA of the cluster has finished its MMAs and copies: the K, V and
+    // Q / dO buffers are free to take the partial sums
+    cluster_sync_all();
+    if (warp >= 2 && fin) {
+      if (nsplit == 2) dkdv_send<32>(tmem_row, sb, r, is_k, 2, rank);
+      else dkdv_send<16>(tmem_row, sb, r, is_k, 4, rank);
+    }
+    cluster_sync_all();
+    if (warp >= 2 && fin) {
+      if (nsplit == 2) dkdv_reduce_store<32>(smem, r, is_k, 2, rank, orow, p.scale, cs);
+      else dkdv_reduce_store<16>(smem, r, is_k, 4, rank, orow, p.scale, cs);
     }
   }
   tc_fence_before();
@@ -1421,9 +1563,35 @@ kl_status attention_fwd_tc(int B, int S, int Hq, int Hkv, const void* q, const v
 
 namespace kl {
 
+int attention_dkdv_split(int B, int S, int Hq, int Hkv, int sms) {
+  // Causal work per (head, key tile kb): ceil((S - 128 kb) / 64) query steps.
+  // Split a kv head's query-head group over 2 or 4 CTAs of a cluster until the
+  // longest key tile's share is at most 1.2x the mean work per SM (measured at
+  // 2048 tokens, 64 / 8 heads: 0.309 ms unsplit, 0.179 ms in pairs, 0.233 ms
+  // in fours); long sequences stay unsplit.
+  const int G = Hq / Hkv;
+  const int nkb = (S + BKV - 1) / BKV;
+  double total = 0.0;
+  for (int kb = 0; kb < nkb; ++kb) total += (S - kb * BKV + 63) / 64;
+  total *= static_cast<double>(B) * Hq;
+  const double per_sm = total / (sms > 0 ? sms : 1);
+  const int nit0 = (S + 63) / 64;
+  int best = 1;
+  for (int n = 1; n <= 4; n *= 2) {
+    if (G % n) continue;
+    best = n;
+    if (static_cast<double>(G / n) * nit0 <= 1.2 * per_sm) break;
+  }
+  return best;
+}
+
 kl_status attention_bwd_tc(int B, int S, int Hq, int Hkv, const void* q, const void* k, const void* v,
-                           const void* dout, const float* lse, const float* Dd, float* dq_acc, float* dk_acc,
-                           float* dv_acc, cudaStream_t st, void* dq_out, const float2* rope_cs) {
+                           const void* dout, const float* lse, const float* Dd, float* dq_acc, void* dq_out,
+                           void* dk_out, void* dv_out, const float2* rope_cs, cudaStream_t st) {
+  if (!dk_out || !dv_out || (!dq_out && !dq_acc))
+    return set_error(KL_ERR_INVALID_ARG, "attention_bwd: null output");
+  if (((reinterpret_cast<uintptr_t>(dk_out) | reinterpret_cast<uintptr_t>(dv_out)) & 15u) != 0)
+    return set_error(KL_ERR_INVALID_ARG, "attention_bwd: dk / dv not 16-byte aligned");
   const uint64_t T = static_cast<uint64_t>(B) * S;
   static uint64_t attr_done = 0;
   int dev = 0;
@@ -1441,12 +1609,18 @@ kl_status attention_bwd_tc(int B, int S, int Hq, int Hkv, const void* q, const v
   p.Dd = Dd;
   p.dq_acc = dq_acc;
   p.dq_out = static_cast<__nv_bfloat16*>(dq_out);
-  p.rope_cs = dq_out ? rope_cs : nullptr;
-  p.dk_acc = dk_acc;
-  p.dv_acc = dv_acc;
+  p.dk_out = static_cast<__nv_bfloat16*>(dk_out);
+  p.dv_out = static_cast<__nv_bfloat16*>(dv_out);
+  p.rope_cs = rope_cs;
   p.S = S;
   p.Hq = Hq;
   p.Hkv = Hkv;
+  p.nsplit = attention_dkdv_split(B, S, Hq, Hkv, num_sms());
+  // tuning override: KL_ATTN_DKDV_SPLIT = 1, 2 or 4 (a divisor of the query-head group)
+  if (const char* e = getenv("KL_ATTN_DKDV_SPLIT")) {
+    const int v = atoi(e);
+    if ((v == 1 || v == 2 || v == 4) && (Hq / Hkv) % v == 0) p.nsplit = v;
+  }
   p.scale_log2 = LOG2E_F / sqrtf(static_cast<float>(HD));
   p.scale = 1.0f / sqrtf(static_cast<float>(HD));
   p.err = device_error_word();
@@ -1458,8 +1632,21 @@ kl_status attention_bwd_tc(int B, int S, int Hq, int Hkv, const void* q, const v
   KL_TRY(map_rows(&p.tmdO, dout, static_cast<uint64_t>(Hq) * HD, T, 64));
   {
     ProfScope ps("attn_bwd_dkdv_tc", st, 8.0 * B * Hq * HD * pairs, 0.0);
-    dim3 grid(Hq, (S + BKV - 1) / BKV, B);
-    launch_pdl(fa_bwd_dkdv_tc_kernel, grid, BWD_THREADS, KV_SMEM, st, p);   // shared memory checked in-kernel
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_enter
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(p.nsplit);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(Hkv * p.nsplit, (S + BKV - 1) / BKV, B);
+    cfg.blockDim = dim3(BWD_THREADS);
+    cfg.dynamicSmemBytes = KV_SMEM;                                    // alignment checked in-kernel
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.nsplit > 1 ? 2 : 1;
+    KL_CUDA(cudaLaunchKernelEx(&cfg, fa_bwd_dkdv_tc_kernel, p));
   }
   KL_CUDA(cudaGetLastError());
   // dQ: Q and dO tiles of 128 rows, K and V tiles of 64 rows

@@ -34,9 +34,6 @@ struct GemmSpec {
   const void* R = nullptr;  // optional addend, [M,N] with row stride ldr
   int64_t ldr = 0;
   int r_dtype = KL_BF16;
-  // Optional fp32 [M,N] scratch: lets a long-K problem with a bf16 output or
-  // an addend be split along K (accumulated here, then finished into C).
-  float* acc_ws = nullptr;
   // Epilogue variant (bf16 operands and outputs, one segment, no addend, no K
   // split); every extra tensor is [M, N] with row stride ldc:
   //   GEMM_EPI_SWIGLU      B = gate weights, B2 = up weights ([N, K] both):
@@ -161,27 +158,32 @@ kl_status attention_fwd(int B, int S, int Hq, int Hkv, int d, int dtype, const v
 // bf16, head dim 128, on the tcgen05 tensor cores (attention_tc.cu).
 kl_status attention_fwd_tc(int B, int S, int Hq, int Hkv, const void* q, const void* k, const void* v,
                            void* o, float* lse, cudaStream_t st);
-// Backward on the tcgen05 tensor cores: dq_acc fully written; dk_acc, dv_acc
-// accumulated (zeroed by the caller).
+// Backward on the tcgen05 tensor cores. dK and dV (summed over each kv head's
+// query heads) are written once as bf16 into dk_out / dv_out; dQ as bf16 into
+// dq_out or, when that is null, as fp32 into dq_acc. With rope_cs ([S][64]
+// cos/sin) dQ (bf16) and dK leave turned back by the rotary angle.
 kl_status attention_bwd_tc(int B, int S, int Hq, int Hkv, const void* q, const void* k, const void* v,
-                           const void* dout, const float* lse, const float* Dd, float* dq_acc, float* dk_acc,
-                           float* dv_acc, cudaStream_t st,
-                           void* dq_out = nullptr, const float2* rope_cs = nullptr);
+                           const void* dout, const float* lse, const float* Dd, float* dq_acc, void* dq_out,
+                           void* dk_out, void* dv_out, const float2* rope_cs, cudaStream_t st);
+// CTAs (a cluster) that share one kv head's key tile in the dK/dV kernel.
+int attention_dkdv_split(int B, int S, int Hq, int Hkv, int sms);
 size_t attention_bwd_ws(int B, int S, int Hq, int Hkv, int d);
-// dq_out/dk_out/dv_out: fp32 accumulators [T,H*d] written by the kernel
-// (inside ws); the caller converts (with rotary backward) afterwards. With
-// dq_out (bf16, tensor-core path) dQ is written there directly instead, turned
-// back by the rotary angles of rope_cs ([S][d/2] cos/sin) when that is given,
-// and *dq_acc is null. The
-// workspace starts with D = rowsum(dO * O) as fp32 [B, Hq, S]; d_ready (bf16)
-// means the caller has already written it there (attention_bwd_d_rows).
+// fp32: dQ, dK, dV as fp32 accumulators [T, H*d] inside ws (*dq_acc, *dk_acc,
+// *dv_acc); the caller converts them (with the rotary backward) afterwards.
+// bf16 (tensor cores): dK and dV go straight to dk_out / dv_out as bf16 and dQ
+// to dq_out (required), dQ and dK turned back by the rotary angles of rope_cs
+// ([S][d/2] cos/sin) when that is given; the three accumulator pointers are
+// null. The workspace starts with D = rowsum(dO * O) as fp32 [B, Hq, S];
+// d_ready (bf16) means the caller has already written it there
+// (attention_bwd_d_rows).
 inline float* attention_bwd_d_rows(void* ws) { return static_cast<float*>(ws); }
 kl_status attention_bwd_accum(int B, int S, int Hq, int Hkv, int d, int dtype, const void* q,
                               const void* k, const void* v, const void* o, const float* lse,
                               const void* dout, void* ws, size_t ws_bytes, float** dq_acc,
                               float** dk_acc, float** dv_acc, cudaStream_t st,
                               bool d_ready = false, void* dq_out = nullptr,
-                              const float2* rope_cs = nullptr);
+                              const float2* rope_cs = nullptr, void* dk_out = nullptr,
+                              void* dv_out = nullptr);
 
 // ---------------------------------------------------------------------------
 // cross entropy (ce.cu)

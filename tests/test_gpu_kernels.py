@@ -130,3 +130,39 @@ def test_attention(kl, dt, B, S, Hq, Hkv, d):
     if S == 1:
         np.testing.assert_allclose(host(Ot).reshape(T, Hq, d), np.repeat(v, Hq // Hkv, axis=1), rtol=1e-2,
                                    atol=1e-2)
+
+
+def _att_bwd(kl, B, S, Hq, Hkv, d, Q, Kt, Vt, Ot, lse, DO):
+    dq, dk, dv = torch.empty_like(Q), torch.empty_like(Kt), torch.empty_like(Vt)
+    ws = torch.empty(kl.kl_attention_bwd_ws_bytes(B, S, Hq, Hkv, d), dtype=torch.uint8, device="cuda")
+    kl.kl_attention_bwd(B, S, Hq, Hkv, d, 1, Q.data_ptr(), Kt.data_ptr(), Vt.data_ptr(), Ot.data_ptr(),
+                        lse.data_ptr(), DO.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                        ws.data_ptr(), ws.numel())
+    torch.cuda.synchronize()
+    return dq, dk, dv
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv", [(1, 300, 8, 1), (2, 130, 16, 2)])
+def test_attention_dkdv_group_split(kl, monkeypatch, B, S, Hq, Hkv):
+    """dK/dV walk a kv head's whole query-head group in one CTA or split it over
+    a cluster of 2 or 4 CTAs (partials summed in rank order through distributed
+    shared memory): every split matches the oracle, and each repeats bit for bit."""
+    d, T = 128, B * S
+    q = synth.round_bf16(synth.normal(5, "att.q", (T, Hq, d)))
+    k = synth.round_bf16(synth.normal(5, "att.k", (T, Hkv, d)))
+    v = synth.round_bf16(synth.normal(5, "att.v", (T, Hkv, d)))
+    do = synth.round_bf16(synth.normal(5, "att.do", (T, Hq, d)))
+    Q, Kt, Vt, DO = (dev(a.reshape(T, -1), torch.bfloat16) for a in (q, k, v, do))
+    Ot = torch.empty_like(Q)
+    lse = torch.empty(B, Hq, S, dtype=torch.float32, device="cuda")
+    kl.kl_attention_fwd(B, S, Hq, Hkv, d, 1, Q.data_ptr(), Kt.data_ptr(), Vt.data_ptr(), Ot.data_ptr(),
+                        lse.data_ptr())
+    _, dk_ref, dv_ref = O.attention_bwd(q, k, v, do, B, S)
+    for split in ("1", "2", "4"):
+        monkeypatch.setenv("KL_ATTN_DKDV_SPLIT", split)
+        _, dk, dv = _att_bwd(kl, B, S, Hq, Hkv, d, Q, Kt, Vt, Ot, lse, DO)
+        assert_rel(host(dk), dk_ref.reshape(T, -1), TOL_BF16, f"dk split {split}")
+        assert_rel(host(dv), dv_ref.reshape(T, -1), TOL_BF16, f"dv split {split}")
+        _, dk2, dv2 = _att_bwd(kl, B, S, Hq, Hkv, d, Q, Kt, Vt, Ot, lse, DO)
+        assert torch.equal(dk, dk2) and torch.equal(dv, dv2), split
+    kl.kl_device_status()
