@@ -41,7 +41,6 @@ struct GemmProb {
   int nseg;
   int kb[GEMM_MAX_SEG];   // k-blocks of each (A, B) segment
   int kb_total;
-  int splits;             // work units per output tile (K split)
   int a_mn, b_mn;
   int a3d, b3d;           // MN-major operand staged by one 3-D copy (both 64-wide atoms)
   int m_tiles, n_tiles;
@@ -51,7 +50,6 @@ struct GemmProb {
   void* C;
   int64_t ldc;
   int c_f32;
-  int atomic;             // fp32 output accumulated with red.add (split problems)
   int vec_ok;
   const void* R;
   int64_t ldr;
@@ -90,10 +88,6 @@ struct Unit {
   int tail;               // scratch slice of a split last-round tile (split * tail_tiles + tile), or -1
 };
 
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
 
 __device__ __forceinline__ void store_chunk(const GemmProb& pr, int row, int col0,
                                             const uint32_t (&v)[32]) {
@@ -102,16 +96,6 @@ __device__ __forceinline__ void store_chunk(const GemmProb& pr, int row, int col
   for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
   const int ncols = min(32, pr.N - col0);
   const bool vec = pr.vec_ok && ncols == 32;
-  if (pr.atomic) {
-    float* c = static_cast<float*>(pr.C) + row * pr.ldc + col0;
-    if (vec) {
-#pragma unroll
-      for (int j = 0; j < 32; j += 4) red_add_v4(c + j, f[j], f[j + 1], f[j + 2], f[j + 3]);
-    } else {
-      for (int j = 0; j < ncols; ++j) atomicAdd(c + j, f[j]);
-    }
-    return;
-  }
   if (pr.R) {
     if (pr.r_f32) {
       const float* r = static_cast<const float*>(pr.R) + row * pr.ldr + col0;
@@ -447,9 +431,8 @@ __device__ __forceinline__ Unit decode_unit_cl(const GemmParams& P, int u) {
   while (p + 1 < P.nprob && u >= P.prob[p + 1].unit_begin) ++p;
   const GemmProb& pr = P.prob[p];
   const int local = u - pr.unit_begin;
-  // K splits are the slowest index: the units in flight share one K range, so
-  // the operand slices they stream stay resident in L2
-  const int ntile = pr.m_tiles * pr.n_tiles;
+  // last-round K splits are the slowest index: the units in flight share one
+  // K range, so the operand slices they stream stay resident in L2
   int si, tile, nsplit;
   Unit r;
   r.p = p;
@@ -462,9 +445,9 @@ __device__ __forceinline__ Unit decode_unit_cl(const GemmParams& P, int u) {
     tile = pr.whole_tiles + (t - si * pr.tail_tiles);
     nsplit = pr.tail_splits;
   } else {
-    si = local / ntile;
-    tile = local - si * ntile;
-    nsplit = pr.splits;
+    si = 0;
+    tile = local;
+    nsplit = 1;
   }
   if (pr.n_fast) {
     r.n0 = (tile % pr.n_tiles) * pr.n_step;
@@ -905,23 +888,6 @@ __global__ void __launch_bounds__(256) gemm_tail_finalize_kernel(const TailFin f
   }
 }
 
-// C = bf16(acc + R): finishes a problem that was accumulated in fp32.
-__global__ void gemm_finalize_kernel(int M, int N, const float* __restrict__ acc,
-                                     void* __restrict__ C, int64_t ldc, int c_f32,
-                                     const void* __restrict__ R, int64_t ldr, int r_f32) {
-  pdl_enter();
-  const int64_t total = static_cast<int64_t>(M) * N;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t r = i / N, c = i - r * N;
-    float v = acc[i];
-    if (R) v += r_f32 ? static_cast<const float*>(R)[r * ldr + c]
-                      : __bfloat162float(static_cast<const __nv_bfloat16*>(R)[r * ldr + c]);
-    if (c_f32) static_cast<float*>(C)[r * ldc + c] = v;
-    else static_cast<__nv_bfloat16*>(C)[r * ldc + c] = __float2bfloat16_rn(v);
-  }
-}
-
 // ---------------------------------------------------------------------------
 // host: tensor maps
 // ---------------------------------------------------------------------------
@@ -1028,15 +994,14 @@ __global__ void __launch_bounds__(256) gemm_f32_kernel(int M, int N, int nseg, G
 
 }  // namespace
 
-// K-split policy: problems with at least SPLIT_MIN_KB k-blocks whose result can
-// be accumulated in fp32 (fp32 output without addend, or a caller-provided
-// fp32 accumulator) are cut along K into units of at most ~UNIT_KB k-blocks,
-// so that no unit is long against a CTA's share of the launch.
-// Tile shape: pairs of CTAs (cta_group::2) on 256 x 256 tiles.
+// Tile shape: pairs of CTAs (cta_group::2) on 256 x 256 tiles. A unit is one
+// whole output tile (the full K range, so every output element is summed in
+// one fixed order); only a launch's last round may cut tiles along K, into
+// per-range scratch slices summed in range order (gemm_tail_finalize_kernel).
+// Long-K problems rely on the heaviest-first order and on the lighter
+// problems of the same launch to even out the CTA pairs' shares.
 constexpr int GEMM_CL = 2;
 constexpr int TILE_M = 256;
-constexpr int SPLIT_MIN_KB = 256;
-constexpr int UNIT_KB = 256;
 
 // Scheduler counters: one pair per launch slot, reused round-robin; each launch
 // re-arms its pair when its last CTA exits.
@@ -1077,19 +1042,16 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
   if (gemm_skinny_fits(specs_in, nspec)) return gemm_skinny(specs_in, nspec, st, label);
   // Heavy units first: order the problems by k-blocks per unit, descending.
   int order[GEMM_MAX_PROB];
-  int splits[GEMM_MAX_PROB];
   int kbt[GEMM_MAX_PROB];
   for (int i = 0; i < nspec; ++i) {
     const GemmSpec& s = specs_in[i];
     int kb = 0;
     for (int g = 0; g < s.nseg && g < GEMM_MAX_SEG; ++g) kb += (s.K[g] + BK - 1) / BK;
-    const bool can_split = s.epi == GEMM_EPI_STORE && ((s.c_dtype == KL_F32 && !s.R) || s.acc_ws);
-    splits[i] = (can_split && kb >= SPLIT_MIN_KB) ? (kb + UNIT_KB - 1) / UNIT_KB : 1;
     kbt[i] = kb;
     order[i] = i;
   }
   for (int a = 1; a < nspec; ++a)
-    for (int b = a; b > 0 && kbt[order[b]] / splits[order[b]] > kbt[order[b - 1]] / splits[order[b - 1]]; --b) {
+    for (int b = a; b > 0 && kbt[order[b]] > kbt[order[b - 1]]; --b) {
       const int t = order[b];
       order[b] = order[b - 1];
       order[b - 1] = t;
@@ -1097,7 +1059,6 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
   GemmParams p;  // built on the host, passed by value into the launch
   memset(&p, 0, sizeof(p));
   int units = 0, tm = 0;
-  bool finalize[GEMM_MAX_PROB] = {};
   double flops = 0.0, bytes = 0.0;
   for (int i = 0; i < nspec; ++i) {
     const int oi = order[i];
@@ -1114,7 +1075,7 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
                                                        s.N % 128 == 0);
       const bool rope_ok = s.epi != GEMM_EPI_ROPE || (s.rope_cs && s.rope_S > 0 && s.N % 128 == 0 &&
                                                       aligned16(s.C) && s.ldc % 8 == 0);
-      if (s.epi > GEMM_EPI_ROPE || s.c_dtype != KL_BF16 || s.R || s.nseg != 1 || s.acc_ws || !pairs_ok ||
+      if (s.epi > GEMM_EPI_ROPE || s.c_dtype != KL_BF16 || s.R || s.nseg != 1 || !pairs_ok ||
           !bwd_ok || !dot_ok || !rope_ok)
         return set_error(KL_ERR_INVALID_ARG, "gemm: problem %d: bad epilogue variant %d", oi, s.epi);
     }
@@ -1179,35 +1140,20 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
     pr.n_tiles = (s.N + pr.n_step - 1) / pr.n_step;
     // keep the smaller operand resident in L2: walk its dimension fastest
     pr.n_fast = s.N < s.M ? 1 : 0;
-    pr.splits = splits[oi] < pr.kb_total ? splits[oi] : pr.kb_total;
-    pr.atomic = pr.splits > 1;
     pr.unit_begin = units;
-    units += pr.m_tiles * pr.n_tiles * pr.splits;
-    const bool direct_f32 = s.c_dtype == KL_F32 && !s.R;
-    if (pr.atomic && !direct_f32) {
-      // accumulate in the caller's fp32 workspace, finish with gemm_finalize_kernel
-      finalize[oi] = true;
-      pr.C = s.acc_ws;
-      pr.ldc = s.N;
-      pr.c_f32 = 1;
-      pr.R = nullptr;
-      pr.vec_ok = aligned16(s.acc_ws) && (s.N * 4) % 16 == 0;
-    } else {
-      pr.C = s.C;
-      pr.ldc = s.ldc;
-      pr.c_f32 = s.c_dtype == KL_F32;
-      pr.R = s.R;
-      pr.ldr = s.ldr;
-      pr.r_f32 = s.r_dtype == KL_F32;
+    units += pr.m_tiles * pr.n_tiles;
+    pr.C = s.C;
+    pr.ldc = s.ldc;
+    pr.c_f32 = s.c_dtype == KL_F32;
+    pr.R = s.R;
+    pr.ldr = s.ldr;
+    pr.r_f32 = s.r_dtype == KL_F32;
+    {
       const size_t ce = dtype_size(s.c_dtype), re = dtype_size(s.r_dtype);
       pr.vec_ok = aligned16(s.C) && (s.ldc * ce) % 16 == 0 &&
                   (!s.R || (aligned16(s.R) && (s.ldr * re) % 16 == 0)) &&
                   (!s.C2 || aligned16(s.C2)) && (!s.C3 || aligned16(s.C3)) && (!s.X1 || aligned16(s.X1)) &&
                   (!s.X2 || aligned16(s.X2));
-    }
-    if (pr.atomic) {
-      if (finalize[oi]) KL_CUDA(cudaMemsetAsync(pr.C, 0, static_cast<size_t>(s.M) * s.N * 4, st));
-      else KL_CUDA(cudaMemset2DAsync(pr.C, static_cast<size_t>(pr.ldc) * 4, 0, static_cast<size_t>(s.N) * 4, s.M, st));
     }
     const double nmul = glu ? 2.0 : 1.0;   // SwiGLU: a gate and an up product
     const double extra = glu ? 2.0 : s.epi == GEMM_EPI_SWIGLU_BWD ? 3.0 : s.epi == GEMM_EPI_ROWDOT ? 1.0 : 0.0;
@@ -1249,7 +1195,7 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
     const GemmSpec& s = specs_in[order[lp]];
     const int tiles = pr.m_tiles * pr.n_tiles;
     const int rem = units % cap;
-    if (rem > 0 && s.tail_ws && pr.splits == 1 && pr.epi == GEMM_EPI_STORE && rem <= tiles &&
+    if (rem > 0 && s.tail_ws && pr.epi == GEMM_EPI_STORE && rem <= tiles &&
         pr.n_step == 256 && (reinterpret_cast<uintptr_t>(s.tail_ws) & 15u) == 0) {
       int ts = cap / rem;
       const int max_ts = pr.kb_total / 8;            // at least 8 k-blocks per piece
@@ -1293,15 +1239,6 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
     KL_CUDA(cudaGetLastError());
   }
   KL_CUDA(cudaGetLastError());
-  for (int i = 0; i < nspec; ++i) {
-    if (!finalize[i]) continue;
-    const GemmSpec& s = specs_in[i];
-    const double n = static_cast<double>(s.M) * s.N;
-    ProfScope ps("gemm_finalize", st, 0.0, n * (4 + dtype_size(s.c_dtype) + (s.R ? dtype_size(s.r_dtype) : 0)));
-    launch_pdl(gemm_finalize_kernel, 4 * num_sms(), 256, 0, st, s.M, s.N, s.acc_ws, s.C, s.ldc, s.c_dtype == KL_F32,
-                                                       s.R, s.ldr, s.r_dtype == KL_F32);
-    KL_CUDA(cudaGetLastError());
-  }
   return KL_OK;
 }
 

@@ -460,7 +460,7 @@ bool skinny_plan(const GemmSpec* s, int n, SkPlan* pl) {
   int mmax = 0, W = 0, tiles = 0;
   for (int i = 0; i < n; ++i) {
     const GemmSpec& g = s[i];
-    if (g.M < 1 || g.M > 128 || g.N < 1 || g.nseg != 1 || g.K[0] < 1 || g.a_mn || g.b_mn || g.acc_ws) return false;
+    if (g.M < 1 || g.M > 128 || g.N < 1 || g.nseg != 1 || g.K[0] < 1 || g.a_mn || g.b_mn) return false;
     if ((g.epi == GEMM_EPI_SWIGLU) != (glu != 0)) return false;
     if (g.epi != GEMM_EPI_STORE && g.epi != GEMM_EPI_SWIGLU) return false;
     if (!g.A[0] || !g.B[0] || !g.C || !al16(g.A[0]) || !al16(g.B[0]) || g.lda[0] % 8 || g.ldb[0] % 8) return false;

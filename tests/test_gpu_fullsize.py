@@ -80,6 +80,33 @@ def test_qwen3_layer_T2048_forward_bit_reproducible(kl):
     assert torch.equal(outs[0][1], outs[1][1])
 
 
+def test_qwen3_layer_T2048_backward_bit_reproducible(kl):
+    """The full-size backward in the bench's launch configuration repeats bit
+    for bit: dX and every weight gradient (the attention's dK/dV partials meet
+    in rank order, every GEMM output element is summed in one fixed order)."""
+    B, S = 1, 2048
+    cfg = L.make_cfg(B, S, **QWEN, dtype=kl.KL_BF16)
+    w = {n: _dev_normal(shp, 0.02, 1.0 if n.startswith("gamma") else 0.0, f"repb.{n}")
+         for n, shp in L.weight_shapes(cfg).items()}
+    X = _dev_normal((B * S, QWEN["H"]), 1.0, 0.0, "repb.X")
+    dY = _dev_normal((B * S, QWEN["H"]), 1.0, 0.0, "repb.dY")
+    ws = L.weights_struct(w)
+    buf = L.LayerBuffers(cfg, "cuda")
+    grads, gst = L.alloc_grads(cfg, "cuda", kl.KL_BF16)
+    Y = torch.empty_like(X)
+    kl.kl_layer_forward(cfg, ws, X.data_ptr(), Y.data_ptr(), buf.saved, buf.fwd_ws.data_ptr(), buf.fwd_ws.numel())
+    outs = []
+    for _ in range(2):
+        dX = torch.empty_like(X)
+        kl.kl_layer_backward(cfg, ws, buf.saved, dY.data_ptr(), dX.data_ptr(), gst, buf.bwd_ws.data_ptr(),
+                             buf.bwd_ws.numel())
+        torch.cuda.synchronize()
+        outs.append([dX.clone()] + [grads[n].clone() for n in sorted(grads)])
+    kl.kl_device_status()
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a, b)
+
+
 def test_attention_S32768_sampled_and_invariants(kl):
     B, S, Hq, Hkv, d = 1, 32768, 64, 8, 128
     T = B * S
