@@ -723,6 +723,8 @@ struct BwdParams {
   __nv_bfloat16* dk_out;             // [T, Hkv*128] bf16 final dK
   __nv_bfloat16* dv_out;             // [T, Hkv*128] bf16 final dV
   const float2* rope_cs;             // [S][64] cos/sin: dQ (with dq_out) and dK turned back by -angle, or null
+  const __nv_bfloat16* kg;           // [T, Hkv*128] K and V (dK/dV kernel: rows read into TMEM)
+  const __nv_bfloat16* vg;
   int S, Hq, Hkv;
   int nsplit;                        // CTAs (one cluster) sharing a kv head's key tile; heads split between them
   float scale_log2, scale;
@@ -744,28 +746,30 @@ struct BwdParams {
 // key position's rotary angle when a table is given) and dV are written once,
 // as bf16: no atomics, and the same bits on every run.
 //
-// Four Q / dO stages let the scores of a step go out two steps ahead of its
-// gradients; they fit because P^T / dS^T are single-buffered (each elementwise
-// warp holds a step's packed values in registers until the previous step's
-// gradient products have released the buffer) and because the dynamic shared
-// memory is taken as 1024-byte aligned (checked at entry) instead of carrying
-// alignment slack.
-constexpr uint32_t KV_OFF_K = 0;
-constexpr uint32_t KV_OFF_V = KV_OFF_K + TILE_BYTES;
+// K and V are the A operands of S^T = K Q^T and dP^T = V dO^T and stay the same
+// for the whole CTA, so they live in tensor memory (loaded once by the
+// elementwise warps): each step's products then read only Q, dO, P^T and dS^T
+// from shared memory, which bounds these N = 64 products when both operands
+// come from shared memory. Tensor memory: S^T | dP^T (one buffer, 64 columns
+// each), K | V (bf16, 64 columns each), dV, dK (128 fp32 columns each).
+// Shared memory: a 4-stage Q / dO ring with the stage's lse / D rows, and
+// double-buffered P^T / dS^T. The dynamic shared memory is taken as 1024-byte
+// aligned (checked at entry).
 constexpr int KV_QS = 4;                                      // stages of the Q / dO / lse / D ring
-constexpr uint32_t KV_OFF_Q = KV_OFF_V + TILE_BYTES;         // KV_QS stages of T64
+constexpr uint32_t KV_OFF_Q = 0;                              // KV_QS stages of T64
 constexpr uint32_t KV_OFF_DO = KV_OFF_Q + KV_QS * T64;       // KV_QS stages of T64
 constexpr uint32_t PT_BYTES = 128 * 64 * 2;                   // 16 KB: 128 key rows x 64 queries
-constexpr uint32_t KV_OFF_P = KV_OFF_DO + KV_QS * T64;       // P^T
-constexpr uint32_t KV_OFF_DS = KV_OFF_P + PT_BYTES;          // dS^T
-constexpr uint32_t KV_OFF_STAT = KV_OFF_DS + PT_BYTES;      // KV_QS stages: lse[64], D[64] (fp32)
+constexpr uint32_t KV_OFF_P = KV_OFF_DO + KV_QS * T64;       // 2 buffers of P^T
+constexpr uint32_t KV_OFF_DS = KV_OFF_P + 2 * PT_BYTES;      // 2 buffers of dS^T
+constexpr uint32_t KV_OFF_STAT = KV_OFF_DS + 2 * PT_BYTES;  // KV_QS stages: lse[64], D[64] (fp32)
 constexpr uint32_t KV_OFF_BAR = KV_OFF_STAT + KV_QS * 512;
 constexpr size_t KV_SMEM = KV_OFF_BAR + 256;
-// The partial-sum exchange reuses K, V and the Q / dO ring: nsplit slots of
-// 128 rows x 4W fp32 (dV low, dV high, dK low, dK high columns) = 128 KB.
+constexpr uint32_t TM_ST = 0, TM_DPT = 64, TM_K = 128, TM_V = 192, TM_DV = 256, TM_DK = 384;
+// The partial-sum exchange reuses the Q / dO ring: nsplit slots of 128 rows x
+// 4W fp32 (dV low, dV high, dK low, dK high columns) = 128 KB.
 constexpr uint32_t KV_OFF_XCH = 0;
 constexpr uint32_t KV_XCH_BYTES = 128 * 256 * 4;
-static_assert(KV_XCH_BYTES <= KV_OFF_P, "exchange slots overlap the P^T buffer");
+static_assert(KV_XCH_BYTES <= KV_OFF_P, "exchange slots overlap the P^T buffers");
 static_assert(KV_SMEM <= 232448, "dK/dV shared memory above the per-CTA limit");
 
 // Writes one key row's finished dV or dK columns [c0, c0 + W) and [64 + c0, ...)
@@ -886,16 +890,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
   uint8_t* smem = kv_smem_raw;
   const uint32_t sb = smem_u32(smem);
   const uint32_t bar = sb + KV_OFF_BAR;
-  const uint32_t kv_full = bar;
-  auto q_full = [&](int s) { return bar + 8 + 8 * s; };              // KV_QS of each ring barrier
-  auto q_free = [&](int s) { return bar + 8 + 8 * KV_QS + 8 * s; };
-  auto st_full = [&](int s) { return bar + 8 + 16 * KV_QS + 8 * s; }; // 2 of each TMEM barrier
-  auto st_free = [&](int s) { return bar + 24 + 16 * KV_QS + 8 * s; };
-  const uint32_t p_full = bar + 40 + 16 * KV_QS;                      // the single P^T / dS^T buffer
-  const uint32_t p_free = bar + 48 + 16 * KV_QS;
-  const uint32_t done = bar + 56 + 16 * KV_QS;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + KV_OFF_BAR + 64 + 16 * KV_QS);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + KV_OFF_BAR + 68 + 16 * KV_QS);
+  auto q_full = [&](int s) { return bar + 8 * s; };                   // KV_QS of each ring barrier
+  auto q_free = [&](int s) { return bar + 8 * KV_QS + 8 * s; };
+  const uint32_t st_full = bar + 16 * KV_QS;                          // S^T / dP^T in TMEM
+  const uint32_t st_free = bar + 16 * KV_QS + 8;
+  auto p_full = [&](int s) { return bar + 16 * KV_QS + 16 + 8 * s; }; // 2 P^T / dS^T buffers
+  auto p_free = [&](int s) { return bar + 16 * KV_QS + 32 + 8 * s; };
+  const uint32_t kv_ready = bar + 16 * KV_QS + 48;                    // K, V written into TMEM
+  const uint32_t done = bar + 16 * KV_QS + 56;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + KV_OFF_BAR + 16 * KV_QS + 64);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + KV_OFF_BAR + 16 * KV_QS + 68);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kb = blockIdx.y;                 // key tiles near the start see the most queries
@@ -913,17 +917,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
                          (reinterpret_cast<uintptr_t>(p.Dd) & 15u) == 0;
 
   if (threadIdx.x == 0) {
-    mbar_init(kv_full, 1);
     for (int s = 0; s < KV_QS; ++s) {
       mbar_init(q_full(s), 1);
       mbar_init(q_free(s), 1);
     }
+    mbar_init(st_full, 1);
+    mbar_init(st_free, BWD_EW);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(st_full(s), 1);
-      mbar_init(st_free(s), BWD_EW);
+      mbar_init(p_full(s), BWD_EW);
+      mbar_init(p_free(s), 1);
     }
-    mbar_init(p_full, BWD_EW);
-    mbar_init(p_free, 1);
+    mbar_init(kv_ready, BWD_EW);
     mbar_init(done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -939,16 +943,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
   bool fin = false;                          // elementwise warps: every MMA of the CTA completed
 
   if (warp == 0) {
-    // ---------------- TMA (whole warp; the elected lane issues) ----------------
+    // ---------------- TMA: Q / dO tiles and lse / D rows (the elected lane issues) ----------------
     const bool el = elect_one();
-    if (el) {
-      mbar_arrive_expect_tx(kv_full, 2 * TILE_BYTES);
-      tma_load_2d(sb + KV_OFF_K, &p.tmK, jh * HD, row0 + k0, kv_full);
-      tma_load_2d(sb + KV_OFF_K + 16384, &p.tmK, jh * HD + 64, row0 + k0, kv_full);
-      tma_load_2d(sb + KV_OFF_V, &p.tmV, jh * HD, row0 + k0, kv_full);
-      tma_load_2d(sb + KV_OFF_V + 16384, &p.tmV, jh * HD + 64, row0 + k0, kv_full);
-    }
-    __syncwarp();
     int issued = 0;
     for (int g = 0; g < nsteps; ++g) {
       const int s = g % KV_QS;
@@ -975,52 +971,50 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
       __syncwarp();
       ++issued;
     }
-    mbar_wait(kv_full, 0, p.err);
     for (int g = (issued > KV_QS ? issued - KV_QS : 0); g < issued; ++g)
       mbar_wait(q_full(g % KV_QS), (g / KV_QS) & 1, p.err);
   } else if (warp == 1) {
     // ---------------- MMA (the elected lane issues) ----------------
-    // S^T / dP^T of step j go out as soon as their TMEM buffer (j & 1) is free
-    // (the elementwise warps have loaded step j - 2) and the step's Q / dO have
-    // landed; the gradient products of step j go out as soon as its P^T / dS^T
-    // are written. One ordered issue stream would hold S^T(j) behind the
-    // gradients of step j - 2 and leave the elementwise warps waiting.
+    // S^T / dP^T of step j go out once the elementwise warps have read step
+    // j - 1's (one TMEM buffer) and step j's Q / dO have landed; the gradient
+    // products of step j once its P^T / dS^T are written. Polling both keeps
+    // the next scores in flight while the elementwise warps work on a step.
     const bool el = elect_one();
     const uint32_t id_st = idesc_bf16_f32(128, 64, 0, 0);
     const uint32_t id_gr = idesc_bf16_f32(128, 128, 0, 1);
-    bool ok = mbar_wait_warp(kv_full, 0, p.err, abort_flag);
+    bool ok = mbar_wait_warp(kv_ready, 0, p.err, abort_flag);
+    if (ok) tc_fence_after();
     if (el && ok) {
       int ns = 0, ng = 0;          // next step whose S^T / dP^T, whose gradients, go out
       uint32_t idle = 0;
       uint64_t since = 0;
       while (ng < nsteps) {
         bool prog = false;
-        if (ng < ns && mbar_test_wait(p_full, ng & 1)) {
+        if (ng < ns && mbar_test_wait(p_full(ng & 1), (ng >> 1) & 1)) {
           tc_fence_after();
-          const int qs = ng % KV_QS;
+          const int qs = ng % KV_QS, pb = ng & 1;
           const uint32_t sq = sb + KV_OFF_Q + qs * T64, sdo = sb + KV_OFF_DO + qs * T64;
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + 256, desc_k64(sb + KV_OFF_P, kk), desc_mn128(sdo, 8192, kk), id_gr,
+            umma_bf16(tmem + TM_DV, desc_k64(sb + KV_OFF_P + pb * PT_BYTES, kk), desc_mn128(sdo, 8192, kk), id_gr,
                       (ng > 0 || kk > 0) ? 1u : 0u);
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + 384, desc_k64(sb + KV_OFF_DS, kk), desc_mn128(sq, 8192, kk), id_gr,
+            umma_bf16(tmem + TM_DK, desc_k64(sb + KV_OFF_DS + pb * PT_BYTES, kk), desc_mn128(sq, 8192, kk), id_gr,
                       (ng > 0 || kk > 0) ? 1u : 0u);
           umma_commit(q_free(qs));
-          umma_commit(p_free);
+          umma_commit(p_free(pb));
           ++ng;
           prog = true;
         }
         if (ns < nsteps && mbar_test_wait(q_full(ns % KV_QS), (ns / KV_QS) & 1) &&
-            (ns < 2 || mbar_test_wait(st_free(ns & 1), ((ns >> 1) & 1) ^ 1u))) {
+            (ns == 0 || mbar_test_wait(st_free, (ns - 1) & 1))) {
           tc_fence_after();
-          const int ss = ns & 1, qs = ns % KV_QS;
+          const int qs = ns % KV_QS;
           const uint32_t sq = sb + KV_OFF_Q + qs * T64, sdo = sb + KV_OFF_DO + qs * T64;
           for (int kk = 0; kk < HD / 16; ++kk)
-            umma_bf16(tmem + ss * 64, desc_k128(sb + KV_OFF_K, 16384, kk), desc_k128(sq, 8192, kk), id_st, kk > 0);
+            umma_bf16_ta(tmem + TM_ST, tmem + TM_K + kk * 8, desc_k128(sq, 8192, kk), id_st, kk > 0);
           for (int kk = 0; kk < HD / 16; ++kk)
-            umma_bf16(tmem + 128 + ss * 64, desc_k128(sb + KV_OFF_V, 16384, kk), desc_k128(sdo, 8192, kk), id_st,
-                      kk > 0);
-          umma_commit(st_full(ss));
+            umma_bf16_ta(tmem + TM_DPT, tmem + TM_V + kk * 8, desc_k128(sdo, 8192, kk), id_st, kk > 0);
+          umma_commit(st_full);
           ++ns;
           prog = true;
         }
@@ -1052,7 +1046,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
     __syncwarp();
     mbar_wait(done, 0, p.err);
   } else if (warp >= 2) {
-    // ---------------- P^T, dS^T (thread = key row) ----------------
+    // ---------------- K, V into TMEM; then P^T, dS^T (thread = key row) ----------------
     // warp 2 + 4 * half + i: lane quarter (warp & 3), queries 32 * half .. + 31 of a step
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
@@ -1060,28 +1054,52 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
     const int r = quarter * 32 + lane;
     const int key = k0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    {
+      // this row's head-dim columns 64 * half .. + 63 of K and V (zero past the sequence),
+      // packed bf16 pairs into TMEM columns TM_K / TM_V + 32 * half .. + 31
+      uint32_t kr[32], vr[32];
+      if (key < p.S) {
+        const int64_t o = (static_cast<int64_t>(row0 + key) * p.Hkv + jh) * HD + half * 64;
+        const uint4* kp = reinterpret_cast<const uint4*>(p.kg + o);
+        const uint4* vp = reinterpret_cast<const uint4*>(p.vg + o);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint4 a = kp[e], c = vp[e];
+          kr[4 * e] = a.x; kr[4 * e + 1] = a.y; kr[4 * e + 2] = a.z; kr[4 * e + 3] = a.w;
+          vr[4 * e] = c.x; vr[4 * e + 1] = c.y; vr[4 * e + 2] = c.z; vr[4 * e + 3] = c.w;
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) kr[e] = vr[e] = 0u;
+      }
+      tmem_st_32x32b_x32(tmem + lane_off + TM_K + half * 32, kr);
+      tmem_st_32x32b_x32(tmem + lane_off + TM_V + half * 32, vr);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(kv_ready);
+    }
     const bool vec_stat = (p.S & 3) == 0;     // rows of lse / D are 16-byte aligned
     bool ok = true;
     for (int g = 0; g < nsteps; ++g) {
-      const int s = g & 1;
-      const uint32_t ph = (g >> 1) & 1;
       const int h = h_first + g / nit;
       const int q0 = k0 + (g % nit) * 64;
       const float* lrow = p.lse + (static_cast<int64_t>(b) * p.Hq + h) * p.S;
       const float* drow = p.Dd + (static_cast<int64_t>(b) * p.Hq + h) * p.S;
-      if (!mbar_wait_warp(st_full(s), ph, p.err, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(st_full, g & 1, p.err, abort_flag)) { ok = false; break; }
       tc_fence_after();
       uint32_t sv[32], dv[32];
-      tmem_ld_32x32b_x32(tmem + lane_off + s * 64 + col0, sv);
-      tmem_ld_32x32b_x32(tmem + lane_off + 128 + s * 64 + col0, dv);
+      tmem_ld_32x32b_x32(tmem + lane_off + TM_ST + col0, sv);
+      tmem_ld_32x32b_x32(tmem + lane_off + TM_DPT + col0, dv);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(st_free(s));
+      if (lane == 0) mbar_arrive(st_free);
       const int lim = key - q0;              // queries q0 + c with c >= lim see this key
-      uint8_t* prow = smem + KV_OFF_P + r * 128;
-      uint8_t* drw = smem + KV_OFF_DS + r * 128;
-      uint4 pst[4], dst[4];                  // this warp's 4 chunks of the row, until the buffer is free
+      const int pb = g & 1;
+      uint8_t* prow = smem + KV_OFF_P + pb * PT_BYTES + r * 128;
+      uint8_t* drw = smem + KV_OFF_DS + pb * PT_BYTES + r * 128;
+      uint4 pst[4], dst[4];                  // this warp's 4 chunks of the row
       // the stage's lse / D copies completed with its Q / dO (q_full), before S^T
       if (stat_smem && !mbar_wait_warp(q_full(g % KV_QS), (g / KV_QS) & 1, p.err, abort_flag)) {
         ok = false;
@@ -1146,8 +1164,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
       };
       if (__any_sync(0xffffffffu, lim > col0)) step(std::true_type{});
       else step(std::false_type{});
-      // the buffer is free once the previous step's gradient products completed
-      if (g >= 1 && !mbar_wait_warp(p_free, (g - 1) & 1, p.err, abort_flag)) { ok = false; break; }
+      // buffer pb is free once step g - 2's gradient products completed
+      if (g >= 2 && !mbar_wait_warp(p_free(pb), ((g >> 1) - 1) & 1, p.err, abort_flag)) { ok = false; break; }
 #pragma unroll
       for (int c8l = 0; c8l < 4; ++c8l) {
         const int off = (((half * 4 + c8l) ^ (r & 7)) << 4);
@@ -1156,7 +1174,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(p_full(pb));
     }
     fin = ok && mbar_wait_warp(done, 0, p.err, abort_flag);
     if (!fin) *abort_flag = 1;
@@ -1171,7 +1189,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
   const int r = quarter * 32 + lane;
   const int key = k0 + r;
   const bool is_k = warp >= 6;
-  const uint32_t tmem_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + (is_k ? 384u : 256u);
+  const uint32_t tmem_row = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + (is_k ? TM_DK : TM_DV);
   __nv_bfloat16* orow = nullptr;
   const float2* cs = nullptr;
   if (warp >= 2 && key < p.S) {
@@ -1189,8 +1207,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
       }
     }
   } else {
-    // every CTA of the cluster has finished its MMAs and copies: the K, V and
-    // Q / dO buffers are free to take the partial sums
+    // every CTA of the cluster has finished its MMAs and copies: the Q / dO
+    // ring is free to take the partial sums
     cluster_sync_all();
     if (warp >= 2 && fin) {
       if (nsplit == 2) dkdv_send<32>(tmem_row, sb, r, is_k, 2, rank);
@@ -1612,6 +1630,8 @@ kl_status attention_bwd_tc(int B, int S, int Hq, int Hkv, const void* q, const v
   p.dk_out = static_cast<__nv_bfloat16*>(dk_out);
   p.dv_out = static_cast<__nv_bfloat16*>(dv_out);
   p.rope_cs = rope_cs;
+  p.kg = static_cast<const __nv_bfloat16*>(k);
+  p.vg = static_cast<const __nv_bfloat16*>(v);
   p.S = S;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -1625,9 +1645,7 @@ kl_status attention_bwd_tc(int B, int S, int Hq, int Hkv, const void* q, const v
   p.scale = 1.0f / sqrtf(static_cast<float>(HD));
   p.err = device_error_word();
   const double pairs = 0.5 * static_cast<double>(S) * (S + 1);
-  // dK / dV: K and V tiles of 128 rows, Q and dO tiles of 64 rows
-  KL_TRY(map_rows(&p.tmK, k, static_cast<uint64_t>(Hkv) * HD, T, 128));
-  KL_TRY(map_rows(&p.tmV, v, static_cast<uint64_t>(Hkv) * HD, T, 128));
+  // dK / dV: Q and dO tiles of 64 rows (K and V rows are read into TMEM by the kernel)
   KL_TRY(map_rows(&p.tmQ, q, static_cast<uint64_t>(Hq) * HD, T, 64));
   KL_TRY(map_rows(&p.tmdO, dout, static_cast<uint64_t>(Hq) * HD, T, 64));
   {
