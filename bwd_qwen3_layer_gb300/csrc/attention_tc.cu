@@ -1232,15 +1232,25 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
 // ---------------------------------------------------------------------------
 // dQ
 // ---------------------------------------------------------------------------
-constexpr uint32_t DQ_OFF_Q = 0;
-constexpr uint32_t DQ_OFF_DO = DQ_OFF_Q + TILE_BYTES;
-constexpr int DQ_KS = 4;                                     // stages of the K / V ring
-constexpr uint32_t DQ_OFF_K = DQ_OFF_DO + TILE_BYTES;       // DQ_KS stages of T64
+// Q and dO, the A operands of S = Q K^T and dP = dO V^T, are the same for the
+// whole CTA and live in tensor memory: the TMA warp stages them in the K / V
+// ring's last two stages, the elementwise warps copy each row into tensor
+// memory, and those stages then join the ring. Shared memory holds the K / V
+// ring and the double-buffered dS. Tensor memory: S (2 x 64 columns), dP
+// (2 x 64), dQ (128), Q and dO (bf16, 64 each).
+constexpr int DQ_KS = 6;                                     // stages of the K / V ring
+constexpr uint32_t DQ_TM_DQ = 256, DQ_TM_Q = 384, DQ_TM_DO = 448;
+constexpr uint32_t DQ_OFF_K = 0;                             // DQ_KS stages of T64
 constexpr uint32_t DQ_OFF_V = DQ_OFF_K + DQ_KS * T64;       // DQ_KS stages of T64
 constexpr uint32_t DQ_OFF_DS = DQ_OFF_V + DQ_KS * T64;      // 2 buffers: 128 rows x 64 keys bf16 (16 KB)
 constexpr uint32_t DQ_OFF_BAR = DQ_OFF_DS + 2 * 16384;
 constexpr size_t DQ_SMEM = 1024 + DQ_OFF_BAR + 256;
 static_assert(DQ_SMEM <= 232448, "dQ shared memory above the per-CTA limit");
+static_assert(DQ_KS >= 4, "Q and dO are staged in the ring's last two stages");
+// staging of Q / dO (128 rows x 128 columns each, two 64-column swizzle blocks of
+// 16 KB): ring stages DQ_KS - 2 and DQ_KS - 1 (a stage is 2 x T64 = 32 KB)
+constexpr uint32_t DQ_STAGE_Q = DQ_OFF_K + (DQ_KS - 2) * T64;     // K slots of the last two stages
+constexpr uint32_t DQ_STAGE_DO = DQ_OFF_V + (DQ_KS - 2) * T64;    // V slots of the last two stages
 
 __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dq_tc_kernel(const __grid_constant__ BwdParams p) {
   pdl_enter();
@@ -1249,16 +1259,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dq_tc_kernel(const __gr
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(smem);
   const uint32_t bar = sb + DQ_OFF_BAR;
-  const uint32_t q_full = bar;
+  const uint32_t q_ready = bar;                                      // Q, dO written into TMEM
   auto kv_full = [&](int s) { return bar + 8 + 8 * s; };             // DQ_KS of each ring barrier
-  auto kv_free = [&](int s) { return bar + 40 + 8 * s; };
-  auto sd_full = [&](int s) { return bar + 72 + 8 * s; };            // 2 of each TMEM / dS barrier
-  auto sd_free = [&](int s) { return bar + 88 + 8 * s; };
-  auto ds_full = [&](int s) { return bar + 104 + 8 * s; };
-  auto ds_free = [&](int s) { return bar + 120 + 8 * s; };
-  const uint32_t done = bar + 136;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + DQ_OFF_BAR + 144);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + DQ_OFF_BAR + 148);
+  auto kv_free = [&](int s) { return bar + 8 + 8 * DQ_KS + 8 * s; };
+  const uint32_t b2 = bar + 8 + 16 * DQ_KS;
+  auto sd_full = [&](int s) { return b2 + 8 * s; };                   // 2 of each TMEM / dS barrier
+  auto sd_free = [&](int s) { return b2 + 16 + 8 * s; };
+  auto ds_full = [&](int s) { return b2 + 32 + 8 * s; };
+  auto ds_free = [&](int s) { return b2 + 48 + 8 * s; };
+  const uint32_t done = b2 + 64;
+  const uint32_t q_staged = b2 + 72;                                 // Q, dO copied into the staging
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + DQ_OFF_BAR + 8 + 16 * DQ_KS + 80);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + DQ_OFF_BAR + 8 + 16 * DQ_KS + 84);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqb = (p.S + BQ - 1) / BQ;
@@ -1270,7 +1282,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dq_tc_kernel(const __gr
   const int nkb = (min(q0 + BQ, p.S) + 63) / 64;            // 64-key tiles up to the diagonal
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    mbar_init(q_ready, BWD_EW);
+    mbar_init(q_staged, 1);
     for (int s = 0; s < DQ_KS; ++s) {
       mbar_init(kv_full(s), 1);
       mbar_init(kv_free(s), 1);
@@ -1298,17 +1311,19 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dq_tc_kernel(const __gr
     // ---------------- TMA (whole warp; the elected lane issues) ----------------
     const bool el = elect_one();
     if (el) {
-      mbar_arrive_expect_tx(q_full, 2 * TILE_BYTES);
-      tma_load_2d(sb + DQ_OFF_Q, &p.tmQ, h * HD, row0 + q0, q_full);
-      tma_load_2d(sb + DQ_OFF_Q + 16384, &p.tmQ, h * HD + 64, row0 + q0, q_full);
-      tma_load_2d(sb + DQ_OFF_DO, &p.tmdO, h * HD, row0 + q0, q_full);
-      tma_load_2d(sb + DQ_OFF_DO + 16384, &p.tmdO, h * HD + 64, row0 + q0, q_full);
+      mbar_arrive_expect_tx(q_staged, 2 * TILE_BYTES);
+      tma_load_2d(sb + DQ_STAGE_Q, &p.tmQ, h * HD, row0 + q0, q_staged);
+      tma_load_2d(sb + DQ_STAGE_Q + 16384, &p.tmQ, h * HD + 64, row0 + q0, q_staged);
+      tma_load_2d(sb + DQ_STAGE_DO, &p.tmdO, h * HD, row0 + q0, q_staged);
+      tma_load_2d(sb + DQ_STAGE_DO + 16384, &p.tmdO, h * HD + 64, row0 + q0, q_staged);
     }
     __syncwarp();
     int issued = 0;
     for (int j = 0; j < nkb; ++j) {
       const int s = j % DQ_KS;
       const uint32_t ph = (j / DQ_KS) & 1;
+      // the last two stages hold the Q / dO staging until it is in tensor memory
+      if (j == DQ_KS - 2 && !mbar_wait_warp(q_ready, 0, p.err, abort_flag)) { *abort_flag = 1; break; }
       if (!mbar_wait_warp(kv_free(s), ph ^ 1u, p.err, abort_flag)) { *abort_flag = 1; break; }
       const int kr = row0 + j * 64;
       if (el) {
@@ -1321,7 +1336,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dq_tc_kernel(const __gr
       __syncwarp();
       ++issued;
     }
-    mbar_wait(q_full, 0, p.err);
+    mbar_wait(q_staged, 0, p.err);
     for (int j = (issued > DQ_KS ? issued - DQ_KS : 0); j < issued; ++j)
       mbar_wait(kv_full(j % DQ_KS), (j / DQ_KS) & 1, p.err);
   } else if (warp == 1) {
@@ -1332,7 +1347,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dq_tc_kernel(const __gr
     const bool el = elect_one();
     const uint32_t id_s = idesc_bf16_f32(128, 64, 0, 0);
     const uint32_t id_q = idesc_bf16_f32(128, 128, 0, 1);
-    bool ok = mbar_wait_warp(q_full, 0, p.err, abort_flag);
+    bool ok = mbar_wait_warp(q_ready, 0, p.err, abort_flag);
+    if (ok) tc_fence_after();
     if (el && ok) {
       int ns = 0, ng = 0;          // next step whose S / dP, whose dQ product, goes out
       uint32_t idle = 0;
@@ -1343,7 +1359,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dq_tc_kernel(const __gr
           tc_fence_after();
           const int sg = ng & 1, ks = ng % DQ_KS;
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + 256, desc_k64(sb + DQ_OFF_DS + sg * 16384, kk),
+            umma_bf16(tmem + DQ_TM_DQ, desc_k64(sb + DQ_OFF_DS + sg * 16384, kk),
                       desc_mn128(sb + DQ_OFF_K + ks * T64, 8192, kk), id_q, (ng > 0 || kk > 0) ? 1u : 0u);
           umma_commit(kv_free(ks));
           umma_commit(ds_free(sg));
@@ -1355,11 +1371,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dq_tc_kernel(const __gr
           tc_fence_after();
           const int ss = ns & 1, ks = ns % DQ_KS;
           for (int kk = 0; kk < HD / 16; ++kk)
-            umma_bf16(tmem + ss * 64, desc_k128(sb + DQ_OFF_Q, 16384, kk),
-                      desc_k128(sb + DQ_OFF_K + ks * T64, 8192, kk), id_s, kk > 0);
+            umma_bf16_ta(tmem + ss * 64, tmem + DQ_TM_Q + kk * 8, desc_k128(sb + DQ_OFF_K + ks * T64, 8192, kk),
+                         id_s, kk > 0);
           for (int kk = 0; kk < HD / 16; ++kk)
-            umma_bf16(tmem + 128 + ss * 64, desc_k128(sb + DQ_OFF_DO, 16384, kk),
-                      desc_k128(sb + DQ_OFF_V + ks * T64, 8192, kk), id_s, kk > 0);
+            umma_bf16_ta(tmem + 128 + ss * 64, tmem + DQ_TM_DO + kk * 8,
+                         desc_k128(sb + DQ_OFF_V + ks * T64, 8192, kk), id_s, kk > 0);
           umma_commit(sd_full(ss));
           ++ns;
           prog = true;
@@ -1399,6 +1415,29 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dq_tc_kernel(const __gr
     const int r = quarter * 32 + lane;
     const int qrow = q0 + r;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    {
+      // this query row's head-dim columns 64 * half .. + 63 of Q and dO (the staged
+      // 128-byte-swizzled block `half`, zero past the sequence), packed bf16 pairs into
+      // TMEM columns DQ_TM_Q / DQ_TM_DO + 32 * half .. + 31
+      uint32_t qv[32], ov[32];
+      const bool staged = mbar_wait_warp(q_staged, 0, p.err, abort_flag);
+      const uint8_t* qs = smem + DQ_STAGE_Q + half * 16384 + r * 128;
+      const uint8_t* os = smem + DQ_STAGE_DO + half * 16384 + r * 128;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int off = (e ^ (r & 7)) << 4;
+        const uint4 a = *reinterpret_cast<const uint4*>(qs + off), c = *reinterpret_cast<const uint4*>(os + off);
+        qv[4 * e] = a.x; qv[4 * e + 1] = a.y; qv[4 * e + 2] = a.z; qv[4 * e + 3] = a.w;
+        ov[4 * e] = c.x; ov[4 * e + 1] = c.y; ov[4 * e + 2] = c.z; ov[4 * e + 3] = c.w;
+      }
+      tmem_st_32x32b_x32(tmem + lane_off + DQ_TM_Q + half * 32, qv);
+      tmem_st_32x32b_x32(tmem + lane_off + DQ_TM_DO + half * 32, ov);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_ready);
+      if (!staged) *abort_flag = 1;
+    }
     const int64_t li = (static_cast<int64_t>(b) * p.Hq + h) * p.S + qrow;
     const float l2 = qrow < p.S ? p.lse[li] * LOG2E_F : INFINITY;
     const float Dq = qrow < p.S ? p.Dd[li] : 0.f;
@@ -1458,8 +1497,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dq_tc_kernel(const __gr
       {
         const int c = half;
         uint32_t va[32], vb[32];   // planes 32c .. 32c+31 and their partners at +64
-        tmem_ld_32x32b_x32(tmem + lane_off + 256 + c * 32, va);
-        tmem_ld_32x32b_x32(tmem + lane_off + 256 + 64 + c * 32, vb);
+        tmem_ld_32x32b_x32(tmem + lane_off + DQ_TM_DQ + c * 32, va);
+        tmem_ld_32x32b_x32(tmem + lane_off + DQ_TM_DQ + 64 + c * 32, vb);
         tmem_ld_wait();
         if (qrow < p.S) {
           float xa[32], xb[32];
@@ -1496,7 +1535,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dq_tc_kernel(const __gr
       for (int cc = 0; cc < 2; ++cc) {
         const int c = half * 2 + cc;
         uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem + lane_off + 256 + c * 32, v);
+        tmem_ld_32x32b_x32(tmem + lane_off + DQ_TM_DQ + c * 32, v);
         tmem_ld_wait();
         if (qrow < p.S) {
 #pragma unroll
@@ -1667,7 +1706,7 @@ kl_status attention_bwd_tc(int B, int S, int Hq, int Hkv, const void* q, const v
     KL_CUDA(cudaLaunchKernelEx(&cfg, fa_bwd_dkdv_tc_kernel, p));
   }
   KL_CUDA(cudaGetLastError());
-  // dQ: Q and dO tiles of 128 rows, K and V tiles of 64 rows
+  // dQ: Q and dO tiles of 128 rows (staged, then moved into TMEM), K and V tiles of 64 rows
   KL_TRY(map_rows(&p.tmQ, q, static_cast<uint64_t>(Hq) * HD, T, 128));
   KL_TRY(map_rows(&p.tmdO, dout, static_cast<uint64_t>(Hq) * HD, T, 128));
   KL_TRY(map_rows(&p.tmK, k, static_cast<uint64_t>(Hkv) * HD, T, 64));

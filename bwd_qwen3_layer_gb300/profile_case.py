@@ -9,7 +9,7 @@ Cases (T = 2048 tokens, hidden 5120, 64/8 heads of 128, intermediate 25600):
   gemm_qkv      q,k,v projections, 2048 x 10240 x 5120
   gemm_dgrad    dm = dY Wd, 2048 x 25600 x 5120 (B MN-major)
   gemm_wgrad    dWd = dY^T m, 5120 x 25600 x 2048 (both MN-major)
-  attn_fwd      causal GQA attention forward, S = 2048
+  attn_fwd      causal GQA attention forward, S = 2048 (--seq to change)
   attn_bwd      its backward
   ce            CE + argmax + dlogits on 4096 x 151936 fp32 logits
   rmsnorm_fwd   RMSNorm forward, 2048 x 5120
@@ -48,6 +48,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("case")
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--seq", type=int, default=T, help="attention cases: sequence length (batch 1)")
     a = ap.parse_args()
     torch.manual_seed(0)
     K.load()
@@ -71,21 +72,22 @@ def main():
         def run():
             K.kl_gemm(M, N, Kd, bf, A.data_ptr(), lda, amn, B.data_ptr(), ldb, bmn, C.data_ptr(), N, bf)
     elif a.case in ("attn_fwd", "attn_bwd"):
-        q, k, v = _rand((T, HQ * D)), _rand((T, HKV * D)), _rand((T, HKV * D))
+        S = a.seq
+        q, k, v = _rand((S, HQ * D)), _rand((S, HKV * D)), _rand((S, HKV * D))
         o = torch.empty_like(q)
-        lse = torch.empty(HQ, T, dtype=torch.float32, device="cuda")
-        K.kl_attention_fwd(1, T, HQ, HKV, D, bf, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+        lse = torch.empty(HQ, S, dtype=torch.float32, device="cuda")
+        K.kl_attention_fwd(1, S, HQ, HKV, D, bf, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                            lse.data_ptr())
-        do = _rand((T, HQ * D))
+        do = _rand((S, HQ * D))
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        ws = torch.empty(K.kl_attention_bwd_ws_bytes(1, T, HQ, HKV, D), dtype=torch.uint8, device="cuda")
+        ws = torch.empty(K.kl_attention_bwd_ws_bytes(1, S, HQ, HKV, D), dtype=torch.uint8, device="cuda")
 
         def run():
             if a.case == "attn_fwd":
-                K.kl_attention_fwd(1, T, HQ, HKV, D, bf, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                K.kl_attention_fwd(1, S, HQ, HKV, D, bf, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                    lse.data_ptr())
             else:
-                K.kl_attention_bwd(1, T, HQ, HKV, D, bf, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                K.kl_attention_bwd(1, S, HQ, HKV, D, bf, q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                    lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                                    ws.data_ptr(), ws.numel())
     elif a.case == "ce":
