@@ -40,7 +40,7 @@ class LayerCfg(ctypes.Structure):
 WEIGHT_FIELDS = ("gamma1", "wq", "wk", "wv", "wo", "gamma2", "wg", "wu", "wd")
 QK_WEIGHT_FIELDS = ("gamma_q", "gamma_k")   # read only with cfg.qk_norm
 SAVED_FIELDS = ("x", "h1", "rstd1", "q", "k", "v", "o", "lse", "x2", "h2", "rstd2", "g", "u", "m",
-                "q_pre", "k_pre", "rstd_q", "rstd_k")
+                "q_pre", "k_pre", "rstd_q", "rstd_k", "rope")
 
 
 class LayerWeights(ctypes.Structure):

@@ -145,6 +145,9 @@ struct Carver {
   }
 };
 
+// The rotary (cos, sin) table [S][d/2] used by the fused q/k projection, dQ and dK epilogues.
+size_t rope_table_bytes(const Dims& D) { return align_up(static_cast<size_t>(D.S) * (D.d / 2) * 8, 256); }
+
 void carve_saved(const Dims& D, Carver& c, kl_layer_saved* s) {
   const size_t T = D.T, es = D.es;
   s->h1 = c.take(T * D.H * es);
@@ -169,10 +172,8 @@ void carve_saved(const Dims& D, Carver& c, kl_layer_saved* s) {
     s->q_pre = s->k_pre = nullptr;
     s->rstd_q = s->rstd_k = nullptr;
   }
+  s->rope = D.dt == KL_BF16 ? static_cast<float*>(c.take(rope_table_bytes(D))) : nullptr;
 }
-
-// The rotary (cos, sin) table [S][d/2] used by the fused q/k projection and dQ epilogues.
-size_t rope_table_bytes(const Dims& D) { return align_up(static_cast<size_t>(D.S) * (D.d / 2) * 8, 256); }
 
 struct BwdWs {
   void *dm, *dg, *du, *dx2, *dO, *dq, *dk, *dv;
@@ -183,7 +184,6 @@ struct BwdWs {
   size_t norm_bytes;
   void* tail;             // fp32 scratch balancing the GEMM launches' last rounds (bf16)
   size_t tail_bytes;
-  float2* rope;           // rotary (cos, sin) table [S][d/2] for the fused dQ rotation (bf16)
   void *qk_q, *qk_k;      // gain-gradient partials of the per-head q / k norms (qk_norm)
   size_t qk_q_bytes, qk_k_bytes;
 };
@@ -206,7 +206,6 @@ void carve_bwd(const Dims& D, Carver& c, BwdWs* w) {
   w->norm = c.take(w->norm_bytes);
   w->tail_bytes = D.dt == KL_BF16 ? gemm_tail_ws_bytes() : 0;
   w->tail = w->tail_bytes ? c.take(w->tail_bytes) : nullptr;
-  w->rope = D.dt == KL_BF16 ? static_cast<float2*>(c.take(rope_table_bytes(D))) : nullptr;
   w->qk_q_bytes = D.qk_norm ? qk_rope_bwd_ws(D.T * D.Hq, D.d) : 0;
   w->qk_k_bytes = D.qk_norm ? qk_rope_bwd_ws(D.T * D.Hkv, D.d) : 0;
   w->qk_q = D.qk_norm ? c.take(w->qk_q_bytes) : nullptr;
@@ -325,7 +324,7 @@ kl_status kl_layer_saved_carve(const kl_layer_cfg* cfg, void* base, size_t bytes
 size_t kl_layer_fwd_workspace_bytes(const kl_layer_cfg* cfg) {
   Dims D;
   if (check_cfg(cfg, &D) != KL_OK) return 0;
-  return D.dt == KL_BF16 ? gemm_tail_ws_bytes() + rope_table_bytes(D) : 256;
+  return D.dt == KL_BF16 ? gemm_tail_ws_bytes() : 256;
 }
 
 size_t kl_layer_bwd_workspace_bytes(const kl_layer_cfg* cfg) {
@@ -360,16 +359,19 @@ kl_status kl_layer_forward(const kl_layer_cfg* cfg, const kl_layer_weights* w, c
     KL_TRY(check_ptrs({w->gamma_q, w->gamma_k}, "layer_forward q/k norm gains"));
     KL_TRY(check_ptrs({s->q_pre, s->k_pre, s->rstd_q, s->rstd_k}, "layer_forward q/k norm buffers"));
   }
-  // bf16 with the full workspace: tail scratch + rotary table (the rotation fused
-  // into the q/k projection's epilogue when neither layer option is on)
-  const bool fused = dt == KL_BF16 && ws && ws_bytes >= kl_layer_fwd_workspace_bytes(cfg) &&
+  // bf16: the rotary table is written with the first norm into the saved set (the
+  // rotation fused into the q/k projection's epilogue when neither layer option is
+  // on; the backward reads the same table); with the workspace, the projections'
+  // last round of tiles is split along K
+  const bool bf = dt == KL_BF16;
+  if (bf && !s->rope) return set_error(KL_ERR_INVALID_ARG, "layer_forward: saved rotary table missing");
+  const bool fused = bf && ws && ws_bytes >= kl_layer_fwd_workspace_bytes(cfg) &&
                      (reinterpret_cast<uintptr_t>(ws) & 255u) == 0;
   const bool options = D.qk_norm || D.inter;
   const size_t tail_bytes = fused ? gemm_tail_ws_bytes() : 0;
-  float2* rope_tab = fused ? reinterpret_cast<float2*>(static_cast<uint8_t*>(ws) + tail_bytes) : nullptr;
+  float2* rope_tab = bf ? reinterpret_cast<float2*>(s->rope) : nullptr;
   s->x = X;
-  KL_TRY(rmsnorm_fwd(T, H, dt, X, w->gamma1, cfg->eps, s->h1, s->rstd1, st));
-  if (fused) KL_TRY(rope_cs_table(D.S, D.d, cfg->rope_base, rope_tab, st));
+  KL_TRY(rmsnorm_fwd(T, H, dt, X, w->gamma1, cfg->eps, s->h1, s->rstd1, st, D.S, D.d, cfg->rope_base, rope_tab));
   {
     // with the q/k norm the projections land in q_pre / k_pre first
     void* qdst = D.qk_norm ? s->q_pre : s->q;
@@ -377,13 +379,11 @@ kl_status kl_layer_forward(const kl_layer_cfg* cfg, const kl_layer_weights* w, c
     GemmSpec g[3] = {proj(T, D.Dq, H, s->h1, H, w->wq, H, qdst, D.Dq, dt),
                      proj(T, D.Dkv, H, s->h1, H, w->wk, H, kdst, D.Dkv, dt),
                      proj(T, D.Dkv, H, s->h1, H, w->wv, H, s->v, D.Dkv, dt)};
-    if (fused) {
-      with_tail(g, 3, ws, tail_bytes);
-      for (int i = 0; i < 2 && !options; ++i) {   // q and k leave the epilogue rotated
-        g[i].epi = GEMM_EPI_ROPE;
-        g[i].rope_cs = rope_tab;
-        g[i].rope_S = D.S;
-      }
+    if (fused) with_tail(g, 3, ws, tail_bytes);
+    for (int i = 0; i < 2 && bf && !options; ++i) {   // q and k leave the epilogue rotated
+      g[i].epi = GEMM_EPI_ROPE;
+      g[i].rope_cs = rope_tab;
+      g[i].rope_S = D.S;
     }
     KL_TRY(run_gemms(dt, g, 3, st, "gemm.fwd_qkv"));
   }
@@ -395,7 +395,7 @@ kl_status kl_layer_forward(const kl_layer_cfg* cfg, const kl_layer_weights* w, c
                        rope_tab, s->q, s->rstd_q, st));
     KL_TRY(qk_rope_fwd(T, D.Hkv, D.S, D.d, dt, ksrc, w->gamma_k, cfg->eps, D.qk_norm, D.inter, cfg->rope_base,
                        rope_tab, s->k, s->rstd_k, st));
-  } else if (!fused) {
+  } else if (!bf) {
     KL_TRY(rope_qk(D.B, D.S, D.Hq, D.Hkv, D.d, cfg->rope_base, dt, s->q, s->k, 1, st));
   }
   KL_TRY(attention_fwd(D.B, D.S, D.Hq, D.Hkv, D.d, dt, s->q, s->k, s->v, s->o, s->lse, st));
@@ -498,13 +498,14 @@ kl_status kl_layer_backward(const kl_layer_cfg* cfg, const kl_layer_weights* w,
     KL_TRY(run_gemms(dt, g, 2, st, "gemm.bwd_o"));
   }
   float *dq_acc = nullptr, *dk_acc = nullptr, *dv_acc = nullptr;
-  if (b.rope) KL_TRY(rope_cs_table(D.S, D.d, cfg->rope_base, b.rope, st));
+  const float2* rope = reinterpret_cast<const float2*>(s->rope);   // bf16: the forward's table
+  if (dt == KL_BF16 && !rope) return set_error(KL_ERR_INVALID_ARG, "layer_backward: saved rotary table missing");
   if (!D.qk_norm && !D.inter) {
     // bf16: dQ leaves the attention kernel rotated back and converted; dK, dV (summed
     // over each kv head's query heads) are finished below
     KL_TRY(attention_bwd_accum(D.B, D.S, D.Hq, D.Hkv, D.d, dt, s->q, s->k, s->v, s->o, s->lse, b.dO,
                                b.att, b.att_bytes, &dq_acc, &dk_acc, &dv_acc, st, d_ready,
-                               b.rope ? b.dq : nullptr, b.rope, b.dk, b.dv));
+                               rope ? b.dq : nullptr, rope, b.dk, b.dv));
     if (dk_acc)   // fp32: the accumulators are rotated back and stored here
       KL_TRY(rope_bwd_convert(D.B, D.S, dq_acc ? D.Hq : 0, D.Hkv, D.d, cfg->rope_base, dt, dq_acc, dk_acc, dv_acc,
                               b.dq, b.dk, b.dv, st));
@@ -517,11 +518,11 @@ kl_status kl_layer_backward(const kl_layer_cfg* cfg, const kl_layer_weights* w,
     // bf16: dQ and dK (still rotated) are read from and rewritten in place in b.dq, b.dk
     const void* dqr = dq_acc ? static_cast<const void*>(dq_acc) : b.dq;
     KL_TRY(qk_rope_bwd(T, D.Hq, D.S, D.d, dt, dqr, dq_acc ? KL_F32 : KL_BF16, s->q_pre, w->gamma_q, s->rstd_q,
-                       D.qk_norm, D.inter, cfg->rope_base, b.rope, b.dq, static_cast<float*>(gr->gamma_q), b.qk_q,
+                       D.qk_norm, D.inter, cfg->rope_base, rope, b.dq, static_cast<float*>(gr->gamma_q), b.qk_q,
                        b.qk_q_bytes, st));
     const void* dkr = dk_acc ? static_cast<const void*>(dk_acc) : b.dk;
     KL_TRY(qk_rope_bwd(T, D.Hkv, D.S, D.d, dt, dkr, dk_acc ? KL_F32 : KL_BF16, s->k_pre, w->gamma_k, s->rstd_k,
-                       D.qk_norm, D.inter, cfg->rope_base, b.rope, b.dk, static_cast<float*>(gr->gamma_k), b.qk_k,
+                       D.qk_norm, D.inter, cfg->rope_base, rope, b.dk, static_cast<float*>(gr->gamma_k), b.qk_k,
                        b.qk_k_bytes, st));
     if (dv_acc) KL_TRY(convert_f32(static_cast<int64_t>(T) * D.Dkv, dt, dv_acc, b.dv, st));
   }

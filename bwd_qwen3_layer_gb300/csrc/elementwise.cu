@@ -63,6 +63,42 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ---------------------------------------------------------------------------
+// RoPE. Plane i pairs element i with element i + d/2 and turns it by the
+// angle s * base^(-2i/d). The angle is reduced exactly in fixed point, as a
+// phase accumulator does: plane i's rate in turns per position,
+// base^(-2i/d) / (2 pi), is formed on the host in fp64 and passed as a 64-bit
+// binary fraction of a turn; on the device s times that rate, taken modulo
+// 2^64 by the integer multiply, is the position's angle in turns modulo one,
+// and its top 32 bits read as a signed integer give the remainder in
+// [-pi, pi) for the fp32 sincosf. No fp64 arithmetic runs on the device; the
+// angle error is ~1e-11 rad from the rate plus 2^-32 of a turn from the
+// truncation, below the fp32 rounding of the remainder itself.
+// ---------------------------------------------------------------------------
+constexpr int ROPE_MAX_HALF = 128;
+struct RopeFreq {
+  uint64_t turn[ROPE_MAX_HALF];   // plane i's rate, turns per position, in units of 2^-64 turn
+};
+
+RopeFreq rope_freq(int d, float base) {
+  RopeFreq f;
+  for (int i = 0; i < ROPE_MAX_HALF; ++i) {
+    const double rate = i < d / 2 ? pow(static_cast<double>(base), -2.0 * i / d) / 6.283185307179586 : 0.0;
+    f.turn[i] = static_cast<uint64_t>(ldexp(rate, 64));   // rate < 1/(2 pi): fits in 64 bits
+  }
+  return f;
+}
+
+__device__ __forceinline__ void rope_cos_sin(int s, uint64_t turn, float dir, float* c, float* sn) {
+  const uint64_t phase = static_cast<uint64_t>(s) * turn;            // turns mod 1, in 2^-64 units
+  const int32_t hi = static_cast<int32_t>(static_cast<uint32_t>(phase >> 32));
+  const float r = static_cast<float>(hi) * 1.46291807926715968e-09f;  // 2 pi / 2^32
+  float sf, cf;
+  sincosf(r, &sf, &cf);
+  *c = cf;
+  *sn = dir * sf;
+}
+
+// ---------------------------------------------------------------------------
 // RMSNorm forward: one warp per row.
 // ---------------------------------------------------------------------------
 template <typename T, bool VEC>
@@ -114,11 +150,15 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_kernel(int rows, int width,
 // once; sum of squares by warp shuffles plus one barrier.
 constexpr int RF_THREADS = 128, RF_MAXC = 8;
 
+// With a table (cs non-null), the CTA of row s < S also writes the rotary
+// (cos, sin) row of position s, [S][half], while its loads are in flight.
 template <typename T, int NC>
 __global__ void __launch_bounds__(RF_THREADS) rmsnorm_fwd_row_kernel(int width, const T* __restrict__ x,
                                                                      const T* __restrict__ gamma, float eps,
                                                                      T* __restrict__ h,
-                                                                     float* __restrict__ rstd) {
+                                                                     float* __restrict__ rstd, int S,
+                                                                     int half, const RopeFreq f,
+                                                                     float2* __restrict__ cs) {
   pdl_enter();
   __shared__ float red[RF_THREADS / 32];
   constexpr int V = Vec<T>::N;
@@ -132,6 +172,13 @@ __global__ void __launch_bounds__(RF_THREADS) rmsnorm_fwd_row_kernel(int width, 
     if (c < chunks) {
       raw[j] = *reinterpret_cast<const uint4*>(x + off + c * V);
       graw[j] = *reinterpret_cast<const uint4*>(gamma + c * V);
+    }
+  }
+  if (cs && row < S) {
+    for (int i = tid; i < half; i += RF_THREADS) {
+      float c, sn;
+      rope_cos_sin(row, f.turn[i], 1.0f, &c, &sn);
+      cs[static_cast<int64_t>(row) * half + i] = make_float2(c, sn);
     }
   }
   float ss = 0.f;
@@ -453,43 +500,10 @@ int rmsnorm_bwd_grid(int rows) {
   return want < cap ? want : cap;
 }
 
-// ---------------------------------------------------------------------------
-// RoPE. Plane i pairs element i with element i + d/2 and turns it by the
-// angle s * base^(-2i/d). The inverse frequencies are formed on the host in
-// fp64 and passed by value; on the device the angle s * inv_freq is formed in
-// fp64 and reduced modulo 2 pi with a two-part constant (Cody and Waite's
-// reduction), so that only a remainder in [-pi, pi] goes to the fp32 sincosf.
-// The absolute error of cos/sin is then a few fp32 ulps of 1 at any position.
-// ---------------------------------------------------------------------------
-constexpr int ROPE_MAX_HALF = 128;
-struct RopeFreq {
-  double inv[ROPE_MAX_HALF];
-};
-
-RopeFreq rope_freq(int d, float base) {
-  RopeFreq f;
-  for (int i = 0; i < ROPE_MAX_HALF; ++i)
-    f.inv[i] = i < d / 2 ? pow(static_cast<double>(base), -2.0 * i / d) : 0.0;
-  return f;
-}
-
-__device__ __forceinline__ void rope_cos_sin(int s, double inv, float dir, float* c, float* sn) {
-  const double two_pi_hi = 6.283185307179586;           // 2 pi rounded to double
-  const double two_pi_lo = 2.4492935982947064e-16;      // 2 pi - two_pi_hi
-  const double a = static_cast<double>(s) * inv;
-  const double k = rint(a * (1.0 / 6.283185307179586));
-  double r = fma(-k, two_pi_hi, a);
-  r = fma(-k, two_pi_lo, r);
-  float sf, cf;
-  sincosf(static_cast<float>(r), &sf, &cf);
-  *c = cf;
-  *sn = dir * sf;
-}
-
 // cos in cs[0, half), dir*sin in cs[half, d); the caller synchronises.
 __device__ __forceinline__ void rope_table(int s, int d, const RopeFreq& f, float dir, float* cs) {
   const int half = d / 2;
-  for (int i = threadIdx.x; i < half; i += blockDim.x) rope_cos_sin(s, f.inv[i], dir, &cs[i], &cs[half + i]);
+  for (int i = threadIdx.x; i < half; i += blockDim.x) rope_cos_sin(s, f.turn[i], dir, &cs[i], &cs[half + i]);
 }
 
 // The (cos, sin) table of every position and plane: consumed by the fused
@@ -501,7 +515,7 @@ __global__ void rope_cs_kernel(int S, int half, RopeFreq f, float2* __restrict__
        idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int s = static_cast<int>(idx / half), i = static_cast<int>(idx - static_cast<int64_t>(s) * half);
     float c, sn;
-    rope_cos_sin(s, f.inv[i], 1.0f, &c, &sn);
+    rope_cos_sin(s, f.turn[i], 1.0f, &c, &sn);
     cs[idx] = make_float2(c, sn);
   }
 }
@@ -663,7 +677,7 @@ __device__ __forceinline__ void plane_idx(int i, int d, int inter, int& ia, int&
 __device__ __forceinline__ float2 plane_cs(int pos, int i, int half, const RopeFreq& f, const float2* tab) {
   if (tab) return tab[static_cast<int64_t>(pos) * half + i];
   float c, sn;
-  rope_cos_sin(pos, f.inv[i], 1.0f, &c, &sn);
+  rope_cos_sin(pos, f.turn[i], 1.0f, &c, &sn);
   return make_float2(c, sn);
 }
 
@@ -944,28 +958,38 @@ int ew_grid(int64_t work_items) {
 }  // namespace
 
 kl_status rmsnorm_fwd(int rows, int width, int dtype, const void* x, const void* gamma, float eps,
-                      void* h, float* rstd, cudaStream_t st) {
+                      void* h, float* rstd, cudaStream_t st, int rope_S, int rope_d, float rope_base,
+                      float2* rope_cs) {
   if (rows < 1 || width < 1 || !x || !gamma || !h || !rstd)
     return set_error(KL_ERR_INVALID_ARG, "rmsnorm_fwd: bad arguments");
-  const int grid = (rows + 7) / 8;
-  ProfScope ps("rmsnorm_fwd", st, 0.0,
-               2.0 * rows * width * dtype_size(dtype) + 4.0 * rows + 1.0 * width * dtype_size(dtype));
   if (dtype != KL_BF16 && dtype != KL_F32) return set_error(KL_ERR_INVALID_ARG, "rmsnorm_fwd: bad dtype %d", dtype);
+  const int grid = (rows + 7) / 8;
   const int V = dtype == KL_BF16 ? 8 : 4;
   const bool vec = width % V == 0 && al16(x) && al16(gamma) && al16(h);
   const int nc = (width / V + RF_THREADS - 1) / RF_THREADS;
-  if (vec && nc <= RF_MAXC) {
+  const bool row_form = vec && nc <= RF_MAXC;
+  // the rotary table rides with the row form (one CTA per row); otherwise its own launch
+  const bool tab = rope_cs && row_form && rope_S <= rows && rope_d >= 2 && (rope_d & 1) == 0 &&
+                   rope_d / 2 <= ROPE_MAX_HALF;
+  if (rope_cs && !tab) KL_TRY(rope_cs_table(rope_S, rope_d, rope_base, rope_cs, st));
+  const int rhalf = tab ? rope_d / 2 : 0;
+  const RopeFreq f = rope_freq(tab ? rope_d : 2, rope_base);
+  float2* cs = tab ? rope_cs : nullptr;
+  ProfScope ps("rmsnorm_fwd", st, 0.0,
+               2.0 * rows * width * dtype_size(dtype) + 4.0 * rows + 1.0 * width * dtype_size(dtype) +
+                   8.0 * rope_S * rhalf);
+  if (row_form) {
     if (dtype == KL_BF16) {
       using T = __nv_bfloat16;
       switch (nc) {
-#define KL_RF_CASE(N) case N: launch_pdl(rmsnorm_fwd_row_kernel<T, N>, rows, RF_THREADS, 0, st, width, (const T*)x, (const T*)gamma, eps, (T*)h, rstd); break;
+#define KL_RF_CASE(N) case N: launch_pdl(rmsnorm_fwd_row_kernel<T, N>, rows, RF_THREADS, 0, st, width, (const T*)x, (const T*)gamma, eps, (T*)h, rstd, rope_S, rhalf, f, cs); break;
         KL_RF_CASE(1) KL_RF_CASE(2) KL_RF_CASE(3) KL_RF_CASE(4) KL_RF_CASE(5) KL_RF_CASE(6) KL_RF_CASE(7) KL_RF_CASE(8)
 #undef KL_RF_CASE
       }
     } else {
       using T = float;
       switch (nc) {
-#define KL_RF_CASE(N) case N: launch_pdl(rmsnorm_fwd_row_kernel<T, N>, rows, RF_THREADS, 0, st, width, (const T*)x, (const T*)gamma, eps, (T*)h, rstd); break;
+#define KL_RF_CASE(N) case N: launch_pdl(rmsnorm_fwd_row_kernel<T, N>, rows, RF_THREADS, 0, st, width, (const T*)x, (const T*)gamma, eps, (T*)h, rstd, rope_S, rhalf, f, cs); break;
         KL_RF_CASE(1) KL_RF_CASE(2) KL_RF_CASE(3) KL_RF_CASE(4) KL_RF_CASE(5) KL_RF_CASE(6) KL_RF_CASE(7) KL_RF_CASE(8)
 #undef KL_RF_CASE
       }

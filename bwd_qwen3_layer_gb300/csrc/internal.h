@@ -100,8 +100,11 @@ kl_status gemm_f32(const GemmSpec& spec, cudaStream_t st, const char* label = "g
 // ---------------------------------------------------------------------------
 // elementwise / normalisation kernels (elementwise.cu)
 // ---------------------------------------------------------------------------
+// With rope_cs, also writes the rotary (cos, sin) table [rope_S][rope_d / 2] of
+// base rope_base (in the same launch when the rows take the row form).
 kl_status rmsnorm_fwd(int rows, int width, int dtype, const void* x, const void* gamma, float eps,
-                      void* h, float* rstd, cudaStream_t st);
+                      void* h, float* rstd, cudaStream_t st, int rope_S = 0, int rope_d = 0,
+                      float rope_base = 0.f, float2* rope_cs = nullptr);
 size_t rmsnorm_bwd_ws(int rows, int width);
 kl_status rmsnorm_bwd(int rows, int width, int dtype, const void* dh, int dh_dtype, const void* x,
                       const void* gamma, const float* rstd, const void* resid, void* dx,

@@ -159,6 +159,9 @@ typedef struct kl_layer_saved {
   void* k_pre;         /* [T,Hkv*d] key projection before its norm          */
   float* rstd_q;       /* [T,Hq]  per-head 1/sqrt(mean(q^2)+eps)            */
   float* rstd_k;       /* [T,Hkv]                                           */
+  /* KL_BF16 only (NULL otherwise): the rotary (cos, sin) pairs [S][d/2] fp32,
+   * written by the forward (with the first norm), read by the backward. */
+  float* rope;
 } kl_layer_saved;
 
 /* Gradients written by the backward (device, caller-owned). Projection

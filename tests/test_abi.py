@@ -53,9 +53,10 @@ def _cfg(**kw):
 def test_saved_and_workspace_sizes(lib):
     cfg = _cfg()
     T, H, I, Dq, Dkv = 2048, 5120, 25600, 8192, 1024
-    need = (3 * T * H + 2 * T * Dq + 2 * T * Dkv + 3 * T * I) * 2 + 2 * T * 4 + 64 * T * 4
+    # bf16 activations, fp32 rstd1/rstd2 and lse, and the rotary (cos, sin) table [S][64]
+    need = (3 * T * H + 2 * T * Dq + 2 * T * Dkv + 3 * T * I) * 2 + 2 * T * 4 + 64 * T * 4 + T * 64 * 8
     got = K.kl_layer_saved_bytes(cfg)
-    assert need <= got <= need + 14 * 256
+    assert need <= got <= need + 15 * 256
     assert K.kl_layer_bwd_workspace_bytes(cfg) > 3 * T * I * 2
     # fp32 saved set is twice as large (up to alignment)
     cfg32 = _cfg(dtype=K.KL_F32, B=1, S=32, H=64, Hq=4, Hkv=2, d=16, I=172)

@@ -48,8 +48,11 @@ def test_rmsnorm(kl, dt, rows, width):
     assert_rel(host(dg), dg_ref, 1e-5, "dgamma")
 
 
-@pytest.mark.parametrize("dt,B,S,heads,d", [(1, 2, 77, 9, 128), (0, 1, 32, 4, 16), (1, 1, 4096, 2, 128)])
+@pytest.mark.parametrize("dt,B,S,heads,d", [(1, 2, 77, 9, 128), (0, 1, 32, 4, 16), (1, 1, 4096, 2, 128),
+                                            (0, 1, 40000, 1, 128)])
 def test_rope(kl, dt, B, S, heads, d):
+    """Both directions against the oracle; the fp32 case at 40000 positions holds
+    the angle reduction (fixed-point turns) to fp32 accuracy far along a sequence."""
     base = 1e6
     x = _maybe_round(synth.normal(0, "rope.x", (B * S, heads, d)), dt)
     X = dev(x.reshape(B * S, heads * d), DT[dt])
