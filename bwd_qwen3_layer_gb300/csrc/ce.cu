@@ -2,18 +2,18 @@
 // GPU LLM training", capability list: GPU lm-head, softmax cross-entropy and
 // argmax fused in a single launch).
 //
-// One row of fp32 logits per 8-CTA thread-block cluster. Each CTA copies its
-// eighth of the row (the vocabulary tile) into shared memory once, reduces
-// max / lowest argmax over it, then replaces each logit by e = exp(z - tile
-// max) and sums them, publishes the three numbers in shared memory and reads
-// its seven peers' through distributed shared memory to form the row's
-// logsumexp and argmax. It then writes dlogits = (e exp(tile max - lse) -
-// onehot) / N for its tile from shared memory: one exp per logit, the row read
-// from HBM exactly once and dlogits written once. The mean loss is reduced in
-// a fixed order by the last cluster to finish (deterministic).
+// One row of fp32 logits per 8-CTA thread-block cluster, each CTA a slice of
+// the vocabulary. Pass 1 reads the slice once and keeps per-thread running
+// summaries (maximum, sum of exponentials against it, lowest argmax); the
+// summaries merge across the warp, the CTA and the cluster (distributed shared
+// memory, rank order) into the row's logsumexp and argmax. Pass 2 reads the
+// slice again from L2 and writes dlogits = (softmax - onehot) / N once. The
+// mean loss is reduced in a fixed order by the last cluster to finish
+// (deterministic).
 #include <cooperative_groups.h>
 #include <limits.h>
 #include <math.h>
+#include <stdlib.h>
 
 #include <mutex>
 
@@ -25,12 +25,47 @@ namespace cg = cooperative_groups;
 namespace kl {
 namespace {
 
-// CTAs per row (cluster size) and threads per CTA. Measured on the 4096 x
-// 151936 workload: 8 x 256 beats 8 x 512 / 384 / 128 and 16 x 256 (two CTAs
-// of ~76 KB shared memory per SM either way).
-constexpr int CLUSTER = 8;
+// CTAs per row (cluster size, a template parameter: 8 portable, 16 with the
+// non-portable opt-in) and threads per CTA.
 constexpr int THREADS = 256;
 constexpr int NWARP = THREADS / 32;
+constexpr float LOG2E = 1.4426950408889634f;
+
+// Pass 1 marks the logits it reads for keeping in L2 (evict-last), pass 2
+// reads them for the last time (evict-first), so the ~150 rows in flight stay
+// in L2 between the passes; dlogits are written evict-first.
+struct f8 {
+  float v[8];
+};
+// 32-byte loads (Blackwell's 256-bit form, which carries the L2 priority)
+__device__ __forceinline__ f8 ld_keep(const float* p) {
+  f8 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::evict_last.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3]), "=f"(r.v[4]), "=f"(r.v[5]), "=f"(r.v[6]),
+                 "=f"(r.v[7])
+               : "l"(p));
+  return r;
+}
+__device__ __forceinline__ f8 ld_last(const float* p) {
+  f8 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::evict_first.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=f"(r.v[0]), "=f"(r.v[1]), "=f"(r.v[2]), "=f"(r.v[3]), "=f"(r.v[4]), "=f"(r.v[5]), "=f"(r.v[6]),
+                 "=f"(r.v[7])
+               : "l"(p));
+  return r;
+}
+__device__ __forceinline__ void st_stream(void* p, uint4 v) {
+  asm volatile("st.global.L1::no_allocate.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// 2^x by the hardware approximation (about 2 ulp; 0 for -inf).
+__device__ __forceinline__ float ex2a(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 struct Part {
   float m;
@@ -38,14 +73,41 @@ struct Part {
   int idx;
 };
 
-__device__ __forceinline__ void better(float& m, int& i, float m2, int i2) {
-  if (m2 > m || (m2 == m && i2 < i)) {
+// (m, s, idx) summarises a set of logits: its maximum m, the sum s of
+// exp(z - m) over it, and the lowest index attaining m. Merging two summaries
+// is exact up to the rescaling's rounding.
+__device__ __forceinline__ void merge(float& m, float& s, int& i, float m2, float s2, int i2) {
+  if (m2 > m) {
+    s = (m > -INFINITY ? s * ex2a((m - m2) * LOG2E) : 0.f) + s2;
     m = m2;
     i = i2;
+  } else {
+    if (m2 > -INFINITY) s += s2 * ex2a((m2 - m) * LOG2E);
+    if (m2 == m && i2 < i) i = i2;
   }
 }
 
-template <bool VEC>
+// Adds logit z at index j to the running summary (m, s, idx).
+__device__ __forceinline__ void add_logit(float& m, float& s, int& i, float z, int j) {
+  if (z > m) {
+    s = (m > -INFINITY ? s * ex2a((m - z) * LOG2E) : 0.f) + 1.f;
+    m = z;
+    i = j;
+  } else if (z > -INFINITY) {
+    s += ex2a((z - m) * LOG2E);
+    if (z == m && j < i) i = j;
+  }
+}
+
+// One row of logits per cluster of CLUSTER CTAs; CTA r takes the r-th slice
+// of the vocabulary. Pass 1 streams the slice once from HBM into per-thread
+// running summaries (maximum, sum of exponentials against it, lowest argmax),
+// merged across the warp, the CTA and (through distributed shared memory, in
+// rank order) the cluster into the row's logsumexp and argmax. Pass 2 reads
+// the slice again, from L2 (the rows in flight fit there), and writes
+// dlogits = (softmax - onehot) / N. No tile is held in shared memory, so eight
+// CTAs fit on an SM and keep enough loads in flight to stream at HBM rate.
+template <int CLUSTER, bool VEC>
 __global__ void __launch_bounds__(THREADS)
     ce_argmax_kernel(int N, int V, int slice, const float* __restrict__ z,
                      const int32_t* __restrict__ targets, float* __restrict__ loss_rows,
@@ -53,13 +115,11 @@ __global__ void __launch_bounds__(THREADS)
                      unsigned int* __restrict__ counter, float* __restrict__ loss,
                      uint32_t* __restrict__ err) {
   pdl_enter();
-  extern __shared__ __align__(16) float sz[];
   __shared__ float red_m[NWARP];
   __shared__ float red_s[NWARP];
   __shared__ int red_i[NWARP];
   __shared__ Part part;
   __shared__ int is_last;
-  __shared__ __align__(8) uint64_t load_bar;
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
   const int n = blockIdx.y;
@@ -68,140 +128,106 @@ __global__ void __launch_bounds__(THREADS)
   const int len = max(0, min(V, c0 + slice) - c0);
   const float* zr = z + static_cast<int64_t>(n) * V + c0;
 
-  // 1. copy the tile to shared memory; running max and lowest argmax
-  float m = -INFINITY;
+  // 1. running summary of this thread's logits (float4 loads, four in flight)
+  float m = -INFINITY, s = 0.f;
   int mi = INT_MAX;
   if (VEC) {
-    // One bulk asynchronous copy of the whole tile (16-byte aligned, length a
-    // multiple of 16 bytes), completed on an mbarrier: the row is in flight at
-    // once instead of one vector per thread.
-    const uint32_t bar = smem_u32(&load_bar);
-    if (threadIdx.x == 0) {
-      mbar_init(bar, 1);
-      fence_mbar_init();
+    constexpr int U = 2;
+    int i = threadIdx.x * 8;
+    for (; i + (U - 1) * THREADS * 8 < len; i += U * THREADS * 8) {
+      f8 a[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) a[u] = ld_keep(zr + i + u * THREADS * 8);
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) add_logit(m, s, mi, a[u].v[e], c0 + i + u * THREADS * 8 + e);
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      if (len > 0) {
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(len) * 4u);
-        bulk_copy_g2s(smem_u32(sz), zr, static_cast<uint32_t>(len) * 4u, bar);
-      } else {
-        mbar_arrive(bar);
-      }
-    }
-    mbar_wait(bar, 0, err);
-    for (int i = threadIdx.x * 4; i < len; i += THREADS * 4) {
-      const float4 a = *reinterpret_cast<const float4*>(sz + i);
-      better(m, mi, a.x, c0 + i);
-      better(m, mi, a.y, c0 + i + 1);
-      better(m, mi, a.z, c0 + i + 2);
-      better(m, mi, a.w, c0 + i + 3);
+    for (; i < len; i += THREADS * 8) {
+      const f8 a = ld_keep(zr + i);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) add_logit(m, s, mi, a.v[e], c0 + i + e);
     }
   } else {
-    for (int i = threadIdx.x; i < len; i += THREADS) {
-      const float a = zr[i];
-      sz[i] = a;
-      better(m, mi, a, c0 + i);
-    }
+    for (int i = threadIdx.x; i < len; i += THREADS) add_logit(m, s, mi, zr[i], c0 + i);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
     const int i2 = __shfl_xor_sync(0xffffffffu, mi, o);
-    better(m, mi, m2, i2);
+    merge(m, s, mi, m2, s2, i2);
   }
   if (lane == 0) {
     red_m[warp] = m;
+    red_s[warp] = s;
     red_i[warp] = mi;
   }
   __syncthreads();
-  float tm = red_m[0];
-  int ti = red_i[0];
-  for (int w = 1; w < NWARP; ++w) better(tm, ti, red_m[w], red_i[w]);
-  // 2. e = exp(z - tile max), kept in place (vector form), and its sum
-  float s = 0.f;
-  if (len > 0) {
-    if (VEC) {
-      for (int i = threadIdx.x * 4; i < len; i += THREADS * 4) {
-        float4 a = *reinterpret_cast<const float4*>(sz + i);
-        a.x = expf(a.x - tm);
-        a.y = expf(a.y - tm);
-        a.z = expf(a.z - tm);
-        a.w = expf(a.w - tm);
-        s += (a.x + a.y) + (a.z + a.w);
-        *reinterpret_cast<float4*>(sz + i) = a;
-      }
-    } else {
-      for (int i = threadIdx.x; i < len; i += THREADS) s += expf(sz[i] - tm);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if (lane == 0) red_s[warp] = s;
-  __syncthreads();
   if (threadIdx.x == 0) {
-    float ts = 0.f;
-    for (int w = 0; w < NWARP; ++w) ts += red_s[w];
+    float tm = red_m[0], ts = red_s[0];
+    int ti = red_i[0];
+    for (int w = 1; w < NWARP; ++w) merge(tm, ts, ti, red_m[w], red_s[w], red_i[w]);
     part.m = tm;
     part.s = ts;
     part.idx = ti;
   }
   cluster.sync();
-  // 3. combine the eight tiles (every CTA does it; fixed rank order)
-  float M = -INFINITY;
+  // 2. the row's summary from the CLUSTER slices (every CTA, fixed rank order)
+  float M = -INFINITY, tot = 0.f;
   int I = INT_MAX;
-  Part ps[CLUSTER];
 #pragma unroll
   for (int r = 0; r < CLUSTER; ++r) {
-    ps[r] = *cluster.map_shared_rank(&part, r);
-    better(M, I, ps[r].m, ps[r].idx);
+    const Part q = *cluster.map_shared_rank(&part, r);
+    merge(M, tot, I, q.m, q.s, q.idx);
   }
-  float tot = 0.f;
-#pragma unroll
-  for (int r = 0; r < CLUSTER; ++r)
-    if (ps[r].s > 0.f) tot += ps[r].s * expf(ps[r].m - M);
   const float lse = M + logf(tot);
+  const float lsel = lse * LOG2E;
   int t = targets[n];
   const bool t_ok = t >= 0 && t < V;
   if (!t_ok) {
     if (threadIdx.x == 0 && rank == 0) record_error(err, KL_DEVERR_TARGET);
     t = -1;
   }
-  // 4. dlogits for this tile
+  // 3. dlogits for this slice (the logits again, now from L2)
   if (dz_f32) {
     float* out = static_cast<float*>(dz) + static_cast<int64_t>(n) * V + c0;
-    const float sc = len > 0 && tm > -INFINITY ? expf(tm - lse) : 0.f;
     for (int i = threadIdx.x; i < len; i += THREADS) {
-      float p = VEC ? sz[i] * sc : expf(sz[i] - lse);
+      float p = ex2a(fmaf(zr[i], LOG2E, -lsel));
       if (c0 + i == t) p -= 1.f;
       out[i] = p * invN;
     }
   } else {
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(dz) + static_cast<int64_t>(n) * V + c0;
     if (VEC) {
-      const float sc = len > 0 && tm > -INFINITY ? expf(tm - lse) : 0.f;   // the tile holds exp(z - tm)
-      for (int i = threadIdx.x * 4; i < len; i += THREADS * 4) {
-        const float4 a = *reinterpret_cast<const float4*>(sz + i);
-        float p0 = a.x * sc, p1 = a.y * sc, p2 = a.z * sc, p3 = a.w * sc;
+#pragma unroll 2
+      for (int i = threadIdx.x * 8; i < len; i += THREADS * 8) {
+        const f8 a = ld_last(zr + i);
+        float p[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) p[e] = ex2a(fmaf(a.v[e], LOG2E, -lsel));
         const int d = t - (c0 + i);
-        if (d == 0) p0 -= 1.f;
-        if (d == 1) p1 -= 1.f;
-        if (d == 2) p2 -= 1.f;
-        if (d == 3) p3 -= 1.f;
-        uint2 o;
-        o.x = pack_bf16x2(p0 * invN, p1 * invN);
-        o.y = pack_bf16x2(p2 * invN, p3 * invN);
-        *reinterpret_cast<uint2*>(out + i) = o;
+        if (d >= 0 && d < 8) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (e == d) p[e] -= 1.f;
+        }
+        uint4 o;
+        o.x = pack_bf16x2(p[0] * invN, p[1] * invN);
+        o.y = pack_bf16x2(p[2] * invN, p[3] * invN);
+        o.z = pack_bf16x2(p[4] * invN, p[5] * invN);
+        o.w = pack_bf16x2(p[6] * invN, p[7] * invN);
+        st_stream(out + i, o);
       }
     } else {
       for (int i = threadIdx.x; i < len; i += THREADS) {
-        float p = expf(sz[i] - lse);
+        float p = ex2a(fmaf(zr[i], LOG2E, -lsel));
         if (c0 + i == t) p -= 1.f;
         out[i] = __float2bfloat16_rn(p * invN);
       }
     }
   }
-  // 5. per-row loss and argmax; the last row to finish reduces the mean
+  // 4. per-row loss and argmax; the last row to finish reduces the mean
   if (rank == 0 && threadIdx.x == 0) {
     const float zt = t_ok ? z[static_cast<int64_t>(n) * V + t] : lse;
     loss_rows[n] = lse - zt;
@@ -233,6 +259,16 @@ __global__ void __launch_bounds__(THREADS)
 
 size_t ce_ws(int N) { return align_up(static_cast<size_t>(N) * 4, 256) + 256; }
 
+// CTAs per row. Tuning override: KL_CE_CLUSTER = 8 or 16.
+int ce_cluster_size(int V) {
+  (void)V;
+  if (const char* e = getenv("KL_CE_CLUSTER")) {
+    const int v = atoi(e);
+    if (v == 8 || v == 16) return v;
+  }
+  return 8;
+}
+
 kl_status ce_argmax(int N, int V, const float* z, const int32_t* targets, float* loss,
                     int32_t* argmax, void* dz, int dz_dtype, void* ws, size_t ws_bytes,
                     cudaStream_t st) {
@@ -240,33 +276,33 @@ kl_status ce_argmax(int N, int V, const float* z, const int32_t* targets, float*
     return set_error(KL_ERR_INVALID_ARG, "ce_argmax: bad arguments");
   if (N > 65535) return set_error(KL_ERR_UNSUPPORTED, "ce_argmax: N above 65535");
   if (!ws || ws_bytes < ce_ws(N)) return set_error(KL_ERR_NO_MEMORY, "ce_argmax: workspace too small");
-  const bool vec = V % 4 == 0 && (reinterpret_cast<uintptr_t>(z) & 15u) == 0 &&
-                   (dz_dtype == KL_F32 || (reinterpret_cast<uintptr_t>(dz) & 7u) == 0);
-  int slice = (V + CLUSTER - 1) / CLUSTER;
-  slice = (slice + 3) / 4 * 4;
-  const size_t smem = static_cast<size_t>(slice) * sizeof(float);
-  if (smem > 200 * 1024) return set_error(KL_ERR_UNSUPPORTED, "ce_argmax: vocabulary %d too large", V);
+  // the vector path: 32-byte logit loads, 16-byte bf16 dlogit stores
+  const bool vec = V % 8 == 0 && (reinterpret_cast<uintptr_t>(z) & 31u) == 0 &&
+                   (dz_dtype == KL_F32 || (reinterpret_cast<uintptr_t>(dz) & 15u) == 0);
+  const int CL = ce_cluster_size(V);
+  int slice = (V + CL - 1) / CL;
+  slice = (slice + 7) / 8 * 8;
   float* loss_rows = static_cast<float*>(ws);
   unsigned int* counter =
       reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + align_up(static_cast<size_t>(N) * 4, 256));
   KL_CUDA(cudaMemsetAsync(counter, 0, sizeof(unsigned int), st));
-  dim3 grid(CLUSTER, N);
+  dim3 grid(CL, N);
   ProfScope ps("ce_argmax", st, 0.0, static_cast<double>(N) * V * (4 + dtype_size(dz_dtype)) + 12.0 * N);
   const float invN = 1.0f / static_cast<float>(N);
   const int f32 = dz_dtype == KL_F32;
   auto launch = [&](auto kernel) -> kl_status {
-    KL_CUDA(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)));
+    if (CL > 8) KL_CUDA(cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CLUSTER;
+    attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see pdl_enter
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.gridDim = grid;
     cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
@@ -274,8 +310,13 @@ kl_status ce_argmax(int N, int V, const float* z, const int32_t* targets, float*
                                device_error_word()));
     return KL_OK;
   };
-  if (vec) KL_TRY(launch(ce_argmax_kernel<true>));
-  else KL_TRY(launch(ce_argmax_kernel<false>));
+  if (CL == 16) {
+    if (vec) KL_TRY(launch(ce_argmax_kernel<16, true>));
+    else KL_TRY(launch(ce_argmax_kernel<16, false>));
+  } else {
+    if (vec) KL_TRY(launch(ce_argmax_kernel<8, true>));
+    else KL_TRY(launch(ce_argmax_kernel<8, false>));
+  }
   KL_CUDA(cudaGetLastError());
   return KL_OK;
 }

@@ -11,7 +11,7 @@ Cases (T = 2048 tokens, hidden 5120, 64/8 heads of 128, intermediate 25600):
   gemm_wgrad    dWd = dY^T m, 5120 x 25600 x 2048 (both MN-major)
   attn_fwd      causal GQA attention forward, S = 2048 (--seq to change)
   attn_bwd      its backward
-  ce            CE + argmax + dlogits on 4096 x 151936 fp32 logits
+  ce            CE + argmax + dlogits on 4096 x 151936 fp32 logits (--rows to change)
   rmsnorm_fwd   RMSNorm forward, 2048 x 5120
   rmsnorm_bwd   RMSNorm backward with fp32 dh and a residual gradient, 2048 x 5120
   rope          in-place rotation of q [2048, 64, 128]
@@ -49,6 +49,7 @@ def main():
     ap.add_argument("case")
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--seq", type=int, default=T, help="attention cases: sequence length (batch 1)")
+    ap.add_argument("--rows", type=int, default=4096, help="ce: rows of logits")
     a = ap.parse_args()
     torch.manual_seed(0)
     K.load()
@@ -91,7 +92,7 @@ def main():
                                    lse.data_ptr(), do.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
                                    ws.data_ptr(), ws.numel())
     elif a.case == "ce":
-        N, V = 4096, 151936
+        N, V = a.rows, 151936
         z = torch.randn(N, V, device="cuda") * 4
         tgt = torch.randint(0, V, (N,), device="cuda", dtype=torch.int32)
         loss = torch.zeros(1, device="cuda")
