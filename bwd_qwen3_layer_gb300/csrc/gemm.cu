@@ -65,6 +65,7 @@ struct GemmProb {
   int dot_S;
   const float2* rope_cs;  // GEMM_EPI_ROPE: [rope_S][64] cos/sin
   int rope_S;
+  int tma_c;              // plain stores leave through shared memory and a TMA store (map tmC[problem])
   int whole_tiles;        // tiles computed whole; the rest (tail) are split along K
   int tail_tiles, tail_splits;
   float* tail_acc;        // [tail_splits][tail_tiles][256][256] fp32, one slice per K range
@@ -73,6 +74,7 @@ struct GemmProb {
 struct GemmParams {
   CUtensorMap tmA[GEMM_MAX_PROB * GEMM_MAX_SEG];
   CUtensorMap tmB[GEMM_MAX_PROB * GEMM_MAX_SEG];
+  CUtensorMap tmC[GEMM_MAX_PROB];   // output maps of the problems with tma_c (box 32 x 32)
   GemmProb prob[GEMM_MAX_PROB];
   int nprob;
   int total_units;
@@ -329,7 +331,13 @@ constexpr int PAIR_THREADS = SPLIT_PRODUCER ? 224 : 192;
 constexpr uint32_t HALF_BYTES = 128 * BK * 2;            // 16 KB
 constexpr uint32_t KB2_BYTES = 2 * HALF_BYTES;           // one k-block: A half + B half
 constexpr uint32_t STAGE2_BYTES = KPS * KB2_BYTES;
-constexpr size_t SMEM2_BYTES = 1024 + STAGES2 * STAGE2_BYTES + 512;
+// Output staging of the plain-store epilogue: per epilogue warp two buffers of
+// 32 rows x 32 columns (4 KB for fp32), filled in the TMA store's swizzled
+// layout (64-byte swizzle for bf16 rows of 64 bytes, 128-byte for fp32 rows).
+constexpr uint32_t STG_BUF = 32 * 32 * 4;
+constexpr uint32_t STG_BYTES = 4 * 2 * STG_BUF;
+constexpr uint32_t BAR_BYTES = 1024;   // barriers and scheduler slots; keeps the staging 1024-aligned
+constexpr size_t SMEM2_BYTES = 1024 + STAGES2 * STAGE2_BYTES + BAR_BYTES + STG_BYTES;
 static_assert(SMEM2_BYTES <= 232448, "pair-kernel shared memory above the per-CTA limit");
 
 __device__ __forceinline__ uint32_t mapa_rank(uint32_t addr, uint32_t rank) {
@@ -483,6 +491,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * STAGES2 + 5 + 2 * SCHED_Q);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   volatile int* qids = reinterpret_cast<volatile int*>(tmem_holder + 2);
+  const uint32_t stg_base = sbase + STAGES2 * STAGE2_BYTES + BAR_BYTES;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -728,6 +737,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
     int q = 0;
     uint32_t qphase = 0;
     int it = 0;
+    uint32_t stg_n = 0;   // chunks this warp has staged (buffer = stg_n & 1)
     while (true) {
       if (!mbar_wait_cl_warp(qfull_bar(q), qphase, p.err, abort_flag)) {
         *abort_flag = 1;
@@ -781,12 +791,44 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
         }
       } else {
         float dot = 0.f;
+        const bool tma_store = pr.tma_c && un.tail < 0;
+        const int wrow0 = un.m0 + 128 * static_cast<int>(peer) + quarter * 32;   // this warp's first row
         for (int c = 0; c < 256 / 32; ++c) {
           const int col0 = un.n0 + c * 32;
           if (col0 >= pr.N) break;
           uint32_t v[32];
           tmem_ld_32x32b_x32(tacc + c * 32, v);
           tmem_ld_wait();
+          if (tma_store) {
+            // the warp's 32 x 32 chunk into a staging buffer (row = lane, in the map's
+            // swizzle), then one TMA store; rows and columns past the output are clipped
+            if (wrow0 >= pr.M) continue;          // a follower half wholly below the output
+            const uint32_t buf = stg_base + static_cast<uint32_t>(quarter * 2 + (stg_n & 1)) * STG_BUF;
+            if (lane == 0) bulk_wait_read<1>();   // the store that last read this buffer is done with it
+            __syncwarp();
+            if (pr.c_f32) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                st_shared_v4(buf + lane * 128 + ((j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                             v[4 * j + 3]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                st_shared_v4(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4),
+                             pack_bf16x2(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1])),
+                             pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
+                             pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
+                             pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
+            }
+            fence_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&p.tmC[un.p], col0, wrow0, buf);
+              bulk_commit_group();
+            }
+            ++stg_n;
+            continue;
+          }
           if (pr.epi == GEMM_EPI_SWIGLU_BWD) {
             const GluRaw cur = glu_next;
             if (c + 1 < 256 / 32) glu_load(pr, row, col0 + 32, glu_next);   // next chunk in flight
@@ -820,6 +862,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
       if (lane == 0) mbar_arrive_cluster(lead_tempty0 + 8u * acc);
       ++it;
     }
+    if (lane == 0) bulk_wait_all();   // every TMA store of this warp has written its tile
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -909,6 +953,22 @@ kl_status make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t out
                      static_cast<int>(r), (unsigned long long)inner, (unsigned long long)outer,
                      (long long)ld);
   return KL_OK;
+}
+
+// Output map of the plain-store epilogue: [M, N] with row stride ldc elements
+// (bf16 or fp32), box 32 columns x 32 rows, the staging buffers' swizzle
+// (64-byte for bf16 rows of 64 bytes, 128-byte for fp32 rows of 128 bytes).
+bool make_map_c(CUtensorMap* m, void* ptr, int M, int N, int64_t ldc, bool f32) {
+  auto fn = tensor_map_encoder();
+  if (!fn) return false;
+  const cuuint64_t es = f32 ? 4 : 2;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ldc) * es};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, ptr, dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // MN-major bf16 operand as a 3-D map: dims {64, K, MN/64} with strides
@@ -1148,6 +1208,9 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
     pr.R = s.R;
     pr.ldr = s.ldr;
     pr.r_f32 = s.r_dtype == KL_F32;
+    // plain stores without an addend leave through shared memory and a TMA store
+    pr.tma_c = s.epi == GEMM_EPI_STORE && !s.R && aligned16(s.C) && (s.ldc * dtype_size(s.c_dtype)) % 16 == 0 &&
+               make_map_c(&p.tmC[i], s.C, s.M, s.N, s.ldc, s.c_dtype == KL_F32);
     {
       const size_t ce = dtype_size(s.c_dtype), re = dtype_size(s.r_dtype);
       pr.vec_ok = aligned16(s.C) && (s.ldc * ce) % 16 == 0 &&
