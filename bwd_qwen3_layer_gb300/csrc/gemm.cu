@@ -65,7 +65,7 @@ struct GemmProb {
   int dot_S;
   const float2* rope_cs;  // GEMM_EPI_ROPE: [rope_S][64] cos/sin
   int rope_S;
-  int tma_c;              // plain stores leave through shared memory and a TMA store (map tmC[problem])
+  int tma_c;              // outputs leave through shared memory and TMA stores (maps tmC[problem][0..2])
   int whole_tiles;        // tiles computed whole; the rest (tail) are split along K
   int tail_tiles, tail_splits;
   float* tail_acc;        // [tail_splits][tail_tiles][256][256] fp32, one slice per K range
@@ -74,7 +74,7 @@ struct GemmProb {
 struct GemmParams {
   CUtensorMap tmA[GEMM_MAX_PROB * GEMM_MAX_SEG];
   CUtensorMap tmB[GEMM_MAX_PROB * GEMM_MAX_SEG];
-  CUtensorMap tmC[GEMM_MAX_PROB];   // output maps of the problems with tma_c (box 32 x 32)
+  CUtensorMap tmC[GEMM_MAX_PROB][3];   // output maps (C, C2, C3) of the problems with tma_c (box 32 x 32)
   GemmProb prob[GEMM_MAX_PROB];
   int nprob;
   int total_units;
@@ -108,7 +108,9 @@ __device__ __forceinline__ void store_chunk(const GemmProb& pr, int row, int col
           f[j] += a.x; f[j + 1] += a.y; f[j + 2] += a.z; f[j + 3] += a.w;
         }
       } else {
-        for (int j = 0; j < ncols; ++j) f[j] += r[j];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < ncols) f[j] += r[j];
       }
     } else {
       const __nv_bfloat16* r = static_cast<const __nv_bfloat16*>(pr.R) + row * pr.ldr + col0;
@@ -122,7 +124,9 @@ __device__ __forceinline__ void store_chunk(const GemmProb& pr, int row, int col
           f[j + 4] += x2.x; f[j + 5] += x2.y; f[j + 6] += x3.x; f[j + 7] += x3.y;
         }
       } else {
-        for (int j = 0; j < ncols; ++j) f[j] += __bfloat162float(r[j]);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < ncols) f[j] += __bfloat162float(r[j]);
       }
     }
   }
@@ -133,7 +137,9 @@ __device__ __forceinline__ void store_chunk(const GemmProb& pr, int row, int col
       for (int j = 0; j < 32; j += 4)
         *reinterpret_cast<float4*>(c + j) = make_float4(f[j], f[j + 1], f[j + 2], f[j + 3]);
     } else {
-      for (int j = 0; j < ncols; ++j) c[j] = f[j];
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < ncols) c[j] = f[j];
     }
   } else {
     __nv_bfloat16* c = static_cast<__nv_bfloat16*>(pr.C) + row * pr.ldc + col0;
@@ -148,7 +154,45 @@ __device__ __forceinline__ void store_chunk(const GemmProb& pr, int row, int col
         *reinterpret_cast<uint4*>(c + j) = o;
       }
     } else {
-      for (int j = 0; j < ncols; ++j) c[j] = __float2bfloat16_rn(f[j]);
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < ncols) c[j] = __float2bfloat16_rn(f[j]);
+    }
+  }
+}
+
+// f += the addend R's 32 columns col0.. of `row` (bf16 or fp32).
+__device__ __forceinline__ void add_residual(const GemmProb& pr, int row, int col0, float (&f)[32]) {
+  const int ncols = min(32, pr.N - col0);
+  const bool vec = pr.vec_ok && ncols == 32;
+  if (pr.r_f32) {
+    const float* r = static_cast<const float*>(pr.R) + row * pr.ldr + col0;
+    if (vec) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(r + j);
+        f[j] += a.x; f[j + 1] += a.y; f[j + 2] += a.z; f[j + 3] += a.w;
+      }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < ncols) f[j] += r[j];
+    }
+  } else {
+    const __nv_bfloat16* r = static_cast<const __nv_bfloat16*>(pr.R) + row * pr.ldr + col0;
+    if (vec) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 8) {
+        const uint4 a = *reinterpret_cast<const uint4*>(r + j);
+        const float2 x0 = unpack_bf16x2(a.x), x1 = unpack_bf16x2(a.y), x2 = unpack_bf16x2(a.z),
+                     x3 = unpack_bf16x2(a.w);
+        f[j] += x0.x; f[j + 1] += x0.y; f[j + 2] += x1.x; f[j + 3] += x1.y;
+        f[j + 4] += x2.x; f[j + 5] += x2.y; f[j + 6] += x3.x; f[j + 7] += x3.y;
+      }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j < ncols) f[j] += __bfloat162float(r[j]);
     }
   }
 }
@@ -182,7 +226,9 @@ __device__ __forceinline__ void store_bf16x32(__nv_bfloat16* p, bool vec, int nc
       *reinterpret_cast<uint4*>(p + j) = o;
     }
   } else {
-    for (int j = 0; j < ncols; ++j) p[j] = __float2bfloat16_rn(f[j]);
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < ncols) p[j] = __float2bfloat16_rn(f[j]);
   }
 }
 
@@ -211,7 +257,11 @@ struct GluRaw {
 };
 __device__ __forceinline__ void glu_load(const GemmProb& pr, int row, int col0, GluRaw& r) {
   const int ncols = min(32, pr.N - col0);
-  if (row >= pr.M || ncols <= 0) return;
+  if (row >= pr.M || ncols <= 0) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) r.g[j] = r.u[j] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
   const int64_t o = static_cast<int64_t>(row) * pr.ldc + col0;
   const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(pr.X1) + o;
   const __nv_bfloat16* u = static_cast<const __nv_bfloat16*>(pr.X2) + o;
@@ -232,7 +282,31 @@ __device__ __forceinline__ void glu_load(const GemmProb& pr, int row, int col0, 
     memcpy(r.u, tu, sizeof(tu));
   }
 }
-// 32 columns of dm (fp32) with the saved g, u -> dg = dm u s (1 + g (1 - s)), du = dm g s.
+// 32 columns of dm (fp32) with the saved g, u -> dg = dm u s (1 + g (1 - s)), du = dm g s (into g, u).
+__device__ __forceinline__ void swiglu_bwd_math(const uint32_t (&v)[32], const GluRaw& r, float (&g)[32],
+                                                float (&u)[32]) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t gw[4] = {r.g[j].x, r.g[j].y, r.g[j].z, r.g[j].w};
+    const uint32_t uw[4] = {r.u[j].x, r.u[j].y, r.u[j].z, r.u[j].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 gf = unpack_bf16x2(gw[e]), uf = unpack_bf16x2(uw[e]);
+      g[8 * j + 2 * e] = gf.x;
+      g[8 * j + 2 * e + 1] = gf.y;
+      u[8 * j + 2 * e] = uf.x;
+      u[8 * j + 2 * e + 1] = uf.y;
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float dm = __uint_as_float(v[j]);
+    const float sg = sigmoid_f(g[j]);
+    const float dg = dm * u[j] * sg * (1.0f + g[j] * (1.0f - sg));
+    u[j] = dm * g[j] * sg;   // du
+    g[j] = dg;
+  }
+}
 __device__ __forceinline__ void store_swiglu_bwd(const GemmProb& pr, int row, int col0, const uint32_t (&v)[32],
                                                  const GluRaw& r) {
   const int ncols = min(32, pr.N - col0);
@@ -339,6 +413,36 @@ constexpr uint32_t STG_BYTES = 4 * 2 * STG_BUF;
 constexpr uint32_t BAR_BYTES = 1024;   // barriers and scheduler slots; keeps the staging 1024-aligned
 constexpr size_t SMEM2_BYTES = 1024 + STAGES2 * STAGE2_BYTES + BAR_BYTES + STG_BYTES;
 static_assert(SMEM2_BYTES <= 232448, "pair-kernel shared memory above the per-CTA limit");
+
+// Stages this warp's 32 x 32 output chunk f (row = lane) in its next staging
+// slot (two per warp at wbase) and TMA-stores it through `map` at {col0,
+// wrow0}, as fp32 or bf16. A slot is rewritten only after the store two
+// chunks back has finished reading it.
+__device__ __forceinline__ void stage_store(uint32_t wbase, uint32_t& n, int lane, const CUtensorMap* map, bool f32,
+                                            int col0, int wrow0, const float (&f)[32]) {
+  const uint32_t buf = wbase + (n & 1u) * STG_BUF;
+  if (lane == 0) bulk_wait_read<1>();
+  __syncwarp();
+  if (f32) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      st_shared_v4(buf + lane * 128 + ((j ^ (lane & 7)) << 4), __float_as_uint(f[4 * j]), __float_as_uint(f[4 * j + 1]),
+                   __float_as_uint(f[4 * j + 2]), __float_as_uint(f[4 * j + 3]));
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      st_shared_v4(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4), pack_bf16x2(f[8 * j], f[8 * j + 1]),
+                   pack_bf16x2(f[8 * j + 2], f[8 * j + 3]), pack_bf16x2(f[8 * j + 4], f[8 * j + 5]),
+                   pack_bf16x2(f[8 * j + 6], f[8 * j + 7]));
+  }
+  fence_async_shared();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, col0, wrow0, buf);
+    bulk_commit_group();
+  }
+  ++n;
+}
 
 __device__ __forceinline__ uint32_t mapa_rank(uint32_t addr, uint32_t rank) {
   uint32_t r;
@@ -737,7 +841,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
     int q = 0;
     uint32_t qphase = 0;
     int it = 0;
-    uint32_t stg_n = 0;   // chunks this warp has staged (buffer = stg_n & 1)
+    uint32_t stg_n = 0;   // chunks this warp has staged (slot = stg_n & 1)
+    const uint32_t wstg = stg_base + static_cast<uint32_t>(quarter) * 2 * STG_BUF;
     while (true) {
       if (!mbar_wait_cl_warp(qfull_bar(q), qphase, p.err, abort_flag)) {
         *abort_flag = 1;
@@ -764,6 +869,12 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
       }
       tc_fence_after();
       const uint32_t tacc = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * 256);
+      // outputs through staged TMA stores (rows and columns past the output are clipped);
+      // a follower half wholly below the output stores nothing
+      const bool staged = pr.tma_c && un.tail < 0;
+      const int wrow0 = un.m0 + 128 * static_cast<int>(peer) + quarter * 32;   // this warp's first row
+      const bool live = wrow0 < pr.M;
+      const CUtensorMap* tmc = p.tmC[un.p];
       if (pr.epi == GEMM_EPI_SWIGLU) {
         // columns 0..127 of the accumulator are g, 128..255 are u, of the same 128 outputs
         for (int c = 0; c < 4; ++c) {
@@ -773,7 +884,22 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
           tmem_ld_32x32b_x32(tacc + c * 32, vg);
           tmem_ld_32x32b_x32(tacc + 128 + c * 32, vu);
           tmem_ld_wait();
-          if (row < pr.M) store_swiglu(pr, row, col0, vg, vu);
+          if (staged) {
+            if (live) {
+              float g[32], u[32], m[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                g[j] = __uint_as_float(vg[j]);
+                u[j] = __uint_as_float(vu[j]);
+                m[j] = g[j] * sigmoid_f(g[j]) * u[j];
+              }
+              stage_store(wstg, stg_n, lane, &tmc[0], false, col0, wrow0, g);
+              stage_store(wstg, stg_n, lane, &tmc[1], false, col0, wrow0, u);
+              stage_store(wstg, stg_n, lane, &tmc[2], false, col0, wrow0, m);
+            }
+          } else if (row < pr.M) {
+            store_swiglu(pr, row, col0, vg, vu);
+          }
         }
       } else if (pr.epi == GEMM_EPI_ROPE) {
         // two heads of 128 columns; plane i pairs column i with i + 64 of its head
@@ -786,55 +912,47 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
             tmem_ld_32x32b_x32(tacc + 128 * hl + 32 * c, va);
             tmem_ld_32x32b_x32(tacc + 128 * hl + 64 + 32 * c, vb);
             tmem_ld_wait();
-            if (row < pr.M) store_rope(pr, row, colA, va, vb, cs + 32 * c);
+            if (staged) {
+              if (live) {
+                float xa[32], xb[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  const float2 t = cs[32 * c + j];
+                  const float x = __uint_as_float(va[j]), y = __uint_as_float(vb[j]);
+                  xa[j] = x * t.x - y * t.y;
+                  xb[j] = x * t.y + y * t.x;
+                }
+                stage_store(wstg, stg_n, lane, &tmc[0], false, colA, wrow0, xa);
+                stage_store(wstg, stg_n, lane, &tmc[0], false, colA + 64, wrow0, xb);
+              }
+            } else if (row < pr.M) {
+              store_rope(pr, row, colA, va, vb, cs + 32 * c);
+            }
           }
         }
       } else {
         float dot = 0.f;
-        const bool tma_store = pr.tma_c && un.tail < 0;
-        const int wrow0 = un.m0 + 128 * static_cast<int>(peer) + quarter * 32;   // this warp's first row
         for (int c = 0; c < 256 / 32; ++c) {
           const int col0 = un.n0 + c * 32;
           if (col0 >= pr.N) break;
           uint32_t v[32];
           tmem_ld_32x32b_x32(tacc + c * 32, v);
           tmem_ld_wait();
-          if (tma_store) {
-            // the warp's 32 x 32 chunk into a staging buffer (row = lane, in the map's
-            // swizzle), then one TMA store; rows and columns past the output are clipped
-            if (wrow0 >= pr.M) continue;          // a follower half wholly below the output
-            const uint32_t buf = stg_base + static_cast<uint32_t>(quarter * 2 + (stg_n & 1)) * STG_BUF;
-            if (lane == 0) bulk_wait_read<1>();   // the store that last read this buffer is done with it
-            __syncwarp();
-            if (pr.c_f32) {
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                st_shared_v4(buf + lane * 128 + ((j ^ (lane & 7)) << 4), v[4 * j], v[4 * j + 1], v[4 * j + 2],
-                             v[4 * j + 3]);
-            } else {
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                st_shared_v4(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4),
-                             pack_bf16x2(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1])),
-                             pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3])),
-                             pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5])),
-                             pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7])));
-            }
-            fence_async_shared();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(&p.tmC[un.p], col0, wrow0, buf);
-              bulk_commit_group();
-            }
-            ++stg_n;
-            continue;
-          }
           if (pr.epi == GEMM_EPI_SWIGLU_BWD) {
             const GluRaw cur = glu_next;
             if (c + 1 < 256 / 32) glu_load(pr, row, col0 + 32, glu_next);   // next chunk in flight
-            if (row < pr.M) store_swiglu_bwd(pr, row, col0, v, cur);
-          } else if (row < pr.M) {
-            if (un.tail >= 0) {
+            if (staged) {
+              if (live) {
+                float dg[32], du[32];
+                swiglu_bwd_math(v, cur, dg, du);
+                stage_store(wstg, stg_n, lane, &tmc[0], false, col0, wrow0, dg);
+                stage_store(wstg, stg_n, lane, &tmc[1], false, col0, wrow0, du);
+              }
+            } else if (row < pr.M) {
+              store_swiglu_bwd(pr, row, col0, v, cur);
+            }
+          } else if (un.tail >= 0) {
+            if (row < pr.M) {
               // a K range of a last-round tile: its own fp32 scratch slice (summed in a fixed order later)
               float4* a = reinterpret_cast<float4*>(pr.tail_acc + (static_cast<int64_t>(un.tail) * 256 + (row - un.m0)) *
                                                                       256 + (col0 - un.n0));
@@ -842,17 +960,27 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1) gemm_bf16_tcp_kernel(const __
               for (int j = 0; j < 32; j += 4)
                 a[j / 4] = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
                                        __uint_as_float(v[j + 3]));
-            } else {
-              store_chunk(pr, row, col0, v);
-              if (pr.epi == GEMM_EPI_ROWDOT) {
-                dot += chunk_rowdot(pr, row, col0, v);
-                if ((c & 3) == 3) {   // the 128 columns of one head are done
-                  const int heads = pr.N >> 7, h = (col0 - 96) >> 7;
-                  const int b = row / pr.dot_S, t = row - b * pr.dot_S;
-                  pr.dot_out[(static_cast<int64_t>(b) * heads + h) * pr.dot_S + t] = dot;
-                  dot = 0.f;
-                }
+            }
+          } else if (staged) {
+            if (live) {
+              float f[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) f[j] = __uint_as_float(v[j]);
+              if (pr.R && row < pr.M) add_residual(pr, row, col0, f);
+              stage_store(wstg, stg_n, lane, &tmc[0], pr.c_f32 != 0, col0, wrow0, f);
+            }
+          } else if (row < pr.M) {
+            store_chunk(pr, row, col0, v);
+          }
+          if (pr.epi == GEMM_EPI_ROWDOT && un.tail < 0) {
+            if (row < pr.M) dot += chunk_rowdot(pr, row, col0, v);
+            if ((c & 3) == 3) {   // the 128 columns of one head are done
+              if (row < pr.M) {
+                const int heads = pr.N >> 7, h = (col0 - 96) >> 7;
+                const int b = row / pr.dot_S, t = row - b * pr.dot_S;
+                pr.dot_out[(static_cast<int64_t>(b) * heads + h) * pr.dot_S + t] = dot;
               }
+              dot = 0.f;
             }
           }
         }
@@ -1208,9 +1336,19 @@ kl_status gemm_bf16(const GemmSpec* specs_in, int nspec, cudaStream_t st, const 
     pr.R = s.R;
     pr.ldr = s.ldr;
     pr.r_f32 = s.r_dtype == KL_F32;
-    // plain stores without an addend leave through shared memory and a TMA store
-    pr.tma_c = s.epi == GEMM_EPI_STORE && !s.R && aligned16(s.C) && (s.ldc * dtype_size(s.c_dtype)) % 16 == 0 &&
-               make_map_c(&p.tmC[i], s.C, s.M, s.N, s.ldc, s.c_dtype == KL_F32);
+    // outputs leave through shared memory and TMA stores: C (with any addend added
+    // first), and C2, C3 of the SwiGLU variants
+    {
+      const bool f32 = s.c_dtype == KL_F32;
+      const bool two = s.epi == GEMM_EPI_SWIGLU || s.epi == GEMM_EPI_SWIGLU_BWD;
+      const bool three = s.epi == GEMM_EPI_SWIGLU;
+      bool ok = aligned16(s.C) && (s.ldc * dtype_size(s.c_dtype)) % 16 == 0 &&
+                (!two || aligned16(s.C2)) && (!three || aligned16(s.C3)) &&
+                make_map_c(&p.tmC[i][0], s.C, s.M, s.N, s.ldc, f32);
+      if (ok && two) ok = make_map_c(&p.tmC[i][1], s.C2, s.M, s.N, s.ldc, false);
+      if (ok && three) ok = make_map_c(&p.tmC[i][2], s.C3, s.M, s.N, s.ldc, false);
+      pr.tma_c = ok ? 1 : 0;
+    }
     {
       const size_t ce = dtype_size(s.c_dtype), re = dtype_size(s.r_dtype);
       pr.vec_ok = aligned16(s.C) && (s.ldc * ce) % 16 == 0 &&
