@@ -87,6 +87,31 @@ __device__ __forceinline__ void merge(float& m, float& s, int& i, float m2, floa
   }
 }
 
+// Adds eight logits a[0..7] at indices j0 .. j0 + 7 (increasing, after every
+// index already summarised by this thread, so a tie never moves the argmax)
+// to the running summary (m, s, idx), with mL = m log2 e kept alongside: one
+// max of the eight, a rescale only when it exceeds the running max, then
+// eight exponentials into the sum.
+__device__ __forceinline__ void add_logits8(float& m, float& mL, float& s, int& i, const float (&a)[8], int j0) {
+  float cm = fmaxf(fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3])), fmaxf(fmaxf(a[4], a[5]), fmaxf(a[6], a[7])));
+  if (cm > m) {
+    s = m > -INFINITY ? s * ex2a(mL - cm * LOG2E) : 0.f;
+    m = cm;
+    mL = cm * LOG2E;
+    int k = 7;
+#pragma unroll
+    for (int e = 6; e >= 0; --e)
+      if (a[e] == cm) k = e;
+    i = j0 + k;
+  }
+  if (m > -INFINITY) {
+    float t = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) t += ex2a(fmaf(a[e], LOG2E, -mL));
+    s += t;
+  }
+}
+
 // Adds logit z at index j to the running summary (m, s, idx).
 __device__ __forceinline__ void add_logit(float& m, float& s, int& i, float z, int j) {
   if (z > m) {
@@ -128,25 +153,23 @@ __global__ void __launch_bounds__(THREADS)
   const int len = max(0, min(V, c0 + slice) - c0);
   const float* zr = z + static_cast<int64_t>(n) * V + c0;
 
-  // 1. running summary of this thread's logits (float4 loads, four in flight)
+  // 1. running summary of this thread's logits (32-byte loads, two in flight)
   float m = -INFINITY, s = 0.f;
   int mi = INT_MAX;
   if (VEC) {
     constexpr int U = 2;
+    float mL = -INFINITY;
     int i = threadIdx.x * 8;
     for (; i + (U - 1) * THREADS * 8 < len; i += U * THREADS * 8) {
       f8 a[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) a[u] = ld_keep(zr + i + u * THREADS * 8);
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) add_logit(m, s, mi, a[u].v[e], c0 + i + u * THREADS * 8 + e);
+      for (int u = 0; u < U; ++u) add_logits8(m, mL, s, mi, a[u].v, c0 + i + u * THREADS * 8);
     }
     for (; i < len; i += THREADS * 8) {
       const f8 a = ld_keep(zr + i);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) add_logit(m, s, mi, a.v[e], c0 + i + e);
+      add_logits8(m, mL, s, mi, a.v, c0 + i);
     }
   } else {
     for (int i = threadIdx.x; i < len; i += THREADS) add_logit(m, s, mi, zr[i], c0 + i);
@@ -200,23 +223,25 @@ __global__ void __launch_bounds__(THREADS)
   } else {
     __nv_bfloat16* out = static_cast<__nv_bfloat16*>(dz) + static_cast<int64_t>(n) * V + c0;
     if (VEC) {
+      // softmax / N = 2^(z log2 e - lse log2 e + log2(1/N)): the 1/N rides in the exponent
+      const float off = -lsel + log2f(invN);
 #pragma unroll 2
       for (int i = threadIdx.x * 8; i < len; i += THREADS * 8) {
         const f8 a = ld_last(zr + i);
         float p[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) p[e] = ex2a(fmaf(a.v[e], LOG2E, -lsel));
+        for (int e = 0; e < 8; ++e) p[e] = ex2a(fmaf(a.v[e], LOG2E, off));
         const int d = t - (c0 + i);
         if (d >= 0 && d < 8) {
 #pragma unroll
           for (int e = 0; e < 8; ++e)
-            if (e == d) p[e] -= 1.f;
+            if (e == d) p[e] -= invN;
         }
         uint4 o;
-        o.x = pack_bf16x2(p[0] * invN, p[1] * invN);
-        o.y = pack_bf16x2(p[2] * invN, p[3] * invN);
-        o.z = pack_bf16x2(p[4] * invN, p[5] * invN);
-        o.w = pack_bf16x2(p[6] * invN, p[7] * invN);
+        o.x = pack_bf16x2(p[0], p[1]);
+        o.y = pack_bf16x2(p[2], p[3]);
+        o.z = pack_bf16x2(p[4], p[5]);
+        o.w = pack_bf16x2(p[6], p[7]);
         st_stream(out + i, o);
       }
     } else {
