@@ -417,10 +417,22 @@ def setup_stream(torch, K, L, synth, device, seed, name="stream"):
 
     def after(args):
         """Destroys the streamed driver, then times the same call with every
-        layer's weights already in device memory (bulk: no uploads)."""
+        layer's weights already in device memory (bulk: no uploads), and the
+        plain host-to-device copy rate of the same pinned weight sets (the
+        host link this box gives the stream)."""
         dev_bytes = K.kl_stream_device_bytes(h)
         K.kl_stream_destroy(h)
         dev_sets = [{n: t.to(device) for n, t in w.items()} for w in hosts]
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for w, dw in zip(hosts, dev_sets):
+            for n in w:
+                dw[n].copy_(w[n], non_blocking=True)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        copy_bytes = sum(t.numel() * t.element_size() for w in hosts for t in w.values())
+        link_gbs = copy_bytes / (c0.elapsed_time(c1) / 1e3) / 1e9
         dstructs = [L.weights_struct(dev_sets[li % distinct]) for li in range(nl)]
         Wd = W.to(device) if train else None
         hb = K.kl_stream_create(K.StreamCfg(cfg, nl, V, mode), dstructs, Wd.data_ptr() if train else None)
@@ -439,7 +451,8 @@ def setup_stream(torch, K, L, synth, device, seed, name="stream"):
             K.kl_stream_destroy(hb)
         del dev_sets, Wd
         return {"driver_device_bytes": dev_bytes, "device_bytes_at_create": free0 - free1,
-                "weight_h2d_bytes_per_step": weight_h2d, "ms_per_step_bulk": round(ms_bulk, 3)}
+                "weight_h2d_bytes_per_step": weight_h2d, "ms_per_step_bulk": round(ms_bulk, 3),
+                "host_link_copy_gbs": round(link_gbs, 1)}
 
     keep = {"objs": (hosts, W, X, tgt, grads, dW, Y, hX, ht, hY, X2, t2), "after": after}
     cfgd = {"workload": wl["desc"], "layers": nl, "batch": B, "seq_len": S, "hidden": H,
