@@ -287,8 +287,9 @@ kl_status kl_device_status(void* stream, uint32_t* bits) {
   KL_CUDA(cudaMemcpyToSymbol(g_device_error_word, &zero, sizeof(zero)));
   if (bits) *bits = v;
   if (v & KL_DEVERR_TIMEOUT) {
-    // a few-rows GEMM that gave up may have left arrival counts behind
-    const kl_status rs = skinny_cnt_reset();
+    // a few-rows GEMM or a fused RMSNorm backward that gave up may have left arrival counts behind
+    kl_status rs = skinny_cnt_reset();
+    if (rs == KL_OK) rs = rms_bar_reset();
     if (rs != KL_OK) return rs;
     return set_error(KL_ERR_TIMEOUT, "a kernel wait timed out (bits 0x%x)", v);
   }

@@ -5,6 +5,8 @@
 // widths allow, fp32 arithmetic, warp-shuffle row reductions.
 #include <math.h>
 
+#include <atomic>
+
 #include "internal.h"
 #include "kl_common.cuh"
 
@@ -360,12 +362,49 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_rows_kernel(
 // packed bf16 and the gain-gradient partial sums as fp32 across the CTA's rows.
 constexpr int RW_THREADS = 256, RW_MAXC = 4;
 
+// Grid-wide barrier of a cooperative launch (every CTA resident): one arrival
+// counter and one generation word per slot in static device memory; the last
+// CTA to arrive re-arms the counter and moves the generation on. The wait is
+// bounded: past the limit it records KL_DEVERR_TIMEOUT and goes on.
+constexpr int RB_BAR_SLOTS = 16;
+__device__ unsigned int g_rms_bar[RB_BAR_SLOTS][2];
+
+__device__ __forceinline__ void grid_barrier(unsigned int* bar, unsigned int nblocks, uint32_t* err) {
+  __threadfence();   // this thread's writes before the arrival
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile unsigned int* gen = bar + 1;
+    const unsigned int g0 = *gen;   // read before arriving: the last arrival moves it on after
+    const unsigned int prev = atomicAdd(bar, 1u);
+    if (prev == nblocks - 1) {
+      atomicExch(bar, 0u);
+      __threadfence();
+      atomicAdd(bar + 1, 1u);
+    } else {
+      const uint64_t t0 = global_timer_ns();
+      uint32_t k = 0;
+      while (*gen == g0) {
+        if ((++k & 255u) == 0 && global_timer_ns() - t0 > KL_WAIT_LIMIT_NS) {
+          record_error(err, KL_DEVERR_TIMEOUT);
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
+
+// With dgamma (a cooperative launch), after its partial row each CTA passes a
+// grid barrier and then sums 32-column slices of dgamma over every CTA's
+// partial row in CTA order (the column-sum step in the same launch).
 template <int NC>
 __global__ void __launch_bounds__(RW_THREADS, 2) rmsnorm_bwd_row8_kernel(
     int rows, int width, const float* __restrict__ dh, const __nv_bfloat16* __restrict__ x,
     const __nv_bfloat16* __restrict__ gamma, const float* __restrict__ rstd,
     const __nv_bfloat16* __restrict__ resid, __nv_bfloat16* __restrict__ dx,
-    float* __restrict__ partial) {
+    float* __restrict__ partial, float* __restrict__ dgamma, unsigned int* __restrict__ bar,
+    uint32_t* __restrict__ err) {
   pdl_enter();
   using T = __nv_bfloat16;
   __shared__ float red[2][RW_THREADS / 32];
@@ -444,6 +483,35 @@ __global__ void __launch_bounds__(RW_THREADS, 2) rmsnorm_bwd_row8_kernel(
       *reinterpret_cast<float4*>(p) = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
       *reinterpret_cast<float4*>(p + 4) = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
     }
+  }
+  if (!dgamma) return;
+  grid_barrier(bar, gridDim.x, err);
+  // dgamma: 32 columns per CTA (8 float4 lanes), the partial rows split over 32
+  // row groups, then a fixed tree over the groups (deterministic)
+  __shared__ float4 cred[32][8];
+  const int cg = tid & 7, rg = tid >> 3;
+  const int nrows = gridDim.x;
+  for (int cb = blockIdx.x; cb * 32 < width; cb += gridDim.x) {
+    const int c = cb * 32 + cg * 4;
+    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c < width) {
+      for (int r2 = rg; r2 < nrows; r2 += 32) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(partial + static_cast<int64_t>(r2) * width + c));
+        sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+      }
+    }
+    cred[rg][cg] = sum;
+    __syncthreads();
+    for (int k = 16; k > 0; k >>= 1) {
+      if (rg < k) {
+        const float4 o = cred[rg + k][cg];
+        float4& m = cred[rg][cg];
+        m.x += o.x; m.y += o.y; m.z += o.z; m.w += o.w;
+      }
+      __syncthreads();
+    }
+    if (rg == 0 && c < width) *reinterpret_cast<float4*>(dgamma + c) = cred[0][cg];
+    __syncthreads();
   }
 }
 
@@ -1010,6 +1078,55 @@ size_t rmsnorm_bwd_ws(int rows, int width) {
   return align_up(static_cast<size_t>(rmsnorm_bwd_grid(rows)) * width * sizeof(float), 256);
 }
 
+// The grid-barrier slot of the next fused RMSNorm backward (round-robin, so
+// launches on different streams that overlap use different slots).
+unsigned int* rms_bar_slot() {
+  static unsigned int* base[64] = {};
+  static std::atomic<unsigned> seq{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!base[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_rms_bar) != cudaSuccess) return nullptr;
+    base[dev] = static_cast<unsigned int*>(ptr);
+  }
+  return base[dev] + 2 * (seq.fetch_add(1) % RB_BAR_SLOTS);
+}
+
+// Cooperative launch (every CTA resident at once, as the grid barrier needs),
+// with programmatic stream serialization where the driver takes both.
+template <typename... KArgs, typename... Args>
+kl_status launch_coop(void (*kern)(KArgs...), int grid, cudaStream_t st, Args&&... args) {
+  static bool with_pdl = true;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(RW_THREADS);
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = with_pdl ? 2 : 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+  if (e != cudaSuccess && with_pdl) {
+    (void)cudaGetLastError();
+    with_pdl = false;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+  }
+  if (e != cudaSuccess) return cuda_check(e, "rmsnorm_bwd cooperative launch");
+  return KL_OK;
+}
+
+kl_status rms_bar_reset() {
+  void* ptr = nullptr;
+  KL_CUDA(cudaGetSymbolAddress(&ptr, g_rms_bar));
+  KL_CUDA(cudaMemset(ptr, 0, sizeof(g_rms_bar)));
+  return KL_OK;
+}
+
 kl_status rmsnorm_bwd(int rows, int width, int dtype, const void* dh, int dh_dtype, const void* x,
                       const void* gamma, const float* rstd, const void* resid, void* dx,
                       float* dgamma, void* ws, size_t ws_bytes, cudaStream_t st) {
@@ -1032,6 +1149,7 @@ kl_status rmsnorm_bwd(int rows, int width, int dtype, const void* dh, int dh_dty
   // generic row form: fp32 dh, width a multiple of 4 up to 8192, 16-byte aligned rows
   const bool rows_form = dh_dtype == KL_F32 && width % 4 == 0 && width <= 256 * 4 * RB_MAXC && aligned &&
                          (width * es) % 16 == 0;
+  bool fused = false;
   {
     ProfScope ps("rmsnorm_bwd", st, 0.0,
                  1.0 * rows * width * (dtype_size(dh_dtype) + (resid ? 3.0 : 2.0) * es) + 4.0 * rows +
@@ -1040,10 +1158,25 @@ kl_status rmsnorm_bwd(int rows, int width, int dtype, const void* dh, int dh_dty
     if (dtype == KL_BF16) {
       using T = __nv_bfloat16;
       if (row8_form) {
+        // one cooperative launch: rows, partial dgamma rows, a grid barrier, the column sums
+        fused = width % 4 == 0 && al16(dgamma);
+        unsigned int* bar = fused ? rms_bar_slot() : nullptr;
+        if (fused && !bar) fused = false;
+        void (*kern)(int, int, const float*, const T*, const T*, const float*, const T*, T*, float*, float*,
+                     unsigned int*, uint32_t*) = nullptr;
         switch (nc8) {
-#define KL_RW_CASE(N) case N: launch_pdl(rmsnorm_bwd_row8_kernel<N>, grid, RW_THREADS, 0, st, rows, width, (const float*)dh, (const T*)x, (const T*)gamma, rstd, (const T*)resid, (T*)dx, partial); break;
-          KL_RW_CASE(1) KL_RW_CASE(2) KL_RW_CASE(3) KL_RW_CASE(4)
-#undef KL_RW_CASE
+          case 1: kern = rmsnorm_bwd_row8_kernel<1>; break;
+          case 2: kern = rmsnorm_bwd_row8_kernel<2>; break;
+          case 3: kern = rmsnorm_bwd_row8_kernel<3>; break;
+          default: kern = rmsnorm_bwd_row8_kernel<4>; break;
+        }
+        if (fused) {
+          KL_TRY(launch_coop(kern, grid, st, rows, width, (const float*)dh, (const T*)x, (const T*)gamma, rstd,
+                             (const T*)resid, (T*)dx, partial, dgamma, bar, device_error_word()));
+        } else {
+          launch_pdl(kern, grid, RW_THREADS, 0, st, rows, width, (const float*)dh, (const T*)x, (const T*)gamma, rstd,
+                     (const T*)resid, (T*)dx, partial, static_cast<float*>(nullptr), static_cast<unsigned int*>(nullptr),
+                     device_error_word());
         }
       } else if (rows_form)
         launch_pdl(rmsnorm_bwd_rows_kernel<T>, grid, 256, 0, st, rows, width, (const float*)dh, (const T*)x, (const T*)gamma, rstd, (const T*)resid, (T*)dx, partial);
@@ -1059,6 +1192,7 @@ kl_status rmsnorm_bwd(int rows, int width, int dtype, const void* dh, int dh_dty
     }
   }
   KL_CUDA(cudaGetLastError());
+  if (fused) return KL_OK;   // the column sums ran in the same launch
   ProfScope ps2("rmsnorm_bwd_colsum", st, 0.0, 4.0 * grid * width + 4.0 * width);
   if (width % 4 == 0 && al16(dgamma))
     launch_pdl(column_sum4_kernel, (width + 31) / 32, 256, 0, st, grid, width, partial, dgamma);

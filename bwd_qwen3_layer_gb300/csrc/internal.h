@@ -94,6 +94,9 @@ kl_status gemm_skinny(const GemmSpec* specs, int nspec, cudaStream_t st, const c
 // Zeroes the few-rows GEMM's arrival counters on the current device
 // (synchronous; used after a launch reported a timeout).
 kl_status skinny_cnt_reset();
+// Zeroes the fused RMSNorm backward's grid-barrier counters on the current
+// device (synchronous; used after a launch reported a timeout).
+kl_status rms_bar_reset();
 // fp32 operands on CUDA cores (one problem).
 kl_status gemm_f32(const GemmSpec& spec, cudaStream_t st, const char* label = "gemm_f32");
 
