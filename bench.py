@@ -34,7 +34,9 @@ metric through the C ABI with each step's inputs copied from pinned host
 memory and its result read back inside the timed region, the copies of step
 k+1 (in) and k-1 (out) running on a copy stream while step k computes, as a
 training or serving loop feeds the GPU (the stream workloads' driver reads its
-results back inside the step, so there the copies stay in line). Every workload's
+results back inside the step, so there the copies stay in line). The default
+layer run adds `later_region`: the same step timed over one second after the
+other regions, when the board has reached its power limit. Every workload's
 inputs exceed L2 (129 MB), so no flush is needed between steps. N > 1 runs N
 independent replicas (weak scaling; the path needs no collective).
 `--impl reference` times the fp64 CPU oracle on a bounded sample of the same
@@ -45,6 +47,7 @@ from __future__ import annotations
 import argparse
 import ctypes
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -536,7 +539,10 @@ def job_throughput(units_per_rank_step, steps, world, ms):
     return units_per_rank_step * steps * world / (ms / 1e3)
 
 
-def bench_ours(args, rank, world, local_rank, dist):
+def bench_ours(args, rank, world, local_rank, dist, later_s=0.0):
+    """Timed regions of one workload: device-resident (value), per-launch
+    events (kernels), end to end (e2e) and, with later_s > 0, a region of at
+    least later_s seconds after those (the board then at its power limit)."""
     import torch
 
     import bwd_qwen3_layer_gb300 as K
@@ -610,6 +616,26 @@ def bench_ours(args, rank, world, local_rank, dist):
     f1.record(stream)
     barrier()
     ms_e2e = f0.elapsed_time(f1)
+
+    # ---- a later, longer region of the same steps (clocks sampled again) ----
+    later = None
+    if later_s > 0:
+        n_later = max(args.steps, int(math.ceil(later_s * 1e3 / (ms / args.steps))))
+        lclk = Clocks(local_rank)
+        barrier()
+        lclk.start()
+        time.sleep(0.25)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        lclk.mark(True)
+        g0.record(stream)
+        for _ in range(n_later):
+            step()
+        g1.record(stream)
+        barrier()
+        lclk.mark(False)
+        (ms_later,) = max_over_ranks([g0.elapsed_time(g1)], dist, device)
+        later = {"steps": n_later, "ms_per_step": round(ms_later / n_later, 4),
+                 "value": round(job_throughput(units, n_later, world, ms_later), 1), "clocks": lclk.stop()}
     K.kl_device_status(stream)
     extra = None
     if isinstance(keep, dict) and "after" in keep:
@@ -618,7 +644,7 @@ def bench_ours(args, rank, world, local_rank, dist):
         extra["weight_h2d_gbs"] = round(extra["weight_h2d_bytes_per_step"] / (ms / args.steps) / 1e6, 1)
     ms, ms_e2e = max_over_ranks([ms, ms_e2e], dist, device)
     return dict(ms=ms, ms_e2e=ms_e2e, ms_prof=ms_prof, prof=prof, clocks=clk, launches=int(launches), units=units,
-                h2d=h2d, d2h=d2h, config=cfgd, extra=extra)
+                h2d=h2d, d2h=d2h, config=cfgd, extra=extra, later=later)
 
 
 # ----------------------------------------------------------------------------
@@ -879,7 +905,8 @@ def main():
 
         dist_mod.init_process_group("nccl")
         dist = dist_mod
-    r = bench_ours(args, rank, world, local_rank, dist)
+    # the headline layer step also runs a one-second region after the others
+    r = bench_ours(args, rank, world, local_rank, dist, later_s=1.0 if args.workload == "layer" else 0.0)
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -889,6 +916,8 @@ def main():
     line.update({"n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
                  "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic"})
     line["config"] = r["config"] | {"parallelism": f"replicas x{world}"}
+    if r["later"] is not None:
+        line["later_region"] = r["later"]
     if world == 1 and args.workload == "layer" and not args.no_extra:
         line["workloads"] = measure_extras(args, pk)
     if world == 1 and not args.no_cpu_baseline:
