@@ -19,7 +19,8 @@ def _maybe_round(a, dt):
     return synth.round_bf16(a) if dt == 1 else a.astype(np.float32).astype(np.float64)
 
 
-@pytest.mark.parametrize("dt,rows,width", [(1, 300, 5120), (1, 37, 200), (0, 33, 64), (0, 5, 70)])
+@pytest.mark.parametrize("dt,rows,width", [(1, 300, 5120), (1, 1500, 5120), (1, 700, 8192), (1, 37, 200),
+                                           (0, 1000, 1024), (0, 33, 64), (0, 5, 70)])
 def test_rmsnorm(kl, dt, rows, width):
     tol = TOL_BF16 if dt == 1 else 1e-6
     x = _maybe_round(synth.normal(0, "rms.x", (rows, width)), dt)
