@@ -52,8 +52,7 @@ constexpr float LN2_F = 0.6931471805599453f;
 constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;          // 2 stages
 constexpr uint32_t OFF_V = OFF_K + 2 * TILE_BYTES;      // 2 stages
-constexpr uint32_t OFF_P = OFF_V + 2 * TILE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_P + TILE_BYTES;
+constexpr uint32_t OFF_BAR = OFF_V + 2 * TILE_BYTES;
 constexpr size_t SMEM_BYTES = 1024 + OFF_BAR + 256;
 
 struct FwdParams {
@@ -208,9 +207,9 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_kernel(const __grid_cons
       if (!mbar_wait_warp(v_full(s), ph, p.err, abort_flag)) return false;
       tc_fence_after();
       if (el) {
-        for (int kk = 0; kk < BKV / 16; ++kk)
-          umma_bf16(tmem + 256, desc_kmajor(sb + OFF_P, kk), desc_mnmajor(sb + OFF_V + s * TILE_BYTES, kk),
-                    idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < BKV / 16; ++kk)   // P from TMEM (the first 64 columns of S[s])
+          umma_bf16_ta(tmem + 256, tmem + s * 128 + kk * 8, desc_mnmajor(sb + OFF_V + s * TILE_BYTES, kk),
+                       idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(v_empty(s));
         umma_commit(p_free);
       }
@@ -250,7 +249,6 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_kernel(const __grid_cons
     const uint32_t oadr = tmem + lane_off + 256;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    uint8_t* prow = smem + OFF_P + r * 128;
     for (int j = 0; j < nkb; ++j) {
       const int s = j & 1;
       const uint32_t ph = (j >> 1) & 1;
@@ -286,9 +284,10 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_kernel(const __grid_cons
       const bool raise = mx > m + 8.0f;
       const float m_new = raise ? mx : m;
       const float alpha = raise ? ex2_approx(m - m_new) : 1.0f;
-      // O and the P buffer are stable once the previous P V product is done
-      if (j >= 1 && !mbar_wait_warp(p_free, (j - 1) & 1, p.err, abort_flag)) { ok = false; break; }
+      // O is stable for a rescale once the previous P V product is done (P
+      // goes into this step's S buffer, which S's completion shows free)
       if (j >= 1 && __any_sync(0xffffffffu, raise)) {
+        if (!mbar_wait_warp(p_free, (j - 1) & 1, p.err, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -301,39 +300,32 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_kernel(const __grid_cons
         }
         tmem_st_wait();
       }
-      // probabilities (one FFMA + one ex2 each), row sum, bf16 P into the
-      // swizzled K-major tile
+      // probabilities (one FFMA + one ex2 each), row sum, bf16 P packed two
+      // keys per column into the first 64 columns of S[s] (the A operand of
+      // the P V product; S has been read into registers)
       const float neg = -m_new;
       const float sc = p.scale_log2;
       float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+      uint32_t pk[64];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c * 32 + e]), sc, neg));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[c * 32 + e + 1]), sc, neg));
-          const float p2 = ex2_approx(fmaf(__uint_as_float(sv[c * 32 + e + 2]), sc, neg));
-          const float p3 = ex2_approx(fmaf(__uint_as_float(sv[c * 32 + e + 3]), sc, neg));
-          r0 += p0;
-          r1 += p1;
-          r2 += p2;
-          r3 += p3;
-          pk[e >> 1] = pack_bf16x2(p0, p1);
-          pk[(e >> 1) + 1] = pack_bf16x2(p2, p3);
-        }
-        uint8_t* blk = prow + (c >> 1) * 16384;   // 64-key swizzle block
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int chunk = (c & 1) * 4 + q;
-          *reinterpret_cast<uint4*>(blk + ((chunk ^ (r & 7)) << 4)) =
-              make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-        }
+      for (int e = 0; e < BKV; e += 4) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), sc, neg));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), sc, neg));
+        const float p2 = ex2_approx(fmaf(__uint_as_float(sv[e + 2]), sc, neg));
+        const float p3 = ex2_approx(fmaf(__uint_as_float(sv[e + 3]), sc, neg));
+        r0 += p0;
+        r1 += p1;
+        r2 += p2;
+        r3 += p3;
+        pk[e >> 1] = pack_bf16x2(p0, p1);
+        pk[(e >> 1) + 1] = pack_bf16x2(p2, p3);
       }
+      tmem_st_32x32b_x32(sadr, *reinterpret_cast<uint32_t(*)[32]>(pk));
+      tmem_st_32x32b_x32(sadr + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
       l = l * alpha + ((r0 + r1) + (r2 + r3));
       m = m_new;
+      tmem_st_wait();
       tc_fence_before();
-      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
@@ -495,9 +487,9 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_persist_kernel(const __g
       if (!mbar_wait_warp(v_full(s), ph, p.err, abort_flag)) return false;
       tc_fence_after();
       if (el) {
-        for (int kk = 0; kk < BKV / 16; ++kk)
-          umma_bf16(tmem + 256 + ob * 128, desc_kmajor(sb + OFF_P, kk), desc_mnmajor(sb + OFF_V + s * TILE_BYTES, kk),
-                    idesc_pv, (!first || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < BKV / 16; ++kk)   // P from TMEM (the first 64 columns of S[s])
+          umma_bf16_ta(tmem + 256 + ob * 128, tmem + s * 128 + kk * 8, desc_mnmajor(sb + OFF_V + s * TILE_BYTES, kk),
+                       idesc_pv, (!first || kk > 0) ? 1u : 0u);
         umma_commit(v_empty(s));
         umma_commit(p_free);
       }
@@ -548,7 +540,6 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_persist_kernel(const __g
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;           // query row within the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    uint8_t* prow = smem + OFF_P + r * 128;
     bool ok = true;
     int g = 0;
     for (int k = 0; ok; ++k) {
@@ -594,9 +585,10 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_persist_kernel(const __g
         const bool raise = mx > m + 8.0f;
         const float m_new = raise ? mx : m;
         const float alpha = raise ? ex2_approx(m - m_new) : 1.0f;
-        // O and the P buffer are stable once the previous P V product is done
-        if (g >= 1 && !mbar_wait_warp(p_free, (g - 1) & 1, p.err, abort_flag)) { ok = false; break; }
+        // O is stable for a rescale once the previous P V product is done (P
+        // goes into this step's S buffer, which S's completion shows free)
         if (j >= 1 && __any_sync(0xffffffffu, raise)) {
+          if (!mbar_wait_warp(p_free, (g - 1) & 1, p.err, abort_flag)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
@@ -609,39 +601,32 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_persist_kernel(const __g
           }
           tmem_st_wait();
         }
-        // probabilities (one FFMA + one ex2 each), row sum, bf16 P into the
-        // swizzled K-major tile
+        // probabilities (one FFMA + one ex2 each), row sum, bf16 P packed two
+        // keys per column into the first 64 columns of S[s] (the A operand of
+        // the P V product; S has been read into registers)
         const float neg = -m_new;
         const float sc = p.scale_log2;
         float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+        uint32_t pk[64];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sv[c * 32 + e]), sc, neg));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sv[c * 32 + e + 1]), sc, neg));
-            const float p2 = ex2_approx(fmaf(__uint_as_float(sv[c * 32 + e + 2]), sc, neg));
-            const float p3 = ex2_approx(fmaf(__uint_as_float(sv[c * 32 + e + 3]), sc, neg));
-            r0 += p0;
-            r1 += p1;
-            r2 += p2;
-            r3 += p3;
-            pk[e >> 1] = pack_bf16x2(p0, p1);
-            pk[(e >> 1) + 1] = pack_bf16x2(p2, p3);
-          }
-          uint8_t* blk = prow + (c >> 1) * 16384;   // 64-key swizzle block
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int chunk = (c & 1) * 4 + q;
-            *reinterpret_cast<uint4*>(blk + ((chunk ^ (r & 7)) << 4)) =
-                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-          }
+        for (int e = 0; e < BKV; e += 4) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), sc, neg));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), sc, neg));
+          const float p2 = ex2_approx(fmaf(__uint_as_float(sv[e + 2]), sc, neg));
+          const float p3 = ex2_approx(fmaf(__uint_as_float(sv[e + 3]), sc, neg));
+          r0 += p0;
+          r1 += p1;
+          r2 += p2;
+          r3 += p3;
+          pk[e >> 1] = pack_bf16x2(p0, p1);
+          pk[(e >> 1) + 1] = pack_bf16x2(p2, p3);
         }
+        tmem_st_32x32b_x32(sadr, *reinterpret_cast<uint32_t(*)[32]>(pk));
+        tmem_st_32x32b_x32(sadr + 32, *reinterpret_cast<uint32_t(*)[32]>(pk + 32));
         l = l * alpha + ((r0 + r1) + (r2 + r3));
         m = m_new;
+        tmem_st_wait();
         tc_fence_before();
-        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(p_full);
       }
