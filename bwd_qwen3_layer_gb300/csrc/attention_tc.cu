@@ -1220,15 +1220,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
 // Q and dO, the A operands of S = Q K^T and dP = dO V^T, are the same for the
 // whole CTA and live in tensor memory: the TMA warp stages them in the K / V
 // ring's last two stages, the elementwise warps copy each row into tensor
-// memory, and those stages then join the ring. Shared memory holds the K / V
-// ring and the double-buffered dS. Tensor memory: S (2 x 64 columns), dP
+// memory, and those stages then join the ring. dS, the A operand of
+// dQ += dS K, also lives in tensor memory: the warp holding keys 32 h .. 32 h +
+// 31 of a step writes their bf16 pairs into the first 16 of its own 32 columns
+// of the step's S buffer once it has read them (so S of step j + 2 is issued
+// only after the dQ product of step j, which reads them). Shared memory holds
+// only the K / V ring. Tensor memory: S (2 x 64 columns, dS inside), dP
 // (2 x 64), dQ (128), Q and dO (bf16, 64 each).
 constexpr int DQ_KS = 6;                                     // stages of the K / V ring
 constexpr uint32_t DQ_TM_DQ = 256, DQ_TM_Q = 384, DQ_TM_DO = 448;
 constexpr uint32_t DQ_OFF_K = 0;                             // DQ_KS stages of T64
 constexpr uint32_t DQ_OFF_V = DQ_OFF_K + DQ_KS * T64;       // DQ_KS stages of T64
-constexpr uint32_t DQ_OFF_DS = DQ_OFF_V + DQ_KS * T64;      // 2 buffers: 128 rows x 64 keys bf16 (16 KB)
-constexpr uint32_t DQ_OFF_BAR = DQ_OFF_DS + 2 * 16384;
+constexpr uint32_t DQ_OFF_BAR = DQ_OFF_V + DQ_KS * T64;
 constexpr size_t DQ_SMEM = 1024 + DQ_OFF_BAR + 256;
 static_assert(DQ_SMEM <= 232448, "dQ shared memory above the per-CTA limit");
 static_assert(DQ_KS >= 4, "Q and dO are staged in the ring's last two stages");
@@ -1249,9 +1252,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dq_tc_kernel(const __gr
   auto kv_free = [&](int s) { return bar + 8 + 8 * DQ_KS + 8 * s; };
   const uint32_t b2 = bar + 8 + 16 * DQ_KS;
   auto sd_full = [&](int s) { return b2 + 8 * s; };                   // 2 of each TMEM / dS barrier
-  auto sd_free = [&](int s) { return b2 + 16 + 8 * s; };
   auto ds_full = [&](int s) { return b2 + 32 + 8 * s; };
-  auto ds_free = [&](int s) { return b2 + 48 + 8 * s; };
   const uint32_t done = b2 + 64;
   const uint32_t q_staged = b2 + 72;                                 // Q, dO copied into the staging
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + DQ_OFF_BAR + 8 + 16 * DQ_KS + 80);
@@ -1275,9 +1276,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dq_tc_kernel(const __gr
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(sd_full(s), 1);
-      mbar_init(sd_free(s), BWD_EW);
       mbar_init(ds_full(s), BWD_EW);
-      mbar_init(ds_free(s), 1);
     }
     mbar_init(done, 1);
     *abort_flag = 0;
@@ -1343,16 +1342,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dq_tc_kernel(const __gr
         if (ng < ns && mbar_test_wait(ds_full(ng & 1), (ng >> 1) & 1)) {
           tc_fence_after();
           const int sg = ng & 1, ks = ng % DQ_KS;
+          // dS from TMEM: keys 16 kk .. 16 kk + 15 in S[sg] columns 32 (kk / 2) + 8 (kk % 2) ..
           for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + DQ_TM_DQ, desc_k64(sb + DQ_OFF_DS + sg * 16384, kk),
-                      desc_mn128(sb + DQ_OFF_K + ks * T64, 8192, kk), id_q, (ng > 0 || kk > 0) ? 1u : 0u);
+            umma_bf16_ta(tmem + DQ_TM_DQ, tmem + sg * 64 + (kk >> 1) * 32 + (kk & 1) * 8,
+                         desc_mn128(sb + DQ_OFF_K + ks * T64, 8192, kk), id_q, (ng > 0 || kk > 0) ? 1u : 0u);
           umma_commit(kv_free(ks));
-          umma_commit(ds_free(sg));
           ++ng;
           prog = true;
         }
-        if (ns < nkb && mbar_test_wait(kv_full(ns % DQ_KS), (ns / DQ_KS) & 1) &&
-            (ns < 2 || mbar_test_wait(sd_free(ns & 1), ((ns >> 1) & 1) ^ 1u))) {
+        // S / dP of step ns overwrite the buffers of step ns - 2: after its dQ
+        // product (issued in order; its dS was written after S and dP were read)
+        if (ns < nkb && ng >= ns - 1 && mbar_test_wait(kv_full(ns % DQ_KS), (ns / DQ_KS) & 1)) {
           tc_fence_after();
           const int ss = ns & 1, ks = ns % DQ_KS;
           for (int kk = 0; kk < HD / 16; ++kk)
@@ -1436,34 +1436,26 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dq_tc_kernel(const __gr
       tmem_ld_32x32b_x32(tmem + lane_off + s * 64 + col0, sv);
       tmem_ld_32x32b_x32(tmem + lane_off + 128 + s * 64 + col0, dv);
       tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sd_free(s));
-      if (j >= 2 && !mbar_wait_warp(ds_free(s), ph ^ 1u, p.err, abort_flag)) { ok = false; break; }
       const int lim = qrow - j * 64;          // keys j*64 + c with c <= lim are kept
-      uint8_t* drw = smem + DQ_OFF_DS + s * 16384 + r * 128;
+      uint32_t pk[16];                        // dS of this warp's 32 keys, bf16 pairs
       auto step = [&](auto masked) {
       constexpr bool MASK = decltype(masked)::value;
 #pragma unroll
-      for (int c8l = 0; c8l < 4; ++c8l) {
-        const int c8 = half * 4 + c8l;
-        uint32_t pk[4];
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          const int c = c8 * 8 + e, cl = c8l * 8 + e;   // step column, column within this warp's half
-          float p0 = ex2_approx(fmaf(__uint_as_float(sv[cl]), p.scale_log2, -l2));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sv[cl + 1]), p.scale_log2, -l2));
-          if (MASK && c > lim) p0 = 0.f;
-          if (MASK && c + 1 > lim) p1 = 0.f;
-          pk[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[cl]) - Dq), p1 * (__uint_as_float(dv[cl + 1]) - Dq));
-        }
-        *reinterpret_cast<uint4*>(drw + ((c8 ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      for (int e = 0; e < 32; e += 2) {
+        const int c = col0 + e;               // step column
+        float p0 = ex2_approx(fmaf(__uint_as_float(sv[e]), p.scale_log2, -l2));
+        float p1 = ex2_approx(fmaf(__uint_as_float(sv[e + 1]), p.scale_log2, -l2));
+        if (MASK && c > lim) p0 = 0.f;
+        if (MASK && c + 1 > lim) p1 = 0.f;
+        pk[e >> 1] = pack_bf16x2(p0 * (__uint_as_float(dv[e]) - Dq), p1 * (__uint_as_float(dv[e + 1]) - Dq));
       }
       };
       // keys j*64 + c with c > lim are masked: only the steps at the diagonal have any
       if (__any_sync(0xffffffffu, lim < col0 + 31)) step(std::true_type{});
       else step(std::false_type{});
-      fence_proxy_async_smem();
+      tmem_st_32x32b_x16(tmem + lane_off + s * 64 + col0, pk);
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(ds_full(s));
     }
