@@ -53,6 +53,9 @@ constexpr uint32_t OFF_Q = 0;
 constexpr uint32_t OFF_K = OFF_Q + TILE_BYTES;          // 2 stages
 constexpr uint32_t OFF_V = OFF_K + 2 * TILE_BYTES;      // 2 stages
 constexpr uint32_t OFF_BAR = OFF_V + 2 * TILE_BYTES;
+// tensor memory of the one-CTA-per-item form: S[0], S[1] (P in the first 64
+// columns of each), O, and Q as bf16 pairs (the A operand of S = Q K^T)
+constexpr uint32_t TM_QF = 384;
 constexpr size_t SMEM_BYTES = 1024 + OFF_BAR + 256;
 
 struct FwdParams {
@@ -119,6 +122,7 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_kernel(const __grid_cons
   auto s_free = [&](int s) { return bar + 88 + 8 * s; };
   const uint32_t p_full = bar + 104;
   const uint32_t p_free = bar + 112;
+  const uint32_t q_tm = bar + 120;     // Q copied into tensor memory
   const uint32_t drain = bar + 152;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + OFF_BAR + 160);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_BAR + 164);
@@ -144,6 +148,7 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_kernel(const __grid_cons
     }
     mbar_init(p_full, 4);
     mbar_init(p_free, 1);
+    mbar_init(q_tm, 4);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -199,7 +204,7 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_kernel(const __grid_cons
     const bool el = elect_one();
     const uint32_t idesc_s = idesc_bf16_f32(128, 128, 0, 0);
     const uint32_t idesc_pv = idesc_bf16_f32(128, 128, 0, 1);
-    bool ok = mbar_wait_warp(q_full, 0, p.err, abort_flag);
+    bool ok = mbar_wait_warp(q_tm, 0, p.err, abort_flag);
     auto issue_pv = [&](int j) -> bool {
       const int s = j & 1;
       const uint32_t ph = (j >> 1) & 1;
@@ -227,8 +232,8 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_kernel(const __grid_cons
       tc_fence_after();
       const uint32_t d = tmem + s * 128;
       if (el) {
-        for (int kk = 0; kk < HD / 16; ++kk)
-          umma_bf16(d, desc_kmajor(sb + OFF_Q, kk), desc_kmajor(sb + OFF_K + s * TILE_BYTES, kk), idesc_s, kk > 0);
+        for (int kk = 0; kk < HD / 16; ++kk)   // Q from TMEM
+          umma_bf16_ta(d, tmem + TM_QF + kk * 8, desc_kmajor(sb + OFF_K + s * TILE_BYTES, kk), idesc_s, kk > 0);
         umma_commit(k_empty(s));
         umma_commit(s_full(s));
       }
@@ -248,8 +253,27 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_kernel(const __grid_cons
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t oadr = tmem + lane_off + 256;
     float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < nkb; ++j) {
+    bool ok = mbar_wait_warp(q_full, 0, p.err, abort_flag);
+    if (ok) {
+      // this row's Q (two 128-byte-swizzled 64-column blocks) into TMEM columns
+      // TM_QF .. + 63 as bf16 pairs: the A operand of every S = Q K^T
+      uint32_t qa[32], qb[32];
+      const uint8_t* qs = smem + OFF_Q + r * 128;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const int off = (e ^ (r & 7)) << 4;
+        const uint4 x = *reinterpret_cast<const uint4*>(qs + off), y = *reinterpret_cast<const uint4*>(qs + 16384 + off);
+        qa[4 * e] = x.x; qa[4 * e + 1] = x.y; qa[4 * e + 2] = x.z; qa[4 * e + 3] = x.w;
+        qb[4 * e] = y.x; qb[4 * e + 1] = y.y; qb[4 * e + 2] = y.z; qb[4 * e + 3] = y.w;
+      }
+      tmem_st_32x32b_x32(tmem + lane_off + TM_QF, qa);
+      tmem_st_32x32b_x32(tmem + lane_off + TM_QF + 32, qb);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(q_tm);
+    }
+    for (int j = 0; ok && j < nkb; ++j) {
       const int s = j & 1;
       const uint32_t ph = (j >> 1) & 1;
       if (!mbar_wait_warp(s_full(s), ph, p.err, abort_flag)) { ok = false; break; }
