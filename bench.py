@@ -875,6 +875,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="layer workload: skip the short runs of the other workloads")
+    ap.add_argument("--no-later", action="store_true",
+                    help="layer workload: skip the one-second later region")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.workload.startswith("stream") and "--steps" not in sys.argv:
@@ -906,7 +908,8 @@ def main():
         dist_mod.init_process_group("nccl")
         dist = dist_mod
     # the headline layer step also runs a one-second region after the others
-    r = bench_ours(args, rank, world, local_rank, dist, later_s=1.0 if args.workload == "layer" else 0.0)
+    r = bench_ours(args, rank, world, local_rank, dist,
+                   later_s=1.0 if args.workload == "layer" and not args.no_later else 0.0)
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
