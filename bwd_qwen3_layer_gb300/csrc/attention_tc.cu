@@ -696,15 +696,17 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_persist_kernel(const __g
 
 // ===========================================================================
 // Backward on the tensor cores. Two kernels, both recomputing P from lse:
-//   dK/dV: CTA = 128 keys of one query head; 64-query tiles from the diagonal
-//          on. S^T = K Q^T and dP^T = V dO^T (TMEM, double-buffered); thread =
-//          key row builds P^T and dS^T = P^T (dP^T - D) as bf16 in swizzled
-//          shared memory; dV += P^T dO and dK += dS^T Q accumulate in TMEM and
-//          are added at the end into the key/value head's fp32 accumulators
-//          (the head's query-head group adds into the same rows).
+//   dK/dV: CTA = 128 keys of one kv head, walking 64-query tiles of every
+//          query head of its GQA group from the diagonal on (at short
+//          sequences the group is split over a 2- or 4-CTA cluster).
+//          S^T = K Q^T and dP^T = V dO^T in TMEM (K and V are TMEM A
+//          operands); thread = key row builds P^T and dS^T = P^T (dP^T - D)
+//          as bf16 in swizzled shared memory; dV += P^T dO and dK += dS^T Q
+//          accumulate in TMEM across the group and are written once as bf16.
 //   dQ:    CTA = 128 queries of one head; 64-key tiles up to the diagonal.
-//          S = Q K^T and dP = dO V^T; thread = query row builds dS; dQ += dS K
-//          accumulates in TMEM and is written once (no atomics).
+//          S = Q K^T and dP = dO V^T (Q and dO are TMEM A operands); thread =
+//          query row builds dS into TMEM; dQ += dS K accumulates in TMEM and
+//          is written once (no atomics).
 // ===========================================================================
 constexpr uint32_t T64 = 64 * 128 * 2;   // 16 KB: a 64-row x 128-column bf16 tile (two 8 KB blocks)
 
