@@ -34,9 +34,11 @@ metric through the C ABI with each step's inputs copied from pinned host
 memory and its result read back inside the timed region, the copies of step
 k+1 (in) and k-1 (out) running on a copy stream while step k computes, as a
 training or serving loop feeds the GPU (the stream workloads' driver reads its
-results back inside the step, so there the copies stay in line). The default
-layer run adds `later_region`: the same step timed over one second after the
-other regions, when the board has reached its power limit. Every workload's
+results back inside the step, so there the copies stay in line). The per-kernel
+region and the e2e region each start after 2 s of idle, so all three short
+regions are timed from the same (burst) state of the board's power average.
+The default layer run adds `later_region`: the same step timed over one second
+after the other regions, when the board has reached its power limit. Every workload's
 inputs exceed L2 (129 MB), so no flush is needed between steps. N > 1 runs N
 independent replicas (weak scaling; the path needs no collective).
 `--impl reference` times the fp64 CPU oracle on a bounded sample of the same
@@ -539,6 +541,9 @@ def job_throughput(units_per_rank_step, steps, world, ms):
     return units_per_rank_step * steps * world / (ms / 1e3)
 
 
+IDLE_S = 2.0   # idle seconds before each timed region after the first
+
+
 def bench_ours(args, rank, world, local_rank, dist, later_s=0.0):
     """Timed regions of one workload: device-resident (value), per-launch
     events (kernels), end to end (e2e) and, with later_s > 0, a region of at
@@ -584,8 +589,12 @@ def bench_ours(args, rank, world, local_rank, dist, later_s=0.0):
     ms = e0.elapsed_time(e1)
 
     # ---- the same steps again with the launch profiler on (CUDA events
-    # around every launch): per-kernel times and roofline fractions ----
+    # around every launch): per-kernel times and roofline fractions. Each
+    # region starts after the same idle time, so the board's power average
+    # is where it was before the first one and every short region is timed
+    # under the same (burst) conditions ----
     barrier()
+    time.sleep(IDLE_S)
     lib.kl_profile_enable(1)
     p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     p0.record(stream)
@@ -605,6 +614,7 @@ def bench_ours(args, rank, world, local_rank, dist, later_s=0.0):
         e2e()
         e2e.end()
     barrier()
+    time.sleep(IDLE_S)
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
     if pipelined:
