@@ -224,6 +224,11 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // events on `st` (construct immediately before the launch; the destructor
 // records the stop event right after it). `flops` and `bytes` are the
 // launch's algorithmic work.
+// Whether the launch profiler is on (kl_profile_enable): launches that would
+// overlap on two streams then run one after the other, so that each one's
+// event-timed duration is its own.
+bool profiling_on();
+
 class ProfScope {
  public:
   ProfScope(const char* name, cudaStream_t st, double flops, double bytes);

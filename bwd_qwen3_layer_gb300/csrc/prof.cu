@@ -62,6 +62,12 @@ ProfScope::~ProfScope() {
   cudaEventRecord(p.events[ev_ + 1], st_);
 }
 
+bool profiling_on() {
+  Profiler& p = prof();
+  std::lock_guard<std::mutex> lk(p.mu);
+  return p.on;
+}
+
 }  // namespace kl
 
 using namespace kl;
