@@ -855,13 +855,15 @@ def summarize(r, workload, steps, world, pk):
     return out
 
 
-EXTRAS = {"attention": (5, 3), "lmhead": (10, 3), "stream": (3, 3), "decode": (20, 3)}
+EXTRAS = {"attention": (5, 3), "lmhead": (10, 3), "stream": (3, 3), "stream_recompute": (3, 3),
+          "stream_fwd64": (3, 3), "decode": (20, 3)}
 
 
 def measure_extras(args, pk):
-    """Short runs of the long-context attention, lm-head, 8-layer stream and
-    paged decode workloads in the same process, each with its own timed
-    region, per-kernel figures and clock record (steps, warm-up per EXTRAS)."""
+    """Short runs of the long-context attention, lm-head, 8-layer stream (and
+    its recompute mode), 64-layer streamed forward and paged decode workloads
+    in the same process, each with its own timed region, per-kernel figures
+    and clock record (steps, warm-up per EXTRAS)."""
     out = {}
     for wl, (steps, warm) in EXTRAS.items():
         a = argparse.Namespace(**vars(args))
