@@ -774,12 +774,19 @@ def oracle_sample(workload: str, steps: int):
     return units / sec, sec, cores, desc
 
 
-def pick_tensor_peak(pk, region_ms):
+def pick_tensor_peak(pk, region_ms, clocks=None):
     """The tensor-core denominator for kernels timed in a region of region_ms:
     the burst GEMM figure for a short region (the board has not yet reached its
-    power cap), the sustained one for a region of half a second or more."""
+    power cap), the sustained one for a region of half a second or more, unless
+    the region's clock record shows the SMs at (within 3 % of) their maximum
+    clock throughout the median, i.e. the board was not held at its power cap
+    (a stream step waiting on a slow host link): then the burst figure."""
     if region_ms < 500.0:
         return pk["bf16_tflops"], f"{pk['src']} bf16_tflops (burst: timed region {region_ms / 1e3:.2f} s < 0.5 s)"
+    sm, smax = (clocks or {}).get("sm_mhz"), (clocks or {}).get("sm_max_mhz")
+    if sm and smax and sm >= 0.97 * smax:
+        return (pk["bf16_tflops"], f"{pk['src']} bf16_tflops (burst: timed region {region_ms / 1e3:.2f} s at a median "
+                                   f"SM clock of {sm:.0f} of {smax:.0f} MHz, not power-capped)")
     return (pk["bf16_tflops_sustained"],
             f"{pk['src']} bf16_tflops_sustained (timed region {region_ms / 1e3:.2f} s >= 0.5 s)")
 
@@ -789,7 +796,7 @@ def summarize(r, workload, steps, world, pk):
     roofline of one bench_ours result."""
     value = job_throughput(r["units"], steps, world, r["ms"])
     e2e = job_throughput(r["units"], steps, world, r["ms_e2e"])
-    tpk, tsrc = pick_tensor_peak(pk, r["ms_prof"])
+    tpk, tsrc = pick_tensor_peak(pk, r["ms_prof"], r["clocks"])
     prof = r["prof"]
     total_ms = sum(v["ms"] for v in prof.values()) or 1.0
     kernels, above = {}, []
@@ -843,7 +850,7 @@ def summarize(r, workload, steps, world, pk):
     agg_tflops = total_flops / (r["ms"] / steps / 1e3) / 1e12
     out = {"value": round(value, 1), "unit": "tokens/s", "ms_per_step": round(r["ms"] / steps, 4)}
     if total_flops > 0:
-        bpk, bsrc = pick_tensor_peak(pk, r["ms"])
+        bpk, bsrc = pick_tensor_peak(pk, r["ms"], r["clocks"])
         out.update(tensor_frac_aggregate=round(agg_tflops / bpk, 4), aggregate_tflops=round(agg_tflops, 2),
                    aggregate_peak_src=bsrc)
     out.update(roofline=roof, kernels=kernels, kernels_frac_above_1=above, gpu_launches=r["launches"],

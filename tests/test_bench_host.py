@@ -50,6 +50,11 @@ def test_tensor_peak_follows_region_length():
     pk = {"bf16_tflops": 1925.9, "bf16_tflops_sustained": 1745.7, "hbm_gbs": 6667.9, "src": "measured"}
     assert b.pick_tensor_peak(pk, 82.0)[0] == 1925.9
     assert b.pick_tensor_peak(pk, 950.0)[0] == 1745.7
+    # a long region whose clock record shows the board at its power cap: sustained
+    assert b.pick_tensor_peak(pk, 950.0, {"sm_mhz": 1650.0, "sm_max_mhz": 2070.0})[0] == 1745.7
+    # a long region at full clock (waiting on a slow host link, not power-capped): burst
+    assert b.pick_tensor_peak(pk, 950.0, {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0})[0] == 1925.9
+    assert b.pick_tensor_peak(pk, 950.0, {"sm_mhz": None, "sm_max_mhz": None})[0] == 1745.7
 
 
 def test_summary_flags_fraction_above_one():
