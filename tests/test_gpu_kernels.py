@@ -170,3 +170,49 @@ def test_attention_dkdv_group_split(kl, monkeypatch, B, S, Hq, Hkv):
         _, dk2, dv2 = _att_bwd(kl, B, S, Hq, Hkv, d, Q, Kt, Vt, Ot, lse, DO)
         assert torch.equal(dk, dk2) and torch.equal(dv, dv2), split
     kl.kl_device_status()
+
+
+def test_attention_bwd_overlap_matches_serial_and_joins(kl):
+    """At long sequences the dK/dV kernel runs on a second stream beside the dQ
+    kernel (fork and join events). The overlapped backward gives the same bits
+    as the one-after-the-other backward (which the launch profiler forces), and
+    a library kernel launched on the caller's stream right behind it, with no
+    host synchronisation (programmatic dependent launch), reads the finished dK."""
+    B, S, Hq, Hkv, d = 1, 16384, 64, 8, 128
+    T = B * S
+    dn = lambda shp, name: synth.device_normal(shp, 1.0, 0.0, 5, name, torch.bfloat16, "cuda")  # noqa: E731
+    Q, DO = dn((T, Hq * d), "ov.q"), dn((T, Hq * d), "ov.do")
+    Kt, Vt = dn((T, Hkv * d), "ov.k"), dn((T, Hkv * d), "ov.v")
+    Ot = torch.empty_like(Q)
+    lse = torch.empty(B, Hq, S, dtype=torch.float32, device="cuda")
+    kl.kl_attention_fwd(B, S, Hq, Hkv, d, 1, Q.data_ptr(), Kt.data_ptr(), Vt.data_ptr(), Ot.data_ptr(),
+                        lse.data_ptr())
+    ws = torch.empty(kl.kl_attention_bwd_ws_bytes(B, S, Hq, Hkv, d), dtype=torch.uint8, device="cuda")
+
+    def bwd():
+        dq, dk, dv = torch.empty_like(Q), torch.empty_like(Kt), torch.empty_like(Vt)
+        kl.kl_attention_bwd(B, S, Hq, Hkv, d, 1, Q.data_ptr(), Kt.data_ptr(), Vt.data_ptr(), Ot.data_ptr(),
+                            lse.data_ptr(), DO.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                            ws.data_ptr(), ws.numel())
+        return dq, dk, dv
+
+    lib = kl.load()
+    lib.kl_profile_enable(1)
+    serial = bwd()
+    torch.cuda.synchronize()
+    lib.kl_profile_enable(0)
+    ones = torch.ones(Hkv * d, dtype=torch.bfloat16, device="cuda")
+    h_next, r_next = torch.empty_like(Kt), torch.empty(T, dtype=torch.float32, device="cuda")
+    overlapped = bwd()
+    kl.kl_rmsnorm_fwd(T, Hkv * d, 1, overlapped[1].data_ptr(), ones.data_ptr(), 1e-6, h_next.data_ptr(),
+                      r_next.data_ptr())
+    torch.cuda.synchronize()
+    for a, b, name in zip(serial, overlapped, ("dq", "dk", "dv")):
+        assert torch.equal(a, b), name
+    h_ref, r_ref = torch.empty_like(Kt), torch.empty(T, dtype=torch.float32, device="cuda")
+    kl.kl_rmsnorm_fwd(T, Hkv * d, 1, overlapped[1].data_ptr(), ones.data_ptr(), 1e-6, h_ref.data_ptr(),
+                      r_ref.data_ptr())
+    torch.cuda.synchronize()
+    assert torch.equal(h_next, h_ref) and torch.equal(r_next, r_ref)
+    assert float(overlapped[1].float().abs().sum()) > 0.0
+    kl.kl_device_status()
