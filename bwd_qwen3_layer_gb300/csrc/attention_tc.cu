@@ -14,12 +14,15 @@
 //                 S_j  = Q K_j^T   -> TMEM S[j%2]  (128 x 128 fp32)
 //                 O   += P_j V_j   -> TMEM O[item%2] (128 x 128 fp32)
 //               S_{j+1} is issued before P_j V_j so the tensor core computes
-//               the next scores while the softmax warps work on P_j.
+//               the next scores while the softmax warps work on P_j. P_j is
+//               the TMEM A operand of its product (the one-CTA-per-item form
+//               also holds Q in TMEM), so the products read only K and V from
+//               shared memory.
 //   warps 2..5  softmax: thread = query row = TMEM lane. Two passes over S_j
-//               (row max, then exp2 / row sum / bf16 P written to shared memory
-//               in the 128-byte-swizzled K-major layout the MMA reads). The
-//               running max is only raised when a row's max grows by more than
-//               2^8 (then that warp rescales its O rows in TMEM); otherwise P is
+//               (row max, then exp2 / row sum / bf16 P written with tcgen05.st
+//               into the first 64 columns of S_j's own buffer). The running
+//               max is only raised when a row's max grows by more than 2^8
+//               (then that warp rescales its O rows in TMEM); otherwise P is
 //               taken against the stale max, which the final O / l cancels.
 // Every wait is bounded; a timeout records KL_DEVERR_TIMEOUT and unwinds.
 #include <cudaTypedefs.h>

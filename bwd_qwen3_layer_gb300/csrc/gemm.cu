@@ -10,8 +10,11 @@
 // accumulates in TMEM (two 256-column fp32 accumulators per CTA, so one tile's
 // epilogue overlaps the next tile's main loop); four epilogue warps read their
 // TMEM lane quarter (tcgen05.ld 32x32b.x32), add the optional residual,
-// convert and store. Work units (a tile, or a K range of a tile for long fp32
-// outputs) are handed out by a global atomic counter, heaviest problems first.
+// convert and store. Work units (whole output tiles, each summed over its
+// whole K range in one order; when the last round would leave pairs idle, its
+// tiles split along K into per-range fp32 slices that gemm_tail_finalize_kernel
+// sums in range order) are handed out by a global atomic counter, heaviest
+// problems first.
 // Operands may be K-major or MN-major (the transpose bits of the instruction
 // descriptor), so dX and dW need no transposed copies. Up to four problems
 // share one launch (for example the q/k/v projections, or a dX and a dW
