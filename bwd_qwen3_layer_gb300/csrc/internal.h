@@ -220,15 +220,15 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
-// Counts a kernel launch and, while profiling is on, brackets it with CUDA
-// events on `st` (construct immediately before the launch; the destructor
-// records the stop event right after it). `flops` and `bytes` are the
-// launch's algorithmic work.
 // Whether the launch profiler is on (kl_profile_enable): launches that would
 // overlap on two streams then run one after the other, so that each one's
 // event-timed duration is its own.
 bool profiling_on();
 
+// Counts a kernel launch and, while profiling is on, brackets it with CUDA
+// events on `st` (construct immediately before the launch; the destructor
+// records the stop event right after it). `flops` and `bytes` are the
+// launch's algorithmic work.
 class ProfScope {
  public:
   ProfScope(const char* name, cudaStream_t st, double flops, double bytes);
