@@ -82,6 +82,7 @@ _SIGNATURES = {
     "kl_status_str": (ctypes.c_char_p, [ctypes.c_int]),
     "kl_last_error": (ctypes.c_char_p, []),
     "kl_device_status": (ctypes.c_int, [_vp, _P(ctypes.c_uint32)]),
+    "kl_test_abandon_counters": (ctypes.c_int, []),
     "kl_layer_saved_bytes": (_sz, [_P(LayerCfg)]),
     "kl_layer_saved_carve": (ctypes.c_int, [_P(LayerCfg), _vp, _sz, _P(LayerSaved)]),
     "kl_layer_fwd_workspace_bytes": (_sz, [_P(LayerCfg)]),
@@ -327,6 +328,10 @@ def kl_device_status(stream=None) -> int:
     bits = ctypes.c_uint32(0)
     check(load().kl_device_status(_stream(stream), ctypes.byref(bits)))
     return bits.value
+
+
+def kl_test_abandon_counters() -> None:
+    check(load().kl_test_abandon_counters())
 
 
 def kl_stream_create(cfg: StreamCfg, host_layers, host_lm_head: int) -> int:

@@ -297,6 +297,17 @@ kl_status kl_device_status(void* stream, uint32_t* bits) {
   return KL_OK;
 }
 
+kl_status kl_test_abandon_counters(void) {
+  KL_CUDA(cudaDeviceSynchronize());
+  KL_TRY(skinny_cnt_abandon());
+  KL_TRY(rms_bar_abandon());
+  uint32_t v = 0;
+  KL_CUDA(cudaMemcpyFromSymbol(&v, g_device_error_word, sizeof(v)));
+  v |= KL_DEVERR_TIMEOUT;
+  KL_CUDA(cudaMemcpyToSymbol(g_device_error_word, &v, sizeof(v)));
+  return KL_OK;
+}
+
 size_t kl_layer_saved_bytes(const kl_layer_cfg* cfg) {
   Dims D;
   if (check_cfg(cfg, &D) != KL_OK) return 0;

@@ -1127,6 +1127,15 @@ kl_status rms_bar_reset() {
   return KL_OK;
 }
 
+kl_status rms_bar_abandon() {
+  // one arrival counted in every slot, the barrier never completed (generations kept)
+  unsigned int h[RB_BAR_SLOTS][2];
+  KL_CUDA(cudaMemcpyFromSymbol(h, g_rms_bar, sizeof(h)));
+  for (int s = 0; s < RB_BAR_SLOTS; ++s) h[s][0] = 1u;
+  KL_CUDA(cudaMemcpyToSymbol(g_rms_bar, h, sizeof(h)));
+  return KL_OK;
+}
+
 kl_status rmsnorm_bwd(int rows, int width, int dtype, const void* dh, int dh_dtype, const void* x,
                       const void* gamma, const float* rstd, const void* resid, void* dx,
                       float* dgamma, void* ws, size_t ws_bytes, cudaStream_t st) {

@@ -30,6 +30,7 @@
 #include <string.h>
 
 #include <atomic>
+#include <vector>
 
 #include "internal.h"
 #include "kl_common.cuh"
@@ -496,6 +497,13 @@ kl_status skinny_cnt_reset() {
   void* ptr = nullptr;
   KL_CUDA(cudaGetSymbolAddress(&ptr, g_skinny_cnt));
   KL_CUDA(cudaMemset(ptr, 0, sizeof(g_skinny_cnt)));
+  return KL_OK;
+}
+
+kl_status skinny_cnt_abandon() {
+  // one piece counted on every tile of every slot, the tile never finished
+  std::vector<unsigned int> ones(sizeof(g_skinny_cnt) / sizeof(unsigned int), 1u);
+  KL_CUDA(cudaMemcpyToSymbol(g_skinny_cnt, ones.data(), sizeof(g_skinny_cnt)));
   return KL_OK;
 }
 

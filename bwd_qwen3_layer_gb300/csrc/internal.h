@@ -97,6 +97,11 @@ kl_status skinny_cnt_reset();
 // Zeroes the fused RMSNorm backward's grid-barrier counters on the current
 // device (synchronous; used after a launch reported a timeout).
 kl_status rms_bar_reset();
+// Test hooks (synchronous): leave every few-rows arrival counter, and every
+// RMSNorm grid-barrier arrival counter, as a launch that gave up on a wait can
+// leave it (one arrival counted, never completed).
+kl_status skinny_cnt_abandon();
+kl_status rms_bar_abandon();
 // fp32 operands on CUDA cores (one problem).
 kl_status gemm_f32(const GemmSpec& spec, cudaStream_t st, const char* label = "gemm_f32");
 

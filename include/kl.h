@@ -89,6 +89,16 @@ KL_API const char* kl_last_error(void);
  * word. Returns KL_OK if it was zero, KL_ERR_TIMEOUT or KL_ERR_DEVICE if a
  * kernel recorded a fault; *bits (may be NULL) receives the raw word. */
 KL_API kl_status kl_device_status(void* stream, uint32_t* bits);
+/* Test hook for the recovery path above (no counterpart on the pages): waits
+ * for the whole device, then leaves the arrival counters of the few-rows GEMM
+ * and of the fused RMSNorm backward's grid barrier as a launch that gave up on
+ * a wait can leave them (one arrival counted, never completed) and sets
+ * KL_DEVERR_TIMEOUT in the error word, which is what such a launch does. The
+ * next kl_device_status returns KL_ERR_TIMEOUT and zeroes those counters;
+ * a launch of either kernel before that call reads the stale counts (wrong
+ * results, no hang: neither kernel waits on these counters without a limit).
+ * Returns KL_OK or KL_ERR_CUDA. */
+KL_API kl_status kl_test_abandon_counters(void);
 
 /* Launch profiler. Every kernel launch of the library is counted. While
  * profiling is on, each launch is also bracketed by CUDA events on its
