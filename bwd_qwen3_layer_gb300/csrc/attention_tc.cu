@@ -890,6 +890,25 @@ __device__ __forceinline__ void dkdv_reduce_store(const uint8_t* smem, int r, bo
   if (row) dkdv_store_row<W>(row, W * static_cast<int>(rank), lo, hi, is_k, scale, cs);
 }
 
+// Bounded wait by one thread that also gives up when the CTA's abort flag is
+// set (another role stopped): false then, or on timeout (recorded).
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, uint32_t* err,
+                                                   volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  uint32_t n = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++n & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > KL_WAIT_LIMIT_NS) {
+        record_error(err, KL_DEVERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+  return true;
+}
+
 __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __grid_constant__ BwdParams p) {
   pdl_enter();
   extern __shared__ __align__(1024) uint8_t kv_smem_raw[];
@@ -992,66 +1011,51 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) fa_bwd_dkdv_tc_kernel(const __
     // ---------------- MMA (the elected lane issues) ----------------
     // S^T / dP^T of step j go out once the elementwise warps have read step
     // j - 1's (one TMEM buffer) and step j's Q / dO have landed; the gradient
-    // products of step j once its P^T / dS^T are written. Polling both keeps
-    // the next scores in flight while the elementwise warps work on a step.
+    // products of step j - 1 once its P^T / dS^T are written. The elementwise
+    // warps read a step's scores before they write its P^T / dS^T and finish a
+    // step before they read the next one's, so the issuer waits for the events
+    // in that order (S^T of step j, then the gradients of step j - 1) with
+    // blocking, bounded waits instead of polling both conditions (~1 % faster
+    // at 32768 tokens). The next scores stay one step ahead.
     const bool el = elect_one();
     const uint32_t id_st = idesc_bf16_f32(128, 64, 0, 0);
     const uint32_t id_gr = idesc_bf16_f32(128, 128, 0, 1);
     bool ok = mbar_wait_warp(kv_ready, 0, p.err, abort_flag);
     if (ok) tc_fence_after();
     if (el && ok) {
-      int ns = 0, ng = 0;          // next step whose S^T / dP^T, whose gradients, go out
-      uint32_t idle = 0;
-      uint64_t since = 0;
-      while (ng < nsteps) {
-        bool prog = false;
-        if (ng < ns && mbar_test_wait(p_full(ng & 1), (ng >> 1) & 1)) {
+      for (int j = 0; j <= nsteps; ++j) {
+        if (j < nsteps) {
+          const int qs = j % KV_QS;
+          if (!mbar_wait_or_abort(q_full(qs), (j / KV_QS) & 1, p.err, abort_flag) ||
+              (j > 0 && !mbar_wait_or_abort(st_free, (j - 1) & 1, p.err, abort_flag))) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const int qs = ng % KV_QS, pb = ng & 1;
-          const uint32_t sq = sb + KV_OFF_Q + qs * T64, sdo = sb + KV_OFF_DO + qs * T64;
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + TM_DV, desc_k64(sb + KV_OFF_P + pb * PT_BYTES, kk), desc_mn128(sdo, 8192, kk), id_gr,
-                      (ng > 0 || kk > 0) ? 1u : 0u);
-          for (int kk = 0; kk < 4; ++kk)
-            umma_bf16(tmem + TM_DK, desc_k64(sb + KV_OFF_DS + pb * PT_BYTES, kk), desc_mn128(sq, 8192, kk), id_gr,
-                      (ng > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(q_free(qs));
-          umma_commit(p_free(pb));
-          ++ng;
-          prog = true;
-        }
-        if (ns < nsteps && mbar_test_wait(q_full(ns % KV_QS), (ns / KV_QS) & 1) &&
-            (ns == 0 || mbar_test_wait(st_free, (ns - 1) & 1))) {
-          tc_fence_after();
-          const int qs = ns % KV_QS;
           const uint32_t sq = sb + KV_OFF_Q + qs * T64, sdo = sb + KV_OFF_DO + qs * T64;
           for (int kk = 0; kk < HD / 16; ++kk)
             umma_bf16_ta(tmem + TM_ST, tmem + TM_K + kk * 8, desc_k128(sq, 8192, kk), id_st, kk > 0);
           for (int kk = 0; kk < HD / 16; ++kk)
             umma_bf16_ta(tmem + TM_DPT, tmem + TM_V + kk * 8, desc_k128(sdo, 8192, kk), id_st, kk > 0);
           umma_commit(st_full);
-          ++ns;
-          prog = true;
         }
-        if (prog) {
-          idle = 0;
-          since = 0;
-          continue;
-        }
-        // nothing ready: keep polling, bounded (the other roles stop on the abort flag)
-        if (*abort_flag) {
-          ok = false;
-          break;
-        }
-        if ((++idle & 1023u) == 0) {
-          const uint64_t now = global_timer_ns();
-          if (since == 0) {
-            since = now;
-          } else if (now - since > KL_WAIT_LIMIT_NS) {
-            record_error(p.err, KL_DEVERR_TIMEOUT);
+        if (j > 0) {
+          const int g = j - 1;
+          if (!mbar_wait_or_abort(p_full(g & 1), (g >> 1) & 1, p.err, abort_flag)) {
             ok = false;
             break;
           }
+          tc_fence_after();
+          const int qs = g % KV_QS, pb = g & 1;
+          const uint32_t sq = sb + KV_OFF_Q + qs * T64, sdo = sb + KV_OFF_DO + qs * T64;
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem + TM_DV, desc_k64(sb + KV_OFF_P + pb * PT_BYTES, kk), desc_mn128(sdo, 8192, kk), id_gr,
+                      (g > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk)
+            umma_bf16(tmem + TM_DK, desc_k64(sb + KV_OFF_DS + pb * PT_BYTES, kk), desc_mn128(sq, 8192, kk), id_gr,
+                      (g > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(q_free(qs));
+          umma_commit(p_free(pb));
         }
       }
     }
