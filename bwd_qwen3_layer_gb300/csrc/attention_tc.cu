@@ -357,8 +357,13 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_kernel(const __grid_cons
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
-    // O / l and lse once the last P V product is done
-    if (ok && mbar_wait_warp(p_free, (nkb - 1) & 1, p.err, abort_flag)) {
+    // O / l and lse once the last P V product is done. p_free completes once per
+    // P V product, and the last scores' completion shows only the product two
+    // steps back done (the one before is issued after those scores): a parity
+    // wait for the last one alone would pass while the barrier is still a phase
+    // behind it, so the product before it is waited for first.
+    if (ok && (nkb < 2 || mbar_wait_warp(p_free, (nkb - 2) & 1, p.err, abort_flag)) &&
+        mbar_wait_warp(p_free, (nkb - 1) & 1, p.err, abort_flag)) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       __nv_bfloat16* orow = p.o + (static_cast<int64_t>(row0 + qrow) * p.Hq + h) * HD;
@@ -659,7 +664,12 @@ __global__ void __launch_bounds__(THREADS, 1) fa_fwd_tc_persist_kernel(const __g
         if (lane == 0) mbar_arrive(p_full);
       }
       if (!ok) break;
-      // O / l and lse once the item's last P V product (step g - 1) is done
+      // O / l and lse once the item's last P V product (step g - 1) is done. p_free
+      // completes once per P V product; step g - 1's scores completing shows only
+      // step g - 3's product done (step g - 2's is issued after those scores), and a
+      // parity wait for step g - 1's alone would pass while the barrier is still at
+      // step g - 2's phase: wait for that one first.
+      if (g >= 2 && !mbar_wait_warp(p_free, (g - 2) & 1, p.err, abort_flag)) { ok = false; break; }
       if (!mbar_wait_warp(p_free, (g - 1) & 1, p.err, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
