@@ -301,6 +301,14 @@ kl_status ce_argmax(int N, int V, const float* z, const int32_t* targets, float*
     return set_error(KL_ERR_INVALID_ARG, "ce_argmax: bad arguments");
   if (N > 65535) return set_error(KL_ERR_UNSUPPORTED, "ce_argmax: N above 65535");
   if (!ws || ws_bytes < ce_ws(N)) return set_error(KL_ERR_NO_MEMORY, "ce_argmax: workspace too small");
+  {
+    // dlogits must not overlap the logits: a row's loss reads its target logit
+    // after the other CTAs of the row have written their dlogits slices
+    const uintptr_t z0 = reinterpret_cast<uintptr_t>(z), d0 = reinterpret_cast<uintptr_t>(dz);
+    const uintptr_t nv = static_cast<uintptr_t>(N) * static_cast<uintptr_t>(V);
+    if (z0 < d0 + nv * dtype_size(dz_dtype) && d0 < z0 + nv * 4)
+      return set_error(KL_ERR_INVALID_ARG, "ce_argmax: dlogits overlaps the logits");
+  }
   // the vector path: 32-byte logit loads, 16-byte bf16 dlogit stores
   const bool vec = V % 8 == 0 && (reinterpret_cast<uintptr_t>(z) & 31u) == 0 &&
                    (dz_dtype == KL_F32 || (reinterpret_cast<uintptr_t>(dz) & 15u) == 0);

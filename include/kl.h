@@ -240,7 +240,9 @@ KL_API kl_status kl_lmhead_ce_argmax(const kl_lmhead_cfg* cfg, const void* X, co
 
 /* The single-launch cross-entropy step alone, on given fp32 logits z [N,V]:
  * loss (device fp32 scalar, mean over rows), argmax int32 [N], dlogits [N,V]
- * of type dz_dtype, scaled by 1/N. Workspace: kl_ce_workspace_bytes(N). */
+ * of type dz_dtype, scaled by 1/N. Workspace: kl_ce_workspace_bytes(N).
+ * dlogits must not overlap z (KL_ERR_INVALID_ARG): a row's loss reads its
+ * target logit after the row's dlogits are written. */
 KL_API size_t kl_ce_workspace_bytes(int32_t N);
 KL_API kl_status kl_ce_argmax(int32_t N, int32_t V, const float* z, const int32_t* targets,
                        float* loss, int32_t* argmax, void* dlogits, int32_t dz_dtype,

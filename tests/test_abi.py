@@ -105,6 +105,13 @@ def test_lmhead_and_ce_host_checks(lib):
     assert K.kl_lmhead_workspace_bytes(K.LmheadCfg(8, 8, 8, K.KL_F32, K.KL_BF16)) == 0
     assert lib.kl_ce_argmax(0, 10, None, None, None, None, None, K.KL_F32, None, 0, None) == K.KL_ERR_INVALID_ARG
     assert lib.kl_ce_argmax(4, 10, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 5, 0x1000, 1 << 20, None) == K.KL_ERR_INVALID_ARG
+    # dlogits overlapping the logits (in place, or bf16 dlogits starting inside z) is rejected
+    # before any launch; disjoint buffers pass this check (and would then need a GPU)
+    ws = 0x100000
+    for dz, dt in ((0x10000, K.KL_F32), (0x10000 + 4 * 40 - 2, K.KL_BF16), (0x10000 - 4 * 40 + 2, K.KL_F32)):
+        assert lib.kl_ce_argmax(4, 10, 0x10000, 0x2000, 0x3000, 0x4000, dz, dt, ws, 1 << 20, None) \
+            == K.KL_ERR_INVALID_ARG, hex(dz)
+        assert "overlaps" in K.last_error()
 
 
 def test_gemm_host_checks(lib):
