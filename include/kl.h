@@ -276,9 +276,11 @@ KL_API kl_status kl_ce_argmax_noalloc(int32_t N, int32_t V, const float* z, cons
  * a_mn_major = 0: A is [M,K] with row stride lda (K contiguous);
  *            = 1: A is stored [K,M] with row stride lda (M contiguous).
  * b_mn_major = 0: B is [N,K] row stride ldb; = 1: B is stored [K,N].
- * A, B have type `dtype`; C has c_dtype; R (may be NULL) has c_dtype... or
- * r_dtype, [M,N] row stride ldr. KL_BF16 runs on the tensor cores and needs
- * lda, ldb, K multiples of 8; KL_F32 on CUDA cores. */
+ * A, B have type `dtype`; C has c_dtype; R (may be NULL) has r_dtype, [M,N]
+ * row stride ldr. KL_BF16 runs on the tensor cores and needs lda, ldb, K
+ * multiples of 8; KL_F32 on CUDA cores. C must not overlap A or B (output
+ * tiles are written while other tiles still read the operands); R may be C
+ * itself (each element's addend is read before that element is written). */
 KL_API kl_status kl_gemm(int32_t M, int32_t N, int32_t K, int32_t dtype,
                   const void* A, int64_t lda, int32_t a_mn_major,
                   const void* B, int64_t ldb, int32_t b_mn_major,

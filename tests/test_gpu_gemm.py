@@ -56,6 +56,30 @@ def test_gemm_bf16_out_with_residual(kl, a_mn, b_mn):
     assert_rel(host(C), O.linear(A, B) + R, 4e-3, "C+R bf16")
 
 
+@pytest.mark.parametrize("M,N,K,dt", [(392, 520, 264, 1), (2048, 5120, 1024, 1), (64, 1344, 2560, 1),
+                                      (200, 296, 136, 0)])
+def test_gemm_residual_in_place(kl, M, N, K, dt):
+    """R may be C itself (C = A B^T + C): every path reads an element's addend
+    before writing it, whole tiles, K-split last-round tiles, the few-rows kernel
+    and the fp32 kernel alike. The in-place result equals the out-of-place one
+    bit for bit."""
+    A, B, R = _operands(M, N, K, 9, bf16=dt == 1)
+    tdt = torch.bfloat16 if dt == 1 else torch.float32
+    a, b, r = dev(A, tdt), dev(B, tdt), dev(R, tdt)
+    nb = kl.kl_gemm_scratch_bytes()
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    C = torch.empty((M, N), dtype=tdt, device="cuda")
+    kl.kl_gemm_ex(M, N, K, dt, a.data_ptr(), K, 0, b.data_ptr(), K, 0, C.data_ptr(), N, dt,
+                  r.data_ptr(), N, dt, ws=ws.data_ptr(), ws_bytes=nb)
+    Ci = r.clone()
+    kl.kl_gemm_ex(M, N, K, dt, a.data_ptr(), K, 0, b.data_ptr(), K, 0, Ci.data_ptr(), N, dt,
+                  Ci.data_ptr(), N, dt, ws=ws.data_ptr(), ws_bytes=nb)
+    torch.cuda.synchronize()
+    kl.kl_device_status()
+    assert_rel(host(C), O.linear(A, B) + R, 4e-3 if dt == 1 else 1e-5, "C+R")
+    assert torch.equal(Ci, C)
+
+
 def test_gemm_bf16_zero_is_exact(kl):
     """A zero operand gives an exact zero product and the residual passes bit-exactly."""
     M, N, K = 256, 256, 128
